@@ -1,0 +1,348 @@
+"""Benchmark of the ZeRO per-rank mixed-precision AdamW step on GB300.
+
+One step = the whole hot path over one rank's shard: pass 1 (unscale,
+overflow, global squared norm), the decision kernel and pass 2 (clip, AdamW,
+cast), all through the C ABI.  Default workload: the GPT-2 1.5B model state
+flattened into 16 ZeRO shards, rank 0's shard of 97,350,784 params, fp16
+gradients (x65536 loss scale), fp32 master/momentum/variance, fp16 params.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+N > 1 (under torchrun): rank r updates shard r of the same layout and the
+ranks sum their 16-byte (sum g^2, found_inf) partials with one all-reduce
+between the passes: the one exchange of the step (weak scaling).
+--impl reference times the oracle (plain scalar C, host cores) on a bounded
+sample of the same workload.  Prints one JSON line (rank 0).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "Adam-step params/sec & achieved HBM GB/s vs GB300 roofline (28 B/param), 1 GPU"
+UNIT = "params/s"
+BYTES_ADAM = 28  # pass 2: read g16 2 + p/m/v 12, write p/m/v 12 + p16 2
+BYTES_STEP = 30  # + pass 1 reading g16 again
+WORKLOAD = "gpt2_1p5b_nd16"
+L2_BYTES = 129e6
+
+
+def kernel_source_hash() -> str:
+    csrc = os.path.join(ROOT, "zero_partitioned_mixed_layout_gb300", "csrc")
+    h = hashlib.sha256()
+    for f in sorted(os.listdir(csrc)):
+        if f.endswith((".cu", ".h", ".cpp")):
+            h.update(open(os.path.join(csrc, f), "rb").read())
+    return h.hexdigest()[:16]
+
+
+def committed_traffic():
+    """DRAM bytes per pass-2 launch from the committed ncu summary, if it was
+    taken on the current kernel source (else None)."""
+    path = os.path.join(ROOT, "profiles", "adam_pass2_gpt2_nd16_traffic.json")
+    try:
+        d = json.load(open(path))
+    except (OSError, ValueError):
+        return None
+    if d.get("kernel_source_sha256_16") != kernel_source_hash():
+        return None
+    return d.get("dram_bytes_per_launch")
+
+
+def measured_peaks():
+    try:
+        return json.load(open(os.path.join(ROOT, "MEASURED_PEAKS.json")))
+    except (OSError, ValueError):
+        return None
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled every 200 ms."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        self.rows = []
+        if self.proc is None:
+            return False
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        for line in out.splitlines():
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) >= 9:
+                self.rows.append(parts)
+        return False
+
+    def summary(self):
+        if not getattr(self, "rows", None):
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"]}
+        sm = [float(r[1]) for r in self.rows if r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in self.rows if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in self.rows for i in range(4) if r[5 + i] == "Active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": reasons,
+                "samples": len(self.rows)}
+
+
+def dist_env():
+    return (int(os.environ.get("RANK", "0")), int(os.environ.get("WORLD_SIZE", "1")),
+            int(os.environ.get("LOCAL_RANK", "0")))
+
+
+# ------------------------------------------------------------------ oracle arm
+
+def oracle_run(n_sample: int, steps: int, warmup: int):
+    """The oracle as it stands (single-threaded scalar C) on the first
+    n_sample elements of the workload's shard: `warmup` untimed and `steps`
+    timed full steps (norm, decision, update)."""
+    import numpy as np
+
+    import oracle
+    import zero_synth as zs
+    w = zs.WORKLOADS[WORKLOAD]
+    oracle.build()
+    p = zs.host_master(n_sample, 0)
+    m = np.zeros(n_sample, np.float32)
+    v = np.zeros(n_sample, np.float32)
+    plp = np.zeros(n_sample, np.uint16)
+    g = zs.host_grad(n_sample, 0, 0, w["loss_scale"], "f16")
+    hp = oracle.HParams()
+    sc = oracle.Scaler(loss_scale=w["loss_scale"])
+    for _ in range(warmup):
+        oracle.adam_step([g], "f16", [p], [m], [v], [plp], "f16", hp, sc)
+    t0 = time.perf_counter()
+    for _ in range(steps):
+        oracle.adam_step([g], "f16", [p], [m], [v], [plp], "f16", hp, sc)
+    dt = time.perf_counter() - t0
+    return n_sample * steps / dt, dt
+
+
+def run_reference(args):
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return
+    n_sample = 1 << 24
+    value, dt = oracle_run(n_sample, args.steps, args.warmup)
+    sample = (f"first {n_sample} params of the {WORKLOAD} rank-0 shard, {args.steps} timed steps "
+              f"after {args.warmup} warm-up; full step (norm, decision, update) per step")
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * dt / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "data": "synthetic",
+        "config": {"workload": WORKLOAD, "sample_params": n_sample},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+# ------------------------------------------------------------------ our arm
+
+def run_ours(args):
+    import torch
+    import torch.distributed as dist
+
+    import zero_partitioned_mixed_layout_gb300 as zp
+    import zero_synth as zs
+
+    rank, world, local = dist_env()
+    if world > 1:
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    dev = torch.device("cuda", torch.cuda.current_device())
+    w = zs.WORKLOADS[WORKLOAD]
+    lay = zp.zero_partition_layout(w["numel"](), w["nd"], w["align"])
+    S = lay.shard_numel
+    shard = rank % w["nd"]
+    scale = w["loss_scale"]
+
+    dp = torch.empty(S, dtype=torch.float32, device=dev)
+    zs.device_master_into(dp, 1000 + shard)
+    dm = torch.zeros(S, dtype=torch.float32, device=dev)
+    dv = torch.zeros(S, dtype=torch.float32, device=dev)
+    dlp = torch.empty(S, dtype=torch.float16, device=dev)
+    dg = torch.empty(S, dtype=torch.float16, device=dev)
+    zs.device_grad_into(dg, 1000 + shard, 0, scale)
+    state = zp.new_state(scale, dev)
+    ws = zp.new_workspace(1, S, dev)
+    hp = zp.HParams(**zs.HPARAMS, max_norm=w["max_norm"])
+    stream = torch.cuda.current_stream(dev)
+
+    def exchange():
+        if world > 1:
+            dist.all_reduce(state[:16].view(torch.float64))
+
+    def step(ev=None):
+        zp.zero_grad_norm_overflow(dg, state, ws, stream=stream)
+        exchange()
+        if ev is not None:
+            ev[0].record(stream)
+        zp.zero_adam_step(dg, dp, dm, dv, dlp, hp, state, ws, stream=stream)
+        if ev is not None:
+            ev[1].record(stream)
+
+    def barrier():
+        torch.cuda.synchronize(dev)
+        if world > 1:
+            dist.barrier()
+        torch.cuda.synchronize(dev)
+
+    for _ in range(args.warmup):
+        step()
+    barrier()
+    st = zp.parse_state(state)
+    assert st["last_skipped"] == 0 and st["step"] == args.warmup, st
+
+    events = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+              for _ in range(args.steps)]
+    t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(dev.index if world == 1 else local) as clk:
+        barrier()
+        t_start.record(stream)
+        for k in range(args.steps):
+            step(events[k])
+        t_end.record(stream)
+        barrier()
+    ms = t_start.elapsed_time(t_end)
+    adam_ms = statistics.mean(a.elapsed_time(b) for a, b in events)
+    st = zp.parse_state(state)
+    assert st["last_skipped"] == 0 and st["step"] == args.warmup + args.steps, st
+    if world > 1:
+        t = torch.tensor([ms, adam_ms], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms, adam_ms = t.tolist()
+    ms_per_step = ms / args.steps
+    value = world * S / (ms_per_step * 1e-3)
+
+    # end to end through the public API from pinned host memory: the step's
+    # gradient in (H2D), the step, the 64-byte state out (D2H) and read on
+    # the host every step
+    e2e = None
+    if rank == 0 or world > 1:
+        hg = torch.empty(S, dtype=torch.float16, pin_memory=True)
+        hg.copy_(dg.cpu())
+        hs = torch.empty(zp.STATE_BYTES, dtype=torch.uint8, pin_memory=True)
+        for _ in range(2):
+            dg.copy_(hg, non_blocking=True)
+            step()
+            hs.copy_(state, non_blocking=True)
+            stream.synchronize()
+        barrier()
+        t0 = time.perf_counter()
+        for _ in range(args.steps):
+            dg.copy_(hg, non_blocking=True)
+            step()
+            hs.copy_(state, non_blocking=True)
+            stream.synchronize()
+            assert zp.parse_state(bytes(hs.numpy().tobytes()))["last_skipped"] == 0
+        barrier()
+        e2e_s = (time.perf_counter() - t0) / args.steps
+        if world > 1:
+            t = torch.tensor([e2e_s], dtype=torch.float64, device=dev)
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            e2e_s = t.item()
+        e2e = {"value": world * S / e2e_s, "unit": UNIT, "h2d_bytes_per_step": 2 * S,
+               "d2h_bytes_per_step": zp.STATE_BYTES,
+               "note": "fp16 gradient copied from pinned host memory, step, state read back "
+                       "and checked on the host every step"}
+
+    if rank != 0:
+        if world > 1:
+            dist.destroy_process_group()
+        return
+
+    peaks = measured_peaks()
+    peak = peaks["hbm_gbs"] if peaks else 6800.0
+    achieved = BYTES_ADAM * S / (adam_ms * 1e-3) / 1e9
+    cpu = None
+    if not args.no_cpu_baseline and world == 1:
+        n_sample = 1 << 24
+        cv, cdt = oracle_run(n_sample, 3, 0)
+        cpu = {"value": cv, "unit": UNIT, "cores": 1, "kind": "oracle",
+               "sample": f"first {n_sample} params of the same shard, 3 full steps, "
+                         f"{cdt:.1f} s, single-threaded scalar C"}
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": {
+            "workload": "GPT-2 1.5B state (48 layers, hidden 1600, vocab 50257) in 16 ZeRO "
+                        "shards, one shard per GPU",
+            "shard_params": S, "grad_dtype": "f16", "param_dtype": "f16",
+            "state_dtype": "f32", "loss_scale": scale, "clip": w["max_norm"],
+            "l2": f"inputs larger than L2 ({BYTES_STEP * S / 1e9:.2f} GB per step vs "
+                  f"{L2_BYTES / 1e6:.0f} MB), no flush",
+            "parallelism": f"zero-dp{world}" if world > 1 else "zero-shard",
+        },
+        "hbm_gbs_28B": BYTES_ADAM * S / (ms_per_step * 1e-3) / 1e9,
+        "hbm_gbs_step_30B": BYTES_STEP * S / (ms_per_step * 1e-3) / 1e9,
+        "passes_ms": {"adam_step": adam_ms, "whole_step": ms_per_step},
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                     "frac": achieved / peak, "traffic": committed_traffic(),
+                     "kernel": "zero_adam_step (decision + pass 2), 28 B/param",
+                     "peak_source": "MEASURED_PEAKS.json hbm_gbs (of measured)" if peaks
+                     else "fallback 6.8 TB/s (of fallback)"},
+        "cpu_baseline": cpu,
+        "e2e": e2e,
+        "gpu_launches": 3 * args.steps,
+        "clocks": clk.summary(),
+    }
+    print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        import zero_partitioned_mixed_layout_gb300 as zp
+        from zero_partitioned_mixed_layout_gb300 import _build
+        _build.build()
+        zp.lib()
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,208 @@
+/*
+ * zero_pml.h -- C ABI of the ZeRO partitioned mixed-precision optimizer step
+ * for NVIDIA GB300 (sm_103a).
+ *
+ * The library does the per-rank part of a ZeRO data-parallel training step:
+ * the model states are flattened and partitioned over Nd ranks, and for one
+ * rank's shard hand-written CUDA kernels run the mixed-precision AdamW update
+ * with dynamic loss scaling and global gradient-norm clipping.
+ *
+ * Sources (web pages on ZeRO / DeepSpeed):
+ *   [ZeRO card] "ZeRO: Memory Optimizations Toward Training Trillion
+ *               Parameter Models - 中文验证版" (ai-papers.xuzou.cn/zh/papers/zero_2019/),
+ *               sections 瓶颈 (bottleneck), 方法适配 (method), 证据 (evidence).
+ *   [DS news]   DeepSpeed release news (lxsoso.com/blog/19320.html).
+ *   [ZeRO-2]    "探秘微软大规模人工智能的新框架 ZeRO-2" (infoq.cn).
+ * The update equations, which the pages do not print, are Adam (Kingma & Ba
+ * 2015) with decoupled weight decay (Loshchilov & Hutter 2019) and dynamic
+ * loss scaling (Micikevicius et al. 2018).
+ *
+ * Conventions for every entry point:
+ *   - Returns ZERO_OK (0) or a negative ZERO_E* code; zero_strerror() names
+ *     it.  Arguments are checked on the host before anything is enqueued: a
+ *     call that returns an argument error has launched nothing and changed
+ *     nothing.  No C++ exception crosses the ABI.
+ *   - The caller owns all memory.  The library never allocates device
+ *     memory; it works in caller-provided device buffers and a caller-provided
+ *     device workspace (see zero_workspace_bytes).
+ *   - `stream` is a cudaStream_t passed as void* (NULL = the legacy default
+ *     stream).  Device work is enqueued asynchronously on it, on the calling
+ *     thread's current CUDA device; no call synchronises the host.
+ *   - Device arrays must start on a 16-byte boundary (ZERO_EALIGN otherwise);
+ *     any element count is accepted, including 0 and counts of 2^31 and more.
+ *   - Element types: ZERO_F16 (IEEE binary16), ZERO_BF16 (bfloat16),
+ *     ZERO_F32 (IEEE binary32).
+ */
+#ifndef ZERO_PML_H
+#define ZERO_PML_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* ------------------------------------------------------------------ codes */
+
+#define ZERO_OK 0
+#define ZERO_EINVAL (-1)     /* a required pointer is NULL, or a bad flag/count */
+#define ZERO_EALIGN (-2)     /* a device array does not start on 16 bytes */
+#define ZERO_EDTYPE (-3)     /* an element type that this argument does not take */
+#define ZERO_ESIZE (-4)      /* element counts that do not match across lists */
+#define ZERO_EWORKSPACE (-5) /* workspace NULL or smaller than required */
+#define ZERO_ECAPACITY (-6)  /* an output array is too small (see *n_frags) */
+#define ZERO_ECUDA (-7)      /* the CUDA runtime reported an error */
+#define ZERO_ELAYOUT (-8)    /* nd < 1, align < 1 or not a power of two */
+
+#define ZERO_F16 0
+#define ZERO_BF16 1
+#define ZERO_F32 2
+
+/* Text of a ZERO_* code; for ZERO_ECUDA, the last CUDA error seen by this
+ * library on the calling thread is appended.  Never NULL.  The string stays
+ * valid until the next call on the same thread. */
+const char *zero_strerror(int code);
+
+/* ------------------------------------------------------------------ layout */
+
+/* One piece of a tensor inside one rank's shard. */
+typedef struct zero_frag {
+    int64_t tensor;        /* index in the tensor list */
+    int64_t tensor_offset; /* first element of the piece, within the tensor */
+    int64_t rank;          /* owning rank, 0 .. nd-1 */
+    int64_t shard_offset;  /* first element of the piece, within that rank's shard */
+    int64_t length;        /* elements in the piece (> 0) */
+} zero_frag_t;
+
+/* The flat partition of the model states over nd data-parallel ranks
+ * ([ZeRO card §方法适配]: states are split across DP ranks, not replicated).
+ *
+ * The tensors (numel[0..n_tensors-1] elements each) are concatenated in list
+ * order into one flat buffer; its length is padded at the tail up to a
+ * multiple of nd*align; rank r owns the contiguous shard [r*S, (r+1)*S) with
+ *     S = ceil(total / (nd*align)) * align.
+ * A tensor that straddles a shard boundary is cut there.  The same layout
+ * serves every state (fp16 params/grads, fp32 master/momentum/variance), so
+ * one rank's shard of each is one contiguous array of S elements.
+ *
+ * Host only (no device work).  Outputs: *shard_numel = S, *padded_total =
+ * nd*S, tensor_offset[i] = flat offset of tensor i (array of n_tensors, may
+ * be NULL), frags[0..] the pieces in flat order (may be NULL when frag_cap is
+ * 0).  *n_frags always receives the number of pieces; if it exceeds frag_cap,
+ * the first frag_cap are written and ZERO_ECAPACITY is returned.
+ * Errors: ZERO_EINVAL (numel NULL with n_tensors > 0, negative numel or
+ * n_tensors, NULL outputs), ZERO_ELAYOUT (nd < 1, align < 1 or not a power of
+ * two, or a padded total past 2^62). */
+int zero_partition_layout(const int64_t *numel, int64_t n_tensors, int32_t nd, int64_t align,
+                          int64_t *shard_numel, int64_t *padded_total, int64_t *tensor_offset,
+                          zero_frag_t *frags, int64_t frag_cap, int64_t *n_frags);
+
+/* ------------------------------------------------------------------ state */
+
+/* Per-rank optimizer state that lives in device memory (64 bytes, 8-byte
+ * aligned).  The first two fields are the step's partial reduction: on a
+ * multi-rank run they are the 16 bytes to sum over the ranks between
+ * zero_grad_norm_overflow and zero_adam_step. */
+typedef struct zero_state {
+    double sumsq;         /* sum of squares of the unscaled gradient, this step */
+    double found_inf;     /* > 0 if any gradient element was +-inf or NaN */
+    double loss_scale;    /* S: gradients arrive multiplied by S (a power of two) */
+    int64_t step;         /* t: steps applied so far (skipped steps excluded) */
+    int64_t good_steps;   /* clean steps since the scale last changed */
+    int64_t skipped;      /* total skipped steps */
+    double last_norm;     /* global L2 norm of the unscaled gradient, last step */
+    float last_clip;      /* clip coefficient applied by the last step (1 = none) */
+    int32_t last_skipped; /* 1 if the last step was skipped */
+} zero_state_t;
+
+/* Fills a HOST zero_state_t for a fresh optimizer: zero moments counters,
+ * the given initial loss scale (a power of two, >= 1).  Copy it to the
+ * device state buffer before the first step.  Errors: ZERO_EINVAL. */
+int zero_state_init(zero_state_t *host_state, double initial_loss_scale);
+
+/* AdamW and loss-scaler settings, read on the host at each zero_adam_step. */
+typedef struct zero_hparams {
+    double lr, beta1, beta2, eps, weight_decay;
+    double max_norm;      /* global-norm clip threshold; <= 0 turns clipping off */
+    double min_scale;     /* floor of the loss scale on overflow (>= 1) */
+    int64_t scale_window; /* clean steps in a row before the scale doubles (>= 1) */
+} zero_hparams_t;
+
+/* ------------------------------------------------------------------ lists */
+
+/* A list of n device arrays of one element type: ptrs[i] holds numel[i]
+ * elements.  ptrs and numel are HOST arrays; ptrs[i] are device pointers.
+ * A flat shard is a list of one array. */
+typedef struct zero_tlist {
+    void *const *ptrs;
+    const int64_t *numel;
+    int64_t n;
+    int32_t dtype;
+} zero_tlist_t;
+
+/* Bytes of device workspace that zero_grad_norm_overflow and zero_adam_step
+ * need for lists of up to max_tensors arrays holding up to max_total_numel
+ * elements in all.  The workspace must start on a 256-byte boundary (as
+ * cudaMalloc and PyTorch allocations do) and be zero-filled before its first
+ * use; each call leaves its reduction counter at zero again.  One workspace
+ * must not be used by two calls that may run at the same time (two streams).
+ * Device pointers passed to the library must be device (or managed) memory;
+ * this is checked for every array of a one-array list and for the first and
+ * last array of a longer list (ZERO_EINVAL). */
+size_t zero_workspace_bytes(int64_t max_tensors, int64_t max_total_numel);
+
+/* ------------------------------------------------------------------ calls */
+
+/* Gradient accumulation over micro-batches ([DS news]: the engine manages
+ * gradient accumulation):
+ *     acc[i] = (overwrite ? 0 : acc[i]) + g_0[i] + g_1[i] + ... + g_{n_bufs-1}[i]
+ * summed in binary32 in micro-batch order (with overwrite the sum starts
+ * from g_0[i]).  acc: device fp32[n]; g: HOST array of n_bufs device
+ * pointers to arrays of `dtype` (F16, BF16 or F32) with n elements;
+ * 1 <= n_bufs <= 8.  Errors: ZERO_EINVAL, ZERO_EDTYPE, ZERO_EALIGN,
+ * ZERO_ECUDA. */
+int zero_accumulate_grads(float *acc, const void *const *g, int32_t n_bufs, int32_t dtype,
+                          int64_t n, int32_t overwrite, void *stream);
+
+/* Pass 1: unscale + overflow detection + squared norm.
+ * For g = float(grad) / loss_scale over every element of `grads`
+ * (F16, BF16 or F32), computes sum g^2 (binary32 partial sums of at most 32
+ * elements, binary64 above, fixed order: the result is the same bit for bit
+ * on every run) and whether any element is +-inf or NaN.  The loss scale is
+ * read from d_state.  With accumulate = 0 the results are written to
+ * d_state->sumsq / found_inf; with accumulate = 1 they are added, so that
+ * several calls (e.g. the Nd shards of a layout on one GPU) fold into one
+ * global norm and overflow flag.  d_state: device zero_state_t.
+ * ws: device workspace of ws_bytes >= zero_workspace_bytes(grads->n, total).
+ * Errors: ZERO_EINVAL, ZERO_EDTYPE, ZERO_EALIGN, ZERO_EWORKSPACE, ZERO_ECUDA. */
+int zero_grad_norm_overflow(const zero_tlist_t *grads, zero_state_t *d_state,
+                            int32_t accumulate, void *ws, size_t ws_bytes, void *stream);
+
+/* Pass 2 (preceded by a one-thread decision kernel): the step.
+ * From d_state's global sumsq / found_inf (left there by
+ * zero_grad_norm_overflow, summed over ranks if there are several):
+ *   - found_inf > 0: the step is skipped -- no state array, p_lp or t is
+ *     touched -- and loss_scale = max(loss_scale / 2, min_scale);
+ *   - otherwise t += 1, the scale doubles after scale_window clean steps in a
+ *     row, and every element is updated in binary32 (no FMA contraction):
+ *         g  = float(grad) * (1/S);  g = g * clip   (clip = max_norm / (norm + 1e-6) when < 1)
+ *         m  = b1*m + (1-b1)*g;      v = b2*v + (1-b2)*(g*g)
+ *         p  = p - (lr/(1-b1^t) * m / (sqrt(v) * (1/sqrt(1-b2^t)) + eps) + lr*wd*p)
+ *         p_lp = p rounded to nearest even
+ *     with every scalar computed in binary64 and rounded once to binary32.
+ * sumsq and found_inf are reset to 0; last_norm, last_clip, last_skipped are
+ * set.  grads: F16, BF16 or F32; master, m, v: F32; p_lp: F16 or BF16, or
+ * NULL for no low-precision copy.  All lists must have the same n and the
+ * same numel per entry.  hp: host.  ws as for zero_grad_norm_overflow.
+ * Errors: ZERO_EINVAL, ZERO_EDTYPE, ZERO_EALIGN, ZERO_ESIZE, ZERO_EWORKSPACE,
+ * ZERO_ECUDA. */
+int zero_adam_step(const zero_tlist_t *grads, const zero_tlist_t *master, const zero_tlist_t *m,
+                   const zero_tlist_t *v, const zero_tlist_t *p_lp, const zero_hparams_t *hp,
+                   zero_state_t *d_state, void *ws, size_t ws_bytes, void *stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* ZERO_PML_H */

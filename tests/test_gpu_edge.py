@@ -1,0 +1,279 @@
+"""GPU edge cases through the C ABI: every element-type pair on ragged sizes,
+overflow at the first / last / tail position, loss-scale floor and growth,
+empty shards, partition invariance over Nd emulated ranks, list versus flat,
+run-to-run determinism, accumulation modes, and argument errors (each
+rejected on the host before any launch)."""
+import ctypes
+
+import numpy as np
+import pytest
+
+import oracle
+import zero_synth as zs
+
+torch = pytest.importorskip("torch")
+pytestmark = pytest.mark.gpu
+
+from gpu_common import (TORCH, assert_f32, assert_lp, hp_pair, oracle_step, to_dev,  # noqa: E402
+                        to_host)
+from test_gpu_parity import run_full  # noqa: E402
+
+
+@pytest.fixture(scope="module")
+def zp():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from zero_partitioned_mixed_layout_gb300 import _build
+    _build.build()
+    import zero_partitioned_mixed_layout_gb300 as zp
+    zp.lib()
+    return zp
+
+
+PAIRS = [("f16", "f16"), ("bf16", "bf16"), ("f32", "bf16"), ("f32", "f16"), ("bf16", "f16"),
+         ("f16", "bf16")]
+
+
+@pytest.mark.parametrize("gdtype,pdtype", PAIRS)
+@pytest.mark.parametrize("n", [1, 7, 8, 9, 17, 255, 2049, 65539, 1_000_003])
+def test_ragged_sizes_all_types(zp, gdtype, pdtype, n):
+    scale = 1.0 if gdtype != "f16" else 4096.0
+    run_full(zp, n, gdtype, pdtype, 2, scale, max_norm=0.5 if n > 100 else 0.0, seed=n)
+
+
+@pytest.mark.parametrize("where", ["first", "last", "tail", "middle"])
+@pytest.mark.parametrize("nan", [False, True])
+@pytest.mark.parametrize("gdtype", ["f16", "bf16", "f32"])
+def test_overflow_positions(zp, where, nan, gdtype):
+    n = 100_005  # 12,500 vectors of 8 and a tail of 5
+    pos = {"first": 0, "last": n - 1, "tail": n - 3, "middle": 54_321}[where]
+    scale = 65536.0 if gdtype == "f16" else 1.0
+    st, skipped = run_full(zp, n, gdtype, "f16" if gdtype == "f16" else "bf16", 3, scale,
+                           inf_step=1, inf_pos=pos, nan=nan)
+    assert skipped == 1 and st["step"] == 2 and st["skipped"] == 1
+    assert st["loss_scale"] == max(scale / 2, 1.0)
+
+
+def test_overflow_on_first_step_then_recovery(zp):
+    st, skipped = run_full(zp, 4099, "f16", "f16", 3, 1024.0, inf_step=0, inf_pos=4098)
+    assert skipped == 1 and st["step"] == 2 and st["loss_scale"] == 512.0
+
+
+def test_scale_floor_and_growth(zp):
+    # floor: repeated overflow at scale 2 with floor 1
+    st, _ = run_full(zp, 1000, "f16", "f16", 2, 2.0, inf_step=0, inf_pos=5)
+    assert st["loss_scale"] == 1.0
+    # growth after a window of 2 clean steps: 8 -> 16 -> 32
+    st, _ = run_full(zp, 1000, "f16", "f16", 5, 8.0, hp_kw=dict(scale_window=2))
+    assert st["loss_scale"] == 32.0 and st["good_steps"] == 1
+
+
+def test_empty_shard(zp):
+    state = zp.new_state(1024.0)
+    ws = zp.new_workspace(1, 0)
+    e16 = torch.empty(0, dtype=torch.float16, device="cuda")
+    e32 = torch.empty(0, dtype=torch.float32, device="cuda")
+    zp.zero_grad_norm_overflow(e16, state, ws)
+    zp.zero_adam_step(e16, e32, e32, e32, e16, zp.HParams(), state, ws)
+    st = zp.parse_state(state)
+    assert st["step"] == 1 and st["last_norm"] == 0.0 and st["last_skipped"] == 0
+
+
+def _shards(n_total, nd, align, seed):
+    """Flat padded master/grad arrays of a layout and their per-rank views."""
+    lay = oracle.partition_layout([n_total], nd, align)
+    p0 = np.zeros(lay.padded_total, np.float32)
+    p0[:n_total] = zs.host_master(n_total, seed)
+    return lay, p0
+
+
+@pytest.mark.parametrize("max_norm", [0.0, 0.3])
+@pytest.mark.parametrize("mode", ["exchange", "accumulate"])
+def test_partition_invariance(zp, max_norm, mode):
+    """Nd = 4 emulated ranks on one GPU, each with its own shard, state and
+    workspace.  The cross-rank sum of (sum g^2, found_inf) is done either by
+    summing the ranks' 16-byte partials (what an all-reduce would do) or by
+    the accumulate flag of pass 1.  With clipping off the concatenated shards
+    equal the unpartitioned update bit for bit.  With clipping on the two
+    norms are summed in different orders; each side is then checked against
+    the oracle (which follows that side's clip coefficient if it rounded the
+    other way) and the norms must agree to 1e-8."""
+    n_total, nd, align = 1_000_003, 4, 128
+    lay, p0 = _shards(n_total, nd, align, 7)
+    S = lay.shard_numel
+    N = lay.padded_total
+    ohp, ghp = hp_pair(max_norm=max_norm)
+    scale = 1024.0
+    full = dict(p=torch.from_numpy(p0.copy()).cuda(), m=torch.zeros(N, device="cuda"),
+                v=torch.zeros(N, device="cuda"),
+                lp=torch.zeros(N, dtype=torch.float16, device="cuda"),
+                st=zp.new_state(scale), ws=zp.new_workspace(1, N))
+    ranks = []
+    for r in range(nd):
+        ranks.append(dict(p=full["p"][r * S:(r + 1) * S].clone(),
+                          m=torch.zeros(S, device="cuda"), v=torch.zeros(S, device="cuda"),
+                          lp=torch.zeros(S, dtype=torch.float16, device="cuda"),
+                          st=zp.new_state(scale), ws=zp.new_workspace(1, S)))
+    # one oracle run following the unpartitioned side, one following the ranks
+    ora = {side: dict(p=p0.copy(), m=np.zeros(N, np.float32), v=np.zeros(N, np.float32),
+                      lp=np.zeros(N, np.uint16), sc=oracle.Scaler(loss_scale=scale))
+           for side in ("full", "ranks")}
+    for k in range(3):
+        g = np.zeros(N, np.float16)
+        g[:n_total] = zs.host_grad(n_total, 7, k, scale, "f16")
+        dg = torch.from_numpy(g).cuda()
+        zp.zero_grad_norm_overflow(dg, full["st"], full["ws"])
+        zp.zero_adam_step(dg, full["p"], full["m"], full["v"], full["lp"], ghp, full["st"],
+                          full["ws"])
+        gs = [dg[r * S:(r + 1) * S] for r in range(nd)]
+        if mode == "exchange":
+            for r in range(nd):
+                zp.zero_grad_norm_overflow(gs[r], ranks[r]["st"], ranks[r]["ws"])
+            partial = sum(rk["st"][:16].view(torch.float64) for rk in ranks)
+            for rk in ranks:
+                rk["st"][:16] = partial.view(torch.uint8)
+        else:
+            for r in range(nd):
+                zp.zero_grad_norm_overflow(gs[r], ranks[0]["st"], ranks[0]["ws"],
+                                           accumulate=r > 0)
+            for rk in ranks[1:]:
+                rk["st"][:16] = ranks[0]["st"][:16]
+        for r in range(nd):
+            rk = ranks[r]
+            zp.zero_adam_step(gs[r], rk["p"], rk["m"], rk["v"], rk["lp"], ghp, rk["st"], rk["ws"])
+        fs = zp.parse_state(full["st"])
+        rs = [zp.parse_state(rk["st"]) for rk in ranks]
+        for x in rs:
+            assert x["step"] == fs["step"] and x["loss_scale"] == fs["loss_scale"]
+            assert x["last_clip"] == rs[0]["last_clip"] and x["last_norm"] == rs[0]["last_norm"]
+            # binary32 partials grouped differently on each side: ~1e-9 apart
+            assert abs(x["last_norm"] - fs["last_norm"]) <= 1e-8 * fs["last_norm"]
+        for side, gst in (("full", fs), ("ranks", rs[0])):
+            o = ora[side]
+            oracle_step([g], "f16", [o["p"]], [o["m"]], [o["v"]], [o["lp"]], "f16", ohp,
+                        o["sc"], gst)
+    cat = {key: torch.cat([rk[key] for rk in ranks]) for key in ("p", "m", "v", "lp")}
+    for key in ("p", "m", "v"):
+        assert_f32(full[key].cpu().numpy(), ora["full"][key], f"unpartitioned {key}")
+        assert_f32(cat[key].cpu().numpy(), ora["ranks"][key], f"concatenated shards {key}")
+    assert np.array_equal(to_host(full["lp"]), ora["full"]["lp"])
+    assert np.array_equal(to_host(cat["lp"]), ora["ranks"]["lp"])
+    if max_norm == 0.0:
+        for key in ("p", "m", "v", "lp"):
+            assert torch.equal(cat[key], full[key]), f"shards differ from the unpartitioned {key}"
+    # the zero padding stays exactly zero
+    assert not full["p"][n_total:].any() and not full["m"][n_total:].any()
+    assert not full["v"][n_total:].any()
+
+
+def test_list_equals_flat(zp):
+    """One flat array versus the same elements cut into a list of arrays
+    (ragged pieces): identical elementwise results, norms within 1e-8."""
+    sizes = [1, 9, 65536, 70001, 3, 131072 * 2 + 5, 8]
+    n = sum(sizes)
+    ohp, ghp = hp_pair()
+    p0 = zs.host_master(n, 3)
+    flat = [torch.from_numpy(p0.copy()).cuda(), torch.zeros(n, device="cuda"),
+            torch.zeros(n, device="cuda"), torch.zeros(n, dtype=torch.float16, device="cuda")]
+    offs = np.concatenate([[0], np.cumsum(sizes)])
+    pieces = [[torch.from_numpy(p0[offs[i]:offs[i + 1]].copy()).cuda(),
+               torch.zeros(sizes[i], device="cuda"), torch.zeros(sizes[i], device="cuda"),
+               torch.zeros(sizes[i], dtype=torch.float16, device="cuda")] for i in range(len(sizes))]
+    st_f, st_l = zp.new_state(256.0), zp.new_state(256.0)
+    ws_f, ws_l = zp.new_workspace(1, n), zp.new_workspace(len(sizes), n)
+    for k in range(3):
+        g = zs.host_grad(n, 3, k, 256.0, "f16")
+        dg = torch.from_numpy(g).cuda()
+        gl = [torch.from_numpy(g[offs[i]:offs[i + 1]].copy()).cuda() for i in range(len(sizes))]
+        zp.zero_grad_norm_overflow(dg, st_f, ws_f)
+        zp.zero_adam_step(dg, *flat, ghp, st_f, ws_f)
+        zp.zero_grad_norm_overflow(gl, st_l, ws_l)
+        zp.zero_adam_step(gl, [q[0] for q in pieces], [q[1] for q in pieces],
+                          [q[2] for q in pieces], [q[3] for q in pieces], ghp, st_l, ws_l)
+        a, b = zp.parse_state(st_f), zp.parse_state(st_l)
+        assert abs(a["last_norm"] - b["last_norm"]) <= 1e-8 * a["last_norm"]
+    for j in range(4):
+        cat = torch.cat([q[j] for q in pieces])
+        assert torch.equal(cat, flat[j])
+
+
+def test_run_to_run_determinism(zp):
+    """Two runs of the same steps give the same bits, norm included."""
+    n = 3_000_017
+    outs = []
+    for _ in range(2):
+        _, ghp = hp_pair(max_norm=0.7)
+        p = torch.from_numpy(zs.host_master(n, 11)).cuda()
+        m, v = torch.zeros(n, device="cuda"), torch.zeros(n, device="cuda")
+        lp = torch.zeros(n, dtype=torch.float16, device="cuda")
+        st, ws = zp.new_state(1024.0), zp.new_workspace(1, n)
+        norms = []
+        for k in range(3):
+            dg = torch.from_numpy(zs.host_grad(n, 11, k, 1024.0, "f16")).cuda()
+            zp.zero_grad_norm_overflow(dg, st, ws)
+            zp.zero_adam_step(dg, p, m, v, lp, ghp, st, ws)
+            norms.append(zp.parse_state(st)["last_norm"])
+        outs.append((norms, p.cpu(), m.cpu(), v.cpu(), lp.cpu()))
+    assert outs[0][0] == outs[1][0]
+    for a, b in zip(outs[0][1:], outs[1][1:]):
+        assert torch.equal(a, b)
+
+
+@pytest.mark.parametrize("gdtype", ["f16", "bf16", "f32"])
+@pytest.mark.parametrize("nb", [1, 2, 4, 8])
+@pytest.mark.parametrize("overwrite", [True, False])
+def test_accumulate(zp, gdtype, nb, overwrite):
+    n = 200_003
+    bufs = [zs.host_grad(n, 5, 0, 1.0, gdtype, micro=j) for j in range(nb)]
+    acc0 = zs.host_normal(n, 1e-3, 5, "misc")
+    ref = acc0.copy()
+    oracle.accumulate(ref, bufs, gdtype, overwrite)
+    dacc = torch.from_numpy(acc0.copy()).cuda()
+    zp.zero_accumulate_grads(dacc, [to_dev(b, gdtype) for b in bufs], overwrite)
+    assert dacc.cpu().numpy().tobytes() == ref.tobytes()
+
+
+def test_argument_errors_launch_nothing(zp):
+    n = 4096
+    g = torch.zeros(n + 8, dtype=torch.float16, device="cuda")
+    p = torch.zeros(n + 8, device="cuda")
+    m, v = torch.zeros(n, device="cuda"), torch.zeros(n, device="cuda")
+    lp = torch.zeros(n, dtype=torch.float16, device="cuda")
+    st = zp.new_state(1024.0)
+    ws = zp.new_workspace(1, n)
+    before = st.clone()
+    hp = zp.HParams()
+    with pytest.raises(zp.ZeroError) as e:  # grad starting 2 bytes off a 16-byte boundary
+        zp.zero_grad_norm_overflow(g[1:n + 1], st, ws)
+    assert e.value.code == -2
+    with pytest.raises(zp.ZeroError) as e:
+        zp.zero_adam_step(g[:n], p[1:n + 1], m, v, lp, hp, st, ws)
+    assert e.value.code == -2
+    with pytest.raises(zp.ZeroError) as e:  # sizes differ
+        zp.zero_adam_step(g[:n], p[:n - 8], m, v, lp, hp, st, ws)
+    assert e.value.code == -4
+    with pytest.raises(zp.ZeroError) as e:  # master must be fp32
+        zp.zero_adam_step(g[:n], g[:n], m, v, lp, hp, st, ws)
+    assert e.value.code == -3
+    with pytest.raises(zp.ZeroError) as e:  # low-precision copy must be 16-bit
+        zp.zero_adam_step(g[:n], p[:n], m, v, p[:n], hp, st, ws)
+    assert e.value.code == -3
+    with pytest.raises(zp.ZeroError) as e:  # workspace too small
+        zp.zero_grad_norm_overflow(g[:n], st, ws[:256])
+    assert e.value.code == -5
+    with pytest.raises(zp.ZeroError) as e:  # bad hyper-parameters
+        zp.zero_adam_step(g[:n], p[:n], m, v, lp, zp.HParams(beta1=1.0), st, ws)
+    assert e.value.code == -1
+    # host memory passed through the raw C ABI is refused
+    host = np.zeros(n, np.float16)
+    lib = zp.lib()
+    from zero_partitioned_mixed_layout_gb300.binding import _TList
+    ptrs = (ctypes.c_void_p * 1)(host.ctypes.data)
+    numel = (ctypes.c_int64 * 1)(n)
+    tl = _TList(ptrs, numel, 1, 0)
+    rc = lib.zero_grad_norm_overflow(ctypes.byref(tl), ctypes.c_void_p(st.data_ptr()), 0,
+                                     ctypes.c_void_p(ws.data_ptr()), ws.numel(),
+                                     ctypes.c_void_p(torch.cuda.current_stream().cuda_stream))
+    assert rc == -1
+    torch.cuda.synchronize()
+    assert torch.equal(st, before), "a rejected call changed the state"

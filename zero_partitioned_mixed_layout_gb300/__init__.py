@@ -1,0 +1,29 @@
+"""ZeRO partitioned mixed-precision optimizer step for NVIDIA GB300 (sm_103a).
+
+The data-parallel hot path of ZeRO: the model states are flattened into one
+padded buffer and partitioned over Nd ranks, and one rank's shard is updated
+by hand-written CUDA kernels (gradient accumulation; unscale + overflow +
+global squared norm; clip + AdamW + cast to fp16/bf16).  The C ABI is in
+``include/zero_pml.h``; this package is its Python binding.
+"""
+from .binding import (  # noqa: F401
+    HParams,
+    Layout,
+    ZeroError,
+    ZERO_BF16,
+    ZERO_F16,
+    ZERO_F32,
+    STATE_BYTES,
+    LIB_PATH,
+    lib,
+    new_state,
+    new_workspace,
+    parse_state,
+    zero_accumulate_grads,
+    zero_adam_step,
+    zero_grad_norm_overflow,
+    zero_partition_layout,
+    zero_state_init,
+    zero_strerror,
+    zero_workspace_bytes,
+)

@@ -1,0 +1,271 @@
+"""Thin Python binding of libzero_pml.so (ctypes): argument marshalling only.
+
+Every function here has the name of the C entry point it calls and does no
+arithmetic of the optimizer step: PyTorch tensors are reduced to device
+pointers and element counts, and every step of the path runs in the CUDA
+kernels of the library.  There is no fallback: if the library is missing or
+was not built for this GPU, the first call raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from dataclasses import dataclass
+from typing import Sequence
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libzero_pml.so")
+
+ZERO_OK = 0
+ZERO_F16, ZERO_BF16, ZERO_F32 = 0, 1, 2
+STATE_BYTES = 64
+
+
+class ZeroError(RuntimeError):
+    def __init__(self, code: int, where: str):
+        self.code = code
+        super().__init__(f"{where}: {zero_strerror(code)} (code {code})")
+
+
+class _Frag(ctypes.Structure):
+    _fields_ = [("tensor", ctypes.c_int64), ("tensor_offset", ctypes.c_int64),
+                ("rank", ctypes.c_int64), ("shard_offset", ctypes.c_int64),
+                ("length", ctypes.c_int64)]
+
+
+class _State(ctypes.Structure):
+    _fields_ = [("sumsq", ctypes.c_double), ("found_inf", ctypes.c_double),
+                ("loss_scale", ctypes.c_double), ("step", ctypes.c_int64),
+                ("good_steps", ctypes.c_int64), ("skipped", ctypes.c_int64),
+                ("last_norm", ctypes.c_double), ("last_clip", ctypes.c_float),
+                ("last_skipped", ctypes.c_int32)]
+
+
+class _HParams(ctypes.Structure):
+    _fields_ = [("lr", ctypes.c_double), ("beta1", ctypes.c_double),
+                ("beta2", ctypes.c_double), ("eps", ctypes.c_double),
+                ("weight_decay", ctypes.c_double), ("max_norm", ctypes.c_double),
+                ("min_scale", ctypes.c_double), ("scale_window", ctypes.c_int64)]
+
+
+class _TList(ctypes.Structure):
+    _fields_ = [("ptrs", ctypes.POINTER(ctypes.c_void_p)),
+                ("numel", ctypes.POINTER(ctypes.c_int64)),
+                ("n", ctypes.c_int64), ("dtype", ctypes.c_int32)]
+
+
+assert ctypes.sizeof(_State) == STATE_BYTES
+
+_lib = None
+
+
+def lib():
+    """The loaded library; raises if it has not been built."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(
+                f"{LIB_PATH} is missing: build it first "
+                "(python -c 'import __graft_entry__ as g; g.build()')")
+        so = ctypes.CDLL(LIB_PATH)
+        vp, i64, i32 = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int32
+        so.zero_strerror.argtypes = [ctypes.c_int]
+        so.zero_strerror.restype = ctypes.c_char_p
+        so.zero_partition_layout.argtypes = [ctypes.POINTER(i64), i64, i32, i64,
+                                             ctypes.POINTER(i64), ctypes.POINTER(i64),
+                                             ctypes.POINTER(i64), ctypes.POINTER(_Frag), i64,
+                                             ctypes.POINTER(i64)]
+        so.zero_state_init.argtypes = [ctypes.POINTER(_State), ctypes.c_double]
+        so.zero_workspace_bytes.argtypes = [i64, i64]
+        so.zero_workspace_bytes.restype = ctypes.c_size_t
+        so.zero_accumulate_grads.argtypes = [vp, ctypes.POINTER(vp), i32, i32, i64, i32, vp]
+        so.zero_grad_norm_overflow.argtypes = [ctypes.POINTER(_TList), vp, i32, vp,
+                                               ctypes.c_size_t, vp]
+        so.zero_adam_step.argtypes = [ctypes.POINTER(_TList)] * 5 + [
+            ctypes.POINTER(_HParams), vp, vp, ctypes.c_size_t, vp]
+        for f in ("zero_partition_layout", "zero_state_init", "zero_accumulate_grads",
+                  "zero_grad_norm_overflow", "zero_adam_step"):
+            getattr(so, f).restype = ctypes.c_int
+        _lib = so
+    return _lib
+
+
+def _check(rc: int, where: str) -> None:
+    if rc != ZERO_OK:
+        raise ZeroError(rc, where)
+
+
+def zero_strerror(code: int) -> str:
+    return lib().zero_strerror(int(code)).decode()
+
+
+# ------------------------------------------------------------------ layout
+
+@dataclass
+class Layout:
+    shard_numel: int
+    padded_total: int
+    tensor_offset: np.ndarray  # int64 [n_tensors]
+    frags: np.ndarray          # int64 [n_frags, 5]: tensor, tensor_offset, rank, shard_offset, length
+
+
+def zero_partition_layout(numel: Sequence[int], nd: int, align: int = 128) -> Layout:
+    """The flat partition of the tensor list over nd ranks (host only)."""
+    n = len(numel)
+    arr = (ctypes.c_int64 * max(n, 1))(*[int(x) for x in numel])
+    offs = (ctypes.c_int64 * max(n, 1))()
+    shard, padded, nfr = ctypes.c_int64(), ctypes.c_int64(), ctypes.c_int64()
+    rc = lib().zero_partition_layout(arr, n, int(nd), int(align), ctypes.byref(shard),
+                                     ctypes.byref(padded), offs, None, 0, ctypes.byref(nfr))
+    if rc not in (ZERO_OK, -6):
+        _check(rc, "zero_partition_layout")
+    cap = nfr.value
+    frags = (_Frag * max(cap, 1))()
+    rc = lib().zero_partition_layout(arr, n, int(nd), int(align), ctypes.byref(shard),
+                                     ctypes.byref(padded), offs, frags, cap, ctypes.byref(nfr))
+    _check(rc, "zero_partition_layout")
+    fr = np.frombuffer(frags, dtype=np.int64, count=5 * cap).reshape(cap, 5).copy()
+    return Layout(shard.value, padded.value, np.frombuffer(offs, np.int64, count=n).copy(), fr)
+
+
+# ------------------------------------------------------------------ state, workspace
+
+def zero_state_init(initial_loss_scale: float) -> bytes:
+    """The 64-byte initial state (host bytes) for a fresh optimizer."""
+    st = _State()
+    _check(lib().zero_state_init(ctypes.byref(st), float(initial_loss_scale)), "zero_state_init")
+    return ctypes.string_at(ctypes.byref(st), STATE_BYTES)
+
+
+def new_state(initial_loss_scale: float, device="cuda"):
+    """A device uint8[64] tensor holding zero_state_init's state."""
+    import torch
+    host = torch.frombuffer(bytearray(zero_state_init(initial_loss_scale)), dtype=torch.uint8)
+    return host.to(device)
+
+
+def parse_state(buf) -> dict:
+    """Decodes a zero_state_t from 64 host bytes (or a tensor holding them)."""
+    if hasattr(buf, "cpu"):
+        buf = bytes(buf.cpu().numpy().tobytes())
+    st = _State.from_buffer_copy(buf)
+    return {name: getattr(st, name) for name, _ in _State._fields_}
+
+
+def zero_workspace_bytes(max_tensors: int, max_total_numel: int) -> int:
+    return int(lib().zero_workspace_bytes(int(max_tensors), int(max_total_numel)))
+
+
+def new_workspace(max_tensors: int, max_total_numel: int, device="cuda"):
+    """A zero-filled device workspace of zero_workspace_bytes() bytes."""
+    import torch
+    return torch.zeros(zero_workspace_bytes(max_tensors, max_total_numel), dtype=torch.uint8,
+                       device=device)
+
+
+# ------------------------------------------------------------------ marshalling
+
+def _dtype_code(t) -> int:
+    import torch
+    m = {torch.float16: ZERO_F16, torch.bfloat16: ZERO_BF16, torch.float32: ZERO_F32}
+    if t.dtype not in m:
+        raise TypeError(f"unsupported element type {t.dtype}")
+    return m[t.dtype]
+
+
+def _device_tensor(t, what: str):
+    if not t.is_cuda:
+        raise ValueError(f"{what} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{what} must be contiguous")
+    return t
+
+
+class _ListArgs:
+    """Keeps the ctypes arrays of one zero_tlist_t alive for the call."""
+
+    def __init__(self, tensors, what: str):
+        if not isinstance(tensors, (list, tuple)):
+            tensors = [tensors]
+        for t in tensors:
+            _device_tensor(t, what)
+        codes = {_dtype_code(t) for t in tensors}
+        if len(codes) > 1:
+            raise TypeError(f"{what}: mixed element types in one list")
+        n = len(tensors)
+        self.ptrs = (ctypes.c_void_p * max(n, 1))(*[t.data_ptr() for t in tensors])
+        self.numel = (ctypes.c_int64 * max(n, 1))(*[t.numel() for t in tensors])
+        self.tl = _TList(self.ptrs, self.numel, n, codes.pop() if codes else ZERO_F32)
+        self.device = tensors[0].device if n else None
+
+
+def _stream_ptr(stream, device):
+    import torch
+    if stream is None:
+        stream = torch.cuda.current_stream(device)
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+@dataclass
+class HParams:
+    lr: float = 1e-3
+    beta1: float = 0.9
+    beta2: float = 0.999
+    eps: float = 1e-8
+    weight_decay: float = 0.01
+    max_norm: float = 0.0
+    min_scale: float = 1.0
+    scale_window: int = 1000
+
+    def _c(self) -> _HParams:
+        return _HParams(self.lr, self.beta1, self.beta2, self.eps, self.weight_decay,
+                        self.max_norm, self.min_scale, int(self.scale_window))
+
+
+# ------------------------------------------------------------------ device calls
+
+def zero_accumulate_grads(acc, grads, overwrite: bool, stream=None) -> None:
+    """acc (=|+=) grads[0] + grads[1] + ... (binary32, micro-batch order)."""
+    _device_tensor(acc, "acc")
+    grads = list(grads)
+    for g in grads:
+        _device_tensor(g, "grad")
+        if g.numel() != acc.numel():
+            raise ValueError("micro-batch gradient and accumulator sizes differ")
+    codes = {_dtype_code(g) for g in grads}
+    if len(codes) != 1:
+        raise TypeError("micro-batch gradients must share one element type")
+    ptrs = (ctypes.c_void_p * len(grads))(*[g.data_ptr() for g in grads])
+    rc = lib().zero_accumulate_grads(ctypes.c_void_p(acc.data_ptr()), ptrs, len(grads),
+                                     codes.pop(), acc.numel(), int(bool(overwrite)),
+                                     _stream_ptr(stream, acc.device))
+    _check(rc, "zero_accumulate_grads")
+
+
+def zero_grad_norm_overflow(grads, state, ws, accumulate: bool = False, stream=None) -> None:
+    """Pass 1 over one array or a list of arrays; results land in ``state``."""
+    la = _ListArgs(grads, "grads")
+    _device_tensor(state, "state")
+    _device_tensor(ws, "workspace")
+    rc = lib().zero_grad_norm_overflow(ctypes.byref(la.tl), ctypes.c_void_p(state.data_ptr()),
+                                       int(bool(accumulate)), ctypes.c_void_p(ws.data_ptr()),
+                                       ws.numel(), _stream_ptr(stream, state.device))
+    _check(rc, "zero_grad_norm_overflow")
+
+
+def zero_adam_step(grads, master, m, v, p_lp, hp: HParams, state, ws, stream=None) -> None:
+    """The decision kernel and pass 2 over one shard or a list of arrays."""
+    lg = _ListArgs(grads, "grads")
+    lp_, lm, lv = _ListArgs(master, "master"), _ListArgs(m, "m"), _ListArgs(v, "v")
+    ll = _ListArgs(p_lp, "p_lp") if p_lp is not None else None
+    _device_tensor(state, "state")
+    _device_tensor(ws, "workspace")
+    h = hp._c()
+    rc = lib().zero_adam_step(ctypes.byref(lg.tl), ctypes.byref(lp_.tl), ctypes.byref(lm.tl),
+                              ctypes.byref(lv.tl), ctypes.byref(ll.tl) if ll else None,
+                              ctypes.byref(h), ctypes.c_void_p(state.data_ptr()),
+                              ctypes.c_void_p(ws.data_ptr()), ws.numel(),
+                              _stream_ptr(stream, state.device))
+    _check(rc, "zero_adam_step")

@@ -1,0 +1,955 @@
+// CUDA part of the C ABI (sm_103a): gradient accumulation, pass 1 (unscale,
+// overflow, squared norm), the one-thread step decision, and pass 2 (clip,
+// AdamW, cast) over one rank's flat shard or over a list of arrays.
+//
+// Sources: "ZeRO: Memory Optimizations Toward Training Trillion Parameter
+// Models - 中文验证版" (ai-papers.xuzou.cn), sections 瓶颈 (bottleneck: the
+// mixed-precision Adam state is fp16 param + grad and fp32 master, momentum,
+// variance) and 方法适配 (method: each data-parallel rank owns one partition
+// of that state and updates only it); DeepSpeed release news
+// (lxsoso.com/blog/19320.html): mixed precision and gradient accumulation.
+// The update is Adam (Kingma & Ba 2015) with decoupled weight decay
+// (Loshchilov & Hutter 2019) and dynamic loss scaling (Micikevicius et al.
+// 2018).
+//
+// Design: every kernel here streams HBM once.  Per element pass 2 reads
+// 2 + 12 bytes and writes 12 + 2 bytes (fp16 grad/param): 28 bytes.  Loads
+// and stores are 16-byte vectors with streaming cache hints, eight elements
+// per thread per iteration; grids are a whole number of waves over the SMs.
+// The element arithmetic uses explicit round-to-nearest intrinsics, so no
+// multiply-add is ever contracted and the result is the IEEE binary32 value
+// of the documented expression, bit for bit.
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+#include <mutex>
+#include <unordered_map>
+#include <vector>
+
+#include "zero_pml_internal.h"
+
+namespace zpml {
+namespace {
+
+constexpr int kWarps = kThreads / 32;
+
+// ------------------------------------------------------------- element types
+
+template <int DT>
+struct Elem;
+
+// binary16: 8 elements in one 16-byte word group
+template <>
+struct Elem<ZERO_F16> {
+    static constexpr int kWords = 1;
+    static constexpr int kBytes = 2;
+    __device__ static __forceinline__ void to_float(const uint4 *w, float *f)
+    {
+        const __half2 *h = reinterpret_cast<const __half2 *>(w);
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            const float2 x = __half22float2(h[k]);
+            f[2 * k] = x.x;
+            f[2 * k + 1] = x.y;
+        }
+    }
+    // A binary16 is inf or NaN iff its exponent field is all ones: adding
+    // 0x0400 to the masked field carries into bit 15 exactly then.
+    __device__ static __forceinline__ uint32_t nonfinite(const uint4 *w)
+    {
+        const uint32_t a = ((w->x & 0x7C007C00u) + 0x04000400u) | ((w->y & 0x7C007C00u) + 0x04000400u) |
+                           ((w->z & 0x7C007C00u) + 0x04000400u) | ((w->w & 0x7C007C00u) + 0x04000400u);
+        return a & 0x80008000u;
+    }
+    __device__ static __forceinline__ float scalar(const void *p, int64_t i)
+    {
+        return __half2float(static_cast<const __half *>(p)[i]);
+    }
+    __device__ static __forceinline__ uint32_t scalar_nonfinite(const void *p, int64_t i)
+    {
+        return (static_cast<const uint16_t *>(p)[i] & 0x7C00u) == 0x7C00u;
+    }
+};
+
+// bfloat16: exponent field 0x7F80
+template <>
+struct Elem<ZERO_BF16> {
+    static constexpr int kWords = 1;
+    static constexpr int kBytes = 2;
+    __device__ static __forceinline__ void to_float(const uint4 *w, float *f)
+    {
+        const __nv_bfloat162 *h = reinterpret_cast<const __nv_bfloat162 *>(w);
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            const float2 x = __bfloat1622float2(h[k]);
+            f[2 * k] = x.x;
+            f[2 * k + 1] = x.y;
+        }
+    }
+    __device__ static __forceinline__ uint32_t nonfinite(const uint4 *w)
+    {
+        const uint32_t a = ((w->x & 0x7F807F80u) + 0x00800080u) | ((w->y & 0x7F807F80u) + 0x00800080u) |
+                           ((w->z & 0x7F807F80u) + 0x00800080u) | ((w->w & 0x7F807F80u) + 0x00800080u);
+        return a & 0x80008000u;
+    }
+    __device__ static __forceinline__ float scalar(const void *p, int64_t i)
+    {
+        return __bfloat162float(static_cast<const __nv_bfloat16 *>(p)[i]);
+    }
+    __device__ static __forceinline__ uint32_t scalar_nonfinite(const void *p, int64_t i)
+    {
+        return (static_cast<const uint16_t *>(p)[i] & 0x7F80u) == 0x7F80u;
+    }
+};
+
+// binary32: 8 elements in two 16-byte words
+template <>
+struct Elem<ZERO_F32> {
+    static constexpr int kWords = 2;
+    static constexpr int kBytes = 4;
+    __device__ static __forceinline__ void to_float(const uint4 *w, float *f)
+    {
+        f[0] = __uint_as_float(w[0].x);
+        f[1] = __uint_as_float(w[0].y);
+        f[2] = __uint_as_float(w[0].z);
+        f[3] = __uint_as_float(w[0].w);
+        f[4] = __uint_as_float(w[1].x);
+        f[5] = __uint_as_float(w[1].y);
+        f[6] = __uint_as_float(w[1].z);
+        f[7] = __uint_as_float(w[1].w);
+    }
+    __device__ static __forceinline__ uint32_t nonfinite(const uint4 *w)
+    {
+        uint32_t a = 0;
+#pragma unroll
+        for (int q = 0; q < 2; ++q)
+            a |= ((w[q].x & 0x7F800000u) + 0x00800000u) | ((w[q].y & 0x7F800000u) + 0x00800000u) |
+                 ((w[q].z & 0x7F800000u) + 0x00800000u) | ((w[q].w & 0x7F800000u) + 0x00800000u);
+        return a & 0x80000000u;
+    }
+    __device__ static __forceinline__ float scalar(const void *p, int64_t i)
+    {
+        return static_cast<const float *>(p)[i];
+    }
+    __device__ static __forceinline__ uint32_t scalar_nonfinite(const void *p, int64_t i)
+    {
+        return (__float_as_uint(static_cast<const float *>(p)[i]) & 0x7F800000u) == 0x7F800000u;
+    }
+};
+
+// Low-precision parameter copy: binary32 -> 16-bit, round to nearest even.
+template <int PT>
+struct LowP;
+
+template <>
+struct LowP<ZERO_F16> {
+    __device__ static __forceinline__ uint4 pack(const float *f)
+    {
+        uint4 r;
+        __half2 h0 = __floats2half2_rn(f[0], f[1]), h1 = __floats2half2_rn(f[2], f[3]);
+        __half2 h2 = __floats2half2_rn(f[4], f[5]), h3 = __floats2half2_rn(f[6], f[7]);
+        r.x = *reinterpret_cast<uint32_t *>(&h0);
+        r.y = *reinterpret_cast<uint32_t *>(&h1);
+        r.z = *reinterpret_cast<uint32_t *>(&h2);
+        r.w = *reinterpret_cast<uint32_t *>(&h3);
+        return r;
+    }
+    __device__ static __forceinline__ void store(void *p, int64_t i, float x)
+    {
+        static_cast<__half *>(p)[i] = __float2half_rn(x);
+    }
+};
+
+template <>
+struct LowP<ZERO_BF16> {
+    __device__ static __forceinline__ uint4 pack(const float *f)
+    {
+        uint4 r;
+        __nv_bfloat162 h0 = __floats2bfloat162_rn(f[0], f[1]), h1 = __floats2bfloat162_rn(f[2], f[3]);
+        __nv_bfloat162 h2 = __floats2bfloat162_rn(f[4], f[5]), h3 = __floats2bfloat162_rn(f[6], f[7]);
+        r.x = *reinterpret_cast<uint32_t *>(&h0);
+        r.y = *reinterpret_cast<uint32_t *>(&h1);
+        r.z = *reinterpret_cast<uint32_t *>(&h2);
+        r.w = *reinterpret_cast<uint32_t *>(&h3);
+        return r;
+    }
+    __device__ static __forceinline__ void store(void *p, int64_t i, float x)
+    {
+        static_cast<__nv_bfloat16 *>(p)[i] = __float2bfloat16_rn(x);
+    }
+};
+
+// ------------------------------------------------------------- reductions
+
+__device__ __forceinline__ double warp_sum(double x)
+{
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1)
+        x += __shfl_xor_sync(0xffffffffu, x, o);
+    return x;
+}
+
+// binary32 sum of 8 lanes in a fixed tree
+__device__ __forceinline__ float tree8(const float *a)
+{
+    return __fadd_rn(__fadd_rn(__fadd_rn(a[0], a[1]), __fadd_rn(a[2], a[3])),
+                     __fadd_rn(__fadd_rn(a[4], a[5]), __fadd_rn(a[6], a[7])));
+}
+
+// Block sum (fixed order) of a per-thread binary64 value and OR of a flag.
+// Result valid in thread 0.
+__device__ __forceinline__ void block_reduce(double &tot, uint32_t &bad)
+{
+    __shared__ double s_tot[kWarps];
+    __shared__ uint32_t s_bad[kWarps];
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    tot = warp_sum(tot);
+    const uint32_t b = __any_sync(0xffffffffu, bad != 0);
+    if (lane == 0) {
+        s_tot[warp] = tot;
+        s_bad[warp] = b;
+    }
+    __syncthreads();
+    if (warp == 0) {
+        double t = lane < kWarps ? s_tot[lane] : 0.0;
+        const uint32_t bb = __any_sync(0xffffffffu, lane < kWarps && s_bad[lane] != 0);
+        tot = warp_sum(t);
+        bad = bb;
+    }
+    __syncthreads();
+}
+
+// End of the norm pass in every block: publish this block's partial; the
+// block that takes the last ticket sums all partials in block order and
+// writes (or adds) the unscaled totals into the state.  No block waits on
+// another: the last block to arrive does the final sum.
+__device__ void norm_finish(double tot, uint32_t bad, double2 *partials, WsHeader *hdr,
+                            zero_state_t *st, int accumulate)
+{
+    __shared__ bool s_last;
+    block_reduce(tot, bad);
+    if (threadIdx.x == 0) {
+        partials[blockIdx.x] = make_double2(tot, bad ? 1.0 : 0.0);
+        __threadfence();
+        const unsigned int ticket = atomicAdd(&hdr->ticket, 1u);
+        s_last = (ticket == gridDim.x - 1);
+    }
+    __syncthreads();
+    if (!s_last)
+        return;
+    __threadfence();
+    double t = 0.0;
+    uint32_t b = 0;
+    for (int j = threadIdx.x; j < (int)gridDim.x; j += kThreads) {
+        const double2 q = __ldcg(partials + j);
+        t += q.x;
+        b |= (q.y != 0.0);
+    }
+    block_reduce(t, b);
+    if (threadIdx.x == 0) {
+        // the partials hold sums of squares of the stored (scaled) gradient;
+        // the loss scale is a power of two, so this rescaling is exact
+        const double inv = 1.0 / st->loss_scale;
+        const double sum = t * inv * inv;
+        st->sumsq = accumulate ? st->sumsq + sum : sum;
+        st->found_inf = (accumulate ? st->found_inf : 0.0) + (b ? 1.0 : 0.0);
+        hdr->ticket = 0u;
+    }
+}
+
+// ------------------------------------------------------------- pass 1
+
+// Squares of 4 vectors (32 elements) into 8 binary32 lanes, then one binary64
+// add per thread: the binary64 pipe sees one add per 32 elements.
+template <int GT>
+__device__ __forceinline__ void norm_group(const uint4 (*w)[Elem<GT>::kWords], int count, double &tot,
+                                           uint32_t &bad)
+{
+    float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+        if (k < count) {
+            bad |= Elem<GT>::nonfinite(w[k]);
+            float f[8];
+            Elem<GT>::to_float(w[k], f);
+#pragma unroll
+            for (int e = 0; e < 8; ++e)
+                acc[e] = __fmaf_rn(f[e], f[e], acc[e]);
+        }
+    }
+    tot += (double)tree8(acc);
+}
+
+// Vectors [0, nv) of one array, thread `t` of `nt` taking vectors
+// t, t + nt, ... four at a time; then the scalar tail [8*nv, n).
+template <int GT>
+__device__ __forceinline__ void norm_range(const void *g, int64_t n, int64_t t, int64_t nt, double &tot,
+                                           uint32_t &bad)
+{
+    constexpr int W = Elem<GT>::kWords;
+    const uint4 *gv = static_cast<const uint4 *>(g);
+    const int64_t nv = n >> 3;
+    for (int64_t i = t; i < nv; i += 4 * nt) {
+        uint4 w[4][W];
+        int count = 0;
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            const int64_t j = i + k * nt;
+            if (j < nv) {
+#pragma unroll
+                for (int q = 0; q < W; ++q)
+                    w[k][q] = __ldcs(gv + j * W + q);
+                count = k + 1;
+            }
+        }
+        norm_group<GT>(w, count, tot, bad);
+    }
+    const int64_t tail = n - (nv << 3);
+    if (t < tail) {
+        const float x = Elem<GT>::scalar(g, (nv << 3) + t);
+        bad |= Elem<GT>::scalar_nonfinite(g, (nv << 3) + t);
+        tot += (double)__fmul_rn(x, x);
+    }
+}
+
+template <int GT>
+__global__ void __launch_bounds__(kThreads)
+    k_norm_flat(const void *__restrict__ g, int64_t n, double2 *partials, WsHeader *hdr, zero_state_t *st,
+                int accumulate)
+{
+    double tot = 0.0;
+    uint32_t bad = 0;
+    norm_range<GT>(g, n, (int64_t)blockIdx.x * kThreads + threadIdx.x, (int64_t)gridDim.x * kThreads, tot,
+                   bad);
+    norm_finish(tot, bad, partials, hdr, st, accumulate);
+}
+
+template <int GT>
+__global__ void __launch_bounds__(kThreads)
+    k_norm_list(const TensorEntry *__restrict__ ents, const Chunk *__restrict__ chunks, int64_t n_chunks,
+                double2 *partials, WsHeader *hdr, zero_state_t *st, int accumulate)
+{
+    double tot = 0.0;
+    uint32_t bad = 0;
+    for (int64_t c = blockIdx.x; c < n_chunks; c += gridDim.x) {
+        const Chunk ch = chunks[c];
+        const TensorEntry e = ents[ch.tensor];
+        const int64_t start = (int64_t)ch.index * kChunk;
+        const int64_t len = min(kChunk, e.numel - start);
+        const void *g = static_cast<const char *>(e.g) + start * Elem<GT>::kBytes;
+        norm_range<GT>(g, len, threadIdx.x, kThreads, tot, bad);
+    }
+    norm_finish(tot, bad, partials, hdr, st, accumulate);
+}
+
+// ------------------------------------------------------------- decision
+
+struct DecideArgs {
+    double lr, beta1, beta2, eps, weight_decay, max_norm, min_scale;
+    int64_t scale_window;
+};
+
+// One thread: skip or apply, loss-scale and step bookkeeping, and the step
+// scalars (binary64, each rounded once to binary32).
+__global__ void k_decide(zero_state_t *st, StepScalars *out, DecideArgs a)
+{
+    if (threadIdx.x != 0 || blockIdx.x != 0)
+        return;
+    zero_state_t s = *st;
+    StepScalars o;
+    o.inv_scale = (float)(1.0 / s.loss_scale);
+    o.clip = 1.0f;
+    o.b1 = o.omb1 = o.b2 = o.omb2 = o.eps = o.step_size = o.isb2 = o.lrwd = 0.0f;
+    o.pad = 0;
+    const double norm = sqrt(s.sumsq);
+    if (s.found_inf != 0.0) {
+        o.skip = 1;
+        const double half = s.loss_scale * 0.5;
+        s.loss_scale = half < a.min_scale ? a.min_scale : half;
+        s.good_steps = 0;
+        s.skipped += 1;
+    } else {
+        o.skip = 0;
+        s.step += 1;
+        s.good_steps += 1;
+        if (s.good_steps >= a.scale_window) {
+            s.loss_scale *= 2.0;
+            s.good_steps = 0;
+        }
+        double clip = 1.0;
+        if (a.max_norm > 0.0) {
+            const double c = a.max_norm / (norm + 1e-6);
+            if (c < 1.0)
+                clip = c;
+        }
+        const double t = (double)s.step;
+        const double bc1 = 1.0 - pow(a.beta1, t);
+        const double bc2 = 1.0 - pow(a.beta2, t);
+        o.clip = (float)clip;
+        o.b1 = (float)a.beta1;
+        o.omb1 = (float)(1.0 - a.beta1);
+        o.b2 = (float)a.beta2;
+        o.omb2 = (float)(1.0 - a.beta2);
+        o.eps = (float)a.eps;
+        o.step_size = (float)(a.lr / bc1);
+        o.isb2 = (float)(1.0 / sqrt(bc2));
+        o.lrwd = (float)(a.lr * a.weight_decay);
+    }
+    s.last_norm = norm;
+    s.last_clip = o.clip;
+    s.last_skipped = o.skip;
+    s.sumsq = 0.0;
+    s.found_inf = 0.0;
+    *st = s;
+    *out = o;
+}
+
+// ------------------------------------------------------------- pass 2
+
+// One element of the AdamW update, binary32, every operation rounded to
+// nearest on its own (no contraction):
+//   g = (g_lp * inv_scale) * clip
+//   m' = b1*m + omb1*g;   v' = b2*v + omb2*(g*g)
+//   p' = p - (step_size * m' / (sqrt(v')*isb2 + eps) + lrwd*p)
+__device__ __forceinline__ void adam_elem(float graw, float &p, float &m, float &v, const StepScalars &s)
+{
+    const float g = __fmul_rn(__fmul_rn(graw, s.inv_scale), s.clip);
+    const float m1 = __fadd_rn(__fmul_rn(s.b1, m), __fmul_rn(s.omb1, g));
+    const float v1 = __fadd_rn(__fmul_rn(s.b2, v), __fmul_rn(s.omb2, __fmul_rn(g, g)));
+    const float d = __fadd_rn(__fmul_rn(__fsqrt_rn(v1), s.isb2), s.eps);
+    const float u = __fdiv_rn(m1, d);
+    p = __fsub_rn(p, __fadd_rn(__fmul_rn(s.step_size, u), __fmul_rn(s.lrwd, p)));
+    m = m1;
+    v = v1;
+}
+
+__device__ __forceinline__ void unpack8(const float4 &a, const float4 &b, float *f)
+{
+    f[0] = a.x; f[1] = a.y; f[2] = a.z; f[3] = a.w;
+    f[4] = b.x; f[5] = b.y; f[6] = b.z; f[7] = b.w;
+}
+
+// Vector i (elements 8i .. 8i+7) of one array set.
+template <int GT, int PT>
+__device__ __forceinline__ void adam_vec(const void *g, float *p, float *m, float *v, void *plp, int64_t i,
+                                         const StepScalars &s)
+{
+    constexpr int W = Elem<GT>::kWords;
+    uint4 gw[W];
+#pragma unroll
+    for (int q = 0; q < W; ++q)
+        gw[q] = __ldcs(static_cast<const uint4 *>(g) + i * W + q);
+    float4 *p4 = reinterpret_cast<float4 *>(p) + 2 * i;
+    float4 *m4 = reinterpret_cast<float4 *>(m) + 2 * i;
+    float4 *v4 = reinterpret_cast<float4 *>(v) + 2 * i;
+    const float4 p0 = __ldcs(p4), p1 = __ldcs(p4 + 1);
+    const float4 m0 = __ldcs(m4), m1 = __ldcs(m4 + 1);
+    const float4 v0 = __ldcs(v4), v1 = __ldcs(v4 + 1);
+    float gf[8], pf[8], mf[8], vf[8];
+    Elem<GT>::to_float(gw, gf);
+    unpack8(p0, p1, pf);
+    unpack8(m0, m1, mf);
+    unpack8(v0, v1, vf);
+#pragma unroll
+    for (int e = 0; e < 8; ++e)
+        adam_elem(gf[e], pf[e], mf[e], vf[e], s);
+    __stcs(p4, make_float4(pf[0], pf[1], pf[2], pf[3]));
+    __stcs(p4 + 1, make_float4(pf[4], pf[5], pf[6], pf[7]));
+    __stcs(m4, make_float4(mf[0], mf[1], mf[2], mf[3]));
+    __stcs(m4 + 1, make_float4(mf[4], mf[5], mf[6], mf[7]));
+    __stcs(v4, make_float4(vf[0], vf[1], vf[2], vf[3]));
+    __stcs(v4 + 1, make_float4(vf[4], vf[5], vf[6], vf[7]));
+    if (plp)
+        __stcs(static_cast<uint4 *>(plp) + i, LowP<PT>::pack(pf));
+}
+
+template <int GT, int PT>
+__device__ __forceinline__ void adam_scalar(const void *g, float *p, float *m, float *v, void *plp, int64_t j,
+                                            const StepScalars &s)
+{
+    float pj = p[j], mj = m[j], vj = v[j];
+    adam_elem(Elem<GT>::scalar(g, j), pj, mj, vj, s);
+    p[j] = pj;
+    m[j] = mj;
+    v[j] = vj;
+    if (plp)
+        LowP<PT>::store(plp, j, pj);
+}
+
+template <int GT, int PT>
+__device__ __forceinline__ void adam_range(const void *g, float *p, float *m, float *v, void *plp, int64_t n,
+                                           int64_t t, int64_t nt, const StepScalars &s)
+{
+    const int64_t nv = n >> 3;
+    for (int64_t i = t; i < nv; i += nt)
+        adam_vec<GT, PT>(g, p, m, v, plp, i, s);
+    const int64_t tail = n - (nv << 3);
+    if (t < tail)
+        adam_scalar<GT, PT>(g, p, m, v, plp, (nv << 3) + t, s);
+}
+
+template <int GT, int PT>
+__global__ void __launch_bounds__(kThreads)
+    k_adam_flat(const void *__restrict__ g, float *__restrict__ p, float *__restrict__ m, float *__restrict__ v,
+                void *__restrict__ plp, int64_t n, const StepScalars *__restrict__ scp)
+{
+    const StepScalars s = *scp;
+    if (s.skip)
+        return;
+    adam_range<GT, PT>(g, p, m, v, plp, n, (int64_t)blockIdx.x * kThreads + threadIdx.x,
+                       (int64_t)gridDim.x * kThreads, s);
+}
+
+template <int GT, int PT>
+__global__ void __launch_bounds__(kThreads)
+    k_adam_list(const TensorEntry *__restrict__ ents, const Chunk *__restrict__ chunks, int64_t n_chunks,
+                const StepScalars *__restrict__ scp)
+{
+    const StepScalars s = *scp;
+    if (s.skip)
+        return;
+    for (int64_t c = blockIdx.x; c < n_chunks; c += gridDim.x) {
+        const Chunk ch = chunks[c];
+        const TensorEntry e = ents[ch.tensor];
+        const int64_t start = (int64_t)ch.index * kChunk;
+        const int64_t len = min(kChunk, e.numel - start);
+        const void *g = static_cast<const char *>(e.g) + start * Elem<GT>::kBytes;
+        void *plp = e.plp ? static_cast<void *>(static_cast<char *>(e.plp) + start * 2) : nullptr;
+        adam_range<GT, PT>(g, e.p + start, e.m + start, e.v + start, plp, len, threadIdx.x, kThreads, s);
+    }
+}
+
+// ------------------------------------------------------------- accumulate
+
+struct BufPtrs {
+    const void *p[8];
+};
+
+template <int GT>
+__global__ void __launch_bounds__(kThreads)
+    k_accumulate(float *__restrict__ acc, BufPtrs b, int nb, int64_t n, int overwrite)
+{
+    constexpr int W = Elem<GT>::kWords;
+    const int64_t nv = n >> 3;
+    const int64_t nt = (int64_t)gridDim.x * kThreads;
+    const int64_t t = (int64_t)blockIdx.x * kThreads + threadIdx.x;
+    for (int64_t i = t; i < nv; i += nt) {
+        uint4 w[8][W];
+#pragma unroll
+        for (int k = 0; k < 8; ++k)
+            if (k < nb) {
+#pragma unroll
+                for (int q = 0; q < W; ++q)
+                    w[k][q] = __ldcs(static_cast<const uint4 *>(b.p[k]) + i * W + q);
+            }
+        float4 *a4 = reinterpret_cast<float4 *>(acc) + 2 * i;
+        float a[8];
+        int k0 = 0;
+        if (overwrite) {
+            Elem<GT>::to_float(w[0], a);
+            k0 = 1;
+        } else {
+            unpack8(__ldcs(a4), __ldcs(a4 + 1), a);
+        }
+#pragma unroll
+        for (int k = 0; k < 8; ++k)
+            if (k >= k0 && k < nb) {
+                float f[8];
+                Elem<GT>::to_float(w[k], f);
+#pragma unroll
+                for (int e = 0; e < 8; ++e)
+                    a[e] = __fadd_rn(a[e], f[e]);
+            }
+        __stcs(a4, make_float4(a[0], a[1], a[2], a[3]));
+        __stcs(a4 + 1, make_float4(a[4], a[5], a[6], a[7]));
+    }
+    const int64_t tail = n - (nv << 3);
+    if (t < tail) {
+        const int64_t j = (nv << 3) + t;
+        float a = overwrite ? Elem<GT>::scalar(b.p[0], j) : acc[j];
+#pragma unroll
+        for (int k = 0; k < 8; ++k)
+            if (k >= overwrite && k < nb)
+                a = __fadd_rn(a, Elem<GT>::scalar(b.p[k], j));
+        acc[j] = a;
+    }
+}
+
+// ------------------------------------------------------------- host helpers
+
+int sm_count()
+{
+    static std::mutex mu;
+    static std::unordered_map<int, int> cache;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess)
+        return 0;
+    std::lock_guard<std::mutex> lock(mu);
+    auto it = cache.find(dev);
+    if (it != cache.end())
+        return it->second;
+    int v = 0;
+    if (cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+        return 0;
+    cache[dev] = v;
+    return v;
+}
+
+// Resident blocks per SM of a kernel at kThreads threads (cached per device
+// and kernel).
+int blocks_per_sm(const void *kernel)
+{
+    static std::mutex mu;
+    static std::unordered_map<uint64_t, int> cache;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess)
+        return 1;
+    const uint64_t key = reinterpret_cast<uint64_t>(kernel) ^ ((uint64_t)dev << 56);
+    std::lock_guard<std::mutex> lock(mu);
+    auto it = cache.find(key);
+    if (it != cache.end())
+        return it->second;
+    int b = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b, kernel, kThreads, 0) != cudaSuccess || b < 1)
+        b = 1;
+    cache[key] = b;
+    return b;
+}
+
+// A whole number of waves over the SMs, or fewer blocks if there is less work.
+int grid_for(const void *kernel, int64_t work_items, int cap)
+{
+    const int64_t full = (int64_t)sm_count() * blocks_per_sm(kernel);
+    int64_t g = work_items < full ? work_items : full;
+    if (g > cap)
+        g = cap;
+    return g < 1 ? 1 : (int)g;
+}
+
+int check_launch(const char *what)
+{
+    const cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) {
+        set_cuda_error(what, (int)e, cudaGetErrorString(e));
+        return ZERO_ECUDA;
+    }
+    return ZERO_OK;
+}
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+bool grad_dtype_ok(int32_t d) { return d == ZERO_F16 || d == ZERO_BF16 || d == ZERO_F32; }
+bool lp_dtype_ok(int32_t d) { return d == ZERO_F16 || d == ZERO_BF16; }
+
+// True when the pointer is device memory the kernels may stream (device or
+// managed allocations).  Host memory is refused even where the GPU could
+// reach it: the kernels assume HBM.
+bool device_ptr(const void *p)
+{
+    cudaPointerAttributes a;
+    if (cudaPointerGetAttributes(&a, p) != cudaSuccess) {
+        cudaGetLastError();
+        return false;
+    }
+    return a.type == cudaMemoryTypeDevice || a.type == cudaMemoryTypeManaged;
+}
+
+// Checks one list; on success *total holds its element count.  The device
+// pointers of a one-array list (a flat shard) are checked to be device
+// memory; longer lists are checked on their first and last arrays only, to
+// keep the per-call host cost independent of the list length.
+int check_list(const zero_tlist_t *l, int64_t *total)
+{
+    if (!l || l->n < 0 || (l->n > 0 && (!l->ptrs || !l->numel)))
+        return ZERO_EINVAL;
+    int64_t t = 0;
+    for (int64_t i = 0; i < l->n; ++i) {
+        if (l->numel[i] < 0)
+            return ZERO_EINVAL;
+        if (l->numel[i] > 0) {
+            if (!l->ptrs[i])
+                return ZERO_EINVAL;
+            if (!aligned16(l->ptrs[i]))
+                return ZERO_EALIGN;
+        }
+        t += l->numel[i];
+    }
+    for (int64_t i = 0; i < l->n; ++i) {
+        if (i > 0 && i < l->n - 1)
+            i = l->n - 1;
+        if (l->numel[i] > 0 && !device_ptr(l->ptrs[i]))
+            return ZERO_EINVAL;
+    }
+    *total = t;
+    return ZERO_OK;
+}
+
+int check_same_shape(const zero_tlist_t *a, const zero_tlist_t *b)
+{
+    if (a->n != b->n)
+        return ZERO_ESIZE;
+    for (int64_t i = 0; i < a->n; ++i)
+        if (a->numel[i] != b->numel[i])
+            return ZERO_ESIZE;
+    return ZERO_OK;
+}
+
+int check_ws(void *ws, size_t ws_bytes, int64_t n_tensors, int64_t total)
+{
+    if (!ws || (reinterpret_cast<uintptr_t>(ws) & 255u) != 0)
+        return ws ? ZERO_EALIGN : ZERO_EWORKSPACE;
+    if (ws_bytes < zero_workspace_bytes(n_tensors, total))
+        return ZERO_EWORKSPACE;
+    if (!device_ptr(ws))
+        return ZERO_EINVAL;
+    return ZERO_OK;
+}
+
+// Builds the entry and chunk tables of a list call on the host and copies
+// them into the workspace (stream-ordered).  Returns the chunk count in
+// *n_chunks.
+int upload_table(const zero_tlist_t *g, const zero_tlist_t *p, const zero_tlist_t *m, const zero_tlist_t *v,
+                 const zero_tlist_t *plp, void *ws, cudaStream_t stream, int64_t *n_chunks,
+                 TensorEntry **d_ents, Chunk **d_chunks)
+{
+    const int64_t n = g->n;
+    int64_t chunks = 0;
+    for (int64_t i = 0; i < n; ++i)
+        chunks += (g->numel[i] + kChunk - 1) / kChunk;
+    const size_t ent_bytes = align256((size_t)n * sizeof(TensorEntry));
+    std::vector<unsigned char> host(ent_bytes + (size_t)chunks * sizeof(Chunk));
+    TensorEntry *ents = reinterpret_cast<TensorEntry *>(host.data());
+    Chunk *ch = reinterpret_cast<Chunk *>(host.data() + ent_bytes);
+    int64_t c = 0;
+    for (int64_t i = 0; i < n; ++i) {
+        TensorEntry &e = ents[i];
+        e.g = g->ptrs[i];
+        e.p = p ? static_cast<float *>(p->ptrs[i]) : nullptr;
+        e.m = m ? static_cast<float *>(m->ptrs[i]) : nullptr;
+        e.v = v ? static_cast<float *>(v->ptrs[i]) : nullptr;
+        e.plp = plp ? plp->ptrs[i] : nullptr;
+        e.numel = g->numel[i];
+        const int64_t k = (g->numel[i] + kChunk - 1) / kChunk;
+        for (int64_t j = 0; j < k; ++j) {
+            ch[c].tensor = (int32_t)i;
+            ch[c].index = (int32_t)j;
+            ++c;
+        }
+    }
+    unsigned char *base = static_cast<unsigned char *>(ws) + kWsTable;
+    if (!host.empty() &&
+        cudaMemcpyAsync(base, host.data(), host.size(), cudaMemcpyHostToDevice, stream) != cudaSuccess)
+        return check_launch("workspace table upload");
+    *n_chunks = chunks;
+    *d_ents = reinterpret_cast<TensorEntry *>(base);
+    *d_chunks = reinterpret_cast<Chunk *>(base + ent_bytes);
+    return ZERO_OK;
+}
+
+template <int GT>
+int launch_norm(const zero_tlist_t *grads, int64_t total, zero_state_t *st, int accumulate, void *ws,
+                cudaStream_t stream)
+{
+    unsigned char *w = static_cast<unsigned char *>(ws);
+    WsHeader *hdr = reinterpret_cast<WsHeader *>(w);
+    double2 *partials = reinterpret_cast<double2 *>(w + kWsPartials);
+    if (grads->n <= 1) {
+        const void *g = grads->n == 1 ? grads->ptrs[0] : nullptr;
+        const int64_t n = grads->n == 1 ? grads->numel[0] : 0;
+        const int64_t items = ((n >> 3) + 4 * kThreads - 1) / (4 * kThreads);
+        const int grid = grid_for((const void *)k_norm_flat<GT>, items, kMaxBlocks);
+        k_norm_flat<GT><<<grid, kThreads, 0, stream>>>(g, n, partials, hdr, st, accumulate);
+        return check_launch("zero_grad_norm_overflow");
+    }
+    int64_t n_chunks = 0;
+    TensorEntry *ents = nullptr;
+    Chunk *chunks = nullptr;
+    int rc = upload_table(grads, nullptr, nullptr, nullptr, nullptr, ws, stream, &n_chunks, &ents, &chunks);
+    if (rc != ZERO_OK)
+        return rc;
+    const int grid = grid_for((const void *)k_norm_list<GT>, n_chunks, kMaxBlocks);
+    k_norm_list<GT><<<grid, kThreads, 0, stream>>>(ents, chunks, n_chunks, partials, hdr, st, accumulate);
+    (void)total;
+    return check_launch("zero_grad_norm_overflow");
+}
+
+template <int GT, int PT>
+int launch_adam(const zero_tlist_t *g, const zero_tlist_t *p, const zero_tlist_t *m, const zero_tlist_t *v,
+                const zero_tlist_t *plp, const StepScalars *sc, void *ws, cudaStream_t stream)
+{
+    if (g->n == 0)
+        return ZERO_OK;
+    if (g->n == 1) {
+        const int64_t n = g->numel[0];
+        if (n == 0)
+            return ZERO_OK;
+        const int64_t items = ((n >> 3) + kThreads - 1) / kThreads;
+        const int grid = grid_for((const void *)k_adam_flat<GT, PT>, items, 1 << 30);
+        k_adam_flat<GT, PT><<<grid, kThreads, 0, stream>>>(
+            g->ptrs[0], static_cast<float *>(p->ptrs[0]), static_cast<float *>(m->ptrs[0]),
+            static_cast<float *>(v->ptrs[0]), plp ? plp->ptrs[0] : nullptr, n, sc);
+        return check_launch("zero_adam_step");
+    }
+    int64_t n_chunks = 0;
+    TensorEntry *ents = nullptr;
+    Chunk *chunks = nullptr;
+    int rc = upload_table(g, p, m, v, plp, ws, stream, &n_chunks, &ents, &chunks);
+    if (rc != ZERO_OK || n_chunks == 0)
+        return rc;
+    const int grid = grid_for((const void *)k_adam_list<GT, PT>, n_chunks, 1 << 30);
+    k_adam_list<GT, PT><<<grid, kThreads, 0, stream>>>(ents, chunks, n_chunks, sc);
+    return check_launch("zero_adam_step");
+}
+
+template <int GT>
+int launch_adam_lp(int32_t pdtype, const zero_tlist_t *g, const zero_tlist_t *p, const zero_tlist_t *m,
+                   const zero_tlist_t *v, const zero_tlist_t *plp, const StepScalars *sc, void *ws,
+                   cudaStream_t stream)
+{
+    if (pdtype == ZERO_BF16)
+        return launch_adam<GT, ZERO_BF16>(g, p, m, v, plp, sc, ws, stream);
+    return launch_adam<GT, ZERO_F16>(g, p, m, v, plp, sc, ws, stream);
+}
+
+}  // namespace
+}  // namespace zpml
+
+using namespace zpml;
+
+extern "C" int zero_accumulate_grads(float *acc, const void *const *g, int32_t n_bufs, int32_t dtype,
+                                     int64_t n, int32_t overwrite, void *stream)
+{
+    if (n < 0 || n_bufs < 1 || n_bufs > 8 || !g || (overwrite != 0 && overwrite != 1))
+        return ZERO_EINVAL;
+    if (!grad_dtype_ok(dtype))
+        return ZERO_EDTYPE;
+    if (n == 0)
+        return ZERO_OK;
+    if (!acc)
+        return ZERO_EINVAL;
+    if (!aligned16(acc))
+        return ZERO_EALIGN;
+    BufPtrs b = {};
+    for (int k = 0; k < n_bufs; ++k) {
+        if (!g[k])
+            return ZERO_EINVAL;
+        if (!aligned16(g[k]))
+            return ZERO_EALIGN;
+        b.p[k] = g[k];
+    }
+    if (!device_ptr(acc))
+        return ZERO_EINVAL;
+    for (int k = 0; k < n_bufs; ++k)
+        if (!device_ptr(g[k]))
+            return ZERO_EINVAL;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const int64_t items = ((n >> 3) + kThreads - 1) / kThreads;
+    switch (dtype) {
+    case ZERO_F16: {
+        const int grid = grid_for((const void *)k_accumulate<ZERO_F16>, items, 1 << 30);
+        k_accumulate<ZERO_F16><<<grid, kThreads, 0, s>>>(acc, b, n_bufs, n, overwrite);
+        break;
+    }
+    case ZERO_BF16: {
+        const int grid = grid_for((const void *)k_accumulate<ZERO_BF16>, items, 1 << 30);
+        k_accumulate<ZERO_BF16><<<grid, kThreads, 0, s>>>(acc, b, n_bufs, n, overwrite);
+        break;
+    }
+    default: {
+        const int grid = grid_for((const void *)k_accumulate<ZERO_F32>, items, 1 << 30);
+        k_accumulate<ZERO_F32><<<grid, kThreads, 0, s>>>(acc, b, n_bufs, n, overwrite);
+        break;
+    }
+    }
+    return check_launch("zero_accumulate_grads");
+}
+
+extern "C" int zero_grad_norm_overflow(const zero_tlist_t *grads, zero_state_t *d_state, int32_t accumulate,
+                                       void *ws, size_t ws_bytes, void *stream)
+{
+    if (!d_state || (accumulate != 0 && accumulate != 1))
+        return ZERO_EINVAL;
+    if ((reinterpret_cast<uintptr_t>(d_state) & 7u) != 0)
+        return ZERO_EALIGN;
+    if (!device_ptr(d_state))
+        return ZERO_EINVAL;
+    int64_t total = 0;
+    int rc = check_list(grads, &total);
+    if (rc != ZERO_OK)
+        return rc;
+    if (!grad_dtype_ok(grads->dtype))
+        return ZERO_EDTYPE;
+    rc = check_ws(ws, ws_bytes, grads->n, total);
+    if (rc != ZERO_OK)
+        return rc;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    switch (grads->dtype) {
+    case ZERO_F16: return launch_norm<ZERO_F16>(grads, total, d_state, accumulate, ws, s);
+    case ZERO_BF16: return launch_norm<ZERO_BF16>(grads, total, d_state, accumulate, ws, s);
+    default: return launch_norm<ZERO_F32>(grads, total, d_state, accumulate, ws, s);
+    }
+}
+
+extern "C" int zero_adam_step(const zero_tlist_t *grads, const zero_tlist_t *master, const zero_tlist_t *m,
+                              const zero_tlist_t *v, const zero_tlist_t *p_lp, const zero_hparams_t *hp,
+                              zero_state_t *d_state, void *ws, size_t ws_bytes, void *stream)
+{
+    if (!hp || !d_state)
+        return ZERO_EINVAL;
+    if ((reinterpret_cast<uintptr_t>(d_state) & 7u) != 0)
+        return ZERO_EALIGN;
+    if (!device_ptr(d_state))
+        return ZERO_EINVAL;
+    if (!(hp->lr >= 0.0) || !(hp->beta1 >= 0.0 && hp->beta1 < 1.0) || !(hp->beta2 >= 0.0 && hp->beta2 < 1.0) ||
+        !(hp->eps >= 0.0) || !(hp->weight_decay >= 0.0) || !(hp->min_scale >= 1.0) || hp->scale_window < 1 ||
+        hp->max_norm != hp->max_norm)
+        return ZERO_EINVAL;
+    int64_t total = 0, t2 = 0;
+    int rc = check_list(grads, &total);
+    if (rc != ZERO_OK)
+        return rc;
+    const zero_tlist_t *states[3] = {master, m, v};
+    for (const zero_tlist_t *l : states) {
+        if ((rc = check_list(l, &t2)) != ZERO_OK)
+            return rc;
+        if (l->dtype != ZERO_F32)
+            return ZERO_EDTYPE;
+        if ((rc = check_same_shape(grads, l)) != ZERO_OK)
+            return rc;
+    }
+    if (p_lp) {
+        if ((rc = check_list(p_lp, &t2)) != ZERO_OK)
+            return rc;
+        if (!lp_dtype_ok(p_lp->dtype))
+            return ZERO_EDTYPE;
+        if ((rc = check_same_shape(grads, p_lp)) != ZERO_OK)
+            return rc;
+    }
+    if (!grad_dtype_ok(grads->dtype))
+        return ZERO_EDTYPE;
+    if ((rc = check_ws(ws, ws_bytes, grads->n, total)) != ZERO_OK)
+        return rc;
+
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    StepScalars *sc = reinterpret_cast<StepScalars *>(static_cast<unsigned char *>(ws) + kWsScalars);
+    DecideArgs a;
+    a.lr = hp->lr;
+    a.beta1 = hp->beta1;
+    a.beta2 = hp->beta2;
+    a.eps = hp->eps;
+    a.weight_decay = hp->weight_decay;
+    a.max_norm = hp->max_norm;
+    a.min_scale = hp->min_scale;
+    a.scale_window = hp->scale_window;
+    k_decide<<<1, 32, 0, s>>>(d_state, sc, a);
+    if ((rc = check_launch("zero_adam_step (decision)")) != ZERO_OK)
+        return rc;
+    const int32_t pd = p_lp ? p_lp->dtype : ZERO_F16;
+    switch (grads->dtype) {
+    case ZERO_F16: return launch_adam_lp<ZERO_F16>(pd, grads, master, m, v, p_lp, sc, ws, s);
+    case ZERO_BF16: return launch_adam_lp<ZERO_BF16>(pd, grads, master, m, v, p_lp, sc, ws, s);
+    default: return launch_adam_lp<ZERO_F32>(pd, grads, master, m, v, p_lp, sc, ws, s);
+    }
+}

@@ -1,0 +1,81 @@
+// Internal definitions shared by the host part (host.cpp) and the CUDA part
+// (zero_pml.cu) of the library: workspace layout, the per-step scalar block
+// and the thread-local CUDA error record.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+
+#include "zero_pml.h"
+
+namespace zpml {
+
+// Threads per block of every streaming kernel.
+constexpr int kThreads = 256;
+// Upper bound on the grid of the norm pass (one binary64 partial per block).
+constexpr int kMaxBlocks = 4096;
+// Elements per work item when the arrays come as a list (multiple of 8, so
+// every chunk but a tensor's last starts and ends on a 16-byte boundary).
+constexpr int64_t kChunk = 1 << 16;
+
+// The scalars of one step's element update, written by the decision kernel
+// and read by every block of pass 2 (binary32, as the update runs).
+struct StepScalars {
+    float inv_scale;  // 1 / S
+    float clip;       // 1, or max_norm / (norm + 1e-6) when below 1
+    float b1, omb1;   // beta1, 1 - beta1
+    float b2, omb2;   // beta2, 1 - beta2
+    float eps;
+    float step_size;  // lr / (1 - beta1^t)
+    float isb2;       // 1 / sqrt(1 - beta2^t)
+    float lrwd;       // lr * weight_decay
+    int32_t skip;
+    int32_t pad;
+};
+
+// One array set of a list: the gradient, the fp32 master / momentum /
+// variance and the low-precision copy of one tensor (or one shard).
+struct TensorEntry {
+    const void *g;
+    float *p;
+    float *m;
+    float *v;
+    void *plp;
+    int64_t numel;
+};
+
+// One work item: elements [index * kChunk, min(numel, (index+1) * kChunk))
+// of tensor `tensor`.
+struct Chunk {
+    int32_t tensor;
+    int32_t index;
+};
+
+// Workspace layout (all offsets 256-byte aligned):
+//   [0, 256)            header: reduction ticket
+//   [256, 512)          StepScalars of the current step
+//   [512, 512 + 16*kMaxBlocks)  per-block partials of the norm pass (double2)
+//   then                TensorEntry[max_tensors], Chunk[max_chunks]
+struct WsHeader {
+    unsigned int ticket;
+};
+constexpr size_t kWsScalars = 256;
+constexpr size_t kWsPartials = 512;
+constexpr size_t kWsTable = kWsPartials + 16 * (size_t)kMaxBlocks;
+
+inline size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
+
+inline int64_t max_chunks(int64_t max_tensors, int64_t max_total_numel)
+{
+    return max_tensors + max_total_numel / kChunk + 1;
+}
+
+inline size_t table_bytes(int64_t n_tensors, int64_t n_chunks)
+{
+    return align256((size_t)n_tensors * sizeof(TensorEntry)) + align256((size_t)n_chunks * sizeof(Chunk));
+}
+
+// Records a CUDA error message for zero_strerror on this thread.
+void set_cuda_error(const char *what, int cuda_code, const char *cuda_msg);
+
+}  // namespace zpml
