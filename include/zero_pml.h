@@ -179,6 +179,29 @@ int zero_accumulate_grads(float *acc, const void *const *g, int32_t n_bufs, int3
 int zero_grad_norm_overflow(const zero_tlist_t *grads, zero_state_t *d_state,
                             int32_t accumulate, void *ws, size_t ws_bytes, void *stream);
 
+/* Pass 1 without a workspace: the same computation and results as
+ * zero_grad_norm_overflow, for callers that cannot allocate device memory
+ * and so cannot provide the workspace -- code running where another
+ * component owns all device memory (a training framework whose caching
+ * allocator has reserved the GPU, a plugin host that hands its plugins only
+ * their input and output buffers) or code that must keep the step's memory
+ * footprint fixed.  The ZeRO pages have no counterpart of this call: it is
+ * an interface convenience of this library.
+ *
+ * The scratch (a reduction ticket and per-block partials, 16,640 bytes) is a
+ * static device array inside the library; every GPU on which the library is
+ * loaded holds it until the process exits.  The first call on a device looks
+ * up that array's device address (with the device current) and caches it;
+ * make that first call before any stream capture.  Each call resets the
+ * ticket on `stream` before its kernel.  All calls share the one array and
+ * it keeps the last call's contents, so calls that can overlap on the GPU
+ * (different streams, or several host threads) race and must not be issued.
+ * Limit: at most 32 arrays in `grads` (any lengths); a longer list returns
+ * ZERO_ECAPACITY.  Allocates nothing (no cudaMalloc / cudaFree).
+ * Errors: as zero_grad_norm_overflow, plus ZERO_ECAPACITY. */
+int zero_grad_norm_overflow_static(const zero_tlist_t *grads, zero_state_t *d_state,
+                                   int32_t accumulate, void *stream);
+
 /* Pass 2 (preceded by a one-thread decision kernel): the step.
  * From d_state's global sumsq / found_inf (left there by
  * zero_grad_norm_overflow, summed over ranks if there are several):

@@ -1,0 +1,95 @@
+"""zero_grad_norm_overflow_static: pass 1 for callers that cannot allocate
+device memory (and so cannot pass a workspace), with its scratch in a static
+device array inside the library.  Called through the C ABI and checked
+against zero_grad_norm_overflow on the same gradients, two calls in a row,
+within the norm tolerance the parity tests use (1e-6 relative)."""
+import ctypes
+
+import pytest
+
+import zero_synth as zs
+
+torch = pytest.importorskip("torch")
+pytestmark = pytest.mark.gpu
+
+from gpu_common import to_dev  # noqa: E402
+
+NORM_REL = 1e-6
+
+
+@pytest.fixture(scope="module")
+def zp():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from zero_partitioned_mixed_layout_gb300 import _build
+    _build.build()
+    import zero_partitioned_mixed_layout_gb300 as zp
+    from zero_partitioned_mixed_layout_gb300.binding import _TList
+    so = zp.lib()
+    so.zero_grad_norm_overflow_static.argtypes = [ctypes.POINTER(_TList), ctypes.c_void_p,
+                                                  ctypes.c_int32, ctypes.c_void_p]
+    so.zero_grad_norm_overflow_static.restype = ctypes.c_int
+    return zp
+
+
+def call_static(zp, arrays, state, accumulate=0):
+    """The raw C call: grads as a zero_tlist_t, state, accumulate, stream."""
+    from zero_partitioned_mixed_layout_gb300.binding import _TList
+    n = len(arrays)
+    ptrs = (ctypes.c_void_p * n)(*[a.data_ptr() for a in arrays])
+    numel = (ctypes.c_int64 * n)(*[a.numel() for a in arrays])
+    code = {torch.float16: 0, torch.bfloat16: 1, torch.float32: 2}[arrays[0].dtype]
+    tl = _TList(ptrs, numel, n, code)
+    return zp.lib().zero_grad_norm_overflow_static(
+        ctypes.byref(tl), ctypes.c_void_p(state.data_ptr()), accumulate,
+        ctypes.c_void_p(torch.cuda.current_stream().cuda_stream))
+
+
+def head(zp, state):
+    st = zp.parse_state(state)
+    return st["sumsq"], st["found_inf"]
+
+
+def grads(sizes, dtype, scale, seed):
+    return [to_dev(zs.host_grad(n, seed, 0, scale, dtype, micro=i), dtype)
+            for i, n in enumerate(sizes)]
+
+
+@pytest.mark.parametrize("dtype", ["f16", "bf16", "f32"])
+@pytest.mark.parametrize("sizes", [[97_350_784], [5, 70_001, 3, 1 << 20]], ids=["flat", "list"])
+def test_static_scratch_matches_workspace_call(zp, dtype, sizes):
+    scale = 1024.0 if dtype == "f16" else 1.0
+    for call in range(2):  # two calls in a row share the static scratch
+        arrays = grads(sizes, dtype, scale, 40 + call)
+        ref_state, st_state = zp.new_state(scale), zp.new_state(scale)
+        ws = zp.new_workspace(len(arrays), sum(sizes))
+        zp.zero_grad_norm_overflow(arrays, ref_state, ws)
+        rc = call_static(zp, arrays, st_state)
+        assert rc == 0, zp.zero_strerror(rc)
+        torch.cuda.synchronize()
+        (s_ref, f_ref), (s_st, f_st) = head(zp, ref_state), head(zp, st_state)
+        assert f_st == f_ref == 0.0
+        assert s_ref > 0 and abs(s_st - s_ref) <= NORM_REL * s_ref
+    # accumulate mode folds a second call into the first, and an overflow in
+    # the second call is counted once
+    arrays = grads(sizes, dtype, scale, 50)
+    st_state = zp.new_state(scale)
+    assert call_static(zp, arrays, st_state, 0) == 0
+    torch.cuda.synchronize()
+    first = head(zp, st_state)[0]
+    arrays[-1][-1] = float("inf")
+    assert call_static(zp, arrays, st_state, 1) == 0
+    torch.cuda.synchronize()
+    assert first > 0 and head(zp, st_state)[1] == 1.0
+
+
+def test_static_scratch_rejects_long_lists(zp):
+    arrays = [torch.ones(16, dtype=torch.float16, device="cuda") for _ in range(33)]
+    state = zp.new_state(1.0)
+    before = state.clone()
+    assert call_static(zp, arrays, state) == -6  # ZERO_ECAPACITY: more than 32 arrays
+    torch.cuda.synchronize()
+    assert torch.equal(before, state), "a rejected call changed the state"
+    assert call_static(zp, arrays[:32], state) == 0
+    torch.cuda.synchronize()
+    assert head(zp, state) == (32 * 16.0, 0.0)

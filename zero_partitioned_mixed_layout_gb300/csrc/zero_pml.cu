@@ -953,3 +953,117 @@ extern "C" int zero_adam_step(const zero_tlist_t *grads, const zero_tlist_t *mas
     default: return launch_adam_lp<ZERO_F32>(pd, grads, master, m, v, p_lp, sc, ws, s);
     }
 }
+
+// ------------------------------------------------------------- pass 1 without workspace
+//
+// A variant of pass 1 for callers that cannot hand the library a device
+// workspace, because they cannot allocate device memory themselves: code that
+// runs where another component owns all device memory (a training framework
+// whose caching allocator has reserved the GPU, a plugin host that gives a
+// plugin only its input and output buffers), or code that must keep the
+// memory footprint of the step fixed.  Its scratch (the reduction ticket and
+// the per-block partials) lives in one file-scope device array that every
+// GPU loading this library holds until the process exits.
+
+namespace zpml {
+namespace {
+
+constexpr int kStaticMaxArrays = 32;   // arrays per call
+constexpr int kStaticMaxBlocks = 1024; // grid cap: one binary64 partial pair per block
+constexpr size_t kStaticScratchBytes = 256 + 16 * (size_t)kStaticMaxBlocks;
+
+static __device__ __align__(256) unsigned char g_norm_scratch[kStaticScratchBytes];
+
+struct StaticArrays {
+    const void *g[kStaticMaxArrays];
+    int64_t n[kStaticMaxArrays];
+};
+
+template <int GT>
+__global__ void __launch_bounds__(kThreads)
+    k_norm_static(StaticArrays a, int n_arrays, unsigned char *scratch, zero_state_t *st, int accumulate)
+{
+    WsHeader *hdr = reinterpret_cast<WsHeader *>(scratch);
+    double2 *partials = reinterpret_cast<double2 *>(scratch + 256);
+    double tot = 0.0;
+    uint32_t bad = 0;
+    const int64_t t = (int64_t)blockIdx.x * kThreads + threadIdx.x;
+    const int64_t nt = (int64_t)gridDim.x * kThreads;
+    for (int k = 0; k < n_arrays; ++k)
+        norm_range<GT>(a.g[k], a.n[k], t, nt, tot, bad);
+    norm_finish(tot, bad, partials, hdr, st, accumulate);
+}
+
+// Device address of g_norm_scratch on the current device, looked up once per
+// device (with that device current) and cached; NULL on failure.
+void *static_scratch()
+{
+    static std::mutex mu;
+    static void *addr[64] = {};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) {
+        cudaGetLastError();
+        return nullptr;
+    }
+    std::lock_guard<std::mutex> lock(mu);
+    if (!addr[dev]) {
+        void *p = nullptr;
+        const cudaError_t e = cudaGetSymbolAddress(&p, g_norm_scratch);
+        if (e != cudaSuccess) {
+            set_cuda_error("zero_grad_norm_overflow_static (scratch address)", (int)e, cudaGetErrorString(e));
+            cudaGetLastError();
+            return nullptr;
+        }
+        addr[dev] = p;
+    }
+    return addr[dev];
+}
+
+template <int GT>
+int launch_norm_static(const zero_tlist_t *grads, int64_t total, zero_state_t *st, int accumulate,
+                       unsigned char *scratch, cudaStream_t stream)
+{
+    StaticArrays a = {};
+    for (int64_t i = 0; i < grads->n; ++i) {
+        a.g[i] = grads->ptrs[i];
+        a.n[i] = grads->numel[i];
+    }
+    const int64_t items = ((total >> 3) + 4 * kThreads - 1) / (4 * kThreads);
+    const int grid = grid_for((const void *)k_norm_static<GT>, items, kStaticMaxBlocks);
+    k_norm_static<GT><<<grid, kThreads, 0, stream>>>(a, (int)grads->n, scratch, st, accumulate);
+    return check_launch("zero_grad_norm_overflow_static");
+}
+
+}  // namespace
+}  // namespace zpml
+
+extern "C" int zero_grad_norm_overflow_static(const zero_tlist_t *grads, zero_state_t *d_state,
+                                              int32_t accumulate, void *stream)
+{
+    if (!d_state || (accumulate != 0 && accumulate != 1))
+        return ZERO_EINVAL;
+    if ((reinterpret_cast<uintptr_t>(d_state) & 7u) != 0)
+        return ZERO_EALIGN;
+    if (!device_ptr(d_state))
+        return ZERO_EINVAL;
+    int64_t total = 0;
+    int rc = check_list(grads, &total);
+    if (rc != ZERO_OK)
+        return rc;
+    if (!grad_dtype_ok(grads->dtype))
+        return ZERO_EDTYPE;
+    if (grads->n > kStaticMaxArrays)
+        return ZERO_ECAPACITY;
+    unsigned char *scratch = static_cast<unsigned char *>(static_scratch());
+    if (!scratch)
+        return ZERO_ECUDA;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    // the ticket must start at zero whatever an earlier call left behind
+    if (cudaMemsetAsync(scratch, 0, 256, s) != cudaSuccess)
+        return check_launch("zero_grad_norm_overflow_static (ticket reset)");
+    switch (grads->dtype) {
+    case ZERO_F16: return launch_norm_static<ZERO_F16>(grads, total, d_state, accumulate, scratch, s);
+    case ZERO_BF16: return launch_norm_static<ZERO_BF16>(grads, total, d_state, accumulate, scratch, s);
+    default: return launch_norm_static<ZERO_F32>(grads, total, d_state, accumulate, scratch, s);
+    }
+}
