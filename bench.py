@@ -30,8 +30,6 @@ sys.path.insert(0, ROOT)
 
 METRIC = "Adam-step params/sec & achieved HBM GB/s vs GB300 roofline (28 B/param), 1 GPU"
 UNIT = "params/s"
-BYTES_ADAM = 28  # pass 2: read g16 2 + p/m/v 12, write p/m/v 12 + p16 2
-BYTES_STEP = 30  # + pass 1 reading g16 again
 WORKLOAD = "gpt2_1p5b_nd16"
 L2_BYTES = 129e6
 
@@ -170,49 +168,124 @@ def run_reference(args):
 
 # ------------------------------------------------------------------ our arm
 
+class Workload:
+    """Device buffers and the step of one benchmark workload on one rank."""
+
+    def __init__(self, name, log2n, rank, dev):
+        import torch
+
+        import zero_partitioned_mixed_layout_gb300 as zp
+        import zero_synth as zs
+        self.zp, self.name, self.dev = zp, name, dev
+        if name == "flat":
+            w = dict(zs.WORKLOADS["tiny"], nd=1, rank=0)
+            numel = [1 << log2n]
+            self.title = f"flat shard of 2^{log2n} params, fp16 grads x1024"
+        else:
+            w = zs.WORKLOADS[name]
+            numel = w["numel"]()
+            self.title = {
+                "gpt2_1p5b_nd16": "GPT-2 1.5B state (48 layers, hidden 1600, vocab 50257) in 16 "
+                                  "ZeRO shards, one shard per GPU",
+                "gpt2_1p5b_full": "GPT-2 1.5B state unpartitioned (Nd = 1) on one GPU, clip 1.0",
+                "tiny": "2-layer hidden-256 transformer state (14 tensors), Nd = 1",
+                "stack_100b_nd400": "100B GPT layer stack (125 x hidden 8192) in 400 ZeRO shards, "
+                                    "one shard; 4 bf16 micro-batch gradients accumulated, clip 1.0",
+                "frag_10k": "10,000 separately allocated tensors (log-normal sizes, median 4096, "
+                            "max 2^24), unflattened multi-tensor path",
+            }[name]
+        self.w = w
+        self.listmode = name == "frag_10k"
+        shard = rank % w["nd"]
+        seed = 1000 + shard
+        self.scale = w["loss_scale"]
+        gdt = {"f16": torch.float16, "bf16": torch.bfloat16}[w["gdtype"]]
+        pdt = {"f16": torch.float16, "bf16": torch.bfloat16}[w["pdtype"]]
+        self.micro = w["micro_batches"]
+        if self.listmode:
+            sizes = numel
+            self.S = sum(sizes)
+            flat_p = torch.empty(self.S, dtype=torch.float32, device=dev)
+            zs.device_master_into(flat_p, seed)
+            flat_g = torch.empty(self.S, dtype=gdt, device=dev)
+            zs.device_grad_into(flat_g, seed, 0, self.scale)
+            offs = [0]
+            for n in sizes:
+                offs.append(offs[-1] + n)
+            # every tensor its own allocation, as an unflattened model's are
+            p = [flat_p[offs[i]:offs[i + 1]].clone() for i in range(len(sizes))]
+            g = [flat_g[offs[i]:offs[i + 1]].clone() for i in range(len(sizes))]
+            del flat_p, flat_g
+            self.p = zp.TensorList(p, "master")
+            self.g = zp.TensorList(g, "grads")
+            self.m = zp.TensorList([torch.zeros(n, device=dev) for n in sizes], "m")
+            self.v = zp.TensorList([torch.zeros(n, device=dev) for n in sizes], "v")
+            self.lp = zp.TensorList([torch.empty(n, dtype=pdt, device=dev) for n in sizes], "p_lp")
+            self.ws = zp.new_workspace(len(sizes), self.S, dev)
+        else:
+            lay = zp.zero_partition_layout(numel, w["nd"], w["align"])
+            S = self.S = lay.shard_numel
+            self.p = torch.empty(S, dtype=torch.float32, device=dev)
+            zs.device_master_into(self.p, seed)
+            self.m = torch.zeros(S, dtype=torch.float32, device=dev)
+            self.v = torch.zeros(S, dtype=torch.float32, device=dev)
+            self.lp = torch.empty(S, dtype=pdt, device=dev)
+            if self.micro > 1:
+                self.bufs = [torch.empty(S, dtype=gdt, device=dev) for _ in range(self.micro)]
+                for j, b in enumerate(self.bufs):
+                    zs.device_grad_into(b, seed, 0, self.scale, micro=j)
+                self.g = torch.empty(S, dtype=torch.float32, device=dev)
+            else:
+                self.g = torch.empty(S, dtype=gdt, device=dev)
+                zs.device_grad_into(self.g, seed, 0, self.scale)
+            self.ws = zp.new_workspace(1, S, dev)
+        self.state = zp.new_state(self.scale, dev)
+        self.hp = zp.HParams(**zs.HPARAMS, max_norm=w["max_norm"])
+        g_bytes = 4 if self.micro > 1 else 2
+        p_bytes = 2
+        # algorithmic bytes per param of pass 2 and of the whole step
+        self.bytes_adam = g_bytes + 12 + 12 + p_bytes
+        self.bytes_step = self.bytes_adam + g_bytes + (self.micro * 2 + 4 if self.micro > 1 else 0)
+        self.launches = 3 + (1 if self.micro > 1 else 0)
+        self.l2_resident = self.bytes_step * self.S < 2 * L2_BYTES
+
+    def step(self, stream, exchange=None, ev=None):
+        zp = self.zp
+        if self.micro > 1:
+            zp.zero_accumulate_grads(self.g, self.bufs, overwrite=True, stream=stream)
+        zp.zero_grad_norm_overflow(self.g, self.state, self.ws, stream=stream)
+        if exchange is not None:
+            exchange(self.state)
+        if ev is not None:
+            ev[0].record(stream)
+        zp.zero_adam_step(self.g, self.p, self.m, self.v, self.lp, self.hp, self.state, self.ws,
+                          stream=stream)
+        if ev is not None:
+            ev[1].record(stream)
+
+
 def run_ours(args):
     import torch
     import torch.distributed as dist
 
     import zero_partitioned_mixed_layout_gb300 as zp
     from zero_partitioned_mixed_layout_gb300.dist import exchange_partials
-    import zero_synth as zs
 
     rank, world, local = dist_env()
     if world > 1:
         torch.cuda.set_device(local)
         dist.init_process_group("nccl")
     dev = torch.device("cuda", torch.cuda.current_device())
-    w = zs.WORKLOADS[WORKLOAD]
-    lay = zp.zero_partition_layout(w["numel"](), w["nd"], w["align"])
-    S = lay.shard_numel
-    shard = rank % w["nd"]
-    scale = w["loss_scale"]
-
-    dp = torch.empty(S, dtype=torch.float32, device=dev)
-    zs.device_master_into(dp, 1000 + shard)
-    dm = torch.zeros(S, dtype=torch.float32, device=dev)
-    dv = torch.zeros(S, dtype=torch.float32, device=dev)
-    dlp = torch.empty(S, dtype=torch.float16, device=dev)
-    dg = torch.empty(S, dtype=torch.float16, device=dev)
-    zs.device_grad_into(dg, 1000 + shard, 0, scale)
-    state = zp.new_state(scale, dev)
-    ws = zp.new_workspace(1, S, dev)
-    hp = zp.HParams(**zs.HPARAMS, max_norm=w["max_norm"])
+    wl = Workload(args.workload, args.log2n, rank, dev)
+    S = wl.S
     stream = torch.cuda.current_stream(dev)
-
-    def exchange():
-        if world > 1:
-            exchange_partials(state)
+    exchange = exchange_partials if world > 1 else None
+    # a buffer larger than L2, rewritten between timed steps of workloads
+    # whose working set would otherwise stay in L2
+    flush = torch.empty(int(2 * L2_BYTES), dtype=torch.uint8, device=dev) if wl.l2_resident else None
 
     def step(ev=None):
-        zp.zero_grad_norm_overflow(dg, state, ws, stream=stream)
-        exchange()
-        if ev is not None:
-            ev[0].record(stream)
-        zp.zero_adam_step(dg, dp, dm, dv, dlp, hp, state, ws, stream=stream)
-        if ev is not None:
-            ev[1].record(stream)
+        wl.step(stream, exchange, ev)
 
     def barrier():
         torch.cuda.synchronize(dev)
@@ -223,12 +296,14 @@ def run_ours(args):
     for _ in range(args.warmup):
         step()
     barrier()
-    st = zp.parse_state(state)
+    st = zp.parse_state(wl.state)
     assert st["last_skipped"] == 0 and st["step"] == args.warmup, st
 
     events = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
               for _ in range(args.steps)]
     t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    step_events = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                   for _ in range(args.steps)] if flush is not None else None
     with ClockSampler(dev.index if world == 1 else local) as clk:
         # the sampler polls every 200 ms: keep the GPU in the same step for a
         # second right before the timed region so that the clock record
@@ -241,12 +316,20 @@ def run_ours(args):
         barrier()
         t_start.record(stream)
         for k in range(args.steps):
+            if flush is not None:
+                flush.fill_(k & 255)
+                step_events[k][0].record(stream)
             step(events[k])
+            if flush is not None:
+                step_events[k][1].record(stream)
         t_end.record(stream)
         barrier()
-    ms = t_start.elapsed_time(t_end)
+    if flush is not None:  # the step alone, L2 flushed before each one
+        ms = sum(a.elapsed_time(b) for a, b in step_events)
+    else:
+        ms = t_start.elapsed_time(t_end)
     adam_ms = statistics.mean(a.elapsed_time(b) for a, b in events)
-    st = zp.parse_state(state)
+    st = zp.parse_state(wl.state)
     assert st["last_skipped"] == 0 and st["step"] >= args.warmup + args.steps, st
     if world > 1:
         t = torch.tensor([ms, adam_ms], dtype=torch.float64, device=dev)
@@ -259,21 +342,21 @@ def run_ours(args):
     # gradient in (H2D), the step, the 64-byte state out (D2H) and read on
     # the host every step
     e2e = None
-    if rank == 0 or world > 1:
-        hg = torch.empty(S, dtype=torch.float16, pin_memory=True)
-        hg.copy_(dg.cpu())
+    if not wl.listmode and wl.micro == 1:
+        hg = torch.empty(S, dtype=wl.g.dtype, pin_memory=True)
+        hg.copy_(wl.g.cpu())
         hs = torch.empty(zp.STATE_BYTES, dtype=torch.uint8, pin_memory=True)
         for _ in range(2):
-            dg.copy_(hg, non_blocking=True)
+            wl.g.copy_(hg, non_blocking=True)
             step()
-            hs.copy_(state, non_blocking=True)
+            hs.copy_(wl.state, non_blocking=True)
             stream.synchronize()
         barrier()
         t0 = time.perf_counter()
         for _ in range(args.steps):
-            dg.copy_(hg, non_blocking=True)
+            wl.g.copy_(hg, non_blocking=True)
             step()
-            hs.copy_(state, non_blocking=True)
+            hs.copy_(wl.state, non_blocking=True)
             stream.synchronize()
             assert zp.parse_state(bytes(hs.numpy().tobytes()))["last_skipped"] == 0
         barrier()
@@ -282,9 +365,9 @@ def run_ours(args):
             t = torch.tensor([e2e_s], dtype=torch.float64, device=dev)
             dist.all_reduce(t, op=dist.ReduceOp.MAX)
             e2e_s = t.item()
-        e2e = {"value": world * S / e2e_s, "unit": UNIT, "h2d_bytes_per_step": 2 * S,
+        e2e = {"value": world * S / e2e_s, "unit": UNIT, "h2d_bytes_per_step": hg.numel() * hg.element_size(),
                "d2h_bytes_per_step": zp.STATE_BYTES,
-               "note": "fp16 gradient copied from pinned host memory, step, state read back "
+               "note": "gradient copied from pinned host memory, step, state read back "
                        "and checked on the host every step"}
 
     if rank != 0:
@@ -294,38 +377,42 @@ def run_ours(args):
 
     peaks = measured_peaks()
     peak = peaks["hbm_gbs"] if peaks else 6800.0
-    achieved = BYTES_ADAM * S / (adam_ms * 1e-3) / 1e9
+    achieved = wl.bytes_adam * S / (adam_ms * 1e-3) / 1e9
     cpu = None
     if not args.no_cpu_baseline and world == 1:
         n_sample = 1 << 24
         cv, cdt = oracle_run(n_sample, 3, 0)
         cpu = {"value": cv, "unit": UNIT, "cores": 1, "kind": "oracle",
-               "sample": f"first {n_sample} params of the same shard, 3 full steps, "
+               "sample": f"first {n_sample} params of the GPT-2 1.5B Nd=16 shard, 3 full steps, "
                          f"{cdt:.1f} s, single-threaded scalar C"}
+    default = args.workload == WORKLOAD
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
         "config": {
-            "workload": "GPT-2 1.5B state (48 layers, hidden 1600, vocab 50257) in 16 ZeRO "
-                        "shards, one shard per GPU",
-            "shard_params": S, "grad_dtype": "f16", "param_dtype": "f16",
-            "state_dtype": "f32", "loss_scale": scale, "clip": w["max_norm"],
-            "l2": f"inputs larger than L2 ({BYTES_STEP * S / 1e9:.2f} GB per step vs "
-                  f"{L2_BYTES / 1e6:.0f} MB), no flush",
+            "workload": wl.title,
+            "shard_params": S, "grad_dtype": wl.w["gdtype"], "param_dtype": wl.w["pdtype"],
+            "state_dtype": "f32", "loss_scale": wl.scale, "clip": wl.w["max_norm"],
+            "micro_batches": wl.micro,
+            "l2": ("L2 flushed (256 MB written) before each timed step; time is the sum of the "
+                   "steps alone" if flush is not None else
+                   f"inputs larger than L2 ({wl.bytes_step * S / 1e9:.2f} GB per step vs "
+                   f"{L2_BYTES / 1e6:.0f} MB), no flush"),
             "parallelism": f"zero-dp{world}" if world > 1 else "zero-shard",
         },
-        "hbm_gbs_28B": BYTES_ADAM * S / (ms_per_step * 1e-3) / 1e9,
-        "hbm_gbs_step_30B": BYTES_STEP * S / (ms_per_step * 1e-3) / 1e9,
+        "hbm_gbs_adam": wl.bytes_adam * S / (adam_ms * 1e-3) / 1e9,
+        "hbm_gbs_step": wl.bytes_step * S / (ms_per_step * 1e-3) / 1e9,
+        "bytes_per_param": {"adam_pass": wl.bytes_adam, "whole_step": wl.bytes_step},
         "passes_ms": {"adam_step": adam_ms, "whole_step": ms_per_step},
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
-                     "frac": achieved / peak, "traffic": committed_traffic(),
-                     "kernel": "zero_adam_step (decision + pass 2), 28 B/param",
+                     "frac": achieved / peak, "traffic": committed_traffic() if default else None,
+                     "kernel": f"zero_adam_step (decision + pass 2), {wl.bytes_adam} B/param",
                      "peak_source": "MEASURED_PEAKS.json hbm_gbs (of measured)" if peaks
                      else "fallback 6.8 TB/s (of fallback)"},
         "cpu_baseline": cpu,
         "e2e": e2e,
-        "gpu_launches": 3 * args.steps,
+        "gpu_launches": wl.launches * args.steps,
         "clocks": dict(clk.summary(), window=f"{args.clock_preroll:.1f} s of the same step "
                        "just before the timed region, and the timed region"),
     }
@@ -341,6 +428,11 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--workload", default=WORKLOAD,
+                    choices=["gpt2_1p5b_nd16", "tiny", "gpt2_1p5b_full", "stack_100b_nd400",
+                             "frag_10k", "flat"],
+                    help="default: the GPT-2 1.5B Nd=16 shard the metric is quoted on")
+    ap.add_argument("--log2n", type=int, default=26, help="size of the flat workload (2^k)")
     ap.add_argument("--clock-preroll", type=float, default=1.0,
                     help="seconds of untimed steps, sampled for clocks, before the timed ones")
     args = ap.parse_args()

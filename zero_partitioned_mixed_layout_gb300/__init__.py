@@ -14,6 +14,7 @@ from .binding import (  # noqa: F401
     ZERO_F16,
     ZERO_F32,
     STATE_BYTES,
+    TensorList,
     LIB_PATH,
     lib,
     new_state,

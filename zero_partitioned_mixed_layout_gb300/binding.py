@@ -186,7 +186,14 @@ def _device_tensor(t, what: str):
 class _ListArgs:
     """Keeps the ctypes arrays of one zero_tlist_t alive for the call."""
 
+    def __new__(cls, tensors, what: str):
+        if isinstance(tensors, TensorList):
+            return tensors._args
+        return super().__new__(cls)
+
     def __init__(self, tensors, what: str):
+        if isinstance(tensors, TensorList):
+            return
         if not isinstance(tensors, (list, tuple)):
             tensors = [tensors]
         for t in tensors:
@@ -199,6 +206,21 @@ class _ListArgs:
         self.numel = (ctypes.c_int64 * max(n, 1))(*[t.numel() for t in tensors])
         self.tl = _TList(self.ptrs, self.numel, n, codes.pop() if codes else ZERO_F32)
         self.device = tensors[0].device if n else None
+
+
+class TensorList:
+    """A list of device tensors marshalled once into a zero_tlist_t.
+
+    Pass it wherever a list of tensors is accepted; long lists (thousands of
+    unflattened tensors) then cost no per-call Python work.  The tensors are
+    referenced, so their storage stays alive while the TensorList does."""
+
+    def __init__(self, tensors, what: str = "tensors"):
+        self.tensors = list(tensors)
+        self._args = _ListArgs(self.tensors, what)
+
+    def __len__(self):
+        return len(self.tensors)
 
 
 def _stream_ptr(stream, device):

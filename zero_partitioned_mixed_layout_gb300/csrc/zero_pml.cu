@@ -369,8 +369,11 @@ __global__ void __launch_bounds__(kThreads)
 // ------------------------------------------------------------- decision
 
 struct DecideArgs {
-    double lr, beta1, beta2, eps, weight_decay, max_norm, min_scale;
+    double lr, beta1, beta2, max_norm, min_scale;
     int64_t scale_window;
+    // step scalars that do not depend on the device state, computed on the
+    // host the same way (binary64, rounded once to binary32)
+    float b1, omb1, b2, omb2, eps, lrwd;
 };
 
 // Skip or apply, loss-scale and step bookkeeping, and the step scalars
@@ -378,7 +381,7 @@ struct DecideArgs {
 // this GPU, so the three independent chains -- 1 - beta1^t and the step
 // size, 1 - beta2^t and its inverse square root, the norm and the clip
 // coefficient -- run in three threads; thread 0 then writes the results.
-__global__ void k_decide(zero_state_t *st, StepScalars *out, DecideArgs a)
+__global__ void k_decide(zero_state_t *st, StepScalars *out, const PowCache *cache, DecideArgs a)
 {
     __shared__ float s_val[3];
     __shared__ double s_norm;
@@ -388,13 +391,24 @@ __global__ void k_decide(zero_state_t *st, StepScalars *out, DecideArgs a)
         return;
     const int tid = threadIdx.x;
     zero_state_t s = *st;
-    const double t = (double)(s.step + 1);  // the step count if this step applies
+    const int64_t tn = s.step + 1;  // the step count if this step applies
+    const double t = (double)tn;
+    const PowCache c = *cache;
+    const bool hit = c.t == tn && c.beta1 == a.beta1 && c.beta2 == a.beta2;
     if (tid == 0) {
-        const double bc1 = 1.0 - pow(a.beta1, t);
-        s_val[0] = (float)(a.lr / bc1);
+        if (hit && c.lr == a.lr) {
+            s_val[0] = c.step_size;
+        } else {
+            const double bc1 = hit ? c.bc1 : 1.0 - pow(a.beta1, t);
+            s_val[0] = (float)(a.lr / bc1);
+        }
     } else if (tid == 1) {
-        const double bc2 = 1.0 - pow(a.beta2, t);
-        s_val[1] = (float)(1.0 / sqrt(bc2));
+        if (hit) {
+            s_val[1] = c.isb2;
+        } else {
+            const double bc2 = 1.0 - pow(a.beta2, t);
+            s_val[1] = (float)(1.0 / sqrt(bc2));
+        }
     } else if (tid == 2) {
         const double norm = sqrt(s.sumsq);
         double clip = 1.0;
@@ -410,7 +424,9 @@ __global__ void k_decide(zero_state_t *st, StepScalars *out, DecideArgs a)
     if (tid != 0)
         return;
     StepScalars o;
-    o.inv_scale = (float)(1.0 / s.loss_scale);
+    // S is a power of two: below 2^127 its binary32 reciprocal is exact and
+    // equals the binary64 reciprocal rounded to binary32
+    o.inv_scale = s.loss_scale <= 0x1p126 ? __frcp_rn((float)s.loss_scale) : (float)(1.0 / s.loss_scale);
     o.clip = 1.0f;
     o.b1 = o.omb1 = o.b2 = o.omb2 = o.eps = o.step_size = o.isb2 = o.lrwd = 0.0f;
     o.pad = 0;
@@ -430,15 +446,19 @@ __global__ void k_decide(zero_state_t *st, StepScalars *out, DecideArgs a)
             s.good_steps = 0;
         }
         o.clip = s_val[2];
-        o.b1 = (float)a.beta1;
-        o.omb1 = (float)(1.0 - a.beta1);
-        o.b2 = (float)a.beta2;
-        o.omb2 = (float)(1.0 - a.beta2);
-        o.eps = (float)a.eps;
+        o.b1 = a.b1;
+        o.omb1 = a.omb1;
+        o.b2 = a.b2;
+        o.omb2 = a.omb2;
+        o.eps = a.eps;
         o.step_size = s_val[0];
         o.isb2 = s_val[1];
-        o.lrwd = (float)(a.lr * a.weight_decay);
+        o.lrwd = a.lrwd;
     }
+    o.lr = a.lr;
+    o.beta1 = a.beta1;
+    o.beta2 = a.beta2;
+    o.next_t = s.step + 1;
     s.last_norm = norm;
     s.last_clip = o.clip;
     s.last_skipped = o.skip;
@@ -446,6 +466,25 @@ __global__ void k_decide(zero_state_t *st, StepScalars *out, DecideArgs a)
     s.found_inf = 0.0;
     *st = s;
     *out = o;
+}
+
+// The bias-correction terms for the next step (the same expressions as the
+// decision kernel's), written by one thread of pass 2 after its own
+// elements; the next decision kernel picks them up if its tags match.
+__device__ __forceinline__ void precompute_next(const StepScalars *scp, PowCache *cache)
+{
+    const int64_t tn = scp->next_t;
+    const double lr = scp->lr, beta1 = scp->beta1, beta2 = scp->beta2;
+    const double t = (double)tn;
+    const double bc1 = 1.0 - pow(beta1, t);
+    const double bc2 = 1.0 - pow(beta2, t);
+    cache->t = tn;
+    cache->beta1 = beta1;
+    cache->beta2 = beta2;
+    cache->lr = lr;
+    cache->bc1 = bc1;
+    cache->step_size = (float)(lr / bc1);
+    cache->isb2 = (float)(1.0 / sqrt(bc2));
 }
 
 // ------------------------------------------------------------- pass 2
@@ -538,9 +577,9 @@ __device__ __forceinline__ void adam_range(const void *g, float *p, float *m, fl
 // schedule streams the five arrays at about 7.0 TB/s where persistent
 // grid-stride grids of 1 to 16 blocks per SM reach 5.1 to 6.8 TB/s.
 template <int GT, int PT>
-__global__ void __launch_bounds__(kThreads)
+__global__ void __launch_bounds__(kThreads, 5)
     k_adam_flat(const void *__restrict__ g, float *__restrict__ p, float *__restrict__ m, float *__restrict__ v,
-                void *__restrict__ plp, int64_t n, const StepScalars *__restrict__ scp)
+                void *__restrict__ plp, int64_t n, const StepScalars *__restrict__ scp, PowCache *cache)
 {
     pdl_wait();
     const StepScalars s = *scp;
@@ -552,17 +591,21 @@ __global__ void __launch_bounds__(kThreads)
         adam_vec<GT, PT>(g, p, m, v, plp, i, s);
     else if (i - nv < (n & 7))
         adam_scalar<GT, PT>(g, p, m, v, plp, (nv << 3) + (i - nv), s);
+    if (i == 0)
+        precompute_next(scp, cache);
 }
 
 template <int GT, int PT>
 __global__ void __launch_bounds__(kThreads)
     k_adam_list(const TensorEntry *__restrict__ ents, const Chunk *__restrict__ chunks, int64_t n_chunks,
-                const StepScalars *__restrict__ scp)
+                const StepScalars *__restrict__ scp, PowCache *cache)
 {
     pdl_wait();
     const StepScalars s = *scp;
     if (s.skip)
         return;
+    if (blockIdx.x == 0 && threadIdx.x == 0)
+        precompute_next(scp, cache);
     for (int64_t c = blockIdx.x; c < n_chunks; c += gridDim.x) {
         const Chunk ch = chunks[c];
         const TensorEntry e = ents[ch.tensor];
@@ -855,6 +898,7 @@ template <int GT, int PT>
 int launch_adam(const zero_tlist_t *g, const zero_tlist_t *p, const zero_tlist_t *m, const zero_tlist_t *v,
                 const zero_tlist_t *plp, const StepScalars *sc, void *ws, cudaStream_t stream)
 {
+    PowCache *cache = reinterpret_cast<PowCache *>(static_cast<unsigned char *>(ws) + kWsPowCache);
     if (g->n == 0)
         return ZERO_OK;
     if (g->n == 1) {
@@ -868,7 +912,7 @@ int launch_adam(const zero_tlist_t *g, const zero_tlist_t *p, const zero_tlist_t
             return ZERO_EINVAL;
         launch_pdl(k_adam_flat<GT, PT>, (int)grid, kThreads, stream, (const void *)g->ptrs[0],
                    static_cast<float *>(p->ptrs[0]), static_cast<float *>(m->ptrs[0]),
-                   static_cast<float *>(v->ptrs[0]), plp ? plp->ptrs[0] : nullptr, n, sc);
+                   static_cast<float *>(v->ptrs[0]), plp ? plp->ptrs[0] : nullptr, n, sc, cache);
         return check_launch("zero_adam_step");
     }
     int64_t n_chunks = 0;
@@ -879,7 +923,7 @@ int launch_adam(const zero_tlist_t *g, const zero_tlist_t *p, const zero_tlist_t
         return rc;
     const int grid = grid_for((const void *)k_adam_list<GT, PT>, n_chunks, 1 << 30);
     launch_pdl(k_adam_list<GT, PT>, grid, kThreads, stream, (const TensorEntry *)ents, (const Chunk *)chunks,
-               n_chunks, (const StepScalars *)sc);
+               n_chunks, (const StepScalars *)sc, cache);
     return check_launch("zero_adam_step");
 }
 
@@ -1018,12 +1062,17 @@ extern "C" int zero_adam_step(const zero_tlist_t *grads, const zero_tlist_t *mas
     a.lr = hp->lr;
     a.beta1 = hp->beta1;
     a.beta2 = hp->beta2;
-    a.eps = hp->eps;
-    a.weight_decay = hp->weight_decay;
     a.max_norm = hp->max_norm;
     a.min_scale = hp->min_scale;
     a.scale_window = hp->scale_window;
-    launch_pdl(k_decide, 1, 32, s, d_state, sc, a);
+    a.b1 = (float)hp->beta1;
+    a.omb1 = (float)(1.0 - hp->beta1);
+    a.b2 = (float)hp->beta2;
+    a.omb2 = (float)(1.0 - hp->beta2);
+    a.eps = (float)hp->eps;
+    a.lrwd = (float)(hp->lr * hp->weight_decay);
+    const PowCache *cache = reinterpret_cast<const PowCache *>(static_cast<unsigned char *>(ws) + kWsPowCache);
+    launch_pdl(k_decide, 1, 32, s, d_state, sc, cache, a);
     if ((rc = check_launch("zero_adam_step (decision)")) != ZERO_OK)
         return rc;
     const int32_t pd = p_lp ? p_lp->dtype : ZERO_F16;

@@ -31,6 +31,21 @@ struct StepScalars {
     float lrwd;       // lr * weight_decay
     int32_t skip;
     int32_t pad;
+    // for the bias-correction precompute of the next step (see PowCache)
+    double lr, beta1, beta2;
+    int64_t next_t;   // step count of the next applied step
+};
+
+// The binary64 bias-correction terms of one step count t, computed ahead of
+// time by the first block of pass 2 (off the critical path) for the next
+// step, and used by the next decision kernel when its tags match.
+struct PowCache {
+    int64_t t;             // tag: step count; 0 = empty
+    double beta1, beta2;   // tags
+    double lr;             // tag of step_size
+    double bc1;            // 1 - beta1^t
+    float step_size;       // lr / bc1, rounded once
+    float isb2;            // 1 / sqrt(1 - beta2^t), rounded once
 };
 
 // One array set of a list: the gradient, the fp32 master / momentum /
@@ -53,13 +68,17 @@ struct Chunk {
 
 // Workspace layout (all offsets 256-byte aligned):
 //   [0, 256)            header: reduction ticket
-//   [256, 512)          StepScalars of the current step
+//   [256, 384)          StepScalars of the current step
+//   [384, 512)          PowCache for the next step
 //   [512, 512 + 16*kMaxBlocks)  per-block partials of the norm pass (double2)
 //   then                TensorEntry[max_tensors], Chunk[max_chunks]
 struct WsHeader {
     unsigned int ticket;
 };
 constexpr size_t kWsScalars = 256;
+constexpr size_t kWsPowCache = 384;
+static_assert(sizeof(StepScalars) <= 128, "StepScalars must fit its workspace slot");
+static_assert(sizeof(PowCache) <= 128, "PowCache must fit its workspace slot");
 constexpr size_t kWsPartials = 512;
 constexpr size_t kWsTable = kWsPartials + 16 * (size_t)kMaxBlocks;
 
