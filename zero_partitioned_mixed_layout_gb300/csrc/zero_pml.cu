@@ -37,6 +37,9 @@ namespace zpml {
 namespace {
 
 constexpr int kWarps = kThreads / 32;
+// Bytes at the end of a flat gradient that pass 1 asks L2 to keep for pass 2
+// (GB300 has 126 MB of L2; pass 2's other streams are evict-first).
+constexpr int64_t kL2KeepBytes = 96ll << 20;
 
 // ------------------------------------------------------------- element types
 
@@ -300,11 +303,26 @@ __device__ __forceinline__ void norm_group(const uint4 (*w)[Elem<GT>::kWords], i
     tot += (double)tree8(acc);
 }
 
+// 16-byte load that asks L2 to keep the line (evict-last priority).
+__device__ __forceinline__ uint4 ld_keep(const uint4 *p)
+{
+    uint4 r;
+    uint64_t pol;
+    asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(pol));
+    asm volatile("ld.global.L2::cache_hint.v4.u32 {%0,%1,%2,%3}, [%4], %5;"
+                 : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+                 : "l"(p), "l"(pol));
+    return r;
+}
+
 // Vectors [0, nv) of one array, thread `t` of `nt` taking vectors
-// t, t + nt, ... four at a time; then the scalar tail [8*nv, n).
+// t, t + nt, ... four at a time; then the scalar tail [8*nv, n).  Vectors
+// from `keep_from` on are loaded with evict-last priority: pass 2 walks the
+// shard from its end, so that tail of the gradient is still in L2 when pass
+// 2 reads it again.
 template <int GT>
 __device__ __forceinline__ void norm_range(const void *g, int64_t n, int64_t t, int64_t nt, double &tot,
-                                           uint32_t &bad)
+                                           uint32_t &bad, int64_t keep_from = INT64_MAX)
 {
     constexpr int W = Elem<GT>::kWords;
     const uint4 *gv = static_cast<const uint4 *>(g);
@@ -316,9 +334,15 @@ __device__ __forceinline__ void norm_range(const void *g, int64_t n, int64_t t, 
         for (int k = 0; k < 4; ++k) {
             const int64_t j = i + k * nt;
             if (j < nv) {
+                if (j >= keep_from) {
 #pragma unroll
-                for (int q = 0; q < W; ++q)
-                    w[k][q] = __ldcs(gv + j * W + q);
+                    for (int q = 0; q < W; ++q)
+                        w[k][q] = ld_keep(gv + j * W + q);
+                } else {
+#pragma unroll
+                    for (int q = 0; q < W; ++q)
+                        w[k][q] = __ldcs(gv + j * W + q);
+                }
                 count = k + 1;
             }
         }
@@ -341,8 +365,10 @@ __global__ void __launch_bounds__(kThreads)
     pdl_wait();
     double tot = 0.0;
     uint32_t bad = 0;
+    // keep the last kL2KeepBytes of the gradient in L2 for pass 2
+    const int64_t keep_vectors = kL2KeepBytes / (8 * Elem<GT>::kBytes);
     norm_range<GT>(g, n, (int64_t)blockIdx.x * kThreads + threadIdx.x, (int64_t)gridDim.x * kThreads, tot,
-                   bad);
+                   bad, (n >> 3) - keep_vectors);
     norm_finish(tot, bad, partials, hdr, st, accumulate);
 }
 
@@ -572,12 +598,12 @@ __device__ __forceinline__ void adam_range(const void *g, float *p, float *m, fl
 }
 
 // One thread per 8-element vector, no loop: the grid covers the whole
-// array once (ceil(n / 2048) blocks), the last n mod 8 elements going to the
-// threads just past the last vector.  Measured on GB300 this one-shot
+// array once (ceil(n / 2048) blocks, taken from the end of the array), the
+// last n mod 8 elements going to the threads just past the last vector.  Measured on GB300 this one-shot
 // schedule streams the five arrays at about 7.0 TB/s where persistent
 // grid-stride grids of 1 to 16 blocks per SM reach 5.1 to 6.8 TB/s.
 template <int GT, int PT>
-__global__ void __launch_bounds__(kThreads, 5)
+__global__ void __launch_bounds__(kThreads, 4)
     k_adam_flat(const void *__restrict__ g, float *__restrict__ p, float *__restrict__ m, float *__restrict__ v,
                 void *__restrict__ plp, int64_t n, const StepScalars *__restrict__ scp, PowCache *cache)
 {
@@ -586,12 +612,14 @@ __global__ void __launch_bounds__(kThreads, 5)
     if (s.skip)
         return;
     const int64_t nv = n >> 3;
-    const int64_t i = (int64_t)blockIdx.x * kThreads + threadIdx.x;
+    // blocks walk the shard from its end: pass 1 left that end of the
+    // gradient in L2
+    const int64_t i = (int64_t)(gridDim.x - 1 - blockIdx.x) * kThreads + threadIdx.x;
     if (i < nv)
         adam_vec<GT, PT>(g, p, m, v, plp, i, s);
     else if (i - nv < (n & 7))
         adam_scalar<GT, PT>(g, p, m, v, plp, (nv << 3) + (i - nv), s);
-    if (i == 0)
+    if (blockIdx.x == 0 && threadIdx.x == 0)
         precompute_next(scp, cache);
 }
 
