@@ -2,7 +2,8 @@
 
 One step = the whole hot path over one rank's shard: pass 1 (unscale,
 overflow, global squared norm), the decision kernel and pass 2 (clip, AdamW,
-cast), all through the C ABI.  Default workload: the GPT-2 1.5B model state
+cast), all through the C ABI (zero_step on one GPU; zero_grad_norm_overflow,
+the cross-rank sum and zero_adam_step on several).  Default workload: the GPT-2 1.5B model state
 flattened into 16 ZeRO shards, rank 0's shard of 97,350,784 params, fp16
 gradients (x65536 loss scale), fp32 master/momentum/variance, fp16 params.
 
@@ -253,6 +254,11 @@ class Workload:
         zp = self.zp
         if self.micro > 1:
             zp.zero_accumulate_grads(self.g, self.bufs, overwrite=True, stream=stream)
+        if exchange is None and ev is None:
+            # one rank: the whole step in one call
+            zp.zero_step(self.g, self.p, self.m, self.v, self.lp, self.hp, self.state, self.ws,
+                         stream=stream)
+            return
         zp.zero_grad_norm_overflow(self.g, self.state, self.ws, stream=stream)
         if exchange is not None:
             exchange(self.state)

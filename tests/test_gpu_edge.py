@@ -169,7 +169,9 @@ def test_partition_invariance(zp, max_norm, mode):
 def test_list_equals_flat(zp):
     """One flat array versus the same elements cut into a list of arrays
     (ragged pieces): identical elementwise results, norms within 1e-8."""
-    sizes = [1, 9, 65536, 70001, 3, 131072 * 2 + 5, 8]
+    # 2047, 4094, 2041: a last 2048-element tile whose 8-element vectors and
+    # scalar tail together need more threads than a block has
+    sizes = [1, 9, 65536, 70001, 3, 131072 * 2 + 5, 8, 2047, 4094, 2041, 2048 * 3 + 2045]
     n = sum(sizes)
     ohp, ghp = hp_pair()
     p0 = zs.host_master(n, 3)
@@ -277,3 +279,41 @@ def test_argument_errors_launch_nothing(zp):
     assert rc == -1
     torch.cuda.synchronize()
     assert torch.equal(st, before), "a rejected call changed the state"
+
+
+@pytest.mark.parametrize("kind", ["flat", "list"])
+@pytest.mark.parametrize("max_norm", [0.0, 0.3])
+def test_fused_step_equals_split_calls(zp, kind, max_norm):
+    """zero_step (pass 1, decision and pass 2 in one call, the kernels of a
+    flat shard chained) gives the bits of zero_grad_norm_overflow followed by
+    zero_adam_step, state included, over steps with and without overflow."""
+    sizes = [1_000_003] if kind == "flat" else [5, 70_001, 3, 262_149, 8, 1, 4096, 2047, 6141]
+    total = sum(sizes)
+    p0 = zs.host_master(total, 21)
+    offs = np.concatenate([[0], np.cumsum(sizes)])
+    _, ghp = hp_pair(max_norm=max_norm)
+
+    def make():
+        return dict(
+            p=[torch.from_numpy(p0[offs[i]:offs[i + 1]].copy()).cuda() for i in range(len(sizes))],
+            m=[torch.zeros(n, device="cuda") for n in sizes],
+            v=[torch.zeros(n, device="cuda") for n in sizes],
+            lp=[torch.zeros(n, dtype=torch.float16, device="cuda") for n in sizes],
+            st=zp.new_state(1024.0), ws=zp.new_workspace(len(sizes), total))
+
+    a, b = make(), make()
+    for k in range(4):
+        g = zs.host_grad(total, 21, k, zp.parse_state(a["st"])["loss_scale"], "f16")
+        if k == 1:
+            g[total - 2] = np.inf
+        gl = [torch.from_numpy(g[offs[i]:offs[i + 1]].copy()).cuda() for i in range(len(sizes))]
+        zp.zero_grad_norm_overflow(gl, a["st"], a["ws"])
+        zp.zero_adam_step(gl, a["p"], a["m"], a["v"], a["lp"], ghp, a["st"], a["ws"])
+        zp.zero_step(gl, b["p"], b["m"], b["v"], b["lp"], ghp, b["st"], b["ws"])
+        torch.cuda.synchronize()
+        assert torch.equal(a["st"], b["st"]), f"state differs at step {k}"
+        for key in ("p", "m", "v", "lp"):
+            for x, y in zip(a[key], b[key]):
+                assert torch.equal(x, y), f"{key} differs at step {k}"
+    st = zp.parse_state(b["st"])
+    assert st["step"] == 3 and st["skipped"] == 1

@@ -25,6 +25,7 @@ from .binding import (  # noqa: F401
     zero_grad_norm_overflow,
     zero_partition_layout,
     zero_state_init,
+    zero_step,
     zero_strerror,
     zero_workspace_bytes,
 )

@@ -85,8 +85,9 @@ def lib():
                                                ctypes.c_size_t, vp]
         so.zero_adam_step.argtypes = [ctypes.POINTER(_TList)] * 5 + [
             ctypes.POINTER(_HParams), vp, vp, ctypes.c_size_t, vp]
+        so.zero_step.argtypes = so.zero_adam_step.argtypes
         for f in ("zero_partition_layout", "zero_state_init", "zero_accumulate_grads",
-                  "zero_grad_norm_overflow", "zero_adam_step"):
+                  "zero_grad_norm_overflow", "zero_adam_step", "zero_step"):
             getattr(so, f).restype = ctypes.c_int
         _lib = so
     return _lib
@@ -279,15 +280,24 @@ def zero_grad_norm_overflow(grads, state, ws, accumulate: bool = False, stream=N
 
 def zero_adam_step(grads, master, m, v, p_lp, hp: HParams, state, ws, stream=None) -> None:
     """The decision kernel and pass 2 over one shard or a list of arrays."""
+    _step_call("zero_adam_step", grads, master, m, v, p_lp, hp, state, ws, stream)
+
+
+def zero_step(grads, master, m, v, p_lp, hp: HParams, state, ws, stream=None) -> None:
+    """Pass 1, the decision kernel and pass 2 of a single-rank step in one call."""
+    _step_call("zero_step", grads, master, m, v, p_lp, hp, state, ws, stream)
+
+
+def _step_call(fn, grads, master, m, v, p_lp, hp, state, ws, stream):
     lg = _ListArgs(grads, "grads")
     lp_, lm, lv = _ListArgs(master, "master"), _ListArgs(m, "m"), _ListArgs(v, "v")
     ll = _ListArgs(p_lp, "p_lp") if p_lp is not None else None
     _device_tensor(state, "state")
     _device_tensor(ws, "workspace")
     h = hp._c()
-    rc = lib().zero_adam_step(ctypes.byref(lg.tl), ctypes.byref(lp_.tl), ctypes.byref(lm.tl),
+    rc = getattr(lib(), fn)(ctypes.byref(lg.tl), ctypes.byref(lp_.tl), ctypes.byref(lm.tl),
                               ctypes.byref(lv.tl), ctypes.byref(ll.tl) if ll else None,
                               ctypes.byref(h), ctypes.c_void_p(state.data_ptr()),
                               ctypes.c_void_p(ws.data_ptr()), ws.numel(),
                               _stream_ptr(stream, state.device))
-    _check(rc, "zero_adam_step")
+    _check(rc, fn)

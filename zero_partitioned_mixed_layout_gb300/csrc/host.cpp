@@ -124,5 +124,5 @@ extern "C" size_t zero_workspace_bytes(int64_t max_tensors, int64_t max_total_nu
     if (max_total_numel < 0)
         max_total_numel = 0;
     return zpml::kWsTable +
-           zpml::table_bytes(max_tensors, zpml::max_chunks(max_tensors, max_total_numel));
+           zpml::table_bytes(max_tensors, zpml::max_items(max_tensors, max_total_numel));
 }

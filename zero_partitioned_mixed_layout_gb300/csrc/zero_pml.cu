@@ -359,9 +359,10 @@ __device__ __forceinline__ void norm_range(const void *g, int64_t n, int64_t t, 
 template <int GT>
 __global__ void __launch_bounds__(kThreads)
     k_norm_flat(const void *__restrict__ g, int64_t n, double2 *partials, WsHeader *hdr, zero_state_t *st,
-                int accumulate)
+                int accumulate, int trigger)
 {
-    pdl_launch_next();
+    if (trigger)
+        pdl_launch_next();
     pdl_wait();
     double tot = 0.0;
     uint32_t bad = 0;
@@ -377,7 +378,6 @@ __global__ void __launch_bounds__(kThreads)
     k_norm_list(const TensorEntry *__restrict__ ents, const Chunk *__restrict__ chunks, int64_t n_chunks,
                 double2 *partials, WsHeader *hdr, zero_state_t *st, int accumulate)
 {
-    pdl_launch_next();
     pdl_wait();
     double tot = 0.0;
     uint32_t bad = 0;
@@ -623,9 +623,11 @@ __global__ void __launch_bounds__(kThreads, 4)
         precompute_next(scp, cache);
 }
 
+// Pass 2 over a list: one block per tile of kTile elements of one tensor,
+// one vector per thread (the one-shot schedule of the flat kernel).
 template <int GT, int PT>
-__global__ void __launch_bounds__(kThreads)
-    k_adam_list(const TensorEntry *__restrict__ ents, const Chunk *__restrict__ chunks, int64_t n_chunks,
+__global__ void __launch_bounds__(kThreads, 4)
+    k_adam_list(const TensorEntry *__restrict__ ents, const Chunk *__restrict__ tiles,
                 const StepScalars *__restrict__ scp, PowCache *cache)
 {
     pdl_wait();
@@ -634,15 +636,20 @@ __global__ void __launch_bounds__(kThreads)
         return;
     if (blockIdx.x == 0 && threadIdx.x == 0)
         precompute_next(scp, cache);
-    for (int64_t c = blockIdx.x; c < n_chunks; c += gridDim.x) {
-        const Chunk ch = chunks[c];
-        const TensorEntry e = ents[ch.tensor];
-        const int64_t start = (int64_t)ch.index * kChunk;
-        const int64_t len = min(kChunk, e.numel - start);
-        const void *g = static_cast<const char *>(e.g) + start * Elem<GT>::kBytes;
-        void *plp = e.plp ? static_cast<void *>(static_cast<char *>(e.plp) + start * 2) : nullptr;
-        adam_range<GT, PT>(g, e.p + start, e.m + start, e.v + start, plp, len, threadIdx.x, kThreads, s);
-    }
+    const Chunk tl = tiles[blockIdx.x];
+    const TensorEntry e = ents[tl.tensor];
+    const int64_t start = (int64_t)tl.index * kTile;
+    const int64_t len = min(kTile, e.numel - start);
+    const void *g = static_cast<const char *>(e.g) + start * Elem<GT>::kBytes;
+    void *plp = e.plp ? static_cast<void *>(static_cast<char *>(e.plp) + start * 2) : nullptr;
+    const int64_t nv = len >> 3;
+    const int64_t t = threadIdx.x;
+    if (t < nv)
+        adam_vec<GT, PT>(g, e.p + start, e.m + start, e.v + start, plp, t, s);
+    // the tail of a tensor's last tile (up to 7 elements) goes to threads
+    // 0..6, which may also hold a vector: nv + tail can exceed the block
+    if (t < (len & 7))
+        adam_scalar<GT, PT>(g, e.p + start, e.m + start, e.v + start, plp, (nv << 3) + t, s);
 }
 
 // ------------------------------------------------------------- accumulate
@@ -754,11 +761,14 @@ int grid_for(const void *kernel, int64_t work_items, int cap, int per_sm_cap = 1
     return g < 1 ? 1 : (int)g;
 }
 
-// Launches a kernel with programmatic stream serialisation, so that it can
-// be scheduled while the previous kernel in the stream finishes (the kernel
-// itself waits in pdl_wait() before touching memory).
+// Launches a kernel; with `pdl` set, with programmatic stream
+// serialisation, so that it can be scheduled while the previous kernel in
+// the stream finishes (the kernel itself waits in pdl_wait() before touching
+// memory).  The wait covers the previous KERNEL only: `pdl` is set only where
+// the previous operation in the stream is this library's own kernel of the
+// same call -- never after a copy, a memset or the caller's work.
 template <typename... KArgs, typename... Args>
-cudaError_t launch_pdl(void (*kernel)(KArgs...), int grid, int block, cudaStream_t stream, Args... args)
+cudaError_t launch_k(void (*kernel)(KArgs...), int grid, int block, cudaStream_t stream, bool pdl, Args... args)
 {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)grid);
@@ -769,7 +779,7 @@ cudaError_t launch_pdl(void (*kernel)(KArgs...), int grid, int block, cudaStream
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = pdl ? 1 : 0;
     return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
 }
 
@@ -856,13 +866,13 @@ int check_ws(void *ws, size_t ws_bytes, int64_t n_tensors, int64_t total)
 // them into the workspace (stream-ordered).  Returns the chunk count in
 // *n_chunks.
 int upload_table(const zero_tlist_t *g, const zero_tlist_t *p, const zero_tlist_t *m, const zero_tlist_t *v,
-                 const zero_tlist_t *plp, void *ws, cudaStream_t stream, int64_t *n_chunks,
+                 const zero_tlist_t *plp, void *ws, cudaStream_t stream, int64_t item, int64_t *n_chunks,
                  TensorEntry **d_ents, Chunk **d_chunks)
 {
     const int64_t n = g->n;
     int64_t chunks = 0;
     for (int64_t i = 0; i < n; ++i)
-        chunks += (g->numel[i] + kChunk - 1) / kChunk;
+        chunks += (g->numel[i] + item - 1) / item;
     const size_t ent_bytes = align256((size_t)n * sizeof(TensorEntry));
     std::vector<unsigned char> host(ent_bytes + (size_t)chunks * sizeof(Chunk));
     TensorEntry *ents = reinterpret_cast<TensorEntry *>(host.data());
@@ -876,7 +886,7 @@ int upload_table(const zero_tlist_t *g, const zero_tlist_t *p, const zero_tlist_
         e.v = v ? static_cast<float *>(v->ptrs[i]) : nullptr;
         e.plp = plp ? plp->ptrs[i] : nullptr;
         e.numel = g->numel[i];
-        const int64_t k = (g->numel[i] + kChunk - 1) / kChunk;
+        const int64_t k = (g->numel[i] + item - 1) / item;
         for (int64_t j = 0; j < k; ++j) {
             ch[c].tensor = (int32_t)i;
             ch[c].index = (int32_t)j;
@@ -893,9 +903,12 @@ int upload_table(const zero_tlist_t *g, const zero_tlist_t *p, const zero_tlist_
     return ZERO_OK;
 }
 
+// Pass 1.  `trigger`: the next operation in the stream is this library's
+// decision kernel launched with PDL (the fused step), so the norm kernel may
+// let it be scheduled early.
 template <int GT>
 int launch_norm(const zero_tlist_t *grads, int64_t total, zero_state_t *st, int accumulate, void *ws,
-                cudaStream_t stream)
+                cudaStream_t stream, bool trigger)
 {
     unsigned char *w = static_cast<unsigned char *>(ws);
     WsHeader *hdr = reinterpret_cast<WsHeader *>(w);
@@ -906,29 +919,32 @@ int launch_norm(const zero_tlist_t *grads, int64_t total, zero_state_t *st, int 
         // persistent grid of 4 blocks per SM (measured best for this pass)
         const int64_t items = ((n >> 3) + 4 * kThreads - 1) / (4 * kThreads);
         const int grid = grid_for((const void *)k_norm_flat<GT>, items, kMaxBlocks, 4);
-        launch_pdl(k_norm_flat<GT>, grid, kThreads, stream, g, n, partials, hdr, st, accumulate);
+        launch_k(k_norm_flat<GT>, grid, kThreads, stream, false, g, n, partials, hdr, st, accumulate,
+                 (int)trigger);
         return check_launch("zero_grad_norm_overflow");
     }
     int64_t n_chunks = 0;
     TensorEntry *ents = nullptr;
     Chunk *chunks = nullptr;
-    int rc = upload_table(grads, nullptr, nullptr, nullptr, nullptr, ws, stream, &n_chunks, &ents, &chunks);
+    int rc = upload_table(grads, nullptr, nullptr, nullptr, nullptr, ws, stream, kChunk, &n_chunks, &ents,
+                          &chunks);
     if (rc != ZERO_OK)
         return rc;
     const int grid = grid_for((const void *)k_norm_list<GT>, n_chunks, kMaxBlocks, 4);
-    launch_pdl(k_norm_list<GT>, grid, kThreads, stream, (const TensorEntry *)ents, (const Chunk *)chunks,
-               n_chunks, partials, hdr, st, accumulate);
+    launch_k(k_norm_list<GT>, grid, kThreads, stream, false, (const TensorEntry *)ents, (const Chunk *)chunks,
+             n_chunks, partials, hdr, st, accumulate);
     (void)total;
     return check_launch("zero_grad_norm_overflow");
 }
 
+// Pass 2 (after the decision kernel, with PDL).  For a list the tile table
+// was uploaded before the decision kernel (see run_step).
 template <int GT, int PT>
 int launch_adam(const zero_tlist_t *g, const zero_tlist_t *p, const zero_tlist_t *m, const zero_tlist_t *v,
-                const zero_tlist_t *plp, const StepScalars *sc, void *ws, cudaStream_t stream)
+                const zero_tlist_t *plp, const StepScalars *sc, void *ws, cudaStream_t stream,
+                const TensorEntry *ents, const Chunk *tiles, int64_t n_tiles)
 {
     PowCache *cache = reinterpret_cast<PowCache *>(static_cast<unsigned char *>(ws) + kWsPowCache);
-    if (g->n == 0)
-        return ZERO_OK;
     if (g->n == 1) {
         const int64_t n = g->numel[0];
         if (n == 0)
@@ -936,33 +952,116 @@ int launch_adam(const zero_tlist_t *g, const zero_tlist_t *p, const zero_tlist_t
         // one thread per 8-element vector plus the n mod 8 tail threads
         const int64_t threads = (n >> 3) + (n & 7);
         const int64_t grid = (threads + kThreads - 1) / kThreads;
-        if (grid > 0x7fffffff)  // past 2^42 elements: beyond any device memory
-            return ZERO_EINVAL;
-        launch_pdl(k_adam_flat<GT, PT>, (int)grid, kThreads, stream, (const void *)g->ptrs[0],
-                   static_cast<float *>(p->ptrs[0]), static_cast<float *>(m->ptrs[0]),
-                   static_cast<float *>(v->ptrs[0]), plp ? plp->ptrs[0] : nullptr, n, sc, cache);
+        launch_k(k_adam_flat<GT, PT>, (int)grid, kThreads, stream, true, (const void *)g->ptrs[0],
+                 static_cast<float *>(p->ptrs[0]), static_cast<float *>(m->ptrs[0]),
+                 static_cast<float *>(v->ptrs[0]), plp ? plp->ptrs[0] : nullptr, n, sc, cache);
         return check_launch("zero_adam_step");
     }
-    int64_t n_chunks = 0;
-    TensorEntry *ents = nullptr;
-    Chunk *chunks = nullptr;
-    int rc = upload_table(g, p, m, v, plp, ws, stream, &n_chunks, &ents, &chunks);
-    if (rc != ZERO_OK || n_chunks == 0)
-        return rc;
-    const int grid = grid_for((const void *)k_adam_list<GT, PT>, n_chunks, 1 << 30);
-    launch_pdl(k_adam_list<GT, PT>, grid, kThreads, stream, (const TensorEntry *)ents, (const Chunk *)chunks,
-               n_chunks, (const StepScalars *)sc, cache);
+    if (n_tiles == 0)
+        return ZERO_OK;
+    // one-shot: one block per tile
+    launch_k(k_adam_list<GT, PT>, (int)n_tiles, kThreads, stream, true, ents, tiles, sc, cache);
     return check_launch("zero_adam_step");
 }
 
 template <int GT>
 int launch_adam_lp(int32_t pdtype, const zero_tlist_t *g, const zero_tlist_t *p, const zero_tlist_t *m,
                    const zero_tlist_t *v, const zero_tlist_t *plp, const StepScalars *sc, void *ws,
-                   cudaStream_t stream)
+                   cudaStream_t stream, const TensorEntry *ents, const Chunk *tiles, int64_t n_tiles)
 {
     if (pdtype == ZERO_BF16)
-        return launch_adam<GT, ZERO_BF16>(g, p, m, v, plp, sc, ws, stream);
-    return launch_adam<GT, ZERO_F16>(g, p, m, v, plp, sc, ws, stream);
+        return launch_adam<GT, ZERO_BF16>(g, p, m, v, plp, sc, ws, stream, ents, tiles, n_tiles);
+    return launch_adam<GT, ZERO_F16>(g, p, m, v, plp, sc, ws, stream, ents, tiles, n_tiles);
+}
+
+// Checks the arguments of the decision + pass 2 part of a step.
+int check_step_args(const zero_tlist_t *grads, const zero_tlist_t *master, const zero_tlist_t *m,
+                    const zero_tlist_t *v, const zero_tlist_t *p_lp, const zero_hparams_t *hp,
+                    zero_state_t *d_state, void *ws, size_t ws_bytes, int64_t *total)
+{
+    if (!hp || !d_state)
+        return ZERO_EINVAL;
+    if ((reinterpret_cast<uintptr_t>(d_state) & 7u) != 0)
+        return ZERO_EALIGN;
+    if (!device_ptr(d_state))
+        return ZERO_EINVAL;
+    if (!(hp->lr >= 0.0) || !(hp->beta1 >= 0.0 && hp->beta1 < 1.0) || !(hp->beta2 >= 0.0 && hp->beta2 < 1.0) ||
+        !(hp->eps >= 0.0) || !(hp->weight_decay >= 0.0) || !(hp->min_scale >= 1.0) || hp->scale_window < 1 ||
+        hp->max_norm != hp->max_norm)
+        return ZERO_EINVAL;
+    int64_t t2 = 0;
+    int rc = check_list(grads, total);
+    if (rc != ZERO_OK)
+        return rc;
+    const zero_tlist_t *states[3] = {master, m, v};
+    for (const zero_tlist_t *l : states) {
+        if ((rc = check_list(l, &t2)) != ZERO_OK)
+            return rc;
+        if (l->dtype != ZERO_F32)
+            return ZERO_EDTYPE;
+        if ((rc = check_same_shape(grads, l)) != ZERO_OK)
+            return rc;
+    }
+    if (p_lp) {
+        if ((rc = check_list(p_lp, &t2)) != ZERO_OK)
+            return rc;
+        if (!lp_dtype_ok(p_lp->dtype))
+            return ZERO_EDTYPE;
+        if ((rc = check_same_shape(grads, p_lp)) != ZERO_OK)
+            return rc;
+    }
+    if (!grad_dtype_ok(grads->dtype))
+        return ZERO_EDTYPE;
+    if (grads->n == 1 && ((grads->numel[0] >> 3) + 7) / kThreads >= 0x7fffffff)
+        return ZERO_EINVAL;  // past 2^42 elements: beyond any device memory
+    return check_ws(ws, ws_bytes, grads->n, *total);
+}
+
+// The decision kernel and pass 2 on checked arguments.  A list's tile table
+// is copied into the workspace first, so that nothing but the decision
+// kernel sits between that copy and pass 2.  `decide_pdl`: the previous
+// operation in the stream is this library's pass-1 kernel of the same call.
+int run_step(const zero_tlist_t *grads, const zero_tlist_t *master, const zero_tlist_t *m, const zero_tlist_t *v,
+             const zero_tlist_t *p_lp, const zero_hparams_t *hp, zero_state_t *d_state, void *ws,
+             cudaStream_t s, bool decide_pdl)
+{
+    int rc;
+    TensorEntry *ents = nullptr;
+    Chunk *tiles = nullptr;
+    int64_t n_tiles = 0;
+    if (grads->n > 1) {
+        if ((rc = upload_table(grads, master, m, v, p_lp, ws, s, kTile, &n_tiles, &ents, &tiles)) != ZERO_OK)
+            return rc;
+        if (n_tiles > 0x7fffffff)
+            return ZERO_EINVAL;
+        decide_pdl = false;  // a copy now precedes the decision kernel
+    }
+    StepScalars *sc = reinterpret_cast<StepScalars *>(static_cast<unsigned char *>(ws) + kWsScalars);
+    DecideArgs a;
+    a.lr = hp->lr;
+    a.beta1 = hp->beta1;
+    a.beta2 = hp->beta2;
+    a.max_norm = hp->max_norm;
+    a.min_scale = hp->min_scale;
+    a.scale_window = hp->scale_window;
+    a.b1 = (float)hp->beta1;
+    a.omb1 = (float)(1.0 - hp->beta1);
+    a.b2 = (float)hp->beta2;
+    a.omb2 = (float)(1.0 - hp->beta2);
+    a.eps = (float)hp->eps;
+    a.lrwd = (float)(hp->lr * hp->weight_decay);
+    const PowCache *cache = reinterpret_cast<const PowCache *>(static_cast<unsigned char *>(ws) + kWsPowCache);
+    launch_k(k_decide, 1, 32, s, decide_pdl, d_state, sc, cache, a);
+    if ((rc = check_launch("zero_adam_step (decision)")) != ZERO_OK)
+        return rc;
+    if (grads->n == 0)
+        return ZERO_OK;
+    const int32_t pd = p_lp ? p_lp->dtype : ZERO_F16;
+    switch (grads->dtype) {
+    case ZERO_F16: return launch_adam_lp<ZERO_F16>(pd, grads, master, m, v, p_lp, sc, ws, s, ents, tiles, n_tiles);
+    case ZERO_BF16: return launch_adam_lp<ZERO_BF16>(pd, grads, master, m, v, p_lp, sc, ws, s, ents, tiles, n_tiles);
+    default: return launch_adam_lp<ZERO_F32>(pd, grads, master, m, v, p_lp, sc, ws, s, ents, tiles, n_tiles);
+    }
 }
 
 }  // namespace
@@ -1038,9 +1137,9 @@ extern "C" int zero_grad_norm_overflow(const zero_tlist_t *grads, zero_state_t *
         return rc;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     switch (grads->dtype) {
-    case ZERO_F16: return launch_norm<ZERO_F16>(grads, total, d_state, accumulate, ws, s);
-    case ZERO_BF16: return launch_norm<ZERO_BF16>(grads, total, d_state, accumulate, ws, s);
-    default: return launch_norm<ZERO_F32>(grads, total, d_state, accumulate, ws, s);
+    case ZERO_F16: return launch_norm<ZERO_F16>(grads, total, d_state, accumulate, ws, s, false);
+    case ZERO_BF16: return launch_norm<ZERO_BF16>(grads, total, d_state, accumulate, ws, s, false);
+    default: return launch_norm<ZERO_F32>(grads, total, d_state, accumulate, ws, s, false);
     }
 }
 
@@ -1048,67 +1147,35 @@ extern "C" int zero_adam_step(const zero_tlist_t *grads, const zero_tlist_t *mas
                               const zero_tlist_t *v, const zero_tlist_t *p_lp, const zero_hparams_t *hp,
                               zero_state_t *d_state, void *ws, size_t ws_bytes, void *stream)
 {
-    if (!hp || !d_state)
-        return ZERO_EINVAL;
-    if ((reinterpret_cast<uintptr_t>(d_state) & 7u) != 0)
-        return ZERO_EALIGN;
-    if (!device_ptr(d_state))
-        return ZERO_EINVAL;
-    if (!(hp->lr >= 0.0) || !(hp->beta1 >= 0.0 && hp->beta1 < 1.0) || !(hp->beta2 >= 0.0 && hp->beta2 < 1.0) ||
-        !(hp->eps >= 0.0) || !(hp->weight_decay >= 0.0) || !(hp->min_scale >= 1.0) || hp->scale_window < 1 ||
-        hp->max_norm != hp->max_norm)
-        return ZERO_EINVAL;
-    int64_t total = 0, t2 = 0;
-    int rc = check_list(grads, &total);
+    int64_t total = 0;
+    int rc = check_step_args(grads, master, m, v, p_lp, hp, d_state, ws, ws_bytes, &total);
     if (rc != ZERO_OK)
         return rc;
-    const zero_tlist_t *states[3] = {master, m, v};
-    for (const zero_tlist_t *l : states) {
-        if ((rc = check_list(l, &t2)) != ZERO_OK)
-            return rc;
-        if (l->dtype != ZERO_F32)
-            return ZERO_EDTYPE;
-        if ((rc = check_same_shape(grads, l)) != ZERO_OK)
-            return rc;
-    }
-    if (p_lp) {
-        if ((rc = check_list(p_lp, &t2)) != ZERO_OK)
-            return rc;
-        if (!lp_dtype_ok(p_lp->dtype))
-            return ZERO_EDTYPE;
-        if ((rc = check_same_shape(grads, p_lp)) != ZERO_OK)
-            return rc;
-    }
-    if (!grad_dtype_ok(grads->dtype))
-        return ZERO_EDTYPE;
-    if ((rc = check_ws(ws, ws_bytes, grads->n, total)) != ZERO_OK)
-        return rc;
+    // the caller's work (e.g. the cross-rank sum) may precede the decision
+    // kernel: no early launch for it
+    return run_step(grads, master, m, v, p_lp, hp, d_state, ws, static_cast<cudaStream_t>(stream), false);
+}
 
-    cudaStream_t s = static_cast<cudaStream_t>(stream);
-    StepScalars *sc = reinterpret_cast<StepScalars *>(static_cast<unsigned char *>(ws) + kWsScalars);
-    DecideArgs a;
-    a.lr = hp->lr;
-    a.beta1 = hp->beta1;
-    a.beta2 = hp->beta2;
-    a.max_norm = hp->max_norm;
-    a.min_scale = hp->min_scale;
-    a.scale_window = hp->scale_window;
-    a.b1 = (float)hp->beta1;
-    a.omb1 = (float)(1.0 - hp->beta1);
-    a.b2 = (float)hp->beta2;
-    a.omb2 = (float)(1.0 - hp->beta2);
-    a.eps = (float)hp->eps;
-    a.lrwd = (float)(hp->lr * hp->weight_decay);
-    const PowCache *cache = reinterpret_cast<const PowCache *>(static_cast<unsigned char *>(ws) + kWsPowCache);
-    launch_pdl(k_decide, 1, 32, s, d_state, sc, cache, a);
-    if ((rc = check_launch("zero_adam_step (decision)")) != ZERO_OK)
+extern "C" int zero_step(const zero_tlist_t *grads, const zero_tlist_t *master, const zero_tlist_t *m,
+                         const zero_tlist_t *v, const zero_tlist_t *p_lp, const zero_hparams_t *hp,
+                         zero_state_t *d_state, void *ws, size_t ws_bytes, void *stream)
+{
+    int64_t total = 0;
+    int rc = check_step_args(grads, master, m, v, p_lp, hp, d_state, ws, ws_bytes, &total);
+    if (rc != ZERO_OK)
         return rc;
-    const int32_t pd = p_lp ? p_lp->dtype : ZERO_F16;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    // the three kernels of a flat shard follow one another with nothing in
+    // between: each is scheduled while the previous one drains
+    const bool chain = grads->n == 1;
     switch (grads->dtype) {
-    case ZERO_F16: return launch_adam_lp<ZERO_F16>(pd, grads, master, m, v, p_lp, sc, ws, s);
-    case ZERO_BF16: return launch_adam_lp<ZERO_BF16>(pd, grads, master, m, v, p_lp, sc, ws, s);
-    default: return launch_adam_lp<ZERO_F32>(pd, grads, master, m, v, p_lp, sc, ws, s);
+    case ZERO_F16: rc = launch_norm<ZERO_F16>(grads, total, d_state, 0, ws, s, chain); break;
+    case ZERO_BF16: rc = launch_norm<ZERO_BF16>(grads, total, d_state, 0, ws, s, chain); break;
+    default: rc = launch_norm<ZERO_F32>(grads, total, d_state, 0, ws, s, chain); break;
     }
+    if (rc != ZERO_OK)
+        return rc;
+    return run_step(grads, master, m, v, p_lp, hp, d_state, ws, s, chain);
 }
 
 // ------------------------------------------------------------- pass 1 without workspace

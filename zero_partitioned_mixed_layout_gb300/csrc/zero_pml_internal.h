@@ -17,6 +17,9 @@ constexpr int kMaxBlocks = 4096;
 // Elements per work item when the arrays come as a list (multiple of 8, so
 // every chunk but a tensor's last starts and ends on a 16-byte boundary).
 constexpr int64_t kChunk = 1 << 16;
+// Elements per work item of pass 2 over a list: one block of kThreads
+// threads, one 8-element vector each.
+constexpr int64_t kTile = (int64_t)kThreads * 8;
 
 // The scalars of one step's element update, written by the decision kernel
 // and read by every block of pass 2 (binary32, as the update runs).
@@ -59,8 +62,8 @@ struct TensorEntry {
     int64_t numel;
 };
 
-// One work item: elements [index * kChunk, min(numel, (index+1) * kChunk))
-// of tensor `tensor`.
+// One work item: elements [index * size, min(numel, (index+1) * size)) of
+// tensor `tensor`, size being kChunk (pass 1) or kTile (pass 2).
 struct Chunk {
     int32_t tensor;
     int32_t index;
@@ -71,7 +74,8 @@ struct Chunk {
 //   [256, 384)          StepScalars of the current step
 //   [384, 512)          PowCache for the next step
 //   [512, 512 + 16*kMaxBlocks)  per-block partials of the norm pass (double2)
-//   then                TensorEntry[max_tensors], Chunk[max_chunks]
+//   then                TensorEntry[max_tensors], then the work items of
+//                       the current pass (Chunk[], at most max_items of them)
 struct WsHeader {
     unsigned int ticket;
 };
@@ -84,9 +88,11 @@ constexpr size_t kWsTable = kWsPartials + 16 * (size_t)kMaxBlocks;
 
 inline size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
 
-inline int64_t max_chunks(int64_t max_tensors, int64_t max_total_numel)
+// Upper bound on the work items of a list (pass 2's tiles outnumber pass
+// 1's chunks).
+inline int64_t max_items(int64_t max_tensors, int64_t max_total_numel)
 {
-    return max_tensors + max_total_numel / kChunk + 1;
+    return max_tensors + max_total_numel / kTile + 1;
 }
 
 inline size_t table_bytes(int64_t n_tensors, int64_t n_chunks)
