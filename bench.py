@@ -463,6 +463,140 @@ def run_ours(args):
         dist.destroy_process_group()
 
 
+def run_offload(args):
+    """ZeRO-Offload on the GPT-2 1.5B Nd=16 shard: the fp32 master, momentum
+    and variance (12 B/param) live in pinned host memory, the gradient and
+    the fp16 parameters in HBM.  Main measurement: zero_step with the GPU
+    streaming the host-resident state over NVLink-C2C (12 B/param each way).
+    Also measured: the update on the host cores (zero_offload_decide /
+    zero_offload_apply), with the gradient sent over the link in chunks and
+    the fp16 parameters sent back."""
+    import numpy as np
+    import torch
+
+    import zero_partitioned_mixed_layout_gb300 as zp
+    import zero_synth as zs
+    dev = torch.device("cuda", torch.cuda.current_device())
+    w = zs.WORKLOADS[WORKLOAD]
+    S = zp.zero_partition_layout(w["numel"](), w["nd"], w["align"]).shard_numel
+    threads = zp.default_host_threads()
+    scale = w["loss_scale"]
+    dg = torch.empty(S, dtype=torch.float16, device=dev)
+    zs.device_grad_into(dg, 1000, 0, scale)
+    d_lp = torch.empty(S, dtype=torch.float16, device=dev)
+    hp = zp.HParams(**zs.HPARAMS)
+    stream = torch.cuda.current_stream(dev)
+
+    # -- the GPU streams the host-resident state over the link
+    p = torch.from_numpy(zs.host_master(S, 1000)).pin_memory()
+    m, v = torch.zeros(S).pin_memory(), torch.zeros(S).pin_memory()
+    d_state = zp.new_state(scale, dev)
+    ws = zp.new_workspace(1, S, dev)
+    for _ in range(args.warmup):
+        zp.zero_step(dg, p, m, v, d_lp, hp, d_state, ws, stream=stream)
+    torch.cuda.synchronize(dev)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(dev.index) as clk:
+        e0.record(stream)
+        for _ in range(args.steps):
+            zp.zero_step(dg, p, m, v, d_lp, hp, d_state, ws, stream=stream)
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+    dt_gpu = e0.elapsed_time(e1) / args.steps * 1e-3
+    assert zp.parse_state(d_state)["last_skipped"] == 0
+    # the link's two directions at once: copy-engine H2D and D2H of 1 GiB
+    hb = torch.empty(1 << 30, dtype=torch.uint8, pin_memory=True)
+    db = torch.empty(1 << 30, dtype=torch.uint8, device=dev)
+    hb2 = torch.empty(1 << 30, dtype=torch.uint8, pin_memory=True)
+    db2 = torch.empty(1 << 30, dtype=torch.uint8, device=dev)
+    s2 = torch.cuda.Stream(dev)
+    best = float("inf")
+    for _ in range(3):
+        torch.cuda.synchronize(dev)
+        c0 = time.perf_counter()
+        db.copy_(hb, non_blocking=True)
+        with torch.cuda.stream(s2):
+            hb2.copy_(db2, non_blocking=True)
+        torch.cuda.synchronize(dev)
+        best = min(best, time.perf_counter() - c0)
+    link_peak = 2 * (1 << 30) / best / 1e9
+    del hb, db, hb2, db2
+
+    # -- the update on the host cores
+    hp_, hm_, hv_ = p.clone(), torch.zeros(S), torch.zeros(S)
+    h_g = torch.empty(S, dtype=torch.float16, pin_memory=True)
+    h_lp = torch.empty(S, dtype=torch.float16, pin_memory=True)
+    h_state = torch.empty(zp.STATE_BYTES, dtype=torch.uint8, pin_memory=True)
+    d_state2 = zp.new_state(scale, dev)
+    up = torch.cuda.Stream(dev)
+    chunks = 16
+    edges = [S * c // chunks // 2048 * 2048 for c in range(chunks)] + [S]
+    got = [torch.cuda.Event() for _ in range(chunks)]
+    state_ev, sent = torch.cuda.Event(), torch.cuda.Event()
+
+    def host_step():
+        zp.zero_grad_norm_overflow(dg, d_state2, ws, stream=stream)
+        h_state.copy_(d_state2, non_blocking=True)
+        state_ev.record(stream)
+        for c in range(chunks):
+            h_g[edges[c]:edges[c + 1]].copy_(dg[edges[c]:edges[c + 1]], non_blocking=True)
+            got[c].record(stream)
+        state_ev.synchronize()
+        sc = zp.zero_offload_decide(h_state, hp)
+        for c in range(chunks):
+            lo, hi = edges[c], edges[c + 1]
+            got[c].synchronize()
+            zp.zero_offload_apply(h_g[lo:hi], hp_[lo:hi], hm_[lo:hi], hv_[lo:hi], h_lp[lo:hi], sc,
+                                  n_threads=threads)
+            with torch.cuda.stream(up):
+                d_lp[lo:hi].copy_(h_lp[lo:hi], non_blocking=True)
+        with torch.cuda.stream(up):
+            d_state2.copy_(h_state, non_blocking=True)
+        sent.record(up)
+        stream.wait_event(sent)
+        sent.synchronize()
+
+    for _ in range(min(args.warmup, 3)):
+        host_step()
+    host_steps = max(3, min(args.steps, 10))
+    t0 = time.perf_counter()
+    for _ in range(host_steps):
+        host_step()
+    dt_host = (time.perf_counter() - t0) / host_steps
+    a = np.ones(1 << 28, np.float32)
+    b = np.empty_like(a)
+    zp.zero_offload_copy(b, a, threads)
+    cbest = float("inf")
+    for _ in range(3):
+        c0 = time.perf_counter()
+        zp.zero_offload_copy(b, a, threads)
+        cbest = min(cbest, time.perf_counter() - c0)
+    host_peak = 2 * a.nbytes / cbest / 1e9
+
+    achieved = 24 * S / dt_gpu / 1e9
+    line = {
+        "metric": METRIC, "value": S / dt_gpu, "unit": UNIT, "n_gpus": 1, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": dt_gpu * 1e3, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": {"workload": "ZeRO-Offload on the GPT-2 1.5B Nd=16 rank-0 shard: fp32 master, "
+                               "momentum, variance in pinned host memory, streamed by the GPU over "
+                               "NVLink-C2C (zero_step); gradient and fp16 params in HBM",
+                   "shard_params": S, "c2c_bytes_per_param": {"to_gpu": 12, "to_host": 12}},
+        "roofline": {"bound": "host-link", "achieved": achieved, "peak": link_peak, "unit": "GB/s",
+                     "frac": achieved / link_peak, "traffic": None,
+                     "kernel": "zero_step with host-resident state, 24 B/param over NVLink-C2C",
+                     "peak_source": "copy-engine H2D + D2H of 1 GiB at once, measured in this run"},
+        "host_compute_mode": {
+            "value": S / dt_host, "unit": UNIT, "ms_per_step": dt_host * 1e3, "host_threads": threads,
+            "host_gbs_28B": 28 * S / dt_host / 1e9, "host_copy_peak_gbs": host_peak,
+            "note": "update on the host cores (zero_offload_apply); gradient to the host and fp16 "
+                    "params back over the link in 16 chunks each step"},
+        "gpu_launches": 3 * args.steps,
+        "clocks": clk.summary(),
+    }
+    print(json.dumps(line), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -472,7 +606,7 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--workload", default=WORKLOAD,
                     choices=["gpt2_1p5b_nd16", "tiny", "gpt2_1p5b_full", "stack_100b_nd400",
-                             "frag_10k", "flat"],
+                             "frag_10k", "flat", "offload"],
                     help="default: the GPT-2 1.5B Nd=16 shard the metric is quoted on")
     ap.add_argument("--log2n", type=int, default=26, help="size of the flat workload (2^k)")
     ap.add_argument("--clock-preroll", type=float, default=1.0,
@@ -482,6 +616,10 @@ def main():
         ap.error("--warmup must be at least 3")
     if args.impl == "reference":
         run_reference(args)
+    elif args.workload == "offload":
+        from zero_partitioned_mixed_layout_gb300 import _build
+        _build.build()
+        run_offload(args)
     else:
         import zero_partitioned_mixed_layout_gb300 as zp
         from zero_partitioned_mixed_layout_gb300 import _build

@@ -216,7 +216,11 @@ int zero_grad_norm_overflow_static(const zero_tlist_t *grads, zero_state_t *d_st
  *     with every scalar computed in binary64 and rounded once to binary32.
  * sumsq and found_inf are reset to 0; last_norm, last_clip, last_skipped are
  * set.  grads: F16, BF16 or F32; master, m, v: F32; p_lp: F16 or BF16, or
- * NULL for no low-precision copy.  All lists must have the same n and the
+ * NULL for no low-precision copy.  master, m and v may be pinned HOST memory
+ * (cudaHostAlloc / cudaHostRegister) instead of device memory: the GPU then
+ * streams the optimizer state over the host link (NVLink-C2C on GB300) while
+ * the gradient and the fp16 parameters stay in HBM -- the ZeRO-Offload
+ * memory split with the update still computed by the GPU.  All lists must have the same n and the
  * same numel per entry.  hp: host.  ws as for zero_grad_norm_overflow.
  * Errors: ZERO_EINVAL, ZERO_EDTYPE, ZERO_EALIGN, ZERO_ESIZE, ZERO_EWORKSPACE,
  * ZERO_ECUDA. */
@@ -235,6 +239,54 @@ int zero_adam_step(const zero_tlist_t *grads, const zero_tlist_t *master, const 
 int zero_step(const zero_tlist_t *grads, const zero_tlist_t *master, const zero_tlist_t *m,
               const zero_tlist_t *v, const zero_tlist_t *p_lp, const zero_hparams_t *hp,
               zero_state_t *d_state, void *ws, size_t ws_bytes, void *stream);
+
+/* ------------------------------------------------------------------ offload */
+
+/* ZeRO-Offload with the update on the host cores (DeepSpeed release news,
+ * lxsoso.com/blog/19320.html: ZeRO-Offload extends ZeRO-2 with CPU memory, so
+ * that one GPU trains a model about ten times larger).  (On GB300 the faster
+ * split keeps the state in pinned host memory and lets zero_step /
+ * zero_adam_step stream it over NVLink-C2C; these calls serve hosts whose
+ * link is too slow for that.)  The fp32 master, momentum and variance live in
+ * HOST memory and the host cores update them;
+ * the GPU computes pass 1 (zero_grad_norm_overflow) on its fp16 gradient and
+ * keeps the fp16 parameters.  A step: pass 1 on the GPU; copy the gradient
+ * and the zero_state_t to the host; zero_offload_decide on the host state;
+ * zero_offload_apply (whole arrays or chunk by chunk, as the gradient
+ * arrives); copy the low-precision parameters and the state back.  The
+ * results are those of zero_adam_step bit for bit (same binary32 expression,
+ * same binary64 step scalars). */
+
+/* The binary32 scalars of one step's element update (host). */
+typedef struct zero_offload_scalars {
+    float inv_scale, clip;
+    float beta1, one_minus_beta1, beta2, one_minus_beta2, eps;
+    float step_size;    /* lr / (1 - beta1^t) */
+    float inv_sqrt_bc2; /* 1 / sqrt(1 - beta2^t) */
+    float lr_wd;        /* lr * weight_decay */
+    int32_t skip;       /* 1: the step is skipped, apply does nothing */
+    int32_t reserved;
+} zero_offload_scalars_t;
+
+/* The step decision of zero_adam_step on a HOST zero_state_t whose sumsq and
+ * found_inf hold the step's global values: skip or apply, loss scale, step
+ * count, last norm / clip / skip, and the element scalars in *out.  Resets
+ * sumsq and found_inf.  Errors: ZERO_EINVAL. */
+int zero_offload_decide(zero_state_t *host_state, const zero_hparams_t *hp, zero_offload_scalars_t *out);
+
+/* The element update of zero_adam_step on HOST arrays of n elements, on
+ * n_threads host threads (a persistent pool; the calling thread is one of
+ * them): grad (F16, BF16 or F32), master, m, v (fp32, updated in place),
+ * p_lp (F16 or BF16, or NULL).  Any alignment; chunks of one step may be
+ * applied by separate calls.  Does nothing when sc->skip is set.
+ * Errors: ZERO_EINVAL, ZERO_EDTYPE. */
+int zero_offload_apply(const void *grad, int32_t gdtype, float *master, float *m, float *v, void *p_lp,
+                       int32_t pdtype, int64_t n, const zero_offload_scalars_t *sc, int32_t n_threads);
+
+/* memcpy of `bytes` host bytes on n_threads threads of the same pool, for
+ * staging and for measuring the host-memory bandwidth the apply runs
+ * against.  Errors: ZERO_EINVAL. */
+int zero_offload_copy(void *dst, const void *src, size_t bytes, int32_t n_threads);
 
 #ifdef __cplusplus
 }

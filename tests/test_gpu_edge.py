@@ -317,3 +317,47 @@ def test_fused_step_equals_split_calls(zp, kind, max_norm):
                 assert torch.equal(x, y), f"{key} differs at step {k}"
     st = zp.parse_state(b["st"])
     assert st["step"] == 3 and st["skipped"] == 1
+
+
+@pytest.mark.parametrize("kind", ["flat", "list"])
+@pytest.mark.parametrize("gdtype", ["f16", "f32"])
+def test_16_byte_aligned_state_matches_32(zp, kind, gdtype):
+    """fp32 arrays that start on a 16- but not a 32-byte boundary take the
+    16-byte access form of pass 2; it gives the bits of the 32-byte form."""
+    sizes = [100_003] if kind == "flat" else [4099, 70_001, 2047]
+    total = sum(sizes)
+    offs = np.concatenate([[0], np.cumsum(sizes)])
+    p0 = zs.host_master(total, 51)
+    _, ghp = hp_pair(max_norm=0.3)
+    scale = 1024.0 if gdtype == "f16" else 1.0
+    tdt = TORCH[gdtype]
+
+    def make(shift):
+        # `shift` floats into a 512-byte aligned allocation: 4 -> 16-byte aligned only
+        def arr(n, fill=None, dtype=torch.float32):
+            base = torch.zeros(n + 8, dtype=dtype, device="cuda")
+            out = base[shift:shift + n]
+            if fill is not None:
+                out.copy_(fill)
+            return out
+        return dict(p=[arr(n, torch.from_numpy(p0[offs[i]:offs[i + 1]].copy())) for i, n in enumerate(sizes)],
+                    m=[arr(n) for n in sizes], v=[arr(n) for n in sizes],
+                    lp=[torch.zeros(n, dtype=torch.float16, device="cuda") for n in sizes],
+                    st=zp.new_state(scale), ws=zp.new_workspace(len(sizes), total),
+                    shift=shift, arr=arr)
+
+    a32, a16 = make(0), make(4)
+    assert a16["p"][0].data_ptr() % 32 == 16 and a32["p"][0].data_ptr() % 32 == 0
+    for k in range(3):
+        g = zs.host_grad(total, 51, k, scale, gdtype)
+        gl = [torch.from_numpy(g[offs[i]:offs[i + 1]].copy()).cuda() for i in range(len(sizes))]
+        for d in (a32, a16):
+            gg = gl if gdtype != "f32" else [d["arr"](x.numel(), x, torch.float32) for x in gl]
+            zp.zero_step(gg if kind == "list" else gg[0], d["p"] if kind == "list" else d["p"][0],
+                         d["m"] if kind == "list" else d["m"][0], d["v"] if kind == "list" else d["v"][0],
+                         d["lp"] if kind == "list" else d["lp"][0], ghp, d["st"], d["ws"])
+        torch.cuda.synchronize()
+        assert torch.equal(a32["st"], a16["st"])
+        for key in ("p", "m", "v", "lp"):
+            for x, y in zip(a32[key], a16[key]):
+                assert torch.equal(x, y), f"{key} step {k}"

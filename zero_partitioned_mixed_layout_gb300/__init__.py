@@ -20,7 +20,12 @@ from .binding import (  # noqa: F401
     new_state,
     new_workspace,
     parse_state,
+    OffloadScalars,
+    default_host_threads,
     zero_accumulate_grads,
+    zero_offload_apply,
+    zero_offload_copy,
+    zero_offload_decide,
     zero_adam_step,
     zero_grad_norm_overflow,
     zero_partition_layout,

@@ -1,9 +1,10 @@
 """Builds libzero_pml.so in-tree with nvcc for sm_103a (GB300).
 
-Two translation units compiled in parallel -- the host-only part (layout,
-error strings, state init) and the CUDA part (kernels and device entry
-points) -- linked against the shared CUDA runtime, so that the library and
-PyTorch share one runtime (one current device, one set of streams).
+The translation units are compiled in parallel -- the host-only parts
+(layout, error strings, state init; the offload step on the host cores) with
+g++ and the CUDA part (kernels and device entry points) with nvcc -- and
+linked against the shared CUDA runtime, so that the library and PyTorch share
+one runtime (one current device, one set of streams).
 """
 from __future__ import annotations
 
@@ -66,7 +67,11 @@ def build(force: bool = False, verbose: bool = False) -> str:
         if src.endswith(".cu"):
             jobs.append([nvcc, "-c", src, "-o", obj] + common + cu_flags)
         else:
-            jobs.append([nvcc, "-x", "c++", "-c", src, "-o", obj] + common)
+            # host code: binary32 evaluated as written (no FMA contraction);
+            # no errno from sqrt, so that its loops vectorise (results unchanged)
+            jobs.append(["g++", "-c", src, "-o", obj, "-std=c++17", "-O3", "-fPIC", "-pthread",
+                         "-ffp-contract=off", "-fno-fast-math", "-fno-math-errno", "-Wall",
+                         "-I", INCLUDE, "-I", CSRC])
 
     def run(cmd):
         r = subprocess.run(cmd, capture_output=True, text=True)
@@ -80,6 +85,7 @@ def build(force: bool = False, verbose: bool = False) -> str:
                 raise RuntimeError(f"nvcc failed on {cmd[2]}")
     tmp = LIB + f".tmp{os.getpid()}"
     link = [nvcc, "-shared", "-cudart", "shared"] + ARCH + ["-o", tmp] + objs + [
+        "-Xcompiler", "-pthread",
         "-Xlinker", "-rpath," + os.path.join(cuda, "lib64"), "-Xlinker", "-rpath,$ORIGIN"]
     r = subprocess.run(link, capture_output=True, text=True)
     if r.returncode != 0:

@@ -176,9 +176,10 @@ def _dtype_code(t) -> int:
     return m[t.dtype]
 
 
-def _device_tensor(t, what: str):
-    if not t.is_cuda:
-        raise ValueError(f"{what} must be a CUDA tensor")
+def _device_tensor(t, what: str, allow_pinned: bool = False):
+    if not t.is_cuda and not (allow_pinned and t.is_pinned()):
+        raise ValueError(f"{what} must be a CUDA tensor" +
+                         (" or a pinned host tensor" if allow_pinned else ""))
     if not t.is_contiguous():
         raise ValueError(f"{what} must be contiguous")
     return t
@@ -187,18 +188,18 @@ def _device_tensor(t, what: str):
 class _ListArgs:
     """Keeps the ctypes arrays of one zero_tlist_t alive for the call."""
 
-    def __new__(cls, tensors, what: str):
+    def __new__(cls, tensors, what: str, allow_pinned: bool = False):
         if isinstance(tensors, TensorList):
             return tensors._args
         return super().__new__(cls)
 
-    def __init__(self, tensors, what: str):
+    def __init__(self, tensors, what: str, allow_pinned: bool = False):
         if isinstance(tensors, TensorList):
             return
         if not isinstance(tensors, (list, tuple)):
             tensors = [tensors]
         for t in tensors:
-            _device_tensor(t, what)
+            _device_tensor(t, what, allow_pinned)
         codes = {_dtype_code(t) for t in tensors}
         if len(codes) > 1:
             raise TypeError(f"{what}: mixed element types in one list")
@@ -216,9 +217,9 @@ class TensorList:
     unflattened tensors) then cost no per-call Python work.  The tensors are
     referenced, so their storage stays alive while the TensorList does."""
 
-    def __init__(self, tensors, what: str = "tensors"):
+    def __init__(self, tensors, what: str = "tensors", allow_pinned: bool = False):
         self.tensors = list(tensors)
-        self._args = _ListArgs(self.tensors, what)
+        self._args = _ListArgs(self.tensors, what, allow_pinned)
 
     def __len__(self):
         return len(self.tensors)
@@ -290,7 +291,8 @@ def zero_step(grads, master, m, v, p_lp, hp: HParams, state, ws, stream=None) ->
 
 def _step_call(fn, grads, master, m, v, p_lp, hp, state, ws, stream):
     lg = _ListArgs(grads, "grads")
-    lp_, lm, lv = _ListArgs(master, "master"), _ListArgs(m, "m"), _ListArgs(v, "v")
+    lp_ = _ListArgs(master, "master", allow_pinned=True)
+    lm, lv = _ListArgs(m, "m", allow_pinned=True), _ListArgs(v, "v", allow_pinned=True)
     ll = _ListArgs(p_lp, "p_lp") if p_lp is not None else None
     _device_tensor(state, "state")
     _device_tensor(ws, "workspace")
@@ -301,3 +303,109 @@ def _step_call(fn, grads, master, m, v, p_lp, hp, state, ws, stream):
                               ctypes.c_void_p(ws.data_ptr()), ws.numel(),
                               _stream_ptr(stream, state.device))
     _check(rc, fn)
+
+
+# ------------------------------------------------------------------ offload (host)
+
+class OffloadScalars(ctypes.Structure):
+    """zero_offload_scalars_t: the binary32 scalars of one step's update."""
+    _fields_ = [("inv_scale", ctypes.c_float), ("clip", ctypes.c_float),
+                ("beta1", ctypes.c_float), ("one_minus_beta1", ctypes.c_float),
+                ("beta2", ctypes.c_float), ("one_minus_beta2", ctypes.c_float),
+                ("eps", ctypes.c_float), ("step_size", ctypes.c_float),
+                ("inv_sqrt_bc2", ctypes.c_float), ("lr_wd", ctypes.c_float),
+                ("skip", ctypes.c_int32), ("reserved", ctypes.c_int32)]
+
+
+def _offload_lib():
+    so = lib()
+    if not getattr(so, "_offload_ready", False):
+        vp = ctypes.c_void_p
+        so.zero_offload_decide.argtypes = [vp, ctypes.POINTER(_HParams), ctypes.POINTER(OffloadScalars)]
+        so.zero_offload_apply.argtypes = [vp, ctypes.c_int32, vp, vp, vp, vp, ctypes.c_int32,
+                                          ctypes.c_int64, ctypes.POINTER(OffloadScalars),
+                                          ctypes.c_int32]
+        so.zero_offload_copy.argtypes = [vp, vp, ctypes.c_size_t, ctypes.c_int32]
+        for f in ("zero_offload_decide", "zero_offload_apply", "zero_offload_copy"):
+            getattr(so, f).restype = ctypes.c_int
+        so._offload_ready = True
+    return so
+
+
+def _host_array(x, what, code=None):
+    """(pointer, element count, dtype code) of a host numpy array or CPU
+    tensor; 16-bit patterns stored as uint16 need an explicit code."""
+    if hasattr(x, "data_ptr"):
+        if x.is_cuda:
+            raise ValueError(f"{what} must be in host memory")
+        if not x.is_contiguous():
+            raise ValueError(f"{what} must be contiguous")
+        return x.data_ptr(), x.numel(), _dtype_code(x) if code is None else code
+    if not isinstance(x, np.ndarray) or not x.flags["C_CONTIGUOUS"]:
+        raise ValueError(f"{what} must be a contiguous numpy array or CPU tensor")
+    if code is None:
+        code = {np.dtype(np.float16): ZERO_F16, np.dtype(np.float32): ZERO_F32}.get(x.dtype)
+        if code is None:
+            raise TypeError(f"{what}: pass dtype for {x.dtype} arrays")
+    return x.ctypes.data, x.size, code
+
+
+def default_host_threads() -> int:
+    import os
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
+def zero_offload_decide(host_state, hp: HParams) -> OffloadScalars:
+    """The step decision on a 64-byte host zero_state_t (numpy uint8 array or
+    CPU uint8 tensor), updated in place; returns the element scalars."""
+    ptr, n, _ = _host_array(host_state, "host_state", code=-1)
+    if n != STATE_BYTES:
+        raise ValueError("host_state must hold the 64 bytes of a zero_state_t")
+    out = OffloadScalars()
+    h = hp._c()
+    _check(_offload_lib().zero_offload_decide(ctypes.c_void_p(ptr), ctypes.byref(h),
+                                               ctypes.byref(out)), "zero_offload_decide")
+    return out
+
+
+def zero_offload_apply(grad, master, m, v, p_lp, scalars: OffloadScalars, gdtype=None,
+                       pdtype=None, n_threads: int = 0) -> None:
+    """The element update on host arrays (numpy or CPU tensors); gdtype /
+    pdtype: "f16", "bf16" or "f32" where the array type does not say it."""
+    codes = {"f16": ZERO_F16, "bf16": ZERO_BF16, "f32": ZERO_F32, None: None}
+    gp, n, gc = _host_array(grad, "grad", codes[gdtype])
+    arrs = []
+    for a, name in ((master, "master"), (m, "m"), (v, "v")):
+        ptr, na, code = _host_array(a, name)
+        if code != ZERO_F32:
+            raise TypeError(f"{name} must be float32")
+        if na != n:
+            raise ValueError("array sizes differ")
+        arrs.append(ptr)
+    lp, lc = None, ZERO_F16
+    if p_lp is not None:
+        lptr, ln, lc = _host_array(p_lp, "p_lp", codes[pdtype])
+        if ln != n:
+            raise ValueError("array sizes differ")
+        lp = ctypes.c_void_p(lptr)
+    rc = _offload_lib().zero_offload_apply(
+        ctypes.c_void_p(gp), gc, ctypes.c_void_p(arrs[0]), ctypes.c_void_p(arrs[1]),
+        ctypes.c_void_p(arrs[2]), lp, lc, n, ctypes.byref(scalars),
+        n_threads or default_host_threads())
+    _check(rc, "zero_offload_apply")
+
+
+def zero_offload_copy(dst, src, n_threads: int = 0) -> None:
+    """Multi-threaded host memcpy between equally sized host buffers."""
+    dp, dn, _ = _host_array(dst, "dst", code=-1)
+    sp, sn, _ = _host_array(src, "src", code=-1)
+    nbytes = (dst.nbytes if isinstance(dst, np.ndarray) else dst.numel() * dst.element_size())
+    sbytes = (src.nbytes if isinstance(src, np.ndarray) else src.numel() * src.element_size())
+    if nbytes != sbytes:
+        raise ValueError("buffer sizes differ")
+    _check(_offload_lib().zero_offload_copy(ctypes.c_void_p(dp), ctypes.c_void_p(sp), nbytes,
+                                             n_threads or default_host_threads()),
+           "zero_offload_copy")

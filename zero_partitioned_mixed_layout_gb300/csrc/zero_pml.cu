@@ -538,36 +538,56 @@ __device__ __forceinline__ void unpack8(const float4 &a, const float4 &b, float 
     f[4] = b.x; f[5] = b.y; f[6] = b.z; f[7] = b.w;
 }
 
+// 8 binary32 values at p: one 32-byte access (V32, p on a 32-byte boundary)
+// or two 16-byte accesses, with streaming (evict-first) hints.  Over HBM the
+// two are equally fast; over the host link (state in pinned host memory) the
+// 32-byte form moves 2.4x more data per second.
+template <bool V32>
+__device__ __forceinline__ void ld8f(const float *p, float *f)
+{
+    if (V32) {
+        asm("ld.global.cs.v8.f32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+            : "=f"(f[0]), "=f"(f[1]), "=f"(f[2]), "=f"(f[3]), "=f"(f[4]), "=f"(f[5]), "=f"(f[6]), "=f"(f[7])
+            : "l"(p));
+    } else {
+        unpack8(__ldcs(reinterpret_cast<const float4 *>(p)), __ldcs(reinterpret_cast<const float4 *>(p) + 1), f);
+    }
+}
+
+template <bool V32>
+__device__ __forceinline__ void st8f(float *p, const float *f)
+{
+    if (V32) {
+        asm volatile("st.global.cs.v8.f32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"l"(p), "f"(f[0]), "f"(f[1]),
+                     "f"(f[2]), "f"(f[3]), "f"(f[4]), "f"(f[5]), "f"(f[6]), "f"(f[7])
+                     : "memory");
+    } else {
+        __stcs(reinterpret_cast<float4 *>(p), make_float4(f[0], f[1], f[2], f[3]));
+        __stcs(reinterpret_cast<float4 *>(p) + 1, make_float4(f[4], f[5], f[6], f[7]));
+    }
+}
+
 // Vector i (elements 8i .. 8i+7) of one array set.
-template <int GT, int PT>
+template <int GT, int PT, bool V32>
 __device__ __forceinline__ void adam_vec(const void *g, float *p, float *m, float *v, void *plp, int64_t i,
                                          const StepScalars &s)
 {
-    constexpr int W = Elem<GT>::kWords;
-    uint4 gw[W];
-#pragma unroll
-    for (int q = 0; q < W; ++q)
-        gw[q] = __ldcs(static_cast<const uint4 *>(g) + i * W + q);
-    float4 *p4 = reinterpret_cast<float4 *>(p) + 2 * i;
-    float4 *m4 = reinterpret_cast<float4 *>(m) + 2 * i;
-    float4 *v4 = reinterpret_cast<float4 *>(v) + 2 * i;
-    const float4 p0 = __ldcs(p4), p1 = __ldcs(p4 + 1);
-    const float4 m0 = __ldcs(m4), m1 = __ldcs(m4 + 1);
-    const float4 v0 = __ldcs(v4), v1 = __ldcs(v4 + 1);
     float gf[8], pf[8], mf[8], vf[8];
-    Elem<GT>::to_float(gw, gf);
-    unpack8(p0, p1, pf);
-    unpack8(m0, m1, mf);
-    unpack8(v0, v1, vf);
+    if (GT == ZERO_F32) {
+        ld8f<V32>(static_cast<const float *>(g) + 8 * i, gf);
+    } else {
+        const uint4 gw = __ldcs(static_cast<const uint4 *>(g) + i);
+        Elem<GT>::to_float(&gw, gf);
+    }
+    ld8f<V32>(p + 8 * i, pf);
+    ld8f<V32>(m + 8 * i, mf);
+    ld8f<V32>(v + 8 * i, vf);
 #pragma unroll
     for (int e = 0; e < 8; ++e)
         adam_elem(gf[e], pf[e], mf[e], vf[e], s);
-    __stcs(p4, make_float4(pf[0], pf[1], pf[2], pf[3]));
-    __stcs(p4 + 1, make_float4(pf[4], pf[5], pf[6], pf[7]));
-    __stcs(m4, make_float4(mf[0], mf[1], mf[2], mf[3]));
-    __stcs(m4 + 1, make_float4(mf[4], mf[5], mf[6], mf[7]));
-    __stcs(v4, make_float4(vf[0], vf[1], vf[2], vf[3]));
-    __stcs(v4 + 1, make_float4(vf[4], vf[5], vf[6], vf[7]));
+    st8f<V32>(p + 8 * i, pf);
+    st8f<V32>(m + 8 * i, mf);
+    st8f<V32>(v + 8 * i, vf);
     if (plp)
         __stcs(static_cast<uint4 *>(plp) + i, LowP<PT>::pack(pf));
 }
@@ -585,24 +605,12 @@ __device__ __forceinline__ void adam_scalar(const void *g, float *p, float *m, f
         LowP<PT>::store(plp, j, pj);
 }
 
-template <int GT, int PT>
-__device__ __forceinline__ void adam_range(const void *g, float *p, float *m, float *v, void *plp, int64_t n,
-                                           int64_t t, int64_t nt, const StepScalars &s)
-{
-    const int64_t nv = n >> 3;
-    for (int64_t i = t; i < nv; i += nt)
-        adam_vec<GT, PT>(g, p, m, v, plp, i, s);
-    const int64_t tail = n - (nv << 3);
-    if (t < tail)
-        adam_scalar<GT, PT>(g, p, m, v, plp, (nv << 3) + t, s);
-}
-
 // One thread per 8-element vector, no loop: the grid covers the whole
 // array once (ceil(n / 2048) blocks, taken from the end of the array), the
 // last n mod 8 elements going to the threads just past the last vector.  Measured on GB300 this one-shot
 // schedule streams the five arrays at about 7.0 TB/s where persistent
 // grid-stride grids of 1 to 16 blocks per SM reach 5.1 to 6.8 TB/s.
-template <int GT, int PT>
+template <int GT, int PT, bool V32>
 __global__ void __launch_bounds__(kThreads, 4)
     k_adam_flat(const void *__restrict__ g, float *__restrict__ p, float *__restrict__ m, float *__restrict__ v,
                 void *__restrict__ plp, int64_t n, const StepScalars *__restrict__ scp, PowCache *cache)
@@ -616,7 +624,7 @@ __global__ void __launch_bounds__(kThreads, 4)
     // gradient in L2
     const int64_t i = (int64_t)(gridDim.x - 1 - blockIdx.x) * kThreads + threadIdx.x;
     if (i < nv)
-        adam_vec<GT, PT>(g, p, m, v, plp, i, s);
+        adam_vec<GT, PT, V32>(g, p, m, v, plp, i, s);
     else if (i - nv < (n & 7))
         adam_scalar<GT, PT>(g, p, m, v, plp, (nv << 3) + (i - nv), s);
     if (blockIdx.x == 0 && threadIdx.x == 0)
@@ -625,7 +633,7 @@ __global__ void __launch_bounds__(kThreads, 4)
 
 // Pass 2 over a list: one block per tile of kTile elements of one tensor,
 // one vector per thread (the one-shot schedule of the flat kernel).
-template <int GT, int PT>
+template <int GT, int PT, bool V32>
 __global__ void __launch_bounds__(kThreads, 4)
     k_adam_list(const TensorEntry *__restrict__ ents, const Chunk *__restrict__ tiles,
                 const StepScalars *__restrict__ scp, PowCache *cache)
@@ -645,7 +653,7 @@ __global__ void __launch_bounds__(kThreads, 4)
     const int64_t nv = len >> 3;
     const int64_t t = threadIdx.x;
     if (t < nv)
-        adam_vec<GT, PT>(g, e.p + start, e.m + start, e.v + start, plp, t, s);
+        adam_vec<GT, PT, V32>(g, e.p + start, e.m + start, e.v + start, plp, t, s);
     // the tail of a tensor's last tile (up to 7 elements) goes to threads
     // 0..6, which may also hold a vector: nv + tail can exceed the block
     if (t < (len & 7))
@@ -811,11 +819,25 @@ bool device_ptr(const void *p)
     return a.type == cudaMemoryTypeDevice || a.type == cudaMemoryTypeManaged;
 }
 
+// True for memory the kernels may reach that lives in host memory: pinned
+// (cudaHostAlloc / cudaHostRegister) allocations, mapped into the device
+// address space.  On GB300 the kernels reach it over NVLink-C2C.
+bool pinned_host_ptr(const void *p)
+{
+    cudaPointerAttributes a;
+    if (cudaPointerGetAttributes(&a, p) != cudaSuccess) {
+        cudaGetLastError();
+        return false;
+    }
+    return a.type == cudaMemoryTypeHost && a.devicePointer == p;
+}
+
 // Checks one list; on success *total holds its element count.  The device
 // pointers of a one-array list (a flat shard) are checked to be device
-// memory; longer lists are checked on their first and last arrays only, to
-// keep the per-call host cost independent of the list length.
-int check_list(const zero_tlist_t *l, int64_t *total)
+// memory (or, with allow_host, pinned host memory); longer lists are checked
+// on their first and last arrays only, to keep the per-call host cost
+// independent of the list length.
+int check_list(const zero_tlist_t *l, int64_t *total, bool allow_host = false)
 {
     if (!l || l->n < 0 || (l->n > 0 && (!l->ptrs || !l->numel)))
         return ZERO_EINVAL;
@@ -834,7 +856,7 @@ int check_list(const zero_tlist_t *l, int64_t *total)
     for (int64_t i = 0; i < l->n; ++i) {
         if (i > 0 && i < l->n - 1)
             i = l->n - 1;
-        if (l->numel[i] > 0 && !device_ptr(l->ptrs[i]))
+        if (l->numel[i] > 0 && !device_ptr(l->ptrs[i]) && !(allow_host && pinned_host_ptr(l->ptrs[i])))
             return ZERO_EINVAL;
     }
     *total = t;
@@ -867,7 +889,7 @@ int check_ws(void *ws, size_t ws_bytes, int64_t n_tensors, int64_t total)
 // *n_chunks.
 int upload_table(const zero_tlist_t *g, const zero_tlist_t *p, const zero_tlist_t *m, const zero_tlist_t *v,
                  const zero_tlist_t *plp, void *ws, cudaStream_t stream, int64_t item, int64_t *n_chunks,
-                 TensorEntry **d_ents, Chunk **d_chunks)
+                 TensorEntry **d_ents, Chunk **d_chunks, bool *aligned32 = nullptr)
 {
     const int64_t n = g->n;
     int64_t chunks = 0;
@@ -886,6 +908,14 @@ int upload_table(const zero_tlist_t *g, const zero_tlist_t *p, const zero_tlist_
         e.v = v ? static_cast<float *>(v->ptrs[i]) : nullptr;
         e.plp = plp ? plp->ptrs[i] : nullptr;
         e.numel = g->numel[i];
+        if (aligned32 && e.numel > 0) {
+            uintptr_t bits = reinterpret_cast<uintptr_t>(e.p) | reinterpret_cast<uintptr_t>(e.m) |
+                             reinterpret_cast<uintptr_t>(e.v);
+            if (g->dtype == ZERO_F32)
+                bits |= reinterpret_cast<uintptr_t>(e.g);
+            if (bits & 31u)
+                *aligned32 = false;
+        }
         const int64_t k = (g->numel[i] + item - 1) / item;
         for (int64_t j = 0; j < k; ++j) {
             ch[c].tensor = (int32_t)i;
@@ -938,11 +968,12 @@ int launch_norm(const zero_tlist_t *grads, int64_t total, zero_state_t *st, int 
 }
 
 // Pass 2 (after the decision kernel, with PDL).  For a list the tile table
-// was uploaded before the decision kernel (see run_step).
-template <int GT, int PT>
-int launch_adam(const zero_tlist_t *g, const zero_tlist_t *p, const zero_tlist_t *m, const zero_tlist_t *v,
-                const zero_tlist_t *plp, const StepScalars *sc, void *ws, cudaStream_t stream,
-                const TensorEntry *ents, const Chunk *tiles, int64_t n_tiles)
+// was uploaded before the decision kernel (see run_step).  `aligned32`: every
+// fp32 array starts on a 32-byte boundary, so the 32-byte access form runs.
+template <int GT, int PT, bool V32>
+int launch_adam_v(const zero_tlist_t *g, const zero_tlist_t *p, const zero_tlist_t *m, const zero_tlist_t *v,
+                  const zero_tlist_t *plp, const StepScalars *sc, void *ws, cudaStream_t stream,
+                  const TensorEntry *ents, const Chunk *tiles, int64_t n_tiles)
 {
     PowCache *cache = reinterpret_cast<PowCache *>(static_cast<unsigned char *>(ws) + kWsPowCache);
     if (g->n == 1) {
@@ -952,7 +983,7 @@ int launch_adam(const zero_tlist_t *g, const zero_tlist_t *p, const zero_tlist_t
         // one thread per 8-element vector plus the n mod 8 tail threads
         const int64_t threads = (n >> 3) + (n & 7);
         const int64_t grid = (threads + kThreads - 1) / kThreads;
-        launch_k(k_adam_flat<GT, PT>, (int)grid, kThreads, stream, true, (const void *)g->ptrs[0],
+        launch_k(k_adam_flat<GT, PT, V32>, (int)grid, kThreads, stream, true, (const void *)g->ptrs[0],
                  static_cast<float *>(p->ptrs[0]), static_cast<float *>(m->ptrs[0]),
                  static_cast<float *>(v->ptrs[0]), plp ? plp->ptrs[0] : nullptr, n, sc, cache);
         return check_launch("zero_adam_step");
@@ -960,18 +991,29 @@ int launch_adam(const zero_tlist_t *g, const zero_tlist_t *p, const zero_tlist_t
     if (n_tiles == 0)
         return ZERO_OK;
     // one-shot: one block per tile
-    launch_k(k_adam_list<GT, PT>, (int)n_tiles, kThreads, stream, true, ents, tiles, sc, cache);
+    launch_k(k_adam_list<GT, PT, V32>, (int)n_tiles, kThreads, stream, true, ents, tiles, sc, cache);
     return check_launch("zero_adam_step");
+}
+
+template <int GT, int PT>
+int launch_adam(const zero_tlist_t *g, const zero_tlist_t *p, const zero_tlist_t *m, const zero_tlist_t *v,
+                const zero_tlist_t *plp, const StepScalars *sc, void *ws, cudaStream_t stream,
+                const TensorEntry *ents, const Chunk *tiles, int64_t n_tiles, bool aligned32)
+{
+    if (aligned32)
+        return launch_adam_v<GT, PT, true>(g, p, m, v, plp, sc, ws, stream, ents, tiles, n_tiles);
+    return launch_adam_v<GT, PT, false>(g, p, m, v, plp, sc, ws, stream, ents, tiles, n_tiles);
 }
 
 template <int GT>
 int launch_adam_lp(int32_t pdtype, const zero_tlist_t *g, const zero_tlist_t *p, const zero_tlist_t *m,
                    const zero_tlist_t *v, const zero_tlist_t *plp, const StepScalars *sc, void *ws,
-                   cudaStream_t stream, const TensorEntry *ents, const Chunk *tiles, int64_t n_tiles)
+                   cudaStream_t stream, const TensorEntry *ents, const Chunk *tiles, int64_t n_tiles,
+                   bool aligned32)
 {
     if (pdtype == ZERO_BF16)
-        return launch_adam<GT, ZERO_BF16>(g, p, m, v, plp, sc, ws, stream, ents, tiles, n_tiles);
-    return launch_adam<GT, ZERO_F16>(g, p, m, v, plp, sc, ws, stream, ents, tiles, n_tiles);
+        return launch_adam<GT, ZERO_BF16>(g, p, m, v, plp, sc, ws, stream, ents, tiles, n_tiles, aligned32);
+    return launch_adam<GT, ZERO_F16>(g, p, m, v, plp, sc, ws, stream, ents, tiles, n_tiles, aligned32);
 }
 
 // Checks the arguments of the decision + pass 2 part of a step.
@@ -993,9 +1035,11 @@ int check_step_args(const zero_tlist_t *grads, const zero_tlist_t *master, const
     int rc = check_list(grads, total);
     if (rc != ZERO_OK)
         return rc;
+    // the fp32 state may live in pinned host memory (streamed over the
+    // host link by pass 2: offload of the optimizer state)
     const zero_tlist_t *states[3] = {master, m, v};
     for (const zero_tlist_t *l : states) {
-        if ((rc = check_list(l, &t2)) != ZERO_OK)
+        if ((rc = check_list(l, &t2, true)) != ZERO_OK)
             return rc;
         if (l->dtype != ZERO_F32)
             return ZERO_EDTYPE;
@@ -1029,8 +1073,17 @@ int run_step(const zero_tlist_t *grads, const zero_tlist_t *master, const zero_t
     TensorEntry *ents = nullptr;
     Chunk *tiles = nullptr;
     int64_t n_tiles = 0;
+    bool aligned32 = true;
+    if (grads->n == 1) {
+        uintptr_t bits = reinterpret_cast<uintptr_t>(master->ptrs[0]) | reinterpret_cast<uintptr_t>(m->ptrs[0]) |
+                         reinterpret_cast<uintptr_t>(v->ptrs[0]);
+        if (grads->dtype == ZERO_F32)
+            bits |= reinterpret_cast<uintptr_t>(grads->ptrs[0]);
+        aligned32 = (bits & 31u) == 0;
+    }
     if (grads->n > 1) {
-        if ((rc = upload_table(grads, master, m, v, p_lp, ws, s, kTile, &n_tiles, &ents, &tiles)) != ZERO_OK)
+        if ((rc = upload_table(grads, master, m, v, p_lp, ws, s, kTile, &n_tiles, &ents, &tiles, &aligned32)) !=
+            ZERO_OK)
             return rc;
         if (n_tiles > 0x7fffffff)
             return ZERO_EINVAL;
@@ -1058,9 +1111,12 @@ int run_step(const zero_tlist_t *grads, const zero_tlist_t *master, const zero_t
         return ZERO_OK;
     const int32_t pd = p_lp ? p_lp->dtype : ZERO_F16;
     switch (grads->dtype) {
-    case ZERO_F16: return launch_adam_lp<ZERO_F16>(pd, grads, master, m, v, p_lp, sc, ws, s, ents, tiles, n_tiles);
-    case ZERO_BF16: return launch_adam_lp<ZERO_BF16>(pd, grads, master, m, v, p_lp, sc, ws, s, ents, tiles, n_tiles);
-    default: return launch_adam_lp<ZERO_F32>(pd, grads, master, m, v, p_lp, sc, ws, s, ents, tiles, n_tiles);
+    case ZERO_F16:
+        return launch_adam_lp<ZERO_F16>(pd, grads, master, m, v, p_lp, sc, ws, s, ents, tiles, n_tiles, aligned32);
+    case ZERO_BF16:
+        return launch_adam_lp<ZERO_BF16>(pd, grads, master, m, v, p_lp, sc, ws, s, ents, tiles, n_tiles, aligned32);
+    default:
+        return launch_adam_lp<ZERO_F32>(pd, grads, master, m, v, p_lp, sc, ws, s, ents, tiles, n_tiles, aligned32);
     }
 }
 
