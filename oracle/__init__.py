@@ -88,8 +88,9 @@ def load(path: str):
                                  ctypes.POINTER(_Step)]
     so.zo_adam_apply_sampled.argtypes = [vp, ctypes.c_int, vp, vp, vp, vp, vp,
                                          ctypes.c_int, i64, ctypes.POINTER(_Step)]
+    so.zo_reduce_mean.argtypes = [ctypes.POINTER(vp), i32, ctypes.c_int, i64, vp, ctypes.c_int]
     for f in ("zo_f32_to_lp", "zo_lp_to_f32", "zo_accumulate", "zo_norm_overflow",
-              "zo_decide", "zo_adam_apply", "zo_adam_apply_sampled"):
+              "zo_decide", "zo_adam_apply", "zo_adam_apply_sampled", "zo_reduce_mean"):
         getattr(so, f).restype = None
     return so
 
@@ -194,6 +195,19 @@ def accumulate(acc: np.ndarray, bufs: list[np.ndarray], dtype: str, overwrite: b
     assert acc.dtype == np.float32 and all(a.size == acc.size for a in arrs)
     ptrs = (ctypes.c_void_p * len(arrs))(*[_ptr(a) for a in arrs])
     lib().zo_accumulate(_ptr(acc), ptrs, len(arrs), DTYPES[dtype], acc.size, int(overwrite))
+
+
+def reduce_mean(bufs: list[np.ndarray], dtype: str, out_dtype: str) -> np.ndarray:
+    """ZeRO stage 2's gradient reduction on one shard: the mean over the Nd
+    replicas, binary32 sum in rank order, one division, rounded to out_dtype
+    (uint16 bit patterns for 16-bit outputs, float32 otherwise)."""
+    arrs = [np.ascontiguousarray(_bits(b, dtype)) for b in bufs]
+    n = arrs[0].size
+    assert all(a.size == n for a in arrs) and len(arrs) >= 1
+    out = np.empty(n, np.float32 if out_dtype == "f32" else np.uint16)
+    ptrs = (ctypes.c_void_p * len(arrs))(*[_ptr(a) for a in arrs])
+    lib().zo_reduce_mean(ptrs, len(arrs), DTYPES[dtype], n, _ptr(out), DTYPES[out_dtype])
+    return out
 
 
 def norm_overflow(grads: list[np.ndarray], dtype: str, loss_scale: float):

@@ -147,6 +147,31 @@ void zo_accumulate(float *acc, const void *const *bufs, int32_t n_bufs, int dtyp
     }
 }
 
+/* ---- ZeRO stage 2: the gradient reduction onto the owned shard ------ */
+
+/* [ZeRO card §方法适配] stage 2 partitions the gradients: each rank keeps
+ * only the reduced gradient of its own shard, which the data-parallel
+ * reduce-scatter delivers.  The arithmetic of that reduction, on one rank:
+ *     out[i] = round( (g_0[i] + g_1[i] + ... + g_{Nd-1}[i]) / Nd )
+ * Reading: binary32 sum in rank order starting from float(g_0[i]), one
+ * IEEE binary32 division by Nd (the data-parallel mean), rounded to nearest
+ * even into the output type (binary32 output is stored as is). */
+void zo_reduce_mean(const void *const *bufs, int32_t n_bufs, int dtype, int64_t n, void *out,
+                    int out_dtype)
+{
+    const float count = (float)n_bufs;
+    for (int64_t i = 0; i < n; ++i) {
+        float a = load_elem(bufs[0], dtype, i);
+        for (int32_t k = 1; k < n_bufs; ++k)
+            a = a + load_elem(bufs[k], dtype, i);
+        const float mean = a / count;
+        if (out_dtype == ZO_F32)
+            ((float *)out)[i] = mean;
+        else
+            store_lp(out, out_dtype, i, mean);
+    }
+}
+
 /* ---- pass 1: unscale, overflow, squared norm ------------------------- */
 
 /* Adds sum_i g_i^2 into *sumsq, g_i = float(g_lp_i) * inv_scale (a binary32

@@ -39,6 +39,11 @@ MUTANTS = [
      "for (int32_t j = n_bufs - 1; j >= k; --j)\n            a = a + load_elem(bufs[j], dtype, i);"),
     ("bf16 ties away", "u += 0x7FFFu + ((u >> 16) & 1u);", "u += 0x8000u;"),
     ("f16 truncation", "_Float16 h = (_Float16)x;", "_Float16 h = (_Float16)(x - x * 0x1p-12f);"),
+    ("mean by reciprocal", "const float mean = a / count;", "const float mean = a * (1.0f / count);"),
+    ("mean over one replica fewer", "const float count = (float)n_bufs;",
+     "const float count = (float)(n_bufs > 1 ? n_bufs - 1 : 1);"),
+    ("reduction reversed", "        float a = load_elem(bufs[0], dtype, i);\n        for (int32_t k = 1; k < n_bufs; ++k)\n            a = a + load_elem(bufs[k], dtype, i);",
+     "        float a = load_elem(bufs[n_bufs - 1], dtype, i);\n        for (int32_t k = n_bufs - 2; k >= 0; --k)\n            a = a + load_elem(bufs[k], dtype, i);"),
 ]
 
 PINS = [
@@ -58,6 +63,7 @@ PINS = [
     pins.test_skip_leaves_state_untouched_and_halves_scale,
     pins.test_scale_growth_after_window,
     pins.test_accumulate_order_and_exactness,
+    pins.test_reduce_mean_closed_forms,
 ]
 
 

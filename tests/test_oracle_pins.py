@@ -407,3 +407,37 @@ def test_memory_arithmetic_matches_pages():
     # under stage 2 fits a 32 GB V100 (derived, not printed)
     psi_mp = sum(stack) / d["model_parallel"]
     assert oracle.model_state_bytes(psi_mp, nd=dp, stage=2) < 32e9
+
+
+# ---------------------------------------------------------------- stage-2 reduction
+
+def test_reduce_mean_closed_forms():
+    from fractions import Fraction
+    rng = np.random.default_rng(12)
+    x = f16(rng.standard_normal(5000) * 3)
+    # equal replicas: the mean is the value itself, for any count
+    for k in (1, 2, 3, 7, 16):
+        out = oracle.reduce_mean([x] * k, "f16", "f16")
+        assert np.array_equal(out, x.view(np.uint16))
+    # power-of-two counts: sum exact (integers), division exact
+    ints = [rng.integers(-200, 200, 999).astype(np.float32) for _ in range(8)]
+    out = oracle.reduce_mean([zs.host_cast(a, "bf16") for a in ints], "bf16", "f32")
+    assert np.array_equal(out, sum(ints) / np.float32(8))
+    # three replicas: the correctly rounded binary32 quotient of the exact
+    # integer sum by 3 (a reciprocal multiply rounds some of these the other way)
+    sums = np.arange(1, 20001, dtype=np.int64)
+    a = [np.zeros(sums.size, np.float32), np.zeros(sums.size, np.float32), sums.astype(np.float32)]
+    out = oracle.reduce_mean(a, "f32", "f32")
+    exact = np.array([float(Fraction(int(t), 3)) for t in sums]).astype(np.float32)
+    assert np.array_equal(out, exact)
+    recip = (sums.astype(np.float32) * np.float32(1 / 3)).astype(np.float32)
+    assert not np.array_equal(out, recip)  # the pin distinguishes the two
+    # rank order fixes the rounding: 1 + 2^-24 + 2^-24 + 0 stays 1 (two ties)
+    r = [np.array([v], np.float32) for v in (1.0, 2.0 ** -24, 2.0 ** -24, 0.0)]
+    assert oracle.reduce_mean(r, "f32", "f32")[0] == np.float32(0.25)
+    assert oracle.reduce_mean(r[::-1], "f32", "f32")[0] == (np.float32(1.0) + np.float32(2.0 ** -23)) / 4
+    # an inf in any replica reaches the output
+    y = x.copy()
+    y[10] = np.inf
+    out = oracle.reduce_mean([x, y, x], "f16", "f16").view(np.float16)
+    assert np.isinf(out[10]) and np.isfinite(out[11])
