@@ -463,6 +463,89 @@ def run_ours(args):
         dist.destroy_process_group()
 
 
+def run_stage2(args):
+    """ZeRO stage 2 on one GPU for the GPT-2 1.5B Nd=16 rank-0 shard: the 16
+    ranks' fp16 gradient slices of the shard reduced to their mean with pass
+    1 fused (zero_reduce_grads, 32 + 2 B/param), then the decision and pass 2
+    (zero_adam_step, 28 B/param)."""
+    import torch
+
+    import zero_partitioned_mixed_layout_gb300 as zp
+    import zero_synth as zs
+    dev = torch.device("cuda", torch.cuda.current_device())
+    w = zs.WORKLOADS[WORKLOAD]
+    S = zp.zero_partition_layout(w["numel"](), w["nd"], w["align"]).shard_numel
+    nd = w["nd"]
+    scale = w["loss_scale"]
+    reps = []
+    for r in range(nd):
+        t = torch.empty(S, dtype=torch.float16, device=dev)
+        zs.device_grad_into(t, 2000 + r, 0, scale)
+        reps.append(t)
+    dg = torch.empty(S, dtype=torch.float16, device=dev)
+    dp = torch.empty(S, dtype=torch.float32, device=dev)
+    zs.device_master_into(dp, 2000)
+    dm, dv = torch.zeros(S, device=dev), torch.zeros(S, device=dev)
+    dlp = torch.empty(S, dtype=torch.float16, device=dev)
+    st, ws = zp.new_state(scale, dev), zp.new_workspace(1, S, dev)
+    hp = zp.HParams(**zs.HPARAMS)
+    stream = torch.cuda.current_stream(dev)
+
+    def step(ev=None):
+        if ev:
+            ev[0].record(stream)
+        zp.zero_reduce_grads(reps, dg, st, ws, stream=stream)
+        if ev:
+            ev[1].record(stream)
+        zp.zero_adam_step(dg, dp, dm, dv, dlp, hp, st, ws, stream=stream)
+        if ev:
+            ev[2].record(stream)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize(dev)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(dev.index) as clk:
+        e0.record(stream)
+        for _ in range(args.steps):
+            step()
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+        for k in range(args.steps):
+            step(evs[k])
+        torch.cuda.synchronize(dev)
+    dt = e0.elapsed_time(e1) / args.steps * 1e-3
+    red_ms = statistics.mean(a.elapsed_time(b) for a, b, _ in evs)
+    adam_ms = statistics.mean(b.elapsed_time(c) for _, b, c in evs)
+    assert zp.parse_state(st)["last_skipped"] == 0
+    peaks = measured_peaks()
+    peak = peaks["hbm_gbs"] if peaks else 6800.0
+    red_bytes = 2 * nd + 2
+    achieved = red_bytes * S / (red_ms * 1e-3) / 1e9
+    line = {
+        "metric": METRIC, "value": S / dt, "unit": UNIT, "n_gpus": 1, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": dt * 1e3, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": {"workload": "ZeRO stage 2 on one GPU, GPT-2 1.5B Nd=16 rank-0 shard: mean of "
+                               "the 16 ranks' fp16 gradient slices with pass 1 fused, then the "
+                               "decision and AdamW", "shard_params": S, "replicas": nd,
+                   "l2": "inputs larger than L2, no flush"},
+        "bytes_per_param": {"reduce": red_bytes, "adam_pass": 28, "whole_step": red_bytes + 28},
+        "passes_ms": {"reduce": red_ms, "adam_step": adam_ms, "whole_step": dt * 1e3},
+        "hbm_gbs_step": (red_bytes + 28) * S / dt / 1e9,
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                     "frac": achieved / peak, "traffic": None,
+                     "kernel": f"zero_reduce_grads (reduction + pass 1), {red_bytes} B/param",
+                     "peak_source": "MEASURED_PEAKS.json hbm_gbs (of measured)" if peaks
+                     else "fallback 6.8 TB/s (of fallback)"},
+        "adam_pass_gbs": 28 * S / (adam_ms * 1e-3) / 1e9,
+        "gpu_launches": 3 * args.steps,
+        "clocks": clk.summary(),
+    }
+    print(json.dumps(line), flush=True)
+
+
 def run_offload(args):
     """ZeRO-Offload on the GPT-2 1.5B Nd=16 shard: the fp32 master, momentum
     and variance (12 B/param) live in pinned host memory, the gradient and
@@ -606,7 +689,7 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--workload", default=WORKLOAD,
                     choices=["gpt2_1p5b_nd16", "tiny", "gpt2_1p5b_full", "stack_100b_nd400",
-                             "frag_10k", "flat", "offload"],
+                             "frag_10k", "flat", "offload", "stage2"],
                     help="default: the GPT-2 1.5B Nd=16 shard the metric is quoted on")
     ap.add_argument("--log2n", type=int, default=26, help="size of the flat workload (2^k)")
     ap.add_argument("--clock-preroll", type=float, default=1.0,
@@ -616,10 +699,10 @@ def main():
         ap.error("--warmup must be at least 3")
     if args.impl == "reference":
         run_reference(args)
-    elif args.workload == "offload":
+    elif args.workload in ("offload", "stage2"):
         from zero_partitioned_mixed_layout_gb300 import _build
         _build.build()
-        run_offload(args)
+        (run_offload if args.workload == "offload" else run_stage2)(args)
     else:
         import zero_partitioned_mixed_layout_gb300 as zp
         from zero_partitioned_mixed_layout_gb300 import _build

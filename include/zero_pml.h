@@ -179,6 +179,23 @@ int zero_accumulate_grads(float *acc, const void *const *g, int32_t n_bufs, int3
 int zero_grad_norm_overflow(const zero_tlist_t *grads, zero_state_t *d_state,
                             int32_t accumulate, void *ws, size_t ws_bytes, void *stream);
 
+/* ZeRO stage 2 on one rank ([ZeRO card §方法适配]: stage 2 partitions the
+ * gradients; each rank keeps only the reduced gradient of its shard, which
+ * the data-parallel reduce-scatter delivers): the reduction of the Nd
+ * replicas' slices of this rank's shard fused with pass 1.
+ *     out[i] = round( (replica_0[i] + ... + replica_{Nd-1}[i]) / Nd )
+ * summed in binary32 in rank order, one IEEE division, rounded to nearest
+ * even into out_dtype (F32 output stored as is); then pass 1 over the stored
+ * out, exactly as zero_grad_norm_overflow would compute it (loss scale from
+ * d_state; accumulate as there).  On one GPU this is the arithmetic of the
+ * reduce-scatter with the replicas in local memory.  replicas: HOST array of
+ * n_replicas (1..64) device pointers, n elements of `dtype` each; out: device,
+ * n elements of out_dtype.  ws as for zero_grad_norm_overflow (one array).
+ * Errors: ZERO_EINVAL, ZERO_EDTYPE, ZERO_EALIGN, ZERO_EWORKSPACE, ZERO_ECUDA. */
+int zero_reduce_grads(const void *const *replicas, int32_t n_replicas, int32_t dtype, int64_t n, void *out,
+                      int32_t out_dtype, zero_state_t *d_state, int32_t accumulate, void *ws, size_t ws_bytes,
+                      void *stream);
+
 /* Pass 1 without a workspace: the same computation and results as
  * zero_grad_norm_overflow, for callers that cannot allocate device memory
  * and so cannot provide the workspace -- code running where another

@@ -30,6 +30,7 @@ from .binding import (  # noqa: F401
     zero_grad_norm_overflow,
     zero_partition_layout,
     zero_state_init,
+    zero_reduce_grads,
     zero_step,
     zero_strerror,
     zero_workspace_bytes,

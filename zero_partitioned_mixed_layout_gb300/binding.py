@@ -86,8 +86,10 @@ def lib():
         so.zero_adam_step.argtypes = [ctypes.POINTER(_TList)] * 5 + [
             ctypes.POINTER(_HParams), vp, vp, ctypes.c_size_t, vp]
         so.zero_step.argtypes = so.zero_adam_step.argtypes
+        so.zero_reduce_grads.argtypes = [ctypes.POINTER(vp), i32, i32, i64, vp, i32, vp, i32, vp,
+                                         ctypes.c_size_t, vp]
         for f in ("zero_partition_layout", "zero_state_init", "zero_accumulate_grads",
-                  "zero_grad_norm_overflow", "zero_adam_step", "zero_step"):
+                  "zero_grad_norm_overflow", "zero_adam_step", "zero_step", "zero_reduce_grads"):
             getattr(so, f).restype = ctypes.c_int
         _lib = so
     return _lib
@@ -266,6 +268,31 @@ def zero_accumulate_grads(acc, grads, overwrite: bool, stream=None) -> None:
                                      codes.pop(), acc.numel(), int(bool(overwrite)),
                                      _stream_ptr(stream, acc.device))
     _check(rc, "zero_accumulate_grads")
+
+
+def zero_reduce_grads(replicas, out, state, ws, accumulate: bool = False, stream=None) -> None:
+    """ZeRO stage 2 on one rank: out = mean of the replicas' slices (rank
+    order, one division, rounded to out's type), with pass 1 over out."""
+    replicas = list(replicas)
+    if not 1 <= len(replicas) <= 64:
+        raise ValueError("1 to 64 replicas")
+    for r in replicas:
+        _device_tensor(r, "replica")
+        if r.numel() != out.numel():
+            raise ValueError("replica and output sizes differ")
+    _device_tensor(out, "out")
+    _device_tensor(state, "state")
+    _device_tensor(ws, "workspace")
+    codes = {_dtype_code(r) for r in replicas}
+    if len(codes) != 1:
+        raise TypeError("replicas must share one element type")
+    ptrs = (ctypes.c_void_p * len(replicas))(*[r.data_ptr() for r in replicas])
+    rc = lib().zero_reduce_grads(ptrs, len(replicas), codes.pop(), out.numel(),
+                                 ctypes.c_void_p(out.data_ptr()), _dtype_code(out),
+                                 ctypes.c_void_p(state.data_ptr()), int(bool(accumulate)),
+                                 ctypes.c_void_p(ws.data_ptr()), ws.numel(),
+                                 _stream_ptr(stream, state.device))
+    _check(rc, "zero_reduce_grads")
 
 
 def zero_grad_norm_overflow(grads, state, ws, accumulate: bool = False, stream=None) -> None:

@@ -392,6 +392,132 @@ __global__ void __launch_bounds__(kThreads)
     norm_finish(tot, bad, partials, hdr, st, accumulate);
 }
 
+// ------------------------------------------------------------- stage-2 reduction
+
+// ZeRO stage 2 partitions the gradients: a rank keeps only the reduced
+// gradient of its own shard ("ZeRO: Memory Optimizations Toward Training
+// Trillion Parameter Models - 中文验证版", section 方法适配).  This kernel is the
+// arithmetic of that reduction on one GPU -- the mean over the Nd replicas'
+// slices of the shard, summed in rank order in binary32 and divided once --
+// fused with pass 1 over the stored result.
+
+constexpr int kMaxReplicas = 64;
+
+struct ReplicaPtrs {
+    const void *p[kMaxReplicas];
+};
+
+// Elements 8i .. 8i+7: the rank-ordered binary32 sum over the replicas,
+// loading up to 8 replicas' vectors at a time.
+template <int GT>
+__device__ __forceinline__ void replica_sum(const ReplicaPtrs &r, int nr, int64_t i, float *a)
+{
+    constexpr int W = Elem<GT>::kWords;
+    {
+        uint4 w0[W];
+#pragma unroll
+        for (int q = 0; q < W; ++q)
+            w0[q] = __ldcs(static_cast<const uint4 *>(r.p[0]) + i * W + q);
+        Elem<GT>::to_float(w0, a);
+    }
+    for (int k0 = 1; k0 < nr; k0 += 8) {
+        uint4 w[8][W];
+#pragma unroll
+        for (int j = 0; j < 8; ++j)
+            if (k0 + j < nr) {
+#pragma unroll
+                for (int q = 0; q < W; ++q)
+                    w[j][q] = __ldcs(static_cast<const uint4 *>(r.p[k0 + j]) + i * W + q);
+            }
+#pragma unroll
+        for (int j = 0; j < 8; ++j)
+            if (k0 + j < nr) {
+                float f[8];
+                Elem<GT>::to_float(w[j], f);
+#pragma unroll
+                for (int e = 0; e < 8; ++e)
+                    a[e] = __fadd_rn(a[e], f[e]);
+            }
+    }
+}
+
+// Stores 8 means as the output type; returns the stored values as binary32
+// and their overflow bits.
+template <int OT>
+__device__ __forceinline__ uint32_t store_mean(void *out, int64_t i, const float *mean, float *stored)
+{
+    if constexpr (OT == ZERO_F32) {
+        float4 *o = static_cast<float4 *>(out) + 2 * i;
+        __stcs(o, make_float4(mean[0], mean[1], mean[2], mean[3]));
+        __stcs(o + 1, make_float4(mean[4], mean[5], mean[6], mean[7]));
+        uint4 w[2];
+        w[0] = make_uint4(__float_as_uint(mean[0]), __float_as_uint(mean[1]), __float_as_uint(mean[2]),
+                          __float_as_uint(mean[3]));
+        w[1] = make_uint4(__float_as_uint(mean[4]), __float_as_uint(mean[5]), __float_as_uint(mean[6]),
+                          __float_as_uint(mean[7]));
+#pragma unroll
+        for (int e = 0; e < 8; ++e)
+            stored[e] = mean[e];
+        return Elem<ZERO_F32>::nonfinite(w);
+    } else {
+        const uint4 packed = LowP<OT>::pack(mean);
+        __stcs(static_cast<uint4 *>(out) + i, packed);
+        Elem<OT>::to_float(&packed, stored);
+        return Elem<OT>::nonfinite(&packed);
+    }
+}
+
+template <int OT>
+__device__ __forceinline__ float store_mean_scalar(void *out, int64_t j, float mean, uint32_t &bad)
+{
+    if constexpr (OT == ZERO_F32) {
+        static_cast<float *>(out)[j] = mean;
+        bad |= (__float_as_uint(mean) & 0x7F800000u) == 0x7F800000u;
+        return mean;
+    } else {
+        LowP<OT>::store(out, j, mean);
+        bad |= Elem<OT>::scalar_nonfinite(out, j);
+        return Elem<OT>::scalar(out, j);
+    }
+}
+
+template <int GT, int OT>
+__global__ void __launch_bounds__(kThreads)
+    k_reduce_norm(ReplicaPtrs r, int nr, void *__restrict__ out, int64_t n, double2 *partials, WsHeader *hdr,
+                  zero_state_t *st, int accumulate)
+{
+    pdl_wait();
+    const float count = (float)nr;
+    double tot = 0.0;
+    uint32_t bad = 0;
+    const int64_t nv = n >> 3;
+    const int64_t nt = (int64_t)gridDim.x * kThreads;
+    const int64_t t0 = (int64_t)blockIdx.x * kThreads + threadIdx.x;
+    for (int64_t i = t0; i < nv; i += nt) {
+        float a[8], mean[8], stored[8];
+        replica_sum<GT>(r, nr, i, a);
+#pragma unroll
+        for (int e = 0; e < 8; ++e)
+            mean[e] = __fdiv_rn(a[e], count);
+        bad |= store_mean<OT>(out, i, mean, stored);
+        float sq[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e)
+            sq[e] = __fmul_rn(stored[e], stored[e]);
+        tot += (double)tree8(sq);
+    }
+    const int64_t tail = n - (nv << 3);
+    if (t0 < tail) {
+        const int64_t j = (nv << 3) + t0;
+        float a = Elem<GT>::scalar(r.p[0], j);
+        for (int k = 1; k < nr; ++k)
+            a = __fadd_rn(a, Elem<GT>::scalar(r.p[k], j));
+        const float x = store_mean_scalar<OT>(out, j, __fdiv_rn(a, count), bad);
+        tot += (double)__fmul_rn(x, x);
+    }
+    norm_finish(tot, bad != 0, partials, hdr, st, accumulate);
+}
+
 // ------------------------------------------------------------- decision
 
 struct DecideArgs {
@@ -1171,6 +1297,76 @@ extern "C" int zero_accumulate_grads(float *acc, const void *const *g, int32_t n
     }
     }
     return check_launch("zero_accumulate_grads");
+}
+
+namespace zpml {
+namespace {
+template <int GT, int OT>
+int launch_reduce(const ReplicaPtrs &r, int nr, void *out, int64_t n, zero_state_t *st, int accumulate, void *ws,
+                  cudaStream_t stream)
+{
+    unsigned char *w = static_cast<unsigned char *>(ws);
+    WsHeader *hdr = reinterpret_cast<WsHeader *>(w);
+    double2 *partials = reinterpret_cast<double2 *>(w + kWsPartials);
+    const int64_t items = ((n >> 3) + kThreads - 1) / kThreads;
+    const int grid = grid_for((const void *)k_reduce_norm<GT, OT>, items, kMaxBlocks, 4);
+    launch_k(k_reduce_norm<GT, OT>, grid, kThreads, stream, false, r, nr, out, n, partials, hdr, st, accumulate);
+    return check_launch("zero_reduce_grads");
+}
+
+template <int GT>
+int launch_reduce_ot(int32_t out_dtype, const ReplicaPtrs &r, int nr, void *out, int64_t n, zero_state_t *st,
+                     int accumulate, void *ws, cudaStream_t stream)
+{
+    switch (out_dtype) {
+    case ZERO_F16: return launch_reduce<GT, ZERO_F16>(r, nr, out, n, st, accumulate, ws, stream);
+    case ZERO_BF16: return launch_reduce<GT, ZERO_BF16>(r, nr, out, n, st, accumulate, ws, stream);
+    default: return launch_reduce<GT, ZERO_F32>(r, nr, out, n, st, accumulate, ws, stream);
+    }
+}
+}  // namespace
+}  // namespace zpml
+
+extern "C" int zero_reduce_grads(const void *const *replicas, int32_t n_replicas, int32_t dtype, int64_t n,
+                                 void *out, int32_t out_dtype, zero_state_t *d_state, int32_t accumulate,
+                                 void *ws, size_t ws_bytes, void *stream)
+{
+    if (!replicas || n_replicas < 1 || n_replicas > kMaxReplicas || n < 0 || !d_state ||
+        (accumulate != 0 && accumulate != 1))
+        return ZERO_EINVAL;
+    if (!grad_dtype_ok(dtype) || !grad_dtype_ok(out_dtype))
+        return ZERO_EDTYPE;
+    if ((reinterpret_cast<uintptr_t>(d_state) & 7u) != 0)
+        return ZERO_EALIGN;
+    if (!device_ptr(d_state))
+        return ZERO_EINVAL;
+    ReplicaPtrs r = {};
+    if (n > 0) {
+        if (!out)
+            return ZERO_EINVAL;
+        if (!aligned16(out))
+            return ZERO_EALIGN;
+        if (!device_ptr(out))
+            return ZERO_EINVAL;
+        for (int k = 0; k < n_replicas; ++k) {
+            if (!replicas[k])
+                return ZERO_EINVAL;
+            if (!aligned16(replicas[k]))
+                return ZERO_EALIGN;
+            if (!device_ptr(replicas[k]))
+                return ZERO_EINVAL;
+            r.p[k] = replicas[k];
+        }
+    }
+    int rc = check_ws(ws, ws_bytes, 1, n);
+    if (rc != ZERO_OK)
+        return rc;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    switch (dtype) {
+    case ZERO_F16: return launch_reduce_ot<ZERO_F16>(out_dtype, r, n_replicas, out, n, d_state, accumulate, ws, s);
+    case ZERO_BF16: return launch_reduce_ot<ZERO_BF16>(out_dtype, r, n_replicas, out, n, d_state, accumulate, ws, s);
+    default: return launch_reduce_ot<ZERO_F32>(out_dtype, r, n_replicas, out, n, d_state, accumulate, ws, s);
+    }
 }
 
 extern "C" int zero_grad_norm_overflow(const zero_tlist_t *grads, zero_state_t *d_state, int32_t accumulate,
