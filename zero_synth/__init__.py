@@ -54,6 +54,13 @@ def gpt2_shapes(layers: int = 48, hidden: int = 1600, vocab: int = 50257, positi
     return shapes
 
 
+def gpt2_layer_first(layers: int = 48):
+    """Layer boundaries of ``gpt2_shapes`` as first-tensor indices: the two
+    embeddings, each block's 12 tensors, the final norm's two, then the
+    tensor count."""
+    return [0] + [2 + 12 * k for k in range(layers + 1)] + [2 + 12 * layers + 2]
+
+
 def layer_stack_shapes(layers: int = 125, hidden: int = 8192):
     shapes = []
     for _ in range(layers):
