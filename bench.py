@@ -547,6 +547,90 @@ def run_stage2(args):
     print(json.dumps(line), flush=True)
 
 
+def run_gather(args):
+    """ZeRO stage 3 on one GPU, the GPT-2 1.5B parameters in 16 fp16 shards
+    (S = 97,350,784): the parameter gather back into the 580 tensors
+    (zero_gather_params, one call, 2 + 2 B/param), the same gather layer by
+    layer into one reused layer buffer (the stage-3 schedule of
+    zero_gather_plan: 50 calls), and the inverse scatter (tensors -> shards)."""
+    import torch
+
+    import zero_partitioned_mixed_layout_gb300 as zp
+    import zero_synth as zs
+    dev = torch.device("cuda", torch.cuda.current_device())
+    numel = zs.WORKLOADS[WORKLOAD]["numel"]()
+    nd, align = 16, 128
+    lay = zp.zero_partition_layout(numel, nd, align)
+    S, total = lay.shard_numel, sum(numel)
+    offs = [int(o) for o in lay.tensor_offset]
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(zs.stream_seed(0, "misc"))
+    shards = [torch.randint(-32768, 32767, (S,), dtype=torch.int16, device=dev, generator=gen)
+              .view(torch.float16) for _ in range(nd)]
+    tens = zp.TensorList([torch.empty(n, dtype=torch.float16, device=dev) for n in numel])
+    lf = zs.gpt2_layer_first()
+    plan = zp.zero_gather_plan(numel, lf, nd, align)
+    layer_buf = torch.empty(plan.max_layer_numel, dtype=torch.float16, device=dev)
+    layers = [(layer_buf[:int(plan.layer_flat[L + 1] - plan.layer_flat[L])], int(plan.layer_flat[L]))
+              for L in range(len(lf) - 1)]
+    ws = torch.empty(zp.zero_gather_workspace_bytes(len(numel), nd), dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def full():
+        zp.zero_gather_params(shards, tens, offs, ws, stream=stream)
+
+    def per_layer():
+        for view, o in layers:
+            zp.zero_gather_params(shards, [view], [o], ws, stream=stream)
+
+    def scatter():
+        zp.zero_scatter_params(tens, offs, shards, ws, stream=stream)
+
+    def timed(fn):
+        for _ in range(args.warmup):
+            fn()
+        torch.cuda.synchronize(dev)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(args.steps):
+            fn()
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        return e0.elapsed_time(e1) / args.steps * 1e-3
+
+    with ClockSampler(dev.index) as clk:
+        dt = timed(full)
+        dt_layers = timed(per_layer)
+        dt_scatter = timed(scatter)
+    peaks = measured_peaks()
+    peak = peaks["hbm_gbs"] if peaks else 6800.0
+    achieved = 4 * total / dt / 1e9
+    line = {
+        "metric": "stage-3 parameter gather params/sec & achieved HBM GB/s (4 B/param), 1 GPU",
+        "value": total / dt, "unit": "params/s", "n_gpus": 1, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": dt * 1e3, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f16", "data": "synthetic",
+        "config": {"workload": "ZeRO stage 3 on one GPU: the GPT-2 1.5B parameters (580 tensors, "
+                               "1,557,611,200 fp16 elements) gathered from their 16 flat shards",
+                   "shards": nd, "shard_params": S, "tensors": len(numel),
+                   "l2": "inputs larger than L2 (3.1 GB), no flush"},
+        "per_layer": {"calls": len(layers), "ms_per_pass": dt_layers * 1e3,
+                      "params_per_s": total / dt_layers,
+                      "gbs": 4 * total / dt_layers / 1e9,
+                      "max_layer_params": int(plan.max_layer_numel)},
+        "scatter": {"ms_per_pass": dt_scatter * 1e3, "params_per_s": total / dt_scatter,
+                    "gbs": 4 * total / dt_scatter / 1e9},
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                     "frac": achieved / peak, "traffic": None,
+                     "kernel": "zero_gather_params (one launch over 580 tensors), 4 B/param",
+                     "peak_source": "MEASURED_PEAKS.json hbm_gbs (of measured)" if peaks
+                     else "fallback 6.8 TB/s (of fallback)"},
+        "gpu_launches": args.steps,
+        "clocks": clk.summary(),
+    }
+    print(json.dumps(line), flush=True)
+
+
 def run_offload(args):
     """ZeRO-Offload on the GPT-2 1.5B Nd=16 shard: the fp32 master, momentum
     and variance (12 B/param) live in pinned host memory, the gradient and
@@ -690,7 +774,7 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--workload", default=WORKLOAD,
                     choices=["gpt2_1p5b_nd16", "tiny", "gpt2_1p5b_full", "stack_100b_nd400",
-                             "frag_10k", "flat", "offload", "stage2"],
+                             "frag_10k", "flat", "offload", "stage2", "gather"],
                     help="default: the GPT-2 1.5B Nd=16 shard the metric is quoted on")
     ap.add_argument("--log2n", type=int, default=26, help="size of the flat workload (2^k)")
     ap.add_argument("--clock-preroll", type=float, default=1.0,
@@ -700,10 +784,10 @@ def main():
         ap.error("--warmup must be at least 3")
     if args.impl == "reference":
         run_reference(args)
-    elif args.workload in ("offload", "stage2"):
+    elif args.workload in ("offload", "stage2", "gather"):
         from zero_partitioned_mixed_layout_gb300 import _build
         _build.build()
-        (run_offload if args.workload == "offload" else run_stage2)(args)
+        {"offload": run_offload, "stage2": run_stage2, "gather": run_gather}[args.workload](args)
     else:
         import zero_partitioned_mixed_layout_gb300 as zp
         from zero_partitioned_mixed_layout_gb300 import _build

@@ -305,6 +305,77 @@ int zero_offload_apply(const void *grad, int32_t gdtype, float *master, float *m
  * against.  Errors: ZERO_EINVAL. */
 int zero_offload_copy(void *dst, const void *src, size_t bytes, int32_t n_threads);
 
+/* ------------------------------------------------------------------ stage 3: parameter gather */
+
+/* ZeRO stage 3 partitions the parameters as well ("ZeRO: Memory Optimizations
+ * Toward Training Trillion Parameter Models - 中文验证版", section 方法适配):
+ * a rank keeps only its shard of the flat parameter buffer and assembles a
+ * tensor -- or a whole layer, one at a time, as the ZeRO-Infinity page's
+ * memory-centric tiling does -- from the ranks' shards before using it.
+ * These calls are the data movement of that gather and of its inverse on one
+ * GPU, where the Nd shards are Nd device arrays; with several GPUs it is the
+ * all-gather of a collective library.
+ *
+ * The flat buffer is the concatenation of the Nd shards in rank order
+ * (nd * shard_numel elements, the layout of zero_partition_layout), and a
+ * tensor i covers its flat elements [tensor_offset[i], tensor_offset[i] +
+ * numel[i]).  Elements are copied bit for bit (no conversion); the element
+ * type is the list's (F16, BF16 or F32) and the shards hold the same type.
+ *
+ *   shards         HOST array of nd DEVICE pointers, shard r holding
+ *                  shard_numel elements; each 16-byte aligned.
+ *   tensors        the tensors (zero_tlist_t; device arrays, 16-byte
+ *                  aligned; any element counts).
+ *   tensor_offset  HOST array of tensors->n flat offsets.
+ *   ws             device workspace of at least
+ *                  zero_gather_workspace_bytes(tensors->n, nd) bytes,
+ *                  256-byte aligned; the call copies its tables there in
+ *                  stream order, so one workspace must not serve two calls
+ *                  that can run at the same time.
+ * Tensors must not overlap one another or a shard in memory.  Work is
+ * enqueued on `stream`; nothing is synchronised.
+ * Errors: ZERO_EINVAL (NULL or negative arguments, memory that is not device
+ * memory), ZERO_EALIGN, ZERO_EDTYPE, ZERO_ELAYOUT (a tensor's range outside
+ * [0, nd * shard_numel), or nd * shard_numel past 2^62; for the scatter also
+ * two tensors whose ranges overlap), ZERO_EWORKSPACE, ZERO_ECUDA. */
+size_t zero_gather_workspace_bytes(int64_t n_tensors, int32_t nd);
+
+/* Shards -> tensors (the all-gather). */
+int zero_gather_params(const void *const *shards, int32_t nd, int64_t shard_numel, const zero_tlist_t *tensors,
+                       const int64_t *tensor_offset, void *ws, size_t ws_bytes, void *stream);
+
+/* Tensors -> shards (partitioning a model's tensors into the flat shards).
+ * Flat elements outside every tensor's range (the tail padding) are not
+ * written. */
+int zero_scatter_params(const zero_tlist_t *tensors, const int64_t *tensor_offset, void *const *shards,
+                        int32_t nd, int64_t shard_numel, void *ws, size_t ws_bytes, void *stream);
+
+/* One rank's part of one layer's gather. */
+typedef struct zero_gather_piece {
+    int64_t layer;        /* layer index */
+    int64_t rank;         /* the rank that holds the piece */
+    int64_t shard_offset; /* its first element within that rank's shard */
+    int64_t length;       /* elements (> 0) */
+    int64_t layer_offset; /* where it lands, counted from the layer's first element */
+} zero_gather_piece_t;
+
+/* The per-layer gather schedule of stage 3 (host only).  A layer is a run of
+ * consecutive tensors: layer L holds tensors [layer_first[L],
+ * layer_first[L+1]) (layer_first: n_layers + 1 non-decreasing entries in
+ * [0, n_tensors]).  Its parameters are then one flat range, written to
+ * layer_flat[L] .. layer_flat[L+1] (layer_flat: n_layers + 1 entries, may be
+ * NULL), and each rank whose shard meets that range contributes exactly one
+ * contiguous piece; pieces are listed by layer, then rank.  The layout is
+ * zero_partition_layout's for (numel, n_tensors, nd, align).  *n_pieces
+ * always receives the count; past `cap` only the first cap are written and
+ * ZERO_ECAPACITY is returned.  *max_layer_numel (may be NULL) receives the
+ * largest layer, the size of the buffer one gathered layer needs.
+ * Errors: ZERO_EINVAL, ZERO_ELAYOUT (as zero_partition_layout, or a bad
+ * layer_first), ZERO_ECAPACITY. */
+int zero_gather_plan(const int64_t *numel, int64_t n_tensors, const int64_t *layer_first, int64_t n_layers,
+                     int32_t nd, int64_t align, int64_t *layer_flat, zero_gather_piece_t *pieces, int64_t cap,
+                     int64_t *n_pieces, int64_t *max_layer_numel);
+
 #ifdef __cplusplus
 }
 #endif

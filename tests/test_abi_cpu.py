@@ -128,3 +128,61 @@ def test_binding_refuses_host_tensors(zp):
     with pytest.raises(ValueError):
         zp.zero_grad_norm_overflow(t, torch.zeros(64, dtype=torch.uint8),
                                    torch.zeros(1024, dtype=torch.uint8))
+
+
+# ---------------------------------------------------------------- stage-3 gather plan (host only)
+
+def _plan_as_oracle(plan, n_layers):
+    out = [[] for _ in range(n_layers)]
+    for L, r, so, ln, lo in plan.pieces:
+        out[int(L)].append((int(r), int(so), int(ln), int(lo)))
+    return out
+
+
+@pytest.mark.parametrize("seed", range(12))
+def test_gather_plan_matches_oracle(zp, seed):
+    rng = np.random.default_rng(300 + seed)
+    k = int(rng.integers(0, 40))
+    numel = [int(x) for x in rng.integers(0, 3000, k)]
+    nd = int(rng.integers(1, 20))
+    align = int(2 ** rng.integers(0, 8))
+    cuts = sorted(int(x) for x in rng.integers(0, k + 1, int(rng.integers(0, 6))))
+    layer_first = [0] + cuts + [k]
+    ours = zp.zero_gather_plan(numel, layer_first, nd, align)
+    ref = oracle.gather_plan(numel, layer_first, nd, align)
+    assert _plan_as_oracle(ours, len(ref)) == [lg.pieces for lg in ref]
+    assert list(ours.layer_flat) == [lg.begin for lg in ref] + [ref[-1].end]
+    assert ours.max_layer_numel == max(lg.end - lg.begin for lg in ref)
+
+
+def test_gather_plan_gpt2_matches_oracle(zp):
+    numel = zs.WORKLOADS["gpt2_1p5b_nd16"]["numel"]()
+    lf = zs.gpt2_layer_first()
+    ours = zp.zero_gather_plan(numel, lf, 16, 128)
+    ref = oracle.gather_plan(numel, lf, 16, 128)
+    assert _plan_as_oracle(ours, len(ref)) == [lg.pieces for lg in ref]
+    assert ours.max_layer_numel == (50257 + 1024) * 1600
+
+
+def test_gather_plan_errors(zp):
+    lib = zp.binding._gather_lib()
+    i64 = ctypes.c_int64
+    numel = (i64 * 3)(5, 3, 7)
+    n = i64()
+    for lf in ([0, 2, 1, 3], [0, 4], [-1, 3]):
+        arr = (i64 * len(lf))(*lf)
+        assert lib.zero_gather_plan(numel, 3, arr, len(lf) - 1, 2, 2, None, None, 0, ctypes.byref(n),
+                                    None) == -8
+    arr = (i64 * 2)(0, 3)
+    assert lib.zero_gather_plan(numel, 3, arr, 1, 0, 2, None, None, 0, ctypes.byref(n), None) == -8
+    assert lib.zero_gather_plan(numel, 3, arr, 1, 2, 2, None, None, 0, None, None) == -1
+    # too small an output array: the count still comes back
+    assert lib.zero_gather_plan(numel, 3, arr, 1, 2, 2, None, None, 0, ctypes.byref(n), None) == -6
+    assert n.value == 2
+
+
+def test_gather_workspace_bytes(zp):
+    a = zp.zero_gather_workspace_bytes(580, 16)
+    assert a % 256 == 0 and a >= 580 * 32 + 16 * 8
+    assert zp.zero_gather_workspace_bytes(0, 1) >= 256
+    assert zp.zero_gather_workspace_bytes(10_000, 400) > zp.zero_gather_workspace_bytes(10_000, 1)

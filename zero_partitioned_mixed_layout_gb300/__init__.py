@@ -3,7 +3,10 @@
 The data-parallel hot path of ZeRO: the model states are flattened into one
 padded buffer and partitioned over Nd ranks, and one rank's shard is updated
 by hand-written CUDA kernels (gradient accumulation; unscale + overflow +
-global squared norm; clip + AdamW + cast to fp16/bf16).  The C ABI is in
+global squared norm; clip + AdamW + cast to fp16/bf16).  Around the step:
+the stage-2 gradient reduction fused with the norm pass, the stage-3
+parameter gather (shards back to tensors) with its per-layer plan, and the
+offload step on the host cores.  The C ABI is in
 ``include/zero_pml.h``; this package is its Python binding.
 """
 from .binding import (  # noqa: F401
@@ -34,4 +37,9 @@ from .binding import (  # noqa: F401
     zero_step,
     zero_strerror,
     zero_workspace_bytes,
+    GatherPlan,
+    zero_gather_params,
+    zero_gather_plan,
+    zero_gather_workspace_bytes,
+    zero_scatter_params,
 )

@@ -332,6 +332,116 @@ def _step_call(fn, grads, master, m, v, p_lp, hp, state, ws, stream):
     _check(rc, fn)
 
 
+# ------------------------------------------------------------------ stage 3: parameter gather
+
+class _Piece(ctypes.Structure):
+    _fields_ = [("layer", ctypes.c_int64), ("rank", ctypes.c_int64),
+                ("shard_offset", ctypes.c_int64), ("length", ctypes.c_int64),
+                ("layer_offset", ctypes.c_int64)]
+
+
+def _gather_lib():
+    so = lib()
+    if not getattr(so, "_gather_ready", False):
+        vp, i64, i32 = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int32
+        so.zero_gather_workspace_bytes.argtypes = [i64, i32]
+        so.zero_gather_workspace_bytes.restype = ctypes.c_size_t
+        so.zero_gather_params.argtypes = [ctypes.POINTER(vp), i32, i64, ctypes.POINTER(_TList),
+                                          ctypes.POINTER(i64), vp, ctypes.c_size_t, vp]
+        so.zero_scatter_params.argtypes = [ctypes.POINTER(_TList), ctypes.POINTER(i64),
+                                           ctypes.POINTER(vp), i32, i64, vp, ctypes.c_size_t, vp]
+        so.zero_gather_plan.argtypes = [ctypes.POINTER(i64), i64, ctypes.POINTER(i64), i64, i32, i64,
+                                        ctypes.POINTER(i64), ctypes.POINTER(_Piece), i64,
+                                        ctypes.POINTER(i64), ctypes.POINTER(i64)]
+        for f in ("zero_gather_params", "zero_scatter_params", "zero_gather_plan"):
+            getattr(so, f).restype = ctypes.c_int
+        so._gather_ready = True
+    return so
+
+
+def zero_gather_workspace_bytes(n_tensors: int, nd: int) -> int:
+    return int(_gather_lib().zero_gather_workspace_bytes(int(n_tensors), int(nd)))
+
+
+def _shard_args(shards):
+    shards = list(shards)
+    if not shards:
+        raise ValueError("at least one shard")
+    for t in shards:
+        _device_tensor(t, "shard")
+    if len({t.numel() for t in shards}) != 1:
+        raise ValueError("shards must hold the same number of elements")
+    ptrs = (ctypes.c_void_p * len(shards))(*[t.data_ptr() for t in shards])
+    return shards, ptrs
+
+
+def _offsets(offsets, n):
+    offs = [int(o) for o in offsets]
+    if len(offs) != n:
+        raise ValueError("one flat offset per tensor")
+    return (ctypes.c_int64 * max(n, 1))(*offs)
+
+
+def zero_gather_params(shards, tensors, tensor_offset, ws, stream=None) -> None:
+    """Shards (rank order) -> tensors: tensor i receives flat elements
+    [tensor_offset[i], tensor_offset[i] + numel) of the shards' concatenation."""
+    shards, ptrs = _shard_args(shards)
+    lt = _ListArgs(tensors, "tensors")
+    offs = _offsets(tensor_offset, lt.tl.n)
+    _device_tensor(ws, "workspace")
+    if lt.tl.n and _dtype_code(shards[0]) != lt.tl.dtype:
+        raise TypeError("shards and tensors must share one element type")
+    rc = _gather_lib().zero_gather_params(ptrs, len(shards), shards[0].numel(), ctypes.byref(lt.tl),
+                                          offs, ctypes.c_void_p(ws.data_ptr()), ws.numel(),
+                                          _stream_ptr(stream, ws.device))
+    _check(rc, "zero_gather_params")
+
+
+def zero_scatter_params(tensors, tensor_offset, shards, ws, stream=None) -> None:
+    """Tensors -> shards: the inverse of zero_gather_params (padding untouched)."""
+    shards, ptrs = _shard_args(shards)
+    lt = _ListArgs(tensors, "tensors")
+    offs = _offsets(tensor_offset, lt.tl.n)
+    _device_tensor(ws, "workspace")
+    if lt.tl.n and _dtype_code(shards[0]) != lt.tl.dtype:
+        raise TypeError("shards and tensors must share one element type")
+    rc = _gather_lib().zero_scatter_params(ctypes.byref(lt.tl), offs, ptrs, len(shards),
+                                           shards[0].numel(), ctypes.c_void_p(ws.data_ptr()),
+                                           ws.numel(), _stream_ptr(stream, ws.device))
+    _check(rc, "zero_scatter_params")
+
+
+@dataclass
+class GatherPlan:
+    layer_flat: np.ndarray   # int64 [n_layers + 1]: flat offset of each layer's first element, then the end
+    pieces: np.ndarray       # int64 [n_pieces, 5]: layer, rank, shard_offset, length, layer_offset
+    max_layer_numel: int
+
+
+def zero_gather_plan(numel: Sequence[int], layer_first: Sequence[int], nd: int,
+                     align: int = 128) -> GatherPlan:
+    """The per-layer gather schedule of stage 3 (host only)."""
+    n, nl = len(numel), len(layer_first) - 1
+    if nl < 0:
+        raise ValueError("layer_first needs at least one entry")
+    arr = (ctypes.c_int64 * max(n, 1))(*[int(x) for x in numel])
+    lf = (ctypes.c_int64 * max(nl + 1, 1))(*[int(x) for x in layer_first])
+    flat = (ctypes.c_int64 * max(nl + 1, 1))()
+    npc, big = ctypes.c_int64(), ctypes.c_int64()
+    so = _gather_lib()
+    rc = so.zero_gather_plan(arr, n, lf, nl, int(nd), int(align), flat, None, 0, ctypes.byref(npc),
+                             ctypes.byref(big))
+    if rc not in (ZERO_OK, -6):
+        _check(rc, "zero_gather_plan")
+    cap = npc.value
+    pieces = (_Piece * max(cap, 1))()
+    rc = so.zero_gather_plan(arr, n, lf, nl, int(nd), int(align), flat, pieces, cap, ctypes.byref(npc),
+                             ctypes.byref(big))
+    _check(rc, "zero_gather_plan")
+    pc = np.frombuffer(pieces, dtype=np.int64, count=5 * cap).reshape(cap, 5).copy()
+    return GatherPlan(np.frombuffer(flat, np.int64, count=nl + 1).copy(), pc, big.value)
+
+
 # ------------------------------------------------------------------ offload (host)
 
 class OffloadScalars(ctypes.Structure):

@@ -1,5 +1,6 @@
 // Host-only entry points of the C ABI: error strings, the flat partition
-// layout, the initial optimizer state and the workspace size.
+// layout, the stage-3 per-layer gather plan, the initial optimizer state and
+// the workspace sizes.
 //
 // Layout source: "ZeRO: Memory Optimizations Toward Training Trillion
 // Parameter Models - 中文验证版" (ai-papers.xuzou.cn), section 方法适配
@@ -8,6 +9,7 @@
 #include <cmath>
 #include <cstdio>
 #include <cstring>
+#include <vector>
 
 #include "zero_pml_internal.h"
 
@@ -125,4 +127,64 @@ extern "C" size_t zero_workspace_bytes(int64_t max_tensors, int64_t max_total_nu
         max_total_numel = 0;
     return zpml::kWsTable +
            zpml::table_bytes(max_tensors, zpml::max_items(max_tensors, max_total_numel));
+}
+
+// Stage-3 gather plan.  Same source, same section: stage 3 partitions the
+// parameters too, so each layer's parameters are gathered from the ranks'
+// shards before the layer runs.  A layer's tensors are consecutive in the
+// flat buffer, so the layer is one flat range and meets each rank's shard in
+// at most one contiguous piece.
+extern "C" int zero_gather_plan(const int64_t *numel, int64_t n_tensors, const int64_t *layer_first,
+                                int64_t n_layers, int32_t nd, int64_t align, int64_t *layer_flat,
+                                zero_gather_piece_t *pieces, int64_t cap, int64_t *n_pieces,
+                                int64_t *max_layer_numel)
+{
+    if (n_layers < 0 || (n_layers > 0 && !layer_first) || !n_pieces || cap < 0 || (cap > 0 && !pieces) ||
+        n_tensors < 0)
+        return ZERO_EINVAL;
+    for (int64_t L = 0; L <= n_layers && n_layers > 0; ++L) {
+        const int64_t a = layer_first[L];
+        if (a < 0 || a > n_tensors || (L > 0 && a < layer_first[L - 1]))
+            return ZERO_ELAYOUT;
+    }
+    std::vector<int64_t> offs((size_t)n_tensors + 1);
+    int64_t shard = 0, padded = 0, n_frags = 0;
+    const int rc = zero_partition_layout(numel, n_tensors, nd, align, &shard, &padded, offs.data(), nullptr, 0,
+                                         &n_frags);
+    if (rc != ZERO_OK && rc != ZERO_ECAPACITY)
+        return rc;
+    int64_t total = 0;
+    for (int64_t i = 0; i < n_tensors; ++i)
+        total += numel[i];
+    offs[(size_t)n_tensors] = total;
+
+    int64_t count = 0, biggest = 0;
+    for (int64_t L = 0; L < n_layers; ++L) {
+        const int64_t begin = offs[(size_t)layer_first[L]], end = offs[(size_t)layer_first[L + 1]];
+        if (layer_flat)
+            layer_flat[L] = begin;
+        if (end - begin > biggest)
+            biggest = end - begin;
+        if (begin == end)
+            continue;
+        for (int64_t r = begin / shard; r * shard < end; ++r) {
+            const int64_t lo = begin > r * shard ? begin : r * shard;
+            const int64_t hi = end < (r + 1) * shard ? end : (r + 1) * shard;
+            if (count < cap) {
+                zero_gather_piece_t &p = pieces[count];
+                p.layer = L;
+                p.rank = r;
+                p.shard_offset = lo - r * shard;
+                p.length = hi - lo;
+                p.layer_offset = lo - begin;
+            }
+            ++count;
+        }
+    }
+    if (layer_flat && n_layers > 0)
+        layer_flat[n_layers] = offs[(size_t)layer_first[n_layers]];
+    if (max_layer_numel)
+        *max_layer_numel = biggest;
+    *n_pieces = count;
+    return count > cap ? ZERO_ECAPACITY : ZERO_OK;
 }
