@@ -37,10 +37,10 @@ L2_BYTES = 129e6
 
 def kernel_source_hash() -> str:
     """sha256 (first 16 hex) of the files that define passes 1 and 2: the
-    kernel file and its internal header."""
+    kernel file and the headers it includes."""
     csrc = os.path.join(ROOT, "zero_partitioned_mixed_layout_gb300", "csrc")
     h = hashlib.sha256()
-    for f in ("zero_pml.cu", "zero_pml_internal.h"):
+    for f in ("zero_pml.cu", "common.cuh", "zero_pml_internal.h"):
         h.update(open(os.path.join(csrc, f), "rb").read())
     return h.hexdigest()[:16]
 

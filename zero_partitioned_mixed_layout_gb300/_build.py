@@ -36,7 +36,7 @@ def _cuda_home() -> str:
 
 def _sources():
     return sorted(os.path.join(CSRC, f) for f in os.listdir(CSRC)
-                  if f.endswith((".cu", ".cpp", ".h")))
+                  if f.endswith((".cu", ".cpp", ".h", ".cuh")))
 
 
 def _up_to_date() -> bool:
@@ -60,7 +60,7 @@ def build(force: bool = False, verbose: bool = False) -> str:
     jobs = []
     objs = []
     for src in _sources():
-        if src.endswith(".h"):
+        if src.endswith((".h", ".cuh")):
             continue
         obj = os.path.join(BUILD, os.path.basename(src) + ".o")
         objs.append(obj)

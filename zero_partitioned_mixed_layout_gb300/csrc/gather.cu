@@ -15,13 +15,11 @@
 // it crosses a shard boundary.  Each span is copied with 16-byte stores; when
 // source and destination differ in their offset modulo 16 bytes, each store
 // is assembled from two 16-byte source loads with funnel shifts.
-#include <cuda_runtime.h>
-
 #include <algorithm>
 #include <cstdint>
 #include <vector>
 
-#include "zero_pml_internal.h"
+#include "common.cuh"
 
 namespace zpml {
 namespace {
@@ -179,24 +177,6 @@ __global__ void __launch_bounds__(kThreads, 4) k_gather(const GatherEntry *__res
 
 // ------------------------------------------------------------- host side
 
-bool is_device_memory(const void *p)
-{
-    cudaPointerAttributes a;
-    if (cudaPointerGetAttributes(&a, p) != cudaSuccess) {
-        cudaGetLastError();
-        return false;
-    }
-    return a.type == cudaMemoryTypeDevice || a.type == cudaMemoryTypeManaged;
-}
-
-bool on16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
-
-int cuda_fail(const char *what, cudaError_t e)
-{
-    set_cuda_error(what, (int)e, cudaGetErrorString(e));
-    return ZERO_ECUDA;
-}
-
 size_t entries_bytes(int64_t n) { return align256((size_t)(n > 0 ? n : 1) * sizeof(GatherEntry)); }
 size_t shard_table_bytes(int32_t nd) { return align256((size_t)(nd > 0 ? nd : 1) * sizeof(char *)); }
 
@@ -215,7 +195,7 @@ int run_copy(bool gather, void *const *shards, int32_t nd, int64_t shard_numel, 
     for (int32_t r = 0; r < nd; ++r) {
         if (!shards[r])
             return ZERO_EINVAL;
-        if (!on16(shards[r]))
+        if (!aligned16(shards[r]))
             return ZERO_EALIGN;
     }
     // Entries in list order, empty tensors dropped.
@@ -231,7 +211,7 @@ int run_copy(bool gather, void *const *shards, int32_t nd, int64_t shard_numel, 
             continue;
         if (!tl->ptrs[i])
             return ZERO_EINVAL;
-        if (!on16(tl->ptrs[i]))
+        if (!aligned16(tl->ptrs[i]))
             return ZERO_EALIGN;
         if (o > flat_total || n > flat_total - o)
             return ZERO_ELAYOUT;
@@ -252,9 +232,9 @@ int run_copy(bool gather, void *const *shards, int32_t nd, int64_t shard_numel, 
         return ZERO_EALIGN;
     if (ws_bytes < zero_gather_workspace_bytes(tl->n, nd))
         return ZERO_EWORKSPACE;
-    if (!is_device_memory(ws) || !is_device_memory(shards[0]) || !is_device_memory(shards[nd - 1]))
+    if (!device_ptr(ws) || !device_ptr(shards[0]) || !device_ptr(shards[nd - 1]))
         return ZERO_EINVAL;
-    if (!ents.empty() && (!is_device_memory(ents.front().ptr) || !is_device_memory(ents.back().ptr)))
+    if (!ents.empty() && (!device_ptr(ents.front().ptr) || !device_ptr(ents.back().ptr)))
         return ZERO_EINVAL;
     if (ents.empty())
         return ZERO_OK;
@@ -270,7 +250,7 @@ int run_copy(bool gather, void *const *shards, int32_t nd, int64_t shard_numel, 
     unsigned char *base = static_cast<unsigned char *>(ws);
     cudaError_t e = cudaMemcpyAsync(base, host.data(), host.size(), cudaMemcpyHostToDevice, st);
     if (e != cudaSuccess)
-        return cuda_fail("gather table upload", e);
+        return check_launch("gather table upload");
     char *const *d_shards = reinterpret_cast<char *const *>(base);
     const GatherEntry *d_ents = reinterpret_cast<const GatherEntry *>(base + sb);
     const int64_t n_ents = (int64_t)ents.size(), shard_bytes = shard_numel * es;
@@ -283,8 +263,7 @@ int run_copy(bool gather, void *const *shards, int32_t nd, int64_t shard_numel, 
         k_gather<false, 2><<<grid, block, 0, st>>>(d_ents, n_ents, d_shards, shard_bytes);
     else
         k_gather<false, 4><<<grid, block, 0, st>>>(d_ents, n_ents, d_shards, shard_bytes);
-    e = cudaGetLastError();
-    return e == cudaSuccess ? ZERO_OK : cuda_fail(gather ? "k_gather (gather)" : "k_gather (scatter)", e);
+    return check_launch(gather ? "k_gather (gather)" : "k_gather (scatter)");
 }
 
 }  // namespace

@@ -31,254 +31,14 @@
 #include <unordered_map>
 #include <vector>
 
-#include "zero_pml_internal.h"
+#include "common.cuh"
 
 namespace zpml {
 namespace {
 
-constexpr int kWarps = kThreads / 32;
 // Bytes at the end of a flat gradient that pass 1 asks L2 to keep for pass 2
 // (GB300 has 126 MB of L2; pass 2's other streams are evict-first).
 constexpr int64_t kL2KeepBytes = 96ll << 20;
-
-// ------------------------------------------------------------- element types
-
-template <int DT>
-struct Elem;
-
-// binary16: 8 elements in one 16-byte word group
-template <>
-struct Elem<ZERO_F16> {
-    static constexpr int kWords = 1;
-    static constexpr int kBytes = 2;
-    __device__ static __forceinline__ void to_float(const uint4 *w, float *f)
-    {
-        const __half2 *h = reinterpret_cast<const __half2 *>(w);
-#pragma unroll
-        for (int k = 0; k < 4; ++k) {
-            const float2 x = __half22float2(h[k]);
-            f[2 * k] = x.x;
-            f[2 * k + 1] = x.y;
-        }
-    }
-    // A binary16 is inf or NaN iff its exponent field is all ones: adding
-    // 0x0400 to the masked field carries into bit 15 exactly then.
-    __device__ static __forceinline__ uint32_t nonfinite(const uint4 *w)
-    {
-        const uint32_t a = ((w->x & 0x7C007C00u) + 0x04000400u) | ((w->y & 0x7C007C00u) + 0x04000400u) |
-                           ((w->z & 0x7C007C00u) + 0x04000400u) | ((w->w & 0x7C007C00u) + 0x04000400u);
-        return a & 0x80008000u;
-    }
-    __device__ static __forceinline__ float scalar(const void *p, int64_t i)
-    {
-        return __half2float(static_cast<const __half *>(p)[i]);
-    }
-    __device__ static __forceinline__ uint32_t scalar_nonfinite(const void *p, int64_t i)
-    {
-        return (static_cast<const uint16_t *>(p)[i] & 0x7C00u) == 0x7C00u;
-    }
-};
-
-// bfloat16: exponent field 0x7F80
-template <>
-struct Elem<ZERO_BF16> {
-    static constexpr int kWords = 1;
-    static constexpr int kBytes = 2;
-    __device__ static __forceinline__ void to_float(const uint4 *w, float *f)
-    {
-        const __nv_bfloat162 *h = reinterpret_cast<const __nv_bfloat162 *>(w);
-#pragma unroll
-        for (int k = 0; k < 4; ++k) {
-            const float2 x = __bfloat1622float2(h[k]);
-            f[2 * k] = x.x;
-            f[2 * k + 1] = x.y;
-        }
-    }
-    __device__ static __forceinline__ uint32_t nonfinite(const uint4 *w)
-    {
-        const uint32_t a = ((w->x & 0x7F807F80u) + 0x00800080u) | ((w->y & 0x7F807F80u) + 0x00800080u) |
-                           ((w->z & 0x7F807F80u) + 0x00800080u) | ((w->w & 0x7F807F80u) + 0x00800080u);
-        return a & 0x80008000u;
-    }
-    __device__ static __forceinline__ float scalar(const void *p, int64_t i)
-    {
-        return __bfloat162float(static_cast<const __nv_bfloat16 *>(p)[i]);
-    }
-    __device__ static __forceinline__ uint32_t scalar_nonfinite(const void *p, int64_t i)
-    {
-        return (static_cast<const uint16_t *>(p)[i] & 0x7F80u) == 0x7F80u;
-    }
-};
-
-// binary32: 8 elements in two 16-byte words
-template <>
-struct Elem<ZERO_F32> {
-    static constexpr int kWords = 2;
-    static constexpr int kBytes = 4;
-    __device__ static __forceinline__ void to_float(const uint4 *w, float *f)
-    {
-        f[0] = __uint_as_float(w[0].x);
-        f[1] = __uint_as_float(w[0].y);
-        f[2] = __uint_as_float(w[0].z);
-        f[3] = __uint_as_float(w[0].w);
-        f[4] = __uint_as_float(w[1].x);
-        f[5] = __uint_as_float(w[1].y);
-        f[6] = __uint_as_float(w[1].z);
-        f[7] = __uint_as_float(w[1].w);
-    }
-    __device__ static __forceinline__ uint32_t nonfinite(const uint4 *w)
-    {
-        uint32_t a = 0;
-#pragma unroll
-        for (int q = 0; q < 2; ++q)
-            a |= ((w[q].x & 0x7F800000u) + 0x00800000u) | ((w[q].y & 0x7F800000u) + 0x00800000u) |
-                 ((w[q].z & 0x7F800000u) + 0x00800000u) | ((w[q].w & 0x7F800000u) + 0x00800000u);
-        return a & 0x80000000u;
-    }
-    __device__ static __forceinline__ float scalar(const void *p, int64_t i)
-    {
-        return static_cast<const float *>(p)[i];
-    }
-    __device__ static __forceinline__ uint32_t scalar_nonfinite(const void *p, int64_t i)
-    {
-        return (__float_as_uint(static_cast<const float *>(p)[i]) & 0x7F800000u) == 0x7F800000u;
-    }
-};
-
-// Low-precision parameter copy: binary32 -> 16-bit, round to nearest even.
-template <int PT>
-struct LowP;
-
-template <>
-struct LowP<ZERO_F16> {
-    __device__ static __forceinline__ uint4 pack(const float *f)
-    {
-        uint4 r;
-        __half2 h0 = __floats2half2_rn(f[0], f[1]), h1 = __floats2half2_rn(f[2], f[3]);
-        __half2 h2 = __floats2half2_rn(f[4], f[5]), h3 = __floats2half2_rn(f[6], f[7]);
-        r.x = *reinterpret_cast<uint32_t *>(&h0);
-        r.y = *reinterpret_cast<uint32_t *>(&h1);
-        r.z = *reinterpret_cast<uint32_t *>(&h2);
-        r.w = *reinterpret_cast<uint32_t *>(&h3);
-        return r;
-    }
-    __device__ static __forceinline__ void store(void *p, int64_t i, float x)
-    {
-        static_cast<__half *>(p)[i] = __float2half_rn(x);
-    }
-};
-
-template <>
-struct LowP<ZERO_BF16> {
-    __device__ static __forceinline__ uint4 pack(const float *f)
-    {
-        uint4 r;
-        __nv_bfloat162 h0 = __floats2bfloat162_rn(f[0], f[1]), h1 = __floats2bfloat162_rn(f[2], f[3]);
-        __nv_bfloat162 h2 = __floats2bfloat162_rn(f[4], f[5]), h3 = __floats2bfloat162_rn(f[6], f[7]);
-        r.x = *reinterpret_cast<uint32_t *>(&h0);
-        r.y = *reinterpret_cast<uint32_t *>(&h1);
-        r.z = *reinterpret_cast<uint32_t *>(&h2);
-        r.w = *reinterpret_cast<uint32_t *>(&h3);
-        return r;
-    }
-    __device__ static __forceinline__ void store(void *p, int64_t i, float x)
-    {
-        static_cast<__nv_bfloat16 *>(p)[i] = __float2bfloat16_rn(x);
-    }
-};
-
-// ------------------------------------------------------------- launch order
-
-// Programmatic dependent launch.  A kernel launched with the programmatic
-// stream-serialisation attribute may be scheduled while the kernel before it
-// in the stream is still running; pdl_wait() blocks until that kernel (and
-// so all earlier work in the stream) has completed and its writes are
-// visible, and must come before the first access to memory produced
-// earlier.  For a kernel launched without the attribute it returns at once.
-__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
-
-// Allows the next kernel in the stream to be scheduled now (it still waits
-// in pdl_wait() for this one to finish).  Used only by kernels whose
-// successor needs few SM slots while it waits.
-__device__ __forceinline__ void pdl_launch_next() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
-
-// ------------------------------------------------------------- reductions
-
-__device__ __forceinline__ double warp_sum(double x)
-{
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1)
-        x += __shfl_xor_sync(0xffffffffu, x, o);
-    return x;
-}
-
-// binary32 sum of 8 lanes in a fixed tree
-__device__ __forceinline__ float tree8(const float *a)
-{
-    return __fadd_rn(__fadd_rn(__fadd_rn(a[0], a[1]), __fadd_rn(a[2], a[3])),
-                     __fadd_rn(__fadd_rn(a[4], a[5]), __fadd_rn(a[6], a[7])));
-}
-
-// Block sum (fixed order) of a per-thread binary64 value and OR of a flag.
-// Result valid in thread 0.
-__device__ __forceinline__ void block_reduce(double &tot, uint32_t &bad)
-{
-    __shared__ double s_tot[kWarps];
-    __shared__ uint32_t s_bad[kWarps];
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    tot = warp_sum(tot);
-    const uint32_t b = __any_sync(0xffffffffu, bad != 0);
-    if (lane == 0) {
-        s_tot[warp] = tot;
-        s_bad[warp] = b;
-    }
-    __syncthreads();
-    if (warp == 0) {
-        double t = lane < kWarps ? s_tot[lane] : 0.0;
-        const uint32_t bb = __any_sync(0xffffffffu, lane < kWarps && s_bad[lane] != 0);
-        tot = warp_sum(t);
-        bad = bb;
-    }
-    __syncthreads();
-}
-
-// End of the norm pass in every block: publish this block's partial; the
-// block that takes the last ticket sums all partials in block order and
-// writes (or adds) the unscaled totals into the state.  No block waits on
-// another: the last block to arrive does the final sum.
-__device__ void norm_finish(double tot, uint32_t bad, double2 *partials, WsHeader *hdr,
-                            zero_state_t *st, int accumulate)
-{
-    __shared__ bool s_last;
-    block_reduce(tot, bad);
-    if (threadIdx.x == 0) {
-        partials[blockIdx.x] = make_double2(tot, bad ? 1.0 : 0.0);
-        __threadfence();
-        const unsigned int ticket = atomicAdd(&hdr->ticket, 1u);
-        s_last = (ticket == gridDim.x - 1);
-    }
-    __syncthreads();
-    if (!s_last)
-        return;
-    __threadfence();
-    double t = 0.0;
-    uint32_t b = 0;
-    for (int j = threadIdx.x; j < (int)gridDim.x; j += kThreads) {
-        const double2 q = __ldcg(partials + j);
-        t += q.x;
-        b |= (q.y != 0.0);
-    }
-    block_reduce(t, b);
-    if (threadIdx.x == 0) {
-        // the partials hold sums of squares of the stored (scaled) gradient;
-        // the loss scale is a power of two, so this rescaling is exact
-        const double inv = 1.0 / st->loss_scale;
-        const double sum = t * inv * inv;
-        st->sumsq = accumulate ? st->sumsq + sum : sum;
-        st->found_inf = (accumulate ? st->found_inf : 0.0) + (b ? 1.0 : 0.0);
-        hdr->ticket = 0u;
-    }
-}
 
 // ------------------------------------------------------------- pass 1
 
@@ -518,108 +278,6 @@ __global__ void __launch_bounds__(kThreads)
     norm_finish(tot, bad != 0, partials, hdr, st, accumulate);
 }
 
-// ------------------------------------------------------------- decision
-
-struct DecideArgs {
-    double lr, beta1, beta2, max_norm, min_scale;
-    int64_t scale_window;
-    // step scalars that do not depend on the device state, computed on the
-    // host the same way (binary64, rounded once to binary32)
-    float b1, omb1, b2, omb2, eps, lrwd;
-};
-
-// Skip or apply, loss-scale and step bookkeeping, and the step scalars
-// (binary64, each rounded once to binary32).  Binary64 is a slow pipe on
-// this GPU, so the three independent chains -- 1 - beta1^t and the step
-// size, 1 - beta2^t and its inverse square root, the norm and the clip
-// coefficient -- run in three threads; thread 0 then writes the results.
-__global__ void k_decide(zero_state_t *st, StepScalars *out, const PowCache *cache, DecideArgs a)
-{
-    __shared__ float s_val[3];
-    __shared__ double s_norm;
-    pdl_launch_next();
-    pdl_wait();
-    if (blockIdx.x != 0)
-        return;
-    const int tid = threadIdx.x;
-    zero_state_t s = *st;
-    const int64_t tn = s.step + 1;  // the step count if this step applies
-    const double t = (double)tn;
-    const PowCache c = *cache;
-    const bool hit = c.t == tn && c.beta1 == a.beta1 && c.beta2 == a.beta2;
-    if (tid == 0) {
-        if (hit && c.lr == a.lr) {
-            s_val[0] = c.step_size;
-        } else {
-            const double bc1 = hit ? c.bc1 : 1.0 - pow(a.beta1, t);
-            s_val[0] = (float)(a.lr / bc1);
-        }
-    } else if (tid == 1) {
-        if (hit) {
-            s_val[1] = c.isb2;
-        } else {
-            const double bc2 = 1.0 - pow(a.beta2, t);
-            s_val[1] = (float)(1.0 / sqrt(bc2));
-        }
-    } else if (tid == 2) {
-        const double norm = sqrt(s.sumsq);
-        double clip = 1.0;
-        if (a.max_norm > 0.0) {
-            const double c = a.max_norm / (norm + 1e-6);
-            if (c < 1.0)
-                clip = c;
-        }
-        s_norm = norm;
-        s_val[2] = (float)clip;
-    }
-    __syncthreads();
-    if (tid != 0)
-        return;
-    StepScalars o;
-    // S is a power of two: below 2^127 its binary32 reciprocal is exact and
-    // equals the binary64 reciprocal rounded to binary32
-    o.inv_scale = s.loss_scale <= 0x1p126 ? __frcp_rn((float)s.loss_scale) : (float)(1.0 / s.loss_scale);
-    o.clip = 1.0f;
-    o.b1 = o.omb1 = o.b2 = o.omb2 = o.eps = o.step_size = o.isb2 = o.lrwd = 0.0f;
-    o.pad = 0;
-    const double norm = s_norm;
-    if (s.found_inf != 0.0) {
-        o.skip = 1;
-        const double half = s.loss_scale * 0.5;
-        s.loss_scale = half < a.min_scale ? a.min_scale : half;
-        s.good_steps = 0;
-        s.skipped += 1;
-    } else {
-        o.skip = 0;
-        s.step += 1;
-        s.good_steps += 1;
-        if (s.good_steps >= a.scale_window) {
-            s.loss_scale *= 2.0;
-            s.good_steps = 0;
-        }
-        o.clip = s_val[2];
-        o.b1 = a.b1;
-        o.omb1 = a.omb1;
-        o.b2 = a.b2;
-        o.omb2 = a.omb2;
-        o.eps = a.eps;
-        o.step_size = s_val[0];
-        o.isb2 = s_val[1];
-        o.lrwd = a.lrwd;
-    }
-    o.lr = a.lr;
-    o.beta1 = a.beta1;
-    o.beta2 = a.beta2;
-    o.next_t = s.step + 1;
-    s.last_norm = norm;
-    s.last_clip = o.clip;
-    s.last_skipped = o.skip;
-    s.sumsq = 0.0;
-    s.found_inf = 0.0;
-    *st = s;
-    *out = o;
-}
-
 // The bias-correction terms for the next step (the same expressions as the
 // decision kernel's), written by one thread of pass 2 after its own
 // elements; the next decision kernel picks them up if its tags match.
@@ -840,174 +498,6 @@ __global__ void __launch_bounds__(kThreads)
                 a = __fadd_rn(a, Elem<GT>::scalar(b.p[k], j));
         acc[j] = a;
     }
-}
-
-// ------------------------------------------------------------- host helpers
-
-int sm_count()
-{
-    static std::mutex mu;
-    static std::unordered_map<int, int> cache;
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess)
-        return 0;
-    std::lock_guard<std::mutex> lock(mu);
-    auto it = cache.find(dev);
-    if (it != cache.end())
-        return it->second;
-    int v = 0;
-    if (cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
-        return 0;
-    cache[dev] = v;
-    return v;
-}
-
-// Resident blocks per SM of a kernel at kThreads threads (cached per device
-// and kernel).
-int blocks_per_sm(const void *kernel)
-{
-    static std::mutex mu;
-    static std::unordered_map<uint64_t, int> cache;
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess)
-        return 1;
-    const uint64_t key = reinterpret_cast<uint64_t>(kernel) ^ ((uint64_t)dev << 56);
-    std::lock_guard<std::mutex> lock(mu);
-    auto it = cache.find(key);
-    if (it != cache.end())
-        return it->second;
-    int b = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b, kernel, kThreads, 0) != cudaSuccess || b < 1)
-        b = 1;
-    cache[key] = b;
-    return b;
-}
-
-// A whole number of waves over the SMs (at most per_sm_cap blocks per SM), or
-// fewer blocks if there is less work.
-int grid_for(const void *kernel, int64_t work_items, int cap, int per_sm_cap = 1 << 30)
-{
-    const int bps = blocks_per_sm(kernel);
-    const int64_t full = (int64_t)sm_count() * (bps < per_sm_cap ? bps : per_sm_cap);
-    int64_t g = work_items < full ? work_items : full;
-    if (g > cap)
-        g = cap;
-    return g < 1 ? 1 : (int)g;
-}
-
-// Launches a kernel; with `pdl` set, with programmatic stream
-// serialisation, so that it can be scheduled while the previous kernel in
-// the stream finishes (the kernel itself waits in pdl_wait() before touching
-// memory).  The wait covers the previous KERNEL only: `pdl` is set only where
-// the previous operation in the stream is this library's own kernel of the
-// same call -- never after a copy, a memset or the caller's work.
-template <typename... KArgs, typename... Args>
-cudaError_t launch_k(void (*kernel)(KArgs...), int grid, int block, cudaStream_t stream, bool pdl, Args... args)
-{
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)grid);
-    cfg.blockDim = dim3((unsigned)block);
-    cfg.dynamicSmemBytes = 0;
-    cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = pdl ? 1 : 0;
-    return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
-}
-
-int check_launch(const char *what)
-{
-    const cudaError_t e = cudaGetLastError();
-    if (e != cudaSuccess) {
-        set_cuda_error(what, (int)e, cudaGetErrorString(e));
-        return ZERO_ECUDA;
-    }
-    return ZERO_OK;
-}
-
-bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
-
-bool grad_dtype_ok(int32_t d) { return d == ZERO_F16 || d == ZERO_BF16 || d == ZERO_F32; }
-bool lp_dtype_ok(int32_t d) { return d == ZERO_F16 || d == ZERO_BF16; }
-
-// True when the pointer is device memory the kernels may stream (device or
-// managed allocations).  Host memory is refused even where the GPU could
-// reach it: the kernels assume HBM.
-bool device_ptr(const void *p)
-{
-    cudaPointerAttributes a;
-    if (cudaPointerGetAttributes(&a, p) != cudaSuccess) {
-        cudaGetLastError();
-        return false;
-    }
-    return a.type == cudaMemoryTypeDevice || a.type == cudaMemoryTypeManaged;
-}
-
-// True for memory the kernels may reach that lives in host memory: pinned
-// (cudaHostAlloc / cudaHostRegister) allocations, mapped into the device
-// address space.  On GB300 the kernels reach it over NVLink-C2C.
-bool pinned_host_ptr(const void *p)
-{
-    cudaPointerAttributes a;
-    if (cudaPointerGetAttributes(&a, p) != cudaSuccess) {
-        cudaGetLastError();
-        return false;
-    }
-    return a.type == cudaMemoryTypeHost && a.devicePointer == p;
-}
-
-// Checks one list; on success *total holds its element count.  The device
-// pointers of a one-array list (a flat shard) are checked to be device
-// memory (or, with allow_host, pinned host memory); longer lists are checked
-// on their first and last arrays only, to keep the per-call host cost
-// independent of the list length.
-int check_list(const zero_tlist_t *l, int64_t *total, bool allow_host = false)
-{
-    if (!l || l->n < 0 || (l->n > 0 && (!l->ptrs || !l->numel)))
-        return ZERO_EINVAL;
-    int64_t t = 0;
-    for (int64_t i = 0; i < l->n; ++i) {
-        if (l->numel[i] < 0)
-            return ZERO_EINVAL;
-        if (l->numel[i] > 0) {
-            if (!l->ptrs[i])
-                return ZERO_EINVAL;
-            if (!aligned16(l->ptrs[i]))
-                return ZERO_EALIGN;
-        }
-        t += l->numel[i];
-    }
-    for (int64_t i = 0; i < l->n; ++i) {
-        if (i > 0 && i < l->n - 1)
-            i = l->n - 1;
-        if (l->numel[i] > 0 && !device_ptr(l->ptrs[i]) && !(allow_host && pinned_host_ptr(l->ptrs[i])))
-            return ZERO_EINVAL;
-    }
-    *total = t;
-    return ZERO_OK;
-}
-
-int check_same_shape(const zero_tlist_t *a, const zero_tlist_t *b)
-{
-    if (a->n != b->n)
-        return ZERO_ESIZE;
-    for (int64_t i = 0; i < a->n; ++i)
-        if (a->numel[i] != b->numel[i])
-            return ZERO_ESIZE;
-    return ZERO_OK;
-}
-
-int check_ws(void *ws, size_t ws_bytes, int64_t n_tensors, int64_t total)
-{
-    if (!ws || (reinterpret_cast<uintptr_t>(ws) & 255u) != 0)
-        return ws ? ZERO_EALIGN : ZERO_EWORKSPACE;
-    if (ws_bytes < zero_workspace_bytes(n_tensors, total))
-        return ZERO_EWORKSPACE;
-    if (!device_ptr(ws))
-        return ZERO_EINVAL;
-    return ZERO_OK;
 }
 
 // Builds the entry and chunk tables of a list call on the host and copies
