@@ -17,6 +17,9 @@ Parts:
     inverse layout (shards back to tensors) and its per-layer schedule.
   * ``model_state_bytes`` / ``comm_volume`` -- the pages' memory and
     communication arithmetic.
+  * ``onebit_*`` -- 1-bit Adam's compression stage (worker compression with
+    error feedback, the server's average and recompression, the update with
+    the frozen variance), element arithmetic in ``zero_oracle.c``.
 
 Sources: "ZeRO: Memory Optimizations Toward Training Trillion Parameter
 Models - 中文验证版" (ai-papers.xuzou.cn/zh/papers/zero_2019/), cited as
@@ -92,8 +95,16 @@ def load(path: str):
     so.zo_adam_apply_sampled.argtypes = [vp, ctypes.c_int, vp, vp, vp, vp, vp,
                                          ctypes.c_int, i64, ctypes.POINTER(_Step)]
     so.zo_reduce_mean.argtypes = [ctypes.POINTER(vp), i32, ctypes.c_int, i64, vp, ctypes.c_int]
+    f32 = ctypes.c_float
+    so.zo_onebit_worker.argtypes = [vp, ctypes.c_int, i64, ctypes.POINTER(_Step), vp, vp, vp,
+                                    ctypes.POINTER(f32), f32]
+    so.zo_onebit_server.argtypes = [ctypes.POINTER(vp), vp, i32, i64, vp, vp, ctypes.POINTER(f32),
+                                    f32, i32]
+    so.zo_onebit_update.argtypes = [vp, vp, i64, i64, vp, vp, vp, vp, ctypes.c_int,
+                                    ctypes.POINTER(_Step)]
     for f in ("zo_f32_to_lp", "zo_lp_to_f32", "zo_accumulate", "zo_norm_overflow",
-              "zo_decide", "zo_adam_apply", "zo_adam_apply_sampled", "zo_reduce_mean"):
+              "zo_decide", "zo_adam_apply", "zo_adam_apply_sampled", "zo_reduce_mean",
+              "zo_onebit_worker", "zo_onebit_server", "zo_onebit_update"):
         getattr(so, f).restype = None
     return so
 
@@ -286,6 +297,127 @@ def adam_step(grads: list[np.ndarray], gdtype: str, p: list[np.ndarray], m: list
     for i, g in enumerate(grads):
         adam_apply(g, gdtype, p[i], m[i], v[i], p_lp[i], pdtype, st)
     return st
+
+
+# ---------------------------------------------------------------- 1-bit Adam
+
+def frozen_variance(step: Step, hp: HParams, t_freeze: int) -> Step:
+    """1-bit Adam's compression stage: the step with the variance's bias
+    correction frozen at the last warm-up step T_w, 1/sqrt(1 - b2^T_w)
+    (binary64, rounded once), since the variance itself stays frozen."""
+    import math
+    st = _Step()
+    ctypes.memmove(ctypes.byref(st), ctypes.byref(step._c), ctypes.sizeof(_Step))
+    if not step.skip:
+        st.inv_sqrt_bc2 = float(np.float32(1.0 / math.sqrt(1.0 - hp.beta2 ** float(t_freeze))))
+    scal = dict(step.scalars)
+    scal["inv_sqrt_bc2"] = st.inv_sqrt_bc2
+    return Step(step.skip, step.norm, scal, st)
+
+
+def _words(n: int) -> int:
+    return (n + 31) // 32
+
+
+def onebit_worker(g: np.ndarray, gdtype: str, step: Step, m: np.ndarray, e: np.ndarray,
+                  scale: float | None = None):
+    """Worker side of 1-bit Adam's compressed all-reduce: local momentum
+    b1*m + (1-b1)*g, plus the worker error e, compressed to signs and one
+    scale; e (float32) is updated in place, m is read only.  Returns (bits
+    uint32[n/32], scale); unchanged inputs and (None, None) on a skipped
+    step.  ``scale`` forces the scale (see onebit_compress in the C file)."""
+    ga = np.ascontiguousarray(_bits(g, gdtype))
+    n = ga.size
+    assert m.dtype == np.float32 and e.dtype == np.float32 and m.size == n == e.size
+    bits = np.zeros(_words(n), np.uint32)
+    out = ctypes.c_float(0.0)
+    lib().zo_onebit_worker(_ptr(ga), DTYPES[gdtype], n, ctypes.byref(step._c), _ptr(m), _ptr(e),
+                           _ptr(bits), ctypes.byref(out), -1.0 if scale is None else float(scale))
+    return (None, None) if step.skip else (bits, out.value)
+
+
+def onebit_server(bits: list[np.ndarray], scales: list[float], f: np.ndarray,
+                  scale: float | None = None, skip: bool = False):
+    """Server side for one chunk of S elements: the Nd workers' signs on the
+    chunk (uint32[S/32] each, rank order) and scales, averaged, plus the
+    server error f (float32[S], updated in place), compressed again.
+    Returns (bits uint32[S/32], scale)."""
+    S = f.size
+    arrs = [np.ascontiguousarray(b, dtype=np.uint32) for b in bits]
+    assert all(a.size == _words(S) for a in arrs) and f.dtype == np.float32
+    sc = np.ascontiguousarray(scales, dtype=np.float32)
+    ptrs = (ctypes.c_void_p * len(arrs))(*[_ptr(a) for a in arrs])
+    out_bits = np.zeros(_words(S), np.uint32)
+    out = ctypes.c_float(0.0)
+    lib().zo_onebit_server(ptrs, _ptr(sc), len(arrs), S, _ptr(f), _ptr(out_bits), ctypes.byref(out),
+                           -1.0 if scale is None else float(scale), int(skip))
+    return (None, None) if skip else (out_bits, out.value)
+
+
+def onebit_update(bits: np.ndarray, scales: list[float], S: int, numel: int, p: np.ndarray,
+                  m: np.ndarray, v: np.ndarray, p_lp: np.ndarray | None, pdtype: str,
+                  step: Step) -> None:
+    """Every worker: the synchronised momentum (the servers' signs, chunk j
+    scaled by scales[j]) into m, and the update of p with the frozen
+    variance v, for the first ``numel`` elements; in place."""
+    b = np.ascontiguousarray(bits, dtype=np.uint32)
+    sc = np.ascontiguousarray(scales, dtype=np.float32)
+    assert b.size * 32 >= numel and sc.size * S >= numel
+    for a in (p, m, v):
+        assert a.dtype == np.float32 and a.size >= numel and a.flags["C_CONTIGUOUS"]
+    lp = None if p_lp is None else _bits(p_lp, pdtype)
+    lib().zo_onebit_update(_ptr(b), _ptr(sc), S, numel, _ptr(p), _ptr(m), _ptr(v), _ptr(lp),
+                           DTYPES[pdtype], ctypes.byref(step._c))
+
+
+@dataclass
+class OnebitResult:
+    step: Step
+    worker_bits: list = field(default_factory=list)
+    worker_scales: list = field(default_factory=list)
+    server_bits: list = field(default_factory=list)
+    server_scales: list = field(default_factory=list)
+
+
+def onebit_step(grads: list[np.ndarray], gdtype: str, S: int, numel: int, p: np.ndarray,
+                m: np.ndarray, v: np.ndarray, e_w: list[np.ndarray], e_s: list[np.ndarray],
+                p_lp: np.ndarray | None, pdtype: str, hp: HParams, sc: Scaler, t_freeze: int,
+                worker_scales: list | None = None, server_scales: list | None = None) -> OnebitResult:
+    """One compression-stage step of 1-bit Adam over all Nd = len(grads)
+    workers (every worker holds the same p, m, v; its own gradient and error
+    e_w[i]; rank j serves chunk j with error e_s[j]).  The overflow flag and
+    the squared norm are summed over the workers' gradients.  Optional
+    worker_scales / server_scales force the scales (another implementation's
+    rounding of the norms)."""
+    nd = len(grads)
+    assert p.size == nd * S
+    sumsq, bad = norm_overflow(grads, gdtype, sc.loss_scale)
+    st = frozen_variance(decide(hp, sc, sumsq, bad), hp, t_freeze)
+    res = OnebitResult(st)
+    if st.skip:
+        return res
+    for i in range(nd):
+        b, s_ = onebit_worker(grads[i], gdtype, st, m, e_w[i],
+                              None if worker_scales is None else worker_scales[i])
+        res.worker_bits.append(b)
+        res.worker_scales.append(s_)
+    w = S // 32
+    for j in range(nd):
+        b, s_ = onebit_server([res.worker_bits[i][j * w:(j + 1) * w] for i in range(nd)],
+                              res.worker_scales, e_s[j],
+                              None if server_scales is None else server_scales[j])
+        res.server_bits.append(b)
+        res.server_scales.append(s_)
+    onebit_update(np.concatenate(res.server_bits), res.server_scales, S, numel, p, m, v, p_lp,
+                  pdtype, st)
+    return res
+
+
+def onebit_comm_ratio(warmup_fraction: float, full_bits: int = 32) -> float:
+    """Communication of plain data-parallel Adam over 1-bit Adam's, per
+    element and step: the warm-up steps send full-precision values, the rest
+    one bit (the scales are negligible)."""
+    return full_bits / (warmup_fraction * full_bits + (1.0 - warmup_fraction))
 
 
 # ---------------------------------------------------------------- layout

@@ -317,3 +317,113 @@ void zo_adam_apply_sampled(const void *g, int gdtype, const int64_t *idx, float 
             store_lp(p_lp, pdtype, j, p[j]);
     }
 }
+
+/* ---- 1-bit Adam: the compression stage ------------------------------- */
+
+/* [DS news] names 1-bit Adam: Adam with up to 5x less communication and
+ * Adam's convergence, 3.5x faster where communication is the bottleneck.
+ * The pages give no algorithm.  The reading follows the outline of the
+ * published method (Tang et al. 2021, "1-bit Adam: Communication Efficient
+ * Large-Scale Training with Adam's Convergence Speed"):
+ *   - a warm-up of T_w steps of plain Adam (zo_adam_apply above);
+ *   - then the variance is frozen at its value after step T_w, and with it
+ *     its bias correction 1/sqrt(1 - b2^T_w); each worker i updates its
+ *     momentum locally from the last synchronised momentum m,
+ *         m_i = b1*m + (1-b1)*g_i        (g_i unscaled and clipped as above),
+ *     and the workers average their momenta through a compressed all-reduce
+ *     with error feedback at both ends:
+ *       worker i:  x = m_i + e_i;  c_i = C(x);  e_i <- x - c_i
+ *                  (chunk j of c_i's signs and its scale go to rank j);
+ *       rank j:    y = (sum over i of c_i on chunk j) / Nd + f_j;
+ *                  s_j = C(y);  f_j <- y - s_j  (s_j goes to every worker);
+ *       worker:    m = the concatenation of the s_j, the new synchronised
+ *                  momentum, and
+ *                  p <- p - (lr/(1-b1^t) * m / (sqrt(v) * isb2(T_w) + eps) + lr*wd*p).
+ * Choices the outline leaves open, made here: the 1-bit compressor is
+ * C(x) = scale * sign(x) with scale = ||x||_2 / sqrt(n) (the compressed
+ * vector keeps x's L2 norm) and sign(0) = sign(-0) = +1; the squared norm is
+ * summed in binary64 in index order and scale = sqrt(sum / n) is rounded
+ * once to binary32; the server's average is the binary32 sum of the Nd
+ * worker values in rank order followed by one division by Nd; the signs
+ * travel as bits, bit k of 32-bit word w holding element 32w + k, 1 for +.
+ * Binary32 with one rounding per operation, as everywhere in this file. */
+
+/* C applied in place: buf holds x on entry and the new error x - C(x) on
+ * return; the signs go to bits and the scale to *scale.  A scale_in >= 0
+ * replaces the computed scale (a test then follows another implementation's
+ * rounding of the norm). */
+static void onebit_compress(float *buf, int64_t n, uint32_t *bits, float *scale, float scale_in)
+{
+    double s = 0.0;
+    for (int64_t i = 0; i < n; ++i)
+        s += (double)buf[i] * (double)buf[i];
+    const float sc = scale_in >= 0.0f ? scale_in : (float)sqrt(s / (double)n);
+    for (int64_t w = 0; w < (n + 31) / 32; ++w)
+        bits[w] = 0u;
+    for (int64_t i = 0; i < n; ++i) {
+        const int plus = !(buf[i] < 0.0f);
+        if (plus)
+            bits[i / 32] |= 1u << (i % 32);
+        buf[i] = buf[i] - (plus ? sc : -sc);
+    }
+    *scale = sc;
+}
+
+/* Worker i: local momentum from the synchronised m, error feedback and
+ * compression.  e (the worker's error, n elements) is updated; m is read
+ * only.  A skipped step touches nothing. */
+void zo_onebit_worker(const void *g, int gdtype, int64_t n, const zo_step *s, const float *m,
+                      float *e, uint32_t *bits, float *scale, float scale_in)
+{
+    if (s->skip)
+        return;
+    for (int64_t i = 0; i < n; ++i) {
+        float gi = load_elem(g, gdtype, i) * s->inv_scale;
+        if (s->clip != 1.0f)
+            gi = gi * s->clip;
+        const float mi = s->beta1 * m[i] + s->one_minus_beta1 * gi;
+        e[i] = mi + e[i];
+    }
+    onebit_compress(e, n, bits, scale, scale_in);
+}
+
+/* Rank j as the server of its chunk of S elements: the Nd workers' signs
+ * on that chunk (bits[i]: S/32 words) with their scales, averaged, plus the
+ * server error f (S elements, updated), compressed again. */
+void zo_onebit_server(const uint32_t *const *bits, const float *scales, int32_t nd, int64_t S,
+                      float *f, uint32_t *out_bits, float *out_scale, float scale_in, int32_t skip)
+{
+    if (skip)
+        return;
+    const float count = (float)nd;
+    for (int64_t i = 0; i < S; ++i) {
+        float a = 0.0f;
+        for (int32_t k = 0; k < nd; ++k) {
+            const float c = ((bits[k][i / 32] >> (i % 32)) & 1u) ? scales[k] : -scales[k];
+            a = k == 0 ? c : a + c;
+        }
+        f[i] = a / count + f[i];
+    }
+    onebit_compress(f, S, out_bits, out_scale, scale_in);
+}
+
+/* Every worker: the synchronised momentum from the servers' signs (bits:
+ * Nd*S/32 words, chunk j from rank j) and scales, then the parameter update
+ * with the frozen variance, for the first `numel` elements (the rest of the
+ * padded buffer is not parameters). */
+void zo_onebit_update(const uint32_t *bits, const float *scales, int64_t S, int64_t numel, float *p,
+                      float *m, const float *v, void *p_lp, int pdtype, const zo_step *s)
+{
+    if (s->skip)
+        return;
+    for (int64_t i = 0; i < numel; ++i) {
+        const float sc = scales[i / S];
+        const float mi = ((bits[i / 32] >> (i % 32)) & 1u) ? sc : -sc;
+        const float denom = sqrtf(v[i]) * s->inv_sqrt_bc2 + s->eps;
+        const float u = mi / denom;
+        p[i] = p[i] - (s->step_size * u + s->lr_wd * p[i]);
+        m[i] = mi;
+        if (p_lp)
+            store_lp(p_lp, pdtype, i, p[i]);
+    }
+}
