@@ -688,6 +688,108 @@ def run_gather(args):
     print(json.dumps(line), flush=True)
 
 
+def run_onebit(args):
+    """1-bit Adam's compression stage on rank 0 of 16 for GPT-2 1.5B: every
+    worker holds the whole model (n = 16 x 97,350,784 padded elements); a
+    step is pass 1 on the local fp16 gradient, the worker compression (local
+    momentum + error feedback -> signs and a scale), the server compression
+    of chunk 0 from the 16 workers' signs (the other 15 are received
+    messages), and the update from the 16 servers' signs with the frozen
+    variance."""
+    import torch
+
+    import zero_partitioned_mixed_layout_gb300 as zp
+    import zero_synth as zs
+    dev = torch.device("cuda", torch.cuda.current_device())
+    numel_list = zs.WORKLOADS[WORKLOAD]["numel"]()
+    nd = 16
+    S = zp.zero_partition_layout(numel_list, nd, 128).shard_numel
+    numel, n = sum(numel_list), nd * S
+    g = torch.empty(n, dtype=torch.float16, device=dev)
+    zs.device_grad_into(g, 40, 0, 65536.0)
+    m = zs.device_normal(n, 1e-3, 41, "misc", 1)
+    v = zs.device_normal(n, 1e-3, 41, "misc", 2).square_()
+    p = zs.device_normal(n, 0.02, 41, "master")
+    plp = p.half()
+    e_w = torch.zeros(n, device=dev)
+    e_s = torch.zeros(S, device=dev)
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(zs.stream_seed(0, "misc", 42))
+    bits = torch.zeros(n // 32, dtype=torch.int32, device=dev)
+    others = [torch.randint(-2 ** 31, 2 ** 31 - 1, (S // 32,), dtype=torch.int32, device=dev, generator=gen)
+              for _ in range(nd - 1)]
+    wscale = torch.rand(nd, device=dev, generator=gen) * 1e-3 + 1e-4
+    sbits = torch.randint(-2 ** 31, 2 ** 31 - 1, (n // 32,), dtype=torch.int32, device=dev, generator=gen)
+    sscale = torch.rand(nd, device=dev, generator=gen) * 1e-3 + 1e-4
+    state = torch.frombuffer(bytearray(zp.zero_state_init(65536.0)), dtype=torch.uint8).to(dev)
+    state[24:32] = torch.tensor([1000], dtype=torch.int64).view(torch.uint8).to(dev)  # warm-up done
+    ws = zp.new_workspace(1, n, dev)
+    hp = zp.HParams(**zs.HPARAMS)
+    stream = torch.cuda.current_stream(dev)
+    wlist = [bits[:S // 32]] + others
+
+    def step(ev=None):
+        if ev:
+            ev[0].record(stream)
+        zp.zero_grad_norm_overflow(g, state, ws, stream=stream)
+        zp.zero_onebit_worker(g, m, e_w, bits, wscale[0:1], hp, 1000, state, ws, stream=stream)
+        if ev:
+            ev[1].record(stream)
+        zp.zero_onebit_server(wlist, wscale, e_s, sbits[:S // 32], sscale[0:1], ws, stream=stream)
+        if ev:
+            ev[2].record(stream)
+        zp.zero_onebit_update(sbits, sscale, S, numel, p, m, v, plp, ws, stream=stream)
+        if ev:
+            ev[3].record(stream)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize(dev)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(dev.index) as clk:
+        e0.record(stream)
+        for _ in range(args.steps):
+            step()
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
+        for k in range(args.steps):
+            step(evs[k])
+        torch.cuda.synchronize(dev)
+    st = zp.parse_state(state)
+    assert st["last_skipped"] == 0 and st["step"] == 1000 + 2 * args.steps + args.warmup
+    dt = e0.elapsed_time(e1) / args.steps * 1e-3
+    ms = [statistics.mean(ev[k].elapsed_time(ev[k + 1]) for ev in evs) for k in range(3)]
+    # bytes per element of the padded buffer
+    b_worker = 2 + 14 + 8 + 1 / 8                  # pass 1, worker, signs
+    b_server = (nd / 8 + 16 + 1 / 8) / nd            # per element of the whole buffer
+    b_update = 1 / 8 + 12 + 4 + 2
+    b_step = b_worker + b_server + b_update
+    peaks = measured_peaks()
+    peak = peaks["hbm_gbs"] if peaks else 6800.0
+    achieved = b_step * n / dt / 1e9
+    line = {
+        "metric": "1-bit Adam compression-stage step params/sec & achieved HBM GB/s, 1 GPU",
+        "value": n / dt, "unit": "params/s", "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": dt * 1e3, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "f32", "data": "synthetic",
+        "config": {"workload": "1-bit Adam, GPT-2 1.5B (1,557,611,200 params padded to 16 x 97,350,784), "
+                               "rank 0 of 16, fp16 gradient and parameters, fp32 state; the other ranks' "
+                               "signs and scales are synthetic messages", "elements": n,
+                   "l2": "inputs larger than L2, no flush"},
+        "bytes_per_param": {"pass1_and_worker": b_worker, "server": b_server, "update": b_update,
+                            "whole_step": b_step},
+        "passes_ms": {"pass1_and_worker": ms[0], "server": ms[1], "update": ms[2], "whole_step": dt * 1e3},
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
+                     "traffic": None, "kernel": f"whole compression-stage step, {b_step:.2f} B/param",
+                     "peak_source": "MEASURED_PEAKS.json hbm_gbs (of measured)" if peaks
+                     else "fallback 6.8 TB/s (of fallback)"},
+        "gpu_launches": 7 * args.steps,
+        "clocks": clk.summary(),
+    }
+    print(json.dumps(line), flush=True)
+
+
 def run_offload(args):
     """ZeRO-Offload on the GPT-2 1.5B Nd=16 shard: the fp32 master, momentum
     and variance (12 B/param) live in pinned host memory, the gradient and
@@ -831,7 +933,7 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--workload", default=WORKLOAD,
                     choices=["gpt2_1p5b_nd16", "tiny", "gpt2_1p5b_full", "stack_100b_nd400",
-                             "frag_10k", "flat", "offload", "stage2", "gather"],
+                             "frag_10k", "flat", "offload", "stage2", "gather", "onebit"],
                     help="default: the GPT-2 1.5B Nd=16 shard the metric is quoted on")
     ap.add_argument("--log2n", type=int, default=26, help="size of the flat workload (2^k)")
     ap.add_argument("--clock-preroll", type=float, default=1.0,
@@ -841,10 +943,11 @@ def main():
         ap.error("--warmup must be at least 3")
     if args.impl == "reference":
         run_reference(args)
-    elif args.workload in ("offload", "stage2", "gather"):
+    elif args.workload in ("offload", "stage2", "gather", "onebit"):
         from zero_partitioned_mixed_layout_gb300 import _build
         _build.build()
-        {"offload": run_offload, "stage2": run_stage2, "gather": run_gather}[args.workload](args)
+        {"offload": run_offload, "stage2": run_stage2, "gather": run_gather,
+         "onebit": run_onebit}[args.workload](args)
     else:
         import zero_partitioned_mixed_layout_gb300 as zp
         from zero_partitioned_mixed_layout_gb300 import _build

@@ -376,6 +376,66 @@ int zero_gather_plan(const int64_t *numel, int64_t n_tensors, const int64_t *lay
                      int32_t nd, int64_t align, int64_t *layer_flat, zero_gather_piece_t *pieces, int64_t cap,
                      int64_t *n_pieces, int64_t *max_layer_numel);
 
+/* ------------------------------------------------------------------ 1-bit Adam */
+
+/* 1-bit Adam (DeepSpeed release news, lxsoso.com/blog/19320.html: Adam with
+ * up to 5x less communication and Adam's convergence).  The page gives no
+ * algorithm; these calls follow the outline of the published method (Tang et
+ * al. 2021): after a warm-up of T_w plain steps (zero_adam_step), the
+ * variance is frozen and the workers average their MOMENTUM, not their
+ * gradient, through an all-reduce compressed to one bit per element with
+ * error feedback at both ends.  One compression-stage step of rank r of Nd
+ * (n = Nd * S elements, the padded flat layout; rank r serves chunk r,
+ * elements [r*S, (r+1)*S)):
+ *
+ *   zero_grad_norm_overflow(g)         overflow flag (and norm) of the local
+ *                                      gradient, summed over the ranks
+ *   zero_onebit_worker                 x = b1*m + (1-b1)*g + e_w;
+ *                                      e_w <- x - C(x); signs, scale of C(x)
+ *   (exchange: chunk j of every worker's signs and its scale to rank j)
+ *   zero_onebit_server                 y = mean over workers of C(x_i) on
+ *                                      chunk r, + e_s; e_s <- y - C(y)
+ *   (exchange: every rank's server signs and scale to every worker)
+ *   zero_onebit_update                 m <- the servers' C(y_j), all chunks;
+ *                                      p <- p - (lr/(1-b1^t) * m /
+ *                                      (sqrt(v) * isb2(T_w) + eps) + lr*wd*p)
+ *
+ * The compressor: C(x) = scale * sign(x) with scale = ||x||_2 / sqrt(len)
+ * (binary64 sum, rounded once to binary32) and sign(0) = +1.  Signs travel
+ * as 32-bit words, bit k of word w holding element 32w + k, 1 for +.  The
+ * server's mean is the binary32 sum over workers in rank order followed by
+ * one division by Nd.  Element arithmetic is binary32, each operation
+ * rounded on its own.  The three calls of one step use the same state and
+ * workspace (zero_workspace_bytes(1, n)) in stream order; the worker call's
+ * decision (skip on overflow, loss scale, step count) holds for the other
+ * two, and a skipped step changes nothing.  n and S must be multiples of 32
+ * (ZERO_ESIZE); arrays 16-byte aligned.  Errors otherwise as
+ * zero_adam_step. */
+
+/* Worker side.  grad: n elements (F16, BF16 or F32); m: the synchronised
+ * momentum (fp32, read); e_w: the worker error (fp32, updated); bits: n/32
+ * words (written); scale: one device float (written).  freeze_step: T_w,
+ * the count of the last warm-up step (>= 1). */
+int zero_onebit_worker(const void *grad, int32_t gdtype, const float *m, float *e_w, int64_t n, uint32_t *bits,
+                       float *scale, const zero_hparams_t *hp, int64_t freeze_step, zero_state_t *d_state, void *ws,
+                       size_t ws_bytes, void *stream);
+
+/* Server side for this rank's chunk of S elements.  worker_bits: HOST array
+ * of nd device pointers, each to S/32 words (the chunk's signs from worker
+ * i); worker_scales: device array of nd floats; e_s: the server error (S
+ * fp32, updated); bits: S/32 words and scale: one device float (written). */
+int zero_onebit_server(const uint32_t *const *worker_bits, const float *worker_scales, int32_t nd, int64_t S,
+                       float *e_s, uint32_t *bits, float *scale, void *ws, size_t ws_bytes, void *stream);
+
+/* Update.  bits: nd*S/32 words, the servers' signs in rank order;
+ * server_scales: device array of nd floats; p, m, v: fp32 arrays of at
+ * least `numel` elements (p and m written, v read); p_lp: F16 or BF16
+ * copy of p (or NULL).  Elements from `numel` to nd*S (padding) are not
+ * touched. */
+int zero_onebit_update(const uint32_t *bits, const float *server_scales, int32_t nd, int64_t S, int64_t numel,
+                       float *p, float *m, const float *v, void *p_lp, int32_t pdtype, void *ws, size_t ws_bytes,
+                       void *stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -382,17 +382,22 @@ class OnebitResult:
 def onebit_step(grads: list[np.ndarray], gdtype: str, S: int, numel: int, p: np.ndarray,
                 m: np.ndarray, v: np.ndarray, e_w: list[np.ndarray], e_s: list[np.ndarray],
                 p_lp: np.ndarray | None, pdtype: str, hp: HParams, sc: Scaler, t_freeze: int,
-                worker_scales: list | None = None, server_scales: list | None = None) -> OnebitResult:
+                worker_scales: list | None = None, server_scales: list | None = None,
+                clip: float | None = None) -> OnebitResult:
     """One compression-stage step of 1-bit Adam over all Nd = len(grads)
     workers (every worker holds the same p, m, v; its own gradient and error
     e_w[i]; rank j serves chunk j with error e_s[j]).  The overflow flag and
     the squared norm are summed over the workers' gradients.  Optional
     worker_scales / server_scales force the scales (another implementation's
-    rounding of the norms)."""
+    rounding of the norms); ``clip`` likewise forces the binary32 clip
+    coefficient (see with_clip)."""
     nd = len(grads)
     assert p.size == nd * S
     sumsq, bad = norm_overflow(grads, gdtype, sc.loss_scale)
-    st = frozen_variance(decide(hp, sc, sumsq, bad), hp, t_freeze)
+    st = decide(hp, sc, sumsq, bad)
+    if clip is not None and not st.skip:
+        st = with_clip(st, clip)
+    st = frozen_variance(st, hp, t_freeze)
     res = OnebitResult(st)
     if st.skip:
         return res

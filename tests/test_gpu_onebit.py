@@ -1,0 +1,290 @@
+"""1-bit Adam's compression stage on one GPU against the oracle: the Nd
+workers, the Nd servers and the update of one compression-stage step, each
+worker and server as the rank it would be (its own state and workspace), bit
+for bit once the GPU's scales are handed to the oracle (the binary64 norm is
+summed in another order: the scales themselves agree within 2^-22); and the
+benchmark's full-size step on sampled elements plus the norm property."""
+import numpy as np
+import pytest
+
+import oracle
+import zero_synth as zs
+
+torch = pytest.importorskip("torch")
+pytestmark = pytest.mark.gpu
+
+from gpu_common import TORCH, to_dev, to_host  # noqa: E402
+
+SCALE_REL = 2.0 ** -22
+
+
+@pytest.fixture(scope="module")
+def zp():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from zero_partitioned_mixed_layout_gb300 import _build
+    _build.build()
+    import zero_partitioned_mixed_layout_gb300 as zp
+    zp.lib()
+    return zp
+
+
+def state_at(zp, loss_scale, step):
+    """A device state after `step` applied warm-up steps."""
+    st = zp.binding._State()
+    zp.binding.lib().zero_state_init(zp.binding.ctypes.byref(st), float(loss_scale))
+    st.step = int(step)
+    raw = bytes(zp.binding.ctypes.string_at(zp.binding.ctypes.byref(st), zp.STATE_BYTES))
+    return torch.frombuffer(bytearray(raw), dtype=torch.uint8).cuda()
+
+
+def words(t):
+    return t.cpu().numpy().view(np.uint32)
+
+
+def bit_at(w, idx):
+    """Sign bits of elements idx from packed words (bit k of word j is
+    element 32j + k)."""
+    return ((w[idx >> 5] >> (idx & 31).astype(np.uint32)) & 1).astype(np.uint8)
+
+
+def pack(b):
+    """Bits (one per element, in order) to packed words."""
+    b = np.pad(np.asarray(b, np.uint8), (0, (-len(b)) % 32))
+    return np.packbits(b, bitorder="little").view(np.uint32)
+
+
+def run_gpu_step(zp, d, nd, S, numel, hp, T, pdtype):
+    """One compression-stage step of every rank on the device arrays in d."""
+    n = nd * S
+    for i in range(nd):
+        for k in range(nd):
+            zp.zero_grad_norm_overflow(d["g"][k], d["state"][i], d["ws"][i], accumulate=k > 0)
+    for i in range(nd):
+        zp.zero_onebit_worker(d["g"][i], d["m"], d["ew"][i], d["wbits"][i], d["wscale"][i:i + 1], hp, T,
+                              d["state"][i], d["ws"][i])
+    w = S // 32
+    for j in range(nd):
+        zp.zero_onebit_server([d["wbits"][i][j * w:(j + 1) * w] for i in range(nd)], d["wscale"], d["es"][j],
+                              d["sbits"][j * w:(j + 1) * w], d["sscale"][j:j + 1], d["ws"][j])
+    zp.zero_onebit_update(d["sbits"], d["sscale"], S, numel, d["p"], d["m"], d["v"], d["plp"], d["ws"][0])
+    torch.cuda.synchronize()
+    assert n == d["p"].numel()
+
+
+def setup(zp, nd, S, gdtype, pdtype, seed, loss_scale, T, inf_at=None):
+    n = nd * S
+    rng = np.random.default_rng(seed)
+    h = {
+        "g": [zs.host_grad(n, seed + i, 0, loss_scale, gdtype) for i in range(nd)],
+        "p": zs.host_master(n, seed),
+        "m": (rng.standard_normal(n) * 1e-3).astype(np.float32),
+        "v": (rng.uniform(0.1, 1.0, n) * 1e-6).astype(np.float32),
+        "ew": [(rng.standard_normal(n) * 1e-4).astype(np.float32) for _ in range(nd)],
+        "es": [(rng.standard_normal(S) * 1e-4).astype(np.float32) for _ in range(nd)],
+    }
+    if inf_at is not None:
+        g = h["g"][inf_at[0]]
+        (g.view(np.uint16) if gdtype != "f32" else g.view(np.uint32))[inf_at[1]] = \
+            {"f16": 0x7C00, "bf16": 0x7F80, "f32": 0x7F800000}[gdtype]
+    h["plp"] = oracle.to_lp(h["p"], pdtype) if pdtype else None
+    d = {
+        "g": [to_dev(g, gdtype) for g in h["g"]],
+        "p": to_dev(h["p"], "f32"), "m": to_dev(h["m"], "f32"), "v": to_dev(h["v"], "f32"),
+        "ew": [to_dev(e, "f32") for e in h["ew"]], "es": [to_dev(e, "f32") for e in h["es"]],
+        "plp": (to_dev(h["plp"].view(np.float16) if pdtype == "f16" else h["plp"], pdtype)
+                if pdtype else None),
+        "wbits": [torch.zeros(n // 32, dtype=torch.int32, device="cuda") for _ in range(nd)],
+        "wscale": torch.zeros(nd, dtype=torch.float32, device="cuda"),
+        "sbits": torch.zeros(n // 32, dtype=torch.int32, device="cuda"),
+        "sscale": torch.zeros(nd, dtype=torch.float32, device="cuda"),
+        "state": [state_at(zp, loss_scale, T) for _ in range(nd)],
+        "ws": [zp.new_workspace(1, n) for _ in range(nd)],
+    }
+    return h, d
+
+
+def check_step(zp, h, d, nd, S, numel, gdtype, pdtype, hp, sc, T):
+    """Runs the oracle's step with the GPU's scales and compares everything."""
+    ew0 = [e.copy() for e in h["ew"]]
+    # the scales the oracle computes itself agree with the GPU's closely
+    free = oracle.onebit_step(h["g"], gdtype, S, numel, h["p"].copy(), h["m"].copy(), h["v"],
+                              [e.copy() for e in h["ew"]], [e.copy() for e in h["es"]], None, "f16", hp,
+                              oracle.Scaler(sc.loss_scale, sc.step, sc.good_steps), T)
+    gw = d["wscale"].cpu().numpy()
+    gs = d["sscale"].cpu().numpy()
+    st0 = zp.parse_state(d["state"][0])
+    res = oracle.onebit_step(h["g"], gdtype, S, numel, h["p"], h["m"], h["v"], h["ew"], h["es"], h["plp"],
+                             pdtype or "f16", hp, sc, T, worker_scales=list(gw), server_scales=list(gs),
+                             clip=st0["last_clip"])
+    for i in range(nd):
+        st = zp.parse_state(d["state"][i])
+        assert bool(st["last_skipped"]) == res.step.skip and st["step"] == sc.step
+        assert st["loss_scale"] == sc.loss_scale
+    if res.step.skip:
+        return res
+    for i in range(nd):
+        assert abs(gw[i] - free.worker_scales[i]) <= SCALE_REL * free.worker_scales[i], f"worker {i} scale"
+        assert np.array_equal(words(d["wbits"][i]), res.worker_bits[i]), f"worker {i} signs"
+        assert to_host(d["ew"][i]).tobytes() == h["ew"][i].tobytes(), f"worker {i} error"
+    for j in range(nd):
+        assert abs(gs[j] - free.server_scales[j]) <= 4 * SCALE_REL * free.server_scales[j], f"server {j} scale"
+        assert to_host(d["es"][j]).tobytes() == h["es"][j].tobytes(), f"server {j} error"
+    assert np.array_equal(words(d["sbits"]), np.concatenate(res.server_bits))
+    assert to_host(d["p"]).tobytes() == h["p"].tobytes(), "master"
+    assert to_host(d["m"]).tobytes() == h["m"].tobytes(), "momentum"
+    if pdtype:
+        assert np.array_equal(to_host(d["plp"]), h["plp"]), "low-precision params"
+    assert any((e != e0).any() for e, e0 in zip(h["ew"], ew0))
+    return res
+
+
+@pytest.mark.parametrize("nd,S", [(1, 1024), (2, 2048), (3, 4096), (4, 65_536), (16, 8192)])
+@pytest.mark.parametrize("gdtype,pdtype", [("f16", "f16"), ("bf16", "bf16"), ("f32", None)])
+def test_onebit_step_matches_oracle(zp, nd, S, gdtype, pdtype):
+    T = 100
+    scale = 1.0 if gdtype == "bf16" else 1024.0
+    h, d = setup(zp, nd, S, gdtype, pdtype, 7 * nd + S, scale, T)
+    numel = nd * S - 13
+    hp = oracle.HParams()
+    zhp = zp.HParams()
+    run_gpu_step(zp, d, nd, S, numel, zhp, T, pdtype)
+    check_step(zp, h, d, nd, S, numel, gdtype, pdtype, hp, oracle.Scaler(scale, T), T)
+
+
+def test_onebit_three_steps_with_clipping(zp):
+    nd, S, T = 4, 4096, 20
+    h, d = setup(zp, nd, S, "f16", "f16", 99, 1024.0, T)
+    hp = oracle.HParams(max_norm=0.05)
+    zhp = zp.HParams(max_norm=0.05)
+    sc = oracle.Scaler(1024.0, T)
+    for step in range(3):
+        for i in range(nd):
+            h["g"][i] = zs.host_grad(nd * S, 500 + 10 * step + i, step, 1024.0, "f16")
+            d["g"][i] = to_dev(h["g"][i], "f16")
+        run_gpu_step(zp, d, nd, S, nd * S, zhp, T, "f16")
+        res = check_step(zp, h, d, nd, S, nd * S, "f16", "f16", hp, sc, T)
+        assert res.step.scalars["clip"] < 1.0
+
+
+def test_onebit_overflow_skips_everything(zp):
+    nd, S, T = 2, 2048, 30
+    h, d = setup(zp, nd, S, "f16", "f16", 5, 4096.0, T, inf_at=(1, 777))
+    before = {k: [to_host(t).tobytes() for t in (d[k] if isinstance(d[k], list) else [d[k]])]
+              for k in ("p", "m", "ew", "es", "plp")}
+    run_gpu_step(zp, d, nd, S, nd * S, zp.HParams(), T, "f16")
+    for k, v in before.items():
+        assert [to_host(t).tobytes() for t in (d[k] if isinstance(d[k], list) else [d[k]])] == v, k
+    st = zp.parse_state(d["state"][0])
+    assert st["last_skipped"] == 1 and st["step"] == T and st["loss_scale"] == 2048.0
+
+
+def test_onebit_full_size_rank0_sampled(zp):
+    """The benchmark's call sequence at full size (GPT-2 1.5B, Nd = 16,
+    rank 0): the worker over all 1,557,612,544 elements, the server on
+    chunk 0 with the other workers' signs and scales as received messages,
+    and the update; sampled elements against the oracle (with the GPU's
+    scales) and the scales against the norm property ||x||_2 = scale *
+    sqrt(n) evaluated in binary64 on the device."""
+    numel_list = zs.WORKLOADS["gpt2_1p5b_nd16"]["numel"]()
+    nd = 16
+    lay = zp.zero_partition_layout(numel_list, nd, 128)
+    S, numel = lay.shard_numel, sum(numel_list)
+    n = nd * S
+    dev = torch.device("cuda")
+    g = torch.empty(n, dtype=torch.float16, device=dev)
+    zs.device_grad_into(g, 31, 0, 65536.0)
+    m = zs.device_normal(n, 1e-3, 32, "misc", 1)
+    e = zs.device_normal(n, 1e-4, 32, "misc", 2)
+    v = zs.device_normal(n, 1e-3, 32, "misc", 3).square_()
+    p = zs.device_normal(n, 0.02, 32, "master")
+    plp = p.half()
+    idx = zs.sample_indices(n, 200_000, 5)
+    ti = torch.from_numpy(idx).to(dev)
+    h_g, h_m, h_e = to_host(g[ti]), to_host(m[ti]), to_host(e[ti])
+    h_p, h_v = to_host(p[ti]), to_host(v[ti])
+    state = state_at(zp, 65536.0, 1000)
+    ws = zp.new_workspace(1, n)
+    zp.zero_grad_norm_overflow(g, state, ws)
+    bits = torch.zeros(n // 32, dtype=torch.int32, device=dev)
+    wscale = torch.zeros(nd, dtype=torch.float32, device=dev)
+    hp = zp.HParams()
+    zp.zero_onebit_worker(g, m, e, bits, wscale[0:1], hp, 1000, state, ws)
+    torch.cuda.synchronize()
+    # the norm property, in binary64 on the device: x = e' + scale*sign(x)
+    sc0 = float(wscale[0])
+    shifts = torch.arange(32, device=dev, dtype=torch.int32)
+    tot = 0.0
+    for s0 in range(0, n, 1 << 27):
+        s1 = min(n, s0 + (1 << 27))
+        plus = ((bits[s0 // 32:s1 // 32].view(-1, 1) >> shifts) & 1).reshape(-1).bool()
+        x = e[s0:s1].double() + torch.where(plus, sc0, -sc0).double()
+        tot += float((x * x).sum())
+    norm = (tot / n) ** 0.5
+    assert abs(sc0 - norm) <= SCALE_REL * norm
+    # sampled elements, with the GPU's scale
+    hp_o = oracle.HParams()
+    st = oracle.frozen_variance(oracle.decide(hp_o, oracle.Scaler(65536.0, 1000), 0.0, 0), hp_o, 1000)
+    ob, _ = oracle.onebit_worker(h_g, "f16", st, h_m, h_e, scale=sc0)
+    w_all = words(bits)
+    assert np.array_equal(bit_at(w_all, idx), bit_at(ob, np.arange(idx.size)))
+    assert to_host(e[ti]).tobytes() == h_e.tobytes()
+    # server on chunk 0: the other workers' signs and scales are messages
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(zs.stream_seed(0, "misc", 9))
+    others = [torch.randint(-2 ** 31, 2 ** 31 - 1, (S // 32,), dtype=torch.int32, device=dev, generator=gen)
+              for _ in range(nd - 1)]
+    wscale[1:] = torch.rand(nd - 1, device=dev, generator=gen) * 1e-3 + 1e-4
+    es = zs.device_normal(S, 1e-4, 33, "misc", 4)
+    sbits = torch.randint(-2 ** 31, 2 ** 31 - 1, (n // 32,), dtype=torch.int32, device=dev, generator=gen)
+    sscale = torch.rand(nd, device=dev, generator=gen) * 1e-3 + 1e-4
+    sidx = zs.sample_indices(S, 50_000, 6)
+    tsi = torch.from_numpy(sidx).to(dev)
+    f = np.concatenate([to_host(es[tsi]), np.zeros((-sidx.size) % 32, np.float32)])
+    chunk_words = [w_all[:S // 32]] + [words(o) for o in others]
+    sub = [pack(bit_at(w, sidx)) for w in chunk_words]
+    zp.zero_onebit_server([bits[:S // 32]] + others, wscale, es, sbits[:S // 32], sscale[0:1], ws)
+    torch.cuda.synchronize()
+    s0 = float(sscale[0])
+    ob, _ = oracle.onebit_server(sub, list(wscale.cpu().numpy()), f, scale=s0)
+    assert to_host(es[tsi]).tobytes() == f[:sidx.size].tobytes()
+    assert np.array_equal(bit_at(words(sbits[:S // 32]), sidx), bit_at(ob, np.arange(sidx.size)))
+    # the update; the other chunks' signs and scales are messages
+    tail_p, tail_m = to_host(p[numel:]).copy(), to_host(m[numel:]).copy()
+    zp.zero_onebit_update(sbits, sscale, S, numel, p, m, v, plp, ws)
+    torch.cuda.synchronize()
+    keep = idx < numel
+    uidx = idx[keep]
+    tu = torch.from_numpy(uidx).to(dev)
+    hp_s, hv_s = h_p[keep].copy(), h_v[keep].copy()
+    hm_s = np.zeros_like(hp_s)
+    per_scale = sscale.cpu().numpy()[uidx // S]
+    # S = 1: each sampled element is its own chunk with its own scale
+    oracle.onebit_update(pack(bit_at(words(sbits), uidx)), list(per_scale), 1, uidx.size, hp_s, hm_s, hv_s,
+                         None, "f16", st)
+    assert to_host(p[tu]).tobytes() == hp_s.tobytes()
+    assert to_host(m[tu]).tobytes() == hm_s.tobytes()
+    assert np.array_equal(to_host(plp[tu]), oracle.to_lp(hp_s, "f16"))
+    # the padding past numel is not parameters: untouched
+    assert to_host(p[numel:]).tobytes() == tail_p.tobytes()
+    assert to_host(m[numel:]).tobytes() == tail_m.tobytes()
+
+
+def test_onebit_argument_errors(zp):
+    dev = "cuda"
+    g = torch.zeros(100, dtype=torch.float16, device=dev)  # not a multiple of 32
+    f = torch.zeros(100, device=dev)
+    bits = torch.zeros(3, dtype=torch.int32, device=dev)
+    st, ws = state_at(zp, 1.0, 5), zp.new_workspace(1, 128)
+    with pytest.raises(zp.ZeroError) as e:
+        zp.zero_onebit_worker(g, f, f.clone(), bits, torch.zeros(1, device=dev), zp.HParams(), 5, st, ws)
+    assert e.value.code == -4
+    g = torch.zeros(128, dtype=torch.float16, device=dev)
+    f = torch.zeros(128, device=dev)
+    bits = torch.zeros(4, dtype=torch.int32, device=dev)
+    with pytest.raises(zp.ZeroError) as e:  # freeze step must be a step count
+        zp.zero_onebit_worker(g, f, f.clone(), bits, torch.zeros(1, device=dev), zp.HParams(), 0, st, ws)
+    assert e.value.code == -1
+    with pytest.raises(zp.ZeroError) as e:  # numel past nd * S
+        zp.zero_onebit_update(bits, torch.ones(1, device=dev), 128, 129, f, f.clone(), f.clone(), None, ws)
+    assert e.value.code == -4

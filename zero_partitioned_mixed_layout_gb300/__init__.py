@@ -5,8 +5,8 @@ padded buffer and partitioned over Nd ranks, and one rank's shard is updated
 by hand-written CUDA kernels (gradient accumulation; unscale + overflow +
 global squared norm; clip + AdamW + cast to fp16/bf16).  Around the step:
 the stage-2 gradient reduction fused with the norm pass, the stage-3
-parameter gather (shards back to tensors) with its per-layer plan, and the
-offload step on the host cores.  The C ABI is in
+parameter gather (shards back to tensors) with its per-layer plan, the
+offload step on the host cores, and 1-bit Adam's compression stage.  The C ABI is in
 ``include/zero_pml.h``; this package is its Python binding.
 """
 from .binding import (  # noqa: F401
@@ -42,4 +42,7 @@ from .binding import (  # noqa: F401
     zero_gather_plan,
     zero_gather_workspace_bytes,
     zero_scatter_params,
+    zero_onebit_server,
+    zero_onebit_update,
+    zero_onebit_worker,
 )

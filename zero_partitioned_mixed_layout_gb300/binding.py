@@ -442,6 +442,103 @@ def zero_gather_plan(numel: Sequence[int], layer_first: Sequence[int], nd: int,
     return GatherPlan(np.frombuffer(flat, np.int64, count=nl + 1).copy(), pc, big.value)
 
 
+# ------------------------------------------------------------------ 1-bit Adam
+
+def _onebit_lib():
+    so = lib()
+    if not getattr(so, "_onebit_ready", False):
+        vp, i64, i32 = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int32
+        so.zero_onebit_worker.argtypes = [vp, i32, vp, vp, i64, vp, vp, ctypes.POINTER(_HParams), i64, vp,
+                                          vp, ctypes.c_size_t, vp]
+        so.zero_onebit_server.argtypes = [ctypes.POINTER(vp), vp, i32, i64, vp, vp, vp, vp, ctypes.c_size_t,
+                                          vp]
+        so.zero_onebit_update.argtypes = [vp, vp, i32, i64, i64, vp, vp, vp, vp, i32, vp, ctypes.c_size_t,
+                                          vp]
+        for f in ("zero_onebit_worker", "zero_onebit_server", "zero_onebit_update"):
+            getattr(so, f).restype = ctypes.c_int
+        so._onebit_ready = True
+    return so
+
+
+def _words_tensor(t, what: str, n_words: int | None = None):
+    """A device int32 tensor used as packed sign words."""
+    import torch
+    _device_tensor(t, what)
+    if t.dtype != torch.int32:
+        raise TypeError(f"{what} must be an int32 tensor of packed sign words")
+    if n_words is not None and t.numel() != n_words:
+        raise ValueError(f"{what} must hold {n_words} words")
+    return t
+
+
+def _f32_tensor(t, what: str, n: int | None = None):
+    import torch
+    _device_tensor(t, what)
+    if t.dtype != torch.float32:
+        raise TypeError(f"{what} must be float32")
+    if n is not None and t.numel() != n:
+        raise ValueError(f"{what} must hold {n} elements")
+    return t
+
+
+def zero_onebit_worker(grad, m, e_w, bits, scale, hp: HParams, freeze_step: int, state, ws,
+                       stream=None) -> None:
+    """1-bit Adam, worker side: the decision (variance frozen at step
+    freeze_step), then x = b1*m + (1-b1)*g + e_w compressed to signs (bits,
+    int32[n/32]) and one scale (float32[1]); e_w updated."""
+    n = grad.numel()
+    _device_tensor(grad, "grad")
+    _f32_tensor(m, "m", n), _f32_tensor(e_w, "e_w", n), _f32_tensor(scale, "scale", 1)
+    _words_tensor(bits, "bits", n // 32)
+    _device_tensor(state, "state"), _device_tensor(ws, "workspace")
+    h = hp._c()
+    rc = _onebit_lib().zero_onebit_worker(
+        ctypes.c_void_p(grad.data_ptr()), _dtype_code(grad), ctypes.c_void_p(m.data_ptr()),
+        ctypes.c_void_p(e_w.data_ptr()), n, ctypes.c_void_p(bits.data_ptr()),
+        ctypes.c_void_p(scale.data_ptr()), ctypes.byref(h), int(freeze_step),
+        ctypes.c_void_p(state.data_ptr()), ctypes.c_void_p(ws.data_ptr()), ws.numel(),
+        _stream_ptr(stream, state.device))
+    _check(rc, "zero_onebit_worker")
+
+
+def zero_onebit_server(worker_bits, worker_scales, e_s, bits, scale, ws, stream=None) -> None:
+    """1-bit Adam, server side for this rank's chunk of S = e_s.numel()
+    elements: worker_bits (Nd int32 tensors of S/32 words, rank order) and
+    worker_scales (float32[Nd]) averaged, plus e_s, compressed again."""
+    S = e_s.numel()
+    wb = [_words_tensor(b, "worker bits", S // 32) for b in worker_bits]
+    _f32_tensor(worker_scales, "worker_scales", len(wb)), _f32_tensor(e_s, "e_s")
+    _words_tensor(bits, "bits", S // 32), _f32_tensor(scale, "scale", 1), _device_tensor(ws, "workspace")
+    ptrs = (ctypes.c_void_p * max(len(wb), 1))(*[b.data_ptr() for b in wb])
+    rc = _onebit_lib().zero_onebit_server(
+        ptrs, ctypes.c_void_p(worker_scales.data_ptr()), len(wb), S, ctypes.c_void_p(e_s.data_ptr()),
+        ctypes.c_void_p(bits.data_ptr()), ctypes.c_void_p(scale.data_ptr()),
+        ctypes.c_void_p(ws.data_ptr()), ws.numel(), _stream_ptr(stream, ws.device))
+    _check(rc, "zero_onebit_server")
+
+
+def zero_onebit_update(bits, server_scales, S: int, numel: int, p, m, v, p_lp, ws, stream=None) -> None:
+    """1-bit Adam, every worker: m = the servers' signs times their scales
+    (chunk j of S elements from server j), and p updated with the frozen v,
+    for the first numel elements; p_lp (fp16/bf16) follows p if given."""
+    nd = server_scales.numel()
+    _words_tensor(bits, "bits", nd * S // 32), _f32_tensor(server_scales, "server_scales")
+    for t, name in ((p, "p"), (m, "m"), (v, "v")):
+        _f32_tensor(t, name)
+        if t.numel() < numel:
+            raise ValueError(f"{name} holds fewer than numel elements")
+    lp, code = None, ZERO_F16
+    if p_lp is not None:
+        _device_tensor(p_lp, "p_lp")
+        lp, code = ctypes.c_void_p(p_lp.data_ptr()), _dtype_code(p_lp)
+    _device_tensor(ws, "workspace")
+    rc = _onebit_lib().zero_onebit_update(
+        ctypes.c_void_p(bits.data_ptr()), ctypes.c_void_p(server_scales.data_ptr()), nd, int(S), int(numel),
+        ctypes.c_void_p(p.data_ptr()), ctypes.c_void_p(m.data_ptr()), ctypes.c_void_p(v.data_ptr()), lp, code,
+        ctypes.c_void_p(ws.data_ptr()), ws.numel(), _stream_ptr(stream, ws.device))
+    _check(rc, "zero_onebit_update")
+
+
 # ------------------------------------------------------------------ offload (host)
 
 class OffloadScalars(ctypes.Structure):

@@ -12,6 +12,7 @@
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
+#include <cmath>
 #include <cstdint>
 #include <mutex>
 #include <unordered_map>
@@ -270,7 +271,42 @@ struct DecideArgs {
     // step scalars that do not depend on the device state, computed on the
     // host the same way (binary64, rounded once to binary32)
     float b1, omb1, b2, omb2, eps, lrwd;
+    // 1-bit Adam's compression stage: the variance and its bias correction
+    // are frozen at the last warm-up step; isb2 is then that step's value
+    int32_t frozen;
+    float isb2_frozen;
 };
+
+// Hyper-parameters in range: lr, eps, weight decay >= 0, betas in [0, 1),
+// a scale floor >= 1, a growth window >= 1, max_norm not NaN.
+inline bool hparams_ok(const zero_hparams_t *hp)
+{
+    return hp->lr >= 0.0 && hp->beta1 >= 0.0 && hp->beta1 < 1.0 && hp->beta2 >= 0.0 && hp->beta2 < 1.0 &&
+           hp->eps >= 0.0 && hp->weight_decay >= 0.0 && hp->min_scale >= 1.0 && hp->scale_window >= 1 &&
+           hp->max_norm == hp->max_norm;
+}
+
+// The decision's arguments from the host hyper-parameters; freeze_step > 0
+// freezes the variance correction at 1/sqrt(1 - beta2^freeze_step).
+inline DecideArgs decide_args(const zero_hparams_t *hp, int64_t freeze_step = 0)
+{
+    DecideArgs a;
+    a.lr = hp->lr;
+    a.beta1 = hp->beta1;
+    a.beta2 = hp->beta2;
+    a.max_norm = hp->max_norm;
+    a.min_scale = hp->min_scale;
+    a.scale_window = hp->scale_window;
+    a.b1 = (float)hp->beta1;
+    a.omb1 = (float)(1.0 - hp->beta1);
+    a.b2 = (float)hp->beta2;
+    a.omb2 = (float)(1.0 - hp->beta2);
+    a.eps = (float)hp->eps;
+    a.lrwd = (float)(hp->lr * hp->weight_decay);
+    a.frozen = freeze_step > 0;
+    a.isb2_frozen = a.frozen ? (float)(1.0 / std::sqrt(1.0 - std::pow(hp->beta2, (double)freeze_step))) : 0.0f;
+    return a;
+}
 
 // Skip or apply, loss-scale and step bookkeeping, and the step scalars
 // (binary64, each rounded once to binary32).  Binary64 is a slow pipe on
@@ -299,7 +335,9 @@ __global__ void k_decide(zero_state_t *st, StepScalars *out, const PowCache *cac
             s_val[0] = (float)(a.lr / bc1);
         }
     } else if (tid == 1) {
-        if (hit) {
+        if (a.frozen) {
+            s_val[1] = a.isb2_frozen;
+        } else if (hit) {
             s_val[1] = c.isb2;
         } else {
             const double bc2 = 1.0 - pow(a.beta2, t);

@@ -1,0 +1,415 @@
+// 1-bit Adam's compression stage on one rank: the worker side (local
+// momentum, error feedback, compression to signs and one scale), the server
+// side for the rank's chunk (the workers' mean, error feedback,
+// recompression) and the update with the frozen variance.
+//
+// Source: DeepSpeed release news (lxsoso.com/blog/19320.html) names 1-bit
+// Adam: up to 5x less communication than Adam with Adam's convergence.  The
+// page gives no algorithm; the steps follow the outline of the published
+// method (Tang et al. 2021): warm-up with plain Adam, then a frozen variance
+// and a momentum all-reduce compressed to one bit per element with error
+// feedback on the workers and on the servers.
+//
+// Every pass streams HBM.  A compression needs the L2 norm of its whole
+// input before any sign can be turned into an error, so it takes two
+// kernels: the first forms the input (stored in place of the error) and its
+// squared norm (binary32 squares in 8 lanes, one binary64 add per 32
+// elements, fixed-order block partials, the last block finishing the sum and
+// writing the scale); the second writes the signs, packed 32 to a word with
+// two warp shuffles, and the new error.  Bytes per element: worker 14 + 8
+// (fp16 gradient), server (Nd/8 + 8) + 8 per chunk element, update 18.
+#include <vector>
+
+#include "common.cuh"
+
+namespace zpml {
+namespace {
+
+__device__ __forceinline__ void ld8(const float *p, float *f)
+{
+    const float4 a = __ldcs(reinterpret_cast<const float4 *>(p));
+    const float4 b = __ldcs(reinterpret_cast<const float4 *>(p) + 1);
+    f[0] = a.x; f[1] = a.y; f[2] = a.z; f[3] = a.w;
+    f[4] = b.x; f[5] = b.y; f[6] = b.z; f[7] = b.w;
+}
+
+__device__ __forceinline__ void st8(float *p, const float *f)
+{
+    __stcs(reinterpret_cast<float4 *>(p), make_float4(f[0], f[1], f[2], f[3]));
+    __stcs(reinterpret_cast<float4 *>(p) + 1, make_float4(f[4], f[5], f[6], f[7]));
+}
+
+// End of a squared-norm pass: publish this block's partial; the block that
+// takes the last ticket sums the partials in block order and writes the
+// compressor's scale sqrt(sum / len), rounded once to binary32.
+__device__ void scale_finish(double tot, double2 *partials, WsHeader *hdr, int64_t len, float *scale)
+{
+    __shared__ bool s_last;
+    uint32_t none = 0;
+    block_reduce(tot, none);
+    if (threadIdx.x == 0) {
+        partials[blockIdx.x] = make_double2(tot, 0.0);
+        __threadfence();
+        s_last = atomicAdd(&hdr->ticket, 1u) == gridDim.x - 1;
+    }
+    __syncthreads();
+    if (!s_last)
+        return;
+    __threadfence();
+    double t = 0.0;
+    for (int j = threadIdx.x; j < (int)gridDim.x; j += kThreads)
+        t += __ldcg(partials + j).x;
+    block_reduce(t, none);
+    if (threadIdx.x == 0) {
+        *scale = (float)sqrt(t / (double)len);
+        hdr->ticket = 0u;
+    }
+}
+
+// Squares of one 8-element group into a binary32 lane sum; every 4 groups
+// (32 elements) the lane sum goes into the binary64 total.
+struct SquareSum {
+    double tot = 0.0;
+    float part = 0.0f;
+    int groups = 0;
+    __device__ __forceinline__ void add(const float *x)
+    {
+        float sq[8];
+#pragma unroll
+        for (int k = 0; k < 8; ++k)
+            sq[k] = __fmul_rn(x[k], x[k]);
+        part = __fadd_rn(part, tree8(sq));
+        if (++groups == 4) {
+            tot += (double)part;
+            part = 0.0f;
+            groups = 0;
+        }
+    }
+    __device__ __forceinline__ double total() const { return tot + (double)part; }
+};
+
+// Worker, first pass: x = b1*m + (1-b1)*g + e (g unscaled, clipped), stored
+// over e; the squared norm of x into the scale.
+template <int GT>
+__global__ void __launch_bounds__(kThreads) k_onebit_worker(const void *g, const float *m, float *e, int64_t n,
+                                                            const StepScalars *scp, double2 *partials,
+                                                            WsHeader *hdr, float *scale)
+{
+    pdl_wait();
+    const StepScalars s = *scp;
+    if (s.skip)
+        return;
+    constexpr int W = Elem<GT>::kWords;
+    const uint4 *gv = static_cast<const uint4 *>(g);
+    SquareSum acc;
+    const int64_t nv = n >> 3;
+    for (int64_t i = (int64_t)blockIdx.x * kThreads + threadIdx.x; i < nv; i += (int64_t)gridDim.x * kThreads) {
+        uint4 w[W];
+#pragma unroll
+        for (int q = 0; q < W; ++q)
+            w[q] = __ldcs(gv + i * W + q);
+        float gf[8], mf[8], x[8];
+        Elem<GT>::to_float(w, gf);
+        ld8(m + 8 * i, mf);
+        ld8(e + 8 * i, x);
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+            const float gk = __fmul_rn(__fmul_rn(gf[k], s.inv_scale), s.clip);
+            const float mk = __fadd_rn(__fmul_rn(s.b1, mf[k]), __fmul_rn(s.omb1, gk));
+            x[k] = __fadd_rn(mk, x[k]);
+        }
+        st8(e + 8 * i, x);
+        acc.add(x);
+    }
+    scale_finish(acc.total(), partials, hdr, n, scale);
+}
+
+// Server, first pass over the chunk: y = (sum over workers in rank order of
+// +-scale_k) / Nd + f, stored over f; the squared norm of y into the scale.
+__global__ void __launch_bounds__(kThreads) k_onebit_server(const uint32_t *const *wbits, const float *wscales,
+                                                            int nd, float *f, int64_t S, const StepScalars *scp,
+                                                            double2 *partials, WsHeader *hdr, float *scale)
+{
+    pdl_wait();
+    if (scp->skip)
+        return;
+    const float count = (float)nd;
+    SquareSum acc;
+    const int64_t nv = S >> 3;
+    for (int64_t i = (int64_t)blockIdx.x * kThreads + threadIdx.x; i < nv; i += (int64_t)gridDim.x * kThreads) {
+        float a[8];
+        for (int k = 0; k < nd; ++k) {
+            const uint32_t byte = (__ldg(wbits[k] + (i >> 2)) >> (8 * (i & 3))) & 0xFFu;
+            const float sc = __ldg(wscales + k);
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                const float c = ((byte >> j) & 1u) ? sc : -sc;
+                a[j] = k == 0 ? c : __fadd_rn(a[j], c);
+            }
+        }
+        float y[8];
+        ld8(f + 8 * i, y);
+#pragma unroll
+        for (int j = 0; j < 8; ++j)
+            y[j] = __fadd_rn(__fdiv_rn(a[j], count), y[j]);
+        st8(f + 8 * i, y);
+        acc.add(y);
+    }
+    scale_finish(acc.total(), partials, hdr, S, scale);
+}
+
+// Second pass of a compression (worker or server): the signs of x, 32 to a
+// word, and the new error x - scale*sign(x) over x.  One 8-element group
+// per thread (one-shot grid); the four threads of a word meet by shuffles.
+__global__ void __launch_bounds__(kThreads) k_onebit_sign(float *x, int64_t n, const float *scale, uint32_t *bits,
+                                                          const StepScalars *scp)
+{
+    pdl_wait();
+    if (scp->skip)
+        return;
+    const float sc = *scale;
+    const int64_t i = (int64_t)blockIdx.x * kThreads + threadIdx.x;
+    const int64_t nv = n >> 3;
+    uint32_t byte = 0;
+    if (i < nv) {
+        float v[8];
+        ld8(x + 8 * i, v);
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+            const bool plus = !(v[k] < 0.0f);
+            byte |= (uint32_t)plus << k;
+            v[k] = __fsub_rn(v[k], plus ? sc : -sc);
+        }
+        st8(x + 8 * i, v);
+    }
+    uint32_t w = byte << (8 * (threadIdx.x & 3));
+    w |= __shfl_xor_sync(0xffffffffu, w, 1);
+    w |= __shfl_xor_sync(0xffffffffu, w, 2);
+    if ((threadIdx.x & 3) == 0 && i < nv)
+        bits[i >> 2] = w;
+}
+
+// One element of the update with the frozen variance:
+//   m = +-scale;  p = p - (step_size * m / (sqrt(v)*isb2 + eps) + lrwd*p)
+__device__ __forceinline__ void onebit_elem(float mi, float vi, float &p, const StepScalars &s)
+{
+    const float d = __fadd_rn(__fmul_rn(__fsqrt_rn(vi), s.isb2), s.eps);
+    const float u = __fdiv_rn(mi, d);
+    p = __fsub_rn(p, __fadd_rn(__fmul_rn(s.step_size, u), __fmul_rn(s.lrwd, p)));
+}
+
+constexpr int kNoLowP = -1;
+
+// The update: one 8-element group per thread (one-shot grid); the last
+// thread takes the elements past the last whole group.
+template <int PT>
+__global__ void __launch_bounds__(kThreads) k_onebit_update(const uint32_t *bits, const float *scales, int64_t S,
+                                                            int64_t numel, float *p, float *m, const float *v,
+                                                            void *plp, const StepScalars *scp)
+{
+    const StepScalars s = *scp;
+    if (s.skip)
+        return;
+    const int64_t i = (int64_t)blockIdx.x * kThreads + threadIdx.x;
+    const int64_t nfull = numel >> 3;
+    if (i < nfull) {
+        const uint32_t byte = (__ldg(bits + (i >> 2)) >> (8 * (i & 3))) & 0xFFu;
+        const float sc = __ldg(scales + (8 * i) / S);
+        float vf[8], pf[8], mf[8];
+        ld8(v + 8 * i, vf);
+        ld8(p + 8 * i, pf);
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+            mf[k] = ((byte >> k) & 1u) ? sc : -sc;
+            onebit_elem(mf[k], vf[k], pf[k], s);
+        }
+        st8(m + 8 * i, mf);
+        st8(p + 8 * i, pf);
+        if constexpr (PT != kNoLowP)
+            __stcs(reinterpret_cast<uint4 *>(plp) + i, LowP<PT>::pack(pf));
+    } else if (i == nfull) {
+        for (int64_t j = 8 * nfull; j < numel; ++j) {
+            const float sc = scales[j / S];
+            const float mi = ((bits[j >> 5] >> (j & 31)) & 1u) ? sc : -sc;
+            float pj = p[j];
+            onebit_elem(mi, v[j], pj, s);
+            p[j] = pj;
+            m[j] = mi;
+            if constexpr (PT != kNoLowP)
+                LowP<PT>::store(plp, j, pj);
+        }
+    }
+}
+
+// ------------------------------------------------------------- host side
+
+bool aligned4(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 3u) == 0; }
+
+int check_ws_table(void *ws, size_t ws_bytes, size_t table)
+{
+    if (!ws)
+        return ZERO_EWORKSPACE;
+    if ((reinterpret_cast<uintptr_t>(ws) & 255u) != 0)
+        return ZERO_EALIGN;
+    if (ws_bytes < kWsTable + table)
+        return ZERO_EWORKSPACE;
+    return device_ptr(ws) ? ZERO_OK : ZERO_EINVAL;
+}
+
+StepScalars *step_scalars(void *ws)
+{
+    return reinterpret_cast<StepScalars *>(static_cast<unsigned char *>(ws) + kWsScalars);
+}
+
+template <int GT>
+int launch_worker(const void *g, const float *m, float *e, int64_t n, uint32_t *bits, float *scale, void *ws,
+                  cudaStream_t st)
+{
+    unsigned char *w = static_cast<unsigned char *>(ws);
+    WsHeader *hdr = reinterpret_cast<WsHeader *>(w);
+    double2 *partials = reinterpret_cast<double2 *>(w + kWsPartials);
+    const StepScalars *sc = step_scalars(ws);
+    const int64_t nv = n >> 3;
+    const int grid = grid_for((const void *)k_onebit_worker<GT>, (nv + kThreads - 1) / kThreads, kMaxBlocks, 4);
+    launch_k(k_onebit_worker<GT>, grid, kThreads, st, true, g, m, e, n, sc, partials, hdr, scale);
+    int rc = check_launch("zero_onebit_worker (first pass)");
+    if (rc != ZERO_OK)
+        return rc;
+    launch_k(k_onebit_sign, (int)((nv + kThreads - 1) / kThreads), kThreads, st, true, e, n, (const float *)scale,
+             bits, sc);
+    return check_launch("zero_onebit_worker (signs)");
+}
+
+template <int PT>
+int launch_update(const uint32_t *bits, const float *scales, int64_t S, int64_t numel, float *p, float *m,
+                  const float *v, void *plp, void *ws, cudaStream_t st)
+{
+    const int64_t threads = (numel >> 3) + 1;
+    launch_k(k_onebit_update<PT>, (int)((threads + kThreads - 1) / kThreads), kThreads, st, false, bits, scales, S,
+             numel, p, m, v, plp, (const StepScalars *)step_scalars(ws));
+    return check_launch("zero_onebit_update");
+}
+
+}  // namespace
+}  // namespace zpml
+
+using namespace zpml;
+
+extern "C" int zero_onebit_worker(const void *grad, int32_t gdtype, const float *m, float *e_w, int64_t n,
+                                  uint32_t *bits, float *scale, const zero_hparams_t *hp, int64_t freeze_step,
+                                  zero_state_t *d_state, void *ws, size_t ws_bytes, void *stream)
+{
+    if (!hp || !d_state || n < 0 || freeze_step < 1 || !hparams_ok(hp))
+        return ZERO_EINVAL;
+    if (!grad_dtype_ok(gdtype))
+        return ZERO_EDTYPE;
+    if (n % 32 != 0 || (n >> 3) / kThreads >= 0x7fffffff)
+        return ZERO_ESIZE;
+    if ((reinterpret_cast<uintptr_t>(d_state) & 7u) != 0)
+        return ZERO_EALIGN;
+    if (n > 0) {
+        if (!grad || !m || !e_w || !bits || !scale)
+            return ZERO_EINVAL;
+        if (!aligned16(grad) || !aligned16(m) || !aligned16(e_w) || !aligned4(bits) || !aligned4(scale))
+            return ZERO_EALIGN;
+        if (!device_ptr(grad) || !device_ptr(m) || !device_ptr(e_w) || !device_ptr(bits) || !device_ptr(scale))
+            return ZERO_EINVAL;
+    }
+    if (!device_ptr(d_state))
+        return ZERO_EINVAL;
+    int rc = check_ws(ws, ws_bytes, 1, n);
+    if (rc != ZERO_OK)
+        return rc;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    const DecideArgs a = decide_args(hp, freeze_step);
+    const PowCache *cache = reinterpret_cast<const PowCache *>(static_cast<unsigned char *>(ws) + kWsPowCache);
+    launch_k(k_decide, 1, 32, st, false, d_state, step_scalars(ws), cache, a);
+    if ((rc = check_launch("zero_onebit_worker (decision)")) != ZERO_OK || n == 0)
+        return rc;
+    switch (gdtype) {
+    case ZERO_F16: return launch_worker<ZERO_F16>(grad, m, e_w, n, bits, scale, ws, st);
+    case ZERO_BF16: return launch_worker<ZERO_BF16>(grad, m, e_w, n, bits, scale, ws, st);
+    default: return launch_worker<ZERO_F32>(grad, m, e_w, n, bits, scale, ws, st);
+    }
+}
+
+extern "C" int zero_onebit_server(const uint32_t *const *worker_bits, const float *worker_scales, int32_t nd,
+                                  int64_t S, float *e_s, uint32_t *bits, float *scale, void *ws, size_t ws_bytes,
+                                  void *stream)
+{
+    if (nd < 1 || S < 0 || !worker_bits || !worker_scales)
+        return ZERO_EINVAL;
+    if (S % 32 != 0 || (S >> 3) / kThreads >= 0x7fffffff)
+        return ZERO_ESIZE;
+    for (int32_t k = 0; k < nd; ++k) {
+        if (!worker_bits[k])
+            return ZERO_EINVAL;
+        if (!aligned4(worker_bits[k]))
+            return ZERO_EALIGN;
+    }
+    if (!aligned4(worker_scales) || !device_ptr(worker_scales) || !device_ptr(worker_bits[0]) ||
+        !device_ptr(worker_bits[nd - 1]))
+        return !aligned4(worker_scales) ? ZERO_EALIGN : ZERO_EINVAL;
+    if (S > 0) {
+        if (!e_s || !bits || !scale)
+            return ZERO_EINVAL;
+        if (!aligned16(e_s) || !aligned4(bits) || !aligned4(scale))
+            return ZERO_EALIGN;
+        if (!device_ptr(e_s) || !device_ptr(bits) || !device_ptr(scale))
+            return ZERO_EINVAL;
+    }
+    const size_t table = align256((size_t)nd * sizeof(void *));
+    int rc = check_ws_table(ws, ws_bytes, table);
+    if (rc != ZERO_OK)
+        return rc;
+    if (S == 0)
+        return ZERO_OK;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    unsigned char *w = static_cast<unsigned char *>(ws);
+    std::vector<const uint32_t *> host(worker_bits, worker_bits + nd);
+    if (cudaMemcpyAsync(w + kWsTable, host.data(), (size_t)nd * sizeof(void *), cudaMemcpyHostToDevice, st) !=
+        cudaSuccess)
+        return check_launch("zero_onebit_server (table upload)");
+    const StepScalars *sc = step_scalars(ws);
+    const int64_t nv = S >> 3;
+    const int grid = grid_for((const void *)k_onebit_server, (nv + kThreads - 1) / kThreads, kMaxBlocks, 4);
+    launch_k(k_onebit_server, grid, kThreads, st, false, (const uint32_t *const *)(w + kWsTable), worker_scales,
+             (int)nd, e_s, S, sc, reinterpret_cast<double2 *>(w + kWsPartials), reinterpret_cast<WsHeader *>(w),
+             scale);
+    if ((rc = check_launch("zero_onebit_server (first pass)")) != ZERO_OK)
+        return rc;
+    launch_k(k_onebit_sign, (int)((nv + kThreads - 1) / kThreads), kThreads, st, true, e_s, S, (const float *)scale,
+             bits, sc);
+    return check_launch("zero_onebit_server (signs)");
+}
+
+extern "C" int zero_onebit_update(const uint32_t *bits, const float *server_scales, int32_t nd, int64_t S,
+                                  int64_t numel, float *p, float *m, const float *v, void *p_lp, int32_t pdtype,
+                                  void *ws, size_t ws_bytes, void *stream)
+{
+    if (nd < 1 || S < 0 || numel < 0 || !server_scales)
+        return ZERO_EINVAL;
+    if (S % 32 != 0 || S > ((int64_t)1 << 62) / nd || numel > (int64_t)nd * S || (numel >> 3) / kThreads >= 0x7fffffff)
+        return ZERO_ESIZE;
+    if (p_lp && !lp_dtype_ok(pdtype))
+        return ZERO_EDTYPE;
+    if (numel > 0) {
+        if (!bits || !p || !m || !v)
+            return ZERO_EINVAL;
+        if (!aligned4(bits) || !aligned4(server_scales) || !aligned16(p) || !aligned16(m) || !aligned16(v) ||
+            (p_lp && !aligned16(p_lp)))
+            return ZERO_EALIGN;
+        if (!device_ptr(bits) || !device_ptr(server_scales) || !device_ptr(p) || !device_ptr(m) || !device_ptr(v) ||
+            (p_lp && !device_ptr(p_lp)))
+            return ZERO_EINVAL;
+    }
+    int rc = check_ws_table(ws, ws_bytes, 0);
+    if (rc != ZERO_OK || numel == 0)
+        return rc;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if (!p_lp)
+        return launch_update<kNoLowP>(bits, server_scales, S, numel, p, m, v, nullptr, ws, st);
+    if (pdtype == ZERO_BF16)
+        return launch_update<ZERO_BF16>(bits, server_scales, S, numel, p, m, v, p_lp, ws, st);
+    return launch_update<ZERO_F16>(bits, server_scales, S, numel, p, m, v, p_lp, ws, st);
+}

@@ -643,9 +643,7 @@ int check_step_args(const zero_tlist_t *grads, const zero_tlist_t *master, const
         return ZERO_EALIGN;
     if (!device_ptr(d_state))
         return ZERO_EINVAL;
-    if (!(hp->lr >= 0.0) || !(hp->beta1 >= 0.0 && hp->beta1 < 1.0) || !(hp->beta2 >= 0.0 && hp->beta2 < 1.0) ||
-        !(hp->eps >= 0.0) || !(hp->weight_decay >= 0.0) || !(hp->min_scale >= 1.0) || hp->scale_window < 1 ||
-        hp->max_norm != hp->max_norm)
+    if (!hparams_ok(hp))
         return ZERO_EINVAL;
     int64_t t2 = 0;
     int rc = check_list(grads, total);
@@ -706,19 +704,7 @@ int run_step(const zero_tlist_t *grads, const zero_tlist_t *master, const zero_t
         decide_pdl = false;  // a copy now precedes the decision kernel
     }
     StepScalars *sc = reinterpret_cast<StepScalars *>(static_cast<unsigned char *>(ws) + kWsScalars);
-    DecideArgs a;
-    a.lr = hp->lr;
-    a.beta1 = hp->beta1;
-    a.beta2 = hp->beta2;
-    a.max_norm = hp->max_norm;
-    a.min_scale = hp->min_scale;
-    a.scale_window = hp->scale_window;
-    a.b1 = (float)hp->beta1;
-    a.omb1 = (float)(1.0 - hp->beta1);
-    a.b2 = (float)hp->beta2;
-    a.omb2 = (float)(1.0 - hp->beta2);
-    a.eps = (float)hp->eps;
-    a.lrwd = (float)(hp->lr * hp->weight_decay);
+    const DecideArgs a = decide_args(hp);
     const PowCache *cache = reinterpret_cast<const PowCache *>(static_cast<unsigned char *>(ws) + kWsPowCache);
     launch_k(k_decide, 1, 32, s, decide_pdl, d_state, sc, cache, a);
     if ((rc = check_launch("zero_adam_step (decision)")) != ZERO_OK)
