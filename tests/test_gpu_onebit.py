@@ -285,6 +285,7 @@ def test_onebit_argument_errors(zp):
     with pytest.raises(zp.ZeroError) as e:  # freeze step must be a step count
         zp.zero_onebit_worker(g, f, f.clone(), bits, torch.zeros(1, device=dev), zp.HParams(), 0, st, ws)
     assert e.value.code == -1
+    big = torch.zeros(256, device=dev)
     with pytest.raises(zp.ZeroError) as e:  # numel past nd * S
-        zp.zero_onebit_update(bits, torch.ones(1, device=dev), 128, 129, f, f.clone(), f.clone(), None, ws)
+        zp.zero_onebit_update(bits, torch.ones(1, device=dev), 128, 129, big, big.clone(), big.clone(), None, ws)
     assert e.value.code == -4
