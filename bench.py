@@ -695,7 +695,9 @@ def run_onebit(args):
     momentum + error feedback -> signs and a scale), the server compression
     of chunk 0 from the 16 workers' signs (the other 15 are received
     messages), and the update from the 16 servers' signs with the frozen
-    variance."""
+    variance.  The synchronised momentum stays in its compressed form
+    between steps (the previous servers' signs and scales): the worker reads
+    it from there and the update writes no dense copy."""
     import torch
 
     import zero_partitioned_mixed_layout_gb300 as zp
@@ -707,7 +709,6 @@ def run_onebit(args):
     numel, n = sum(numel_list), nd * S
     g = torch.empty(n, dtype=torch.float16, device=dev)
     zs.device_grad_into(g, 40, 0, 65536.0)
-    m = zs.device_normal(n, 1e-3, 41, "misc", 1)
     v = zs.device_normal(n, 1e-3, 41, "misc", 2).square_()
     p = zs.device_normal(n, 0.02, 41, "master")
     plp = p.half()
@@ -732,13 +733,16 @@ def run_onebit(args):
         if ev:
             ev[0].record(stream)
         zp.zero_grad_norm_overflow(g, state, ws, stream=stream)
-        zp.zero_onebit_worker(g, m, e_w, bits, wscale[0:1], hp, 1000, state, ws, stream=stream)
+        # the momentum: last step's server signs and scales (chunk 0 from this
+        # rank's server, the rest received), read before this step's server
+        # overwrites chunk 0
+        zp.zero_onebit_worker(g, (sbits, sscale), e_w, bits, wscale[0:1], hp, 1000, state, ws, stream=stream)
         if ev:
             ev[1].record(stream)
         zp.zero_onebit_server(wlist, wscale, e_s, sbits[:S // 32], sscale[0:1], ws, stream=stream)
         if ev:
             ev[2].record(stream)
-        zp.zero_onebit_update(sbits, sscale, S, numel, p, m, v, plp, ws, stream=stream)
+        zp.zero_onebit_update(sbits, sscale, S, numel, p, None, v, plp, ws, stream=stream)
         if ev:
             ev[3].record(stream)
 
@@ -760,10 +764,10 @@ def run_onebit(args):
     assert st["last_skipped"] == 0 and st["step"] == 1000 + 2 * args.steps + args.warmup
     dt = e0.elapsed_time(e1) / args.steps * 1e-3
     ms = [statistics.mean(ev[k].elapsed_time(ev[k + 1]) for ev in evs) for k in range(3)]
-    # bytes per element of the padded buffer
-    b_worker = 2 + 14 + 8 + 1 / 8                  # pass 1, worker, signs
+    # bytes per element of the padded buffer (the momentum read as signs: 1/8)
+    b_worker = 2 + (2 + 1 / 8 + 8) + 8 + 1 / 8     # pass 1, worker, signs
     b_server = (nd / 8 + 16 + 1 / 8) / nd            # per element of the whole buffer
-    b_update = 1 / 8 + 12 + 4 + 2
+    b_update = 1 / 8 + 8 + 4 + 2                     # signs, v and p; p and p_lp
     b_step = b_worker + b_server + b_update
     peaks = measured_peaks()
     peak = peaks["hbm_gbs"] if peaks else 6800.0

@@ -412,26 +412,34 @@ int zero_gather_plan(const int64_t *numel, int64_t n_tensors, const int64_t *lay
  * (ZERO_ESIZE); arrays 16-byte aligned.  Errors otherwise as
  * zero_adam_step. */
 
-/* Worker side.  grad: n elements (F16, BF16 or F32); m: the synchronised
- * momentum (fp32, read); e_w: the worker error (fp32, updated); bits: n/32
- * words (written); scale: one device float (written).  freeze_step: T_w,
- * the count of the last warm-up step (>= 1). */
-int zero_onebit_worker(const void *grad, int32_t gdtype, const float *m, float *e_w, int64_t n, uint32_t *bits,
-                       float *scale, const zero_hparams_t *hp, int64_t freeze_step, zero_state_t *d_state, void *ws,
+/* Worker side.  grad: n elements (F16, BF16 or F32).  The synchronised
+ * momentum comes either dense, m (fp32, n elements, read), or -- with m
+ * NULL -- compressed, as the previous step's servers left it: m_bits (n/32
+ * words) and m_scales (n/S floats), element i being +-m_scales[i / S] (S a
+ * multiple of 32 dividing n; ignored when m is given).  After the first
+ * compression step the compressed form is exact and saves the 4 bytes per
+ * element of a dense momentum on both the update's write and this read.
+ * e_w: the worker error (fp32, updated); bits: n/32 words (written); scale:
+ * one device float (written).  freeze_step: T_w, the count of the last
+ * warm-up step (>= 1). */
+int zero_onebit_worker(const void *grad, int32_t gdtype, const float *m, const uint32_t *m_bits,
+                       const float *m_scales, int64_t S, float *e_w, int64_t n, uint32_t *bits, float *scale,
+                       const zero_hparams_t *hp, int64_t freeze_step, zero_state_t *d_state, void *ws,
                        size_t ws_bytes, void *stream);
 
 /* Server side for this rank's chunk of S elements.  worker_bits: HOST array
  * of nd device pointers, each to S/32 words (the chunk's signs from worker
  * i); worker_scales: device array of nd floats; e_s: the server error (S
- * fp32, updated); bits: S/32 words and scale: one device float (written). */
+ * fp32, updated); bits: S/32 words and scale: one device float (written).
+ * At most 4096 workers (ZERO_ECAPACITY). */
 int zero_onebit_server(const uint32_t *const *worker_bits, const float *worker_scales, int32_t nd, int64_t S,
                        float *e_s, uint32_t *bits, float *scale, void *ws, size_t ws_bytes, void *stream);
 
 /* Update.  bits: nd*S/32 words, the servers' signs in rank order;
  * server_scales: device array of nd floats; p, m, v: fp32 arrays of at
- * least `numel` elements (p and m written, v read); p_lp: F16 or BF16
- * copy of p (or NULL).  Elements from `numel` to nd*S (padding) are not
- * touched. */
+ * least `numel` elements (p written, v read; m, the dense momentum, written
+ * if not NULL); p_lp: F16 or BF16 copy of p (or NULL).  Elements from
+ * `numel` to nd*S (padding) are not touched. */
 int zero_onebit_update(const uint32_t *bits, const float *server_scales, int32_t nd, int64_t S, int64_t numel,
                        float *p, float *m, const float *v, void *p_lp, int32_t pdtype, void *ws, size_t ws_bytes,
                        void *stream);

@@ -54,20 +54,24 @@ def pack(b):
     return np.packbits(b, bitorder="little").view(np.uint32)
 
 
-def run_gpu_step(zp, d, nd, S, numel, hp, T, pdtype):
-    """One compression-stage step of every rank on the device arrays in d."""
+def run_gpu_step(zp, d, nd, S, numel, hp, T, pdtype, compressed=False):
+    """One compression-stage step of every rank on the device arrays in d.
+    compressed: the workers read the momentum as the previous step's server
+    signs and scales, and the update leaves the dense m alone."""
     n = nd * S
     for i in range(nd):
         for k in range(nd):
             zp.zero_grad_norm_overflow(d["g"][k], d["state"][i], d["ws"][i], accumulate=k > 0)
+    mom = (d["sbits"].clone(), d["sscale"].clone()) if compressed else d["m"]
     for i in range(nd):
-        zp.zero_onebit_worker(d["g"][i], d["m"], d["ew"][i], d["wbits"][i], d["wscale"][i:i + 1], hp, T,
+        zp.zero_onebit_worker(d["g"][i], mom, d["ew"][i], d["wbits"][i], d["wscale"][i:i + 1], hp, T,
                               d["state"][i], d["ws"][i])
     w = S // 32
     for j in range(nd):
         zp.zero_onebit_server([d["wbits"][i][j * w:(j + 1) * w] for i in range(nd)], d["wscale"], d["es"][j],
                               d["sbits"][j * w:(j + 1) * w], d["sscale"][j:j + 1], d["ws"][j])
-    zp.zero_onebit_update(d["sbits"], d["sscale"], S, numel, d["p"], d["m"], d["v"], d["plp"], d["ws"][0])
+    zp.zero_onebit_update(d["sbits"], d["sscale"], S, numel, d["p"], None if compressed else d["m"], d["v"],
+                          d["plp"], d["ws"][0])
     torch.cuda.synchronize()
     assert n == d["p"].numel()
 
@@ -104,8 +108,9 @@ def setup(zp, nd, S, gdtype, pdtype, seed, loss_scale, T, inf_at=None):
     return h, d
 
 
-def check_step(zp, h, d, nd, S, numel, gdtype, pdtype, hp, sc, T):
-    """Runs the oracle's step with the GPU's scales and compares everything."""
+def check_step(zp, h, d, nd, S, numel, gdtype, pdtype, hp, sc, T, dense_m=True):
+    """Runs the oracle's step with the GPU's scales and compares everything
+    (the dense m only when the GPU wrote it)."""
     ew0 = [e.copy() for e in h["ew"]]
     # the scales the oracle computes itself agree with the GPU's closely
     free = oracle.onebit_step(h["g"], gdtype, S, numel, h["p"].copy(), h["m"].copy(), h["v"],
@@ -132,7 +137,8 @@ def check_step(zp, h, d, nd, S, numel, gdtype, pdtype, hp, sc, T):
         assert to_host(d["es"][j]).tobytes() == h["es"][j].tobytes(), f"server {j} error"
     assert np.array_equal(words(d["sbits"]), np.concatenate(res.server_bits))
     assert to_host(d["p"]).tobytes() == h["p"].tobytes(), "master"
-    assert to_host(d["m"]).tobytes() == h["m"].tobytes(), "momentum"
+    if dense_m:
+        assert to_host(d["m"]).tobytes() == h["m"].tobytes(), "momentum"
     if pdtype:
         assert np.array_equal(to_host(d["plp"]), h["plp"]), "low-precision params"
     assert any((e != e0).any() for e, e0 in zip(h["ew"], ew0))
@@ -165,6 +171,30 @@ def test_onebit_three_steps_with_clipping(zp):
         run_gpu_step(zp, d, nd, S, nd * S, zhp, T, "f16")
         res = check_step(zp, h, d, nd, S, nd * S, "f16", "f16", hp, sc, T)
         assert res.step.scalars["clip"] < 1.0
+
+
+@pytest.mark.parametrize("nd,S", [(1, 1024), (4, 8192), (16, 2048)])
+def test_onebit_compressed_momentum(zp, nd, S):
+    """Step 1 from the dense warm-up momentum; steps 2 and 3 read the
+    momentum as the previous servers' signs and scales (the update writes no
+    dense m): the same results as the oracle's dense momentum, which after a
+    compression step is exactly +-scale."""
+    T = 60
+    h, d = setup(zp, nd, S, "f16", "f16", 300 + nd, 1024.0, T)
+    n = nd * S
+    hp, zhp = oracle.HParams(), zp.HParams()
+    sc = oracle.Scaler(1024.0, T)
+    for step in range(3):
+        for i in range(nd):
+            h["g"][i] = zs.host_grad(n, 700 + 10 * step + i, step, 1024.0, "f16")
+            d["g"][i] = to_dev(h["g"][i], "f16")
+        run_gpu_step(zp, d, nd, S, n - 5, zhp, T, "f16", compressed=step > 0)
+        check_step(zp, h, d, nd, S, n - 5, "f16", "f16", hp, sc, T, dense_m=step == 0)
+    # the compressed momentum the GPU holds is the oracle's dense one
+    sb, ss = words(d["sbits"]), d["sscale"].cpu().numpy()
+    idx = np.arange(n - 5)
+    dense = np.where(bit_at(sb, idx) == 1, ss[idx // S], -ss[idx // S]).astype(np.float32)
+    assert dense.tobytes() == h["m"][:n - 5].tobytes()
 
 
 def test_onebit_overflow_skips_everything(zp):

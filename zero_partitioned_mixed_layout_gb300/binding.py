@@ -448,8 +448,8 @@ def _onebit_lib():
     so = lib()
     if not getattr(so, "_onebit_ready", False):
         vp, i64, i32 = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int32
-        so.zero_onebit_worker.argtypes = [vp, i32, vp, vp, i64, vp, vp, ctypes.POINTER(_HParams), i64, vp,
-                                          vp, ctypes.c_size_t, vp]
+        so.zero_onebit_worker.argtypes = [vp, i32, vp, vp, vp, i64, vp, i64, vp, vp, ctypes.POINTER(_HParams),
+                                          i64, vp, vp, ctypes.c_size_t, vp]
         so.zero_onebit_server.argtypes = [ctypes.POINTER(vp), vp, i32, i64, vp, vp, vp, vp, ctypes.c_size_t,
                                           vp]
         so.zero_onebit_update.argtypes = [vp, vp, i32, i64, i64, vp, vp, vp, vp, i32, vp, ctypes.c_size_t,
@@ -485,15 +485,26 @@ def zero_onebit_worker(grad, m, e_w, bits, scale, hp: HParams, freeze_step: int,
                        stream=None) -> None:
     """1-bit Adam, worker side: the decision (variance frozen at step
     freeze_step), then x = b1*m + (1-b1)*g + e_w compressed to signs (bits,
-    int32[n/32]) and one scale (float32[1]); e_w updated."""
+    int32[n/32]) and one scale (float32[1]); e_w updated.  m is the dense
+    momentum (float32[n]) or the compressed one, a tuple (signs int32[n/32],
+    scales float32[Nd]) from the previous step's servers."""
     n = grad.numel()
     _device_tensor(grad, "grad")
-    _f32_tensor(m, "m", n), _f32_tensor(e_w, "e_w", n), _f32_tensor(scale, "scale", 1)
+    _f32_tensor(e_w, "e_w", n), _f32_tensor(scale, "scale", 1)
     _words_tensor(bits, "bits", n // 32)
     _device_tensor(state, "state"), _device_tensor(ws, "workspace")
+    if isinstance(m, (tuple, list)):
+        mb, ms = m
+        _words_tensor(mb, "momentum signs", n // 32), _f32_tensor(ms, "momentum scales")
+        if n % ms.numel() != 0:
+            raise ValueError("momentum scales must split n into equal chunks")
+        dense, mbp, msp, chunk = None, ctypes.c_void_p(mb.data_ptr()), ctypes.c_void_p(ms.data_ptr()), n // ms.numel()
+    else:
+        _f32_tensor(m, "m", n)
+        dense, mbp, msp, chunk = ctypes.c_void_p(m.data_ptr()), None, None, 0
     h = hp._c()
     rc = _onebit_lib().zero_onebit_worker(
-        ctypes.c_void_p(grad.data_ptr()), _dtype_code(grad), ctypes.c_void_p(m.data_ptr()),
+        ctypes.c_void_p(grad.data_ptr()), _dtype_code(grad), dense, mbp, msp, chunk,
         ctypes.c_void_p(e_w.data_ptr()), n, ctypes.c_void_p(bits.data_ptr()),
         ctypes.c_void_p(scale.data_ptr()), ctypes.byref(h), int(freeze_step),
         ctypes.c_void_p(state.data_ptr()), ctypes.c_void_p(ws.data_ptr()), ws.numel(),
@@ -520,10 +531,13 @@ def zero_onebit_server(worker_bits, worker_scales, e_s, bits, scale, ws, stream=
 def zero_onebit_update(bits, server_scales, S: int, numel: int, p, m, v, p_lp, ws, stream=None) -> None:
     """1-bit Adam, every worker: m = the servers' signs times their scales
     (chunk j of S elements from server j), and p updated with the frozen v,
-    for the first numel elements; p_lp (fp16/bf16) follows p if given."""
+    for the first numel elements; p_lp (fp16/bf16) follows p if given; m may
+    be None (the momentum then lives on in its compressed form only)."""
     nd = server_scales.numel()
     _words_tensor(bits, "bits", nd * S // 32), _f32_tensor(server_scales, "server_scales")
     for t, name in ((p, "p"), (m, "m"), (v, "v")):
+        if t is None and name == "m":
+            continue
         _f32_tensor(t, name)
         if t.numel() < numel:
             raise ValueError(f"{name} holds fewer than numel elements")
@@ -534,7 +548,8 @@ def zero_onebit_update(bits, server_scales, S: int, numel: int, p, m, v, p_lp, w
     _device_tensor(ws, "workspace")
     rc = _onebit_lib().zero_onebit_update(
         ctypes.c_void_p(bits.data_ptr()), ctypes.c_void_p(server_scales.data_ptr()), nd, int(S), int(numel),
-        ctypes.c_void_p(p.data_ptr()), ctypes.c_void_p(m.data_ptr()), ctypes.c_void_p(v.data_ptr()), lp, code,
+        ctypes.c_void_p(p.data_ptr()), None if m is None else ctypes.c_void_p(m.data_ptr()),
+        ctypes.c_void_p(v.data_ptr()), lp, code,
         ctypes.c_void_p(ws.data_ptr()), ws.numel(), _stream_ptr(stream, ws.device))
     _check(rc, "zero_onebit_update")
 

@@ -41,8 +41,9 @@ __device__ __forceinline__ void st8(float *p, const float *f)
 
 // End of a squared-norm pass: publish this block's partial; the block that
 // takes the last ticket sums the partials in block order and writes the
-// compressor's scale sqrt(sum / len), rounded once to binary32.
-__device__ void scale_finish(double tot, double2 *partials, WsHeader *hdr, int64_t len, float *scale)
+// compressor's scale sqrt(sum / len), rounded once to binary32 (not on a
+// skipped step, whose blocks still pass here to keep the ticket in step).
+__device__ void scale_finish(double tot, double2 *partials, WsHeader *hdr, int64_t len, float *scale, bool skip)
 {
     __shared__ bool s_last;
     uint32_t none = 0;
@@ -61,7 +62,8 @@ __device__ void scale_finish(double tot, double2 *partials, WsHeader *hdr, int64
         t += __ldcg(partials + j).x;
     block_reduce(t, none);
     if (threadIdx.x == 0) {
-        *scale = (float)sqrt(t / (double)len);
+        if (!skip)
+            *scale = (float)sqrt(t / (double)len);
         hdr->ticket = 0u;
     }
 }
@@ -88,21 +90,50 @@ struct SquareSum {
     __device__ __forceinline__ double total() const { return tot + (double)part; }
 };
 
+// The skip flag of these kernels comes from device memory.  They do not
+// return early on it: a data-dependent exit ahead of the block barriers of
+// the reduction cost a third of the streaming rate of the loop on GB300 (the
+// same loop with the flag as a kernel argument, or folded into the loop
+// bound as here, runs at the copy rate).  A skipped step runs no
+// iterations and writes nothing.
+
+// The synchronised momentum of one 8-element group: dense (fp32 array) or
+// compressed (the previous step's server signs and per-chunk scales, the
+// form the update produces: every element is +-scale of its chunk).
+struct Momentum {
+    const float *dense;    // or NULL
+    const uint32_t *bits;  // compressed form
+    const float *scales;
+    int64_t chunk;         // S
+};
+
+template <bool kCompressed>
+__device__ __forceinline__ void load_momentum(const Momentum &mm, int64_t i, float *f)
+{
+    if constexpr (kCompressed) {
+        const uint32_t byte = (__ldg(mm.bits + (i >> 2)) >> (8 * (i & 3))) & 0xFFu;
+        const float sc = __ldg(mm.scales + (8 * i) / mm.chunk);
+#pragma unroll
+        for (int k = 0; k < 8; ++k)
+            f[k] = ((byte >> k) & 1u) ? sc : -sc;
+    } else {
+        ld8(mm.dense + 8 * i, f);
+    }
+}
+
 // Worker, first pass: x = b1*m + (1-b1)*g + e (g unscaled, clipped), stored
 // over e; the squared norm of x into the scale.
-template <int GT>
-__global__ void __launch_bounds__(kThreads) k_onebit_worker(const void *g, const float *m, float *e, int64_t n,
+template <int GT, bool kCompressed>
+__global__ void __launch_bounds__(kThreads) k_onebit_worker(const void *g, Momentum mm, float *e, int64_t n,
                                                             const StepScalars *scp, double2 *partials,
                                                             WsHeader *hdr, float *scale)
 {
     pdl_wait();
     const StepScalars s = *scp;
-    if (s.skip)
-        return;
     constexpr int W = Elem<GT>::kWords;
     const uint4 *gv = static_cast<const uint4 *>(g);
     SquareSum acc;
-    const int64_t nv = n >> 3;
+    const int64_t nv = s.skip ? 0 : n >> 3;
     for (int64_t i = (int64_t)blockIdx.x * kThreads + threadIdx.x; i < nv; i += (int64_t)gridDim.x * kThreads) {
         uint4 w[W];
 #pragma unroll
@@ -110,7 +141,7 @@ __global__ void __launch_bounds__(kThreads) k_onebit_worker(const void *g, const
             w[q] = __ldcs(gv + i * W + q);
         float gf[8], mf[8], x[8];
         Elem<GT>::to_float(w, gf);
-        ld8(m + 8 * i, mf);
+        load_momentum<kCompressed>(mm, i, mf);
         ld8(e + 8 * i, x);
 #pragma unroll
         for (int k = 0; k < 8; ++k) {
@@ -121,30 +152,54 @@ __global__ void __launch_bounds__(kThreads) k_onebit_worker(const void *g, const
         st8(e + 8 * i, x);
         acc.add(x);
     }
-    scale_finish(acc.total(), partials, hdr, n, scale);
+    scale_finish(acc.total(), partials, hdr, n, scale, s.skip != 0);
 }
 
 // Server, first pass over the chunk: y = (sum over workers in rank order of
 // +-scale_k) / Nd + f, stored over f; the squared norm of y into the scale.
+// The workers' sign pointers and scales sit in shared memory; each thread
+// loads the words of 8 workers before it adds them in.
+constexpr int kServerBatch = 8;
+// Workers per server call: their pointers and scales (12 bytes each) fit the
+// default 48 KiB of dynamic shared memory.
+constexpr int kMaxServerWorkers = 4096;
+
 __global__ void __launch_bounds__(kThreads) k_onebit_server(const uint32_t *const *wbits, const float *wscales,
                                                             int nd, float *f, int64_t S, const StepScalars *scp,
                                                             double2 *partials, WsHeader *hdr, float *scale)
 {
+    extern __shared__ unsigned char s_raw[];
+    const uint32_t **s_ptr = reinterpret_cast<const uint32_t **>(s_raw);
+    float *s_scale = reinterpret_cast<float *>(s_raw + sizeof(void *) * (size_t)nd);
     pdl_wait();
-    if (scp->skip)
-        return;
+    for (int k = threadIdx.x; k < nd; k += kThreads) {
+        s_ptr[k] = wbits[k];
+        s_scale[k] = wscales[k];
+    }
+    __syncthreads();
+    const bool skip = scp->skip != 0;
     const float count = (float)nd;
     SquareSum acc;
-    const int64_t nv = S >> 3;
+    const int64_t nv = skip ? 0 : S >> 3;
     for (int64_t i = (int64_t)blockIdx.x * kThreads + threadIdx.x; i < nv; i += (int64_t)gridDim.x * kThreads) {
         float a[8];
-        for (int k = 0; k < nd; ++k) {
-            const uint32_t byte = (__ldg(wbits[k] + (i >> 2)) >> (8 * (i & 3))) & 0xFFu;
-            const float sc = __ldg(wscales + k);
+        const int shift = 8 * (int)(i & 3);
+        for (int k0 = 0; k0 < nd; k0 += kServerBatch) {
+            uint32_t w[kServerBatch];
 #pragma unroll
-            for (int j = 0; j < 8; ++j) {
-                const float c = ((byte >> j) & 1u) ? sc : -sc;
-                a[j] = k == 0 ? c : __fadd_rn(a[j], c);
+            for (int q = 0; q < kServerBatch; ++q)
+                w[q] = k0 + q < nd ? __ldg(s_ptr[k0 + q] + (i >> 2)) : 0u;
+#pragma unroll
+            for (int q = 0; q < kServerBatch; ++q) {
+                if (k0 + q < nd) {
+                    const uint32_t byte = (w[q] >> shift) & 0xFFu;
+                    const float sc = s_scale[k0 + q];
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) {
+                        const float c = ((byte >> j) & 1u) ? sc : -sc;
+                        a[j] = k0 + q == 0 ? c : __fadd_rn(a[j], c);
+                    }
+                }
             }
         }
         float y[8];
@@ -155,7 +210,7 @@ __global__ void __launch_bounds__(kThreads) k_onebit_server(const uint32_t *cons
         st8(f + 8 * i, y);
         acc.add(y);
     }
-    scale_finish(acc.total(), partials, hdr, S, scale);
+    scale_finish(acc.total(), partials, hdr, S, scale, skip);
 }
 
 // Second pass of a compression (worker or server): the signs of x, 32 to a
@@ -165,11 +220,9 @@ __global__ void __launch_bounds__(kThreads) k_onebit_sign(float *x, int64_t n, c
                                                           const StepScalars *scp)
 {
     pdl_wait();
-    if (scp->skip)
-        return;
     const float sc = *scale;
     const int64_t i = (int64_t)blockIdx.x * kThreads + threadIdx.x;
-    const int64_t nv = n >> 3;
+    const int64_t nv = scp->skip ? 0 : n >> 3;
     uint32_t byte = 0;
     if (i < nv) {
         float v[8];
@@ -201,17 +254,17 @@ __device__ __forceinline__ void onebit_elem(float mi, float vi, float &p, const 
 constexpr int kNoLowP = -1;
 
 // The update: one 8-element group per thread (one-shot grid); the last
-// thread takes the elements past the last whole group.
+// thread takes the elements past the last whole group.  m (the dense
+// momentum) is written only when given: the next worker can read the
+// momentum in its compressed form instead.
 template <int PT>
 __global__ void __launch_bounds__(kThreads) k_onebit_update(const uint32_t *bits, const float *scales, int64_t S,
                                                             int64_t numel, float *p, float *m, const float *v,
                                                             void *plp, const StepScalars *scp)
 {
     const StepScalars s = *scp;
-    if (s.skip)
-        return;
     const int64_t i = (int64_t)blockIdx.x * kThreads + threadIdx.x;
-    const int64_t nfull = numel >> 3;
+    const int64_t nfull = s.skip ? -1 : numel >> 3;
     if (i < nfull) {
         const uint32_t byte = (__ldg(bits + (i >> 2)) >> (8 * (i & 3))) & 0xFFu;
         const float sc = __ldg(scales + (8 * i) / S);
@@ -223,7 +276,8 @@ __global__ void __launch_bounds__(kThreads) k_onebit_update(const uint32_t *bits
             mf[k] = ((byte >> k) & 1u) ? sc : -sc;
             onebit_elem(mf[k], vf[k], pf[k], s);
         }
-        st8(m + 8 * i, mf);
+        if (m)
+            st8(m + 8 * i, mf);
         st8(p + 8 * i, pf);
         if constexpr (PT != kNoLowP)
             __stcs(reinterpret_cast<uint4 *>(plp) + i, LowP<PT>::pack(pf));
@@ -234,7 +288,8 @@ __global__ void __launch_bounds__(kThreads) k_onebit_update(const uint32_t *bits
             float pj = p[j];
             onebit_elem(mi, v[j], pj, s);
             p[j] = pj;
-            m[j] = mi;
+            if (m)
+                m[j] = mi;
             if constexpr (PT != kNoLowP)
                 LowP<PT>::store(plp, j, pj);
         }
@@ -261,8 +316,8 @@ StepScalars *step_scalars(void *ws)
     return reinterpret_cast<StepScalars *>(static_cast<unsigned char *>(ws) + kWsScalars);
 }
 
-template <int GT>
-int launch_worker(const void *g, const float *m, float *e, int64_t n, uint32_t *bits, float *scale, void *ws,
+template <int GT, bool kCompressed>
+int launch_worker(const void *g, const Momentum &mm, float *e, int64_t n, uint32_t *bits, float *scale, void *ws,
                   cudaStream_t st)
 {
     unsigned char *w = static_cast<unsigned char *>(ws);
@@ -270,14 +325,23 @@ int launch_worker(const void *g, const float *m, float *e, int64_t n, uint32_t *
     double2 *partials = reinterpret_cast<double2 *>(w + kWsPartials);
     const StepScalars *sc = step_scalars(ws);
     const int64_t nv = n >> 3;
-    const int grid = grid_for((const void *)k_onebit_worker<GT>, (nv + kThreads - 1) / kThreads, kMaxBlocks, 4);
-    launch_k(k_onebit_worker<GT>, grid, kThreads, st, true, g, m, e, n, sc, partials, hdr, scale);
+    const int grid =
+        grid_for((const void *)k_onebit_worker<GT, kCompressed>, (nv + kThreads - 1) / kThreads, kMaxBlocks, 4);
+    launch_k(k_onebit_worker<GT, kCompressed>, grid, kThreads, st, true, g, mm, e, n, sc, partials, hdr, scale);
     int rc = check_launch("zero_onebit_worker (first pass)");
     if (rc != ZERO_OK)
         return rc;
     launch_k(k_onebit_sign, (int)((nv + kThreads - 1) / kThreads), kThreads, st, true, e, n, (const float *)scale,
              bits, sc);
     return check_launch("zero_onebit_worker (signs)");
+}
+
+template <int GT>
+int launch_worker_m(const void *g, const Momentum &mm, float *e, int64_t n, uint32_t *bits, float *scale, void *ws,
+                    cudaStream_t st)
+{
+    return mm.dense ? launch_worker<GT, false>(g, mm, e, n, bits, scale, ws, st)
+                    : launch_worker<GT, true>(g, mm, e, n, bits, scale, ws, st);
 }
 
 template <int PT>
@@ -295,8 +359,9 @@ int launch_update(const uint32_t *bits, const float *scales, int64_t S, int64_t 
 
 using namespace zpml;
 
-extern "C" int zero_onebit_worker(const void *grad, int32_t gdtype, const float *m, float *e_w, int64_t n,
-                                  uint32_t *bits, float *scale, const zero_hparams_t *hp, int64_t freeze_step,
+extern "C" int zero_onebit_worker(const void *grad, int32_t gdtype, const float *m, const uint32_t *m_bits,
+                                  const float *m_scales, int64_t S, float *e_w, int64_t n, uint32_t *bits,
+                                  float *scale, const zero_hparams_t *hp, int64_t freeze_step,
                                   zero_state_t *d_state, void *ws, size_t ws_bytes, void *stream)
 {
     if (!hp || !d_state || n < 0 || freeze_step < 1 || !hparams_ok(hp))
@@ -307,13 +372,30 @@ extern "C" int zero_onebit_worker(const void *grad, int32_t gdtype, const float 
         return ZERO_ESIZE;
     if ((reinterpret_cast<uintptr_t>(d_state) & 7u) != 0)
         return ZERO_EALIGN;
+    Momentum mm = {m, m_bits, m_scales, S};
     if (n > 0) {
-        if (!grad || !m || !e_w || !bits || !scale)
+        if (!grad || !e_w || !bits || !scale)
             return ZERO_EINVAL;
-        if (!aligned16(grad) || !aligned16(m) || !aligned16(e_w) || !aligned4(bits) || !aligned4(scale))
+        if (!aligned16(grad) || !aligned16(e_w) || !aligned4(bits) || !aligned4(scale))
             return ZERO_EALIGN;
-        if (!device_ptr(grad) || !device_ptr(m) || !device_ptr(e_w) || !device_ptr(bits) || !device_ptr(scale))
+        if (!device_ptr(grad) || !device_ptr(e_w) || !device_ptr(bits) || !device_ptr(scale))
             return ZERO_EINVAL;
+        if (m) {
+            if (!aligned16(m))
+                return ZERO_EALIGN;
+            if (!device_ptr(m))
+                return ZERO_EINVAL;
+        } else {
+            // the compressed momentum: S-element chunks, one scale each
+            if (!m_bits || !m_scales || S <= 0)
+                return ZERO_EINVAL;
+            if (S % 32 != 0 || n % S != 0)
+                return ZERO_ESIZE;
+            if (!aligned4(m_bits) || !aligned4(m_scales))
+                return ZERO_EALIGN;
+            if (!device_ptr(m_bits) || !device_ptr(m_scales))
+                return ZERO_EINVAL;
+        }
     }
     if (!device_ptr(d_state))
         return ZERO_EINVAL;
@@ -327,9 +409,9 @@ extern "C" int zero_onebit_worker(const void *grad, int32_t gdtype, const float 
     if ((rc = check_launch("zero_onebit_worker (decision)")) != ZERO_OK || n == 0)
         return rc;
     switch (gdtype) {
-    case ZERO_F16: return launch_worker<ZERO_F16>(grad, m, e_w, n, bits, scale, ws, st);
-    case ZERO_BF16: return launch_worker<ZERO_BF16>(grad, m, e_w, n, bits, scale, ws, st);
-    default: return launch_worker<ZERO_F32>(grad, m, e_w, n, bits, scale, ws, st);
+    case ZERO_F16: return launch_worker_m<ZERO_F16>(grad, mm, e_w, n, bits, scale, ws, st);
+    case ZERO_BF16: return launch_worker_m<ZERO_BF16>(grad, mm, e_w, n, bits, scale, ws, st);
+    default: return launch_worker_m<ZERO_F32>(grad, mm, e_w, n, bits, scale, ws, st);
     }
 }
 
@@ -339,6 +421,8 @@ extern "C" int zero_onebit_server(const uint32_t *const *worker_bits, const floa
 {
     if (nd < 1 || S < 0 || !worker_bits || !worker_scales)
         return ZERO_EINVAL;
+    if (nd > kMaxServerWorkers)
+        return ZERO_ECAPACITY;
     if (S % 32 != 0 || (S >> 3) / kThreads >= 0x7fffffff)
         return ZERO_ESIZE;
     for (int32_t k = 0; k < nd; ++k) {
@@ -373,9 +457,13 @@ extern "C" int zero_onebit_server(const uint32_t *const *worker_bits, const floa
     const StepScalars *sc = step_scalars(ws);
     const int64_t nv = S >> 3;
     const int grid = grid_for((const void *)k_onebit_server, (nv + kThreads - 1) / kThreads, kMaxBlocks, 4);
-    launch_k(k_onebit_server, grid, kThreads, st, false, (const uint32_t *const *)(w + kWsTable), worker_scales,
-             (int)nd, e_s, S, sc, reinterpret_cast<double2 *>(w + kWsPartials), reinterpret_cast<WsHeader *>(w),
-             scale);
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)grid);
+    cfg.blockDim = dim3((unsigned)kThreads);
+    cfg.dynamicSmemBytes = (size_t)nd * (sizeof(void *) + sizeof(float));
+    cfg.stream = st;
+    cudaLaunchKernelEx(&cfg, k_onebit_server, (const uint32_t *const *)(w + kWsTable), worker_scales, (int)nd, e_s,
+                       S, sc, reinterpret_cast<double2 *>(w + kWsPartials), reinterpret_cast<WsHeader *>(w), scale);
     if ((rc = check_launch("zero_onebit_server (first pass)")) != ZERO_OK)
         return rc;
     launch_k(k_onebit_sign, (int)((nv + kThreads - 1) / kThreads), kThreads, st, true, e_s, S, (const float *)scale,
@@ -394,13 +482,13 @@ extern "C" int zero_onebit_update(const uint32_t *bits, const float *server_scal
     if (p_lp && !lp_dtype_ok(pdtype))
         return ZERO_EDTYPE;
     if (numel > 0) {
-        if (!bits || !p || !m || !v)
+        if (!bits || !p || !v)
             return ZERO_EINVAL;
-        if (!aligned4(bits) || !aligned4(server_scales) || !aligned16(p) || !aligned16(m) || !aligned16(v) ||
+        if (!aligned4(bits) || !aligned4(server_scales) || !aligned16(p) || (m && !aligned16(m)) || !aligned16(v) ||
             (p_lp && !aligned16(p_lp)))
             return ZERO_EALIGN;
-        if (!device_ptr(bits) || !device_ptr(server_scales) || !device_ptr(p) || !device_ptr(m) || !device_ptr(v) ||
-            (p_lp && !device_ptr(p_lp)))
+        if (!device_ptr(bits) || !device_ptr(server_scales) || !device_ptr(p) || (m && !device_ptr(m)) ||
+            !device_ptr(v) || (p_lp && !device_ptr(p_lp)))
             return ZERO_EINVAL;
     }
     int rc = check_ws_table(ws, ws_bytes, 0);
