@@ -436,10 +436,11 @@ int zero_onebit_server(const uint32_t *const *worker_bits, const float *worker_s
                        float *e_s, uint32_t *bits, float *scale, void *ws, size_t ws_bytes, void *stream);
 
 /* Update.  bits: nd*S/32 words, the servers' signs in rank order;
- * server_scales: device array of nd floats; p, m, v: fp32 arrays of at
- * least `numel` elements (p written, v read; m, the dense momentum, written
- * if not NULL); p_lp: F16 or BF16 copy of p (or NULL).  Elements from
- * `numel` to nd*S (padding) are not touched. */
+ * server_scales: device array of nd floats; m: the dense momentum, nd*S
+ * fp32 elements (the whole padded buffer, which the compressed all-reduce
+ * covers), written if not NULL; p, v: fp32 arrays of at least `numel`
+ * elements (p written, v read); p_lp: F16 or BF16 copy of p (or NULL).
+ * Parameters from `numel` to nd*S (padding) are not touched. */
 int zero_onebit_update(const uint32_t *bits, const float *server_scales, int32_t nd, int64_t S, int64_t numel,
                        float *p, float *m, const float *v, void *p_lp, int32_t pdtype, void *ws, size_t ws_bytes,
                        void *stream);

@@ -100,7 +100,7 @@ def load(path: str):
                                     ctypes.POINTER(f32), f32]
     so.zo_onebit_server.argtypes = [ctypes.POINTER(vp), vp, i32, i64, vp, vp, ctypes.POINTER(f32),
                                     f32, i32]
-    so.zo_onebit_update.argtypes = [vp, vp, i64, i64, vp, vp, vp, vp, ctypes.c_int,
+    so.zo_onebit_update.argtypes = [vp, vp, i64, i64, i64, vp, vp, vp, vp, ctypes.c_int,
                                     ctypes.POINTER(_Step)]
     for f in ("zo_f32_to_lp", "zo_lp_to_f32", "zo_accumulate", "zo_norm_overflow",
               "zo_decide", "zo_adam_apply", "zo_adam_apply_sampled", "zo_reduce_mean",
@@ -358,15 +358,18 @@ def onebit_update(bits: np.ndarray, scales: list[float], S: int, numel: int, p: 
                   m: np.ndarray, v: np.ndarray, p_lp: np.ndarray | None, pdtype: str,
                   step: Step) -> None:
     """Every worker: the synchronised momentum (the servers' signs, chunk j
-    scaled by scales[j]) into m, and the update of p with the frozen
-    variance v, for the first ``numel`` elements; in place."""
+    scaled by scales[j]) into m over the whole padded buffer of
+    len(scales) * S elements, and the update of p with the frozen variance
+    v for the first ``numel`` elements; in place."""
     b = np.ascontiguousarray(bits, dtype=np.uint32)
     sc = np.ascontiguousarray(scales, dtype=np.float32)
-    assert b.size * 32 >= numel and sc.size * S >= numel
-    for a in (p, m, v):
+    n = sc.size * S
+    assert b.size * 32 >= n and numel <= n
+    assert m.dtype == np.float32 and m.size >= n and m.flags["C_CONTIGUOUS"]
+    for a in (p, v):
         assert a.dtype == np.float32 and a.size >= numel and a.flags["C_CONTIGUOUS"]
     lp = None if p_lp is None else _bits(p_lp, pdtype)
-    lib().zo_onebit_update(_ptr(b), _ptr(sc), S, numel, _ptr(p), _ptr(m), _ptr(v), _ptr(lp),
+    lib().zo_onebit_update(_ptr(b), _ptr(sc), S, n, numel, _ptr(p), _ptr(m), _ptr(v), _ptr(lp),
                            DTYPES[pdtype], ctypes.byref(step._c))
 
 

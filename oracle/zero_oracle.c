@@ -408,21 +408,24 @@ void zo_onebit_server(const uint32_t *const *bits, const float *scales, int32_t 
 }
 
 /* Every worker: the synchronised momentum from the servers' signs (bits:
- * Nd*S/32 words, chunk j from rank j) and scales, then the parameter update
- * with the frozen variance, for the first `numel` elements (the rest of the
- * padded buffer is not parameters). */
-void zo_onebit_update(const uint32_t *bits, const float *scales, int64_t S, int64_t numel, float *p,
-                      float *m, const float *v, void *p_lp, int pdtype, const zo_step *s)
+ * n/32 words, n = Nd*S, chunk j from rank j) and scales over the whole
+ * padded buffer (the compressed all-reduce runs over all n elements), then
+ * the parameter update with the frozen variance for the first `numel`
+ * elements (the rest of the padded buffer is not parameters). */
+void zo_onebit_update(const uint32_t *bits, const float *scales, int64_t S, int64_t n, int64_t numel,
+                      float *p, float *m, const float *v, void *p_lp, int pdtype, const zo_step *s)
 {
     if (s->skip)
         return;
-    for (int64_t i = 0; i < numel; ++i) {
+    for (int64_t i = 0; i < n; ++i) {
         const float sc = scales[i / S];
         const float mi = ((bits[i / 32] >> (i % 32)) & 1u) ? sc : -sc;
+        m[i] = mi;
+        if (i >= numel)
+            continue;
         const float denom = sqrtf(v[i]) * s->inv_sqrt_bc2 + s->eps;
         const float u = mi / denom;
         p[i] = p[i] - (s->step_size * u + s->lr_wd * p[i]);
-        m[i] = mi;
         if (p_lp)
             store_lp(p_lp, pdtype, i, p[i]);
     }

@@ -192,9 +192,9 @@ def test_onebit_compressed_momentum(zp, nd, S):
         check_step(zp, h, d, nd, S, n - 5, "f16", "f16", hp, sc, T, dense_m=step == 0)
     # the compressed momentum the GPU holds is the oracle's dense one
     sb, ss = words(d["sbits"]), d["sscale"].cpu().numpy()
-    idx = np.arange(n - 5)
+    idx = np.arange(n)
     dense = np.where(bit_at(sb, idx) == 1, ss[idx // S], -ss[idx // S]).astype(np.float32)
-    assert dense.tobytes() == h["m"][:n - 5].tobytes()
+    assert dense.tobytes() == h["m"].tobytes()
 
 
 def test_onebit_overflow_skips_everything(zp):
@@ -280,7 +280,7 @@ def test_onebit_full_size_rank0_sampled(zp):
     assert to_host(es[tsi]).tobytes() == f[:sidx.size].tobytes()
     assert np.array_equal(bit_at(words(sbits[:S // 32]), sidx), bit_at(ob, np.arange(sidx.size)))
     # the update; the other chunks' signs and scales are messages
-    tail_p, tail_m = to_host(p[numel:]).copy(), to_host(m[numel:]).copy()
+    tail_p = to_host(p[numel:]).copy()
     zp.zero_onebit_update(sbits, sscale, S, numel, p, m, v, plp, ws)
     torch.cuda.synchronize()
     keep = idx < numel
@@ -295,9 +295,13 @@ def test_onebit_full_size_rank0_sampled(zp):
     assert to_host(p[tu]).tobytes() == hp_s.tobytes()
     assert to_host(m[tu]).tobytes() == hm_s.tobytes()
     assert np.array_equal(to_host(plp[tu]), oracle.to_lp(hp_s, "f16"))
-    # the padding past numel is not parameters: untouched
+    # the padding past numel is not parameters: untouched; the momentum
+    # covers the whole padded buffer
     assert to_host(p[numel:]).tobytes() == tail_p.tobytes()
-    assert to_host(m[numel:]).tobytes() == tail_m.tobytes()
+    tail = np.arange(numel, n)
+    sw, ss = words(sbits), sscale.cpu().numpy()
+    want_m = np.where(bit_at(sw, tail) == 1, ss[tail // S], -ss[tail // S]).astype(np.float32)
+    assert to_host(m[numel:]).tobytes() == want_m.tobytes()
 
 
 def test_onebit_argument_errors(zp):

@@ -535,12 +535,12 @@ def zero_onebit_update(bits, server_scales, S: int, numel: int, p, m, v, p_lp, w
     be None (the momentum then lives on in its compressed form only)."""
     nd = server_scales.numel()
     _words_tensor(bits, "bits", nd * S // 32), _f32_tensor(server_scales, "server_scales")
-    for t, name in ((p, "p"), (m, "m"), (v, "v")):
-        if t is None and name == "m":
-            continue
+    for t, name in ((p, "p"), (v, "v")):
         _f32_tensor(t, name)
         if t.numel() < numel:
             raise ValueError(f"{name} holds fewer than numel elements")
+    if m is not None:
+        _f32_tensor(m, "m", nd * S)
     lp, code = None, ZERO_F16
     if p_lp is not None:
         _device_tensor(p_lp, "p_lp")

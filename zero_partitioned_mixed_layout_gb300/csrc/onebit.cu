@@ -253,43 +253,44 @@ __device__ __forceinline__ void onebit_elem(float mi, float vi, float &p, const 
 
 constexpr int kNoLowP = -1;
 
-// The update: one 8-element group per thread (one-shot grid); the last
-// thread takes the elements past the last whole group.  m (the dense
-// momentum) is written only when given: the next worker can read the
-// momentum in its compressed form instead.
+// The update: one 8-element group per thread (one-shot grid) over the whole
+// padded buffer of n = Nd*S elements.  The momentum covers all of it; the
+// parameters only the first numel elements (the group that straddles numel
+// goes element by element).  m (the dense momentum) is written only when
+// given: the next worker can read the momentum in its compressed form.
 template <int PT>
 __global__ void __launch_bounds__(kThreads) k_onebit_update(const uint32_t *bits, const float *scales, int64_t S,
-                                                            int64_t numel, float *p, float *m, const float *v,
-                                                            void *plp, const StepScalars *scp)
+                                                            int64_t n, int64_t numel, float *p, float *m,
+                                                            const float *v, void *plp, const StepScalars *scp)
 {
     const StepScalars s = *scp;
     const int64_t i = (int64_t)blockIdx.x * kThreads + threadIdx.x;
-    const int64_t nfull = s.skip ? -1 : numel >> 3;
-    if (i < nfull) {
-        const uint32_t byte = (__ldg(bits + (i >> 2)) >> (8 * (i & 3))) & 0xFFu;
-        const float sc = __ldg(scales + (8 * i) / S);
-        float vf[8], pf[8], mf[8];
+    const int64_t nv = s.skip ? 0 : n >> 3;
+    if (i >= nv)
+        return;
+    const uint32_t byte = (__ldg(bits + (i >> 2)) >> (8 * (i & 3))) & 0xFFu;
+    const float sc = __ldg(scales + (8 * i) / S);
+    float mf[8];
+#pragma unroll
+    for (int k = 0; k < 8; ++k)
+        mf[k] = ((byte >> k) & 1u) ? sc : -sc;
+    if (m)
+        st8(m + 8 * i, mf);
+    if (8 * i + 8 <= numel) {
+        float vf[8], pf[8];
         ld8(v + 8 * i, vf);
         ld8(p + 8 * i, pf);
 #pragma unroll
-        for (int k = 0; k < 8; ++k) {
-            mf[k] = ((byte >> k) & 1u) ? sc : -sc;
+        for (int k = 0; k < 8; ++k)
             onebit_elem(mf[k], vf[k], pf[k], s);
-        }
-        if (m)
-            st8(m + 8 * i, mf);
         st8(p + 8 * i, pf);
         if constexpr (PT != kNoLowP)
             __stcs(reinterpret_cast<uint4 *>(plp) + i, LowP<PT>::pack(pf));
-    } else if (i == nfull) {
-        for (int64_t j = 8 * nfull; j < numel; ++j) {
-            const float sc = scales[j / S];
-            const float mi = ((bits[j >> 5] >> (j & 31)) & 1u) ? sc : -sc;
+    } else {
+        for (int64_t j = 8 * i; j < numel; ++j) {
             float pj = p[j];
-            onebit_elem(mi, v[j], pj, s);
+            onebit_elem(((byte >> (j - 8 * i)) & 1u) ? sc : -sc, v[j], pj, s);
             p[j] = pj;
-            if (m)
-                m[j] = mi;
             if constexpr (PT != kNoLowP)
                 LowP<PT>::store(plp, j, pj);
         }
@@ -345,12 +346,12 @@ int launch_worker_m(const void *g, const Momentum &mm, float *e, int64_t n, uint
 }
 
 template <int PT>
-int launch_update(const uint32_t *bits, const float *scales, int64_t S, int64_t numel, float *p, float *m,
-                  const float *v, void *plp, void *ws, cudaStream_t st)
+int launch_update(const uint32_t *bits, const float *scales, int64_t S, int64_t n, int64_t numel, float *p,
+                  float *m, const float *v, void *plp, void *ws, cudaStream_t st)
 {
-    const int64_t threads = (numel >> 3) + 1;
+    const int64_t threads = n >> 3;
     launch_k(k_onebit_update<PT>, (int)((threads + kThreads - 1) / kThreads), kThreads, st, false, bits, scales, S,
-             numel, p, m, v, plp, (const StepScalars *)step_scalars(ws));
+             n, numel, p, m, v, plp, (const StepScalars *)step_scalars(ws));
     return check_launch("zero_onebit_update");
 }
 
@@ -477,27 +478,35 @@ extern "C" int zero_onebit_update(const uint32_t *bits, const float *server_scal
 {
     if (nd < 1 || S < 0 || numel < 0 || !server_scales)
         return ZERO_EINVAL;
-    if (S % 32 != 0 || S > ((int64_t)1 << 62) / nd || numel > (int64_t)nd * S || (numel >> 3) / kThreads >= 0x7fffffff)
+    if (S % 32 != 0 || S > ((int64_t)1 << 62) / nd || numel > (int64_t)nd * S ||
+        (((int64_t)nd * S) >> 3) / kThreads >= 0x7fffffff)
         return ZERO_ESIZE;
     if (p_lp && !lp_dtype_ok(pdtype))
         return ZERO_EDTYPE;
-    if (numel > 0) {
-        if (!bits || !p || !v)
+    if ((int64_t)nd * S > 0) {
+        if (!bits)
             return ZERO_EINVAL;
-        if (!aligned4(bits) || !aligned4(server_scales) || !aligned16(p) || (m && !aligned16(m)) || !aligned16(v) ||
-            (p_lp && !aligned16(p_lp)))
+        if (!aligned4(bits) || !aligned4(server_scales) || (m && !aligned16(m)))
             return ZERO_EALIGN;
-        if (!device_ptr(bits) || !device_ptr(server_scales) || !device_ptr(p) || (m && !device_ptr(m)) ||
-            !device_ptr(v) || (p_lp && !device_ptr(p_lp)))
+        if (!device_ptr(bits) || !device_ptr(server_scales) || (m && !device_ptr(m)))
+            return ZERO_EINVAL;
+    }
+    if (numel > 0) {
+        if (!p || !v)
+            return ZERO_EINVAL;
+        if (!aligned16(p) || !aligned16(v) || (p_lp && !aligned16(p_lp)))
+            return ZERO_EALIGN;
+        if (!device_ptr(p) || !device_ptr(v) || (p_lp && !device_ptr(p_lp)))
             return ZERO_EINVAL;
     }
     int rc = check_ws_table(ws, ws_bytes, 0);
-    if (rc != ZERO_OK || numel == 0)
+    const int64_t n = (int64_t)nd * S;
+    if (rc != ZERO_OK || n == 0)
         return rc;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     if (!p_lp)
-        return launch_update<kNoLowP>(bits, server_scales, S, numel, p, m, v, nullptr, ws, st);
+        return launch_update<kNoLowP>(bits, server_scales, S, n, numel, p, m, v, nullptr, ws, st);
     if (pdtype == ZERO_BF16)
-        return launch_update<ZERO_BF16>(bits, server_scales, S, numel, p, m, v, p_lp, ws, st);
-    return launch_update<ZERO_F16>(bits, server_scales, S, numel, p, m, v, p_lp, ws, st);
+        return launch_update<ZERO_BF16>(bits, server_scales, S, n, numel, p, m, v, p_lp, ws, st);
+    return launch_update<ZERO_F16>(bits, server_scales, S, n, numel, p, m, v, p_lp, ws, st);
 }
