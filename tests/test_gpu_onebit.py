@@ -321,5 +321,5 @@ def test_onebit_argument_errors(zp):
     assert e.value.code == -1
     big = torch.zeros(256, device=dev)
     with pytest.raises(zp.ZeroError) as e:  # numel past nd * S
-        zp.zero_onebit_update(bits, torch.ones(1, device=dev), 128, 129, big, big.clone(), big.clone(), None, ws)
+        zp.zero_onebit_update(bits, torch.ones(1, device=dev), 128, 129, big, None, big.clone(), None, ws)
     assert e.value.code == -4
