@@ -382,19 +382,19 @@ def run_ours(args):
             if flush is not None:
                 flush.fill_(k & 255)
                 step_events[k][0].record(stream)
-            step(None if flush is None else events[k])
+            step()
             if flush is not None:
                 step_events[k][1].record(stream)
         t_end.record(stream)
         barrier()
-        if flush is None:
-            # the same number of steps again with events around
-            # zero_adam_step, for the dominant kernel's own duration (the
-            # events break the launch overlap, so these steps are not the
-            # ones the step time comes from)
-            for k in range(args.steps):
-                step(events[k])
-            barrier()
+        # the same number of steps again with events around zero_adam_step,
+        # for the dominant kernel's own duration (the events break the launch
+        # overlap, so these steps are not the ones the step time comes from)
+        for k in range(args.steps):
+            if flush is not None:
+                flush.fill_(k & 255)
+            step(events[k])
+        barrier()
     if flush is not None:  # the step alone, L2 flushed before each one
         ms = sum(a.elapsed_time(b) for a, b in step_events)
     else:
