@@ -34,8 +34,9 @@ def _free():
 
 
 def run_full(zp, n, gdtype, pdtype, steps, scale, max_norm=0.0, seed=0, inf_step=None,
-             inf_pos=None, nan=False, hp_kw=None):
-    """Full-array comparison of a flat shard of n elements over `steps` steps."""
+             inf_pos=None, nan=False, hp_kw=None, whole=False):
+    """Full-array comparison of a flat shard of n elements over `steps` steps
+    (whole: the step through zero_step, else pass 1 and zero_adam_step)."""
     ohp, ghp = hp_pair(max_norm=max_norm, **(hp_kw or {}))
     p0 = zs.host_master(n, seed)
     dp = torch.from_numpy(p0.copy()).cuda()
@@ -56,8 +57,11 @@ def run_full(zp, n, gdtype, pdtype, steps, scale, max_norm=0.0, seed=0, inf_step
             g[pos] = zs.host_cast(np.array([bad], np.float32), gdtype)[0]
         dg = to_dev(g, gdtype)
         before = [to_host(t) for t in (dp, dm, dv, dlp)]
-        zp.zero_grad_norm_overflow(dg, state, ws)
-        zp.zero_adam_step(dg, dp, dm, dv, dlp, ghp, state, ws)
+        if whole:
+            zp.zero_step(dg, dp, dm, dv, dlp, ghp, state, ws)
+        else:
+            zp.zero_grad_norm_overflow(dg, state, ws)
+            zp.zero_adam_step(dg, dp, dm, dv, dlp, ghp, state, ws)
         gst = zp.parse_state(state)
         st = oracle_step([g], gdtype, [p], [m], [v], [plp], pdtype, ohp, sc, gst)
         after = [to_host(t) for t in (dp, dm, dv, dlp)]

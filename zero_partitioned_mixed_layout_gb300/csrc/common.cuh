@@ -308,55 +308,11 @@ inline DecideArgs decide_args(const zero_hparams_t *hp, int64_t freeze_step = 0)
     return a;
 }
 
-// Skip or apply, loss-scale and step bookkeeping, and the step scalars
-// (binary64, each rounded once to binary32).  Binary64 is a slow pipe on
-// this GPU, so the three independent chains -- 1 - beta1^t and the step
-// size, 1 - beta2^t and its inverse square root, the norm and the clip
-// coefficient -- run in three threads; thread 0 then writes the results.
-__global__ void k_decide(zero_state_t *st, StepScalars *out, const PowCache *cache, DecideArgs a)
+// Thread 0's part of the decision: the skip, the loss scale and counters,
+// and the step scalars from the three chains' results.
+__device__ __forceinline__ void decide_write(zero_state_t *st, StepScalars *out, const DecideArgs &a, zero_state_t s,
+                                             const float *s_val, double norm)
 {
-    __shared__ float s_val[3];
-    __shared__ double s_norm;
-    pdl_launch_next();
-    pdl_wait();
-    if (blockIdx.x != 0)
-        return;
-    const int tid = threadIdx.x;
-    zero_state_t s = *st;
-    const int64_t tn = s.step + 1;  // the step count if this step applies
-    const double t = (double)tn;
-    const PowCache c = *cache;
-    const bool hit = c.t == tn && c.beta1 == a.beta1 && c.beta2 == a.beta2;
-    if (tid == 0) {
-        if (hit && c.lr == a.lr) {
-            s_val[0] = c.step_size;
-        } else {
-            const double bc1 = hit ? c.bc1 : 1.0 - pow(a.beta1, t);
-            s_val[0] = (float)(a.lr / bc1);
-        }
-    } else if (tid == 1) {
-        if (a.frozen) {
-            s_val[1] = a.isb2_frozen;
-        } else if (hit) {
-            s_val[1] = c.isb2;
-        } else {
-            const double bc2 = 1.0 - pow(a.beta2, t);
-            s_val[1] = (float)(1.0 / sqrt(bc2));
-        }
-    } else if (tid == 2) {
-        const double norm = sqrt(s.sumsq);
-        double clip = 1.0;
-        if (a.max_norm > 0.0) {
-            const double c = a.max_norm / (norm + 1e-6);
-            if (c < 1.0)
-                clip = c;
-        }
-        s_norm = norm;
-        s_val[2] = (float)clip;
-    }
-    __syncthreads();
-    if (tid != 0)
-        return;
     StepScalars o;
     // S is a power of two: below 2^127 its binary32 reciprocal is exact and
     // equals the binary64 reciprocal rounded to binary32
@@ -364,7 +320,6 @@ __global__ void k_decide(zero_state_t *st, StepScalars *out, const PowCache *cac
     o.clip = 1.0f;
     o.b1 = o.omb1 = o.b2 = o.omb2 = o.eps = o.step_size = o.isb2 = o.lrwd = 0.0f;
     o.pad = 0;
-    const double norm = s_norm;
     if (s.found_inf != 0.0) {
         o.skip = 1;
         const double half = s.loss_scale * 0.5;
@@ -402,6 +357,65 @@ __global__ void k_decide(zero_state_t *st, StepScalars *out, const PowCache *cac
     *out = o;
 }
 
+
+// Skip or apply, loss-scale and step bookkeeping, and the step scalars
+// (binary64, each rounded once to binary32).  Binary64 is a slow pipe on
+// this GPU, so the three independent chains -- 1 - beta1^t and the step
+// size, 1 - beta2^t and its inverse square root, the norm and the clip
+// coefficient -- run in three threads; thread 0 then writes the results.
+// Block code: every thread of the block calls it (it holds a block
+// barrier).
+__device__ __forceinline__ void decide_block(zero_state_t *st, StepScalars *out, const PowCache *cache,
+                                             const DecideArgs &a)
+{
+    __shared__ float s_val[3];
+    __shared__ double s_norm;
+    const int tid = threadIdx.x;
+    zero_state_t s = *st;
+    const int64_t tn = s.step + 1;  // the step count if this step applies
+    const double t = (double)tn;
+    const PowCache c = *cache;
+    const bool hit = c.t == tn && c.beta1 == a.beta1 && c.beta2 == a.beta2;
+    if (tid == 0) {
+        if (hit && c.lr == a.lr) {
+            s_val[0] = c.step_size;
+        } else {
+            const double bc1 = hit ? c.bc1 : 1.0 - pow(a.beta1, t);
+            s_val[0] = (float)(a.lr / bc1);
+        }
+    } else if (tid == 1) {
+        if (a.frozen) {
+            s_val[1] = a.isb2_frozen;
+        } else if (hit) {
+            s_val[1] = c.isb2;
+        } else {
+            const double bc2 = 1.0 - pow(a.beta2, t);
+            s_val[1] = (float)(1.0 / sqrt(bc2));
+        }
+    } else if (tid == 2) {
+        const double norm = sqrt(s.sumsq);
+        double clip = 1.0;
+        if (a.max_norm > 0.0) {
+            const double c = a.max_norm / (norm + 1e-6);
+            if (c < 1.0)
+                clip = c;
+        }
+        s_norm = norm;
+        s_val[2] = (float)clip;
+    }
+    __syncthreads();
+    if (tid == 0)
+        decide_write(st, out, a, s, s_val, s_norm);
+}
+
+__global__ void k_decide(zero_state_t *st, StepScalars *out, const PowCache *cache, DecideArgs a)
+{
+    pdl_launch_next();
+    pdl_wait();
+    if (blockIdx.x != 0)
+        return;
+    decide_block(st, out, cache, a);
+}
 // ------------------------------------------------------------- host helpers
 
 int sm_count()
