@@ -315,10 +315,11 @@ def test_fused_step_equals_split_calls(zp, kind, max_norm):
             assert torch.equal(a["st"], b["st"]), f"state differs at step {k}"
         else:
             # a flat shard this small runs as one kernel, whose squared norm
-            # groups its partial sums differently: the norm agrees to
-            # rounding, everything else exactly
+            # groups its binary32 lane sums differently: the norm agrees
+            # within the norm's bar (1e-6 relative), everything else exactly
             sa, sb = zp.parse_state(a["st"]), zp.parse_state(b["st"])
-            assert abs(sa.pop("last_norm") - sb.pop("last_norm")) <= 1e-12 * max(1.0, sb.get("last_norm", 1.0))
+            na, nb = sa.pop("last_norm"), sb.pop("last_norm")
+            assert abs(na - nb) <= 1e-6 * abs(na), f"norm differs at step {k}"
             assert sa == sb, f"state differs at step {k}"
         for key in ("p", "m", "v", "lp"):
             for x, y in zip(a[key], b[key]):
