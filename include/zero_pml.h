@@ -246,18 +246,13 @@ int zero_adam_step(const zero_tlist_t *grads, const zero_tlist_t *master, const 
                    zero_state_t *d_state, void *ws, size_t ws_bytes, void *stream);
 
 /* One whole step of a single-rank shard in one call: zero_grad_norm_overflow
- * (accumulate = 0) followed by zero_adam_step on the same lists.  Use it when
- * no cross-rank sum has to happen between the passes ([ZeRO card §方法适配]:
- * each rank updates its own partition; with one rank, or when the norm and
- * overflow of this shard alone decide the step).  For a one-array list of
- * up to 2^22 elements the step runs as one cooperative kernel (pass 1, the
- * decision in the block that finishes pass 1 last, then pass 2 once it has
- * released the others): the results are those of the two calls, except that
- * the squared norm groups its partial sums differently (the norm agrees to
- * rounding).  Longer one-array lists chain the three kernels so that each is
- * scheduled while the previous one drains (bit-identical to the two calls),
- * and longer lists run the two calls.  Arguments and errors as
- * zero_adam_step. */
+ * (accumulate = 0) followed by zero_adam_step on the same lists, with the
+ * same results bit for bit.  Use it when no cross-rank sum has to happen
+ * between the passes ([ZeRO card §方法适配]: each rank updates its own
+ * partition; with one rank, or when the norm and overflow of this shard
+ * alone decide the step).  For a one-array list the three kernels are
+ * chained so that each is scheduled while the previous one drains.
+ * Arguments and errors as zero_adam_step. */
 int zero_step(const zero_tlist_t *grads, const zero_tlist_t *master, const zero_tlist_t *m,
               const zero_tlist_t *v, const zero_tlist_t *p_lp, const zero_hparams_t *hp,
               zero_state_t *d_state, void *ws, size_t ws_bytes, void *stream);

@@ -311,16 +311,7 @@ def test_fused_step_equals_split_calls(zp, kind, max_norm):
         zp.zero_adam_step(gl, a["p"], a["m"], a["v"], a["lp"], ghp, a["st"], a["ws"])
         zp.zero_step(gl, b["p"], b["m"], b["v"], b["lp"], ghp, b["st"], b["ws"])
         torch.cuda.synchronize()
-        if kind == "list":
-            assert torch.equal(a["st"], b["st"]), f"state differs at step {k}"
-        else:
-            # a flat shard this small runs as one kernel, whose squared norm
-            # groups its binary32 lane sums differently: the norm agrees
-            # within the norm's bar (1e-6 relative), everything else exactly
-            sa, sb = zp.parse_state(a["st"]), zp.parse_state(b["st"])
-            na, nb = sa.pop("last_norm"), sb.pop("last_norm")
-            assert na == nb or abs(na - nb) <= 1e-6 * abs(na), f"norm differs at step {k}"
-            assert sa == sb, f"state differs at step {k}"
+        assert torch.equal(a["st"], b["st"]), f"state differs at step {k}"
         for key in ("p", "m", "v", "lp"):
             for x, y in zip(a[key], b[key]):
                 assert torch.equal(x, y), f"{key} differs at step {k}"
@@ -329,11 +320,10 @@ def test_fused_step_equals_split_calls(zp, kind, max_norm):
 
 
 @pytest.mark.parametrize("gdtype,pdtype", PAIRS)
-@pytest.mark.parametrize("n", [1, 7, 8, 9, 2049, 65539, 1_000_003, 1 << 22, (1 << 22) + 3])
+@pytest.mark.parametrize("n", [1, 7, 8, 9, 2049, 65539, 1_000_003, (1 << 22) + 3])
 def test_whole_step_call_against_oracle(zp, gdtype, pdtype, n):
-    """zero_step on a flat shard -- one kernel up to 2^22 elements, the
-    three-kernel chain beyond -- against the oracle, with clipping and an
-    overflow step."""
+    """zero_step on a flat shard (the three kernels chained) against the
+    oracle, with clipping and an overflow step."""
     scale = 1.0 if gdtype != "f16" else 4096.0
     st, skipped = run_full(zp, n, gdtype, pdtype, 3, scale, max_norm=0.5 if n > 100 else 0.0, seed=n + 5,
                            inf_step=1, whole=True)
@@ -349,8 +339,8 @@ def test_whole_step_call_overflow_positions(zp, where):
 
 
 def test_whole_step_call_many_steps_workspace_reuse(zp):
-    """Twenty steps through one workspace: the one-kernel step's ticket and
-    release count carry over from step to step."""
+    """Twenty chained steps through one workspace: the reduction ticket and
+    the bias-correction cache carry over from step to step."""
     n = 300_001
     st, skipped = run_full(zp, n, "bf16", "bf16", 20, 1.0, max_norm=0.2, seed=77, whole=True)
     assert skipped == 0 and st["step"] == 20

@@ -415,107 +415,6 @@ __global__ void __launch_bounds__(kThreads, 4)
         precompute_next(scp, cache);
 }
 
-// ------------------------------------------------------------- fused step
-
-// A small shard's step is bound by latency, not bandwidth: three kernels,
-// each with its launch, its ramp and its drain, for a few microseconds of
-// data.  Up to this many elements zero_step runs the step as one kernel.
-constexpr int64_t kFusedMaxElems = (int64_t)1 << 22;
-// Polls of the decision flag (each after a short sleep): far beyond the
-// length of any fused step.  A wait that runs out sets WsHeader::error and
-// its block skips pass 2.
-constexpr unsigned kFusedWaitLimit = 1u << 24;
-
-// The step scalars as written by another block of this kernel: read past
-// L1 (which is not coherent across SMs).
-__device__ __forceinline__ StepScalars load_scalars_cg(const StepScalars *scp)
-{
-    static_assert(sizeof(StepScalars) % 16 == 0, "StepScalars is read as 16-byte words");
-    StepScalars s;
-    uint4 *d = reinterpret_cast<uint4 *>(&s);
-    const uint4 *q = reinterpret_cast<const uint4 *>(scp);
-#pragma unroll
-    for (int k = 0; k < (int)(sizeof(StepScalars) / 16); ++k)
-        d[k] = __ldcg(q + k);
-    return s;
-}
-
-// The whole step of a flat shard in one cooperative launch (every block
-// resident): pass 1 over a grid-stride share, block partials; the block that
-// arrives last sums them in block order, runs the decision and releases the
-// others through WsHeader::epoch; then pass 2 over the same grid-stride
-// share.  The arithmetic is that of the three-kernel step; only the
-// grouping of the squared norm's partial sums differs.  (No L2 keep: the
-// shard is small.)
-template <int GT, int PT, bool V32>
-__global__ void __launch_bounds__(kThreads, 2)
-    k_step_fused(const void *__restrict__ g, float *__restrict__ p, float *__restrict__ m, float *__restrict__ v,
-                 void *__restrict__ plp, int64_t n, zero_state_t *st, StepScalars *scp, PowCache *cache,
-                 DecideArgs a, double2 *partials, WsHeader *hdr)
-{
-    __shared__ unsigned s_gen;
-    __shared__ bool s_last, s_ok;
-    const int64_t t = (int64_t)blockIdx.x * kThreads + threadIdx.x;
-    const int64_t nt = (int64_t)gridDim.x * kThreads;
-    double tot = 0.0;
-    uint32_t bad = 0;
-    norm_range<GT>(g, n, t, nt, tot, bad);
-    block_reduce(tot, bad);
-    if (threadIdx.x == 0) {
-        s_gen = *reinterpret_cast<volatile unsigned *>(&hdr->epoch);
-        partials[blockIdx.x] = make_double2(tot, bad ? 1.0 : 0.0);
-        __threadfence();
-        s_last = atomicAdd(&hdr->ticket, 1u) == gridDim.x - 1;
-        s_ok = true;
-    }
-    __syncthreads();
-    if (s_last) {
-        __threadfence();
-        double sum = 0.0;
-        uint32_t b = 0;
-        for (int j = threadIdx.x; j < (int)gridDim.x; j += kThreads) {
-            const double2 q = __ldcg(partials + j);
-            sum += q.x;
-            b |= (q.y != 0.0);
-        }
-        block_reduce(sum, b);
-        if (threadIdx.x == 0) {
-            // sums of squares of the stored gradient; the scale is a power of two
-            const double inv = 1.0 / st->loss_scale;
-            st->sumsq = sum * inv * inv;
-            st->found_inf = b ? 1.0 : 0.0;
-            hdr->ticket = 0u;
-        }
-        __syncthreads();
-        decide_block(st, scp, cache, a);
-        __syncthreads();
-        if (threadIdx.x == 0) {
-            __threadfence();
-            atomicAdd(&hdr->epoch, 1u);
-        }
-    } else if (threadIdx.x == 0) {
-        unsigned polls = 0;
-        while (*reinterpret_cast<volatile unsigned *>(&hdr->epoch) == s_gen && ++polls < kFusedWaitLimit)
-            __nanosleep(64);
-        if (polls >= kFusedWaitLimit) {
-            atomicExch(&hdr->error, 1u);
-            s_ok = false;
-        }
-        __threadfence();
-    }
-    __syncthreads();
-    if (!s_ok)
-        return;
-    const StepScalars s = load_scalars_cg(scp);
-    const int64_t nv = s.skip ? 0 : n >> 3;
-    for (int64_t i = t; i < nv; i += nt)
-        adam_vec<GT, PT, V32>(g, p, m, v, plp, i, s);
-    if (!s.skip && t < (n & 7))
-        adam_scalar<GT, PT>(g, p, m, v, plp, (n >> 3 << 3) + t, s);
-    if (blockIdx.x == 0 && threadIdx.x == 0)
-        precompute_next(&s, cache);
-}
-
 // Pass 2 over a list: one block per tile of kTile elements of one tensor,
 // one vector per thread (the one-shot schedule of the flat kernel).
 template <int GT, int PT, bool V32>
@@ -731,59 +630,6 @@ int launch_adam_lp(int32_t pdtype, const zero_tlist_t *g, const zero_tlist_t *p,
     if (pdtype == ZERO_BF16)
         return launch_adam<GT, ZERO_BF16>(g, p, m, v, plp, sc, ws, stream, ents, tiles, n_tiles, aligned32);
     return launch_adam<GT, ZERO_F16>(g, p, m, v, plp, sc, ws, stream, ents, tiles, n_tiles, aligned32);
-}
-
-// The fused step of one flat shard (checked arguments, n <= kFusedMaxElems).
-template <int GT, int PT, bool V32>
-int launch_fused_v(const zero_tlist_t *g, const zero_tlist_t *p, const zero_tlist_t *m, const zero_tlist_t *v,
-                   const zero_tlist_t *plp, const zero_hparams_t *hp, zero_state_t *st, void *ws,
-                   cudaStream_t stream)
-{
-    unsigned char *w = static_cast<unsigned char *>(ws);
-    const int64_t n = g->numel[0];
-    auto kernel = k_step_fused<GT, PT, V32>;
-    const int64_t want = ((n >> 3) + kThreads - 1) / kThreads;
-    // every block must be resident at once: at most the occupancy, and the
-    // launch is cooperative, so the driver refuses a grid that would not fit
-    const int grid = grid_for((const void *)kernel, want, kMaxBlocks, 2);
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)grid);
-    cfg.blockDim = dim3((unsigned)kThreads);
-    cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeCooperative;
-    attr[0].val.cooperative = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    const DecideArgs a = decide_args(hp);
-    cudaLaunchKernelEx(&cfg, kernel, g->ptrs[0], static_cast<float *>(p->ptrs[0]), static_cast<float *>(m->ptrs[0]),
-                       static_cast<float *>(v->ptrs[0]), plp ? plp->ptrs[0] : nullptr, n, st,
-                       reinterpret_cast<StepScalars *>(w + kWsScalars), reinterpret_cast<PowCache *>(w + kWsPowCache),
-                       a, reinterpret_cast<double2 *>(w + kWsPartials), reinterpret_cast<WsHeader *>(w));
-    return check_launch("zero_step (fused)");
-}
-
-template <int GT, int PT>
-int launch_fused(const zero_tlist_t *g, const zero_tlist_t *p, const zero_tlist_t *m, const zero_tlist_t *v,
-                 const zero_tlist_t *plp, const zero_hparams_t *hp, zero_state_t *st, void *ws, cudaStream_t stream)
-{
-    uintptr_t bits = reinterpret_cast<uintptr_t>(p->ptrs[0]) | reinterpret_cast<uintptr_t>(m->ptrs[0]) |
-                     reinterpret_cast<uintptr_t>(v->ptrs[0]);
-    if (g->dtype == ZERO_F32)
-        bits |= reinterpret_cast<uintptr_t>(g->ptrs[0]);
-    if ((bits & 31u) == 0)
-        return launch_fused_v<GT, PT, true>(g, p, m, v, plp, hp, st, ws, stream);
-    return launch_fused_v<GT, PT, false>(g, p, m, v, plp, hp, st, ws, stream);
-}
-
-template <int GT>
-int launch_fused_lp(const zero_tlist_t *g, const zero_tlist_t *p, const zero_tlist_t *m, const zero_tlist_t *v,
-                    const zero_tlist_t *plp, const zero_hparams_t *hp, zero_state_t *st, void *ws,
-                    cudaStream_t stream)
-{
-    if (plp && plp->dtype == ZERO_BF16)
-        return launch_fused<GT, ZERO_BF16>(g, p, m, v, plp, hp, st, ws, stream);
-    return launch_fused<GT, ZERO_F16>(g, p, m, v, plp, hp, st, ws, stream);
 }
 
 // Checks the arguments of the decision + pass 2 part of a step.
@@ -1047,14 +893,6 @@ extern "C" int zero_step(const zero_tlist_t *grads, const zero_tlist_t *master, 
     if (rc != ZERO_OK)
         return rc;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    if (grads->n == 1 && total > 0 && total <= kFusedMaxElems) {
-        // a small flat shard: the whole step as one kernel
-        switch (grads->dtype) {
-        case ZERO_F16: return launch_fused_lp<ZERO_F16>(grads, master, m, v, p_lp, hp, d_state, ws, s);
-        case ZERO_BF16: return launch_fused_lp<ZERO_BF16>(grads, master, m, v, p_lp, hp, d_state, ws, s);
-        default: return launch_fused_lp<ZERO_F32>(grads, master, m, v, p_lp, hp, d_state, ws, s);
-        }
-    }
     // the three kernels of a flat shard follow one another with nothing in
     // between: each is scheduled while the previous one drains
     const bool chain = grads->n == 1;

@@ -78,8 +78,6 @@ struct Chunk {
 //                       the current pass (Chunk[], at most max_items of them)
 struct WsHeader {
     unsigned int ticket;
-    unsigned int epoch;  // the fused step's release count (see k_step_fused)
-    unsigned int error;  // set if a bounded wait of the fused step ran out
 };
 constexpr size_t kWsScalars = 256;
 constexpr size_t kWsPowCache = 384;
