@@ -56,6 +56,10 @@ def layouts():
         numel[int(rng.integers(0, k))] = int(rng.integers(0, 3))
         out.append((numel, int(rng.integers(1, 17)), int(2 ** rng.integers(0, 8))))
     out.append(([int(x) for x in rng.integers(1, 300, 200)], 16, 8))  # many short tensors
+    # more shards than the kernel argument block holds (the table goes
+    # through the workspace), with few and with many tensors
+    out.append(([int(x) for x in rng.integers(0, 50, 20)], 300, 1))
+    out.append(([int(x) for x in rng.integers(0, 50, 100)], 300, 2))
     return out
 
 

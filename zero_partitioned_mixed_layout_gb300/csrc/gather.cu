@@ -143,10 +143,11 @@ __device__ __forceinline__ void copy_span(char *dst, const char *src, int64_t le
     }
 }
 
-// One block per tile.  kGather: shards -> tensors; else tensors -> shards.
+// One block per tile: finds its tensor, then copies the tile's spans.
+// kGather: shards -> tensors; else tensors -> shards.
 template <bool kGather, int ES>
-__global__ void __launch_bounds__(kThreads, 4) k_gather(const GatherEntry *__restrict__ ents, int64_t n_ents,
-                                                     char *const *__restrict__ shards, int64_t shard_bytes)
+__device__ __forceinline__ void gather_tile(const GatherEntry *ents, int64_t n_ents, char *const *shards,
+                                            int64_t shard_bytes)
 {
     const int64_t tile = blockIdx.x;
     int64_t lo = 0, hi = n_ents - 1;
@@ -173,6 +174,31 @@ __global__ void __launch_bounds__(kThreads, 4) k_gather(const GatherEntry *__res
             copy_span<ES>(s, t, len);
         b += len;
     }
+}
+
+// The tables in device memory (the workspace).
+template <bool kGather, int ES>
+__global__ void __launch_bounds__(kThreads, 4) k_gather(const GatherEntry *__restrict__ ents, int64_t n_ents,
+                                                     char *const *__restrict__ shards, int64_t shard_bytes)
+{
+    gather_tile<kGather, ES>(ents, n_ents, shards, shard_bytes);
+}
+
+// Small calls (a layer of the per-layer schedule, a few tensors): the
+// tables travel in the kernel's argument block, so the call uploads nothing
+// before its launch.
+constexpr int kArgEntries = 64;
+constexpr int kArgShards = 256;
+struct GatherArgs {
+    GatherEntry ents[kArgEntries];
+    char *shards[kArgShards];
+};
+
+template <bool kGather, int ES>
+__global__ void __launch_bounds__(kThreads, 4) k_gather_args(const __grid_constant__ GatherArgs a, int64_t n_ents,
+                                                          int64_t shard_bytes)
+{
+    gather_tile<kGather, ES>(a.ents, n_ents, a.shards, shard_bytes);
 }
 
 // ------------------------------------------------------------- host side
@@ -240,21 +266,36 @@ int run_copy(bool gather, void *const *shards, int32_t nd, int64_t shard_numel, 
         return ZERO_OK;
     if (tiles > 0x7fffffff)
         return ZERO_ELAYOUT;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    const int64_t n_ents = (int64_t)ents.size(), shard_bytes = shard_numel * es;
+    const dim3 grid((unsigned)tiles), block(kThreads);
+    if (n_ents <= kArgEntries && nd <= kArgShards) {
+        GatherArgs a;
+        std::copy(ents.begin(), ents.end(), a.ents);
+        for (int32_t r = 0; r < nd; ++r)
+            a.shards[r] = static_cast<char *>(shards[r]);
+        if (gather && es == 2)
+            k_gather_args<true, 2><<<grid, block, 0, st>>>(a, n_ents, shard_bytes);
+        else if (gather)
+            k_gather_args<true, 4><<<grid, block, 0, st>>>(a, n_ents, shard_bytes);
+        else if (es == 2)
+            k_gather_args<false, 2><<<grid, block, 0, st>>>(a, n_ents, shard_bytes);
+        else
+            k_gather_args<false, 4><<<grid, block, 0, st>>>(a, n_ents, shard_bytes);
+        return check_launch(gather ? "k_gather (gather)" : "k_gather (scatter)");
+    }
 
     // Tables: the shard pointers, then the entries.
     const size_t sb = shard_table_bytes(nd);
     std::vector<unsigned char> host(sb + ents.size() * sizeof(GatherEntry));
     std::copy(shards, shards + nd, reinterpret_cast<void **>(host.data()));
     std::copy(ents.begin(), ents.end(), reinterpret_cast<GatherEntry *>(host.data() + sb));
-    cudaStream_t st = static_cast<cudaStream_t>(stream);
     unsigned char *base = static_cast<unsigned char *>(ws);
     cudaError_t e = cudaMemcpyAsync(base, host.data(), host.size(), cudaMemcpyHostToDevice, st);
     if (e != cudaSuccess)
         return check_launch("gather table upload");
     char *const *d_shards = reinterpret_cast<char *const *>(base);
     const GatherEntry *d_ents = reinterpret_cast<const GatherEntry *>(base + sb);
-    const int64_t n_ents = (int64_t)ents.size(), shard_bytes = shard_numel * es;
-    const dim3 grid((unsigned)tiles), block(kThreads);
     if (gather && es == 2)
         k_gather<true, 2><<<grid, block, 0, st>>>(d_ents, n_ents, d_shards, shard_bytes);
     else if (gather)
