@@ -263,6 +263,75 @@ __device__ void norm_finish(double tot, uint32_t bad, double2 *partials, WsHeade
     }
 }
 
+// The end of a one-shot reduction (one partial per block, any number of
+// blocks up to kGroupBlocks * kMaxGroups), deterministic and without any
+// block waiting on another: each block publishes its partial; the last block
+// of its group of kGroupBlocks sums the group's partials in block order; the
+// last group to finish sums the group partials in group order.  Returns true
+// in thread 0 of that final block, with the grand totals in tot and bad.
+__device__ bool group_finish(double &tot, uint32_t &bad, double2 *block_partials, GroupArea *ga, WsHeader *hdr)
+{
+    __shared__ bool s_flag;
+    block_reduce(tot, bad);
+    const unsigned g = blockIdx.x / kGroupBlocks;
+    const unsigned g0 = g * kGroupBlocks;
+    const unsigned gsize = gridDim.x - g0 < (unsigned)kGroupBlocks ? gridDim.x - g0 : (unsigned)kGroupBlocks;
+    const unsigned ngroups = (gridDim.x + kGroupBlocks - 1) / kGroupBlocks;
+    double2 *gpart = reinterpret_cast<double2 *>(ga->partials);
+    if (threadIdx.x == 0) {
+        block_partials[blockIdx.x] = make_double2(tot, bad ? 1.0 : 0.0);
+        __threadfence();
+        s_flag = atomicAdd(&ga->tickets[g], 1u) == gsize - 1;
+    }
+    __syncthreads();
+    if (!s_flag)
+        return false;
+    __threadfence();
+    double t = 0.0;
+    uint32_t b = 0;
+    for (unsigned j = threadIdx.x; j < gsize; j += kThreads) {
+        const double2 q = __ldcg(block_partials + g0 + j);
+        t += q.x;
+        b |= (q.y != 0.0);
+    }
+    block_reduce(t, b);
+    if (threadIdx.x == 0) {
+        ga->tickets[g] = 0u;
+        gpart[g] = make_double2(t, b ? 1.0 : 0.0);
+        __threadfence();
+        s_flag = atomicAdd(&hdr->ticket, 1u) == ngroups - 1;
+    }
+    __syncthreads();
+    if (!s_flag)
+        return false;
+    __threadfence();
+    t = 0.0;
+    b = 0;
+    for (unsigned j = threadIdx.x; j < ngroups; j += kThreads) {
+        const double2 q = __ldcg(gpart + j);
+        t += q.x;
+        b |= (q.y != 0.0);
+    }
+    block_reduce(t, b);
+    if (threadIdx.x != 0)
+        return false;
+    hdr->ticket = 0u;
+    tot = t;
+    bad = b;
+    return true;
+}
+
+// The squared norm and overflow of a reduction pass written into the state:
+// the partials hold sums of squares of the stored (scaled) gradient; the loss
+// scale is a power of two, so the rescaling is exact.
+__device__ __forceinline__ void write_norm(zero_state_t *st, double tot, uint32_t bad, int accumulate)
+{
+    const double inv = 1.0 / st->loss_scale;
+    const double sum = tot * inv * inv;
+    st->sumsq = accumulate ? st->sumsq + sum : sum;
+    st->found_inf = (accumulate ? st->found_inf : 0.0) + (bad ? 1.0 : 0.0);
+}
+
 // ------------------------------------------------------------- decision
 
 struct DecideArgs {

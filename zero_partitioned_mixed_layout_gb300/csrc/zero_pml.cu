@@ -241,41 +241,55 @@ __device__ __forceinline__ float store_mean_scalar(void *out, int64_t j, float m
     }
 }
 
-template <int GT, int OT>
+// Vectors per thread of the stage-2 reduction's one-shot grid (measured best
+// of 1, 2 and 4).
+constexpr int kReduceVectors = 2;
+
+// The reduction with pass 1 fused: one-shot grid, V vectors per thread, one
+// partial per block and the two-level deterministic finish.  On GB300 this
+// schedule streams 16 replicas at 6.9 TB/s where a persistent grid of 4
+// blocks per SM reached 6.65 TB/s.
+template <int GT, int OT, int V>
 __global__ void __launch_bounds__(kThreads)
-    k_reduce_norm(ReplicaPtrs r, int nr, void *__restrict__ out, int64_t n, double2 *partials, WsHeader *hdr,
-                  zero_state_t *st, int accumulate)
+    k_reduce_norm(ReplicaPtrs r, int nr, void *__restrict__ out, int64_t n, double2 *block_partials,
+                   GroupArea *ga, WsHeader *hdr, zero_state_t *st, int accumulate)
 {
     pdl_wait();
     const float count = (float)nr;
-    double tot = 0.0;
     uint32_t bad = 0;
     const int64_t nv = n >> 3;
-    const int64_t nt = (int64_t)gridDim.x * kThreads;
-    const int64_t t0 = (int64_t)blockIdx.x * kThreads + threadIdx.x;
-    for (int64_t i = t0; i < nv; i += nt) {
-        float a[8], mean[8], stored[8];
-        replica_sum<GT>(r, nr, i, a);
+    const int64_t base = (int64_t)blockIdx.x * kThreads * V + threadIdx.x;
+    float part = 0.0f;
 #pragma unroll
-        for (int e = 0; e < 8; ++e)
-            mean[e] = __fdiv_rn(a[e], count);
-        bad |= store_mean<OT>(out, i, mean, stored);
-        float sq[8];
+    for (int u = 0; u < V; ++u) {
+        const int64_t i = base + (int64_t)u * kThreads;
+        if (i < nv) {
+            float a[8], mean[8], stored[8];
+            replica_sum<GT>(r, nr, i, a);
 #pragma unroll
-        for (int e = 0; e < 8; ++e)
-            sq[e] = __fmul_rn(stored[e], stored[e]);
-        tot += (double)tree8(sq);
+            for (int e = 0; e < 8; ++e)
+                mean[e] = __fdiv_rn(a[e], count);
+            bad |= store_mean<OT>(out, i, mean, stored);
+            float sq[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e)
+                sq[e] = __fmul_rn(stored[e], stored[e]);
+            part = __fadd_rn(part, tree8(sq));
+        }
     }
+    double tot = (double)part;
     const int64_t tail = n - (nv << 3);
-    if (t0 < tail) {
-        const int64_t j = (nv << 3) + t0;
+    if (blockIdx.x == 0 && threadIdx.x < tail) {
+        const int64_t j = (nv << 3) + threadIdx.x;
         float a = Elem<GT>::scalar(r.p[0], j);
         for (int k = 1; k < nr; ++k)
             a = __fadd_rn(a, Elem<GT>::scalar(r.p[k], j));
         const float x = store_mean_scalar<OT>(out, j, __fdiv_rn(a, count), bad);
         tot += (double)__fmul_rn(x, x);
     }
-    norm_finish(tot, bad != 0, partials, hdr, st, accumulate);
+    uint32_t b = bad != 0;
+    if (group_finish(tot, b, block_partials, ga, hdr))
+        write_norm(st, tot, b, accumulate);
 }
 
 // The bias-correction terms for the next step (the same expressions as the
@@ -783,10 +797,15 @@ int launch_reduce(const ReplicaPtrs &r, int nr, void *out, int64_t n, zero_state
 {
     unsigned char *w = static_cast<unsigned char *>(ws);
     WsHeader *hdr = reinterpret_cast<WsHeader *>(w);
-    double2 *partials = reinterpret_cast<double2 *>(w + kWsPartials);
-    const int64_t items = ((n >> 3) + kThreads - 1) / kThreads;
-    const int grid = grid_for((const void *)k_reduce_norm<GT, OT>, items, kMaxBlocks, 4);
-    launch_k(k_reduce_norm<GT, OT>, grid, kThreads, stream, false, r, nr, out, n, partials, hdr, st, accumulate);
+    // one partial per block in the table region (which holds at least
+    // n / 256 bytes: ceil(n / 4096) partials of 16 bytes), the group area
+    // after the norm partials
+    constexpr int V = kReduceVectors;
+    const int64_t blocks = ((n >> 3) + (int64_t)kThreads * V - 1) / ((int64_t)kThreads * V);
+    const int grid = blocks > 0 ? (int)blocks : 1;
+    launch_k(k_reduce_norm<GT, OT, V>, grid, kThreads, stream, false, r, nr, out, n,
+             reinterpret_cast<double2 *>(w + kWsTable), reinterpret_cast<GroupArea *>(w + kWsGroups), hdr, st,
+             accumulate);
     return check_launch("zero_reduce_grads");
 }
 
@@ -810,6 +829,8 @@ extern "C" int zero_reduce_grads(const void *const *replicas, int32_t n_replicas
     if (!replicas || n_replicas < 1 || n_replicas > kMaxReplicas || n < 0 || !d_state ||
         (accumulate != 0 && accumulate != 1))
         return ZERO_EINVAL;
+    if ((n >> 3) / ((int64_t)kThreads * kReduceVectors) >= (int64_t)kGroupBlocks * kMaxGroups)
+        return ZERO_ESIZE;  // past 2^34 elements: more blocks than the finish has groups for
     if (!grad_dtype_ok(dtype) || !grad_dtype_ok(out_dtype))
         return ZERO_EDTYPE;
     if ((reinterpret_cast<uintptr_t>(d_state) & 7u) != 0)

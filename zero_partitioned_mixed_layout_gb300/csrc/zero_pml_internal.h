@@ -10,6 +10,12 @@
 
 namespace zpml {
 
+// 16 bytes holding a double2 (the CUDA vector type is not visible to the
+// host-only translation units that include this header)
+struct alignas(16) double2_storage {
+    double x, y;
+};
+
 // Threads per block of every streaming kernel.
 constexpr int kThreads = 256;
 // Upper bound on the grid of the norm pass (one binary64 partial per block).
@@ -74,8 +80,12 @@ struct Chunk {
 //   [256, 384)          StepScalars of the current step
 //   [384, 512)          PowCache for the next step
 //   [512, 512 + 16*kMaxBlocks)  per-block partials of the norm pass (double2)
+//   then                GroupArea: tickets and partials of the block groups
+//                       of a one-shot reduction
 //   then                TensorEntry[max_tensors], then the work items of
-//                       the current pass (Chunk[], at most max_items of them)
+//                       the current pass (Chunk[], at most max_items of
+//                       them); a flat one-shot reduction keeps its per-block
+//                       partials here instead
 struct WsHeader {
     unsigned int ticket;
 };
@@ -84,7 +94,19 @@ constexpr size_t kWsPowCache = 384;
 static_assert(sizeof(StepScalars) <= 128, "StepScalars must fit its workspace slot");
 static_assert(sizeof(PowCache) <= 128, "PowCache must fit its workspace slot");
 constexpr size_t kWsPartials = 512;
-constexpr size_t kWsTable = kWsPartials + 16 * (size_t)kMaxBlocks;
+
+// A one-shot reduction's blocks report in groups of kGroupBlocks: the last
+// block of a group sums the group's partials in block order, the last group
+// to finish sums the group partials in group order.  Its tickets start at
+// zero (a fresh workspace is zero-filled) and every finisher resets its own.
+constexpr int kGroupBlocks = 1024;
+constexpr int kMaxGroups = 4096;
+struct GroupArea {
+    unsigned int tickets[kMaxGroups];
+    double2_storage partials[kMaxGroups];
+};
+constexpr size_t kWsGroups = kWsPartials + 16 * (size_t)kMaxBlocks;
+constexpr size_t kWsTable = (kWsGroups + sizeof(GroupArea) + 255) & ~(size_t)255;
 
 inline size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
 
