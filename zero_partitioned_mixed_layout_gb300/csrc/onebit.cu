@@ -39,20 +39,34 @@ __device__ __forceinline__ void st8(float *p, const float *f)
     __stcs(reinterpret_cast<float4 *>(p) + 1, make_float4(f[4], f[5], f[6], f[7]));
 }
 
-// End of a squared-norm pass (one-shot grid): the two-level deterministic
-// finish, then the compressor's scale sqrt(sum / len), rounded once to
-// binary32 (not on a skipped step, whose blocks still report to keep the
-// tickets in step).
-__device__ __forceinline__ void scale_finish(double tot, double2 *block_partials, GroupArea *ga, WsHeader *hdr,
-                                             int64_t len, float *scale, bool skip)
+// End of a squared-norm pass: publish this block's partial; the block that
+// takes the last ticket sums the partials in block order and writes the
+// compressor's scale sqrt(sum / len), rounded once to binary32 (not on a
+// skipped step, whose blocks still pass here to keep the ticket in step).
+__device__ void scale_finish(double tot, double2 *partials, WsHeader *hdr, int64_t len, float *scale, bool skip)
 {
+    __shared__ bool s_last;
     uint32_t none = 0;
-    if (group_finish(tot, none, block_partials, ga, hdr) && !skip)
-        *scale = (float)sqrt(tot / (double)len);
+    block_reduce(tot, none);
+    if (threadIdx.x == 0) {
+        partials[blockIdx.x] = make_double2(tot, 0.0);
+        __threadfence();
+        s_last = atomicAdd(&hdr->ticket, 1u) == gridDim.x - 1;
+    }
+    __syncthreads();
+    if (!s_last)
+        return;
+    __threadfence();
+    double t = 0.0;
+    for (int j = threadIdx.x; j < (int)gridDim.x; j += kThreads)
+        t += __ldcg(partials + j).x;
+    block_reduce(t, none);
+    if (threadIdx.x == 0) {
+        if (!skip)
+            *scale = (float)sqrt(t / (double)len);
+        hdr->ticket = 0u;
+    }
 }
-
-// Vectors per thread of the one-shot reduction passes.
-constexpr int kVectors = 2;
 
 // Squares of one 8-element group into a binary32 lane sum; every 4 groups
 // (32 elements) the lane sum goes into the binary64 total.
@@ -112,7 +126,7 @@ __device__ __forceinline__ void load_momentum(const Momentum &mm, int64_t i, flo
 template <int GT, bool kCompressed>
 __global__ void __launch_bounds__(kThreads) k_onebit_worker(const void *g, Momentum mm, float *e, int64_t n,
                                                             const StepScalars *scp, double2 *partials,
-                                                            GroupArea *ga, WsHeader *hdr, float *scale)
+                                                            WsHeader *hdr, float *scale)
 {
     pdl_wait();
     const StepScalars s = *scp;
@@ -120,12 +134,7 @@ __global__ void __launch_bounds__(kThreads) k_onebit_worker(const void *g, Momen
     const uint4 *gv = static_cast<const uint4 *>(g);
     SquareSum acc;
     const int64_t nv = s.skip ? 0 : n >> 3;
-    const int64_t base = (int64_t)blockIdx.x * kThreads * kVectors + threadIdx.x;
-#pragma unroll
-    for (int u = 0; u < kVectors; ++u) {
-        const int64_t i = base + (int64_t)u * kThreads;
-        if (i >= nv)
-            break;
+    for (int64_t i = (int64_t)blockIdx.x * kThreads + threadIdx.x; i < nv; i += (int64_t)gridDim.x * kThreads) {
         uint4 w[W];
 #pragma unroll
         for (int q = 0; q < W; ++q)
@@ -143,7 +152,7 @@ __global__ void __launch_bounds__(kThreads) k_onebit_worker(const void *g, Momen
         st8(e + 8 * i, x);
         acc.add(x);
     }
-    scale_finish(acc.total(), partials, ga, hdr, n, scale, s.skip != 0);
+    scale_finish(acc.total(), partials, hdr, n, scale, s.skip != 0);
 }
 
 // Server, first pass over the chunk: y = (sum over workers in rank order of
@@ -157,8 +166,7 @@ constexpr int kMaxServerWorkers = 4096;
 
 __global__ void __launch_bounds__(kThreads) k_onebit_server(const uint32_t *const *wbits, const float *wscales,
                                                             int nd, float *f, int64_t S, const StepScalars *scp,
-                                                            double2 *partials, GroupArea *ga, WsHeader *hdr,
-                                                            float *scale)
+                                                            double2 *partials, WsHeader *hdr, float *scale)
 {
     extern __shared__ unsigned char s_raw[];
     const uint32_t **s_ptr = reinterpret_cast<const uint32_t **>(s_raw);
@@ -173,12 +181,7 @@ __global__ void __launch_bounds__(kThreads) k_onebit_server(const uint32_t *cons
     const float count = (float)nd;
     SquareSum acc;
     const int64_t nv = skip ? 0 : S >> 3;
-    const int64_t base = (int64_t)blockIdx.x * kThreads * kVectors + threadIdx.x;
-#pragma unroll
-    for (int u = 0; u < kVectors; ++u) {
-        const int64_t i = base + (int64_t)u * kThreads;
-        if (i >= nv)
-            break;
+    for (int64_t i = (int64_t)blockIdx.x * kThreads + threadIdx.x; i < nv; i += (int64_t)gridDim.x * kThreads) {
         float a[8];
         const int shift = 8 * (int)(i & 3);
         for (int k0 = 0; k0 < nd; k0 += kServerBatch) {
@@ -207,7 +210,7 @@ __global__ void __launch_bounds__(kThreads) k_onebit_server(const uint32_t *cons
         st8(f + 8 * i, y);
         acc.add(y);
     }
-    scale_finish(acc.total(), partials, ga, hdr, S, scale, skip);
+    scale_finish(acc.total(), partials, hdr, S, scale, skip);
 }
 
 // Second pass of a compression (worker or server): the signs of x, 32 to a
@@ -298,13 +301,6 @@ __global__ void __launch_bounds__(kThreads) k_onebit_update(const uint32_t *bits
 
 bool aligned4(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 3u) == 0; }
 
-// Blocks of a one-shot reduction pass over nv vectors (at least one).
-int blocks_for(int64_t nv)
-{
-    const int64_t b = (nv + (int64_t)kThreads * kVectors - 1) / ((int64_t)kThreads * kVectors);
-    return b > 0 ? (int)b : 1;
-}
-
 int check_ws_table(void *ws, size_t ws_bytes, size_t table)
 {
     if (!ws)
@@ -326,14 +322,13 @@ int launch_worker(const void *g, const Momentum &mm, float *e, int64_t n, uint32
                   cudaStream_t st)
 {
     unsigned char *w = static_cast<unsigned char *>(ws);
+    WsHeader *hdr = reinterpret_cast<WsHeader *>(w);
+    double2 *partials = reinterpret_cast<double2 *>(w + kWsPartials);
     const StepScalars *sc = step_scalars(ws);
     const int64_t nv = n >> 3;
-    // one-shot grid; its block partials in the table region (n / 256 bytes
-    // at least, ceil(n / 4096) partials of 16 bytes)
-    const int grid = blocks_for(nv);
-    launch_k(k_onebit_worker<GT, kCompressed>, grid, kThreads, st, true, g, mm, e, n, sc,
-             reinterpret_cast<double2 *>(w + kWsTable), reinterpret_cast<GroupArea *>(w + kWsGroups),
-             reinterpret_cast<WsHeader *>(w), scale);
+    const int grid =
+        grid_for((const void *)k_onebit_worker<GT, kCompressed>, (nv + kThreads - 1) / kThreads, kMaxBlocks, 4);
+    launch_k(k_onebit_worker<GT, kCompressed>, grid, kThreads, st, true, g, mm, e, n, sc, partials, hdr, scale);
     int rc = check_launch("zero_onebit_worker (first pass)");
     if (rc != ZERO_OK)
         return rc;
@@ -449,7 +444,7 @@ extern "C" int zero_onebit_server(const uint32_t *const *worker_bits, const floa
             return ZERO_EINVAL;
     }
     const size_t table = align256((size_t)nd * sizeof(void *));
-    int rc = check_ws_table(ws, ws_bytes, table + (size_t)blocks_for(S >> 3) * sizeof(double2));
+    int rc = check_ws_table(ws, ws_bytes, table);
     if (rc != ZERO_OK)
         return rc;
     if (S == 0)
@@ -462,15 +457,14 @@ extern "C" int zero_onebit_server(const uint32_t *const *worker_bits, const floa
         return check_launch("zero_onebit_server (table upload)");
     const StepScalars *sc = step_scalars(ws);
     const int64_t nv = S >> 3;
-    const int grid = blocks_for(nv);
+    const int grid = grid_for((const void *)k_onebit_server, (nv + kThreads - 1) / kThreads, kMaxBlocks, 4);
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)grid);
     cfg.blockDim = dim3((unsigned)kThreads);
     cfg.dynamicSmemBytes = (size_t)nd * (sizeof(void *) + sizeof(float));
     cfg.stream = st;
     cudaLaunchKernelEx(&cfg, k_onebit_server, (const uint32_t *const *)(w + kWsTable), worker_scales, (int)nd, e_s,
-                       S, sc, reinterpret_cast<double2 *>(w + kWsTable + table),
-                       reinterpret_cast<GroupArea *>(w + kWsGroups), reinterpret_cast<WsHeader *>(w), scale);
+                       S, sc, reinterpret_cast<double2 *>(w + kWsPartials), reinterpret_cast<WsHeader *>(w), scale);
     if ((rc = check_launch("zero_onebit_server (first pass)")) != ZERO_OK)
         return rc;
     launch_k(k_onebit_sign, (int)((nv + kThreads - 1) / kThreads), kThreads, st, true, e_s, S, (const float *)scale,
