@@ -250,9 +250,9 @@ int zero_adam_step(const zero_tlist_t *grads, const zero_tlist_t *master, const 
  * same results bit for bit.  Use it when no cross-rank sum has to happen
  * between the passes ([ZeRO card §方法适配]: each rank updates its own
  * partition; with one rank, or when the norm and overflow of this shard
- * alone decide the step).  For a one-array list the three kernels are
- * chained so that each is scheduled while the previous one drains.
- * Arguments and errors as zero_adam_step. */
+ * alone decide the step).  For a one-array list the last block of pass 1
+ * takes the decision (no decision kernel) and pass 2 is scheduled while
+ * pass 1 drains.  Arguments and errors as zero_adam_step. */
 int zero_step(const zero_tlist_t *grads, const zero_tlist_t *master, const zero_tlist_t *m,
               const zero_tlist_t *v, const zero_tlist_t *p_lp, const zero_hparams_t *hp,
               zero_state_t *d_state, void *ws, size_t ws_bytes, void *stream);

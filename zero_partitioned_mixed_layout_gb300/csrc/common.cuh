@@ -228,8 +228,9 @@ __device__ __forceinline__ void block_reduce(double &tot, uint32_t &bad)
 // End of the norm pass in every block: publish this block's partial; the
 // block that takes the last ticket sums all partials in block order and
 // writes (or adds) the unscaled totals into the state.  No block waits on
-// another: the last block to arrive does the final sum.
-__device__ void norm_finish(double tot, uint32_t bad, double2 *partials, WsHeader *hdr,
+// another: the last block to arrive does the final sum.  Returns true in
+// every thread of that last block.
+__device__ bool norm_finish(double tot, uint32_t bad, double2 *partials, WsHeader *hdr,
                             zero_state_t *st, int accumulate)
 {
     __shared__ bool s_last;
@@ -242,7 +243,7 @@ __device__ void norm_finish(double tot, uint32_t bad, double2 *partials, WsHeade
     }
     __syncthreads();
     if (!s_last)
-        return;
+        return false;
     __threadfence();
     double t = 0.0;
     uint32_t b = 0;
@@ -261,6 +262,7 @@ __device__ void norm_finish(double tot, uint32_t bad, double2 *partials, WsHeade
         st->found_inf = (accumulate ? st->found_inf : 0.0) + (b ? 1.0 : 0.0);
         hdr->ticket = 0u;
     }
+    return true;
 }
 
 // The end of a one-shot reduction (one partial per block, any number of

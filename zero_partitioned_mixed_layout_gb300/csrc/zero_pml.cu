@@ -116,10 +116,18 @@ __device__ __forceinline__ void norm_range(const void *g, int64_t n, int64_t t, 
     }
 }
 
+// The step decision, for a pass 1 whose last block takes it (a single-rank
+// step: no cross-rank sum between the passes).
+struct FoldedDecision {
+    StepScalars *scp;     // NULL: pass 1 alone
+    const PowCache *cache;
+    DecideArgs a;
+};
+
 template <int GT>
 __global__ void __launch_bounds__(kThreads)
     k_norm_flat(const void *__restrict__ g, int64_t n, double2 *partials, WsHeader *hdr, zero_state_t *st,
-                int accumulate, int trigger)
+                int accumulate, int trigger, FoldedDecision fd)
 {
     if (trigger)
         pdl_launch_next();
@@ -130,7 +138,12 @@ __global__ void __launch_bounds__(kThreads)
     const int64_t keep_vectors = kL2KeepBytes / (8 * Elem<GT>::kBytes);
     norm_range<GT>(g, n, (int64_t)blockIdx.x * kThreads + threadIdx.x, (int64_t)gridDim.x * kThreads, tot,
                    bad, (n >> 3) - keep_vectors);
-    norm_finish(tot, bad, partials, hdr, st, accumulate);
+    if (norm_finish(tot, bad, partials, hdr, st, accumulate) && fd.scp) {
+        // the last block, its totals in the state: the decision here saves
+        // the decision kernel's launch and its dependency hop
+        __syncthreads();
+        decide_block(st, fd.scp, fd.cache, fd.a);
+    }
 }
 
 template <int GT>
@@ -568,7 +581,7 @@ int upload_table(const zero_tlist_t *g, const zero_tlist_t *p, const zero_tlist_
 // let it be scheduled early.
 template <int GT>
 int launch_norm(const zero_tlist_t *grads, int64_t total, zero_state_t *st, int accumulate, void *ws,
-                cudaStream_t stream, bool trigger)
+                cudaStream_t stream, bool trigger, const FoldedDecision &fd = FoldedDecision{})
 {
     unsigned char *w = static_cast<unsigned char *>(ws);
     WsHeader *hdr = reinterpret_cast<WsHeader *>(w);
@@ -580,7 +593,7 @@ int launch_norm(const zero_tlist_t *grads, int64_t total, zero_state_t *st, int 
         const int64_t items = ((n >> 3) + 4 * kThreads - 1) / (4 * kThreads);
         const int grid = grid_for((const void *)k_norm_flat<GT>, items, kMaxBlocks, 4);
         launch_k(k_norm_flat<GT>, grid, kThreads, stream, false, g, n, partials, hdr, st, accumulate,
-                 (int)trigger);
+                 (int)trigger, fd);
         return check_launch("zero_grad_norm_overflow");
     }
     int64_t n_chunks = 0;
@@ -689,6 +702,34 @@ int check_step_args(const zero_tlist_t *grads, const zero_tlist_t *master, const
     return check_ws(ws, ws_bytes, grads->n, *total);
 }
 
+// Pass 2 on checked arguments (after this call's decision).
+int launch_pass2(const zero_tlist_t *grads, const zero_tlist_t *master, const zero_tlist_t *m,
+                 const zero_tlist_t *v, const zero_tlist_t *p_lp, const StepScalars *sc, void *ws, cudaStream_t s,
+                 const TensorEntry *ents, const Chunk *tiles, int64_t n_tiles, bool aligned32)
+{
+    const int32_t pd = p_lp ? p_lp->dtype : ZERO_F16;
+    switch (grads->dtype) {
+    case ZERO_F16:
+        return launch_adam_lp<ZERO_F16>(pd, grads, master, m, v, p_lp, sc, ws, s, ents, tiles, n_tiles, aligned32);
+    case ZERO_BF16:
+        return launch_adam_lp<ZERO_BF16>(pd, grads, master, m, v, p_lp, sc, ws, s, ents, tiles, n_tiles, aligned32);
+    default:
+        return launch_adam_lp<ZERO_F32>(pd, grads, master, m, v, p_lp, sc, ws, s, ents, tiles, n_tiles, aligned32);
+    }
+}
+
+// Every fp32 array of a one-array list (and an fp32 gradient) starts on a
+// 32-byte boundary: pass 2 may use its 32-byte access form.
+bool flat_aligned32(const zero_tlist_t *grads, const zero_tlist_t *master, const zero_tlist_t *m,
+                    const zero_tlist_t *v)
+{
+    uintptr_t bits = reinterpret_cast<uintptr_t>(master->ptrs[0]) | reinterpret_cast<uintptr_t>(m->ptrs[0]) |
+                     reinterpret_cast<uintptr_t>(v->ptrs[0]);
+    if (grads->dtype == ZERO_F32)
+        bits |= reinterpret_cast<uintptr_t>(grads->ptrs[0]);
+    return (bits & 31u) == 0;
+}
+
 // The decision kernel and pass 2 on checked arguments.  A list's tile table
 // is copied into the workspace first, so that nothing but the decision
 // kernel sits between that copy and pass 2.  `decide_pdl`: the previous
@@ -701,14 +742,7 @@ int run_step(const zero_tlist_t *grads, const zero_tlist_t *master, const zero_t
     TensorEntry *ents = nullptr;
     Chunk *tiles = nullptr;
     int64_t n_tiles = 0;
-    bool aligned32 = true;
-    if (grads->n == 1) {
-        uintptr_t bits = reinterpret_cast<uintptr_t>(master->ptrs[0]) | reinterpret_cast<uintptr_t>(m->ptrs[0]) |
-                         reinterpret_cast<uintptr_t>(v->ptrs[0]);
-        if (grads->dtype == ZERO_F32)
-            bits |= reinterpret_cast<uintptr_t>(grads->ptrs[0]);
-        aligned32 = (bits & 31u) == 0;
-    }
+    bool aligned32 = grads->n != 1 || flat_aligned32(grads, master, m, v);
     if (grads->n > 1) {
         if ((rc = upload_table(grads, master, m, v, p_lp, ws, s, kTile, &n_tiles, &ents, &tiles, &aligned32)) !=
             ZERO_OK)
@@ -725,15 +759,7 @@ int run_step(const zero_tlist_t *grads, const zero_tlist_t *master, const zero_t
         return rc;
     if (grads->n == 0)
         return ZERO_OK;
-    const int32_t pd = p_lp ? p_lp->dtype : ZERO_F16;
-    switch (grads->dtype) {
-    case ZERO_F16:
-        return launch_adam_lp<ZERO_F16>(pd, grads, master, m, v, p_lp, sc, ws, s, ents, tiles, n_tiles, aligned32);
-    case ZERO_BF16:
-        return launch_adam_lp<ZERO_BF16>(pd, grads, master, m, v, p_lp, sc, ws, s, ents, tiles, n_tiles, aligned32);
-    default:
-        return launch_adam_lp<ZERO_F32>(pd, grads, master, m, v, p_lp, sc, ws, s, ents, tiles, n_tiles, aligned32);
-    }
+    return launch_pass2(grads, master, m, v, p_lp, sc, ws, s, ents, tiles, n_tiles, aligned32);
 }
 
 }  // namespace
@@ -914,17 +940,31 @@ extern "C" int zero_step(const zero_tlist_t *grads, const zero_tlist_t *master, 
     if (rc != ZERO_OK)
         return rc;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    // the three kernels of a flat shard follow one another with nothing in
-    // between: each is scheduled while the previous one drains
-    const bool chain = grads->n == 1;
+    if (grads->n == 1) {
+        // a flat shard: the last block of pass 1 takes the decision, and
+        // pass 2 follows with nothing in between (scheduled while pass 1
+        // drains)
+        unsigned char *w = static_cast<unsigned char *>(ws);
+        StepScalars *sc = reinterpret_cast<StepScalars *>(w + kWsScalars);
+        const FoldedDecision fd = {sc, reinterpret_cast<const PowCache *>(w + kWsPowCache), decide_args(hp)};
+        switch (grads->dtype) {
+        case ZERO_F16: rc = launch_norm<ZERO_F16>(grads, total, d_state, 0, ws, s, true, fd); break;
+        case ZERO_BF16: rc = launch_norm<ZERO_BF16>(grads, total, d_state, 0, ws, s, true, fd); break;
+        default: rc = launch_norm<ZERO_F32>(grads, total, d_state, 0, ws, s, true, fd); break;
+        }
+        if (rc != ZERO_OK)
+            return rc;
+        return launch_pass2(grads, master, m, v, p_lp, sc, ws, s, nullptr, nullptr, 0,
+                            flat_aligned32(grads, master, m, v));
+    }
     switch (grads->dtype) {
-    case ZERO_F16: rc = launch_norm<ZERO_F16>(grads, total, d_state, 0, ws, s, chain); break;
-    case ZERO_BF16: rc = launch_norm<ZERO_BF16>(grads, total, d_state, 0, ws, s, chain); break;
-    default: rc = launch_norm<ZERO_F32>(grads, total, d_state, 0, ws, s, chain); break;
+    case ZERO_F16: rc = launch_norm<ZERO_F16>(grads, total, d_state, 0, ws, s, false); break;
+    case ZERO_BF16: rc = launch_norm<ZERO_BF16>(grads, total, d_state, 0, ws, s, false); break;
+    default: rc = launch_norm<ZERO_F32>(grads, total, d_state, 0, ws, s, false); break;
     }
     if (rc != ZERO_OK)
         return rc;
-    return run_step(grads, master, m, v, p_lp, hp, d_state, ws, s, chain);
+    return run_step(grads, master, m, v, p_lp, hp, d_state, ws, s, false);
 }
 
 // ------------------------------------------------------------- pass 1 without workspace
