@@ -406,7 +406,7 @@ int zero_gather_plan(const int64_t *numel, int64_t n_tensors, const int64_t *lay
  * server's mean is the binary32 sum over workers in rank order followed by
  * one division by Nd.  Element arithmetic is binary32, each operation
  * rounded on its own.  The three calls of one step use the same state and
- * workspace (zero_workspace_bytes(1, n)) in stream order; the worker call's
+ * workspace (zero_workspace_bytes(Nd, n)) in stream order; the worker call's
  * decision (skip on overflow, loss scale, step count) holds for the other
  * two, and a skipped step changes nothing.  n and S must be multiples of 32
  * (ZERO_ESIZE); arrays 16-byte aligned.  Errors otherwise as

@@ -111,8 +111,13 @@ def test_workspace_bytes(zp):
     a = zp.zero_workspace_bytes(1, 1000)
     b = zp.zero_workspace_bytes(1, 1 << 30)
     c = zp.zero_workspace_bytes(10_000, 1 << 30)
-    assert 0 < a < b < c
-    assert a % 256 == 0 and c % 256 == 0
+    d = zp.zero_workspace_bytes(10_000, 1000)
+    # the table region holds a list's table (O(tensors)) or a flat pass's
+    # block partials (O(elements)), whichever is larger
+    assert 0 < a < b <= c and a < d <= c
+    assert d - a >= 10_000 * 48 + 2 * 10_001 * 8 - 4096
+    assert b - a >= ((1 << 30) - 1000) // 256 - 512
+    assert all(x % 256 == 0 for x in (a, b, c, d))
 
 
 def test_error_strings(zp):

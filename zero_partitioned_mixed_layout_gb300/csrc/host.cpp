@@ -125,8 +125,7 @@ extern "C" size_t zero_workspace_bytes(int64_t max_tensors, int64_t max_total_nu
         max_tensors = 1;
     if (max_total_numel < 0)
         max_total_numel = 0;
-    return zpml::kWsTable +
-           zpml::table_bytes(max_tensors, zpml::max_items(max_tensors, max_total_numel));
+    return zpml::kWsTable + zpml::table_bytes(max_tensors, max_total_numel);
 }
 
 // Stage-3 gather plan.  Same source, same section: stage 3 partitions the

@@ -146,18 +146,33 @@ __global__ void __launch_bounds__(kThreads)
     }
 }
 
+// The tensor that holds work item `item` of a list: the last t with
+// first[t] <= item (empty tensors share their successor's first item).
+__device__ __forceinline__ int64_t find_tensor(const int64_t *__restrict__ first, int64_t n, int64_t item)
+{
+    int64_t lo = 0, hi = n - 1;
+    while (lo < hi) {
+        const int64_t mid = (lo + hi + 1) >> 1;
+        if (__ldg(first + mid) <= item)
+            lo = mid;
+        else
+            hi = mid - 1;
+    }
+    return lo;
+}
+
 template <int GT>
 __global__ void __launch_bounds__(kThreads)
-    k_norm_list(const TensorEntry *__restrict__ ents, const Chunk *__restrict__ chunks, int64_t n_chunks,
-                double2 *partials, WsHeader *hdr, zero_state_t *st, int accumulate)
+    k_norm_list(const TensorEntry *__restrict__ ents, const int64_t *__restrict__ first, int64_t n_ents,
+                int64_t n_chunks, double2 *partials, WsHeader *hdr, zero_state_t *st, int accumulate)
 {
     pdl_wait();
     double tot = 0.0;
     uint32_t bad = 0;
     for (int64_t c = blockIdx.x; c < n_chunks; c += gridDim.x) {
-        const Chunk ch = chunks[c];
-        const TensorEntry e = ents[ch.tensor];
-        const int64_t start = (int64_t)ch.index * kChunk;
+        const int64_t t = find_tensor(first, n_ents, c);
+        const TensorEntry e = ents[t];
+        const int64_t start = (c - first[t]) * kChunk;
         const int64_t len = min(kChunk, e.numel - start);
         const void *g = static_cast<const char *>(e.g) + start * Elem<GT>::kBytes;
         norm_range<GT>(g, len, threadIdx.x, kThreads, tot, bad);
@@ -446,7 +461,7 @@ __global__ void __launch_bounds__(kThreads, 4)
 // one vector per thread (the one-shot schedule of the flat kernel).
 template <int GT, int PT, bool V32>
 __global__ void __launch_bounds__(kThreads, 4)
-    k_adam_list(const TensorEntry *__restrict__ ents, const Chunk *__restrict__ tiles,
+    k_adam_list(const TensorEntry *__restrict__ ents, const int64_t *__restrict__ first, int64_t n_ents,
                 const StepScalars *__restrict__ scp, PowCache *cache)
 {
     pdl_wait();
@@ -455,9 +470,10 @@ __global__ void __launch_bounds__(kThreads, 4)
         return;
     if (blockIdx.x == 0 && threadIdx.x == 0)
         precompute_next(scp, cache);
-    const Chunk tl = tiles[blockIdx.x];
-    const TensorEntry e = ents[tl.tensor];
-    const int64_t start = (int64_t)tl.index * kTile;
+    const int64_t tile = blockIdx.x;
+    const int64_t tn = find_tensor(first, n_ents, tile);
+    const TensorEntry e = ents[tn];
+    const int64_t start = (tile - first[tn]) * kTile;
     const int64_t len = min(kTile, e.numel - start);
     const void *g = static_cast<const char *>(e.g) + start * Elem<GT>::kBytes;
     void *plp = e.plp ? static_cast<void *>(static_cast<char *>(e.plp) + start * 2) : nullptr;
@@ -527,22 +543,30 @@ __global__ void __launch_bounds__(kThreads)
     }
 }
 
-// Builds the entry and chunk tables of a list call on the host and copies
-// them into the workspace (stream-ordered).  Returns the chunk count in
-// *n_chunks.
-int upload_table(const zero_tlist_t *g, const zero_tlist_t *p, const zero_tlist_t *m, const zero_tlist_t *v,
-                 const zero_tlist_t *plp, void *ws, cudaStream_t stream, int64_t item, int64_t *n_chunks,
-                 TensorEntry **d_ents, Chunk **d_chunks, bool *aligned32 = nullptr)
+// A list's table as copied into the workspace.
+struct ListDev {
+    const TensorEntry *ents = nullptr;
+    const int64_t *first_tile = nullptr;   // n + 1 prefix of pass-2 tiles
+    const int64_t *first_chunk = nullptr;  // n + 1 prefix of pass-1 chunks
+    int64_t n = 0, n_tiles = 0, n_chunks = 0;
+    bool aligned32 = true;                 // every fp32 array on 32 bytes
+};
+
+// Builds a list's table on the host -- one entry per tensor and the two
+// per-tensor prefixes of work items, O(tensors) -- and copies it into the
+// workspace (stream-ordered).  p, m, v, plp may be NULL (pass 1 alone).
+int upload_list(const zero_tlist_t *g, const zero_tlist_t *p, const zero_tlist_t *m, const zero_tlist_t *v,
+                const zero_tlist_t *plp, void *ws, cudaStream_t stream, ListDev *L)
 {
     const int64_t n = g->n;
-    int64_t chunks = 0;
-    for (int64_t i = 0; i < n; ++i)
-        chunks += (g->numel[i] + item - 1) / item;
     const size_t ent_bytes = align256((size_t)n * sizeof(TensorEntry));
-    std::vector<unsigned char> host(ent_bytes + (size_t)chunks * sizeof(Chunk));
+    const size_t pre_bytes = align256((size_t)(n + 1) * sizeof(int64_t));
+    std::vector<unsigned char> host(ent_bytes + 2 * pre_bytes);
     TensorEntry *ents = reinterpret_cast<TensorEntry *>(host.data());
-    Chunk *ch = reinterpret_cast<Chunk *>(host.data() + ent_bytes);
-    int64_t c = 0;
+    int64_t *ft = reinterpret_cast<int64_t *>(host.data() + ent_bytes);
+    int64_t *fc = reinterpret_cast<int64_t *>(host.data() + ent_bytes + pre_bytes);
+    bool a32 = true;
+    int64_t tiles = 0, chunks = 0;
     for (int64_t i = 0; i < n; ++i) {
         TensorEntry &e = ents[i];
         e.g = g->ptrs[i];
@@ -551,29 +575,32 @@ int upload_table(const zero_tlist_t *g, const zero_tlist_t *p, const zero_tlist_
         e.v = v ? static_cast<float *>(v->ptrs[i]) : nullptr;
         e.plp = plp ? plp->ptrs[i] : nullptr;
         e.numel = g->numel[i];
-        if (aligned32 && e.numel > 0) {
+        if (p && e.numel > 0) {
             uintptr_t bits = reinterpret_cast<uintptr_t>(e.p) | reinterpret_cast<uintptr_t>(e.m) |
                              reinterpret_cast<uintptr_t>(e.v);
             if (g->dtype == ZERO_F32)
                 bits |= reinterpret_cast<uintptr_t>(e.g);
             if (bits & 31u)
-                *aligned32 = false;
+                a32 = false;
         }
-        const int64_t k = (g->numel[i] + item - 1) / item;
-        for (int64_t j = 0; j < k; ++j) {
-            ch[c].tensor = (int32_t)i;
-            ch[c].index = (int32_t)j;
-            ++c;
-        }
+        ft[i] = tiles;
+        fc[i] = chunks;
+        tiles += (e.numel + kTile - 1) / kTile;
+        chunks += (e.numel + kChunk - 1) / kChunk;
     }
+    ft[n] = tiles;
+    fc[n] = chunks;
     unsigned char *base = static_cast<unsigned char *>(ws) + kWsTable;
-    if (!host.empty() &&
-        cudaMemcpyAsync(base, host.data(), host.size(), cudaMemcpyHostToDevice, stream) != cudaSuccess)
+    if (cudaMemcpyAsync(base, host.data(), host.size(), cudaMemcpyHostToDevice, stream) != cudaSuccess)
         return check_launch("workspace table upload");
-    *n_chunks = chunks;
-    *d_ents = reinterpret_cast<TensorEntry *>(base);
-    *d_chunks = reinterpret_cast<Chunk *>(base + ent_bytes);
-    return ZERO_OK;
+    L->ents = reinterpret_cast<const TensorEntry *>(base);
+    L->first_tile = reinterpret_cast<const int64_t *>(base + ent_bytes);
+    L->first_chunk = reinterpret_cast<const int64_t *>(base + ent_bytes + pre_bytes);
+    L->n = n;
+    L->n_tiles = tiles;
+    L->n_chunks = chunks;
+    L->aligned32 = a32;
+    return tiles > 0x7fffffff ? ZERO_EINVAL : ZERO_OK;
 }
 
 // Pass 1.  `trigger`: the next operation in the stream is this library's
@@ -581,7 +608,8 @@ int upload_table(const zero_tlist_t *g, const zero_tlist_t *p, const zero_tlist_
 // let it be scheduled early.
 template <int GT>
 int launch_norm(const zero_tlist_t *grads, int64_t total, zero_state_t *st, int accumulate, void *ws,
-                cudaStream_t stream, bool trigger, const FoldedDecision &fd = FoldedDecision{})
+                cudaStream_t stream, bool trigger, const FoldedDecision &fd = FoldedDecision{},
+                const ListDev *pre = nullptr)
 {
     unsigned char *w = static_cast<unsigned char *>(ws);
     WsHeader *hdr = reinterpret_cast<WsHeader *>(w);
@@ -596,16 +624,17 @@ int launch_norm(const zero_tlist_t *grads, int64_t total, zero_state_t *st, int 
                  (int)trigger, fd);
         return check_launch("zero_grad_norm_overflow");
     }
-    int64_t n_chunks = 0;
-    TensorEntry *ents = nullptr;
-    Chunk *chunks = nullptr;
-    int rc = upload_table(grads, nullptr, nullptr, nullptr, nullptr, ws, stream, kChunk, &n_chunks, &ents,
-                          &chunks);
-    if (rc != ZERO_OK)
-        return rc;
-    const int grid = grid_for((const void *)k_norm_list<GT>, n_chunks, kMaxBlocks, 4);
-    launch_k(k_norm_list<GT>, grid, kThreads, stream, false, (const TensorEntry *)ents, (const Chunk *)chunks,
-             n_chunks, partials, hdr, st, accumulate);
+    ListDev L;
+    if (pre) {
+        L = *pre;
+    } else {
+        const int rc = upload_list(grads, nullptr, nullptr, nullptr, nullptr, ws, stream, &L);
+        if (rc != ZERO_OK)
+            return rc;
+    }
+    const int grid = grid_for((const void *)k_norm_list<GT>, L.n_chunks, kMaxBlocks, 4);
+    launch_k(k_norm_list<GT>, grid, kThreads, stream, false, L.ents, L.first_chunk, L.n, L.n_chunks, partials,
+             hdr, st, accumulate);
     (void)total;
     return check_launch("zero_grad_norm_overflow");
 }
@@ -615,8 +644,7 @@ int launch_norm(const zero_tlist_t *grads, int64_t total, zero_state_t *st, int 
 // fp32 array starts on a 32-byte boundary, so the 32-byte access form runs.
 template <int GT, int PT, bool V32>
 int launch_adam_v(const zero_tlist_t *g, const zero_tlist_t *p, const zero_tlist_t *m, const zero_tlist_t *v,
-                  const zero_tlist_t *plp, const StepScalars *sc, void *ws, cudaStream_t stream,
-                  const TensorEntry *ents, const Chunk *tiles, int64_t n_tiles)
+                  const zero_tlist_t *plp, const StepScalars *sc, void *ws, cudaStream_t stream, const ListDev &L)
 {
     PowCache *cache = reinterpret_cast<PowCache *>(static_cast<unsigned char *>(ws) + kWsPowCache);
     if (g->n == 1) {
@@ -631,32 +659,32 @@ int launch_adam_v(const zero_tlist_t *g, const zero_tlist_t *p, const zero_tlist
                  static_cast<float *>(v->ptrs[0]), plp ? plp->ptrs[0] : nullptr, n, sc, cache);
         return check_launch("zero_adam_step");
     }
-    if (n_tiles == 0)
+    if (L.n_tiles == 0)
         return ZERO_OK;
     // one-shot: one block per tile
-    launch_k(k_adam_list<GT, PT, V32>, (int)n_tiles, kThreads, stream, true, ents, tiles, sc, cache);
+    launch_k(k_adam_list<GT, PT, V32>, (int)L.n_tiles, kThreads, stream, true, L.ents, L.first_tile, L.n, sc,
+             cache);
     return check_launch("zero_adam_step");
 }
 
 template <int GT, int PT>
 int launch_adam(const zero_tlist_t *g, const zero_tlist_t *p, const zero_tlist_t *m, const zero_tlist_t *v,
-                const zero_tlist_t *plp, const StepScalars *sc, void *ws, cudaStream_t stream,
-                const TensorEntry *ents, const Chunk *tiles, int64_t n_tiles, bool aligned32)
+                const zero_tlist_t *plp, const StepScalars *sc, void *ws, cudaStream_t stream, const ListDev &L,
+                bool aligned32)
 {
     if (aligned32)
-        return launch_adam_v<GT, PT, true>(g, p, m, v, plp, sc, ws, stream, ents, tiles, n_tiles);
-    return launch_adam_v<GT, PT, false>(g, p, m, v, plp, sc, ws, stream, ents, tiles, n_tiles);
+        return launch_adam_v<GT, PT, true>(g, p, m, v, plp, sc, ws, stream, L);
+    return launch_adam_v<GT, PT, false>(g, p, m, v, plp, sc, ws, stream, L);
 }
 
 template <int GT>
 int launch_adam_lp(int32_t pdtype, const zero_tlist_t *g, const zero_tlist_t *p, const zero_tlist_t *m,
                    const zero_tlist_t *v, const zero_tlist_t *plp, const StepScalars *sc, void *ws,
-                   cudaStream_t stream, const TensorEntry *ents, const Chunk *tiles, int64_t n_tiles,
-                   bool aligned32)
+                   cudaStream_t stream, const ListDev &L, bool aligned32)
 {
     if (pdtype == ZERO_BF16)
-        return launch_adam<GT, ZERO_BF16>(g, p, m, v, plp, sc, ws, stream, ents, tiles, n_tiles, aligned32);
-    return launch_adam<GT, ZERO_F16>(g, p, m, v, plp, sc, ws, stream, ents, tiles, n_tiles, aligned32);
+        return launch_adam<GT, ZERO_BF16>(g, p, m, v, plp, sc, ws, stream, L, aligned32);
+    return launch_adam<GT, ZERO_F16>(g, p, m, v, plp, sc, ws, stream, L, aligned32);
 }
 
 // Checks the arguments of the decision + pass 2 part of a step.
@@ -705,16 +733,13 @@ int check_step_args(const zero_tlist_t *grads, const zero_tlist_t *master, const
 // Pass 2 on checked arguments (after this call's decision).
 int launch_pass2(const zero_tlist_t *grads, const zero_tlist_t *master, const zero_tlist_t *m,
                  const zero_tlist_t *v, const zero_tlist_t *p_lp, const StepScalars *sc, void *ws, cudaStream_t s,
-                 const TensorEntry *ents, const Chunk *tiles, int64_t n_tiles, bool aligned32)
+                 const ListDev &L, bool aligned32)
 {
     const int32_t pd = p_lp ? p_lp->dtype : ZERO_F16;
     switch (grads->dtype) {
-    case ZERO_F16:
-        return launch_adam_lp<ZERO_F16>(pd, grads, master, m, v, p_lp, sc, ws, s, ents, tiles, n_tiles, aligned32);
-    case ZERO_BF16:
-        return launch_adam_lp<ZERO_BF16>(pd, grads, master, m, v, p_lp, sc, ws, s, ents, tiles, n_tiles, aligned32);
-    default:
-        return launch_adam_lp<ZERO_F32>(pd, grads, master, m, v, p_lp, sc, ws, s, ents, tiles, n_tiles, aligned32);
+    case ZERO_F16: return launch_adam_lp<ZERO_F16>(pd, grads, master, m, v, p_lp, sc, ws, s, L, aligned32);
+    case ZERO_BF16: return launch_adam_lp<ZERO_BF16>(pd, grads, master, m, v, p_lp, sc, ws, s, L, aligned32);
+    default: return launch_adam_lp<ZERO_F32>(pd, grads, master, m, v, p_lp, sc, ws, s, L, aligned32);
     }
 }
 
@@ -730,26 +755,27 @@ bool flat_aligned32(const zero_tlist_t *grads, const zero_tlist_t *master, const
     return (bits & 31u) == 0;
 }
 
-// The decision kernel and pass 2 on checked arguments.  A list's tile table
-// is copied into the workspace first, so that nothing but the decision
-// kernel sits between that copy and pass 2.  `decide_pdl`: the previous
-// operation in the stream is this library's pass-1 kernel of the same call.
+// The decision kernel and pass 2 on checked arguments.  A list's table is
+// copied into the workspace first (unless `pre` says this call already did,
+// before its pass 1), so that nothing but the decision kernel sits between
+// that copy and pass 2.  `decide_pdl`: the previous operation in the stream
+// is this library's pass-1 kernel of the same call.
 int run_step(const zero_tlist_t *grads, const zero_tlist_t *master, const zero_tlist_t *m, const zero_tlist_t *v,
              const zero_tlist_t *p_lp, const zero_hparams_t *hp, zero_state_t *d_state, void *ws,
-             cudaStream_t s, bool decide_pdl)
+             cudaStream_t s, bool decide_pdl, const ListDev *pre = nullptr)
 {
     int rc;
-    TensorEntry *ents = nullptr;
-    Chunk *tiles = nullptr;
-    int64_t n_tiles = 0;
+    ListDev L;
     bool aligned32 = grads->n != 1 || flat_aligned32(grads, master, m, v);
     if (grads->n > 1) {
-        if ((rc = upload_table(grads, master, m, v, p_lp, ws, s, kTile, &n_tiles, &ents, &tiles, &aligned32)) !=
-            ZERO_OK)
-            return rc;
-        if (n_tiles > 0x7fffffff)
-            return ZERO_EINVAL;
-        decide_pdl = false;  // a copy now precedes the decision kernel
+        if (pre) {
+            L = *pre;
+        } else {
+            if ((rc = upload_list(grads, master, m, v, p_lp, ws, s, &L)) != ZERO_OK)
+                return rc;
+            decide_pdl = false;  // a copy now precedes the decision kernel
+        }
+        aligned32 = L.aligned32;
     }
     StepScalars *sc = reinterpret_cast<StepScalars *>(static_cast<unsigned char *>(ws) + kWsScalars);
     const DecideArgs a = decide_args(hp);
@@ -759,7 +785,7 @@ int run_step(const zero_tlist_t *grads, const zero_tlist_t *master, const zero_t
         return rc;
     if (grads->n == 0)
         return ZERO_OK;
-    return launch_pass2(grads, master, m, v, p_lp, sc, ws, s, ents, tiles, n_tiles, aligned32);
+    return launch_pass2(grads, master, m, v, p_lp, sc, ws, s, L, aligned32);
 }
 
 }  // namespace
@@ -954,17 +980,21 @@ extern "C" int zero_step(const zero_tlist_t *grads, const zero_tlist_t *master, 
         }
         if (rc != ZERO_OK)
             return rc;
-        return launch_pass2(grads, master, m, v, p_lp, sc, ws, s, nullptr, nullptr, 0,
-                            flat_aligned32(grads, master, m, v));
+        return launch_pass2(grads, master, m, v, p_lp, sc, ws, s, ListDev{}, flat_aligned32(grads, master, m, v));
     }
+    // a list: its table copied once, for both passes, before pass 1
+    ListDev L;
+    if (grads->n > 1 && (rc = upload_list(grads, master, m, v, p_lp, ws, s, &L)) != ZERO_OK)
+        return rc;
+    const ListDev *pre = grads->n > 1 ? &L : nullptr;
     switch (grads->dtype) {
-    case ZERO_F16: rc = launch_norm<ZERO_F16>(grads, total, d_state, 0, ws, s, false); break;
-    case ZERO_BF16: rc = launch_norm<ZERO_BF16>(grads, total, d_state, 0, ws, s, false); break;
-    default: rc = launch_norm<ZERO_F32>(grads, total, d_state, 0, ws, s, false); break;
+    case ZERO_F16: rc = launch_norm<ZERO_F16>(grads, total, d_state, 0, ws, s, false, FoldedDecision{}, pre); break;
+    case ZERO_BF16: rc = launch_norm<ZERO_BF16>(grads, total, d_state, 0, ws, s, false, FoldedDecision{}, pre); break;
+    default: rc = launch_norm<ZERO_F32>(grads, total, d_state, 0, ws, s, false, FoldedDecision{}, pre); break;
     }
     if (rc != ZERO_OK)
         return rc;
-    return run_step(grads, master, m, v, p_lp, hp, d_state, ws, s, false);
+    return run_step(grads, master, m, v, p_lp, hp, d_state, ws, s, pre != nullptr, pre);
 }
 
 // ------------------------------------------------------------- pass 1 without workspace

@@ -68,12 +68,6 @@ struct TensorEntry {
     int64_t numel;
 };
 
-// One work item: elements [index * size, min(numel, (index+1) * size)) of
-// tensor `tensor`, size being kChunk (pass 1) or kTile (pass 2).
-struct Chunk {
-    int32_t tensor;
-    int32_t index;
-};
 
 // Workspace layout (all offsets 256-byte aligned):
 //   [0, 256)            header: reduction ticket
@@ -82,10 +76,11 @@ struct Chunk {
 //   [512, 512 + 16*kMaxBlocks)  per-block partials of the norm pass (double2)
 //   then                GroupArea: tickets and partials of the block groups
 //                       of a one-shot reduction
-//   then                TensorEntry[max_tensors], then the work items of
-//                       the current pass (Chunk[], at most max_items of
-//                       them); a flat one-shot reduction keeps its per-block
-//                       partials here instead
+//   then                a list's table: TensorEntry[n], then for each
+//                       tensor the index of its first pass-2 tile and of
+//                       its first pass-1 chunk (two int64 prefix arrays of
+//                       n + 1); a flat one-shot reduction keeps its
+//                       per-block partials here instead
 struct WsHeader {
     unsigned int ticket;
 };
@@ -110,16 +105,15 @@ constexpr size_t kWsTable = (kWsGroups + sizeof(GroupArea) + 255) & ~(size_t)255
 
 inline size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
 
-// Upper bound on the work items of a list (pass 2's tiles outnumber pass
-// 1's chunks).
-inline int64_t max_items(int64_t max_tensors, int64_t max_total_numel)
+// Bytes of the table region: a list's table for n_tensors tensors, and at
+// least one 16-byte partial per 4096 elements of a flat pass over
+// total_numel elements.
+inline size_t table_bytes(int64_t n_tensors, int64_t total_numel)
 {
-    return max_tensors + max_total_numel / kTile + 1;
-}
-
-inline size_t table_bytes(int64_t n_tensors, int64_t n_chunks)
-{
-    return align256((size_t)n_tensors * sizeof(TensorEntry)) + align256((size_t)n_chunks * sizeof(Chunk));
+    const size_t list = align256((size_t)n_tensors * sizeof(TensorEntry)) +
+                        2 * align256((size_t)(n_tensors + 1) * sizeof(int64_t));
+    const size_t flat = align256((size_t)(total_numel / 256) + 256);
+    return list > flat ? list : flat;
 }
 
 // Records a CUDA error message for zero_strerror on this thread.
