@@ -169,8 +169,15 @@ __global__ void __launch_bounds__(kThreads)
     pdl_wait();
     double tot = 0.0;
     uint32_t bad = 0;
-    for (int64_t c = blockIdx.x; c < n_chunks; c += gridDim.x) {
-        const int64_t t = find_tensor(first, n_ents, c);
+    // a contiguous run of chunks per block: one search for its first
+    // chunk's tensor, then the tensor index only steps forward
+    const int64_t per = (n_chunks + gridDim.x - 1) / gridDim.x;
+    const int64_t c0 = (int64_t)blockIdx.x * per;
+    const int64_t c1 = c0 + per < n_chunks ? c0 + per : n_chunks;
+    int64_t t = c0 < c1 ? find_tensor(first, n_ents, c0) : 0;
+    for (int64_t c = c0; c < c1; ++c) {
+        while (__ldg(first + t + 1) <= c)
+            ++t;
         const TensorEntry e = ents[t];
         const int64_t start = (c - first[t]) * kChunk;
         const int64_t len = min(kChunk, e.numel - start);
