@@ -24,10 +24,14 @@
  *     nothing.  No C++ exception crosses the ABI.
  *   - The caller owns all memory.  The library never allocates device
  *     memory; it works in caller-provided device buffers and a caller-provided
- *     device workspace (see zero_workspace_bytes).
+ *     device workspace (see zero_workspace_bytes).  Calls that copy a table
+ *     into the workspace (lists of arrays, the parameter gather, the 1-bit
+ *     server) stage it through two pinned host buffers per device that the
+ *     library allocates on first use and keeps until the process exits.
  *   - `stream` is a cudaStream_t passed as void* (NULL = the legacy default
  *     stream).  Device work is enqueued asynchronously on it, on the calling
- *     thread's current CUDA device; no call synchronises the host.
+ *     thread's current CUDA device; no call synchronises the host (a table
+ *     copy may wait for the copy two table copies earlier to have finished).
  *   - Device arrays must start on a 16-byte boundary (ZERO_EALIGN otherwise);
  *     any element count is accepted, including 0 and counts of 2^31 and more.
  *   - Element types: ZERO_F16 (IEEE binary16), ZERO_BF16 (bfloat16),

@@ -14,6 +14,7 @@
 
 #include <cmath>
 #include <cstdint>
+#include <cstring>
 #include <mutex>
 #include <unordered_map>
 
@@ -570,6 +571,57 @@ int check_launch(const char *what)
         return ZERO_ECUDA;
     }
     return ZERO_OK;
+}
+
+// Copies a host-built table into the workspace without stalling the host.
+// A copy from pageable memory makes the host wait until the stream has
+// drained, which leaves the GPU idle between consecutive calls; the table is
+// therefore staged through one of two pinned host buffers per device,
+// allocated on first use and grown as needed, each reused only once the
+// copy out of it two uploads ago has completed (an event, long past by
+// then).  If pinned memory cannot be had, the copy goes from pageable memory.
+cudaError_t stage_upload(void *dst, const void *src, size_t bytes, cudaStream_t stream)
+{
+    struct Ring {
+        void *buf[2] = {nullptr, nullptr};
+        size_t cap[2] = {0, 0};
+        cudaEvent_t ev[2] = {nullptr, nullptr};
+        int next = 0;
+    };
+    static std::mutex mu;
+    static std::unordered_map<int, Ring> rings;
+    if (bytes == 0)
+        return cudaSuccess;
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess)
+        return e;
+    std::lock_guard<std::mutex> lock(mu);
+    Ring &r = rings[dev];
+    const int k = r.next;
+    r.next ^= 1;
+    if (r.ev[k] && (e = cudaEventSynchronize(r.ev[k])) != cudaSuccess)
+        return e;
+    if (r.cap[k] < bytes) {
+        if (r.buf[k])
+            cudaFreeHost(r.buf[k]);
+        r.buf[k] = nullptr;
+        r.cap[k] = 0;
+        const size_t want = bytes + bytes / 2;
+        if (cudaHostAlloc(&r.buf[k], want, cudaHostAllocDefault) == cudaSuccess) {
+            r.cap[k] = want;
+        } else {
+            cudaGetLastError();
+            r.buf[k] = nullptr;
+            return cudaMemcpyAsync(dst, src, bytes, cudaMemcpyHostToDevice, stream);
+        }
+    }
+    std::memcpy(r.buf[k], src, bytes);
+    if ((e = cudaMemcpyAsync(dst, r.buf[k], bytes, cudaMemcpyHostToDevice, stream)) != cudaSuccess)
+        return e;
+    if (!r.ev[k] && (e = cudaEventCreateWithFlags(&r.ev[k], cudaEventDisableTiming)) != cudaSuccess)
+        return e;
+    return cudaEventRecord(r.ev[k], stream);
 }
 
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }

@@ -452,8 +452,7 @@ extern "C" int zero_onebit_server(const uint32_t *const *worker_bits, const floa
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     unsigned char *w = static_cast<unsigned char *>(ws);
     std::vector<const uint32_t *> host(worker_bits, worker_bits + nd);
-    if (cudaMemcpyAsync(w + kWsTable, host.data(), (size_t)nd * sizeof(void *), cudaMemcpyHostToDevice, st) !=
-        cudaSuccess)
+    if (stage_upload(w + kWsTable, host.data(), (size_t)nd * sizeof(void *), st) != cudaSuccess)
         return check_launch("zero_onebit_server (table upload)");
     const StepScalars *sc = step_scalars(ws);
     const int64_t nv = S >> 3;

@@ -598,7 +598,7 @@ int upload_list(const zero_tlist_t *g, const zero_tlist_t *p, const zero_tlist_t
     ft[n] = tiles;
     fc[n] = chunks;
     unsigned char *base = static_cast<unsigned char *>(ws) + kWsTable;
-    if (cudaMemcpyAsync(base, host.data(), host.size(), cudaMemcpyHostToDevice, stream) != cudaSuccess)
+    if (stage_upload(base, host.data(), host.size(), stream) != cudaSuccess)
         return check_launch("workspace table upload");
     L->ents = reinterpret_cast<const TensorEntry *>(base);
     L->first_tile = reinterpret_cast<const int64_t *>(base + ent_bytes);
