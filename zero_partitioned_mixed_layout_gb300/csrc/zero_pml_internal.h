@@ -69,6 +69,13 @@ struct TensorEntry {
 };
 
 
+// One work item of a list: elements [index * size, min(numel, (index+1) *
+// size)) of tensor `tensor`, size being kChunk (pass 1) or kTile (pass 2).
+struct WorkItem {
+    int32_t tensor;
+    int32_t index;
+};
+
 // Workspace layout (all offsets 256-byte aligned):
 //   [0, 256)            header: reduction ticket
 //   [256, 384)          StepScalars of the current step
@@ -76,11 +83,11 @@ struct TensorEntry {
 //   [512, 512 + 16*kMaxBlocks)  per-block partials of the norm pass (double2)
 //   then                GroupArea: tickets and partials of the block groups
 //                       of a one-shot reduction
-//   then                a list's table: TensorEntry[n], then for each
-//                       tensor the index of its first pass-2 tile and of
-//                       its first pass-1 chunk (two int64 prefix arrays of
-//                       n + 1); a flat one-shot reduction keeps its
-//                       per-block partials here instead
+//   then                a list's table: TensorEntry[n], then the work
+//                       items of pass 2 (one per kTile elements of each
+//                       tensor) and of pass 1 (one per kChunk); a flat
+//                       one-shot reduction keeps its per-block partials
+//                       here instead
 struct WsHeader {
     unsigned int ticket;
 };
@@ -105,13 +112,15 @@ constexpr size_t kWsTable = (kWsGroups + sizeof(GroupArea) + 255) & ~(size_t)255
 
 inline size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
 
-// Bytes of the table region: a list's table for n_tensors tensors, and at
-// least one 16-byte partial per 4096 elements of a flat pass over
-// total_numel elements.
+// Bytes of the table region: a list's table for up to n_tensors tensors of
+// total_numel elements (entries, pass-2 tiles, pass-1 chunks; each tensor
+// adds at most one partial item to each), and at least one 16-byte partial
+// per 4096 elements of a flat pass over total_numel elements.
 inline size_t table_bytes(int64_t n_tensors, int64_t total_numel)
 {
     const size_t list = align256((size_t)n_tensors * sizeof(TensorEntry)) +
-                        2 * align256((size_t)(n_tensors + 1) * sizeof(int64_t));
+                        align256((size_t)(total_numel / kTile + n_tensors + 1) * sizeof(WorkItem)) +
+                        align256((size_t)(total_numel / kChunk + n_tensors + 1) * sizeof(WorkItem));
     const size_t flat = align256((size_t)(total_numel / 256) + 256);
     return list > flat ? list : flat;
 }
