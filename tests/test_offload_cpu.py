@@ -140,3 +140,24 @@ def test_copy_and_errors(zp):
     with pytest.raises(zp.ZeroError):
         zp.zero_offload_apply(np.zeros(4, np.float16), np.zeros(4, np.float32), np.zeros(4, np.float32),
                               np.zeros(4, np.float32), None, zp.OffloadScalars(), n_threads=-1)
+
+
+def test_every_f16_gradient_value_converts_exactly(zp):
+    """All 63,488 finite binary16 values (and +-inf) through the host update
+    with beta1 = 0 and no loss scale: the new momentum is the gradient's
+    binary32 value, which must equal numpy's exact conversion."""
+    bits = np.arange(1 << 16, dtype=np.uint32).astype(np.uint16)
+    finite = (bits & 0x7C00) != 0x7C00
+    infs = (bits & 0x7FFF) == 0x7C00
+    keep = bits[finite | infs]
+    g = keep.view(np.float16)
+    n = g.size
+    st = host_state(zp, 1.0)
+    sc = zp.zero_offload_decide(st, zp.HParams(beta1=0.0))
+    p = np.zeros(n, np.float32)
+    m = np.zeros(n, np.float32)
+    v = np.zeros(n, np.float32)
+    zp.zero_offload_apply(np.ascontiguousarray(g), p, m, v, None, sc, n_threads=2)
+    # m' = 0*0 + 1*g: -0 comes out as +0 (0 + -0 = +0), every other value as is
+    want = np.float32(0.0) + g.astype(np.float32)
+    assert m.tobytes() == want.tobytes()

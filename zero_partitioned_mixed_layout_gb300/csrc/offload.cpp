@@ -118,11 +118,26 @@ private:
     bool stop_ = false;
 };
 
+// binary16 -> binary32, exact, in integer and binary32 operations that the
+// compiler vectorises (a _Float16 conversion is not vectorised for the
+// generic Arm target): the exponent and mantissa move to the binary32
+// positions and one exact multiplication by 2^112 rebiases the exponent (a
+// subnormal half becomes a subnormal single before the multiplication and a
+// normal one after it); an all-ones exponent (inf, NaN) maps to all ones.
+// NaN payloads are kept as they are (a skipped step never reads them).
 inline float from_f16(uint16_t b)
 {
-    _Float16 h;
-    std::memcpy(&h, &b, sizeof h);
-    return (float)h;
+    const uint32_t em = (uint32_t)(b & 0x7FFFu) << 13;
+    float f;
+    std::memcpy(&f, &em, sizeof f);
+    f = f * 0x1p112f;
+    uint32_t r;
+    std::memcpy(&r, &f, sizeof r);
+    r = (b & 0x7C00u) == 0x7C00u ? (em | 0x7F800000u) : r;
+    r |= (uint32_t)(b & 0x8000u) << 16;
+    float out;
+    std::memcpy(&out, &r, sizeof out);
+    return out;
 }
 
 inline uint16_t to_f16(float x)
