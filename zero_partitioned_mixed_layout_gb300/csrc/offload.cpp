@@ -133,7 +133,8 @@ inline float from_f16(uint16_t b)
     f = f * 0x1p112f;
     uint32_t r;
     std::memcpy(&r, &f, sizeof r);
-    r = (b & 0x7C00u) == 0x7C00u ? (em | 0x7F800000u) : r;
+    const uint32_t special = 0u - (uint32_t)((b & 0x7C00u) == 0x7C00u);  // all ones for inf / NaN
+    r = (r & ~special) | ((em | 0x7F800000u) & special);
     r |= (uint32_t)(b & 0x8000u) << 16;
     float out;
     std::memcpy(&out, &r, sizeof out);
