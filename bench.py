@@ -474,15 +474,18 @@ def run_ours(args):
     achieved = wl.bytes_adam * S / (adam_ms * 1e-3) / 1e9
     cpu = None
     if not args.no_cpu_baseline and world == 1:
-        n_sample = 1 << 24
-        cv, cdt = oracle_run(n_sample, 3, 0)
-        av, adt, procs = oracle_run_all_cores(n_sample, 3, 1)
+        # about 10-20 s of CPU work in all: 10 full steps of 2^24 params on
+        # one core, then on every core at once
+        n_sample, c_steps = 1 << 24, 10
+        cv, cdt = oracle_run(n_sample, c_steps, 1)
+        av, adt, procs = oracle_run_all_cores(n_sample, c_steps, 1)
         cpu = {"value": av, "unit": UNIT, "cores": procs, "kind": "oracle",
-               "sample": f"{procs} processes (one per host core), each 3 full steps on its own "
+               "sample": f"{procs} processes (one per host core), each {c_steps} full steps on its own "
                          f"{n_sample} params shaped like the GPT-2 1.5B Nd=16 shard, "
-                         f"{adt:.1f} s wall; the oracle as it stands (single-threaded scalar C)",
+                         f"{adt:.1f} s wall ({procs * adt:.0f} s of CPU); the oracle as it stands "
+                         f"(single-threaded scalar C)",
                "single_core": {"value": cv, "unit": UNIT, "cores": 1, "seconds": cdt,
-                               "sample": f"first {n_sample} params of the shard, 3 full steps"}}
+                               "sample": f"first {n_sample} params of the shard, {c_steps} full steps"}}
     default = args.workload == WORKLOAD
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
