@@ -36,6 +36,21 @@
  *     any element count is accepted, including 0 and counts of 2^31 and more.
  *   - Element types: ZERO_F16 (IEEE binary16), ZERO_BF16 (bfloat16),
  *     ZERO_F32 (IEEE binary32).
+ *   - CUDA graphs.  A call whose device work is kernels alone may be issued
+ *     while `stream` is being captured; the graph then holds the pointers,
+ *     sizes and hyperparameters of the captured call, while the device state
+ *     (loss scale, step count, the norm) moves on at every replay exactly as
+ *     it would over the same calls issued one by one.  These are: zero_step,
+ *     zero_adam_step and zero_grad_norm_overflow on one array per list (a
+ *     flat shard), zero_accumulate_grads, zero_reduce_grads,
+ *     zero_grad_norm_overflow_static (after a first call outside capture),
+ *     zero_gather_params / zero_scatter_params with at most 64 tensors and
+ *     256 shards, zero_onebit_worker, zero_onebit_server with at most 256
+ *     workers, and zero_onebit_update.  A call that would copy a host-built
+ *     table (a list of several arrays, a larger gather or server) returns
+ *     ZERO_ECAPTURE under capture, having enqueued nothing: a captured copy
+ *     would read the staging buffer when the graph is replayed, after later
+ *     calls have reused it.  Issue those calls outside capture.
  */
 #ifndef ZERO_PML_H
 #define ZERO_PML_H
@@ -58,6 +73,7 @@ extern "C" {
 #define ZERO_ECAPACITY (-6)  /* an output array is too small (see *n_frags) */
 #define ZERO_ECUDA (-7)      /* the CUDA runtime reported an error */
 #define ZERO_ELAYOUT (-8)    /* nd < 1, align < 1 or not a power of two */
+#define ZERO_ECAPTURE (-9)   /* a table copy asked for while the stream is captured */
 
 #define ZERO_F16 0
 #define ZERO_BF16 1
@@ -435,7 +451,13 @@ int zero_onebit_worker(const void *grad, int32_t gdtype, const float *m, const u
  * of nd device pointers, each to S/32 words (the chunk's signs from worker
  * i); worker_scales: device array of nd floats; e_s: the server error (S
  * fp32, updated); bits: S/32 words and scale: one device float (written).
- * At most 4096 workers (ZERO_ECAPACITY). */
+ * At most 4096 workers (ZERO_ECAPACITY).  Up to 256 workers the pointers
+ * travel as a launch argument; beyond, as a table copied into the
+ * workspace (not capturable: ZERO_ECAPTURE under stream capture).  The
+ * result is the rank-order sum itself: each block tabulates the sums of the
+ * first min(nd, 14) workers' terms for every sign pattern, with the same
+ * additions in the same order, and adds the remaining workers' terms to the
+ * entry an element's signs select. */
 int zero_onebit_server(const uint32_t *const *worker_bits, const float *worker_scales, int32_t nd, int64_t S,
                        float *e_s, uint32_t *bits, float *scale, void *ws, size_t ws_bytes, void *stream);
 

@@ -121,7 +121,7 @@ def test_workspace_bytes(zp):
 
 
 def test_error_strings(zp):
-    for code in range(0, -9, -1):
+    for code in range(0, -10, -1):
         s = zp.zero_strerror(code)
         assert s and s != "unknown error code"
     assert zp.zero_strerror(-99) == "unknown error code"

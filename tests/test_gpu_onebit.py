@@ -323,3 +323,72 @@ def test_onebit_argument_errors(zp):
     with pytest.raises(zp.ZeroError) as e:  # numel past nd * S
         zp.zero_onebit_update(bits, torch.ones(1, device=dev), 128, 129, big, None, big.clone(), None, ws)
     assert e.value.code == -4
+
+
+def server_case(zp, nd, S, seed, T=10):
+    """Random worker signs and scales and a server error for one chunk, with
+    the step's decision (no overflow) taken in the workspace by a worker call
+    on 32 elements."""
+    rng = np.random.default_rng(seed)
+    w = S // 32
+    hb = [rng.integers(0, 2 ** 32, w, dtype=np.uint64).astype(np.uint32) for _ in range(nd)]
+    hs = rng.uniform(1e-4, 1.1e-3, nd).astype(np.float32)
+    hf = (rng.standard_normal(S) * 1e-4).astype(np.float32)
+    d = {
+        "wbits": [torch.from_numpy(b.view(np.int32)).cuda() for b in hb],
+        "wscale": torch.from_numpy(hs).cuda(),
+        "es": torch.from_numpy(hf.copy()).cuda(),
+        "bits": torch.zeros(w, dtype=torch.int32, device="cuda"),
+        "scale": torch.zeros(1, dtype=torch.float32, device="cuda"),
+        "state": state_at(zp, 1024.0, T),
+        "ws": zp.new_workspace(nd, nd * S),
+    }
+    z = torch.zeros(32, dtype=torch.float32, device="cuda")
+    zp.zero_onebit_worker(torch.zeros(32, dtype=torch.float16, device="cuda"), z, z.clone(),
+                          torch.zeros(1, dtype=torch.int32, device="cuda"),
+                          torch.zeros(1, dtype=torch.float32, device="cuda"), zp.HParams(), T,
+                          d["state"], d["ws"])
+    return hb, hs, hf, d
+
+
+def check_server(hb, hs, hf, d):
+    """The GPU's server pass against the oracle's (handed the GPU's scale):
+    the new error and the signs bit for bit, the scale within the norm's
+    summation-order bound."""
+    torch.cuda.synchronize()
+    gs = float(d["scale"][0])
+    _, free = oracle.onebit_server([b.copy() for b in hb], list(hs), hf.copy())
+    assert abs(gs - free) <= 4 * SCALE_REL * free, "server scale"
+    f = hf.copy()
+    ob, _ = oracle.onebit_server(hb, list(hs), f, scale=gs)
+    assert to_host(d["es"]).tobytes() == f.tobytes(), "server error"
+    assert np.array_equal(words(d["bits"]), ob), "server signs"
+
+
+@pytest.mark.parametrize("nd,S", [(1, 1184), (5, 4128), (8, 1184), (9, 4128), (14, 8192), (15, 4128),
+                                  (16, 1_280_000), (17, 4128), (24, 1184), (33, 8192), (256, 4128),
+                                  (257, 1184), (300, 4128)])
+def test_onebit_server_worker_counts(zp, nd, S):
+    """The server pass over every split of its sum: the tabulated first
+    min(nd, 14) workers, workers 14 and 15 added after the table, whole and
+    partial groups of 8 past 16; power-of-two counts (the mean as a product)
+    and others (a division); pointers as a launch argument (nd <= 256) and
+    as a workspace table; chunks that end inside a warp's 1024 elements."""
+    hb, hs, hf, d = server_case(zp, nd, S, 1000 + nd)
+    zp.zero_onebit_server(d["wbits"], d["wscale"], d["es"], d["bits"], d["scale"], d["ws"])
+    check_server(hb, hs, hf, d)
+
+
+def test_onebit_server_equal_scales(zp):
+    """Equal worker scales and a zero server error: the table holds many
+    equal entries and every element with as many + as - signs sums to an
+    exact zero (the mean's zero numerator takes the division's special
+    path on other counts; here the product)."""
+    nd, S = 16, 8192
+    hb, hs, hf, d = server_case(zp, nd, S, 4242)
+    hs[:] = np.float32(5e-4)
+    d["wscale"].copy_(torch.from_numpy(hs))
+    hf[:] = 0.0
+    d["es"].zero_()
+    zp.zero_onebit_server(d["wbits"], d["wscale"], d["es"], d["bits"], d["scale"], d["ws"])
+    check_server(hb, hs, hf, d)

@@ -13,6 +13,7 @@ from .binding import (  # noqa: F401
     HParams,
     Layout,
     ZeroError,
+    ZERO_ECAPTURE,
     ZERO_BF16,
     ZERO_F16,
     ZERO_F32,

@@ -19,6 +19,7 @@ _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "libzero_pml.so")
 
 ZERO_OK = 0
+ZERO_ECAPTURE = -9
 ZERO_F16, ZERO_BF16, ZERO_F32 = 0, 1, 2
 STATE_BYTES = 64
 

@@ -580,7 +580,7 @@ int check_launch(const char *what)
 // allocated on first use and grown as needed, each reused only once the
 // copy out of it two uploads ago has completed (an event, long past by
 // then).  If pinned memory cannot be had, the copy goes from pageable memory.
-cudaError_t stage_upload(void *dst, const void *src, size_t bytes, cudaStream_t stream)
+cudaError_t stage_copy(void *dst, const void *src, size_t bytes, cudaStream_t stream)
 {
     struct Ring {
         void *buf[2] = {nullptr, nullptr};
@@ -590,8 +590,6 @@ cudaError_t stage_upload(void *dst, const void *src, size_t bytes, cudaStream_t 
     };
     static std::mutex mu;
     static std::unordered_map<int, Ring> rings;
-    if (bytes == 0)
-        return cudaSuccess;
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess)
@@ -622,6 +620,28 @@ cudaError_t stage_upload(void *dst, const void *src, size_t bytes, cudaStream_t 
     if (!r.ev[k] && (e = cudaEventCreateWithFlags(&r.ev[k], cudaEventDisableTiming)) != cudaSuccess)
         return e;
     return cudaEventRecord(r.ev[k], stream);
+}
+
+// The table copy of a call, or ZERO_ECAPTURE with nothing enqueued while
+// `stream` is being captured into a graph: a captured copy would read the
+// staging buffer when the graph is replayed, after later calls have reused
+// it.  Returns ZERO_OK, ZERO_ECAPTURE or ZERO_ECUDA (the message under `what`).
+int stage_upload(void *dst, const void *src, size_t bytes, cudaStream_t stream, const char *what)
+{
+    if (bytes == 0)
+        return ZERO_OK;
+    cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+    cudaError_t e = cudaStreamIsCapturing(stream, &cs);
+    if (e == cudaSuccess && cs != cudaStreamCaptureStatusNone)
+        return ZERO_ECAPTURE;
+    if (e == cudaSuccess)
+        e = stage_copy(dst, src, bytes, stream);
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        set_cuda_error(what, (int)e, cudaGetErrorString(e));
+        return ZERO_ECUDA;
+    }
+    return ZERO_OK;
 }
 
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }

@@ -291,8 +291,9 @@ int run_copy(bool gather, void *const *shards, int32_t nd, int64_t shard_numel, 
     std::copy(shards, shards + nd, reinterpret_cast<void **>(host.data()));
     std::copy(ents.begin(), ents.end(), reinterpret_cast<GatherEntry *>(host.data() + sb));
     unsigned char *base = static_cast<unsigned char *>(ws);
-    if (stage_upload(base, host.data(), host.size(), st) != cudaSuccess)
-        return check_launch("gather table upload");
+    const int rc = stage_upload(base, host.data(), host.size(), st, "gather table upload");
+    if (rc != ZERO_OK)
+        return rc;
     char *const *d_shards = reinterpret_cast<char *const *>(base);
     const GatherEntry *d_ents = reinterpret_cast<const GatherEntry *>(base + sb);
     if (gather && es == 2)

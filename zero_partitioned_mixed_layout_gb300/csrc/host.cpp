@@ -39,6 +39,9 @@ extern "C" const char *zero_strerror(int code)
     case ZERO_ECAPACITY: base = "output array too small"; break;
     case ZERO_ECUDA: base = "CUDA runtime error"; break;
     case ZERO_ELAYOUT: base = "bad layout parameters (nd < 1, align not a power of two, or too large)"; break;
+    case ZERO_ECAPTURE:
+        base = "this call copies a host table, which a stream capture cannot hold; issue it outside capture";
+        break;
     default: base = "unknown error code"; break;
     }
     if (code == ZERO_ECUDA && zpml::g_err[0])

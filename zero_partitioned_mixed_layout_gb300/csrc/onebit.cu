@@ -157,60 +157,211 @@ __global__ void __launch_bounds__(kThreads) k_onebit_worker(const void *g, Momen
 
 // Server, first pass over the chunk: y = (sum over workers in rank order of
 // +-scale_k) / Nd + f, stored over f; the squared norm of y into the scale.
-// The workers' sign pointers and scales sit in shared memory; each thread
-// loads the words of 8 workers before it adds them in.
-constexpr int kServerBatch = 8;
-// Workers per server call: their pointers and scales (12 bytes each) fit the
-// default 48 KiB of dynamic shared memory.
+//
+// Per element the sum is Nd dependent binary32 additions, which would make
+// the pass bound by instruction issue rather than by memory.  But an element
+// enters the sum only through its Nd signs, and the scales are the same for
+// the whole chunk: so each block first tabulates, in shared memory, the
+// rank-order sum for every sign pattern of the first P = min(Nd, 14) workers
+// (2^P binary32 values, built one worker at a time with the very additions
+// an element would make), and an element then looks its first P signs up
+// and adds the remaining workers' terms in rank order.  Same additions,
+// same order, same bits.
+//
+// Data movement: a warp takes 1024 elements at a time (128 vectors of 8;
+// lane l holds vectors v0 + l + 32v, v = 0..3), so that its load of one
+// worker's 32 sign words is one full 128-byte line; shuffles hand each lane
+// the words of its vectors.  A vector's signs from 8 workers are 8 bytes;
+// an 8x8 bit-matrix transpose turns them into one byte per element, bit q
+// for worker q of the group.  Bytes per chunk element: Nd/8 + 4 + 4.
+constexpr int kTableBits = 14;
+// Workers per server call: their pointers and scales (12 bytes each) and
+// the 64 KiB table fit in shared memory.
 constexpr int kMaxServerWorkers = 4096;
+// Workers whose sign pointers travel as a launch argument (no table copy,
+// so that the call can be captured into a graph).
+constexpr int kArgWorkers = 256;
+struct WorkerPtrs {
+    const uint32_t *p[kArgWorkers];
+};
 
-__global__ void __launch_bounds__(kThreads) k_onebit_server(const uint32_t *const *wbits, const float *wscales,
-                                                            int nd, float *f, int64_t S, const StepScalars *scp,
-                                                            double2 *partials, WsHeader *hdr, float *scale)
+// 8x8 bit-matrix transpose (Hacker's Delight, section 7-3, the three-step
+// swap of 1x1, 2x2 and 4x4 blocks): bit c of byte r <-> bit r of byte c.
+__device__ __forceinline__ uint64_t transpose8(uint64_t x)
 {
-    extern __shared__ unsigned char s_raw[];
-    const uint32_t **s_ptr = reinterpret_cast<const uint32_t **>(s_raw);
-    float *s_scale = reinterpret_cast<float *>(s_raw + sizeof(void *) * (size_t)nd);
+    uint64_t t = (x ^ (x >> 7)) & 0x00AA00AA00AA00AAull;
+    x ^= t ^ (t << 7);
+    t = (x ^ (x >> 14)) & 0x0000CCCC0000CCCCull;
+    x ^= t ^ (t << 14);
+    t = (x ^ (x >> 28)) & 0x00000000F0F0F0F0ull;
+    x ^= t ^ (t << 28);
+    return x;
+}
+
+// The signs of 8 workers for this lane's vector (words w[0..7] of the
+// warp's 32-word span, from lane `src`; byte `psel` selects this lane's
+// byte): byte j of the result holds element j's signs, bit q = worker q.
+__device__ __forceinline__ uint64_t group_signs(const uint32_t *w, int src, uint32_t psel)
+{
+    uint32_t b[2];
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+        const uint32_t x0 = __shfl_sync(0xffffffffu, w[4 * h], src);
+        const uint32_t x1 = __shfl_sync(0xffffffffu, w[4 * h + 1], src);
+        const uint32_t x2 = __shfl_sync(0xffffffffu, w[4 * h + 2], src);
+        const uint32_t x3 = __shfl_sync(0xffffffffu, w[4 * h + 3], src);
+        b[h] = __byte_perm(__byte_perm(x0, x1, psel), __byte_perm(x2, x3, psel), 0x5410);
+    }
+    return transpose8((uint64_t)b[0] | ((uint64_t)b[1] << 32));
+}
+
+// +scale where the sign bit (at bit 31 of t) is set, -scale where it is
+// clear: the scale's bits with the sign bit flipped.
+__device__ __forceinline__ float signed_scale(uint32_t scale_bits, uint32_t t)
+{
+    return __uint_as_float(scale_bits ^ (~t & 0x80000000u));
+}
+
+// The dynamic shared memory of the server: the table, the worker pointers
+// and the scales.
+__host__ __device__ constexpr size_t server_smem_bytes(int nd)
+{
+    return sizeof(float) * ((size_t)1 << (nd < kTableBits ? nd : kTableBits)) +
+           (sizeof(void *) + sizeof(float)) * (size_t)nd;
+}
+
+template <bool kPow2>
+__device__ __forceinline__ void server_body(const uint32_t *const *wbits, const float *wscales, int nd, float inv_nd,
+                                            float *f, int64_t S, const StepScalars *scp, double2 *partials,
+                                            WsHeader *hdr, float *scale)
+{
+    extern __shared__ __align__(16) unsigned char s_raw[];
+    const int P = nd < kTableBits ? nd : kTableBits;
+    float *T = reinterpret_cast<float *>(s_raw);
+    const uint32_t **s_ptr = reinterpret_cast<const uint32_t **>(s_raw + sizeof(float) * ((size_t)1 << P));
+    float *s_scale = reinterpret_cast<float *>(s_ptr + nd);
     pdl_wait();
     for (int k = threadIdx.x; k < nd; k += kThreads) {
         s_ptr[k] = wbits[k];
         s_scale[k] = wscales[k];
     }
     __syncthreads();
+    // T[p] = the rank-order sum over workers k < P of +-scale_k (+ where
+    // bit k of p is set), the first term taken as it is
+    if (threadIdx.x < 2)
+        T[threadIdx.x] = threadIdx.x ? s_scale[0] : -s_scale[0];
+    __syncthreads();
+    for (int k = 1; k < P; ++k) {
+        const int half = 1 << k;
+        const float sk = s_scale[k];
+        for (int q = threadIdx.x; q < half; q += kThreads) {
+            const float t = T[q];
+            T[q + half] = __fadd_rn(t, sk);
+            T[q] = __fadd_rn(t, -sk);
+        }
+        __syncthreads();
+    }
     const bool skip = scp->skip != 0;
+    const int lane = threadIdx.x & 31;
+    const uint32_t psel = (uint32_t)(lane & 3) | ((uint32_t)((lane & 3) + 4) << 4);
+    const uint32_t pmask = (1u << P) - 1u;
+    // workers P..15 that the table leaves out (none when Nd <= 14)
+    const int upto16 = nd < 16 ? nd : 16;
+    const uint32_t sb14 = 14 < upto16 ? __float_as_uint(s_scale[14]) : 0u;
+    const uint32_t sb15 = 15 < upto16 ? __float_as_uint(s_scale[15]) : 0u;
     const float count = (float)nd;
+    const int64_t nv = skip ? 0 : S >> 3, nw = S >> 5;
+    const int64_t chunks = (nv + 127) >> 7;
     SquareSum acc;
-    const int64_t nv = skip ? 0 : S >> 3;
-    for (int64_t i = (int64_t)blockIdx.x * kThreads + threadIdx.x; i < nv; i += (int64_t)gridDim.x * kThreads) {
-        float a[8];
-        const int shift = 8 * (int)(i & 3);
-        for (int k0 = 0; k0 < nd; k0 += kServerBatch) {
-            uint32_t w[kServerBatch];
+    for (int64_t c = (int64_t)blockIdx.x * kWarps + (threadIdx.x >> 5); c < chunks;
+         c += (int64_t)gridDim.x * kWarps) {
+        const int64_t v0 = c << 7, w0 = c << 5;
+        const bool wok = w0 + lane < nw;
+        float y[4][8];
 #pragma unroll
-            for (int q = 0; q < kServerBatch; ++q)
-                w[q] = k0 + q < nd ? __ldg(s_ptr[k0 + q] + (i >> 2)) : 0u;
+        for (int v = 0; v < 4; ++v) {
+            const int64_t i = v0 + lane + 32 * v;
+            if (i < nv)
+                ld8(f + 8 * i, y[v]);
+        }
+        float a[4][8];
+        {
+            uint32_t w[16];
 #pragma unroll
-            for (int q = 0; q < kServerBatch; ++q) {
-                if (k0 + q < nd) {
-                    const uint32_t byte = (w[q] >> shift) & 0xFFu;
-                    const float sc = s_scale[k0 + q];
+            for (int k = 0; k < 16; ++k)
+                w[k] = k < nd && wok ? __ldg(s_ptr[k] + w0 + lane) : 0u;
 #pragma unroll
-                    for (int j = 0; j < 8; ++j) {
-                        const float c = ((byte >> j) & 1u) ? sc : -sc;
-                        a[j] = k0 + q == 0 ? c : __fadd_rn(a[j], c);
+            for (int v = 0; v < 4; ++v) {
+                const int src = 8 * v + (lane >> 2);
+                const uint64_t lo = group_signs(w, src, psel), hi = group_signs(w + 8, src, psel);
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                    const uint32_t pl = (uint32_t)(lo >> (8 * j)) & 0xFFu, ph = (uint32_t)(hi >> (8 * j)) & 0xFFu;
+                    float x = T[(pl | (ph << 8)) & pmask];
+                    if (P == 14 && upto16 > 14)
+                        x = __fadd_rn(x, signed_scale(sb14, ph << 25));
+                    if (P == 14 && upto16 > 15)
+                        x = __fadd_rn(x, signed_scale(sb15, ph << 24));
+                    a[v][j] = x;
+                }
+            }
+        }
+        // workers 16 and up, 8 at a time
+        for (int g = 16; g < nd; g += 8) {
+            uint32_t w[8];
+#pragma unroll
+            for (int q = 0; q < 8; ++q)
+                w[q] = g + q < nd && wok ? __ldg(s_ptr[g + q] + w0 + lane) : 0u;
+#pragma unroll
+            for (int v = 0; v < 4; ++v) {
+                const uint64_t gs = group_signs(w, 8 * v + (lane >> 2), psel);
+#pragma unroll
+                for (int q = 0; q < 8; ++q) {
+                    if (g + q < nd) {
+                        const uint32_t sb = __float_as_uint(s_scale[g + q]);
+#pragma unroll
+                        for (int j = 0; j < 8; ++j)
+                            a[v][j] = __fadd_rn(a[v][j], signed_scale(sb, (uint32_t)(gs >> (8 * j)) << (31 - q)));
                     }
                 }
             }
         }
-        float y[8];
-        ld8(f + 8 * i, y);
 #pragma unroll
-        for (int j = 0; j < 8; ++j)
-            y[j] = __fadd_rn(__fdiv_rn(a[j], count), y[j]);
-        st8(f + 8 * i, y);
-        acc.add(y);
+        for (int v = 0; v < 4; ++v) {
+            const int64_t i = v0 + lane + 32 * v;
+            if (i < nv) {
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                    // a power-of-two count: the product by its reciprocal is
+                    // the correctly rounded quotient itself
+                    const float mean = kPow2 ? __fmul_rn(a[v][j], inv_nd) : __fdiv_rn(a[v][j], count);
+                    y[v][j] = __fadd_rn(mean, y[v][j]);
+                }
+                st8(f + 8 * i, y[v]);
+                acc.add(y[v]);
+            }
+        }
     }
     scale_finish(acc.total(), partials, hdr, S, scale, skip);
+}
+
+// The worker pointers from a table in the workspace, or as a launch argument.
+template <bool kPow2>
+__global__ void __launch_bounds__(kThreads, 2) k_onebit_server(const uint32_t *const *wbits, const float *wscales,
+                                                               int nd, float inv_nd, float *f, int64_t S,
+                                                               const StepScalars *scp, double2 *partials,
+                                                               WsHeader *hdr, float *scale)
+{
+    server_body<kPow2>(wbits, wscales, nd, inv_nd, f, S, scp, partials, hdr, scale);
+}
+
+template <bool kPow2>
+__global__ void __launch_bounds__(kThreads, 2) k_onebit_server_args(const __grid_constant__ WorkerPtrs wp,
+                                                                    const float *wscales, int nd, float inv_nd,
+                                                                    float *f, int64_t S, const StepScalars *scp,
+                                                                    double2 *partials, WsHeader *hdr, float *scale)
+{
+    server_body<kPow2>(wp.p, wscales, nd, inv_nd, f, S, scp, partials, hdr, scale);
 }
 
 // Second pass of a compression (worker or server): the signs of x, 32 to a
@@ -443,7 +594,10 @@ extern "C" int zero_onebit_server(const uint32_t *const *worker_bits, const floa
         if (!device_ptr(e_s) || !device_ptr(bits) || !device_ptr(scale))
             return ZERO_EINVAL;
     }
-    const size_t table = align256((size_t)nd * sizeof(void *));
+    // up to kArgWorkers pointers go as a launch argument; more, as a table
+    // in the workspace
+    const bool by_arg = nd <= kArgWorkers;
+    const size_t table = by_arg ? 0 : align256((size_t)nd * sizeof(void *));
     int rc = check_ws_table(ws, ws_bytes, table);
     if (rc != ZERO_OK)
         return rc;
@@ -451,19 +605,48 @@ extern "C" int zero_onebit_server(const uint32_t *const *worker_bits, const floa
         return ZERO_OK;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     unsigned char *w = static_cast<unsigned char *>(ws);
-    std::vector<const uint32_t *> host(worker_bits, worker_bits + nd);
-    if (stage_upload(w + kWsTable, host.data(), (size_t)nd * sizeof(void *), st) != cudaSuccess)
-        return check_launch("zero_onebit_server (table upload)");
+    if (!by_arg) {
+        std::vector<const uint32_t *> host(worker_bits, worker_bits + nd);
+        rc = stage_upload(w + kWsTable, host.data(), (size_t)nd * sizeof(void *), st,
+                          "zero_onebit_server (table upload)");
+        if (rc != ZERO_OK)
+            return rc;
+    }
     const StepScalars *sc = step_scalars(ws);
     const int64_t nv = S >> 3;
-    const int grid = grid_for((const void *)k_onebit_server, (nv + kThreads - 1) / kThreads, kMaxBlocks, 4);
+    // persistent: two blocks per SM (each holds its own table), a warp per
+    // 1024 elements at a time
+    const int64_t warps = (nv + 127) >> 7;
+    int64_t grid = (int64_t)sm_count() * 2;
+    if (grid > (warps + kWarps - 1) / kWarps)
+        grid = (warps + kWarps - 1) / kWarps;
+    if (grid > kMaxBlocks)
+        grid = kMaxBlocks;
+    if (grid < 1)
+        grid = 1;
+    const bool pow2 = (nd & (nd - 1)) == 0;
+    const float inv_nd = pow2 ? 1.0f / (float)nd : 0.0f;  // exact: nd <= 2^12
+    const size_t smem = server_smem_bytes(nd);
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)grid);
     cfg.blockDim = dim3((unsigned)kThreads);
-    cfg.dynamicSmemBytes = (size_t)nd * (sizeof(void *) + sizeof(float));
+    cfg.dynamicSmemBytes = smem;
     cfg.stream = st;
-    cudaLaunchKernelEx(&cfg, k_onebit_server, (const uint32_t *const *)(w + kWsTable), worker_scales, (int)nd, e_s,
-                       S, sc, reinterpret_cast<double2 *>(w + kWsPartials), reinterpret_cast<WsHeader *>(w), scale);
+    double2 *partials = reinterpret_cast<double2 *>(w + kWsPartials);
+    WsHeader *hdr = reinterpret_cast<WsHeader *>(w);
+    if (by_arg) {
+        WorkerPtrs wp = {};
+        for (int32_t k = 0; k < nd; ++k)
+            wp.p[k] = worker_bits[k];
+        auto kern = pow2 ? k_onebit_server_args<true> : k_onebit_server_args<false>;
+        cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        cudaLaunchKernelEx(&cfg, kern, wp, worker_scales, (int)nd, inv_nd, e_s, S, sc, partials, hdr, scale);
+    } else {
+        auto kern = pow2 ? k_onebit_server<true> : k_onebit_server<false>;
+        cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        cudaLaunchKernelEx(&cfg, kern, (const uint32_t *const *)(w + kWsTable), worker_scales, (int)nd, inv_nd, e_s,
+                           S, sc, partials, hdr, scale);
+    }
     if ((rc = check_launch("zero_onebit_server (first pass)")) != ZERO_OK)
         return rc;
     launch_k(k_onebit_sign, (int)((nv + kThreads - 1) / kThreads), kThreads, st, true, e_s, S, (const float *)scale,

@@ -582,8 +582,11 @@ int upload_list(const zero_tlist_t *g, const zero_tlist_t *p, const zero_tlist_t
             ch[c++] = WorkItem{(int32_t)i, (int32_t)j};
     }
     unsigned char *base = static_cast<unsigned char *>(ws) + kWsTable;
-    if (!host.empty() && stage_upload(base, host.data(), host.size(), stream) != cudaSuccess)
-        return check_launch("workspace table upload");
+    if (!host.empty()) {
+        const int rc = stage_upload(base, host.data(), host.size(), stream, "workspace table upload");
+        if (rc != ZERO_OK)
+            return rc;
+    }
     L->ents = reinterpret_cast<const TensorEntry *>(base);
     L->tiles = reinterpret_cast<const WorkItem *>(base + ent_bytes);
     L->chunks = reinterpret_cast<const WorkItem *>(base + ent_bytes + tile_bytes);
