@@ -805,6 +805,83 @@ def run_onebit(args):
     print(json.dumps(line), flush=True)
 
 
+def run_onebit_server(args):
+    """1-bit Adam's server call alone: chunk 0 of the GPT-2 1.5B layout in
+    16 shards (S = 97,350,784 elements), the 16 workers' signs and scales as
+    received messages; per call the first pass (the workers' mean from the
+    tabulated rank-order sums, plus the server error, and its squared norm)
+    and the sign pass (signs and the new error).  About 0.6 GB on the
+    device: the size for a full ncu capture of the server kernel."""
+    import torch
+
+    import zero_partitioned_mixed_layout_gb300 as zp
+    import zero_synth as zs
+    dev = torch.device("cuda", torch.cuda.current_device())
+    nd = 16
+    S = zp.zero_partition_layout(zs.WORKLOADS[WORKLOAD]["numel"](), nd, 128).shard_numel
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(zs.stream_seed(0, "misc", 43))
+    wbits = [torch.randint(-2 ** 31, 2 ** 31 - 1, (S // 32,), dtype=torch.int32, device=dev, generator=gen)
+             for _ in range(nd)]
+    wscale = torch.rand(nd, device=dev, generator=gen) * 1e-3 + 1e-4
+    e_s = zs.device_normal(S, 1e-4, 44, "misc", 5)
+    sbits = torch.zeros(S // 32, dtype=torch.int32, device=dev)
+    sscale = torch.zeros(1, device=dev)
+    state = torch.frombuffer(bytearray(zp.zero_state_init(65536.0)), dtype=torch.uint8).to(dev)
+    state[24:32] = torch.tensor([1000], dtype=torch.int64).view(torch.uint8).to(dev)  # warm-up done
+    ws = zp.new_workspace(nd, nd * S, dev)
+    stream = torch.cuda.current_stream(dev)
+    # the step's decision (no overflow) in the workspace, from a worker call
+    # on 32 elements
+    z = torch.zeros(32, device=dev)
+    zp.zero_onebit_worker(torch.zeros(32, dtype=torch.float16, device=dev), z, z.clone(),
+                          torch.zeros(1, dtype=torch.int32, device=dev), torch.zeros(1, device=dev),
+                          zp.HParams(**zs.HPARAMS), 1000, state, ws, stream=stream)
+
+    def step():
+        zp.zero_onebit_server(wbits, wscale, e_s, sbits, sscale, ws, stream=stream)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize(dev)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(dev.index) as clk:
+        t0 = time.perf_counter()
+        while time.perf_counter() - t0 < args.clock_preroll:
+            for _ in range(20):
+                step()
+            torch.cuda.synchronize(dev)
+        e0.record(stream)
+        for _ in range(args.steps):
+            step()
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+    dt = e0.elapsed_time(e1) / args.steps * 1e-3
+    # per chunk element: the workers' signs, e_s read and written (first
+    # pass); e_s read and written, the signs written (sign pass)
+    b_elem = nd / 8 + 8 + 8 + 1 / 8
+    peaks = measured_peaks()
+    peak = peaks["hbm_gbs"] if peaks else 6800.0
+    achieved = b_elem * S / dt / 1e9
+    line = {
+        "metric": "1-bit Adam server call chunk elements/sec & achieved HBM GB/s, 1 GPU",
+        "value": S / dt, "unit": "elements/s", "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": dt * 1e3, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "f32", "data": "synthetic",
+        "config": {"workload": "1-bit Adam server, chunk 0 of GPT-2 1.5B in 16 shards (97,350,784 elements), "
+                               "16 workers' random signs and scales", "elements": S, "workers": nd,
+                   "l2": "inputs larger than L2 (0.6 GB per call), no flush"},
+        "bytes_per_element": b_elem,
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
+                     "traffic": None, "kernel": f"server call (first pass + sign pass), {b_elem:.3f} B/element",
+                     "peak_source": "MEASURED_PEAKS.json hbm_gbs (of measured)" if peaks
+                     else "fallback 6.8 TB/s (of fallback)"},
+        "gpu_launches": 2 * args.steps,
+        "clocks": clk.summary(),
+    }
+    print(json.dumps(line), flush=True)
+
+
 def run_offload(args):
     """ZeRO-Offload on the GPT-2 1.5B Nd=16 shard: the fp32 master, momentum
     and variance (12 B/param) live in pinned host memory, the gradient and
@@ -948,7 +1025,7 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--workload", default=WORKLOAD,
                     choices=["gpt2_1p5b_nd16", "tiny", "gpt2_1p5b_full", "stack_100b_nd400",
-                             "frag_10k", "flat", "offload", "stage2", "gather", "onebit"],
+                             "frag_10k", "flat", "offload", "stage2", "gather", "onebit", "onebit_server"],
                     help="default: the GPT-2 1.5B Nd=16 shard the metric is quoted on")
     ap.add_argument("--log2n", type=int, default=26, help="size of the flat workload (2^k)")
     ap.add_argument("--clock-preroll", type=float, default=1.0,
@@ -958,11 +1035,11 @@ def main():
         ap.error("--warmup must be at least 3")
     if args.impl == "reference":
         run_reference(args)
-    elif args.workload in ("offload", "stage2", "gather", "onebit"):
+    elif args.workload in ("offload", "stage2", "gather", "onebit", "onebit_server"):
         from zero_partitioned_mixed_layout_gb300 import _build
         _build.build()
         {"offload": run_offload, "stage2": run_stage2, "gather": run_gather,
-         "onebit": run_onebit}[args.workload](args)
+         "onebit": run_onebit, "onebit_server": run_onebit_server}[args.workload](args)
     else:
         import zero_partitioned_mixed_layout_gb300 as zp
         from zero_partitioned_mixed_layout_gb300 import _build
