@@ -147,6 +147,29 @@ def test_server_average_is_the_correctly_rounded_mean(nd):
             assert abs(Fraction(float(y)) - q) <= abs(Fraction(float(nb)) - q)
 
 
+def test_server_sum_runs_in_rank_order():
+    """The workers' terms are added in rank order, starting from worker 0's
+    term: with scales 1, 2^-24, 2^-24 and every sign +, 1 + 2^-24 is a tie
+    that rounds to 1, twice, so the mean is binary32(1/3); the reverse order
+    (2^-24 + 2^-24 = 2^-23 exactly, then 1 + 2^-23 exactly) would give
+    binary32((1 + 2^-23)/3), one ulp above.  With worker 0's sign -, the
+    first addition -1 + 2^-24 is exact (1 - 2^-24 is a binary32 value) and
+    so is the second: the mean is binary32((-1 + 2^-23)/3)."""
+    S = 64
+    scales = [F32(1.0), F32(2.0 ** -24), F32(2.0 ** -24)]
+    plus = [np.full(S // 32, 0xFFFFFFFF, np.uint32) for _ in range(3)]
+    f = np.zeros(S, F32)
+    oracle.onebit_server(plus, scales, f, scale=0.0)
+    third = F32(F32(1.0) / F32(3.0))
+    assert (f == third).all()
+    assert third != F32(float(Fraction(1) + Fraction(1, 2 ** 23)) / 3.0)
+    minus0 = [np.zeros(S // 32, np.uint32)] + plus[1:]
+    f = np.zeros(S, F32)
+    oracle.onebit_server(minus0, scales, f, scale=0.0)
+    want = F32(float(Fraction(-1) + Fraction(1, 2 ** 23))) / F32(3.0)
+    assert (f == want).all()
+
+
 def test_server_error_feedback_telescopes():
     rng = np.random.default_rng(9)
     S, nd, T = 640, 4, 20
@@ -258,6 +281,7 @@ PINS = [
     test_worker_error_feedback_telescopes,
     test_worker_local_momentum_without_gradient,
     lambda: [test_server_average_is_the_correctly_rounded_mean(nd) for nd in (1, 2, 3, 5)],
+    test_server_sum_runs_in_rank_order,
     test_server_error_feedback_telescopes,
     test_variance_correction_frozen_at_the_last_warmup_step,
     lambda: [test_whole_step_with_exact_compression_matches_binary64(nd) for nd in (1, 2, 4)],
@@ -276,6 +300,11 @@ C_MUTANTS = [
     ("server mean over nd - 1", "const float count = (float)nd;",
      "const float count = (float)(nd > 1 ? nd - 1 : 1);"),
     ("server error feedback dropped", "f[i] = a / count + f[i];", "f[i] = a / count;"),
+    ("server sum in reverse rank order",
+     "for (int32_t k = 0; k < nd; ++k) {\n            const float c = ((bits[k][i / 32] >> (i % 32)) & 1u) ? "
+     "scales[k] : -scales[k];\n            a = k == 0 ? c : a + c;",
+     "for (int32_t k = nd - 1; k >= 0; --k) {\n            const float c = ((bits[k][i / 32] >> (i % 32)) & 1u) ? "
+     "scales[k] : -scales[k];\n            a = k == nd - 1 ? c : a + c;"),
     ("momentum not synchronised", "        m[i] = mi;\n        if (i >= numel)", "        if (i >= numel)"),
     ("local momentum drops beta1", "const float mi = s->beta1 * m[i] + s->one_minus_beta1 * gi;",
      "const float mi = s->one_minus_beta1 * gi;"),
