@@ -805,6 +805,76 @@ def run_onebit(args):
     print(json.dumps(line), flush=True)
 
 
+def run_graph(args):
+    """Small shards, back to back and L2-resident (no flush: the state of
+    these shards fits in L2 and stays there): the step issued as calls
+    through the Python binding, against the same step captured once into a
+    CUDA graph and replayed.  Below a few million params the GPU work of a
+    step is a few microseconds and the host's cost per call (argument
+    marshalling and checks, two launches) sets the pace; a replay launches
+    both kernels with one call.  The tiny configuration (1,836,288 params)
+    is the line's value; flat 2^16 and 2^20 shards are reported beside it."""
+    import torch
+
+    dev = torch.device("cuda", torch.cuda.current_device())
+    stream = torch.cuda.current_stream(dev)
+
+    def measure(wl):
+        for _ in range(args.warmup):
+            wl.step(stream)
+        torch.cuda.synchronize(dev)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        t0 = time.perf_counter()
+        e0.record(stream)
+        for _ in range(args.steps):
+            wl.step(stream)
+        e1.record(stream)
+        host_eager = (time.perf_counter() - t0) / args.steps
+        torch.cuda.synchronize(dev)
+        eager = e0.elapsed_time(e1) / args.steps
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            wl.step(torch.cuda.current_stream(dev))
+        for _ in range(args.warmup):
+            graph.replay()
+        torch.cuda.synchronize(dev)
+        t0 = time.perf_counter()
+        e0.record(stream)
+        for _ in range(args.steps):
+            graph.replay()
+        e1.record(stream)
+        host_graph = (time.perf_counter() - t0) / args.steps
+        torch.cuda.synchronize(dev)
+        replay = e0.elapsed_time(e1) / args.steps
+        st = wl.zp.parse_state(wl.state)
+        assert st["last_skipped"] == 0 and st["step"] == 2 * (args.warmup + args.steps), st
+        return {"params": wl.S, "eager_ms": eager, "graph_ms": replay,
+                "eager_params_per_s": wl.S / (eager * 1e-3), "graph_params_per_s": wl.S / (replay * 1e-3),
+                "host_us_per_call": host_eager * 1e6, "host_us_per_replay": host_graph * 1e6}
+
+    with ClockSampler(dev.index) as clk:
+        tiny = measure(Workload("tiny", 0, 0, dev))
+        flat = {f"2^{k}": measure(Workload("flat", k, 0, dev)) for k in (16, 20)}
+    peaks = measured_peaks()
+    line = {
+        "metric": "Adam-step params/sec, small L2-resident shard, CUDA-graph replay (eager calls beside it), 1 GPU",
+        "value": tiny["graph_params_per_s"], "unit": UNIT, "n_gpus": 1, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": tiny["graph_ms"], "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": {"workload": "2-layer hidden-256 transformer state (14 tensors, 1,836,288 params), Nd = 1, "
+                               "fp16 grads x 1024; zero_step captured once and replayed",
+                   "l2": "L2-resident: no flush, the 55 MB step stays in the 126 MB L2 (labelled, not a "
+                         "roofline figure)"},
+        "tiny": tiny, "flat": flat,
+        "roofline": {"bound": "latency", "achieved": None, "peak": peaks["hbm_gbs"] if peaks else 6800.0,
+                     "unit": "GB/s", "frac": None, "traffic": None,
+                     "kernel": "two launches per step; the step is bound by launch and host latency"},
+        "gpu_launches": 3 * 2 * 2 * args.steps,  # 3 shards x (calls + replays) x 2 kernels a step
+        "clocks": clk.summary(),
+    }
+    print(json.dumps(line), flush=True)
+
+
 def run_onebit_server(args):
     """1-bit Adam's server call alone: chunk 0 of the GPT-2 1.5B layout in
     16 shards (S = 97,350,784 elements), the 16 workers' signs and scales as
@@ -1025,7 +1095,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--workload", default=WORKLOAD,
                     choices=["gpt2_1p5b_nd16", "tiny", "gpt2_1p5b_full", "stack_100b_nd400",
-                             "frag_10k", "flat", "offload", "stage2", "gather", "onebit", "onebit_server"],
+                             "frag_10k", "flat", "offload", "stage2", "gather", "onebit", "onebit_server",
+                             "graph"],
                     help="default: the GPT-2 1.5B Nd=16 shard the metric is quoted on")
     ap.add_argument("--log2n", type=int, default=26, help="size of the flat workload (2^k)")
     ap.add_argument("--clock-preroll", type=float, default=1.0,
@@ -1035,11 +1106,11 @@ def main():
         ap.error("--warmup must be at least 3")
     if args.impl == "reference":
         run_reference(args)
-    elif args.workload in ("offload", "stage2", "gather", "onebit", "onebit_server"):
+    elif args.workload in ("offload", "stage2", "gather", "onebit", "onebit_server", "graph"):
         from zero_partitioned_mixed_layout_gb300 import _build
         _build.build()
         {"offload": run_offload, "stage2": run_stage2, "gather": run_gather,
-         "onebit": run_onebit, "onebit_server": run_onebit_server}[args.workload](args)
+         "onebit": run_onebit, "onebit_server": run_onebit_server, "graph": run_graph}[args.workload](args)
     else:
         import zero_partitioned_mixed_layout_gb300 as zp
         from zero_partitioned_mixed_layout_gb300 import _build

@@ -388,3 +388,48 @@ def test_16_byte_aligned_state_matches_32(zp, kind, gdtype):
         for key in ("p", "m", "v", "lp"):
             for x, y in zip(a32[key], a16[key]):
                 assert torch.equal(x, y), f"{key} step {k}"
+
+
+@pytest.mark.parametrize("whole", [True, False])
+def test_learning_rate_schedule_and_beta_change(zp, whole):
+    """Forty steps with the learning rate changed at every step (linear
+    warm-up, then cosine decay), the betas changed at step 25 and an
+    overflow at step 10.  The bias corrections come from the cached window
+    of step counts (refilled every 16 steps and on the beta change), the
+    step size from the cached 1 - beta1^t divided by the new rate on the
+    device; every element of every step against the oracle (whole: through
+    zero_step, else pass 1 and zero_adam_step)."""
+    import math
+    n, seed, scale = 50_001, 91, 1024.0
+    p0 = zs.host_master(n, seed)
+    dp = torch.from_numpy(p0.copy()).cuda()
+    dm = torch.zeros(n, dtype=torch.float32, device="cuda")
+    dv = torch.zeros(n, dtype=torch.float32, device="cuda")
+    dlp = torch.zeros(n, dtype=torch.float16, device="cuda")
+    state = zp.new_state(scale)
+    ws = zp.new_workspace(1, n)
+    p, m, v = p0.copy(), np.zeros(n, np.float32), np.zeros(n, np.float32)
+    plp = np.zeros(n, np.uint16)
+    sc = oracle.Scaler(loss_scale=scale)
+    skipped = 0
+    for k in range(40):
+        lr = 1e-3 * min(1.0, (k + 1) / 8) * 0.5 * (1.0 + math.cos(math.pi * k / 40))
+        b1, b2 = (0.9, 0.999) if k < 25 else (0.85, 0.99)
+        ohp, ghp = hp_pair(lr=lr, beta1=b1, beta2=b2, max_norm=0.5)
+        g = zs.host_grad(n, seed, k, sc.loss_scale, "f16")
+        if k == 10:
+            g[zs.inf_index(n, seed, k)] = zs.host_cast(np.array([np.inf], np.float32), "f16")[0]
+        dg = to_dev(g, "f16")
+        if whole:
+            zp.zero_step(dg, dp, dm, dv, dlp, ghp, state, ws)
+        else:
+            zp.zero_grad_norm_overflow(dg, state, ws)
+            zp.zero_adam_step(dg, dp, dm, dv, dlp, ghp, state, ws)
+        gst = zp.parse_state(state)
+        st = oracle_step([g], "f16", [p], [m], [v], [plp], "f16", ohp, sc, gst)
+        skipped += st.skip
+        assert_f32(to_host(dp), p, f"master step {k}")
+        assert_f32(to_host(dm), m, f"m step {k}")
+        assert_f32(to_host(dv), v, f"v step {k}")
+        assert np.array_equal(to_host(dlp), plp), f"p_lp step {k}"
+    assert skipped == 1 and zp.parse_state(state)["step"] == 39

@@ -432,11 +432,12 @@ __device__ __forceinline__ void decide_write(zero_state_t *st, StepScalars *out,
 
 // Skip or apply, loss-scale and step bookkeeping, and the step scalars
 // (binary64, each rounded once to binary32).  Binary64 is a slow pipe on
-// this GPU, so the three independent chains -- 1 - beta1^t and the step
-// size, 1 - beta2^t and its inverse square root, the norm and the clip
-// coefficient -- run in three threads; thread 0 then writes the results.
-// Block code: every thread of the block calls it (it holds a block
-// barrier).
+// this GPU, so the independent chains run side by side: lanes 0 and 1 of
+// warp 0 take 1 - beta1^t with the step size and 1 - beta2^t with its
+// inverse square root (from the cache window when its tags match, else one
+// converged pow each), warp 1 the norm and the clip coefficient; thread 0
+// then writes the results.  Block code: every thread of the block (at
+// least 64) calls it (it holds a block barrier).
 __device__ __forceinline__ void decide_block(zero_state_t *st, StepScalars *out, const PowCache *cache,
                                              const DecideArgs &a)
 {
@@ -445,26 +446,20 @@ __device__ __forceinline__ void decide_block(zero_state_t *st, StepScalars *out,
     const int tid = threadIdx.x;
     zero_state_t s = *st;
     const int64_t tn = s.step + 1;  // the step count if this step applies
-    const double t = (double)tn;
-    const PowCache c = *cache;
-    const bool hit = c.t == tn && c.beta1 == a.beta1 && c.beta2 == a.beta2;
-    if (tid == 0) {
-        if (hit && c.lr == a.lr) {
-            s_val[0] = c.step_size;
+    if (tid < 2) {
+        const bool hit = cache->t0 > 0 && tn >= cache->t0 && tn < cache->t0 + kPowWindow &&
+                         cache->beta1 == a.beta1 && cache->beta2 == a.beta2;
+        const int j = hit ? (int)(tn - cache->t0) : 0;
+        if (tid == 0 && hit && cache->lr == a.lr) {
+            s_val[0] = cache->step_size[j];
+        } else if (tid == 1 && (a.frozen || hit)) {
+            s_val[1] = a.frozen ? a.isb2_frozen : cache->isb2[j];
         } else {
-            const double bc1 = hit ? c.bc1 : 1.0 - pow(a.beta1, t);
-            s_val[0] = (float)(a.lr / bc1);
+            // the cache's expressions, evaluated here
+            const double bc = tid == 0 && hit ? cache->bc1[j] : 1.0 - pow(tid ? a.beta2 : a.beta1, (double)tn);
+            s_val[tid] = tid ? (float)(1.0 / sqrt(bc)) : (float)(a.lr / bc);
         }
-    } else if (tid == 1) {
-        if (a.frozen) {
-            s_val[1] = a.isb2_frozen;
-        } else if (hit) {
-            s_val[1] = c.isb2;
-        } else {
-            const double bc2 = 1.0 - pow(a.beta2, t);
-            s_val[1] = (float)(1.0 / sqrt(bc2));
-        }
-    } else if (tid == 2) {
+    } else if (tid == 32) {
         const double norm = sqrt(s.sumsq);
         double clip = 1.0;
         if (a.max_norm > 0.0) {
@@ -478,6 +473,36 @@ __device__ __forceinline__ void decide_block(zero_state_t *st, StepScalars *out,
     __syncthreads();
     if (tid == 0)
         decide_write(st, out, a, s, s_val, s_norm);
+}
+
+// The bias-correction window for the next applied step, if the cache does
+// not cover it: warp code (all 32 lanes of one warp), lanes 0..15 taking
+// 1 - beta1^t and lanes 16..31 1 - beta2^t for t = next_t .. next_t + 15 in
+// one converged pow.  The same expressions as the decision's own.  A change
+// of the learning rate alone refills nothing: the decision then divides the
+// new rate by the cached 1 - beta1^t (a schedule changes it every step).
+__device__ __forceinline__ void refill_pow_window(const StepScalars *scp, PowCache *cache)
+{
+    const int lane = threadIdx.x & 31;
+    const int64_t tn = scp->next_t;
+    const double lr = scp->lr, beta1 = scp->beta1, beta2 = scp->beta2;
+    if (cache->t0 > 0 && tn >= cache->t0 && tn < cache->t0 + kPowWindow && cache->beta1 == beta1 &&
+        cache->beta2 == beta2)
+        return;
+    const int j = lane & (kPowWindow - 1);
+    const double bc = 1.0 - pow(lane < kPowWindow ? beta1 : beta2, (double)(tn + j));
+    if (lane < kPowWindow) {
+        cache->bc1[j] = bc;
+        cache->step_size[j] = (float)(lr / bc);
+    } else {
+        cache->isb2[j] = (float)(1.0 / sqrt(bc));
+    }
+    if (lane == 0) {
+        cache->t0 = tn;
+        cache->beta1 = beta1;
+        cache->beta2 = beta2;
+        cache->lr = lr;
+    }
 }
 
 __global__ void k_decide(zero_state_t *st, StepScalars *out, const PowCache *cache, DecideArgs a)

@@ -305,25 +305,6 @@ __global__ void __launch_bounds__(kThreads)
         write_norm(st, tot, b, accumulate);
 }
 
-// The bias-correction terms for the next step (the same expressions as the
-// decision kernel's), written by one thread of pass 2 after its own
-// elements; the next decision kernel picks them up if its tags match.
-__device__ __forceinline__ void precompute_next(const StepScalars *scp, PowCache *cache)
-{
-    const int64_t tn = scp->next_t;
-    const double lr = scp->lr, beta1 = scp->beta1, beta2 = scp->beta2;
-    const double t = (double)tn;
-    const double bc1 = 1.0 - pow(beta1, t);
-    const double bc2 = 1.0 - pow(beta2, t);
-    cache->t = tn;
-    cache->beta1 = beta1;
-    cache->beta2 = beta2;
-    cache->lr = lr;
-    cache->bc1 = bc1;
-    cache->step_size = (float)(lr / bc1);
-    cache->isb2 = (float)(1.0 / sqrt(bc2));
-}
-
 // ------------------------------------------------------------- pass 2
 
 // One element of the AdamW update, binary32, every operation rounded to
@@ -438,8 +419,8 @@ __global__ void __launch_bounds__(kThreads, 4)
         adam_vec<GT, PT, V32>(g, p, m, v, plp, i, s);
     else if (i - nv < (n & 7))
         adam_scalar<GT, PT>(g, p, m, v, plp, (nv << 3) + (i - nv), s);
-    if (blockIdx.x == 0 && threadIdx.x == 0)
-        precompute_next(scp, cache);
+    if (blockIdx.x == 0 && threadIdx.x < 32)
+        refill_pow_window(scp, cache);
 }
 
 // Pass 2 over a list: one block per tile of kTile elements of one tensor,
@@ -453,8 +434,8 @@ __global__ void __launch_bounds__(kThreads, 4)
     const StepScalars s = *scp;
     if (s.skip)
         return;
-    if (blockIdx.x == 0 && threadIdx.x == 0)
-        precompute_next(scp, cache);
+    if (blockIdx.x == 0 && threadIdx.x < 32)
+        refill_pow_window(scp, cache);
     const WorkItem tl = tiles[blockIdx.x];
     const TensorEntry e = ents[tl.tensor];
     const int64_t start = (int64_t)tl.index * kTile;
@@ -773,7 +754,7 @@ int run_step(const zero_tlist_t *grads, const zero_tlist_t *master, const zero_t
     StepScalars *sc = reinterpret_cast<StepScalars *>(static_cast<unsigned char *>(ws) + kWsScalars);
     const DecideArgs a = decide_args(hp);
     const PowCache *cache = reinterpret_cast<const PowCache *>(static_cast<unsigned char *>(ws) + kWsPowCache);
-    launch_k(k_decide, 1, 32, s, decide_pdl, d_state, sc, cache, a);
+    launch_k(k_decide, 1, 64, s, decide_pdl, d_state, sc, cache, a);
     if ((rc = check_launch("zero_adam_step (decision)")) != ZERO_OK)
         return rc;
     if (grads->n == 0)

@@ -40,21 +40,25 @@ struct StepScalars {
     float lrwd;       // lr * weight_decay
     int32_t skip;
     int32_t pad;
-    // for the bias-correction precompute of the next step (see PowCache)
+    // for the bias-correction window of the next steps (see PowCache)
     double lr, beta1, beta2;
     int64_t next_t;   // step count of the next applied step
 };
 
-// The binary64 bias-correction terms of one step count t, computed ahead of
-// time by the first block of pass 2 (off the critical path) for the next
-// step, and used by the next decision kernel when its tags match.
+// The binary64 bias-correction terms of a window of kPowWindow consecutive
+// step counts [t0, t0 + kPowWindow), computed ahead of time by one warp of
+// pass 2 (one warp-wide pow: a lane per term) whenever the next step count
+// leaves the window, and used by the decision when its tags match.  A
+// binary64 pow is slow on this GPU (about 4 us for one call), so one call
+// per kPowWindow steps keeps it off every step's critical path.
+constexpr int kPowWindow = 16;
 struct PowCache {
-    int64_t t;             // tag: step count; 0 = empty
-    double beta1, beta2;   // tags
-    double lr;             // tag of step_size
-    double bc1;            // 1 - beta1^t
-    float step_size;       // lr / bc1, rounded once
-    float isb2;            // 1 / sqrt(1 - beta2^t), rounded once
+    int64_t t0;                   // tag: first step count of the window; 0 = empty
+    double beta1, beta2;          // tags
+    double lr;                    // tag of step_size
+    double bc1[kPowWindow];       // 1 - beta1^t
+    float step_size[kPowWindow];  // lr / bc1, rounded once
+    float isb2[kPowWindow];       // 1 / sqrt(1 - beta2^t), rounded once
 };
 
 // One array set of a list: the gradient, the fp32 master / momentum /
@@ -76,11 +80,11 @@ struct WorkItem {
     int32_t index;
 };
 
-// Workspace layout (all offsets 256-byte aligned):
+// Workspace layout (all offsets 128-byte aligned):
 //   [0, 256)            header: reduction ticket
 //   [256, 384)          StepScalars of the current step
-//   [384, 512)          PowCache for the next step
-//   [512, 512 + 16*kMaxBlocks)  per-block partials of the norm pass (double2)
+//   [384, 768)          PowCache: the bias corrections of a window of steps
+//   [768, 768 + 16*kMaxBlocks)  per-block partials of the norm pass (double2)
 //   then                GroupArea: tickets and partials of the block groups
 //                       of a one-shot reduction
 //   then                a list's table: TensorEntry[n], then the work
@@ -93,9 +97,9 @@ struct WsHeader {
 };
 constexpr size_t kWsScalars = 256;
 constexpr size_t kWsPowCache = 384;
-static_assert(sizeof(StepScalars) <= 128, "StepScalars must fit its workspace slot");
-static_assert(sizeof(PowCache) <= 128, "PowCache must fit its workspace slot");
-constexpr size_t kWsPartials = 512;
+constexpr size_t kWsPartials = 768;
+static_assert(sizeof(StepScalars) <= kWsPowCache - kWsScalars, "StepScalars must fit its workspace slot");
+static_assert(sizeof(PowCache) <= kWsPartials - kWsPowCache, "PowCache must fit its workspace slot");
 
 // A one-shot reduction's blocks report in groups of kGroupBlocks: the last
 // block of a group sums the group's partials in block order, the last group
