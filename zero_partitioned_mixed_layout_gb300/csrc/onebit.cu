@@ -16,8 +16,11 @@
 // squared norm (binary32 squares in 8 lanes, one binary64 add per 32
 // elements, fixed-order block partials, the last block finishing the sum and
 // writing the scale); the second writes the signs, packed 32 to a word with
-// two warp shuffles, and the new error.  Bytes per element: worker 14 + 8
-// (fp16 gradient), server (Nd/8 + 8) + 8 per chunk element, update 18.
+// two warp shuffles, and the new error.  Bytes per element with an fp16
+// gradient: worker 2 + 1/8 + 8 with the momentum as the servers' signs (2 +
+// 4 + 8 with a dense one), then 8 + 1/8 for the signs; server (Nd/8 + 8) +
+// 8 + 1/8 per chunk element; update 1/8 + 12 + 2 (+ 4 with a dense
+// momentum written).
 #include <vector>
 
 #include "common.cuh"
