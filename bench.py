@@ -32,6 +32,28 @@ sys.path.insert(0, ROOT)
 METRIC = "Adam-step params/sec & achieved HBM GB/s vs GB300 roofline (28 B/param), 1 GPU"
 UNIT = "params/s"
 WORKLOAD = "gpt2_1p5b_nd16"
+TITLES = {
+    "gpt2_1p5b_nd16": "GPT-2 1.5B state (48 layers, hidden 1600, vocab 50257) in 16 "
+                      "ZeRO shards, one shard per GPU",
+    "gpt2_1p5b_full": "GPT-2 1.5B state unpartitioned (Nd = 1) on one GPU, clip 1.0",
+    "tiny": "2-layer hidden-256 transformer state (14 tensors), Nd = 1",
+    "stack_100b_nd400": "100B GPT layer stack (125 x hidden 8192) in 400 ZeRO shards, "
+                        "one shard; 4 bf16 micro-batch gradients accumulated, clip 1.0",
+    "frag_10k": "10,000 separately allocated tensors (log-normal sizes, median 4096, "
+                "max 2^24), unflattened multi-tensor path",
+}
+
+
+def step_config(title, w, S, l2, world=1):
+    """The `config` of a step line: the workload and its shard, the same for
+    both arms."""
+    return {
+        "workload": title,
+        "shard_params": S, "grad_dtype": w["gdtype"], "param_dtype": w["pdtype"],
+        "state_dtype": "f32", "loss_scale": w["loss_scale"], "clip": w["max_norm"],
+        "micro_batches": w["micro_batches"], "l2": l2,
+        "parallelism": f"zero-dp{world}" if world > 1 else "zero-shard",
+    }
 L2_BYTES = 129e6
 
 
@@ -200,6 +222,10 @@ def run_reference(args):
     rank, world, _ = dist_env()
     if rank != 0:
         return
+    import oracle
+    import zero_synth as zs
+    w = zs.WORKLOADS[WORKLOAD]
+    S = oracle.partition_layout(w["numel"](), w["nd"], w["align"]).shard_numel
     n_sample = 1 << 24
     one, one_dt = oracle_run(n_sample, args.steps, args.warmup)
     value, dt, procs = oracle_run_all_cores(n_sample, args.steps, args.warmup)
@@ -211,7 +237,9 @@ def run_reference(args):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * dt / args.steps,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
         "data": "synthetic",
-        "config": {"workload": WORKLOAD, "sample_params": n_sample},
+        "config": dict(step_config(TITLES[WORKLOAD], w, S, "host cores: each process steps its own sample of the "
+                                   "shard (the oracle does not use the GPU)", args.gpus),
+                       sample_params=n_sample),
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": procs, "kind": "oracle",
                          "sample": sample,
                          "single_core": {"value": one, "unit": UNIT, "cores": 1,
@@ -239,16 +267,7 @@ class Workload:
         else:
             w = zs.WORKLOADS[name]
             numel = w["numel"]()
-            self.title = {
-                "gpt2_1p5b_nd16": "GPT-2 1.5B state (48 layers, hidden 1600, vocab 50257) in 16 "
-                                  "ZeRO shards, one shard per GPU",
-                "gpt2_1p5b_full": "GPT-2 1.5B state unpartitioned (Nd = 1) on one GPU, clip 1.0",
-                "tiny": "2-layer hidden-256 transformer state (14 tensors), Nd = 1",
-                "stack_100b_nd400": "100B GPT layer stack (125 x hidden 8192) in 400 ZeRO shards, "
-                                    "one shard; 4 bf16 micro-batch gradients accumulated, clip 1.0",
-                "frag_10k": "10,000 separately allocated tensors (log-normal sizes, median 4096, "
-                            "max 2^24), unflattened multi-tensor path",
-            }[name]
+            self.title = TITLES[name]
         self.w = w
         self.listmode = name == "frag_10k"
         shard = rank % w["nd"]
@@ -499,17 +518,12 @@ def run_ours(args):
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
-        "config": {
-            "workload": wl.title,
-            "shard_params": S, "grad_dtype": wl.w["gdtype"], "param_dtype": wl.w["pdtype"],
-            "state_dtype": "f32", "loss_scale": wl.scale, "clip": wl.w["max_norm"],
-            "micro_batches": wl.micro,
-            "l2": ("L2 flushed (256 MB written) before each timed step; time is the sum of the "
-                   "steps alone" if flush is not None else
-                   f"inputs larger than L2 ({wl.bytes_step * S / 1e9:.2f} GB per step vs "
-                   f"{L2_BYTES / 1e6:.0f} MB), no flush"),
-            "parallelism": f"zero-dp{world}" if world > 1 else "zero-shard",
-        },
+        "config": step_config(
+            wl.title, wl.w, S,
+            "L2 flushed (256 MB written) before each timed step; time is the sum of the steps alone"
+            if flush is not None else
+            f"inputs larger than L2 ({wl.bytes_step * S / 1e9:.2f} GB per step vs {L2_BYTES / 1e6:.0f} MB), "
+            "no flush", world),
         "hbm_gbs_adam": wl.bytes_adam * S / (adam_ms * 1e-3) / 1e9,
         "hbm_gbs_step": wl.bytes_step * S / (ms_per_step * 1e-3) / 1e9,
         "bytes_per_param": {"adam_pass": wl.bytes_adam, "whole_step": wl.bytes_step},
