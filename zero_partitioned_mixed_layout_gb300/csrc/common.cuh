@@ -505,13 +505,21 @@ __device__ __forceinline__ void refill_pow_window(const StepScalars *scp, PowCac
     }
 }
 
-__global__ void k_decide(zero_state_t *st, StepScalars *out, const PowCache *cache, DecideArgs a)
+// The decision as a kernel of one block of 64 threads.  `refill`: then
+// also the bias-correction window for the next step (warp 0, after the
+// decision), for callers whose streaming kernels do not refill it.
+__global__ void k_decide(zero_state_t *st, StepScalars *out, PowCache *cache, DecideArgs a, int refill)
 {
     pdl_launch_next();
     pdl_wait();
     if (blockIdx.x != 0)
         return;
     decide_block(st, out, cache, a);
+    if (!refill)
+        return;
+    __syncthreads();
+    if (threadIdx.x < 32 && !out->skip)
+        refill_pow_window(out, cache);
 }
 // ------------------------------------------------------------- host helpers
 

@@ -415,13 +415,9 @@ constexpr int kNoLowP = -1;
 template <int PT>
 __global__ void __launch_bounds__(kThreads) k_onebit_update(const uint32_t *bits, const float *scales, int64_t S,
                                                             int64_t n, int64_t numel, float *p, float *m,
-                                                            const float *v, void *plp, const StepScalars *scp,
-                                                            PowCache *cache)
+                                                            const float *v, void *plp, const StepScalars *scp)
 {
     const StepScalars s = *scp;
-    // the next decisions' step sizes, a window at a time (warp 0 of block 0)
-    if (blockIdx.x == 0 && threadIdx.x < 32 && !s.skip)
-        refill_pow_window(scp, cache);
     const int64_t i = (int64_t)blockIdx.x * kThreads + threadIdx.x;
     const int64_t nv = s.skip ? 0 : n >> 3;
     if (i >= nv)
@@ -509,8 +505,7 @@ int launch_update(const uint32_t *bits, const float *scales, int64_t S, int64_t 
 {
     const int64_t threads = n >> 3;
     launch_k(k_onebit_update<PT>, (int)((threads + kThreads - 1) / kThreads), kThreads, st, false, bits, scales, S,
-             n, numel, p, m, v, plp, (const StepScalars *)step_scalars(ws),
-             reinterpret_cast<PowCache *>(static_cast<unsigned char *>(ws) + kWsPowCache));
+             n, numel, p, m, v, plp, (const StepScalars *)step_scalars(ws));
     return check_launch("zero_onebit_update");
 }
 
@@ -564,8 +559,10 @@ extern "C" int zero_onebit_worker(const void *grad, int32_t gdtype, const float 
         return rc;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     const DecideArgs a = decide_args(hp, freeze_step);
-    const PowCache *cache = reinterpret_cast<const PowCache *>(static_cast<unsigned char *>(ws) + kWsPowCache);
-    launch_k(k_decide, 1, 64, st, false, d_state, step_scalars(ws), cache, a);
+    PowCache *cache = reinterpret_cast<PowCache *>(static_cast<unsigned char *>(ws) + kWsPowCache);
+    // the decision also refills the bias-correction window: the 1-bit kernels
+    // do not (its binary64 pow would raise their register counts)
+    launch_k(k_decide, 1, 64, st, false, d_state, step_scalars(ws), cache, a, 1);
     if ((rc = check_launch("zero_onebit_worker (decision)")) != ZERO_OK || n == 0)
         return rc;
     switch (gdtype) {

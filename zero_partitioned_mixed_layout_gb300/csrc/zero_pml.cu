@@ -753,8 +753,8 @@ int run_step(const zero_tlist_t *grads, const zero_tlist_t *master, const zero_t
     }
     StepScalars *sc = reinterpret_cast<StepScalars *>(static_cast<unsigned char *>(ws) + kWsScalars);
     const DecideArgs a = decide_args(hp);
-    const PowCache *cache = reinterpret_cast<const PowCache *>(static_cast<unsigned char *>(ws) + kWsPowCache);
-    launch_k(k_decide, 1, 64, s, decide_pdl, d_state, sc, cache, a);
+    PowCache *cache = reinterpret_cast<PowCache *>(static_cast<unsigned char *>(ws) + kWsPowCache);
+    launch_k(k_decide, 1, 64, s, decide_pdl, d_state, sc, cache, a, 0);
     if ((rc = check_launch("zero_adam_step (decision)")) != ZERO_OK)
         return rc;
     if (grads->n == 0)
