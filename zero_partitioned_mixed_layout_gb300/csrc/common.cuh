@@ -226,13 +226,47 @@ __device__ __forceinline__ void block_reduce(double &tot, uint32_t &bad)
     __syncthreads();
 }
 
+// Shared-memory copies of the state and of the bias-correction cache, the
+// inputs of the decision: loaded by the block together with what it waits
+// for anyway (the partials of the norm), so that the decision issues no
+// dependent global load of its own.
+struct DecideShared {
+    zero_state_t s;
+    PowCache c;
+};
+
+// Block code: the state and (if `cache` is not NULL) the cache into `sh`,
+// 8 bytes per thread; visible after the caller's next barrier.
+__device__ __forceinline__ void decide_load(const zero_state_t *st, const PowCache *cache, DecideShared *sh)
+{
+    constexpr int kS = sizeof(zero_state_t) / 8, kC = sizeof(PowCache) / 8;
+    static_assert(sizeof(zero_state_t) % 8 == 0 && sizeof(PowCache) % 8 == 0, "8-byte words");
+    const int k = threadIdx.x;
+    if (k < kS)
+        reinterpret_cast<uint64_t *>(&sh->s)[k] = reinterpret_cast<const uint64_t *>(st)[k];
+    else if (cache && k < kS + kC)
+        reinterpret_cast<uint64_t *>(&sh->c)[k - kS] = reinterpret_cast<const uint64_t *>(cache)[k - kS];
+}
+
+// 1 / S for the loss scale S.  S is a power of two (the initial scale is
+// checked, and it is only ever halved or doubled): its reciprocal is then
+// exact, the exponent negated with a zero fraction, which spares the slow
+// binary64 division; any other value takes the division.
+__device__ __forceinline__ double inverse_scale(double x)
+{
+    const long long b = __double_as_longlong(x);
+    if ((b & 0x000FFFFFFFFFFFFFLL) == 0 && b >= 0x3FF0000000000000LL && b <= 0x7FD0000000000000LL)
+        return __longlong_as_double(0x7FE0000000000000LL - b);
+    return 1.0 / x;
+}
+
 // End of the norm pass in every block: publish this block's partial; the
 // block that takes the last ticket sums all partials in block order and
 // writes (or adds) the unscaled totals into the state.  No block waits on
 // another: the last block to arrive does the final sum.  Returns true in
 // every thread of that last block.
 __device__ bool norm_finish(double tot, uint32_t bad, double2 *partials, WsHeader *hdr,
-                            zero_state_t *st, int accumulate)
+                            zero_state_t *st, int accumulate, DecideShared *sh, const PowCache *cache = nullptr)
 {
     __shared__ bool s_last;
     block_reduce(tot, bad);
@@ -246,6 +280,8 @@ __device__ bool norm_finish(double tot, uint32_t bad, double2 *partials, WsHeade
     if (!s_last)
         return false;
     __threadfence();
+    // the state (and the cache, for a decision taken here) beside the partials
+    decide_load(st, cache, sh);
     double t = 0.0;
     uint32_t b = 0;
     for (int j = threadIdx.x; j < (int)gridDim.x; j += kThreads) {
@@ -257,10 +293,12 @@ __device__ bool norm_finish(double tot, uint32_t bad, double2 *partials, WsHeade
     if (threadIdx.x == 0) {
         // the partials hold sums of squares of the stored (scaled) gradient;
         // the loss scale is a power of two, so this rescaling is exact
-        const double inv = 1.0 / st->loss_scale;
+        const double inv = inverse_scale(sh->s.loss_scale);
         const double sum = t * inv * inv;
-        st->sumsq = accumulate ? st->sumsq + sum : sum;
-        st->found_inf = (accumulate ? st->found_inf : 0.0) + (b ? 1.0 : 0.0);
+        sh->s.sumsq = accumulate ? sh->s.sumsq + sum : sum;
+        sh->s.found_inf = (accumulate ? sh->s.found_inf : 0.0) + (b ? 1.0 : 0.0);
+        st->sumsq = sh->s.sumsq;
+        st->found_inf = sh->s.found_inf;
         hdr->ticket = 0u;
     }
     return true;
@@ -438,34 +476,35 @@ __device__ __forceinline__ void decide_write(zero_state_t *st, StepScalars *out,
 // converged pow each), warp 1 the norm and the clip coefficient; thread 0
 // then writes the results.  Block code: every thread of the block (at
 // least 64) calls it (it holds a block barrier).
-__device__ __forceinline__ void decide_block(zero_state_t *st, StepScalars *out, const PowCache *cache,
+__device__ __forceinline__ void decide_block(zero_state_t *st, StepScalars *out, const DecideShared &sh,
                                              const DecideArgs &a)
 {
     __shared__ float s_val[3];
     __shared__ double s_norm;
     const int tid = threadIdx.x;
-    zero_state_t s = *st;
+    const zero_state_t &s = sh.s;
+    const PowCache &c = sh.c;
     const int64_t tn = s.step + 1;  // the step count if this step applies
     if (tid < 2) {
-        const bool hit = cache->t0 > 0 && tn >= cache->t0 && tn < cache->t0 + kPowWindow &&
-                         cache->beta1 == a.beta1 && cache->beta2 == a.beta2;
-        const int j = hit ? (int)(tn - cache->t0) : 0;
-        if (tid == 0 && hit && cache->lr == a.lr) {
-            s_val[0] = cache->step_size[j];
+        const bool hit = c.t0 > 0 && tn >= c.t0 && tn < c.t0 + kPowWindow && c.beta1 == a.beta1 &&
+                         c.beta2 == a.beta2;
+        const int j = hit ? (int)(tn - c.t0) : 0;
+        if (tid == 0 && hit && c.lr == a.lr) {
+            s_val[0] = c.step_size[j];
         } else if (tid == 1 && (a.frozen || hit)) {
-            s_val[1] = a.frozen ? a.isb2_frozen : cache->isb2[j];
+            s_val[1] = a.frozen ? a.isb2_frozen : c.isb2[j];
         } else {
             // the cache's expressions, evaluated here
-            const double bc = tid == 0 && hit ? cache->bc1[j] : 1.0 - pow(tid ? a.beta2 : a.beta1, (double)tn);
+            const double bc = tid == 0 && hit ? c.bc1[j] : 1.0 - pow(tid ? a.beta2 : a.beta1, (double)tn);
             s_val[tid] = tid ? (float)(1.0 / sqrt(bc)) : (float)(a.lr / bc);
         }
     } else if (tid == 32) {
         const double norm = sqrt(s.sumsq);
         double clip = 1.0;
         if (a.max_norm > 0.0) {
-            const double c = a.max_norm / (norm + 1e-6);
-            if (c < 1.0)
-                clip = c;
+            const double q = a.max_norm / (norm + 1e-6);
+            if (q < 1.0)
+                clip = q;
         }
         s_norm = norm;
         s_val[2] = (float)clip;
@@ -514,7 +553,10 @@ __global__ void k_decide(zero_state_t *st, StepScalars *out, PowCache *cache, De
     pdl_wait();
     if (blockIdx.x != 0)
         return;
-    decide_block(st, out, cache, a);
+    __shared__ DecideShared sh;
+    decide_load(st, cache, &sh);
+    __syncthreads();
+    decide_block(st, out, sh, a);
     if (!refill)
         return;
     __syncthreads();

@@ -125,7 +125,7 @@ struct FoldedDecision {
 };
 
 template <int GT>
-__global__ void __launch_bounds__(kThreads)
+__global__ void __launch_bounds__(kThreads, 4)
     k_norm_flat(const void *__restrict__ g, int64_t n, double2 *partials, WsHeader *hdr, zero_state_t *st,
                 int accumulate, int trigger, FoldedDecision fd)
 {
@@ -138,16 +138,17 @@ __global__ void __launch_bounds__(kThreads)
     const int64_t keep_vectors = kL2KeepBytes / (8 * Elem<GT>::kBytes);
     norm_range<GT>(g, n, (int64_t)blockIdx.x * kThreads + threadIdx.x, (int64_t)gridDim.x * kThreads, tot,
                    bad, (n >> 3) - keep_vectors);
-    if (norm_finish(tot, bad, partials, hdr, st, accumulate) && fd.scp) {
+    __shared__ DecideShared sh;
+    if (norm_finish(tot, bad, partials, hdr, st, accumulate, &sh, fd.scp ? fd.cache : nullptr) && fd.scp) {
         // the last block, its totals in the state: the decision here saves
         // the decision kernel's launch and its dependency hop
         __syncthreads();
-        decide_block(st, fd.scp, fd.cache, fd.a);
+        decide_block(st, fd.scp, sh, fd.a);
     }
 }
 
 template <int GT>
-__global__ void __launch_bounds__(kThreads)
+__global__ void __launch_bounds__(kThreads, 4)
     k_norm_list(const TensorEntry *__restrict__ ents, const WorkItem *__restrict__ chunks, int64_t n_chunks,
                 double2 *partials, WsHeader *hdr, zero_state_t *st, int accumulate)
 {
@@ -162,7 +163,8 @@ __global__ void __launch_bounds__(kThreads)
         const void *g = static_cast<const char *>(e.g) + start * Elem<GT>::kBytes;
         norm_range<GT>(g, len, threadIdx.x, kThreads, tot, bad);
     }
-    norm_finish(tot, bad, partials, hdr, st, accumulate);
+    __shared__ DecideShared sh;
+    norm_finish(tot, bad, partials, hdr, st, accumulate, &sh);
 }
 
 // ------------------------------------------------------------- stage-2 reduction
@@ -1008,7 +1010,8 @@ __global__ void __launch_bounds__(kThreads)
     const int64_t nt = (int64_t)gridDim.x * kThreads;
     for (int k = 0; k < n_arrays; ++k)
         norm_range<GT>(a.g[k], a.n[k], t, nt, tot, bad);
-    norm_finish(tot, bad, partials, hdr, st, accumulate);
+    __shared__ DecideShared sh;
+    norm_finish(tot, bad, partials, hdr, st, accumulate, &sh);
 }
 
 // Device address of g_norm_scratch on the current device, looked up once per
