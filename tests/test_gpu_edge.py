@@ -433,3 +433,58 @@ def test_learning_rate_schedule_and_beta_change(zp, whole):
         assert_f32(to_host(dv), v, f"v step {k}")
         assert np.array_equal(to_host(dlp), plp), f"p_lp step {k}"
     assert skipped == 1 and zp.parse_state(state)["step"] == 39
+
+
+def test_list_steps_from_two_host_threads(zp):
+    """Two host threads issue list-mode steps at the same time, each on its
+    own stream, workspace and tensors: their tables go through the shared
+    pinned staging ring, and every result equals the same steps issued from
+    one thread, bit for bit."""
+    import threading
+
+    sizes = [[4099, 70_001, 2047, 1], [333, 65_536, 12_345]]
+    _, ghp = hp_pair(max_norm=0.3)
+
+    def make(k):
+        rng = np.random.default_rng(500 + k)
+        return {
+            "g": [[torch.from_numpy((rng.standard_normal(n) * 0.01).astype(np.float16)).cuda() for n in sizes[k]]
+                  for _ in range(6)],
+            "p": [torch.from_numpy(rng.standard_normal(n).astype(np.float32)).cuda() for n in sizes[k]],
+            "m": [torch.zeros(n, device="cuda") for n in sizes[k]],
+            "v": [torch.zeros(n, device="cuda") for n in sizes[k]],
+            "lp": [torch.zeros(n, dtype=torch.float16, device="cuda") for n in sizes[k]],
+            "st": zp.new_state(1.0), "ws": zp.new_workspace(len(sizes[k]), sum(sizes[k])),
+        }
+
+    def run(d, stream):
+        with torch.cuda.stream(stream):
+            for g in d["g"]:
+                zp.zero_step(g, d["p"], d["m"], d["v"], d["lp"], ghp, d["st"], d["ws"], stream=stream)
+        stream.synchronize()
+
+    def result(d):
+        return [to_host(t).tobytes() for t in d["p"] + d["m"] + d["v"] + d["lp"]] + [d["st"].cpu().numpy().tobytes()]
+
+    alone = [make(0), make(1)]
+    for d in alone:
+        run(d, torch.cuda.Stream())
+    both = [make(0), make(1)]
+    streams = [torch.cuda.Stream(), torch.cuda.Stream()]
+    errors = []
+
+    def worker(k):
+        try:
+            run(both[k], streams[k])
+        except Exception as e:  # noqa: BLE001 - reported below
+            errors.append(e)
+
+    threads = [threading.Thread(target=worker, args=(k,)) for k in range(2)]
+    for t in threads:
+        t.start()
+    for t in threads:
+        t.join()
+    assert not errors, errors
+    for k in range(2):
+        assert result(both[k]) == result(alone[k]), f"thread {k}"
+        assert zp.parse_state(both[k]["st"])["step"] == 6
