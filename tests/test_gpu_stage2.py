@@ -90,3 +90,59 @@ def test_stage2_step_against_oracle(zp, max_norm):
         assert_f32(dm.cpu().numpy(), m, f"m step {k}")
         assert_f32(dv.cpu().numpy(), v, f"v step {k}")
         assert_lp(to_host(dlp), p, "f16", f"p_lp step {k}")
+
+
+@pytest.mark.parametrize("inf_at", [None, 13_000_017])
+def test_reduce_across_block_groups(zp, inf_at):
+    """20,000,003 elements over 16 replicas: 4,883 blocks, five groups of the
+    one-shot finish (the last one partial), every element and the global
+    sum of squares against the oracle; an inf in one replica inside the
+    third group reaches the flag through the group finish."""
+    n, nr, scale = 20_000_003, 16, 256.0
+    reps = [zs.host_grad(n, 90 + k, 0, scale, "f16") for k in range(nr)]
+    if inf_at is not None:
+        reps[5][inf_at] = np.float16(np.inf)
+    want = oracle.reduce_mean(reps, "f16", "f16")
+    sumsq, bad = oracle.norm_overflow([want.view(np.float16)], "f16", scale)
+    out = torch.empty(n, dtype=torch.float16, device="cuda")
+    st = zp.new_state(scale)
+    ws = zp.new_workspace(1, n)
+    zp.zero_reduce_grads([to_dev(r, "f16") for r in reps], out, st, ws)
+    got = to_host(out)
+    assert got.tobytes() == want.tobytes(), "reduced gradient differs from the oracle"
+    s = zp.parse_state(st)
+    assert s["found_inf"] == float(bad) == (0.0 if inf_at is None else 1.0)
+    if inf_at is None:
+        assert abs(s["sumsq"] - sumsq) <= 1e-6 * sumsq
+
+
+def test_stage2_reduce_full_size_sampled(zp):
+    """The benchmark's stage-2 reduction as it is timed: the GPT-2 1.5B
+    Nd=16 rank-0 shard (97,350,784 elements), 16 fp16 replicas drawn on the
+    device, 23,768 blocks in 24 groups of the one-shot finish.  Sampled
+    elements of the mean against the oracle, and the global sum of squares
+    of the whole stored result against the oracle's pass 1 over it."""
+    w = zs.WORKLOADS["gpt2_1p5b_nd16"]
+    S = zp.zero_partition_layout(w["numel"](), w["nd"], w["align"]).shard_numel
+    nr, scale = 16, 65536.0
+    reps = []
+    for r in range(nr):
+        t = torch.empty(S, dtype=torch.float16, device="cuda")
+        zs.device_grad_into(t, 2000 + r, 0, scale)
+        reps.append(t)
+    out = torch.empty(S, dtype=torch.float16, device="cuda")
+    st = zp.new_state(scale)
+    ws = zp.new_workspace(1, S)
+    zp.zero_reduce_grads(reps, out, st, ws)
+    torch.cuda.synchronize()
+    idx = zs.sample_indices(S, 200_000, 21)
+    ti = torch.from_numpy(idx).cuda()
+    want = oracle.reduce_mean([to_host(r[ti]).view(np.float16) for r in reps], "f16", "f16")
+    assert to_host(out[ti]).tobytes() == want.tobytes(), "sampled mean differs from the oracle"
+    full = to_host(out).view(np.float16)
+    sumsq, bad = oracle.norm_overflow([full], "f16", scale)
+    s = zp.parse_state(st)
+    assert s["found_inf"] == float(bad) == 0.0
+    assert abs(s["sumsq"] - sumsq) <= 1e-6 * sumsq
+    del reps
+    torch.cuda.empty_cache()
