@@ -145,7 +145,7 @@ int zero_state_init(zero_state_t *host_state, double initial_loss_scale);
 typedef struct zero_hparams {
     double lr, beta1, beta2, eps, weight_decay;
     double max_norm;      /* global-norm clip threshold; <= 0 turns clipping off */
-    double min_scale;     /* floor of the loss scale on overflow (>= 1) */
+    double min_scale;     /* floor of the loss scale on overflow (a power of two >= 1) */
     int64_t scale_window; /* clean steps in a row before the scale doubles (>= 1) */
 } zero_hparams_t;
 

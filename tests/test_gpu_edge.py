@@ -266,6 +266,9 @@ def test_argument_errors_launch_nothing(zp):
     with pytest.raises(zp.ZeroError) as e:  # bad hyper-parameters
         zp.zero_adam_step(g[:n], p[:n], m, v, lp, zp.HParams(beta1=1.0), st, ws)
     assert e.value.code == -1
+    with pytest.raises(zp.ZeroError) as e:  # a scale floor that is not a power of two
+        zp.zero_step(g[:n], p[:n], m, v, lp, zp.HParams(min_scale=3.0), st, ws)
+    assert e.value.code == -1
     # host memory passed through the raw C ABI is refused
     host = np.zeros(n, np.float16)
     lib = zp.lib()

@@ -161,3 +161,14 @@ def test_every_f16_gradient_value_converts_exactly(zp):
     # m' = 0*0 + 1*g: -0 comes out as +0 (0 + -0 = +0), every other value as is
     want = np.float32(0.0) + g.astype(np.float32)
     assert m.tobytes() == want.tobytes()
+
+
+def test_decide_refuses_a_scale_floor_that_is_not_a_power_of_two(zp):
+    """Halving down to a floor that is not a power of two would leave a loss
+    scale whose reciprocal is inexact: such a floor is refused."""
+    st = host_state(zp, 1024.0, found_inf=1.0)
+    with pytest.raises(zp.ZeroError) as e:
+        zp.zero_offload_decide(st, zp.HParams(min_scale=3.0))
+    assert e.value.code == -1
+    sc = zp.zero_offload_decide(st, zp.HParams(min_scale=4.0))
+    assert sc is not None

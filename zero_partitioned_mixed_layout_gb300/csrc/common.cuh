@@ -389,11 +389,14 @@ struct DecideArgs {
 
 // Hyper-parameters in range: lr, eps, weight decay >= 0, betas in [0, 1),
 // a scale floor >= 1, a growth window >= 1, max_norm not NaN.
+// The floor of the loss scale is a power of two like the scale itself, so
+// that halving down to it keeps the scale a power of two.
 inline bool hparams_ok(const zero_hparams_t *hp)
 {
+    int e = 0;
     return hp->lr >= 0.0 && hp->beta1 >= 0.0 && hp->beta1 < 1.0 && hp->beta2 >= 0.0 && hp->beta2 < 1.0 &&
-           hp->eps >= 0.0 && hp->weight_decay >= 0.0 && hp->min_scale >= 1.0 && hp->scale_window >= 1 &&
-           hp->max_norm == hp->max_norm;
+           hp->eps >= 0.0 && hp->weight_decay >= 0.0 && hp->min_scale >= 1.0 && std::isfinite(hp->min_scale) &&
+           std::frexp(hp->min_scale, &e) == 0.5 && hp->scale_window >= 1 && hp->max_norm == hp->max_norm;
 }
 
 // The decision's arguments from the host hyper-parameters; freeze_step > 0

@@ -237,6 +237,9 @@ extern "C" int zero_offload_decide(zero_state_t *st, const zero_hparams_t *hp, z
         !(hp->eps >= 0.0) || !(hp->weight_decay >= 0.0) || !(hp->min_scale >= 1.0) || hp->scale_window < 1 ||
         hp->max_norm != hp->max_norm || !(st->loss_scale >= 1.0))
         return ZERO_EINVAL;
+    int e = 0;
+    if (!std::isfinite(hp->min_scale) || std::frexp(hp->min_scale, &e) != 0.5)  // a power of two
+        return ZERO_EINVAL;
     zero_offload_scalars_t o;
     std::memset(&o, 0, sizeof o);
     o.inv_scale = (float)(1.0 / st->loss_scale);
