@@ -239,7 +239,7 @@ int zero_reduce_grads(const void *const *replicas, int32_t n_replicas, int32_t d
 int zero_grad_norm_overflow_static(const zero_tlist_t *grads, zero_state_t *d_state,
                                    int32_t accumulate, void *stream);
 
-/* Pass 2 (preceded by a one-thread decision kernel): the step.
+/* Pass 2 (preceded by a decision kernel of one small block): the step.
  * From d_state's global sumsq / found_inf (left there by
  * zero_grad_norm_overflow, summed over ranks if there are several):
  *   - found_inf > 0: the step is skipped -- no state array, p_lp or t is
