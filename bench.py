@@ -319,23 +319,35 @@ class Workload:
         p_bytes = 2
         # algorithmic bytes per param of pass 2 and of the whole step
         self.bytes_adam = g_bytes + 12 + 12 + p_bytes
-        self.bytes_step = self.bytes_adam + g_bytes + (self.micro * 2 + 4 if self.micro > 1 else 0)
-        self.launches = 3 + (1 if self.micro > 1 else 0)  # see launches_per_step
+        # micro-batches: the accumulation carries pass 1 (the fp32 sums are
+        # not read back), so pass 1 adds no bytes of its own
+        self.bytes_step = self.bytes_adam + (self.micro * 2 + 4 if self.micro > 1 else g_bytes)
         self.l2_resident = self.bytes_step * self.S < 2 * L2_BYTES
 
     def launches_per_step(self, exchange=None) -> int:
         """Library kernels one timed step launches: zero_step on a flat shard
         is pass 1 (with the decision in its last block) and pass 2; a list,
         or a step with a cross-rank exchange, also launches the decision
-        kernel; micro-batches add the accumulation."""
-        base = 2 if (exchange is None and not self.listmode) else 3
-        return base + (1 if self.micro > 1 else 0)
+        kernel; micro-batches: the accumulation with pass 1, the decision
+        and pass 2."""
+        if self.micro > 1:
+            return 3
+        return 2 if (exchange is None and not self.listmode) else 3
 
     def step(self, stream, exchange=None, ev=None, g=None):
         zp = self.zp
         g = self.g if g is None else g
         if self.micro > 1:
-            zp.zero_accumulate_grads(g, self.bufs, overwrite=True, stream=stream)
+            # the accumulation with pass 1 fused, then the decision and pass 2
+            zp.zero_accumulate_grads_norm(g, self.bufs, self.state, self.ws, overwrite=True, stream=stream)
+            if exchange is not None:
+                exchange(self.state)
+            if ev is not None:
+                ev[0].record(stream)
+            zp.zero_adam_step(g, self.p, self.m, self.v, self.lp, self.hp, self.state, self.ws, stream=stream)
+            if ev is not None:
+                ev[1].record(stream)
+            return
         if exchange is None and ev is None:
             # one rank: the whole step in one call
             zp.zero_step(g, self.p, self.m, self.v, self.lp, self.hp, self.state, self.ws,

@@ -235,6 +235,84 @@ def test_accumulate(zp, gdtype, nb, overwrite):
     assert dacc.cpu().numpy().tobytes() == ref.tobytes()
 
 
+@pytest.mark.parametrize("gdtype,nb,overwrite,n", [
+    ("f16", 1, True, 9), ("bf16", 4, True, 200_003), ("bf16", 4, False, 200_003), ("f32", 2, False, 65_541),
+    ("f16", 8, True, 1_000_003), ("bf16", 4, True, 20_000_003)])
+def test_accumulate_norm(zp, gdtype, nb, overwrite, n):
+    """Accumulation fused with pass 1: the stored sums bit for bit as the
+    oracle's accumulation, and the squared norm and overflow of the sums as
+    the oracle's pass 1 over them, from a ragged 9 elements to 20,000,003
+    (many iterations of the persistent grid)."""
+    scale = 1024.0 if gdtype == "f16" else 1.0
+    bufs = [zs.host_grad(n, 7, 0, scale, gdtype, micro=j) for j in range(nb)]
+    acc0 = zs.host_normal(n, 1e-3, 7, "misc")
+    ref = acc0.copy()
+    oracle.accumulate(ref, bufs, gdtype, overwrite)
+    sumsq, bad = oracle.norm_overflow([ref], "f32", scale)
+    dacc = torch.from_numpy(acc0.copy()).cuda()
+    st = zp.new_state(scale)
+    ws = zp.new_workspace(1, n)
+    zp.zero_accumulate_grads_norm(dacc, [to_dev(b, gdtype) for b in bufs], st, ws, overwrite)
+    assert dacc.cpu().numpy().tobytes() == ref.tobytes()
+    s = zp.parse_state(st)
+    assert s["found_inf"] == float(bad) == 0.0
+    assert abs(s["sumsq"] - sumsq) <= 1e-6 * sumsq
+    # accumulate = True folds a second call (here overwriting acc) into the same sum
+    ref2 = ref.copy()
+    oracle.accumulate(ref2, bufs, gdtype, True)
+    sumsq2, _ = oracle.norm_overflow([ref2], "f32", scale)
+    zp.zero_accumulate_grads_norm(dacc, [to_dev(b, gdtype) for b in bufs], st, ws, True, accumulate=True)
+    assert dacc.cpu().numpy().tobytes() == ref2.tobytes()
+    assert abs(zp.parse_state(st)["sumsq"] - (sumsq + sumsq2)) <= 1e-6 * (sumsq + sumsq2)
+
+
+@pytest.mark.parametrize("where", ["vector", "tail"])
+def test_accumulate_norm_overflow(zp, where):
+    n = 100_005
+    bufs = [zs.host_grad(n, 8, 0, 1.0, "bf16", micro=j) for j in range(4)]
+    pos = 4097 if where == "vector" else n - 2
+    bufs[3].view(np.uint16)[pos] = 0x7F80  # +inf in the last micro-batch
+    acc = torch.empty(n, device="cuda")
+    st = zp.new_state(1.0)
+    ws = zp.new_workspace(1, n)
+    zp.zero_accumulate_grads_norm(acc, [to_dev(b, "bf16") for b in bufs], st, ws, True)
+    assert zp.parse_state(st)["found_inf"] == 1.0
+    assert np.isinf(acc.cpu().numpy()[pos])
+
+
+def test_accumulate_norm_then_step_against_oracle(zp):
+    """Three steps of four bf16 micro-batches with clipping: the fused
+    accumulation + pass 1, then the decision and pass 2, every element of
+    every step against the oracle's accumulation and step."""
+    n, micro, seed = 300_007, 4, 31
+    ohp, ghp = hp_pair(max_norm=0.05)
+    p0 = zs.host_master(n, seed)
+    dp = torch.from_numpy(p0.copy()).cuda()
+    dm = torch.zeros(n, device="cuda")
+    dv = torch.zeros(n, device="cuda")
+    dlp = torch.zeros(n, dtype=torch.bfloat16, device="cuda")
+    dacc = torch.empty(n, device="cuda")
+    state = zp.new_state(1.0)
+    ws = zp.new_workspace(1, n)
+    p, m, v = p0.copy(), np.zeros(n, np.float32), np.zeros(n, np.float32)
+    plp = np.zeros(n, np.uint16)
+    sc = oracle.Scaler(loss_scale=1.0)
+    for k in range(3):
+        bufs = [zs.host_grad(n, seed, k, 1.0, "bf16", micro=j) for j in range(micro)]
+        acc = np.zeros(n, np.float32)
+        oracle.accumulate(acc, bufs, "bf16", True)
+        zp.zero_accumulate_grads_norm(dacc, [to_dev(b, "bf16") for b in bufs], state, ws, True)
+        zp.zero_adam_step(dacc, dp, dm, dv, dlp, ghp, state, ws)
+        gst = zp.parse_state(state)
+        oracle_step([acc], "f32", [p], [m], [v], [plp], "bf16", ohp, sc, gst)
+        assert dacc.cpu().numpy().tobytes() == acc.tobytes()
+        assert_f32(to_host(dp), p, f"master step {k}")
+        assert_f32(to_host(dm), m, f"m step {k}")
+        assert_f32(to_host(dv), v, f"v step {k}")
+        assert np.array_equal(to_host(dlp), plp), f"p_lp step {k}"
+    assert zp.parse_state(state)["step"] == 3
+
+
 def test_argument_errors_launch_nothing(zp):
     n = 4096
     g = torch.zeros(n + 8, dtype=torch.float16, device="cuda")

@@ -27,6 +27,7 @@ from .binding import (  # noqa: F401
     OffloadScalars,
     default_host_threads,
     zero_accumulate_grads,
+    zero_accumulate_grads_norm,
     zero_offload_apply,
     zero_offload_copy,
     zero_offload_decide,

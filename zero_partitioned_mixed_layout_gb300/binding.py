@@ -82,6 +82,8 @@ def lib():
         so.zero_workspace_bytes.argtypes = [i64, i64]
         so.zero_workspace_bytes.restype = ctypes.c_size_t
         so.zero_accumulate_grads.argtypes = [vp, ctypes.POINTER(vp), i32, i32, i64, i32, vp]
+        so.zero_accumulate_grads_norm.argtypes = [vp, ctypes.POINTER(vp), i32, i32, i64, i32, vp, i32, vp,
+                                                  ctypes.c_size_t, vp]
         so.zero_grad_norm_overflow.argtypes = [ctypes.POINTER(_TList), vp, i32, vp,
                                                ctypes.c_size_t, vp]
         so.zero_adam_step.argtypes = [ctypes.POINTER(_TList)] * 5 + [
@@ -90,7 +92,8 @@ def lib():
         so.zero_reduce_grads.argtypes = [ctypes.POINTER(vp), i32, i32, i64, vp, i32, vp, i32, vp,
                                          ctypes.c_size_t, vp]
         for f in ("zero_partition_layout", "zero_state_init", "zero_accumulate_grads",
-                  "zero_grad_norm_overflow", "zero_adam_step", "zero_step", "zero_reduce_grads"):
+                  "zero_accumulate_grads_norm", "zero_grad_norm_overflow", "zero_adam_step", "zero_step",
+                  "zero_reduce_grads"):
             getattr(so, f).restype = ctypes.c_int
         _lib = so
     return _lib
@@ -269,6 +272,31 @@ def zero_accumulate_grads(acc, grads, overwrite: bool, stream=None) -> None:
                                      codes.pop(), acc.numel(), int(bool(overwrite)),
                                      _stream_ptr(stream, acc.device))
     _check(rc, "zero_accumulate_grads")
+
+
+def zero_accumulate_grads_norm(acc, grads, state, ws, overwrite: bool, accumulate: bool = False,
+                               stream=None) -> None:
+    """zero_accumulate_grads, then pass 1 (the squared norm and overflow of
+    the stored sums into ``state``), in one pass over the micro-batches."""
+    _device_tensor(acc, "acc")
+    if _dtype_code(acc) != ZERO_F32:
+        raise TypeError("acc must be float32")
+    grads = list(grads)
+    for g in grads:
+        _device_tensor(g, "grad")
+        if g.numel() != acc.numel():
+            raise ValueError("micro-batch gradient and accumulator sizes differ")
+    codes = {_dtype_code(g) for g in grads}
+    if len(codes) != 1:
+        raise TypeError("micro-batch gradients must share one element type")
+    _device_tensor(state, "state")
+    _device_tensor(ws, "workspace")
+    ptrs = (ctypes.c_void_p * len(grads))(*[g.data_ptr() for g in grads])
+    rc = lib().zero_accumulate_grads_norm(ctypes.c_void_p(acc.data_ptr()), ptrs, len(grads), codes.pop(),
+                                          acc.numel(), int(bool(overwrite)), ctypes.c_void_p(state.data_ptr()),
+                                          int(bool(accumulate)), ctypes.c_void_p(ws.data_ptr()), ws.numel(),
+                                          _stream_ptr(stream, acc.device))
+    _check(rc, "zero_accumulate_grads_norm")
 
 
 def zero_reduce_grads(replicas, out, state, ws, accumulate: bool = False, stream=None) -> None:
