@@ -130,9 +130,13 @@ def test_error_strings(zp):
 def test_binding_refuses_host_tensors(zp):
     torch = pytest.importorskip("torch")
     t = torch.zeros(16)
+    st, ws = torch.zeros(64, dtype=torch.uint8), torch.zeros(1024, dtype=torch.uint8)
     with pytest.raises(ValueError):
-        zp.zero_grad_norm_overflow(t, torch.zeros(64, dtype=torch.uint8),
-                                   torch.zeros(1024, dtype=torch.uint8))
+        zp.zero_grad_norm_overflow(t, st, ws)
+    with pytest.raises(ValueError):
+        zp.zero_accumulate_grads_norm(t, [torch.zeros(16, dtype=torch.float16)], st, ws, True)
+    with pytest.raises(ValueError):
+        zp.zero_step(torch.zeros(16, dtype=torch.float16), t, t.clone(), t.clone(), None, zp.HParams(), st, ws)
 
 
 # ---------------------------------------------------------------- stage-3 gather plan (host only)
