@@ -426,7 +426,10 @@ __global__ void __launch_bounds__(kThreads, 4)
 }
 
 // Pass 2 over a list: one block per tile of kTile elements of one tensor,
-// one vector per thread (the one-shot schedule of the flat kernel).
+// kTileVectors vectors per thread (one-shot).  Two vectors (4096-element
+// tiles) measured best over 10,000 tensors: 1.01 of the copy peak against
+// 0.98 with one and 1.00 with four; each block first reads its work item and
+// its tensor's entry, and larger tiles pay that once for more elements.
 template <int GT, int PT, bool V32>
 __global__ void __launch_bounds__(kThreads, 4)
     k_adam_list(const TensorEntry *__restrict__ ents, const WorkItem *__restrict__ tiles,
@@ -446,8 +449,10 @@ __global__ void __launch_bounds__(kThreads, 4)
     void *plp = e.plp ? static_cast<void *>(static_cast<char *>(e.plp) + start * 2) : nullptr;
     const int64_t nv = len >> 3;
     const int64_t t = threadIdx.x;
-    if (t < nv)
-        adam_vec<GT, PT, V32>(g, e.p + start, e.m + start, e.v + start, plp, t, s);
+#pragma unroll
+    for (int u = 0; u < kTileVectors; ++u)
+        if (t + u * kThreads < nv)
+            adam_vec<GT, PT, V32>(g, e.p + start, e.m + start, e.v + start, plp, t + u * kThreads, s);
     // the tail of a tensor's last tile (up to 7 elements) goes to threads
     // 0..6, which may also hold a vector: nv + tail can exceed the block
     if (t < (len & 7))

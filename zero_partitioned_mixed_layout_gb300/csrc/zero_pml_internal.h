@@ -25,7 +25,8 @@ constexpr int kMaxBlocks = 4096;
 constexpr int64_t kChunk = 1 << 16;
 // Elements per work item of pass 2 over a list: one block of kThreads
 // threads, one 8-element vector each.
-constexpr int64_t kTile = (int64_t)kThreads * 8;
+constexpr int kTileVectors = 2;  // 8-element vectors per thread of a pass-2 list tile
+constexpr int64_t kTile = (int64_t)kThreads * 8 * kTileVectors;
 
 // The scalars of one step's element update, written by the decision kernel
 // and read by every block of pass 2 (binary32, as the update runs).
