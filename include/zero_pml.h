@@ -42,8 +42,8 @@
  *     (loss scale, step count, the norm) moves on at every replay exactly as
  *     it would over the same calls issued one by one.  These are: zero_step,
  *     zero_adam_step and zero_grad_norm_overflow on one array per list (a
- *     flat shard), zero_accumulate_grads, zero_accumulate_grads_norm,
- *     zero_reduce_grads,
+ *     flat shard), zero_step_prepared (any list), zero_accumulate_grads,
+ *     zero_accumulate_grads_norm, zero_reduce_grads,
  *     zero_grad_norm_overflow_static (after a first call outside capture),
  *     zero_gather_params / zero_scatter_params with at most 64 tensors and
  *     256 shards, zero_onebit_worker, zero_onebit_server with at most 256
@@ -51,7 +51,8 @@
  *     table (a list of several arrays, a larger gather or server) returns
  *     ZERO_ECAPTURE under capture, having enqueued nothing: a captured copy
  *     would read the staging buffer when the graph is replayed, after later
- *     calls have reused it.  Issue those calls outside capture.
+ *     calls have reused it.  Issue those calls outside capture (for a list
+ *     step: prepare it outside, then capture zero_step_prepared).
  */
 #ifndef ZERO_PML_H
 #define ZERO_PML_H
@@ -289,6 +290,40 @@ int zero_adam_step(const zero_tlist_t *grads, const zero_tlist_t *master, const 
 int zero_step(const zero_tlist_t *grads, const zero_tlist_t *master, const zero_tlist_t *m,
               const zero_tlist_t *v, const zero_tlist_t *p_lp, const zero_hparams_t *hp,
               zero_state_t *d_state, void *ws, size_t ws_bytes, void *stream);
+
+/* A prepared step: the tables of a list of arrays built and copied into the
+ * workspace once, for steps that then copy nothing from the host.
+ *
+ * zero_list_prepare checks the lists as zero_adam_step does, copies the list's
+ * table into `ws` (stream-ordered on `stream`) and fills *plan (a HOST struct
+ * the caller keeps; its fields are the library's).  zero_step_prepared then
+ * runs zero_step over those lists from the resident table: pass 1, the
+ * decision and pass 2, with the results of zero_step bit for bit.  It copies
+ * nothing from the host, so it can be captured into a CUDA graph (the plan
+ * itself cannot be prepared under capture: ZERO_ECAPTURE), and its host cost
+ * does not grow with the number of arrays.  The arrays, their sizes and
+ * their element types are fixed at preparation; their contents change
+ * between steps as usual.  While a plan is in use its workspace serves that
+ * plan alone: a call that copies another table into it, or keeps block
+ * partials in its table region (zero_reduce_grads, the gather and the 1-bit
+ * server), overwrites the plan's table.  `ws` must be the workspace the plan
+ * was prepared in (ZERO_EINVAL otherwise).  A one-array list is accepted
+ * (the plan then holds its five pointers).  Errors: as zero_adam_step, plus
+ * ZERO_ECAPTURE from zero_list_prepare. */
+typedef struct zero_list_plan {
+    const void *ws;                         /* the workspace holding the table */
+    const void *ents, *tiles, *chunks;      /* the table's parts in ws (device) */
+    void *one[5];                           /* a one-array list: grad, master, m, v, p_lp */
+    int64_t n, total, n_tiles, n_chunks;    /* arrays, elements, work items of pass 2 and pass 1 */
+    int32_t gdtype, pdtype;                 /* element types; pdtype -1: no low-precision copy */
+    int32_t aligned32, reserved;
+} zero_list_plan_t;
+
+int zero_list_prepare(const zero_tlist_t *grads, const zero_tlist_t *master, const zero_tlist_t *m,
+                      const zero_tlist_t *v, const zero_tlist_t *p_lp, void *ws, size_t ws_bytes,
+                      zero_list_plan_t *plan, void *stream);
+int zero_step_prepared(const zero_list_plan_t *plan, const zero_hparams_t *hp, zero_state_t *d_state, void *ws,
+                       size_t ws_bytes, void *stream);
 
 /* ------------------------------------------------------------------ offload */
 

@@ -195,3 +195,23 @@ def test_gather_workspace_bytes(zp):
     assert a % 256 == 0 and a >= 580 * 32 + 16 * 8
     assert zp.zero_gather_workspace_bytes(0, 1) >= 256
     assert zp.zero_gather_workspace_bytes(10_000, 400) > zp.zero_gather_workspace_bytes(10_000, 1)
+
+
+def test_plan_struct_layout_matches_the_header(zp, tmp_path):
+    """The binding's copy of zero_list_plan_t has the C struct's size and
+    field offsets (compiled from the header with gcc)."""
+    import ctypes
+    import os
+    import subprocess
+    from zero_partitioned_mixed_layout_gb300 import binding
+    inc = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include")
+    src = tmp_path / "layout.c"
+    src.write_text('#include <stddef.h>\n#include <stdio.h>\n#include "zero_pml.h"\n'
+                   'int main(void) { printf("%zu %zu %zu %zu\\n", sizeof(zero_list_plan_t), '
+                   'offsetof(zero_list_plan_t, one), offsetof(zero_list_plan_t, n), '
+                   'offsetof(zero_list_plan_t, gdtype)); return 0; }\n')
+    exe = tmp_path / "layout"
+    subprocess.run(["gcc", "-std=c11", "-I", inc, str(src), "-o", str(exe)], check=True)
+    got = [int(x) for x in subprocess.run([str(exe)], check=True, capture_output=True, text=True).stdout.split()]
+    P = binding._ListPlan
+    assert got == [ctypes.sizeof(P), P.one.offset, P.n.offset, P.gdtype.offset]

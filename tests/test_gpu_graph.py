@@ -225,3 +225,125 @@ def test_gather_graph_replay(zp):
     full = torch.cat(shards)
     for t, off, k in zip(outs, lay.tensor_offset, numel):
         assert torch.equal(t, full[off:off + k])
+
+
+def _list_case(sizes, gdtype, pdtype, seed, scale):
+    rng = np.random.default_rng(seed)
+    d = {
+        "p": [torch.from_numpy(rng.standard_normal(n).astype(np.float32) * 0.02).cuda() for n in sizes],
+        "m": [torch.zeros(n, device="cuda") for n in sizes],
+        "v": [torch.zeros(n, device="cuda") for n in sizes],
+        "lp": [torch.zeros(n, dtype=TORCH[pdtype], device="cuda") for n in sizes],
+        "g": [torch.zeros(n, dtype=TORCH[gdtype], device="cuda") for n in sizes],
+    }
+    return d
+
+
+def _grads(sizes, gdtype, seed, k, scale, inf=False):
+    out = [zs.host_grad(n, seed + i, k, scale, gdtype) for i, n in enumerate(sizes)]
+    if inf:
+        out[1][7] = zs.host_cast(np.array([np.inf], np.float32), gdtype)[0]
+    return out
+
+
+@pytest.mark.parametrize("gdtype,pdtype", [("f16", "f16"), ("bf16", "bf16"), ("f32", "f16")])
+def test_prepared_list_step_equals_zero_step(zp, gdtype, pdtype):
+    """A prepared list step gives zero_step's results bit for bit, step
+    after step (an overflow in step 2), with the table copied once."""
+    sizes = [4099, 70_001, 2047, 1, 12_345]
+    scale = 1024.0 if gdtype == "f16" else 1.0
+    _, ghp = hp_pair(max_norm=0.3)
+    a, b = _list_case(sizes, gdtype, pdtype, 1, scale), _list_case(sizes, gdtype, pdtype, 1, scale)
+    sa, sb = zp.new_state(scale), zp.new_state(scale)
+    wa, wb = zp.new_workspace(len(sizes), sum(sizes)), zp.new_workspace(len(sizes), sum(sizes))
+    plan = zp.zero_list_prepare(b["g"], b["p"], b["m"], b["v"], b["lp"], wb)
+    assert plan.n == len(sizes)
+    for k in range(4):
+        hg = _grads(sizes, gdtype, 40, k, scale, inf=(k == 2))
+        for t, x in zip(a["g"], hg):
+            t.copy_(to_dev(x, gdtype))
+        for t, x in zip(b["g"], hg):
+            t.copy_(to_dev(x, gdtype))
+        zp.zero_step(a["g"], a["p"], a["m"], a["v"], a["lp"], ghp, sa, wa)
+        zp.zero_step_prepared(plan, ghp, sb, wb)
+        torch.cuda.synchronize()
+        for key in ("p", "m", "v", "lp"):
+            for x, y in zip(a[key], b[key]):
+                assert to_host(x).tobytes() == to_host(y).tobytes(), f"{key} step {k}"
+        assert sa.cpu().numpy().tobytes() == sb.cpu().numpy().tobytes()
+    assert zp.parse_state(sb)["step"] == 3 and zp.parse_state(sb)["skipped"] == 1
+
+
+def test_prepared_list_step_graph_replays_match_oracle(zp):
+    """A list step prepared once, then captured and replayed four times with
+    new gradients copied into the captured tensors: every element of every
+    step against the oracle."""
+    sizes = [4099, 70_001, 2047, 1, 12_345]
+    gdtype, pdtype, scale = "f16", "f16", 4096.0
+    ohp, ghp = hp_pair(max_norm=0.3)
+    d = _list_case(sizes, gdtype, pdtype, 2, scale)
+    host = {"p": [to_host(t).copy() for t in d["p"]], "m": [np.zeros(n, np.float32) for n in sizes],
+            "v": [np.zeros(n, np.float32) for n in sizes], "lp": [np.zeros(n, np.uint16) for n in sizes]}
+    state = zp.new_state(scale)
+    ws = zp.new_workspace(len(sizes), sum(sizes))
+    plan = zp.zero_list_prepare(d["g"], d["p"], d["m"], d["v"], d["lp"], ws)
+    zp.zero_grad_norm_overflow(d["g"][0], zp.new_state(scale), zp.new_workspace(1, sizes[0]))  # kernels loaded
+    torch.cuda.synchronize()
+    graph = capture(lambda: zp.zero_step_prepared(plan, ghp, state, ws))
+    assert zp.parse_state(state)["step"] == 0
+    sc = oracle.Scaler(loss_scale=scale)
+    for k in range(4):
+        hg = _grads(sizes, gdtype, 50, k, sc.loss_scale, inf=(k == 1))
+        for t, x in zip(d["g"], hg):
+            t.copy_(to_dev(x, gdtype))
+        graph.replay()
+        torch.cuda.synchronize()
+        gst = zp.parse_state(state)
+        oracle_step(hg, gdtype, host["p"], host["m"], host["v"], host["lp"], pdtype, ohp, sc, gst)
+        for i in range(len(sizes)):
+            assert_f32(to_host(d["p"][i]), host["p"][i], f"master {i} step {k}")
+            assert_f32(to_host(d["m"][i]), host["m"][i], f"m {i} step {k}")
+            assert_f32(to_host(d["v"][i]), host["v"][i], f"v {i} step {k}")
+            assert np.array_equal(to_host(d["lp"][i]), host["lp"][i]), f"p_lp {i} step {k}"
+    assert zp.parse_state(state)["step"] == 3
+
+
+def test_prepare_refused_under_capture_and_plan_checks(zp):
+    """Preparing copies a table: refused under capture.  A plan runs only in
+    the workspace it was prepared in.  A one-array plan runs zero_step."""
+    sizes = [1000, 2048]
+    _, ghp = hp_pair()
+    d = _list_case(sizes, "f16", "f16", 3, 1.0)
+    ws = zp.new_workspace(len(sizes), sum(sizes))
+    errors = []
+
+    def body():
+        try:
+            zp.zero_list_prepare(d["g"], d["p"], d["m"], d["v"], d["lp"], ws)
+        except zp.ZeroError as e:
+            errors.append(e)
+        marker.add_(1.0)
+
+    marker = torch.zeros(1, device="cuda")
+    capture(body)
+    assert len(errors) == 1 and errors[0].code == zp.ZERO_ECAPTURE
+    plan = zp.zero_list_prepare(d["g"], d["p"], d["m"], d["v"], d["lp"], ws)
+    other = zp.new_workspace(len(sizes), sum(sizes))
+    with pytest.raises(zp.ZeroError) as e:
+        zp.zero_step_prepared(plan, ghp, zp.new_state(1.0), other)
+    assert e.value.code == -1
+    # one array
+    n = 50_001
+    one = _list_case([n], "bf16", "bf16", 4, 1.0)
+    two = _list_case([n], "bf16", "bf16", 4, 1.0)
+    hg = _grads([n], "bf16", 60, 0, 1.0)
+    one["g"][0].copy_(to_dev(hg[0], "bf16"))
+    two["g"][0].copy_(to_dev(hg[0], "bf16"))
+    s1, s2 = zp.new_state(1.0), zp.new_state(1.0)
+    w1, w2 = zp.new_workspace(1, n), zp.new_workspace(1, n)
+    p1 = zp.zero_list_prepare(one["g"], one["p"], one["m"], one["v"], one["lp"], w1)
+    zp.zero_step_prepared(p1, ghp, s1, w1)
+    zp.zero_step(two["g"][0], two["p"][0], two["m"][0], two["v"][0], two["lp"][0], ghp, s2, w2)
+    torch.cuda.synchronize()
+    for key in ("p", "m", "v", "lp"):
+        assert to_host(one[key][0]).tobytes() == to_host(two[key][0]).tobytes(), key

@@ -37,6 +37,9 @@ from .binding import (  # noqa: F401
     zero_state_init,
     zero_reduce_grads,
     zero_step,
+    ListPlan,
+    zero_list_prepare,
+    zero_step_prepared,
     zero_strerror,
     zero_workspace_bytes,
     GatherPlan,

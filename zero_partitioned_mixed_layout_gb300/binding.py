@@ -345,6 +345,69 @@ def zero_step(grads, master, m, v, p_lp, hp: HParams, state, ws, stream=None) ->
     _step_call("zero_step", grads, master, m, v, p_lp, hp, state, ws, stream)
 
 
+class _ListPlan(ctypes.Structure):
+    _fields_ = [("ws", ctypes.c_void_p), ("ents", ctypes.c_void_p), ("tiles", ctypes.c_void_p),
+                ("chunks", ctypes.c_void_p), ("one", ctypes.c_void_p * 5), ("n", ctypes.c_int64),
+                ("total", ctypes.c_int64), ("n_tiles", ctypes.c_int64), ("n_chunks", ctypes.c_int64),
+                ("gdtype", ctypes.c_int32), ("pdtype", ctypes.c_int32), ("aligned32", ctypes.c_int32),
+                ("reserved", ctypes.c_int32)]
+
+
+class ListPlan:
+    """A list step prepared once (its tables resident in the workspace): see
+    zero_list_prepare.  Holds references to the tensors and the workspace."""
+
+    def __init__(self, c_plan, keep):
+        self._c = c_plan
+        self._keep = keep
+
+    @property
+    def n(self) -> int:
+        return int(self._c.n)
+
+
+def _plan_lib():
+    so = lib()
+    if not getattr(so, "_plan_ready", False):
+        vp = ctypes.c_void_p
+        so.zero_list_prepare.argtypes = [ctypes.POINTER(_TList)] * 5 + [vp, ctypes.c_size_t,
+                                                                         ctypes.POINTER(_ListPlan), vp]
+        so.zero_step_prepared.argtypes = [ctypes.POINTER(_ListPlan), ctypes.POINTER(_HParams), vp, vp,
+                                          ctypes.c_size_t, vp]
+        so.zero_list_prepare.restype = ctypes.c_int
+        so.zero_step_prepared.restype = ctypes.c_int
+        so._plan_ready = True
+    return so
+
+
+def zero_list_prepare(grads, master, m, v, p_lp, ws, stream=None) -> ListPlan:
+    """The tables of a list step copied into ``ws`` once; the returned plan
+    runs the step with zero_step_prepared, copying nothing from the host
+    (capturable into a CUDA graph)."""
+    lg = _ListArgs(grads, "grads")
+    lp_ = _ListArgs(master, "master", allow_pinned=True)
+    lm, lv = _ListArgs(m, "m", allow_pinned=True), _ListArgs(v, "v", allow_pinned=True)
+    ll = _ListArgs(p_lp, "p_lp") if p_lp is not None else None
+    _device_tensor(ws, "workspace")
+    plan = _ListPlan()
+    rc = _plan_lib().zero_list_prepare(ctypes.byref(lg.tl), ctypes.byref(lp_.tl), ctypes.byref(lm.tl),
+                                       ctypes.byref(lv.tl), ctypes.byref(ll.tl) if ll else None,
+                                       ctypes.c_void_p(ws.data_ptr()), ws.numel(), ctypes.byref(plan),
+                                       _stream_ptr(stream, ws.device))
+    _check(rc, "zero_list_prepare")
+    return ListPlan(plan, (grads, master, m, v, p_lp, ws, lg, lp_, lm, lv, ll))
+
+
+def zero_step_prepared(plan: ListPlan, hp: HParams, state, ws, stream=None) -> None:
+    """zero_step over the prepared lists, from their resident tables."""
+    _device_tensor(state, "state")
+    _device_tensor(ws, "workspace")
+    h = hp._c()
+    rc = _plan_lib().zero_step_prepared(ctypes.byref(plan._c), ctypes.byref(h), ctypes.c_void_p(state.data_ptr()),
+                                        ctypes.c_void_p(ws.data_ptr()), ws.numel(), _stream_ptr(stream, state.device))
+    _check(rc, "zero_step_prepared")
+
+
 def _step_call(fn, grads, master, m, v, p_lp, hp, state, ws, stream):
     lg = _ListArgs(grads, "grads")
     lp_ = _ListArgs(master, "master", allow_pinned=True)

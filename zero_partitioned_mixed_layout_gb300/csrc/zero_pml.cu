@@ -749,9 +749,8 @@ int launch_adam_lp(int32_t pdtype, const zero_tlist_t *g, const zero_tlist_t *p,
 }
 
 // Checks the arguments of the decision + pass 2 part of a step.
-int check_step_args(const zero_tlist_t *grads, const zero_tlist_t *master, const zero_tlist_t *m,
-                    const zero_tlist_t *v, const zero_tlist_t *p_lp, const zero_hparams_t *hp,
-                    zero_state_t *d_state, void *ws, size_t ws_bytes, int64_t *total)
+// The state and hyper-parameter arguments of a step.
+int check_state_hp(const zero_hparams_t *hp, zero_state_t *d_state)
 {
     if (!hp || !d_state)
         return ZERO_EINVAL;
@@ -761,6 +760,13 @@ int check_step_args(const zero_tlist_t *grads, const zero_tlist_t *master, const
         return ZERO_EINVAL;
     if (!hparams_ok(hp))
         return ZERO_EINVAL;
+    return ZERO_OK;
+}
+
+// The lists of a step and the workspace for them.
+int check_lists(const zero_tlist_t *grads, const zero_tlist_t *master, const zero_tlist_t *m,
+                const zero_tlist_t *v, const zero_tlist_t *p_lp, void *ws, size_t ws_bytes, int64_t *total)
+{
     int64_t t2 = 0;
     int rc = check_list(grads, total);
     if (rc != ZERO_OK)
@@ -789,6 +795,14 @@ int check_step_args(const zero_tlist_t *grads, const zero_tlist_t *master, const
     if (grads->n == 1 && ((grads->numel[0] >> 3) + 7) / kThreads >= 0x7fffffff)
         return ZERO_EINVAL;  // past 2^42 elements: beyond any device memory
     return check_ws(ws, ws_bytes, grads->n, *total);
+}
+
+int check_step_args(const zero_tlist_t *grads, const zero_tlist_t *master, const zero_tlist_t *m,
+                    const zero_tlist_t *v, const zero_tlist_t *p_lp, const zero_hparams_t *hp,
+                    zero_state_t *d_state, void *ws, size_t ws_bytes, int64_t *total)
+{
+    const int rc = check_state_hp(hp, d_state);
+    return rc != ZERO_OK ? rc : check_lists(grads, master, m, v, p_lp, ws, ws_bytes, total);
 }
 
 // Pass 2 on checked arguments (after this call's decision).
@@ -1116,6 +1130,91 @@ extern "C" int zero_step(const zero_tlist_t *grads, const zero_tlist_t *master, 
     if (rc != ZERO_OK)
         return rc;
     return run_step(grads, master, m, v, p_lp, hp, d_state, ws, s, pre != nullptr, pre);
+}
+
+// ------------------------------------------------------------- prepared steps
+
+extern "C" int zero_list_prepare(const zero_tlist_t *grads, const zero_tlist_t *master, const zero_tlist_t *m,
+                                 const zero_tlist_t *v, const zero_tlist_t *p_lp, void *ws, size_t ws_bytes,
+                                 zero_list_plan_t *plan, void *stream)
+{
+    if (!plan)
+        return ZERO_EINVAL;
+    int64_t total = 0;
+    int rc = check_lists(grads, master, m, v, p_lp, ws, ws_bytes, &total);
+    if (rc != ZERO_OK)
+        return rc;
+    zero_list_plan_t P;
+    std::memset(&P, 0, sizeof P);
+    P.ws = ws;
+    P.n = grads->n;
+    P.total = total;
+    P.gdtype = grads->dtype;
+    P.pdtype = p_lp ? p_lp->dtype : -1;
+    P.aligned32 = 1;
+    if (grads->n == 1) {
+        P.one[0] = grads->ptrs[0];
+        P.one[1] = master->ptrs[0];
+        P.one[2] = m->ptrs[0];
+        P.one[3] = v->ptrs[0];
+        P.one[4] = p_lp ? p_lp->ptrs[0] : nullptr;
+    } else if (grads->n > 1) {
+        ListDev L;
+        if ((rc = upload_list(grads, master, m, v, p_lp, ws, static_cast<cudaStream_t>(stream), &L)) != ZERO_OK)
+            return rc;
+        P.ents = L.ents;
+        P.tiles = L.tiles;
+        P.chunks = L.chunks;
+        P.n_tiles = L.n_tiles;
+        P.n_chunks = L.n_chunks;
+        P.aligned32 = L.aligned32 ? 1 : 0;
+    }
+    *plan = P;
+    return ZERO_OK;
+}
+
+extern "C" int zero_step_prepared(const zero_list_plan_t *plan, const zero_hparams_t *hp, zero_state_t *d_state,
+                                  void *ws, size_t ws_bytes, void *stream)
+{
+    if (!plan || plan->ws != ws || plan->n < 0 || !grad_dtype_ok(plan->gdtype) ||
+        (plan->pdtype != -1 && !lp_dtype_ok(plan->pdtype)))
+        return ZERO_EINVAL;
+    int rc = check_state_hp(hp, d_state);
+    if (rc != ZERO_OK)
+        return rc;
+    if ((rc = check_ws(ws, ws_bytes, plan->n, plan->total)) != ZERO_OK)
+        return rc;
+    if (plan->n <= 1) {
+        // a one-array list (or none): zero_step on the pointers the plan holds
+        void *g[1] = {plan->one[0]}, *p[1] = {plan->one[1]}, *mm[1] = {plan->one[2]}, *vv[1] = {plan->one[3]},
+             *lp[1] = {plan->one[4]};
+        const int64_t numel[1] = {plan->total};
+        const zero_tlist_t tg = {g, numel, plan->n, plan->gdtype}, tp = {p, numel, plan->n, ZERO_F32},
+                           tm = {mm, numel, plan->n, ZERO_F32}, tv = {vv, numel, plan->n, ZERO_F32},
+                           tl = {lp, numel, plan->n, plan->pdtype};
+        return zero_step(&tg, &tp, &tm, &tv, plan->pdtype >= 0 ? &tl : nullptr, hp, d_state, ws, ws_bytes, stream);
+    }
+    // the lists as far as the launches read them (their count and types);
+    // every array pointer comes from the resident table
+    const zero_tlist_t tg = {nullptr, nullptr, plan->n, plan->gdtype}, tf = {nullptr, nullptr, plan->n, ZERO_F32},
+                       tl = {nullptr, nullptr, plan->n, plan->pdtype};
+    ListDev L;
+    L.ents = static_cast<const TensorEntry *>(plan->ents);
+    L.tiles = static_cast<const WorkItem *>(plan->tiles);
+    L.chunks = static_cast<const WorkItem *>(plan->chunks);
+    L.n = plan->n;
+    L.n_tiles = plan->n_tiles;
+    L.n_chunks = plan->n_chunks;
+    L.aligned32 = plan->aligned32 != 0;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    switch (plan->gdtype) {
+    case ZERO_F16: rc = launch_norm<ZERO_F16>(&tg, plan->total, d_state, 0, ws, s, false, FoldedDecision{}, &L); break;
+    case ZERO_BF16: rc = launch_norm<ZERO_BF16>(&tg, plan->total, d_state, 0, ws, s, false, FoldedDecision{}, &L); break;
+    default: rc = launch_norm<ZERO_F32>(&tg, plan->total, d_state, 0, ws, s, false, FoldedDecision{}, &L); break;
+    }
+    if (rc != ZERO_OK)
+        return rc;
+    return run_step(&tg, &tf, &tf, &tf, plan->pdtype >= 0 ? &tl : nullptr, hp, d_state, ws, s, true, &L);
 }
 
 // ------------------------------------------------------------- pass 1 without workspace
