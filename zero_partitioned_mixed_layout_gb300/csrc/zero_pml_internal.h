@@ -22,7 +22,7 @@ constexpr int kThreads = 256;
 constexpr int kMaxBlocks = 4096;
 // Elements per work item when the arrays come as a list (multiple of 8, so
 // every chunk but a tensor's last starts and ends on a 16-byte boundary).
-constexpr int64_t kChunk = 1 << 16;
+constexpr int64_t kChunk = 1 << 13;  // elements of a pass-1 list work item (one warp each)
 // Elements per work item of pass 2 over a list: one block of kThreads
 // threads, one 8-element vector each.
 constexpr int kTileVectors = 2;  // 8-element vectors per thread of a pass-2 list tile
