@@ -254,7 +254,7 @@ def run_reference(args):
 class Workload:
     """Device buffers and the step of one benchmark workload on one rank."""
 
-    def __init__(self, name, log2n, rank, dev):
+    def __init__(self, name, log2n, rank, dev, prepared=False):
         import torch
 
         import zero_partitioned_mixed_layout_gb300 as zp
@@ -296,6 +296,9 @@ class Workload:
             self.v = zp.TensorList([torch.zeros(n, device=dev) for n in sizes], "v")
             self.lp = zp.TensorList([torch.empty(n, dtype=pdt, device=dev) for n in sizes], "p_lp")
             self.ws = zp.new_workspace(len(sizes), self.S, dev)
+            # prepared: the tables copied once, each step copies nothing
+            self.plan = (zp.zero_list_prepare(self.g, self.p, self.m, self.v, self.lp, self.ws)
+                         if prepared else None)
         else:
             lay = zp.zero_partition_layout(numel, w["nd"], w["align"])
             S = self.S = lay.shard_numel
@@ -350,8 +353,11 @@ class Workload:
             return
         if exchange is None and ev is None:
             # one rank: the whole step in one call
-            zp.zero_step(g, self.p, self.m, self.v, self.lp, self.hp, self.state, self.ws,
-                         stream=stream)
+            if getattr(self, "plan", None) is not None:
+                zp.zero_step_prepared(self.plan, self.hp, self.state, self.ws, stream=stream)
+            else:
+                zp.zero_step(g, self.p, self.m, self.v, self.lp, self.hp, self.state, self.ws,
+                             stream=stream)
             return
         zp.zero_grad_norm_overflow(g, self.state, self.ws, stream=stream)
         if exchange is not None:
@@ -376,7 +382,7 @@ def run_ours(args):
         torch.cuda.set_device(local)
         dist.init_process_group("nccl")
     dev = torch.device("cuda", torch.cuda.current_device())
-    wl = Workload(args.workload, args.log2n, rank, dev)
+    wl = Workload(args.workload, args.log2n, rank, dev, prepared=args.prepared)
     S = wl.S
     stream = torch.cuda.current_stream(dev)
     exchange = exchange_partials if world > 1 else None
@@ -531,7 +537,8 @@ def run_ours(args):
         "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
         "config": step_config(
-            wl.title, wl.w, S,
+            wl.title + ("; the list step prepared once (zero_step_prepared)" if getattr(wl, "plan", None) else ""),
+            wl.w, S,
             "L2 flushed (256 MB written) before each timed step; time is the sum of the steps alone"
             if flush is not None else
             f"inputs larger than L2 ({wl.bytes_step * S / 1e9:.2f} GB per step vs {L2_BYTES / 1e6:.0f} MB), "
@@ -1125,6 +1132,8 @@ def main():
                              "graph"],
                     help="default: the GPT-2 1.5B Nd=16 shard the metric is quoted on")
     ap.add_argument("--log2n", type=int, default=26, help="size of the flat workload (2^k)")
+    ap.add_argument("--prepared", action="store_true",
+                    help="frag_10k: the list step prepared once (zero_list_prepare / zero_step_prepared)")
     ap.add_argument("--clock-preroll", type=float, default=1.0,
                     help="seconds of untimed steps, sampled for clocks, before the timed ones")
     args = ap.parse_args()
