@@ -163,9 +163,11 @@ typedef struct zero_tlist {
     int32_t dtype;
 } zero_tlist_t;
 
-/* Bytes of device workspace that zero_grad_norm_overflow and zero_adam_step
- * need for lists of up to max_tensors arrays holding up to max_total_numel
- * elements in all.  The workspace must start on a 256-byte boundary (as
+/* Bytes of device workspace that zero_grad_norm_overflow, zero_adam_step,
+ * zero_step and zero_list_prepare need for lists of up to max_tensors arrays
+ * holding up to max_total_numel elements in all (zero_accumulate_grads_norm
+ * and zero_reduce_grads: one array of n elements; the 1-bit Adam calls:
+ * zero_workspace_bytes(Nd, Nd * S)).  The workspace must start on a 256-byte boundary (as
  * cudaMalloc and PyTorch allocations do) and be zero-filled before its first
  * use; each call leaves its reduction counter at zero again.  One workspace
  * must not be used by two calls that may run at the same time (two streams).
