@@ -399,8 +399,10 @@ def run_ours(args):
             dist.barrier()
         torch.cuda.synchronize(dev)
 
+    torch.cuda.nvtx.range_push(f"warm-up ({wl.name})")
     for _ in range(args.warmup):
         step()
+    torch.cuda.nvtx.range_pop()
     barrier()
     st = zp.parse_state(wl.state)
     assert st["last_skipped"] == 0 and st["step"] == args.warmup, st
@@ -421,7 +423,9 @@ def run_ours(args):
             torch.cuda.synchronize(dev)
         barrier()
         # the timed steps: nothing else in the stream between kernels, so
-        # each kernel launches while the previous one drains
+        # each kernel launches while the previous one drains (the NVTX range
+        # only marks them on a profiler's timeline)
+        torch.cuda.nvtx.range_push(f"timed steps ({wl.name})")
         t_start.record(stream)
         for k in range(args.steps):
             if flush is not None:
@@ -431,6 +435,7 @@ def run_ours(args):
             if flush is not None:
                 step_events[k][1].record(stream)
         t_end.record(stream)
+        torch.cuda.nvtx.range_pop()
         barrier()
         # the same number of steps again with events around zero_adam_step,
         # for the dominant kernel's own duration (the events break the launch
