@@ -54,7 +54,19 @@ def step_config(title, w, S, l2, world=1):
         "micro_batches": w["micro_batches"], "l2": l2,
         "parallelism": f"zero-dp{world}" if world > 1 else "zero-shard",
     }
+
+
 L2_BYTES = 129e6
+
+
+def nvtx(call, *args):
+    """torch.cuda.nvtx.range_push / range_pop, for a profiler's timeline; a
+    torch built without NVTX raises RuntimeError, and the bench runs on."""
+    import torch
+    try:
+        getattr(torch.cuda.nvtx, call)(*args)
+    except RuntimeError:
+        pass
 
 
 def kernel_source_hash() -> str:
@@ -399,10 +411,10 @@ def run_ours(args):
             dist.barrier()
         torch.cuda.synchronize(dev)
 
-    torch.cuda.nvtx.range_push(f"warm-up ({wl.name})")
+    nvtx("range_push", f"warm-up ({wl.name})")
     for _ in range(args.warmup):
         step()
-    torch.cuda.nvtx.range_pop()
+    nvtx("range_pop")
     barrier()
     st = zp.parse_state(wl.state)
     assert st["last_skipped"] == 0 and st["step"] == args.warmup, st
@@ -425,7 +437,7 @@ def run_ours(args):
         # the timed steps: nothing else in the stream between kernels, so
         # each kernel launches while the previous one drains (the NVTX range
         # only marks them on a profiler's timeline)
-        torch.cuda.nvtx.range_push(f"timed steps ({wl.name})")
+        nvtx("range_push", f"timed steps ({wl.name})")
         t_start.record(stream)
         for k in range(args.steps):
             if flush is not None:
@@ -435,7 +447,7 @@ def run_ours(args):
             if flush is not None:
                 step_events[k][1].record(stream)
         t_end.record(stream)
-        torch.cuda.nvtx.range_pop()
+        nvtx("range_pop")
         barrier()
         # the same number of steps again with events around zero_adam_step,
         # for the dominant kernel's own duration (the events break the launch
