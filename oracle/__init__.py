@@ -97,9 +97,9 @@ def load(path: str):
     so.zo_reduce_mean.argtypes = [ctypes.POINTER(vp), i32, ctypes.c_int, i64, vp, ctypes.c_int]
     f32 = ctypes.c_float
     so.zo_onebit_worker.argtypes = [vp, ctypes.c_int, i64, ctypes.POINTER(_Step), vp, vp, vp,
-                                    ctypes.POINTER(f32), f32]
+                                    ctypes.POINTER(f32), f32, vp]
     so.zo_onebit_server.argtypes = [ctypes.POINTER(vp), vp, i32, i64, vp, vp, ctypes.POINTER(f32),
-                                    f32, i32]
+                                    f32, i32, vp]
     so.zo_onebit_update.argtypes = [vp, vp, i64, i64, i64, vp, vp, vp, vp, ctypes.c_int,
                                     ctypes.POINTER(_Step)]
     for f in ("zo_f32_to_lp", "zo_lp_to_f32", "zo_accumulate", "zo_norm_overflow",
@@ -319,29 +319,39 @@ def _words(n: int) -> int:
     return (n + 31) // 32
 
 
+def _x_out(x_out: np.ndarray | None, n: int):
+    if x_out is None:
+        return None
+    assert x_out.dtype == np.float32 and x_out.size == n and x_out.flags["C_CONTIGUOUS"]
+    return _ptr(x_out)
+
+
 def onebit_worker(g: np.ndarray, gdtype: str, step: Step, m: np.ndarray, e: np.ndarray,
-                  scale: float | None = None):
+                  scale: float | None = None, x_out: np.ndarray | None = None):
     """Worker side of 1-bit Adam's compressed all-reduce: local momentum
     b1*m + (1-b1)*g, plus the worker error e, compressed to signs and one
     scale; e (float32) is updated in place, m is read only.  Returns (bits
     uint32[n/32], scale); unchanged inputs and (None, None) on a skipped
-    step.  ``scale`` forces the scale (see onebit_compress in the C file)."""
+    step.  ``scale`` forces the scale (see onebit_compress in the C file);
+    ``x_out`` (float32[n]) receives the compressed value x itself."""
     ga = np.ascontiguousarray(_bits(g, gdtype))
     n = ga.size
     assert m.dtype == np.float32 and e.dtype == np.float32 and m.size == n == e.size
     bits = np.zeros(_words(n), np.uint32)
     out = ctypes.c_float(0.0)
     lib().zo_onebit_worker(_ptr(ga), DTYPES[gdtype], n, ctypes.byref(step._c), _ptr(m), _ptr(e),
-                           _ptr(bits), ctypes.byref(out), -1.0 if scale is None else float(scale))
+                           _ptr(bits), ctypes.byref(out), -1.0 if scale is None else float(scale),
+                           _x_out(x_out, n))
     return (None, None) if step.skip else (bits, out.value)
 
 
 def onebit_server(bits: list[np.ndarray], scales: list[float], f: np.ndarray,
-                  scale: float | None = None, skip: bool = False):
+                  scale: float | None = None, skip: bool = False, x_out: np.ndarray | None = None):
     """Server side for one chunk of S elements: the Nd workers' signs on the
     chunk (uint32[S/32] each, rank order) and scales, averaged, plus the
     server error f (float32[S], updated in place), compressed again.
-    Returns (bits uint32[S/32], scale)."""
+    Returns (bits uint32[S/32], scale); ``x_out`` (float32[S]) receives
+    the compressed value itself."""
     S = f.size
     arrs = [np.ascontiguousarray(b, dtype=np.uint32) for b in bits]
     assert all(a.size == _words(S) for a in arrs) and f.dtype == np.float32
@@ -350,7 +360,7 @@ def onebit_server(bits: list[np.ndarray], scales: list[float], f: np.ndarray,
     out_bits = np.zeros(_words(S), np.uint32)
     out = ctypes.c_float(0.0)
     lib().zo_onebit_server(ptrs, _ptr(sc), len(arrs), S, _ptr(f), _ptr(out_bits), ctypes.byref(out),
-                           -1.0 if scale is None else float(scale), int(skip))
+                           -1.0 if scale is None else float(scale), int(skip), _x_out(x_out, S))
     return (None, None) if skip else (out_bits, out.value)
 
 
@@ -380,6 +390,8 @@ class OnebitResult:
     worker_scales: list = field(default_factory=list)
     server_bits: list = field(default_factory=list)
     server_scales: list = field(default_factory=list)
+    worker_x: list = field(default_factory=list)   # each compression's input x
+    server_x: list = field(default_factory=list)
 
 
 def onebit_step(grads: list[np.ndarray], gdtype: str, S: int, numel: int, p: np.ndarray,
@@ -405,17 +417,21 @@ def onebit_step(grads: list[np.ndarray], gdtype: str, S: int, numel: int, p: np.
     if st.skip:
         return res
     for i in range(nd):
+        x = np.empty(nd * S, np.float32)
         b, s_ = onebit_worker(grads[i], gdtype, st, m, e_w[i],
-                              None if worker_scales is None else worker_scales[i])
+                              None if worker_scales is None else worker_scales[i], x_out=x)
         res.worker_bits.append(b)
         res.worker_scales.append(s_)
+        res.worker_x.append(x)
     w = S // 32
     for j in range(nd):
+        x = np.empty(S, np.float32)
         b, s_ = onebit_server([res.worker_bits[i][j * w:(j + 1) * w] for i in range(nd)],
                               res.worker_scales, e_s[j],
-                              None if server_scales is None else server_scales[j])
+                              None if server_scales is None else server_scales[j], x_out=x)
         res.server_bits.append(b)
         res.server_scales.append(s_)
+        res.server_x.append(x)
     onebit_update(np.concatenate(res.server_bits), res.server_scales, S, numel, p, m, v, p_lp,
                   pdtype, st)
     return res

@@ -351,9 +351,14 @@ void zo_adam_apply_sampled(const void *g, int gdtype, const int64_t *idx, float 
 /* C applied in place: buf holds x on entry and the new error x - C(x) on
  * return; the signs go to bits and the scale to *scale.  A scale_in >= 0
  * replaces the computed scale (a test then follows another implementation's
- * rounding of the norm). */
-static void onebit_compress(float *buf, int64_t n, uint32_t *bits, float *scale, float scale_in)
+ * rounding of the norm).  x_out, if not NULL, receives x itself (for
+ * implementations that keep x and its scale and form the error x - C(x)
+ * when they next read it). */
+static void onebit_compress(float *buf, int64_t n, uint32_t *bits, float *scale, float scale_in, float *x_out)
 {
+    if (x_out)
+        for (int64_t i = 0; i < n; ++i)
+            x_out[i] = buf[i];
     double s = 0.0;
     for (int64_t i = 0; i < n; ++i)
         s += (double)buf[i] * (double)buf[i];
@@ -373,7 +378,7 @@ static void onebit_compress(float *buf, int64_t n, uint32_t *bits, float *scale,
  * compression.  e (the worker's error, n elements) is updated; m is read
  * only.  A skipped step touches nothing. */
 void zo_onebit_worker(const void *g, int gdtype, int64_t n, const zo_step *s, const float *m,
-                      float *e, uint32_t *bits, float *scale, float scale_in)
+                      float *e, uint32_t *bits, float *scale, float scale_in, float *x_out)
 {
     if (s->skip)
         return;
@@ -384,14 +389,15 @@ void zo_onebit_worker(const void *g, int gdtype, int64_t n, const zo_step *s, co
         const float mi = s->beta1 * m[i] + s->one_minus_beta1 * gi;
         e[i] = mi + e[i];
     }
-    onebit_compress(e, n, bits, scale, scale_in);
+    onebit_compress(e, n, bits, scale, scale_in, x_out);
 }
 
 /* Rank j as the server of its chunk of S elements: the Nd workers' signs
  * on that chunk (bits[i]: S/32 words) with their scales, averaged, plus the
  * server error f (S elements, updated), compressed again. */
 void zo_onebit_server(const uint32_t *const *bits, const float *scales, int32_t nd, int64_t S,
-                      float *f, uint32_t *out_bits, float *out_scale, float scale_in, int32_t skip)
+                      float *f, uint32_t *out_bits, float *out_scale, float scale_in, int32_t skip,
+                      float *x_out)
 {
     if (skip)
         return;
@@ -404,7 +410,7 @@ void zo_onebit_server(const uint32_t *const *bits, const float *scales, int32_t 
         }
         f[i] = a / count + f[i];
     }
-    onebit_compress(f, S, out_bits, out_scale, scale_in);
+    onebit_compress(f, S, out_bits, out_scale, scale_in, x_out);
 }
 
 /* Every worker: the synchronised momentum from the servers' signs (bits:

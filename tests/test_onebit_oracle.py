@@ -32,10 +32,11 @@ def _compress_step():
     return oracle.decide(_hp(beta1=0.0), oracle.Scaler(loss_scale=1.0), 0.0, 0)
 
 
-def compress(x, e):
-    """C(x + e) through the worker: returns (bits, scale); e updated."""
+def compress(x, e, x_out=None):
+    """C(x + e) through the worker: returns (bits, scale); e updated (and
+    x_out, if given, holds the compressed value x + e)."""
     m = np.zeros(x.size, F32)
-    return oracle.onebit_worker(np.ascontiguousarray(x, F32), "f32", _compress_step(), m, e)
+    return oracle.onebit_worker(np.ascontiguousarray(x, F32), "f32", _compress_step(), m, e, x_out=x_out)
 
 
 def unpack(bits, n):
@@ -76,7 +77,10 @@ def test_compress_scale_is_the_l2_scale_and_signs_are_bits(n):
     e0 = (rng.standard_normal(n) * 1e-4).astype(F32)
     buf = (x + e0).astype(F32)  # the binary32 sum the compressor sees
     e = e0.copy()
-    bits, scale = compress(x, e)
+    seen = np.full(n, np.nan, F32)
+    bits, scale = compress(x, e, seen)
+    # the compressor's input as reported is the binary32 sum itself
+    assert seen.tobytes() == buf.tobytes()
     exact = math.sqrt(math.fsum(float(b) * float(b) for b in buf) / n)
     assert abs(scale - exact) <= 2.0 ** -24 * exact * (1 + 1e-9)
     assert np.array_equal(unpack(bits, n), ~(buf < 0))
@@ -297,6 +301,7 @@ C_MUTANTS = [
     ("error not kept", "buf[i] = buf[i] - (plus ? sc : -sc);", "buf[i] = 0.0f * buf[i];"),
     ("error sign flipped", "buf[i] = buf[i] - (plus ? sc : -sc);", "buf[i] = (plus ? sc : -sc) - buf[i];"),
     ("bits big-endian", "bits[i / 32] |= 1u << (i % 32);", "bits[i / 32] |= 1u << (31 - i % 32);"),
+    ("compressor input not reported", "    if (x_out)\n", "    if (x_out && n < 0)\n"),
     ("server mean over nd - 1", "const float count = (float)nd;",
      "const float count = (float)(nd > 1 ? nd - 1 : 1);"),
     ("server error feedback dropped", "f[i] = a / count + f[i];", "f[i] = a / count;"),
