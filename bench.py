@@ -758,7 +758,9 @@ def run_onebit(args):
     messages), and the update from the 16 servers' signs with the frozen
     variance.  The synchronised momentum stays in its compressed form
     between steps (the previous servers' signs and scales): the worker reads
-    it from there and the update writes no dense copy."""
+    it from there and the update writes no dense copy.  The worker and
+    server errors are held in deferred form (each compression's input and
+    scale), so each compression is one pass."""
     import torch
 
     import zero_partitioned_mixed_layout_gb300 as zp
@@ -773,8 +775,8 @@ def run_onebit(args):
     v = zs.device_normal(n, 1e-3, 41, "misc", 2).square_()
     p = zs.device_normal(n, 0.02, 41, "master")
     plp = p.half()
-    e_w = torch.zeros(n, device=dev)
-    e_s = torch.zeros(S, device=dev)
+    x_w = torch.zeros(n, device=dev)
+    x_s = torch.zeros(S, device=dev)
     gen = torch.Generator(device=dev)
     gen.manual_seed(zs.stream_seed(0, "misc", 42))
     bits = torch.zeros(n // 32, dtype=torch.int32, device=dev)
@@ -797,10 +799,10 @@ def run_onebit(args):
         # the momentum: last step's server signs and scales (chunk 0 from this
         # rank's server, the rest received), read before this step's server
         # overwrites chunk 0
-        zp.zero_onebit_worker(g, (sbits, sscale), e_w, bits, wscale[0:1], hp, 1000, state, ws, stream=stream)
+        zp.zero_onebit_worker(g, (sbits, sscale), x_w, bits, wscale[0:1], hp, 1000, state, ws, stream=stream)
         if ev:
             ev[1].record(stream)
-        zp.zero_onebit_server(wlist, wscale, e_s, sbits[:S // 32], sscale[0:1], ws, stream=stream)
+        zp.zero_onebit_server(wlist, wscale, x_s, sbits[:S // 32], sscale[0:1], ws, stream=stream)
         if ev:
             ev[2].record(stream)
         zp.zero_onebit_update(sbits, sscale, S, numel, p, None, v, plp, ws, stream=stream)
@@ -826,8 +828,8 @@ def run_onebit(args):
     dt = e0.elapsed_time(e1) / args.steps * 1e-3
     ms = [statistics.mean(ev[k].elapsed_time(ev[k + 1]) for ev in evs) for k in range(3)]
     # bytes per element of the padded buffer (the momentum read as signs: 1/8)
-    b_worker = 2 + (2 + 1 / 8 + 8) + 8 + 1 / 8     # pass 1, worker, signs
-    b_server = (nd / 8 + 16 + 1 / 8) / nd            # per element of the whole buffer
+    b_worker = 2 + (2 + 1 / 8 + 8 + 1 / 8)         # pass 1; worker: g, m, x in and out, signs
+    b_server = (nd / 8 + 8 + 1 / 8) / nd             # per element of the whole buffer
     b_update = 1 / 8 + 8 + 4 + 2                     # signs, v and p; p and p_lp
     b_step = b_worker + b_server + b_update
     peaks = measured_peaks()
@@ -849,7 +851,8 @@ def run_onebit(args):
                      "traffic": None, "kernel": f"whole compression-stage step, {b_step:.2f} B/param",
                      "peak_source": "MEASURED_PEAKS.json hbm_gbs (of measured)" if peaks
                      else "fallback 6.8 TB/s (of fallback)"},
-        "gpu_launches": 7 * args.steps,
+        # pass 1, the decision, the worker, the server and the update
+        "gpu_launches": 5 * args.steps,
         "clocks": clk.summary(),
     }
     print(json.dumps(line), flush=True)
@@ -928,10 +931,10 @@ def run_graph(args):
 def run_onebit_server(args):
     """1-bit Adam's server call alone: chunk 0 of the GPT-2 1.5B layout in
     16 shards (S = 97,350,784 elements), the 16 workers' signs and scales as
-    received messages; per call the first pass (the workers' mean from the
-    tabulated rank-order sums, plus the server error, and its squared norm)
-    and the sign pass (signs and the new error).  About 0.6 GB on the
-    device: the size for a full ncu capture of the server kernel."""
+    received messages; per call one pass: the workers' mean from the
+    tabulated rank-order sums, plus the server error (formed from the
+    previous input and scale), its signs and its squared norm.  About 0.6 GB
+    on the device: the size for a full ncu capture of the server kernel."""
     import torch
 
     import zero_partitioned_mixed_layout_gb300 as zp
@@ -944,7 +947,7 @@ def run_onebit_server(args):
     wbits = [torch.randint(-2 ** 31, 2 ** 31 - 1, (S // 32,), dtype=torch.int32, device=dev, generator=gen)
              for _ in range(nd)]
     wscale = torch.rand(nd, device=dev, generator=gen) * 1e-3 + 1e-4
-    e_s = zs.device_normal(S, 1e-4, 44, "misc", 5)
+    x_s = zs.device_normal(S, 1e-4, 44, "misc", 5)
     sbits = torch.zeros(S // 32, dtype=torch.int32, device=dev)
     sscale = torch.zeros(1, device=dev)
     state = torch.frombuffer(bytearray(zp.zero_state_init(65536.0)), dtype=torch.uint8).to(dev)
@@ -959,7 +962,7 @@ def run_onebit_server(args):
                           zp.HParams(**zs.HPARAMS), 1000, state, ws, stream=stream)
 
     def step():
-        zp.zero_onebit_server(wbits, wscale, e_s, sbits, sscale, ws, stream=stream)
+        zp.zero_onebit_server(wbits, wscale, x_s, sbits, sscale, ws, stream=stream)
 
     for _ in range(args.warmup):
         step()
@@ -977,9 +980,9 @@ def run_onebit_server(args):
         e1.record(stream)
         torch.cuda.synchronize(dev)
     dt = e0.elapsed_time(e1) / args.steps * 1e-3
-    # per chunk element: the workers' signs, e_s read and written (first
-    # pass); e_s read and written, the signs written (sign pass)
-    b_elem = nd / 8 + 8 + 8 + 1 / 8
+    # per chunk element: the workers' signs, the previous input read, the
+    # new one and its signs written
+    b_elem = nd / 8 + 8 + 1 / 8
     peaks = measured_peaks()
     peak = peaks["hbm_gbs"] if peaks else 6800.0
     achieved = b_elem * S / dt / 1e9
@@ -993,10 +996,10 @@ def run_onebit_server(args):
                    "l2": "inputs larger than L2 (0.6 GB per call), no flush"},
         "bytes_per_element": b_elem,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
-                     "traffic": None, "kernel": f"server call (first pass + sign pass), {b_elem:.3f} B/element",
+                     "traffic": None, "kernel": f"server call (one pass), {b_elem:.3f} B/element",
                      "peak_source": "MEASURED_PEAKS.json hbm_gbs (of measured)" if peaks
                      else "fallback 6.8 TB/s (of fallback)"},
-        "gpu_launches": 2 * args.steps,
+        "gpu_launches": args.steps,
         "clocks": clk.summary(),
     }
     print(json.dumps(line), flush=True)

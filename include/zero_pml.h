@@ -465,6 +465,7 @@ int zero_gather_plan(const int64_t *numel, int64_t n_tensors, const int64_t *lay
  *   (exchange: chunk j of every worker's signs and its scale to rank j)
  *   zero_onebit_server                 y = mean over workers of C(x_i) on
  *                                      chunk r, + e_s; e_s <- y - C(y)
+ *   (the errors e_w and e_s are held in deferred form, see below)
  *   (exchange: every rank's server signs and scale to every worker)
  *   zero_onebit_update                 m <- the servers' C(y_j), all chunks;
  *                                      p <- p - (lr/(1-b1^t) * m /
@@ -480,7 +481,19 @@ int zero_gather_plan(const int64_t *numel, int64_t n_tensors, const int64_t *lay
  * decision (skip on overflow, loss scale, step count) holds for the other
  * two, and a skipped step changes nothing.  n and S must be multiples of 32
  * (ZERO_ESIZE); arrays 16-byte aligned.  Errors otherwise as
- * zero_adam_step. */
+ * zero_adam_step.
+ *
+ * The errors in deferred form.  Each error is x - C(x) for the input x of
+ * the compression that left it, so the calls keep x itself (x_w, x_s) and
+ * its scale (the call's own `scale`, read on entry and replaced on return)
+ * and form the error x - scale*sign(x) -- one binary32 subtraction, the
+ * same bits as forming it at once -- when the next step reads x.  A
+ * compression is then one pass over its input instead of two (8 bytes per
+ * element less).  Start the compression stage with x_w (x_s) zero and
+ * *scale zero: the error is then zero.  More generally, with *scale zero
+ * the array itself is the error (x - 0*sign(x) = x exactly), which is how to
+ * resume from an explicit error; the error of a pair (x, s) is
+ * x - s where x >= 0 or x is -0, x + s elsewhere. */
 
 /* Worker side.  grad: n elements (F16, BF16 or F32).  The synchronised
  * momentum comes either dense, m (fp32, n elements, read), or -- with m
@@ -489,18 +502,23 @@ int zero_gather_plan(const int64_t *numel, int64_t n_tensors, const int64_t *lay
  * multiple of 32 dividing n; ignored when m is given).  After the first
  * compression step the compressed form is exact and saves the 4 bytes per
  * element of a dense momentum on both the update's write and this read.
- * e_w: the worker error (fp32, updated); bits: n/32 words (written); scale:
- * one device float (written).  freeze_step: T_w, the count of the last
- * warm-up step (>= 1). */
+ * x_w: the worker's error in deferred form (fp32, n elements: the input of
+ * this worker's previous compression on entry, this one's on return);
+ * bits: n/32 words (written); scale: one device float (the previous
+ * compression's scale on entry, this one's on return).  freeze_step: T_w,
+ * the count of the last warm-up step (>= 1). */
 int zero_onebit_worker(const void *grad, int32_t gdtype, const float *m, const uint32_t *m_bits,
-                       const float *m_scales, int64_t S, float *e_w, int64_t n, uint32_t *bits, float *scale,
+                       const float *m_scales, int64_t S, float *x_w, int64_t n, uint32_t *bits, float *scale,
                        const zero_hparams_t *hp, int64_t freeze_step, zero_state_t *d_state, void *ws,
                        size_t ws_bytes, void *stream);
 
 /* Server side for this rank's chunk of S elements.  worker_bits: HOST array
  * of nd device pointers, each to S/32 words (the chunk's signs from worker
- * i); worker_scales: device array of nd floats; e_s: the server error (S
- * fp32, updated); bits: S/32 words and scale: one device float (written).
+ * i); worker_scales: device array of nd floats; x_s: the server's error in
+ * deferred form (S fp32: the input of this rank's previous server
+ * compression on entry, this one's on return); bits: S/32 words (written);
+ * scale: one device float (the previous server compression's scale on
+ * entry, this one's on return).
  * At most 4096 workers (ZERO_ECAPACITY).  Up to 256 workers the pointers
  * travel as a launch argument; beyond, as a table copied into the
  * workspace (not capturable: ZERO_ECAPTURE under stream capture).  The
@@ -509,7 +527,7 @@ int zero_onebit_worker(const void *grad, int32_t gdtype, const float *m, const u
  * additions in the same order, and adds the remaining workers' terms to the
  * entry an element's signs select. */
 int zero_onebit_server(const uint32_t *const *worker_bits, const float *worker_scales, int32_t nd, int64_t S,
-                       float *e_s, uint32_t *bits, float *scale, void *ws, size_t ws_bytes, void *stream);
+                       float *x_s, uint32_t *bits, float *scale, void *ws, size_t ws_bytes, void *stream);
 
 /* Update.  bits: nd*S/32 words, the servers' signs in rank order;
  * server_scales: device array of nd floats; m: the dense momentum, nd*S

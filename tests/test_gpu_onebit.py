@@ -3,7 +3,12 @@ workers, the Nd servers and the update of one compression-stage step, each
 worker and server as the rank it would be (its own state and workspace), bit
 for bit once the GPU's scales are handed to the oracle (the binary64 norm is
 summed in another order: the scales themselves agree within 2^-22); and the
-benchmark's full-size step on sampled elements plus the norm property."""
+benchmark's full-size step on sampled elements plus the norm property.
+
+The GPU holds each error in deferred form (the compression's input x and
+its scale s; the error is x - s*sign(x)); the oracle holds it explicitly.
+The tests compare the GPU's x with the oracle's compressed value and the
+error the pair (x, s) stands for with the oracle's error, bit for bit."""
 import numpy as np
 import pytest
 
@@ -48,6 +53,14 @@ def bit_at(w, idx):
     return ((w[idx >> 5] >> (idx & 31).astype(np.uint32)) & 1).astype(np.uint8)
 
 
+def deferred_error(x, s):
+    """The error a compression with input x (float32) and scale s left:
+    x - s where x is not negative (-0 included), x + s elsewhere; one
+    binary32 rounding."""
+    s = np.float32(s)
+    return np.where(x < 0, x + s, x - s).astype(np.float32)
+
+
 def pack(b):
     """Bits (one per element, in order) to packed words."""
     b = np.pad(np.asarray(b, np.uint8), (0, (-len(b)) % 32))
@@ -84,9 +97,16 @@ def setup(zp, nd, S, gdtype, pdtype, seed, loss_scale, T, inf_at=None):
         "p": zs.host_master(n, seed),
         "m": (rng.standard_normal(n) * 1e-3).astype(np.float32),
         "v": (rng.uniform(0.1, 1.0, n) * 1e-6).astype(np.float32),
-        "ew": [(rng.standard_normal(n) * 1e-4).astype(np.float32) for _ in range(nd)],
-        "es": [(rng.standard_normal(S) * 1e-4).astype(np.float32) for _ in range(nd)],
+        # the errors in the GPU's deferred form: inputs and scales of a
+        # previous compression
+        "xw": [(rng.standard_normal(n) * 1e-4).astype(np.float32) for _ in range(nd)],
+        "xs": [(rng.standard_normal(S) * 1e-4).astype(np.float32) for _ in range(nd)],
+        "sw": rng.uniform(1e-5, 1e-4, nd).astype(np.float32),
+        "ss": rng.uniform(1e-5, 1e-4, nd).astype(np.float32),
     }
+    # the same errors, explicit, for the oracle
+    h["ew"] = [deferred_error(x, s) for x, s in zip(h["xw"], h["sw"])]
+    h["es"] = [deferred_error(x, s) for x, s in zip(h["xs"], h["ss"])]
     if inf_at is not None:
         g = h["g"][inf_at[0]]
         (g.view(np.uint16) if gdtype != "f32" else g.view(np.uint32))[inf_at[1]] = \
@@ -95,13 +115,13 @@ def setup(zp, nd, S, gdtype, pdtype, seed, loss_scale, T, inf_at=None):
     d = {
         "g": [to_dev(g, gdtype) for g in h["g"]],
         "p": to_dev(h["p"], "f32"), "m": to_dev(h["m"], "f32"), "v": to_dev(h["v"], "f32"),
-        "ew": [to_dev(e, "f32") for e in h["ew"]], "es": [to_dev(e, "f32") for e in h["es"]],
+        "ew": [to_dev(x, "f32") for x in h["xw"]], "es": [to_dev(x, "f32") for x in h["xs"]],
         "plp": (to_dev(h["plp"].view(np.float16) if pdtype == "f16" else h["plp"], pdtype)
                 if pdtype else None),
         "wbits": [torch.zeros(n // 32, dtype=torch.int32, device="cuda") for _ in range(nd)],
-        "wscale": torch.zeros(nd, dtype=torch.float32, device="cuda"),
+        "wscale": torch.from_numpy(h["sw"].copy()).cuda(),
         "sbits": torch.zeros(n // 32, dtype=torch.int32, device="cuda"),
-        "sscale": torch.zeros(nd, dtype=torch.float32, device="cuda"),
+        "sscale": torch.from_numpy(h["ss"].copy()).cuda(),
         "state": [state_at(zp, loss_scale, T) for _ in range(nd)],
         "ws": [zp.new_workspace(1, n) for _ in range(nd)],
     }
@@ -131,10 +151,14 @@ def check_step(zp, h, d, nd, S, numel, gdtype, pdtype, hp, sc, T, dense_m=True):
     for i in range(nd):
         assert abs(gw[i] - free.worker_scales[i]) <= SCALE_REL * free.worker_scales[i], f"worker {i} scale"
         assert np.array_equal(words(d["wbits"][i]), res.worker_bits[i]), f"worker {i} signs"
-        assert to_host(d["ew"][i]).tobytes() == h["ew"][i].tobytes(), f"worker {i} error"
+        x = to_host(d["ew"][i])
+        assert x.tobytes() == res.worker_x[i].tobytes(), f"worker {i} compressed value"
+        assert deferred_error(x, gw[i]).tobytes() == h["ew"][i].tobytes(), f"worker {i} error"
     for j in range(nd):
         assert abs(gs[j] - free.server_scales[j]) <= 4 * SCALE_REL * free.server_scales[j], f"server {j} scale"
-        assert to_host(d["es"][j]).tobytes() == h["es"][j].tobytes(), f"server {j} error"
+        x = to_host(d["es"][j])
+        assert x.tobytes() == res.server_x[j].tobytes(), f"server {j} compressed value"
+        assert deferred_error(x, gs[j]).tobytes() == h["es"][j].tobytes(), f"server {j} error"
     assert np.array_equal(words(d["sbits"]), np.concatenate(res.server_bits))
     assert to_host(d["p"]).tobytes() == h["p"].tobytes(), "master"
     if dense_m:
@@ -201,7 +225,7 @@ def test_onebit_overflow_skips_everything(zp):
     nd, S, T = 2, 2048, 30
     h, d = setup(zp, nd, S, "f16", "f16", 5, 4096.0, T, inf_at=(1, 777))
     before = {k: [to_host(t).tobytes() for t in (d[k] if isinstance(d[k], list) else [d[k]])]
-              for k in ("p", "m", "ew", "es", "plp")}
+              for k in ("p", "m", "ew", "es", "plp", "wscale", "sscale", "wbits", "sbits")}
     run_gpu_step(zp, d, nd, S, nd * S, zp.HParams(), T, "f16")
     for k, v in before.items():
         assert [to_host(t).tobytes() for t in (d[k] if isinstance(d[k], list) else [d[k]])] == v, k
@@ -225,6 +249,7 @@ def test_onebit_full_size_rank0_sampled(zp):
     g = torch.empty(n, dtype=torch.float16, device=dev)
     zs.device_grad_into(g, 31, 0, 65536.0)
     m = zs.device_normal(n, 1e-3, 32, "misc", 1)
+    # the worker's error; with its scale 0 the deferred form is the error itself
     e = zs.device_normal(n, 1e-4, 32, "misc", 2)
     v = zs.device_normal(n, 1e-3, 32, "misc", 3).square_()
     p = zs.device_normal(n, 0.02, 32, "master")
@@ -241,24 +266,28 @@ def test_onebit_full_size_rank0_sampled(zp):
     hp = zp.HParams()
     zp.zero_onebit_worker(g, m, e, bits, wscale[0:1], hp, 1000, state, ws)
     torch.cuda.synchronize()
-    # the norm property, in binary64 on the device: x = e' + scale*sign(x)
+    # the norm property, in binary64 on the device, over the compressed
+    # value x the array now holds; and every sign bit is the sign of x
     sc0 = float(wscale[0])
     shifts = torch.arange(32, device=dev, dtype=torch.int32)
     tot = 0.0
     for s0 in range(0, n, 1 << 27):
         s1 = min(n, s0 + (1 << 27))
         plus = ((bits[s0 // 32:s1 // 32].view(-1, 1) >> shifts) & 1).reshape(-1).bool()
-        x = e[s0:s1].double() + torch.where(plus, sc0, -sc0).double()
+        x = e[s0:s1].double()
+        assert torch.equal(plus, ~(x < 0)), f"signs of [{s0}, {s1})"
         tot += float((x * x).sum())
     norm = (tot / n) ** 0.5
     assert abs(sc0 - norm) <= SCALE_REL * norm
     # sampled elements, with the GPU's scale
     hp_o = oracle.HParams()
     st = oracle.frozen_variance(oracle.decide(hp_o, oracle.Scaler(65536.0, 1000), 0.0, 0), hp_o, 1000)
-    ob, _ = oracle.onebit_worker(h_g, "f16", st, h_m, h_e, scale=sc0)
+    xo = np.empty(idx.size, np.float32)
+    ob, _ = oracle.onebit_worker(h_g, "f16", st, h_m, h_e, scale=sc0, x_out=xo)
     w_all = words(bits)
     assert np.array_equal(bit_at(w_all, idx), bit_at(ob, np.arange(idx.size)))
-    assert to_host(e[ti]).tobytes() == h_e.tobytes()
+    assert to_host(e[ti]).tobytes() == xo.tobytes()
+    assert deferred_error(to_host(e[ti]), sc0).tobytes() == h_e.tobytes()
     # server on chunk 0: the other workers' signs and scales are messages
     gen = torch.Generator(device=dev)
     gen.manual_seed(zs.stream_seed(0, "misc", 9))
@@ -270,14 +299,17 @@ def test_onebit_full_size_rank0_sampled(zp):
     sscale = torch.rand(nd, device=dev, generator=gen) * 1e-3 + 1e-4
     sidx = zs.sample_indices(S, 50_000, 6)
     tsi = torch.from_numpy(sidx).to(dev)
-    f = np.concatenate([to_host(es[tsi]), np.zeros((-sidx.size) % 32, np.float32)])
+    # the server's error in deferred form: es and its previous scale sscale[0]
+    f = deferred_error(to_host(es[tsi]), float(sscale[0]))
+    f = np.concatenate([f, np.zeros((-sidx.size) % 32, np.float32)])
     chunk_words = [w_all[:S // 32]] + [words(o) for o in others]
     sub = [pack(bit_at(w, sidx)) for w in chunk_words]
     zp.zero_onebit_server([bits[:S // 32]] + others, wscale, es, sbits[:S // 32], sscale[0:1], ws)
     torch.cuda.synchronize()
     s0 = float(sscale[0])
-    ob, _ = oracle.onebit_server(sub, list(wscale.cpu().numpy()), f, scale=s0)
-    assert to_host(es[tsi]).tobytes() == f[:sidx.size].tobytes()
+    xo = np.empty(f.size, np.float32)
+    ob, _ = oracle.onebit_server(sub, list(wscale.cpu().numpy()), f, scale=s0, x_out=xo)
+    assert to_host(es[tsi]).tobytes() == xo[:sidx.size].tobytes()
     assert np.array_equal(bit_at(words(sbits[:S // 32]), sidx), bit_at(ob, np.arange(sidx.size)))
     # the update; the other chunks' signs and scales are messages
     tail_p = to_host(p[numel:]).copy()
@@ -353,15 +385,18 @@ def server_case(zp, nd, S, seed, T=10):
 
 def check_server(hb, hs, hf, d):
     """The GPU's server pass against the oracle's (handed the GPU's scale):
-    the new error and the signs bit for bit, the scale within the norm's
-    summation-order bound."""
+    the compressed value, the error it stands for and the signs bit for
+    bit, the scale within the norm's summation-order bound.  The server
+    started from scale 0, so its array was the explicit error hf."""
     torch.cuda.synchronize()
     gs = float(d["scale"][0])
     _, free = oracle.onebit_server([b.copy() for b in hb], list(hs), hf.copy())
     assert abs(gs - free) <= 4 * SCALE_REL * free, "server scale"
     f = hf.copy()
-    ob, _ = oracle.onebit_server(hb, list(hs), f, scale=gs)
-    assert to_host(d["es"]).tobytes() == f.tobytes(), "server error"
+    x = np.empty_like(f)
+    ob, _ = oracle.onebit_server(hb, list(hs), f, scale=gs, x_out=x)
+    assert to_host(d["es"]).tobytes() == x.tobytes(), "server compressed value"
+    assert deferred_error(x, gs).tobytes() == f.tobytes(), "server error"
     assert np.array_equal(words(d["bits"]), ob), "server signs"
 
 
@@ -392,3 +427,33 @@ def test_onebit_server_equal_scales(zp):
     d["es"].zero_()
     zp.zero_onebit_server(d["wbits"], d["wscale"], d["es"], d["bits"], d["scale"], d["ws"])
     check_server(hb, hs, hf, d)
+
+
+def _off16(t):
+    """The values of t in a buffer that starts 16 bytes past a 32-byte
+    boundary."""
+    buf = torch.empty(t.numel() + 4, dtype=t.dtype, device=t.device)
+    v = buf[4:]
+    v.copy_(t)
+    assert v.data_ptr() % 32 == 16
+    return v
+
+
+@pytest.mark.parametrize("compressed", [False, True])
+def test_onebit_16_byte_aligned_arrays(zp, compressed):
+    """fp32 arrays on a 16-byte but not a 32-byte boundary take two 16-byte
+    accesses per 8 elements instead of one 32-byte access, in all three
+    calls: the same results bit for bit."""
+    nd, S, T = 4, 4096, 40
+    _, d = setup(zp, nd, S, "f16", "f16", 77, 1024.0, T)
+    clone = {k: ([t.clone() for t in v] if isinstance(v, list) else v.clone()) for k, v in d.items()}
+    for k in ("ew", "es"):
+        clone[k] = [_off16(t) for t in clone[k]]
+    for k in ("p", "m", "v"):
+        clone[k] = _off16(clone[k])
+    for dd in (d, clone):
+        run_gpu_step(zp, dd, nd, S, nd * S - 3, zp.HParams(), T, "f16", compressed=compressed)
+    for k in ("ew", "es", "wbits", "sbits", "wscale", "sscale", "p", "m", "plp", "state"):
+        a = d[k] if isinstance(d[k], list) else [d[k]]
+        b = clone[k] if isinstance(clone[k], list) else [clone[k]]
+        assert [to_host(t).tobytes() for t in a] == [to_host(t).tobytes() for t in b], k

@@ -573,16 +573,19 @@ def _f32_tensor(t, what: str, n: int | None = None):
     return t
 
 
-def zero_onebit_worker(grad, m, e_w, bits, scale, hp: HParams, freeze_step: int, state, ws,
+def zero_onebit_worker(grad, m, x_w, bits, scale, hp: HParams, freeze_step: int, state, ws,
                        stream=None) -> None:
     """1-bit Adam, worker side: the decision (variance frozen at step
     freeze_step), then x = b1*m + (1-b1)*g + e_w compressed to signs (bits,
-    int32[n/32]) and one scale (float32[1]); e_w updated.  m is the dense
-    momentum (float32[n]) or the compressed one, a tuple (signs int32[n/32],
-    scales float32[Nd]) from the previous step's servers."""
+    int32[n/32]) and one scale (float32[1]).  The error e_w is held in
+    deferred form: x_w (float32[n]) and scale hold the previous
+    compression's input and scale on entry (e_w = x_w - scale*sign(x_w);
+    zeros to start) and this one's on return.  m is the dense momentum
+    (float32[n]) or the compressed one, a tuple (signs int32[n/32], scales
+    float32[Nd]) from the previous step's servers."""
     n = grad.numel()
     _device_tensor(grad, "grad")
-    _f32_tensor(e_w, "e_w", n), _f32_tensor(scale, "scale", 1)
+    _f32_tensor(x_w, "x_w", n), _f32_tensor(scale, "scale", 1)
     _words_tensor(bits, "bits", n // 32)
     _device_tensor(state, "state"), _device_tensor(ws, "workspace")
     if isinstance(m, (tuple, list)):
@@ -597,24 +600,27 @@ def zero_onebit_worker(grad, m, e_w, bits, scale, hp: HParams, freeze_step: int,
     h = hp._c()
     rc = _onebit_lib().zero_onebit_worker(
         ctypes.c_void_p(grad.data_ptr()), _dtype_code(grad), dense, mbp, msp, chunk,
-        ctypes.c_void_p(e_w.data_ptr()), n, ctypes.c_void_p(bits.data_ptr()),
+        ctypes.c_void_p(x_w.data_ptr()), n, ctypes.c_void_p(bits.data_ptr()),
         ctypes.c_void_p(scale.data_ptr()), ctypes.byref(h), int(freeze_step),
         ctypes.c_void_p(state.data_ptr()), ctypes.c_void_p(ws.data_ptr()), ws.numel(),
         _stream_ptr(stream, state.device))
     _check(rc, "zero_onebit_worker")
 
 
-def zero_onebit_server(worker_bits, worker_scales, e_s, bits, scale, ws, stream=None) -> None:
-    """1-bit Adam, server side for this rank's chunk of S = e_s.numel()
+def zero_onebit_server(worker_bits, worker_scales, x_s, bits, scale, ws, stream=None) -> None:
+    """1-bit Adam, server side for this rank's chunk of S = x_s.numel()
     elements: worker_bits (Nd int32 tensors of S/32 words, rank order) and
-    worker_scales (float32[Nd]) averaged, plus e_s, compressed again."""
-    S = e_s.numel()
+    worker_scales (float32[Nd]) averaged, plus the server error e_s,
+    compressed again.  e_s in deferred form as in zero_onebit_worker: x_s
+    and scale (float32[1]) hold the previous server compression's input and
+    scale on entry and this one's on return."""
+    S = x_s.numel()
     wb = [_words_tensor(b, "worker bits", S // 32) for b in worker_bits]
-    _f32_tensor(worker_scales, "worker_scales", len(wb)), _f32_tensor(e_s, "e_s")
+    _f32_tensor(worker_scales, "worker_scales", len(wb)), _f32_tensor(x_s, "x_s")
     _words_tensor(bits, "bits", S // 32), _f32_tensor(scale, "scale", 1), _device_tensor(ws, "workspace")
     ptrs = (ctypes.c_void_p * max(len(wb), 1))(*[b.data_ptr() for b in wb])
     rc = _onebit_lib().zero_onebit_server(
-        ptrs, ctypes.c_void_p(worker_scales.data_ptr()), len(wb), S, ctypes.c_void_p(e_s.data_ptr()),
+        ptrs, ctypes.c_void_p(worker_scales.data_ptr()), len(wb), S, ctypes.c_void_p(x_s.data_ptr()),
         ctypes.c_void_p(bits.data_ptr()), ctypes.c_void_p(scale.data_ptr()),
         ctypes.c_void_p(ws.data_ptr()), ws.numel(), _stream_ptr(stream, ws.device))
     _check(rc, "zero_onebit_server")

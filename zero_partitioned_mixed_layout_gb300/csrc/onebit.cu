@@ -11,16 +11,19 @@
 // feedback on the workers and on the servers.
 //
 // Every pass streams HBM.  A compression needs the L2 norm of its whole
-// input before any sign can be turned into an error, so it takes two
-// kernels: the first forms the input (stored in place of the error) and its
+// input before any sign can be turned into an error, and a second pass over
+// the input would cost 8 bytes per element more.  So the error is kept in
+// deferred form: the state array holds the compression's input x itself and
+// the scale array its scale s, and the error x - s*sign(x) is formed (one
+// binary32 subtraction, the same as forming it at once) when the next step
+// reads x.  One pass then reads the previous x, forms the new input and
+// writes it, its signs (packed 32 to a word with two warp shuffles) and its
 // squared norm (binary32 squares in 8 lanes, one binary64 add per 32
-// elements, fixed-order block partials, the last block finishing the sum and
-// writing the scale); the second writes the signs, packed 32 to a word with
-// two warp shuffles, and the new error.  Bytes per element with an fp16
-// gradient: worker 2 + 1/8 + 8 with the momentum as the servers' signs (2 +
-// 4 + 8 with a dense one), then 8 + 1/8 for the signs; server (Nd/8 + 8) +
-// 8 + 1/8 per chunk element; update 1/8 + 12 + 2 (+ 4 with a dense
-// momentum written).
+// elements, fixed-order block partials, the last block finishing the sum
+// and writing the new scale).  Bytes per element with an fp16 gradient:
+// worker 2 + 1/8 + 8 + 1/8 with the momentum as the servers' signs (2 + 4 +
+// 8 + 1/8 with a dense one); server Nd/8 + 8 + 1/8 per chunk element;
+// update 1/8 + 12 + 2 (+ 4 with a dense momentum written).
 #include <vector>
 
 #include "common.cuh"
@@ -28,19 +31,41 @@
 namespace zpml {
 namespace {
 
+// 8 binary32 values at p with streaming (evict-first) hints: one 32-byte
+// access when p is on a 32-byte boundary (W32), else two 16-byte ones.  The
+// 32-byte form matters for the fused compression passes: with two 16-byte
+// accesses a lane's instruction covers half of each 32-byte sector, and the
+// worker pass measured 2.2-5.8 TB/s depending on how the compiler placed
+// the two halves, against 6.7 TB/s with one 32-byte access.
+template <bool W32>
 __device__ __forceinline__ void ld8(const float *p, float *f)
 {
-    const float4 a = __ldcs(reinterpret_cast<const float4 *>(p));
-    const float4 b = __ldcs(reinterpret_cast<const float4 *>(p) + 1);
-    f[0] = a.x; f[1] = a.y; f[2] = a.z; f[3] = a.w;
-    f[4] = b.x; f[5] = b.y; f[6] = b.z; f[7] = b.w;
+    if constexpr (W32) {
+        asm("ld.global.cs.v8.f32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+            : "=f"(f[0]), "=f"(f[1]), "=f"(f[2]), "=f"(f[3]), "=f"(f[4]), "=f"(f[5]), "=f"(f[6]), "=f"(f[7])
+            : "l"(p));
+    } else {
+        const float4 a = __ldcs(reinterpret_cast<const float4 *>(p));
+        const float4 b = __ldcs(reinterpret_cast<const float4 *>(p) + 1);
+        f[0] = a.x; f[1] = a.y; f[2] = a.z; f[3] = a.w;
+        f[4] = b.x; f[5] = b.y; f[6] = b.z; f[7] = b.w;
+    }
 }
 
+template <bool W32>
 __device__ __forceinline__ void st8(float *p, const float *f)
 {
-    __stcs(reinterpret_cast<float4 *>(p), make_float4(f[0], f[1], f[2], f[3]));
-    __stcs(reinterpret_cast<float4 *>(p) + 1, make_float4(f[4], f[5], f[6], f[7]));
+    if constexpr (W32) {
+        asm volatile("st.global.cs.v8.f32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"l"(p), "f"(f[0]), "f"(f[1]),
+                     "f"(f[2]), "f"(f[3]), "f"(f[4]), "f"(f[5]), "f"(f[6]), "f"(f[7])
+                     : "memory");
+    } else {
+        __stcs(reinterpret_cast<float4 *>(p), make_float4(f[0], f[1], f[2], f[3]));
+        __stcs(reinterpret_cast<float4 *>(p) + 1, make_float4(f[4], f[5], f[6], f[7]));
+    }
 }
+
+bool aligned32(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 31u) == 0; }
 
 // End of a squared-norm pass: publish this block's partial; the block that
 // takes the last ticket sums the partials in block order and writes the
@@ -93,6 +118,34 @@ struct SquareSum {
     __device__ __forceinline__ double total() const { return tot + (double)part; }
 };
 
+// The error a compression left, from its input x and scale sc: x - sc where
+// x is not negative (sign +1, also for -0), x + sc where it is.
+__device__ __forceinline__ float deferred_error(float x, float sc)
+{
+    return __fsub_rn(x, !(x < 0.0f) ? sc : -sc);
+}
+
+// Sign bits of one 8-element group: bit k for element k, 1 where the value
+// is not negative (-0 counts as +).
+__device__ __forceinline__ uint32_t sign_byte(const float *x)
+{
+    uint32_t byte = 0;
+#pragma unroll
+    for (int k = 0; k < 8; ++k)
+        byte |= (uint32_t)!(x[k] < 0.0f) << k;
+    return byte;
+}
+
+// The word of 32 signs that four consecutive lanes' bytes make (lane & 3 =
+// the byte's place in the word); warp code, every lane calls it.
+__device__ __forceinline__ uint32_t sign_word(uint32_t byte)
+{
+    uint32_t w = byte << (8 * (threadIdx.x & 3));
+    w |= __shfl_xor_sync(0xffffffffu, w, 1);
+    w |= __shfl_xor_sync(0xffffffffu, w, 2);
+    return w;
+}
+
 // The skip flag of these kernels comes from device memory.  They do not
 // return early on it: a data-dependent exit ahead of the block barriers of
 // the reduction cost a third of the streaming rate of the loop on GB300 (the
@@ -110,7 +163,7 @@ struct Momentum {
     int64_t chunk;         // S
 };
 
-template <bool kCompressed>
+template <bool kCompressed, bool W32>
 __device__ __forceinline__ void load_momentum(const Momentum &mm, int64_t i, float *f)
 {
     if constexpr (kCompressed) {
@@ -120,46 +173,66 @@ __device__ __forceinline__ void load_momentum(const Momentum &mm, int64_t i, flo
         for (int k = 0; k < 8; ++k)
             f[k] = ((byte >> k) & 1u) ? sc : -sc;
     } else {
-        ld8(mm.dense + 8 * i, f);
+        ld8<W32>(mm.dense + 8 * i, f);
     }
 }
 
-// Worker, first pass: x = b1*m + (1-b1)*g + e (g unscaled, clipped), stored
-// over e; the squared norm of x into the scale.
-template <int GT, bool kCompressed>
-__global__ void __launch_bounds__(kThreads) k_onebit_worker(const void *g, Momentum mm, float *e, int64_t n,
+// Worker: x = b1*m + (1-b1)*g + e (g unscaled, clipped), e the error the
+// previous compression left in deferred form (its input xs over which x is
+// stored, and its scale, read here before this compression's scale replaces
+// it); the signs of x and its squared norm into the new scale.  A warp's
+// lanes hold 32 consecutive 8-element groups, so that four lanes make one
+// word of signs.
+template <int GT, bool kCompressed, bool W32>
+__global__ void __launch_bounds__(kThreads) k_onebit_worker(const void *g, Momentum mm, float *xs, int64_t n,
                                                             const StepScalars *scp, double2 *partials,
-                                                            WsHeader *hdr, float *scale)
+                                                            WsHeader *hdr, float *scale, uint32_t *bits)
 {
     pdl_wait();
     const StepScalars s = *scp;
+    // every block reads the old scale before its ticket; the new one is
+    // written by the last block, after every ticket
+    const float prev = *scale;
     constexpr int W = Elem<GT>::kWords;
     const uint4 *gv = static_cast<const uint4 *>(g);
     SquareSum acc;
     const int64_t nv = s.skip ? 0 : n >> 3;
-    for (int64_t i = (int64_t)blockIdx.x * kThreads + threadIdx.x; i < nv; i += (int64_t)gridDim.x * kThreads) {
-        uint4 w[W];
+    const int64_t stride = (int64_t)gridDim.x * kThreads;
+    // the loop runs warp by warp (i0 is the warp's first group), so that the
+    // shuffles of the sign words see every lane
+    for (int64_t i0 = (int64_t)blockIdx.x * kThreads + (threadIdx.x & ~31); i0 < nv; i0 += stride) {
+        const int64_t i = i0 + (threadIdx.x & 31);
+        uint32_t byte = 0;
+        if (i < nv) {
+            uint4 w[W];
 #pragma unroll
-        for (int q = 0; q < W; ++q)
-            w[q] = __ldcs(gv + i * W + q);
-        float gf[8], mf[8], x[8];
-        Elem<GT>::to_float(w, gf);
-        load_momentum<kCompressed>(mm, i, mf);
-        ld8(e + 8 * i, x);
+            for (int q = 0; q < W; ++q)
+                w[q] = __ldcs(gv + i * W + q);
+            float gf[8], mf[8], x[8];
+            Elem<GT>::to_float(w, gf);
+            load_momentum<kCompressed, W32>(mm, i, mf);
+            ld8<W32>(xs + 8 * i, x);
 #pragma unroll
-        for (int k = 0; k < 8; ++k) {
-            const float gk = __fmul_rn(__fmul_rn(gf[k], s.inv_scale), s.clip);
-            const float mk = __fadd_rn(__fmul_rn(s.b1, mf[k]), __fmul_rn(s.omb1, gk));
-            x[k] = __fadd_rn(mk, x[k]);
+            for (int k = 0; k < 8; ++k) {
+                const float gk = __fmul_rn(__fmul_rn(gf[k], s.inv_scale), s.clip);
+                const float mk = __fadd_rn(__fmul_rn(s.b1, mf[k]), __fmul_rn(s.omb1, gk));
+                x[k] = __fadd_rn(mk, deferred_error(x[k], prev));
+            }
+            st8<W32>(xs + 8 * i, x);
+            acc.add(x);
+            byte = sign_byte(x);
         }
-        st8(e + 8 * i, x);
-        acc.add(x);
+        const uint32_t word = sign_word(byte);
+        if ((threadIdx.x & 3) == 0 && i < nv)
+            bits[i >> 2] = word;
     }
     scale_finish(acc.total(), partials, hdr, n, scale, s.skip != 0);
 }
 
-// Server, first pass over the chunk: y = (sum over workers in rank order of
-// +-scale_k) / Nd + f, stored over f; the squared norm of y into the scale.
+// Server over the chunk: y = (sum over workers in rank order of +-scale_k)
+// / Nd + f, f the error the previous compression left in deferred form (its
+// input ys over which y is stored, and its scale); the signs of y and its
+// squared norm into the new scale.
 //
 // Per element the sum is Nd dependent binary32 additions, which would make
 // the pass bound by instruction issue rather than by memory.  But an element
@@ -176,7 +249,7 @@ __global__ void __launch_bounds__(kThreads) k_onebit_worker(const void *g, Momen
 // worker's 32 sign words is one full 128-byte line; shuffles hand each lane
 // the words of its vectors.  A vector's signs from 8 workers are 8 bytes;
 // an 8x8 bit-matrix transpose turns them into one byte per element, bit q
-// for worker q of the group.  Bytes per chunk element: Nd/8 + 4 + 4.
+// for worker q of the group.  Bytes per chunk element: Nd/8 + 4 + 4 + 1/8.
 constexpr int kTableBits = 14;
 // Workers per server call: their pointers and scales (12 bytes each) and
 // the 64 KiB table fit in shared memory.
@@ -233,10 +306,10 @@ __host__ __device__ constexpr size_t server_smem_bytes(int nd)
            (sizeof(void *) + sizeof(float)) * (size_t)nd;
 }
 
-template <bool kPow2>
+template <bool kPow2, bool W32>
 __device__ __forceinline__ void server_body(const uint32_t *const *wbits, const float *wscales, int nd, float inv_nd,
-                                            float *f, int64_t S, const StepScalars *scp, double2 *partials,
-                                            WsHeader *hdr, float *scale)
+                                            float *ys, int64_t S, const StepScalars *scp, double2 *partials,
+                                            WsHeader *hdr, float *scale, uint32_t *bits)
 {
     extern __shared__ __align__(16) unsigned char s_raw[];
     const int P = nd < kTableBits ? nd : kTableBits;
@@ -244,6 +317,8 @@ __device__ __forceinline__ void server_body(const uint32_t *const *wbits, const 
     const uint32_t **s_ptr = reinterpret_cast<const uint32_t **>(s_raw + sizeof(float) * ((size_t)1 << P));
     float *s_scale = reinterpret_cast<float *>(s_ptr + nd);
     pdl_wait();
+    // the old scale, read by every block before its ticket
+    const float prev = *scale;
     for (int k = threadIdx.x; k < nd; k += kThreads) {
         s_ptr[k] = wbits[k];
         s_scale[k] = wscales[k];
@@ -285,7 +360,7 @@ __device__ __forceinline__ void server_body(const uint32_t *const *wbits, const 
         for (int v = 0; v < 4; ++v) {
             const int64_t i = v0 + lane + 32 * v;
             if (i < nv)
-                ld8(f + 8 * i, y[v]);
+                ld8<W32>(ys + 8 * i, y[v]);
         }
         float a[4][8];
         {
@@ -332,68 +407,46 @@ __device__ __forceinline__ void server_body(const uint32_t *const *wbits, const 
 #pragma unroll
         for (int v = 0; v < 4; ++v) {
             const int64_t i = v0 + lane + 32 * v;
+            uint32_t byte = 0;
             if (i < nv) {
 #pragma unroll
                 for (int j = 0; j < 8; ++j) {
                     // a power-of-two count: the product by its reciprocal is
                     // the correctly rounded quotient itself
                     const float mean = kPow2 ? __fmul_rn(a[v][j], inv_nd) : __fdiv_rn(a[v][j], count);
-                    y[v][j] = __fadd_rn(mean, y[v][j]);
+                    y[v][j] = __fadd_rn(mean, deferred_error(y[v][j], prev));
                 }
-                st8(f + 8 * i, y[v]);
+                st8<W32>(ys + 8 * i, y[v]);
                 acc.add(y[v]);
+                byte = sign_byte(y[v]);
             }
+            // lanes 4j..4j+3 hold groups 4j..4j+3 of this v: one word
+            const uint32_t word = sign_word(byte);
+            if ((lane & 3) == 0 && i < nv)
+                bits[i >> 2] = word;
         }
     }
     scale_finish(acc.total(), partials, hdr, S, scale, skip);
 }
 
 // The worker pointers from a table in the workspace, or as a launch argument.
-template <bool kPow2>
+template <bool kPow2, bool W32>
 __global__ void __launch_bounds__(kThreads, 2) k_onebit_server(const uint32_t *const *wbits, const float *wscales,
-                                                               int nd, float inv_nd, float *f, int64_t S,
+                                                               int nd, float inv_nd, float *ys, int64_t S,
                                                                const StepScalars *scp, double2 *partials,
-                                                               WsHeader *hdr, float *scale)
+                                                               WsHeader *hdr, float *scale, uint32_t *bits)
 {
-    server_body<kPow2>(wbits, wscales, nd, inv_nd, f, S, scp, partials, hdr, scale);
+    server_body<kPow2, W32>(wbits, wscales, nd, inv_nd, ys, S, scp, partials, hdr, scale, bits);
 }
 
-template <bool kPow2>
+template <bool kPow2, bool W32>
 __global__ void __launch_bounds__(kThreads, 2) k_onebit_server_args(const __grid_constant__ WorkerPtrs wp,
                                                                     const float *wscales, int nd, float inv_nd,
-                                                                    float *f, int64_t S, const StepScalars *scp,
-                                                                    double2 *partials, WsHeader *hdr, float *scale)
+                                                                    float *ys, int64_t S, const StepScalars *scp,
+                                                                    double2 *partials, WsHeader *hdr, float *scale,
+                                                                    uint32_t *bits)
 {
-    server_body<kPow2>(wp.p, wscales, nd, inv_nd, f, S, scp, partials, hdr, scale);
-}
-
-// Second pass of a compression (worker or server): the signs of x, 32 to a
-// word, and the new error x - scale*sign(x) over x.  One 8-element group
-// per thread (one-shot grid); the four threads of a word meet by shuffles.
-__global__ void __launch_bounds__(kThreads) k_onebit_sign(float *x, int64_t n, const float *scale, uint32_t *bits,
-                                                          const StepScalars *scp)
-{
-    pdl_wait();
-    const float sc = *scale;
-    const int64_t i = (int64_t)blockIdx.x * kThreads + threadIdx.x;
-    const int64_t nv = scp->skip ? 0 : n >> 3;
-    uint32_t byte = 0;
-    if (i < nv) {
-        float v[8];
-        ld8(x + 8 * i, v);
-#pragma unroll
-        for (int k = 0; k < 8; ++k) {
-            const bool plus = !(v[k] < 0.0f);
-            byte |= (uint32_t)plus << k;
-            v[k] = __fsub_rn(v[k], plus ? sc : -sc);
-        }
-        st8(x + 8 * i, v);
-    }
-    uint32_t w = byte << (8 * (threadIdx.x & 3));
-    w |= __shfl_xor_sync(0xffffffffu, w, 1);
-    w |= __shfl_xor_sync(0xffffffffu, w, 2);
-    if ((threadIdx.x & 3) == 0 && i < nv)
-        bits[i >> 2] = w;
+    server_body<kPow2, W32>(wp.p, wscales, nd, inv_nd, ys, S, scp, partials, hdr, scale, bits);
 }
 
 // One element of the update with the frozen variance:
@@ -412,7 +465,7 @@ constexpr int kNoLowP = -1;
 // parameters only the first numel elements (the group that straddles numel
 // goes element by element).  m (the dense momentum) is written only when
 // given: the next worker can read the momentum in its compressed form.
-template <int PT>
+template <int PT, bool W32>
 __global__ void __launch_bounds__(kThreads) k_onebit_update(const uint32_t *bits, const float *scales, int64_t S,
                                                             int64_t n, int64_t numel, float *p, float *m,
                                                             const float *v, void *plp, const StepScalars *scp)
@@ -429,15 +482,15 @@ __global__ void __launch_bounds__(kThreads) k_onebit_update(const uint32_t *bits
     for (int k = 0; k < 8; ++k)
         mf[k] = ((byte >> k) & 1u) ? sc : -sc;
     if (m)
-        st8(m + 8 * i, mf);
+        st8<W32>(m + 8 * i, mf);
     if (8 * i + 8 <= numel) {
         float vf[8], pf[8];
-        ld8(v + 8 * i, vf);
-        ld8(p + 8 * i, pf);
+        ld8<W32>(v + 8 * i, vf);
+        ld8<W32>(p + 8 * i, pf);
 #pragma unroll
         for (int k = 0; k < 8; ++k)
             onebit_elem(mf[k], vf[k], pf[k], s);
-        st8(p + 8 * i, pf);
+        st8<W32>(p + 8 * i, pf);
         if constexpr (PT != kNoLowP)
             __stcs(reinterpret_cast<uint4 *>(plp) + i, LowP<PT>::pack(pf));
     } else {
@@ -471,8 +524,8 @@ StepScalars *step_scalars(void *ws)
     return reinterpret_cast<StepScalars *>(static_cast<unsigned char *>(ws) + kWsScalars);
 }
 
-template <int GT, bool kCompressed>
-int launch_worker(const void *g, const Momentum &mm, float *e, int64_t n, uint32_t *bits, float *scale, void *ws,
+template <int GT, bool kCompressed, bool W32>
+int launch_worker(const void *g, const Momentum &mm, float *xs, int64_t n, uint32_t *bits, float *scale, void *ws,
                   cudaStream_t st)
 {
     unsigned char *w = static_cast<unsigned char *>(ws);
@@ -480,23 +533,23 @@ int launch_worker(const void *g, const Momentum &mm, float *e, int64_t n, uint32
     double2 *partials = reinterpret_cast<double2 *>(w + kWsPartials);
     const StepScalars *sc = step_scalars(ws);
     const int64_t nv = n >> 3;
-    const int grid =
-        grid_for((const void *)k_onebit_worker<GT, kCompressed>, (nv + kThreads - 1) / kThreads, kMaxBlocks, 4);
-    launch_k(k_onebit_worker<GT, kCompressed>, grid, kThreads, st, true, g, mm, e, n, sc, partials, hdr, scale);
-    int rc = check_launch("zero_onebit_worker (first pass)");
-    if (rc != ZERO_OK)
-        return rc;
-    launch_k(k_onebit_sign, (int)((nv + kThreads - 1) / kThreads), kThreads, st, true, e, n, (const float *)scale,
-             bits, sc);
-    return check_launch("zero_onebit_worker (signs)");
+    auto kern = k_onebit_worker<GT, kCompressed, W32>;
+    const int grid = grid_for((const void *)kern, (nv + kThreads - 1) / kThreads, kMaxBlocks, 4);
+    launch_k(kern, grid, kThreads, st, true, g, mm, xs, n, sc, partials, hdr, scale, bits);
+    return check_launch("zero_onebit_worker");
 }
 
+// The worker for the momentum's form and the fp32 arrays' alignment (32
+// bytes: one access per 8 elements).
 template <int GT>
-int launch_worker_m(const void *g, const Momentum &mm, float *e, int64_t n, uint32_t *bits, float *scale, void *ws,
+int launch_worker_m(const void *g, const Momentum &mm, float *xs, int64_t n, uint32_t *bits, float *scale, void *ws,
                     cudaStream_t st)
 {
-    return mm.dense ? launch_worker<GT, false>(g, mm, e, n, bits, scale, ws, st)
-                    : launch_worker<GT, true>(g, mm, e, n, bits, scale, ws, st);
+    if (mm.dense)
+        return aligned32(xs) && aligned32(mm.dense) ? launch_worker<GT, false, true>(g, mm, xs, n, bits, scale, ws, st)
+                                                    : launch_worker<GT, false, false>(g, mm, xs, n, bits, scale, ws, st);
+    return aligned32(xs) ? launch_worker<GT, true, true>(g, mm, xs, n, bits, scale, ws, st)
+                         : launch_worker<GT, true, false>(g, mm, xs, n, bits, scale, ws, st);
 }
 
 template <int PT>
@@ -504,8 +557,10 @@ int launch_update(const uint32_t *bits, const float *scales, int64_t S, int64_t 
                   float *m, const float *v, void *plp, void *ws, cudaStream_t st)
 {
     const int64_t threads = n >> 3;
-    launch_k(k_onebit_update<PT>, (int)((threads + kThreads - 1) / kThreads), kThreads, st, false, bits, scales, S,
-             n, numel, p, m, v, plp, (const StepScalars *)step_scalars(ws));
+    const bool w32 = (!p || aligned32(p)) && (!v || aligned32(v)) && (!m || aligned32(m));
+    auto kern = w32 ? k_onebit_update<PT, true> : k_onebit_update<PT, false>;
+    launch_k(kern, (int)((threads + kThreads - 1) / kThreads), kThreads, st, false, bits, scales, S, n, numel, p, m,
+             v, plp, (const StepScalars *)step_scalars(ws));
     return check_launch("zero_onebit_update");
 }
 
@@ -515,7 +570,7 @@ int launch_update(const uint32_t *bits, const float *scales, int64_t S, int64_t 
 using namespace zpml;
 
 extern "C" int zero_onebit_worker(const void *grad, int32_t gdtype, const float *m, const uint32_t *m_bits,
-                                  const float *m_scales, int64_t S, float *e_w, int64_t n, uint32_t *bits,
+                                  const float *m_scales, int64_t S, float *x_w, int64_t n, uint32_t *bits,
                                   float *scale, const zero_hparams_t *hp, int64_t freeze_step,
                                   zero_state_t *d_state, void *ws, size_t ws_bytes, void *stream)
 {
@@ -529,11 +584,11 @@ extern "C" int zero_onebit_worker(const void *grad, int32_t gdtype, const float 
         return ZERO_EALIGN;
     Momentum mm = {m, m_bits, m_scales, S};
     if (n > 0) {
-        if (!grad || !e_w || !bits || !scale)
+        if (!grad || !x_w || !bits || !scale)
             return ZERO_EINVAL;
-        if (!aligned16(grad) || !aligned16(e_w) || !aligned4(bits) || !aligned4(scale))
+        if (!aligned16(grad) || !aligned16(x_w) || !aligned4(bits) || !aligned4(scale))
             return ZERO_EALIGN;
-        if (!device_ptr(grad) || !device_ptr(e_w) || !device_ptr(bits) || !device_ptr(scale))
+        if (!device_ptr(grad) || !device_ptr(x_w) || !device_ptr(bits) || !device_ptr(scale))
             return ZERO_EINVAL;
         if (m) {
             if (!aligned16(m))
@@ -566,14 +621,14 @@ extern "C" int zero_onebit_worker(const void *grad, int32_t gdtype, const float 
     if ((rc = check_launch("zero_onebit_worker (decision)")) != ZERO_OK || n == 0)
         return rc;
     switch (gdtype) {
-    case ZERO_F16: return launch_worker_m<ZERO_F16>(grad, mm, e_w, n, bits, scale, ws, st);
-    case ZERO_BF16: return launch_worker_m<ZERO_BF16>(grad, mm, e_w, n, bits, scale, ws, st);
-    default: return launch_worker_m<ZERO_F32>(grad, mm, e_w, n, bits, scale, ws, st);
+    case ZERO_F16: return launch_worker_m<ZERO_F16>(grad, mm, x_w, n, bits, scale, ws, st);
+    case ZERO_BF16: return launch_worker_m<ZERO_BF16>(grad, mm, x_w, n, bits, scale, ws, st);
+    default: return launch_worker_m<ZERO_F32>(grad, mm, x_w, n, bits, scale, ws, st);
     }
 }
 
 extern "C" int zero_onebit_server(const uint32_t *const *worker_bits, const float *worker_scales, int32_t nd,
-                                  int64_t S, float *e_s, uint32_t *bits, float *scale, void *ws, size_t ws_bytes,
+                                  int64_t S, float *x_s, uint32_t *bits, float *scale, void *ws, size_t ws_bytes,
                                   void *stream)
 {
     if (nd < 1 || S < 0 || !worker_bits || !worker_scales)
@@ -592,11 +647,11 @@ extern "C" int zero_onebit_server(const uint32_t *const *worker_bits, const floa
         !device_ptr(worker_bits[nd - 1]))
         return !aligned4(worker_scales) ? ZERO_EALIGN : ZERO_EINVAL;
     if (S > 0) {
-        if (!e_s || !bits || !scale)
+        if (!x_s || !bits || !scale)
             return ZERO_EINVAL;
-        if (!aligned16(e_s) || !aligned4(bits) || !aligned4(scale))
+        if (!aligned16(x_s) || !aligned4(bits) || !aligned4(scale))
             return ZERO_EALIGN;
-        if (!device_ptr(e_s) || !device_ptr(bits) || !device_ptr(scale))
+        if (!device_ptr(x_s) || !device_ptr(bits) || !device_ptr(scale))
             return ZERO_EINVAL;
     }
     // up to kArgWorkers pointers go as a launch argument; more, as a table
@@ -630,6 +685,7 @@ extern "C" int zero_onebit_server(const uint32_t *const *worker_bits, const floa
     if (grid < 1)
         grid = 1;
     const bool pow2 = (nd & (nd - 1)) == 0;
+    const bool w32 = aligned32(x_s);
     const float inv_nd = pow2 ? 1.0f / (float)nd : 0.0f;  // exact: nd <= 2^12
     const size_t smem = server_smem_bytes(nd);
     cudaLaunchConfig_t cfg = {};
@@ -643,20 +699,18 @@ extern "C" int zero_onebit_server(const uint32_t *const *worker_bits, const floa
         WorkerPtrs wp = {};
         for (int32_t k = 0; k < nd; ++k)
             wp.p[k] = worker_bits[k];
-        auto kern = pow2 ? k_onebit_server_args<true> : k_onebit_server_args<false>;
+        auto kern = pow2 ? (w32 ? k_onebit_server_args<true, true> : k_onebit_server_args<true, false>)
+                         : (w32 ? k_onebit_server_args<false, true> : k_onebit_server_args<false, false>);
         cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-        cudaLaunchKernelEx(&cfg, kern, wp, worker_scales, (int)nd, inv_nd, e_s, S, sc, partials, hdr, scale);
+        cudaLaunchKernelEx(&cfg, kern, wp, worker_scales, (int)nd, inv_nd, x_s, S, sc, partials, hdr, scale, bits);
     } else {
-        auto kern = pow2 ? k_onebit_server<true> : k_onebit_server<false>;
+        auto kern = pow2 ? (w32 ? k_onebit_server<true, true> : k_onebit_server<true, false>)
+                         : (w32 ? k_onebit_server<false, true> : k_onebit_server<false, false>);
         cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-        cudaLaunchKernelEx(&cfg, kern, (const uint32_t *const *)(w + kWsTable), worker_scales, (int)nd, inv_nd, e_s,
-                           S, sc, partials, hdr, scale);
+        cudaLaunchKernelEx(&cfg, kern, (const uint32_t *const *)(w + kWsTable), worker_scales, (int)nd, inv_nd, x_s,
+                           S, sc, partials, hdr, scale, bits);
     }
-    if ((rc = check_launch("zero_onebit_server (first pass)")) != ZERO_OK)
-        return rc;
-    launch_k(k_onebit_sign, (int)((nv + kThreads - 1) / kThreads), kThreads, st, true, e_s, S, (const float *)scale,
-             bits, sc);
-    return check_launch("zero_onebit_server (signs)");
+    return check_launch("zero_onebit_server");
 }
 
 extern "C" int zero_onebit_update(const uint32_t *bits, const float *server_scales, int32_t nd, int64_t S,
