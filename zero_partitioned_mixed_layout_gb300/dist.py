@@ -9,6 +9,12 @@ updates one partition of the optimizer state; the pages' ZeRO keeps the data
 parallel communication volume, and this 16-byte sum is all the update step
 itself adds).  On one GPU the same sum is formed by the `accumulate` flag of
 zero_grad_norm_overflow instead.
+
+1-bit Adam's compression stage adds two exchanges of signs and scales: after
+zero_onebit_worker, chunk j of every worker's signs (and every worker's
+scale) to rank j, an all-to-all; after zero_onebit_server, every rank's
+chunk signs and scale to every worker, an all-gather.  They move the 1-bit
+messages only: the arithmetic stays in the library's calls on each rank.
 """
 from __future__ import annotations
 
@@ -22,3 +28,50 @@ def exchange_partials(state, group=None) -> None:
         raise ValueError("state must be the uint8 bytes of a zero_state_t")
     head = state[:16].view(torch.float64)
     dist.all_reduce(head, op=dist.ReduceOp.SUM, group=group)
+
+
+def _check_words(bits, what):
+    import torch
+    if bits.dtype != torch.int32 or bits.dim() != 1:
+        raise ValueError(f"{what} must be a 1-D int32 tensor of sign words")
+
+
+def onebit_exchange_worker_signs(bits, scale, group=None):
+    """The worker-side exchange of a 1-bit Adam step (an all-to-all).
+    bits: this rank's signs, int32[n/32] with n = Nd*S (chunk j, words
+    [j*S/32, (j+1)*S/32), goes to rank j); scale: its scale, float32[1].
+    Returns (chunk_bits, worker_scales): the Nd workers' signs on this
+    rank's chunk, int32[Nd, S/32] in rank order (row i is the worker_bits[i]
+    of zero_onebit_server), and every worker's scale, float32[Nd]."""
+    import torch
+    import torch.distributed as dist
+    _check_words(bits, "bits")
+    nd = dist.get_world_size(group)
+    if bits.numel() % nd != 0:
+        raise ValueError("the sign words must split into one equal chunk per rank")
+    if scale.dtype != torch.float32 or scale.numel() != 1:
+        raise ValueError("scale must be one float32")
+    chunk_bits = torch.empty_like(bits)
+    dist.all_to_all_single(chunk_bits, bits.contiguous(), group=group)
+    worker_scales = torch.empty(nd, dtype=torch.float32, device=scale.device)
+    dist.all_gather_into_tensor(worker_scales, scale.reshape(1).contiguous(), group=group)
+    return chunk_bits.view(nd, -1), worker_scales
+
+
+def onebit_exchange_server_signs(chunk_bits, scale, group=None):
+    """The server-side exchange of a 1-bit Adam step (an all-gather).
+    chunk_bits: this rank's server signs, int32[S/32]; scale: float32[1].
+    Returns (bits, server_scales): every rank's chunk signs in rank order,
+    int32[Nd*S/32], and every rank's scale, float32[Nd] -- the bits and
+    server_scales of zero_onebit_update."""
+    import torch
+    import torch.distributed as dist
+    _check_words(chunk_bits, "chunk_bits")
+    if scale.dtype != torch.float32 or scale.numel() != 1:
+        raise ValueError("scale must be one float32")
+    nd = dist.get_world_size(group)
+    bits = torch.empty(nd * chunk_bits.numel(), dtype=torch.int32, device=chunk_bits.device)
+    dist.all_gather_into_tensor(bits, chunk_bits.contiguous(), group=group)
+    server_scales = torch.empty(nd, dtype=torch.float32, device=scale.device)
+    dist.all_gather_into_tensor(server_scales, scale.reshape(1).contiguous(), group=group)
+    return bits, server_scales
