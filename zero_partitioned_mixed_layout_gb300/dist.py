@@ -10,6 +10,14 @@ parallel communication volume, and this 16-byte sum is all the update step
 itself adds).  On one GPU the same sum is formed by the `accumulate` flag of
 zero_grad_norm_overflow instead.
 
+ZeRO stage 2 and stage 3 add one exchange each.  Stage 2 reduces the
+gradient replicas to their owners: here an all-to-all hands every rank all
+replicas of its own shard and zero_reduce_grads forms their mean in rank
+order (fused with pass 1) -- the traffic of a reduce-scatter, with a
+summation order that does not depend on the collective's algorithm.  Stage 3
+gathers the parameter shards before a layer runs: an all-gather, then
+zero_gather_params cuts the tensors out of the shards.
+
 1-bit Adam's compression stage adds two exchanges of signs and scales: after
 zero_onebit_worker, chunk j of every worker's signs (and every worker's
 scale) to rank j, an all-to-all; after zero_onebit_server, every rank's
@@ -28,6 +36,42 @@ def exchange_partials(state, group=None) -> None:
         raise ValueError("state must be the uint8 bytes of a zero_state_t")
     head = state[:16].view(torch.float64)
     dist.all_reduce(head, op=dist.ReduceOp.SUM, group=group)
+
+
+def _flat(t, what):
+    if t.dim() != 1:
+        raise ValueError(f"{what} must be a 1-D tensor")
+    return t.contiguous()
+
+
+def stage2_exchange_grads(grad, group=None):
+    """ZeRO stage 2's gradient exchange (an all-to-all).  grad: this rank's
+    gradient over the whole padded flat buffer, n = Nd*S elements (shard j,
+    [j*S, (j+1)*S), goes to rank j).  Returns [Nd, S] of grad's type: every
+    rank's gradient on this rank's shard, in rank order -- the replicas of
+    zero_reduce_grads (one row each)."""
+    import torch
+    import torch.distributed as dist
+    grad = _flat(grad, "grad")
+    nd = dist.get_world_size(group)
+    if grad.numel() % nd != 0:
+        raise ValueError("the gradient must split into one equal shard per rank")
+    out = torch.empty_like(grad)
+    dist.all_to_all_single(out, grad, group=group)
+    return out.view(nd, -1)
+
+
+def stage3_gather_shards(shard, group=None):
+    """ZeRO stage 3's parameter exchange (an all-gather).  shard: this
+    rank's S elements.  Returns [Nd, S]: every rank's shard in rank order --
+    the shards of zero_gather_params (one row each)."""
+    import torch
+    import torch.distributed as dist
+    shard = _flat(shard, "shard")
+    nd = dist.get_world_size(group)
+    out = torch.empty(nd * shard.numel(), dtype=shard.dtype, device=shard.device)
+    dist.all_gather_into_tensor(out, shard, group=group)
+    return out.view(nd, -1)
 
 
 def _check_words(bits, what):
