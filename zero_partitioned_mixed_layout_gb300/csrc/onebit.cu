@@ -163,12 +163,14 @@ struct Momentum {
     int64_t chunk;         // S
 };
 
+// ci: the chunk of group i, (8i) / S, computed by the caller ahead of its
+// loads (so that the division does not sit between them).
 template <bool kCompressed, bool W32>
-__device__ __forceinline__ void load_momentum(const Momentum &mm, int64_t i, float *f)
+__device__ __forceinline__ void load_momentum(const Momentum &mm, int64_t i, int64_t ci, float *f)
 {
     if constexpr (kCompressed) {
         const uint32_t byte = (__ldg(mm.bits + (i >> 2)) >> (8 * (i & 3))) & 0xFFu;
-        const float sc = __ldg(mm.scales + (8 * i) / mm.chunk);
+        const float sc = __ldg(mm.scales + ci);
 #pragma unroll
         for (int k = 0; k < 8; ++k)
             f[k] = ((byte >> k) & 1u) ? sc : -sc;
@@ -202,6 +204,7 @@ __global__ void __launch_bounds__(kThreads) k_onebit_worker(const void *g, Momen
     // shuffles of the sign words see every lane
     for (int64_t i0 = (int64_t)blockIdx.x * kThreads + (threadIdx.x & ~31); i0 < nv; i0 += stride) {
         const int64_t i = i0 + (threadIdx.x & 31);
+        const int64_t ci = kCompressed ? (8 * i) / mm.chunk : 0;
         uint32_t byte = 0;
         if (i < nv) {
             uint4 w[W];
@@ -210,7 +213,7 @@ __global__ void __launch_bounds__(kThreads) k_onebit_worker(const void *g, Momen
                 w[q] = __ldcs(gv + i * W + q);
             float gf[8], mf[8], x[8];
             Elem<GT>::to_float(w, gf);
-            load_momentum<kCompressed, W32>(mm, i, mf);
+            load_momentum<kCompressed, W32>(mm, i, ci, mf);
             ld8<W32>(xs + 8 * i, x);
 #pragma unroll
             for (int k = 0; k < 8; ++k) {
