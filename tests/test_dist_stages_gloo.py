@@ -92,3 +92,20 @@ def test_stage2_and_stage3_exchanges(world, tmp_path):
         got = np.load(os.path.join(tmp_path, f"rank{r}.npz"))
         assert got["mean"].tobytes() == whole_mean[r * S:(r + 1) * S].tobytes(), f"rank {r}: stage-2 mean"
         assert got["tensors"].tobytes() == want_tensors.tobytes(), f"rank {r}: stage-3 tensors"
+
+
+def test_exchanges_refuse_bad_arguments():
+    """Argument checks come before any collective (no process group here)."""
+    import sys
+    sys.path.insert(0, ROOT)
+    from zero_partitioned_mixed_layout_gb300 import dist as zdist
+    with pytest.raises(ValueError):
+        zdist.stage2_exchange_grads(torch.zeros(4, 8, dtype=torch.float16))
+    with pytest.raises(ValueError):
+        zdist.stage3_gather_shards(torch.zeros(2, 2))
+    with pytest.raises(ValueError):
+        zdist.onebit_exchange_worker_signs(torch.zeros(64), torch.zeros(1))
+    with pytest.raises(ValueError):
+        zdist.onebit_exchange_server_signs(torch.zeros(8, dtype=torch.int64), torch.zeros(1))
+    with pytest.raises(ValueError):
+        zdist.exchange_partials(torch.zeros(8, dtype=torch.uint8))
