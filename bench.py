@@ -155,10 +155,11 @@ def dist_env():
 
 # ------------------------------------------------------------------ oracle arm
 
-def oracle_run(n_sample: int, steps: int, warmup: int):
+def oracle_run(n_sample: int, steps: int, warmup: int, keep: bool = False):
     """The oracle as it stands (single-threaded scalar C) on the first
     n_sample elements of the workload's shard: `warmup` untimed and `steps`
-    timed full steps (norm, decision, update)."""
+    timed full steps (norm, decision, update).  Returns (params/s, seconds,
+    the final (master, m, v, p_lp) arrays if `keep`, else None)."""
     import numpy as np
 
     import oracle
@@ -178,7 +179,51 @@ def oracle_run(n_sample: int, steps: int, warmup: int):
     for _ in range(steps):
         oracle.adam_step([g], "f16", [p], [m], [v], [plp], "f16", hp, sc)
     dt = time.perf_counter() - t0
-    return n_sample * steps / dt, dt
+    return n_sample * steps / dt, dt, ((p, m, v, plp) if keep else None)
+
+
+def parity_vs_oracle(dev, n_sample: int, steps: int, final) -> dict:
+    """The library on the oracle run's inputs (the same seeded arrays and
+    hyper-parameters, the same number of steps), outside the timed region:
+    its final state against the oracle's, element by element.  ulp distances
+    of the fp32 arrays are counted on the ordered integer images of the
+    values."""
+    import numpy as np
+    import torch
+
+    import zero_partitioned_mixed_layout_gb300 as zp
+    import zero_synth as zs
+    w = zs.WORKLOADS[WORKLOAD]
+    p = torch.from_numpy(zs.host_master(n_sample, 0)).to(dev)
+    g = torch.from_numpy(zs.host_grad(n_sample, 0, 0, w["loss_scale"], "f16")).to(dev)
+    m, v = torch.zeros_like(p), torch.zeros_like(p)
+    plp = torch.zeros(n_sample, dtype=torch.float16, device=dev)
+    state, ws = zp.new_state(w["loss_scale"], dev), zp.new_workspace(1, n_sample, dev)
+    for _ in range(steps):
+        zp.zero_step(g, p, m, v, plp, zp.HParams(), state, ws)
+    torch.cuda.synchronize(dev)
+
+    def ordered(a):
+        i = a.view(np.int32).astype(np.int64)
+        return np.where(i < 0, -(i & 0x7FFFFFFF), i)
+
+    out = {"elements": n_sample, "steps": steps}
+    hist = {"0": 0, "1": 0, "2-4": 0, ">4": 0}
+    for name, got, want in (("master", p, final[0]), ("m", m, final[1]), ("v", v, final[2])):
+        a = got.cpu().numpy()
+        d = np.abs(ordered(a) - ordered(want))
+        out[f"{name}_bitwise_equal"] = bool(a.tobytes() == want.tobytes())
+        err = np.abs(a.astype(np.float64) - want.astype(np.float64))
+        out[f"{name}_max_abs_err"] = float(err.max())
+        out[f"{name}_max_rel_err"] = float((err / np.maximum(np.abs(want.astype(np.float64)), 1e-300)).max())
+        hist["0"] += int((d == 0).sum())
+        hist["1"] += int((d == 1).sum())
+        hist["2-4"] += int(((d >= 2) & (d <= 4)).sum())
+        hist[">4"] += int((d > 4).sum())
+    out["fp32_ulp_histogram"] = hist
+    out["p_lp_bitwise_equal"] = bool(plp.cpu().view(torch.int16).numpy().view(np.uint16).tobytes()
+                                     == final[3].tobytes())
+    return out
 
 
 def _oracle_worker(k, n_sample, steps, warmup, barrier, out):
@@ -239,7 +284,7 @@ def run_reference(args):
     w = zs.WORKLOADS[WORKLOAD]
     S = oracle.partition_layout(w["numel"](), w["nd"], w["align"]).shard_numel
     n_sample = 1 << 24
-    one, one_dt = oracle_run(n_sample, args.steps, args.warmup)
+    one, one_dt, _ = oracle_run(n_sample, args.steps, args.warmup)
     value, dt, procs = oracle_run_all_cores(n_sample, args.steps, args.warmup)
     sample = (f"{procs} processes (one per host core), each on its own {n_sample} params of the "
               f"{WORKLOAD} rank-0 shard's inputs, {args.steps} timed steps after {args.warmup} "
@@ -539,7 +584,7 @@ def run_ours(args):
         # about 10-20 s of CPU work in all: 10 full steps of 2^24 params on
         # one core, then on every core at once
         n_sample, c_steps = 1 << 24, 10
-        cv, cdt = oracle_run(n_sample, c_steps, 1)
+        cv, cdt, final = oracle_run(n_sample, c_steps, 1, keep=True)
         av, adt, procs = oracle_run_all_cores(n_sample, c_steps, 1)
         cpu = {"value": av, "unit": UNIT, "cores": procs, "kind": "oracle",
                "sample": f"{procs} processes (one per host core), each {c_steps} full steps on its own "
@@ -547,7 +592,9 @@ def run_ours(args):
                          f"{adt:.1f} s wall ({procs * adt:.0f} s of CPU); the oracle as it stands "
                          f"(single-threaded scalar C)",
                "single_core": {"value": cv, "unit": UNIT, "cores": 1, "seconds": cdt,
-                               "sample": f"first {n_sample} params of the shard, {c_steps} full steps"}}
+                               "sample": f"first {n_sample} params of the shard, {c_steps} full steps"},
+               # the library on the single-core run's inputs, against its result
+               "parity": parity_vs_oracle(dev, n_sample, c_steps + 1, final)}
     default = args.workload == WORKLOAD
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
