@@ -42,6 +42,8 @@ MUTANTS = [
     ("mean by reciprocal", "const float mean = a / count;", "const float mean = a * (1.0f / count);"),
     ("mean over one replica fewer", "const float count = (float)n_bufs;",
      "const float count = (float)(n_bufs > 1 ? n_bufs - 1 : 1);"),
+    ("sampled update reads the gradient at the sample's position",
+     "adam_element(load_elem(g, gdtype, idx[j]), &p[j]", "adam_element(load_elem(g, gdtype, j), &p[j]"),
     ("reduction reversed", "        float a = load_elem(bufs[0], dtype, i);\n        for (int32_t k = 1; k < n_bufs; ++k)\n            a = a + load_elem(bufs[k], dtype, i);",
      "        float a = load_elem(bufs[n_bufs - 1], dtype, i);\n        for (int32_t k = n_bufs - 2; k >= 0; --k)\n            a = a + load_elem(bufs[k], dtype, i);"),
 ]
@@ -64,6 +66,7 @@ PINS = [
     pins.test_scale_growth_after_window,
     pins.test_accumulate_order_and_exactness,
     pins.test_reduce_mean_closed_forms,
+    lambda: pins.test_adam_apply_sampled_equals_whole_update_gathered("f16", "f16"),
 ]
 
 

@@ -441,3 +441,66 @@ def test_reduce_mean_closed_forms():
     y[10] = np.inf
     out = oracle.reduce_mean([x, y, x], "f16", "f16").view(np.float16)
     assert np.isinf(out[10]) and np.isfinite(out[11])
+
+
+# ---------------------------------------------------------------- helpers the GPU tests use
+
+@pytest.mark.parametrize("gdtype,pdtype", [("f16", "f16"), ("bf16", "bf16"), ("f32", "f16")])
+def test_adam_apply_sampled_equals_whole_update_gathered(gdtype, pdtype):
+    """The sampled update (state arrays holding only the sampled elements)
+    against the whole-array update gathered at the samples: equal bit for
+    bit over three steps, for samples that include both ends, repeats and an
+    unsorted order."""
+    rng = np.random.default_rng(21)
+    n = 10_007
+    scale = 1.0 if gdtype == "bf16" else 1024.0
+    idx = np.concatenate([[0, n - 1, 5, 5], rng.integers(0, n, 500)]).astype(np.int64)
+    rng.shuffle(idx)
+    p = zs.host_master(n, 3)
+    m = np.zeros(n, np.float32)
+    v = np.zeros(n, np.float32)
+    plp = np.zeros(n, np.uint16)
+    ps, ms, vs, plps = p[idx].copy(), m[idx].copy(), v[idx].copy(), np.zeros(idx.size, np.uint16)
+    hp = oracle.HParams(max_norm=0.05)
+    sc = oracle.Scaler(loss_scale=scale)
+    for k in range(3):
+        g = zs.host_grad(n, 3, k, scale, gdtype)
+        sumsq, bad = oracle.norm_overflow([g], gdtype, scale)
+        st = oracle.decide(hp, sc, sumsq, bad)
+        oracle.adam_apply(g, gdtype, p, m, v, plp, pdtype, st)
+        oracle.adam_apply_sampled(g, gdtype, idx, ps, ms, vs, plps, pdtype, st)
+        for name, whole, sampled in (("p", p, ps), ("m", m, ms), ("v", v, vs), ("p_lp", plp, plps)):
+            assert whole[idx].tobytes() == sampled.tobytes(), f"{name} step {k}"
+    assert sc.step == 3 and st.scalars["clip"] < 1.0
+
+
+def test_with_clip_changes_only_the_clip_coefficient():
+    """with_clip(step, c) is the step with c as its binary32 clip
+    coefficient and nothing else changed: with c = 1/2 it updates exactly as
+    the unclipped step does on gradients halved beforehand (both products
+    are exact for these normal values), and with the step's own coefficient
+    it is the same step."""
+    rng = np.random.default_rng(22)
+    n = 4096
+    g = (rng.standard_normal(n) * 1e-3).astype(np.float32)
+    hp, sc = oracle.HParams(), oracle.Scaler(loss_scale=1.0)
+    st = oracle.decide(hp, sc, float(np.sum(g.astype(np.float64) ** 2)), 0)
+    assert st.scalars["clip"] == 1.0
+    half = oracle.with_clip(st, 0.5)
+    assert half.scalars["clip"] == 0.5 and half.skip == st.skip and half.norm == st.norm
+    assert {k: x for k, x in half.scalars.items() if k != "clip"} == \
+           {k: x for k, x in st.scalars.items() if k != "clip"}
+    p0 = zs.host_master(n, 4)
+    runs = []
+    for step, grad in ((half, g), (st, g * np.float32(0.5)), (oracle.with_clip(st, 1.0), g * np.float32(0.5))):
+        p, m, v = p0.copy(), np.zeros(n, np.float32), np.zeros(n, np.float32)
+        oracle.adam_apply(grad, "f32", p, m, v, None, "f16", step)
+        runs.append((p, m, v))
+    for a, b in zip(runs[0], runs[1]):
+        assert a.tobytes() == b.tobytes()
+    for a, b in zip(runs[1], runs[2]):
+        assert a.tobytes() == b.tobytes()
+    # and it is not the unclipped update
+    p, m, v = p0.copy(), np.zeros(n, np.float32), np.zeros(n, np.float32)
+    oracle.adam_apply(g, "f32", p, m, v, None, "f16", st)
+    assert m.tobytes() != runs[0][1].tobytes()
