@@ -16,3 +16,15 @@ def pytest_configure(config):
 def cuda_available():
     import torch
     return torch.cuda.is_available()
+
+
+def pytest_terminal_summary(terminalreporter):
+    """The parity record of the GPU tests: steps compared against the oracle,
+    and those whose binary32 clip coefficient differed from the oracle's (from
+    such a step on the elements were held to the tolerance, not to bit
+    identity)."""
+    gc = sys.modules.get("gpu_common")
+    if gc is not None and gc.Parity.steps:
+        terminalreporter.write_line(
+            f"parity: {gc.Parity.steps} applied steps compared with the oracle; "
+            f"clip coefficient differed in {gc.Parity.clip_differs}")

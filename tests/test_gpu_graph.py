@@ -12,7 +12,7 @@ import zero_synth as zs
 torch = pytest.importorskip("torch")
 pytestmark = pytest.mark.gpu
 
-from gpu_common import TORCH, assert_f32, assert_lp, hp_pair, oracle_step, to_dev, to_host  # noqa: E402
+from gpu_common import bound_of, TORCH, assert_f32, assert_lp, assert_lp_copy, hp_pair, oracle_step, to_dev, to_host  # noqa: E402
 
 
 @pytest.fixture(scope="module")
@@ -76,11 +76,11 @@ def test_flat_step_graph_replays_match_oracle(zp, gdtype, pdtype):
         gst = zp.parse_state(state)
         st = oracle_step([g], gdtype, [p], [m], [v], [plp], pdtype, ohp, sc, gst)
         skipped += st.skip
-        assert_f32(to_host(dp), p, f"master step {k}")
-        assert_f32(to_host(dm), m, f"m step {k}")
-        assert_f32(to_host(dv), v, f"v step {k}")
-        assert np.array_equal(to_host(dlp), plp), f"p_lp step {k}"
-        assert_lp(to_host(dlp), p, pdtype, f"p_lp step {k}")
+        assert_f32(to_host(dp), p, f"master step {k}", st.exact, bound_of(st, "p", 0))
+        assert_f32(to_host(dm), m, f"m step {k}", st.exact, bound_of(st, "m", 0))
+        assert_f32(to_host(dv), v, f"v step {k}", st.exact, bound_of(st, "v", 0))
+        assert_lp_copy(to_host(dlp), plp, f"p_lp step {k}", st.exact)
+        assert_lp(to_host(dlp), p, pdtype, f"p_lp step {k}", st.exact, bound_of(st, "p", 0))
     st = zp.parse_state(state)
     assert skipped == 1 and st["step"] == 5 and st["skipped"] == 1
 
@@ -301,12 +301,12 @@ def test_prepared_list_step_graph_replays_match_oracle(zp):
         graph.replay()
         torch.cuda.synchronize()
         gst = zp.parse_state(state)
-        oracle_step(hg, gdtype, host["p"], host["m"], host["v"], host["lp"], pdtype, ohp, sc, gst)
+        st = oracle_step(hg, gdtype, host["p"], host["m"], host["v"], host["lp"], pdtype, ohp, sc, gst)
         for i in range(len(sizes)):
-            assert_f32(to_host(d["p"][i]), host["p"][i], f"master {i} step {k}")
-            assert_f32(to_host(d["m"][i]), host["m"][i], f"m {i} step {k}")
-            assert_f32(to_host(d["v"][i]), host["v"][i], f"v {i} step {k}")
-            assert np.array_equal(to_host(d["lp"][i]), host["lp"][i]), f"p_lp {i} step {k}"
+            assert_f32(to_host(d["p"][i]), host["p"][i], f"master {i} step {k}", st.exact, bound_of(st, "p", i))
+            assert_f32(to_host(d["m"][i]), host["m"][i], f"m {i} step {k}", st.exact, bound_of(st, "m", i))
+            assert_f32(to_host(d["v"][i]), host["v"][i], f"v {i} step {k}", st.exact, bound_of(st, "v", i))
+            assert_lp_copy(to_host(d["lp"][i]), host["lp"][i], f"p_lp {i} step {k}", st.exact)
     assert zp.parse_state(state)["step"] == 3
 
 

@@ -11,7 +11,7 @@ import zero_synth as zs
 torch = pytest.importorskip("torch")
 pytestmark = pytest.mark.gpu
 
-from gpu_common import assert_f32, assert_lp, hp_pair, oracle_step, to_host  # noqa: E402
+from gpu_common import bound_of, assert_f32, assert_lp, assert_lp_copy, hp_pair, oracle_step, to_host  # noqa: E402
 
 
 @pytest.fixture(scope="module")
@@ -54,12 +54,12 @@ def test_offload_step_against_oracle(zp, max_norm):
         d_lp.copy_(h_lp)
         d_state.copy_(h_state)
         gst = zp.parse_state(h_state)
-        oracle_step([g], "f16", [rp], [rm], [rv], [rlp], "f16", ohp, sc_o, gst)
-        assert_f32(p.numpy(), rp, f"master step {k}")
-        assert_f32(m.numpy(), rm, f"m step {k}")
-        assert_f32(v.numpy(), rv, f"v step {k}")
-        assert np.array_equal(to_host(d_lp), rlp), f"fp16 params step {k}"
-        assert_lp(to_host(d_lp), rp, "f16", f"fp16 params step {k}")
+        ost = oracle_step([g], "f16", [rp], [rm], [rv], [rlp], "f16", ohp, sc_o, gst)
+        assert_f32(p.numpy(), rp, f"master step {k}", ost.exact, bound_of(ost, "p", 0))
+        assert_f32(m.numpy(), rm, f"m step {k}", ost.exact, bound_of(ost, "m", 0))
+        assert_f32(v.numpy(), rv, f"v step {k}", ost.exact, bound_of(ost, "v", 0))
+        assert_lp_copy(to_host(d_lp), rlp, f"fp16 params step {k}", ost.exact)
+        assert_lp(to_host(d_lp), rp, "f16", f"fp16 params step {k}", ost.exact, bound_of(ost, "p", 0))
     st = zp.parse_state(d_state)
     assert st["step"] == 2 and st["skipped"] == 1 and st["loss_scale"] == scale / 2
 

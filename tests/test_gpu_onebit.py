@@ -1,8 +1,11 @@
 """1-bit Adam's compression stage on one GPU against the oracle: the Nd
 workers, the Nd servers and the update of one compression-stage step, each
-worker and server as the rank it would be (its own state and workspace), bit
-for bit once the GPU's scales are handed to the oracle (the binary64 norm is
-summed in another order: the scales themselves agree within 2^-22); and the
+worker and server as the rank it would be (its own state and workspace).
+Two comparisons: the oracle running on its own for several steps, every
+value within bounds derived from the two sides' norm summation orders
+(test_onebit_free_running_against_oracle); and, for the element arithmetic
+itself, the oracle handed the GPU's scales, bit for bit (the binary64 norm
+is summed in another order: the scales agree within 2^-22).  Also the
 benchmark's full-size step on sampled elements plus the norm property.
 
 The GPU holds each error in deferred form (the compression's input x and
@@ -195,6 +198,167 @@ def test_onebit_three_steps_with_clipping(zp):
         run_gpu_step(zp, d, nd, S, nd * S, zhp, T, "f16")
         res = check_step(zp, h, d, nd, S, nd * S, "f16", "f16", hp, sc, T)
         assert res.step.scalars["clip"] < 1.0
+
+
+U = 2.0 ** -24        # binary32 unit roundoff
+TINY = 2.0 ** -147    # a few subnormal ulps: the floor of any rounding allowance
+
+
+def _abs(a):
+    return np.abs(np.asarray(a, np.float64))
+
+
+@pytest.mark.parametrize("nd,S", [(4, 4096), (16, 2048)])
+@pytest.mark.parametrize("gdtype,pdtype,max_norm", [("f16", "f16", 0.0), ("bf16", "bf16", 0.05)])
+def test_onebit_free_running_against_oracle(zp, nd, S, gdtype, pdtype, max_norm):
+    """Three compression-stage steps on the GPU and in the oracle, each side
+    taking its own decision, norms and scales: nothing the GPU computes goes
+    into the oracle.  The two sides sum the norms in different orders, so
+    their binary32 scales may differ in the last places; through the error
+    feedback that difference reaches the next step's inputs, and where a
+    compressed value lies within it of zero its sign may come out the other
+    way.  Each step is held to the bounds this implies, derived from the
+    differences that enter the step (rounding allowances of a few ulps per
+    operation where an input differs):
+      * every compressed value x (worker) and y (server) within the bound
+        carried through its arithmetic from the entering differences;
+      * every scale within the difference of the inputs' L2 norms (the
+        triangle inequality) plus the summation-order allowance;
+      * a sign different from the oracle's only where |x| (|y|) is within
+        its bound;
+      * every error, momentum and master within what these imply.
+    (A server's scale is shared by its whole chunk, so a last-place
+    difference in it moves every element's momentum and master a little:
+    the bounds above, not a flat relative bar, are the measure.)  Sign
+    flips must stay rare."""
+    T, steps = 50, 3
+    scale = 1.0 if gdtype == "bf16" else 1024.0
+    h, d = setup(zp, nd, S, gdtype, pdtype, 900 + nd, scale, T)
+    n, numel = nd * S, nd * S - 11
+    hp, zhp = oracle.HParams(max_norm=max_norm), zp.HParams(max_norm=max_norm)
+    sc = oracle.Scaler(scale, T)
+    o = {"p": h["p"].copy(), "m": h["m"].copy(), "v": h["v"].copy(),
+         "ew": [e.copy() for e in h["ew"]], "es": [e.copy() for e in h["es"]],
+         "plp": h["plp"].copy() if pdtype else None}
+    # the GPU's state as it enters a step, on the host (errors explicit)
+    gprev = {"m": to_host(d["m"]), "p": to_host(d["p"]),
+             "ew": [deferred_error(to_host(d["ew"][i]), float(d["wscale"][i])) for i in range(nd)],
+             "es": [deferred_error(to_host(d["es"][j]), float(d["sscale"][j])) for j in range(nd)]}
+    for i in range(nd):  # the same start on both sides
+        assert gprev["ew"][i].tobytes() == o["ew"][i].tobytes()
+        assert gprev["es"][i].tobytes() == o["es"][i].tobytes()
+    touched = np.zeros(n, bool)
+    flips = 0
+    for step in range(steps):
+        for i in range(nd):
+            h["g"][i] = zs.host_grad(n, 950 + 10 * step + i, step, scale, gdtype)
+            d["g"][i] = to_dev(h["g"][i], gdtype)
+        o_in = {"m": o["m"].copy(), "p": o["p"].copy(), "ew": [e.copy() for e in o["ew"]],
+                "es": [e.copy() for e in o["es"]]}
+        run_gpu_step(zp, d, nd, S, numel, zhp, T, pdtype)
+        res = oracle.onebit_step(h["g"], gdtype, S, numel, o["p"], o["m"], o["v"], o["ew"], o["es"],
+                                 o["plp"], pdtype or "f16", hp, sc, T)
+        so = res.step.scalars
+        gst = zp.parse_state(d["state"][0])
+        assert not res.step.skip and not gst["last_skipped"] and gst["step"] == sc.step
+        assert abs(gst["last_norm"] - res.step.norm) <= 1e-6 * res.step.norm
+        clip_o, clip_g = np.float32(so["clip"]), np.float32(gst["last_clip"])
+        b1, omb1 = float(so["beta1"]), float(so["one_minus_beta1"])
+        dm_in = np.abs(gprev["m"].astype(np.float64) - o_in["m"])
+        # ---- workers
+        gw, ow = d["wscale"].cpu().numpy().astype(np.float64), np.array(res.worker_scales, np.float64)
+        wflip = []
+        for i in range(nd):
+            gu = _abs(oracle.from_lp(h["g"][i], gdtype) if gdtype != "f32" else h["g"][i]) * so["inv_scale"]
+            dg = gu * abs(float(clip_g) - float(clip_o))
+            if clip_g != clip_o:
+                dg += 2 * U * gu * max(float(clip_g), float(clip_o))
+            de_in = np.abs(gprev["ew"][i].astype(np.float64) - o_in["ew"][i])
+            x_o, x_g = res.worker_x[i], to_host(d["ew"][i])
+            diff_in = (dm_in > 0) | (de_in > 0) | (dg > 0)
+            bx = b1 * dm_in + omb1 * dg + de_in
+            bx = bx * (1 + 4 * U) + np.where(
+                diff_in, 8 * U * (b1 * _abs(o_in["m"]) + omb1 * gu * float(clip_o) + _abs(o_in["ew"][i])
+                                  + _abs(x_o)) + TINY, 0.0)
+            dx = np.abs(x_g.astype(np.float64) - x_o)
+            assert np.all(dx <= bx), f"step {step} worker {i}: x beyond its bound"
+            bs = np.sqrt(np.sum(bx * bx) / n) * (1 + U) + 2.0 ** -22 * ow[i]
+            assert abs(gw[i] - ow[i]) <= bs, f"step {step} worker {i}: scale {gw[i]!r} oracle {ow[i]!r}"
+            flip = (x_g < 0) != (x_o < 0)
+            assert np.all(_abs(x_o[flip]) <= bx[flip]), f"step {step} worker {i}: a sign flipped beyond its bound"
+            wflip.append(flip)
+            flips += int(flip.sum())
+            touched |= flip
+            e_g = deferred_error(x_g, gw[i])
+            ds = np.where(flip, gw[i] + ow[i], abs(gw[i] - ow[i]))
+            be = dx + ds + np.where((dx > 0) | (ds > 0), 4 * U * (_abs(o["ew"][i]) + _abs(x_o)) + TINY, 0.0)
+            assert np.all(np.abs(e_g.astype(np.float64) - o["ew"][i]) <= be), f"step {step} worker {i}: error"
+            gprev["ew"][i] = e_g
+        # ---- servers
+        gsv, osv = d["sscale"].cpu().numpy().astype(np.float64), np.array(res.server_scales, np.float64)
+        m_all = to_host(d["m"]).astype(np.float64)
+        for j in range(nd):
+            seg = slice(j * S, (j + 1) * S)
+            dc = sum(np.where(wflip[i][seg], gw[i] + ow[i], abs(gw[i] - ow[i])) for i in range(nd))
+            df_in = np.abs(gprev["es"][j].astype(np.float64) - o_in["es"][j])
+            y_o, y_g = res.server_x[j], to_host(d["es"][j])
+            diff_in = (dc > 0) | (df_in > 0)
+            by = dc / nd + df_in
+            # roundings: the rank-order sum (Nd - 1 additions, each within
+            # u of a partial sum <= the sum of the scales), the mean, y
+            by = by * (1 + 4 * U) + np.where(
+                diff_in, 4 * U * (ow.sum() + _abs(y_o) + _abs(o_in["es"][j])) + TINY, 0.0)
+            dy = np.abs(y_g.astype(np.float64) - y_o)
+            assert np.all(dy <= by), f"step {step} server {j}: y beyond its bound"
+            bt = np.sqrt(np.sum(by * by) / S) * (1 + U) + 2.0 ** -20 * osv[j]
+            assert abs(gsv[j] - osv[j]) <= bt, f"step {step} server {j}: scale {gsv[j]!r} oracle {osv[j]!r}"
+            flip = (y_g < 0) != (y_o < 0)
+            assert np.all(_abs(y_o[flip]) <= by[flip]), f"step {step} server {j}: a sign flipped beyond its bound"
+            flips += int(flip.sum())
+            touched[seg] |= flip
+            f_g = deferred_error(y_g, gsv[j])
+            dt = np.where(flip, gsv[j] + osv[j], abs(gsv[j] - osv[j]))
+            bf = dy + dt + np.where((dy > 0) | (dt > 0), 4 * U * (_abs(o["es"][j]) + _abs(y_o)) + TINY, 0.0)
+            assert np.all(np.abs(f_g.astype(np.float64) - o["es"][j]) <= bf), f"step {step} server {j}: error"
+            gprev["es"][j] = f_g
+            # ---- the synchronised momentum of this chunk: +-t exactly
+            assert np.all(np.abs(m_all[seg] - o["m"][seg]) <= dt), f"step {step} chunk {j}: momentum"
+        # ---- the update with the frozen variance
+        p_g = to_host(d["p"])
+        dm = np.abs(m_all - o["m"])[:numel]
+        dp_in = np.abs(gprev["p"].astype(np.float64) - o_in["p"])[:numel]
+        den = np.sqrt(_abs(o["v"][:numel])) * float(so["inv_sqrt_bc2"]) + float(so["eps"])
+        st_sz, lrwd = float(so["step_size"]), float(so["lr_wd"])
+        bp = dp_in * (1 + lrwd) + st_sz * dm / den * (1 + 4 * U)
+        bp += np.where((dp_in > 0) | (dm > 0), 8 * U * (_abs(o["p"][:numel]) + st_sz * _abs(o["m"][:numel]) / den
+                                                        + lrwd * _abs(o_in["p"][:numel])) + TINY, 0.0)
+        assert np.all(np.abs(p_g[:numel].astype(np.float64) - o["p"][:numel]) <= bp), f"step {step}: master"
+        if pdtype:
+            assert np.array_equal(to_host(d["plp"])[:numel], oracle.to_lp(p_g[:numel], pdtype)), \
+                f"step {step}: the low-precision copy is not the GPU master rounded"
+        gprev["m"], gprev["p"] = to_host(d["m"]), p_g
+    # flips are rare events at the edge of zero, not a systematic difference
+    assert flips <= max(4, n // 1000), flips
+    assert touched.sum() <= flips
+
+
+@pytest.mark.parametrize("nd,S", [(2, 4096)])
+def test_onebit_step_with_huge_momentum(zp, nd, S):
+    """Momentum values near 1e21 make the worker's and the server's squares
+    overflow binary32 (binary64 takes over for those vectors): the scales
+    stay finite and within the summation-order bound of the oracle's, and
+    the step is the oracle's bit for bit once handed the GPU's scales."""
+    T = 70
+    h, d = setup(zp, nd, S, "f16", "f16", 4321, 1024.0, T)
+    n = nd * S
+    rng = np.random.default_rng(11)
+    big = rng.choice(n, 40, replace=False)
+    h["m"][big] = (np.where(rng.random(40) < 0.5, -1.0, 1.0) * rng.uniform(1.0, 2.0, 40) * 1e21).astype(np.float32)
+    d["m"].copy_(torch.from_numpy(h["m"]))
+    run_gpu_step(zp, d, nd, S, n, zp.HParams(), T, "f16")
+    gw = d["wscale"].cpu().numpy()
+    assert np.all(np.isfinite(gw)) and np.all(gw > 1e18)
+    check_step(zp, h, d, nd, S, n, "f16", "f16", oracle.HParams(), oracle.Scaler(1024.0, T), T)
 
 
 @pytest.mark.parametrize("nd,S", [(1, 1024), (4, 8192), (16, 2048)])

@@ -11,7 +11,7 @@ import zero_synth as zs
 torch = pytest.importorskip("torch")
 pytestmark = pytest.mark.gpu
 
-from gpu_common import (TORCH, assert_f32, assert_lp, hp_pair, oracle_step, to_dev,  # noqa: E402
+from gpu_common import (bound_of, TORCH, assert_f32, assert_lp, assert_lp_copy, hp_pair, oracle_step, to_dev,  # noqa: E402
                         to_host)
 
 
@@ -69,12 +69,12 @@ def run_full(zp, n, gdtype, pdtype, steps, scale, max_norm=0.0, seed=0, inf_step
             skipped += 1
             for a, b in zip(after, before):
                 assert a.tobytes() == b.tobytes(), "a skipped step changed the state"
-        assert_f32(after[0], p, f"master step {k}")
-        assert_f32(after[1], m, f"m step {k}")
-        assert_f32(after[2], v, f"v step {k}")
-        assert np.array_equal(after[3], plp), f"p_lp step {k} differs from the oracle's copy"
+        assert_f32(after[0], p, f"master step {k}", st.exact, bound_of(st, "p", 0))
+        assert_f32(after[1], m, f"m step {k}", st.exact, bound_of(st, "m", 0))
+        assert_f32(after[2], v, f"v step {k}", st.exact, bound_of(st, "v", 0))
+        assert_lp_copy(after[3], plp, f"p_lp step {k} against the oracle's copy", st.exact)
         if skipped < k + 1:  # at least one step applied: p_lp is the rounded master
-            assert_lp(after[3], p, pdtype, f"p_lp step {k}")
+            assert_lp(after[3], p, pdtype, f"p_lp step {k}", st.exact, bound_of(st, "p", 0))
     return zp.parse_state(state), skipped
 
 
@@ -147,13 +147,13 @@ def sampled_run(zp, n, gdtype, pdtype, steps, scale, max_norm, micro=1, seed=0, 
         zp.zero_grad_norm_overflow(dg, state, ws)
         zp.zero_adam_step(dg, dp, dm, dv, dlp, ghp, state, ws)
         gst = zp.parse_state(state)
-        oracle_step([g_host], g_dtype, [p], [m], [v], [plp], pdtype, ohp, sc, gst,
-                    sampled_idx=idx)
+        st = oracle_step([g_host], g_dtype, [p], [m], [v], [plp], pdtype, ohp, sc, gst,
+                         sampled_idx=idx)
         del g_host
-        assert_f32(dp[didx].cpu().numpy(), p, f"master step {k}")
-        assert_f32(dm[didx].cpu().numpy(), m, f"m step {k}")
-        assert_f32(dv[didx].cpu().numpy(), v, f"v step {k}")
-        assert_lp(to_host(dlp[didx]), p, pdtype, f"p_lp step {k}")
+        assert_f32(dp[didx].cpu().numpy(), p, f"master step {k}", st.exact, bound_of(st, "p", 0))
+        assert_f32(dm[didx].cpu().numpy(), m, f"m step {k}", st.exact, bound_of(st, "m", 0))
+        assert_f32(dv[didx].cpu().numpy(), v, f"v step {k}", st.exact, bound_of(st, "v", 0))
+        assert_lp(to_host(dlp[didx]), p, pdtype, f"p_lp step {k}", st.exact, bound_of(st, "p", 0))
     return zp.parse_state(state)
 
 
@@ -222,8 +222,8 @@ def test_frag_10k_list(zp):
         zp.zero_grad_norm_overflow(dg, state, ws)
         zp.zero_adam_step(dg, dp, dm, dv, dl, ghp, state, ws)
         gst = zp.parse_state(state)
-        oracle_step(gl, "f16", hp_, hm, hv, hl, "f16", ohp, sc, gst)
-        assert_f32(torch.cat(dp).cpu().numpy(), np.concatenate(hp_), f"master step {k}")
-        assert_f32(torch.cat(dm).cpu().numpy(), np.concatenate(hm), f"m step {k}")
-        assert_f32(torch.cat(dv).cpu().numpy(), np.concatenate(hv), f"v step {k}")
-        assert_lp(to_host(torch.cat(dl)), np.concatenate(hp_), "f16", f"p_lp step {k}")
+        st = oracle_step(gl, "f16", hp_, hm, hv, hl, "f16", ohp, sc, gst)
+        assert_f32(torch.cat(dp).cpu().numpy(), np.concatenate(hp_), f"master step {k}", st.exact, bound_of(st, "p", 0))
+        assert_f32(torch.cat(dm).cpu().numpy(), np.concatenate(hm), f"m step {k}", st.exact, bound_of(st, "m", 0))
+        assert_f32(torch.cat(dv).cpu().numpy(), np.concatenate(hv), f"v step {k}", st.exact, bound_of(st, "v", 0))
+        assert_lp(to_host(torch.cat(dl)), np.concatenate(hp_), "f16", f"p_lp step {k}", st.exact, bound_of(st, "p", 0))

@@ -11,7 +11,7 @@ import zero_synth as zs
 torch = pytest.importorskip("torch")
 pytestmark = pytest.mark.gpu
 
-from gpu_common import (TORCH, assert_f32, assert_lp, hp_pair, oracle_step, to_dev,  # noqa: E402
+from gpu_common import (bound_of, TORCH, assert_f32, assert_lp, hp_pair, oracle_step, to_dev,  # noqa: E402
                         to_host)
 
 
@@ -85,11 +85,11 @@ def test_stage2_step_against_oracle(zp, max_norm):
         zp.zero_adam_step(dg, dp, dm, dv, dlp, ghp, st, ws)
         g = oracle.reduce_mean(reps, "f16", "f16").view(np.float16)
         assert to_host(dg).tobytes() == g.view(np.uint16).tobytes()
-        oracle_step([g], "f16", [p], [m], [v], [plp], "f16", ohp, sc, zp.parse_state(st))
-        assert_f32(dp.cpu().numpy(), p, f"master step {k}")
-        assert_f32(dm.cpu().numpy(), m, f"m step {k}")
-        assert_f32(dv.cpu().numpy(), v, f"v step {k}")
-        assert_lp(to_host(dlp), p, "f16", f"p_lp step {k}")
+        ost = oracle_step([g], "f16", [p], [m], [v], [plp], "f16", ohp, sc, zp.parse_state(st))
+        assert_f32(dp.cpu().numpy(), p, f"master step {k}", ost.exact, bound_of(ost, "p", 0))
+        assert_f32(dm.cpu().numpy(), m, f"m step {k}", ost.exact, bound_of(ost, "m", 0))
+        assert_f32(dv.cpu().numpy(), v, f"v step {k}", ost.exact, bound_of(ost, "v", 0))
+        assert_lp(to_host(dlp), p, "f16", f"p_lp step {k}", ost.exact, bound_of(ost, "p", 0))
 
 
 @pytest.mark.parametrize("inf_at", [None, 13_000_017])
