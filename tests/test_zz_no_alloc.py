@@ -1,12 +1,16 @@
 """zero_grad_norm_overflow_static: pass 1 for callers that cannot allocate
 device memory (and so cannot pass a workspace), with its scratch in a static
-device array inside the library.  Called through the C ABI and checked
-against zero_grad_norm_overflow on the same gradients, two calls in a row,
-within the norm tolerance the parity tests use (1e-6 relative)."""
+device array inside the library.  Called through the C ABI and checked,
+two calls in a row, against zero_grad_norm_overflow on the same gradients
+and against the oracle's binary64 sum on host copies of them, within the
+norm tolerance the parity tests use (1e-6 relative); the accumulate mode's
+folded sum against the oracle's sum over both calls' arrays."""
 import ctypes
 
+import numpy as np
 import pytest
 
+import oracle
 import zero_synth as zs
 
 torch = pytest.importorskip("torch")
@@ -50,17 +54,22 @@ def head(zp, state):
     return st["sumsq"], st["found_inf"]
 
 
-def grads(sizes, dtype, scale, seed):
-    return [to_dev(zs.host_grad(n, seed, 0, scale, dtype, micro=i), dtype)
-            for i, n in enumerate(sizes)]
+def host_grads(sizes, dtype, scale, seed):
+    return [zs.host_grad(n, seed, 0, scale, dtype, micro=i) for i, n in enumerate(sizes)]
+
+
+def close(a, b):
+    """Norms within NORM_REL, compared on sums of squares."""
+    return b > 0 and abs(np.sqrt(a) - np.sqrt(b)) <= NORM_REL * np.sqrt(b)
 
 
 @pytest.mark.parametrize("dtype", ["f16", "bf16", "f32"])
 @pytest.mark.parametrize("sizes", [[97_350_784], [5, 70_001, 3, 1 << 20]], ids=["flat", "list"])
-def test_static_scratch_matches_workspace_call(zp, dtype, sizes):
+def test_static_scratch_matches_workspace_call_and_oracle(zp, dtype, sizes):
     scale = 1024.0 if dtype == "f16" else 1.0
     for call in range(2):  # two calls in a row share the static scratch
-        arrays = grads(sizes, dtype, scale, 40 + call)
+        host = host_grads(sizes, dtype, scale, 40 + call)
+        arrays = [to_dev(a, dtype) for a in host]
         ref_state, st_state = zp.new_state(scale), zp.new_state(scale)
         ws = zp.new_workspace(len(arrays), sum(sizes))
         zp.zero_grad_norm_overflow(arrays, ref_state, ws)
@@ -68,19 +77,39 @@ def test_static_scratch_matches_workspace_call(zp, dtype, sizes):
         assert rc == 0, zp.zero_strerror(rc)
         torch.cuda.synchronize()
         (s_ref, f_ref), (s_st, f_st) = head(zp, ref_state), head(zp, st_state)
-        assert f_st == f_ref == 0.0
-        assert s_ref > 0 and abs(s_st - s_ref) <= NORM_REL * s_ref
-    # accumulate mode folds a second call into the first, and an overflow in
-    # the second call is counted once
-    arrays = grads(sizes, dtype, scale, 50)
+        s_ora, f_ora = oracle.norm_overflow(host, dtype, scale)
+        assert f_st == f_ref == 0.0 and f_ora == 0
+        assert close(s_st, s_ref), (s_st, s_ref)
+        assert close(s_st, s_ora), (s_st, s_ora)
+    # accumulate mode folds a second call into the first: the oracle's sum
+    # over both calls' arrays; an overflow in a third call is counted
+    first, second = host_grads(sizes, dtype, scale, 50), host_grads(sizes, dtype, scale, 51)
     st_state = zp.new_state(scale)
-    assert call_static(zp, arrays, st_state, 0) == 0
+    assert call_static(zp, [to_dev(a, dtype) for a in first], st_state, 0) == 0
+    assert call_static(zp, [to_dev(a, dtype) for a in second], st_state, 1) == 0
     torch.cuda.synchronize()
-    first = head(zp, st_state)[0]
-    arrays[-1][-1] = float("inf")
-    assert call_static(zp, arrays, st_state, 1) == 0
+    s_ora, f_ora = oracle.norm_overflow(first + second, dtype, scale)
+    s_st, f_st = head(zp, st_state)
+    assert f_st == 0.0 and f_ora == 0 and close(s_st, s_ora), (s_st, s_ora)
+    third = [to_dev(a, dtype) for a in host_grads(sizes, dtype, scale, 52)]
+    third[-1][-1] = float("inf")
+    assert call_static(zp, third, st_state, 1) == 0
     torch.cuda.synchronize()
-    assert first > 0 and head(zp, st_state)[1] == 1.0
+    assert head(zp, st_state)[1] == 1.0
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+@pytest.mark.parametrize("kind", zs.WIDE_KINDS)
+def test_static_scratch_over_the_binary32_range(zp, dtype, kind):
+    """Magnitudes across the binary32 range (values near 1e20, tiny,
+    subnormal, near the maximum): the norm within 1e-6 of the oracle's."""
+    host = [zs.host_cast(zs.host_wide_range(n, 90 + i, kind), dtype) for i, n in enumerate([100_003, 77])]
+    state = zp.new_state(1.0)
+    assert call_static(zp, [to_dev(a, dtype) for a in host], state) == 0
+    torch.cuda.synchronize()
+    s_st, f_st = head(zp, state)
+    s_ora, f_ora = oracle.norm_overflow(host, dtype, 1.0)
+    assert f_st == 0.0 and f_ora == 0 and close(s_st, s_ora), (kind, s_st, s_ora)
 
 
 def test_static_scratch_rejects_long_lists(zp):

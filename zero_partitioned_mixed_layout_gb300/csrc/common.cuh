@@ -53,6 +53,11 @@ struct Elem<ZERO_F16> {
                            ((w->z & 0x7C007C00u) + 0x04000400u) | ((w->w & 0x7C007C00u) + 0x04000400u);
         return a & 0x80008000u;
     }
+    // magnitude bits of the 8 elements ORed: zero iff every element is +-0
+    __device__ static __forceinline__ uint32_t nonzero(const uint4 *w)
+    {
+        return (w->x | w->y | w->z | w->w) & 0x7FFF7FFFu;
+    }
     __device__ static __forceinline__ float scalar(const void *p, int64_t i)
     {
         return __half2float(static_cast<const __half *>(p)[i]);
@@ -83,6 +88,10 @@ struct Elem<ZERO_BF16> {
         const uint32_t a = ((w->x & 0x7F807F80u) + 0x00800080u) | ((w->y & 0x7F807F80u) + 0x00800080u) |
                            ((w->z & 0x7F807F80u) + 0x00800080u) | ((w->w & 0x7F807F80u) + 0x00800080u);
         return a & 0x80008000u;
+    }
+    __device__ static __forceinline__ uint32_t nonzero(const uint4 *w)
+    {
+        return (w->x | w->y | w->z | w->w) & 0x7FFF7FFFu;
     }
     __device__ static __forceinline__ float scalar(const void *p, int64_t i)
     {
@@ -118,6 +127,10 @@ struct Elem<ZERO_F32> {
             a |= ((w[q].x & 0x7F800000u) + 0x00800000u) | ((w[q].y & 0x7F800000u) + 0x00800000u) |
                  ((w[q].z & 0x7F800000u) + 0x00800000u) | ((w[q].w & 0x7F800000u) + 0x00800000u);
         return a & 0x80000000u;
+    }
+    __device__ static __forceinline__ uint32_t nonzero(const uint4 *w)
+    {
+        return (w[0].x | w[0].y | w[0].z | w[0].w | w[1].x | w[1].y | w[1].z | w[1].w) & 0x7FFFFFFFu;
     }
     __device__ static __forceinline__ float scalar(const void *p, int64_t i)
     {
@@ -201,6 +214,65 @@ __device__ __forceinline__ float tree8(const float *a)
 {
     return __fadd_rn(__fadd_rn(__fadd_rn(a[0], a[1]), __fadd_rn(a[2], a[3])),
                      __fadd_rn(__fadd_rn(a[4], a[5]), __fadd_rn(a[6], a[7])));
+}
+
+// ------------------------------------------------------------- squares in range
+//
+// The norm passes square in binary32 and add each 8-element vector's squares
+// in a fixed binary32 tree before they reach the binary64 total.  Binary16
+// data always fits: |x| <= 65504 and every nonzero binary16 is at least
+// 2^-24, so every square is a normal binary32 between 2^-48 and 2^32.
+// Bfloat16 and binary32 data span binary32's whole range: a square
+// overflows to inf once |x| passes 2^64, and falls below the normal range
+// (losing digits, or vanishing) once |x| drops under 2^-63.  For those types
+// each vector's binary32 sum s is checked before use: it is kept if
+// s < 2^124 (then four such sums still add without overflow) and either
+// s >= 2^-90 (a square under 2^-126 then changes s by less than 2^-33 of
+// itself) or all eight values are zero.  Otherwise -- a value above about
+// 2^62, an inf or NaN, or a vector of tiny values -- the vector's squares are
+// summed again in binary64, which neither overflows nor underflows for any
+// binary32 value.  Typical data never leaves the fast path.
+
+// Magnitude bits of 8 binary32 values ORed: zero iff every value is +-0.
+__device__ __forceinline__ uint32_t nonzero8(const float *f)
+{
+    uint32_t b = 0;
+#pragma unroll
+    for (int e = 0; e < 8; ++e)
+        b |= __float_as_uint(f[e]);
+    return b & 0x7FFFFFFFu;
+}
+
+// Whether the binary32 sum s of a vector's squares may be used (see above).
+__device__ __forceinline__ bool squares_in_range(float s, uint32_t nonzero)
+{
+    return s < 0x1p124f && (s >= 0x1p-90f || nonzero == 0u);
+}
+
+// The vector's squares summed in binary64.
+__device__ __forceinline__ double squares_wide(const float *f)
+{
+    double t = 0.0;
+#pragma unroll
+    for (int e = 0; e < 8; ++e)
+        t = __fma_rn((double)f[e], (double)f[e], t);
+    return t;
+}
+
+// The squares of one vector (8 values f, whose magnitude bits OR to
+// `nonzero`) added to a binary32 partial `part`, or -- out of range -- to
+// the binary64 total `tot`.
+__device__ __forceinline__ void add_squares_checked(const float *f, uint32_t nonzero, float &part, double &tot)
+{
+    float sq[8];
+#pragma unroll
+    for (int e = 0; e < 8; ++e)
+        sq[e] = __fmul_rn(f[e], f[e]);
+    const float s = tree8(sq);
+    if (squares_in_range(s, nonzero))
+        part = __fadd_rn(part, s);
+    else
+        tot += squares_wide(f);
 }
 
 // Block sum (fixed order) of a per-thread binary64 value and OR of a flag.
@@ -753,11 +825,15 @@ bool pinned_host_ptr(const void *p)
     return a.type == cudaMemoryTypeHost && a.devicePointer == p;
 }
 
+// Lists up to this many arrays have every array's pointer checked to be
+// memory the kernels may reach.
+constexpr int64_t kCheckEveryPointer = 64;
+
 // Checks one list; on success *total holds its element count.  The device
-// pointers of a one-array list (a flat shard) are checked to be device
-// memory (or, with allow_host, pinned host memory); longer lists are checked
-// on their first and last arrays only, to keep the per-call host cost
-// independent of the list length.
+// pointers of a list of up to kCheckEveryPointer arrays are each checked to
+// be device memory (or, with allow_host, pinned host memory); longer lists
+// are checked on their first and last arrays only, to keep the per-call host
+// cost independent of the list length (a few hundred nanoseconds per check).
 int check_list(const zero_tlist_t *l, int64_t *total, bool allow_host = false)
 {
     if (!l || l->n < 0 || (l->n > 0 && (!l->ptrs || !l->numel)))
@@ -775,7 +851,7 @@ int check_list(const zero_tlist_t *l, int64_t *total, bool allow_host = false)
         t += l->numel[i];
     }
     for (int64_t i = 0; i < l->n; ++i) {
-        if (i > 0 && i < l->n - 1)
+        if (l->n > kCheckEveryPointer && i > 0 && i < l->n - 1)
             i = l->n - 1;
         if (l->numel[i] > 0 && !device_ptr(l->ptrs[i]) && !(allow_host && pinned_host_ptr(l->ptrs[i])))
             return ZERO_EINVAL;

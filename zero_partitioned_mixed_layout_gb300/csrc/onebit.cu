@@ -18,9 +18,9 @@
 // binary32 subtraction, the same as forming it at once) when the next step
 // reads x.  One pass then reads the previous x, forms the new input and
 // writes it, its signs (packed 32 to a word with two warp shuffles) and its
-// squared norm (binary32 squares in 8 lanes, one binary64 add per 32
-// elements, fixed-order block partials, the last block finishing the sum
-// and writing the new scale).  Bytes per element with an fp16 gradient:
+// squared norm (binary32 squares summed per 8 elements and range-checked,
+// one binary64 add per 32 elements, fixed-order block partials, the last
+// block finishing the sum and writing the new scale).  Bytes per element with an fp16 gradient:
 // worker 2 + 1/8 + 8 + 1/8 with the momentum as the servers' signs (2 + 4 +
 // 8 + 1/8 with a dense one); server Nd/8 + 8 + 1/8 per chunk element;
 // update 1/8 + 12 + 2 (+ 4 with a dense momentum written).
@@ -97,18 +97,17 @@ __device__ void scale_finish(double tot, double2 *partials, WsHeader *hdr, int64
 }
 
 // Squares of one 8-element group into a binary32 lane sum; every 4 groups
-// (32 elements) the lane sum goes into the binary64 total.
+// (32 elements) the lane sum goes into the binary64 total.  The compressed
+// values are binary32 of any size, so each group's binary32 sum is
+// range-checked and an out-of-range group's squares go to the binary64
+// total directly (add_squares_checked).
 struct SquareSum {
     double tot = 0.0;
     float part = 0.0f;
     int groups = 0;
     __device__ __forceinline__ void add(const float *x)
     {
-        float sq[8];
-#pragma unroll
-        for (int k = 0; k < 8; ++k)
-            sq[k] = __fmul_rn(x[k], x[k]);
-        part = __fadd_rn(part, tree8(sq));
+        add_squares_checked(x, nonzero8(x), part, tot);
         if (++groups == 4) {
             tot += (double)part;
             part = 0.0f;

@@ -26,6 +26,9 @@
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
+#include <cuda.h>  // driver types for the context identity (no driver library linked)
+#include <cudaTypedefs.h>
+
 #include <cstdint>
 #include <mutex>
 #include <unordered_map>
@@ -42,25 +45,42 @@ constexpr int64_t kL2KeepBytes = 96ll << 20;
 
 // ------------------------------------------------------------- pass 1
 
-// Squares of 4 vectors (32 elements) into 8 binary32 lanes, then one binary64
-// add per thread: the binary64 pipe sees one add per 32 elements.
+// Squares of 4 vectors (32 elements), then one binary64 add per thread: the
+// binary64 pipe sees one add per 32 elements.  Binary16: 8 binary32 lanes
+// (every square is a normal binary32).  Bfloat16 and binary32: each
+// vector's squares summed in binary32 and range-checked, an out-of-range
+// vector's squares summed in binary64 instead (add_squares_checked).
 template <int GT>
 __device__ __forceinline__ void norm_group(const uint4 (*w)[Elem<GT>::kWords], int count, double &tot,
                                            uint32_t &bad)
 {
-    float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+    if constexpr (GT == ZERO_F16) {
+        float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-    for (int k = 0; k < 4; ++k) {
-        if (k < count) {
-            bad |= Elem<GT>::nonfinite(w[k]);
-            float f[8];
-            Elem<GT>::to_float(w[k], f);
+        for (int k = 0; k < 4; ++k) {
+            if (k < count) {
+                bad |= Elem<GT>::nonfinite(w[k]);
+                float f[8];
+                Elem<GT>::to_float(w[k], f);
 #pragma unroll
-            for (int e = 0; e < 8; ++e)
-                acc[e] = __fmaf_rn(f[e], f[e], acc[e]);
+                for (int e = 0; e < 8; ++e)
+                    acc[e] = __fmaf_rn(f[e], f[e], acc[e]);
+            }
         }
+        tot += (double)tree8(acc);
+    } else {
+        float part = 0.0f;
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            if (k < count) {
+                bad |= Elem<GT>::nonfinite(w[k]);
+                float f[8];
+                Elem<GT>::to_float(w[k], f);
+                add_squares_checked(f, Elem<GT>::nonzero(w[k]), part, tot);
+            }
+        }
+        tot += (double)part;
     }
-    tot += (double)tree8(acc);
 }
 
 // 16-byte load that asks L2 to keep the line (evict-last priority).
@@ -110,9 +130,10 @@ __device__ __forceinline__ void norm_range(const void *g, int64_t n, int64_t t, 
     }
     const int64_t tail = n - (nv << 3);
     if (t < tail) {
-        const float x = Elem<GT>::scalar(g, (nv << 3) + t);
+        // the tail's squares in binary64 (any value of any type)
+        const double x = Elem<GT>::scalar(g, (nv << 3) + t);
         bad |= Elem<GT>::scalar_nonfinite(g, (nv << 3) + t);
-        tot += (double)__fmul_rn(x, x);
+        tot += x * x;
     }
 }
 
@@ -281,6 +302,7 @@ __global__ void __launch_bounds__(kThreads)
     const int64_t nv = n >> 3;
     const int64_t base = (int64_t)blockIdx.x * kThreads * V + threadIdx.x;
     float part = 0.0f;
+    double wide = 0.0;  // squares of out-of-range vectors (bfloat16 / binary32 data)
 #pragma unroll
     for (int u = 0; u < V; ++u) {
         const int64_t i = base + (int64_t)u * kThreads;
@@ -291,22 +313,27 @@ __global__ void __launch_bounds__(kThreads)
             for (int e = 0; e < 8; ++e)
                 mean[e] = __fdiv_rn(a[e], count);
             bad |= store_mean<OT>(out, i, mean, stored);
-            float sq[8];
+            if constexpr (GT == ZERO_F16) {
+                // means of binary16 values: every square is a normal binary32
+                float sq[8];
 #pragma unroll
-            for (int e = 0; e < 8; ++e)
-                sq[e] = __fmul_rn(stored[e], stored[e]);
-            part = __fadd_rn(part, tree8(sq));
+                for (int e = 0; e < 8; ++e)
+                    sq[e] = __fmul_rn(stored[e], stored[e]);
+                part = __fadd_rn(part, tree8(sq));
+            } else {
+                add_squares_checked(stored, nonzero8(stored), part, wide);
+            }
         }
     }
-    double tot = (double)part;
+    double tot = wide + (double)part;
     const int64_t tail = n - (nv << 3);
     if (blockIdx.x == 0 && threadIdx.x < tail) {
         const int64_t j = (nv << 3) + threadIdx.x;
         float a = Elem<GT>::scalar(r.p[0], j);
         for (int k = 1; k < nr; ++k)
             a = __fadd_rn(a, Elem<GT>::scalar(r.p[k], j));
-        const float x = store_mean_scalar<OT>(out, j, __fdiv_rn(a, count), bad);
-        tot += (double)__fmul_rn(x, x);
+        const double x = store_mean_scalar<OT>(out, j, __fdiv_rn(a, count), bad);
+        tot += x * x;
     }
     uint32_t b = bad != 0;
     if (group_finish(tot, b, block_partials, ga, hdr))
@@ -574,11 +601,9 @@ __global__ void __launch_bounds__(kThreads)
                     a[e] = __fadd_rn(a[e], f[e]);
             }
         bad |= store_mean<ZERO_F32>(acc, i, a, stored);
-        float sq[8];
-#pragma unroll
-        for (int e = 0; e < 8; ++e)
-            sq[e] = __fmul_rn(stored[e], stored[e]);
-        part = __fadd_rn(part, tree8(sq));
+        // binary32 sums (of any type, and of whatever acc held): squares
+        // range-checked
+        add_squares_checked(stored, nonzero8(stored), part, tot);
         if (++groups == 4) {
             tot += (double)part;
             part = 0.0f;
@@ -594,8 +619,8 @@ __global__ void __launch_bounds__(kThreads)
         for (int k = 0; k < 8; ++k)
             if (k >= overwrite && k < nb)
                 a = __fadd_rn(a, Elem<GT>::scalar(b.p[k], j));
-        const float x = store_mean_scalar<ZERO_F32>(acc, j, a, bad);
-        tot += (double)__fmul_rn(x, x);
+        const double x = store_mean_scalar<ZERO_F32>(acc, j, a, bad);
+        tot += x * x;
     }
     __shared__ DecideShared sh;
     norm_finish(tot, bad, partials, hdr, st, accumulate, &sh);
@@ -1264,29 +1289,70 @@ __global__ void __launch_bounds__(kThreads)
     norm_finish(tot, bad, partials, hdr, st, accumulate, &sh);
 }
 
-// Device address of g_norm_scratch on the current device, looked up once per
-// device (with that device current) and cached; NULL on failure.
+// The identity of the calling thread's current context (cuCtxGetId, reached
+// through the runtime's driver entry points, so the library does not link
+// the driver library itself); 0 if it cannot be had.  A device reset
+// (cudaDeviceReset) destroys the context and this library's module with it;
+// the next context gets a new identity and the module a new load.
+unsigned long long current_context_id()
+{
+    static PFN_cuCtxGetCurrent_v4000 get_current = nullptr;
+    static PFN_cuCtxGetId_v12000 get_id = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *f = nullptr;
+        cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &f, 4000, cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            get_current = reinterpret_cast<PFN_cuCtxGetCurrent_v4000>(f);
+        f = nullptr;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &f, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            get_id = reinterpret_cast<PFN_cuCtxGetId_v12000>(f);
+        cudaGetLastError();
+    });
+    CUcontext ctx = nullptr;
+    unsigned long long id = 0;
+    if (!get_current || !get_id || get_current(&ctx) != CUDA_SUCCESS || !ctx || get_id(ctx, &id) != CUDA_SUCCESS)
+        return 0;
+    return id;
+}
+
+// Device address of g_norm_scratch in the current context.  Looked up with
+// cudaGetSymbolAddress (the device current) the first time a device is used
+// and cached per device together with the context's identity; looked up
+// again when that identity changes (after a device reset) or cannot be had.
+// NULL on failure.
 void *static_scratch()
 {
+    struct Entry {
+        unsigned long long ctx = 0;
+        void *addr = nullptr;
+    };
     static std::mutex mu;
-    static void *addr[64] = {};
+    static Entry cache[64];
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) {
         cudaGetLastError();
         return nullptr;
     }
+    // the context exists once the caller's tensors do; this call makes sure
+    const unsigned long long ctx = current_context_id();
     std::lock_guard<std::mutex> lock(mu);
-    if (!addr[dev]) {
+    Entry &e = cache[dev];
+    if (!e.addr || ctx == 0 || e.ctx != ctx) {
         void *p = nullptr;
-        const cudaError_t e = cudaGetSymbolAddress(&p, g_norm_scratch);
-        if (e != cudaSuccess) {
-            set_cuda_error("zero_grad_norm_overflow_static (scratch address)", (int)e, cudaGetErrorString(e));
+        const cudaError_t err = cudaGetSymbolAddress(&p, g_norm_scratch);
+        if (err != cudaSuccess) {
+            set_cuda_error("zero_grad_norm_overflow_static (scratch address)", (int)err, cudaGetErrorString(err));
             cudaGetLastError();
+            e = Entry{};
             return nullptr;
         }
-        addr[dev] = p;
+        e.addr = p;
+        e.ctx = ctx;
     }
-    return addr[dev];
+    return e.addr;
 }
 
 template <int GT>

@@ -154,6 +154,38 @@ def host_grad(n: int, seed: int, step: int, scale: float, dtype: str, micro: int
     return host_cast(x, dtype)
 
 
+WIDE_KINDS = ("mixed", "tiny", "subnormal", "max", "sparse_tiny")
+
+
+def host_wide_range(n: int, seed: int, kind: str) -> np.ndarray:
+    """float32 gradients whose magnitudes span the binary32 range, for the
+    norm's range tests (cast to bfloat16 or kept as binary32):
+      mixed       N(0, 1e-3^2), with 1 element in 1000 replaced by
+                  +-U(1, 2) * 1e20 and 1 in 20 by +-U(1, 2) * 1e-30;
+      tiny        N(0, 1) * 1e-25 everywhere;
+      subnormal   N(0, 1) * 1e-40 everywhere (below binary32's normal range);
+      max         +-U(0.5, 1) * 3.3e38 everywhere;
+      sparse_tiny zero except 1 element in 100, +-U(1, 2) * 1e-30."""
+    rng = np.random.default_rng(stream_seed(seed, "misc", n, WIDE_KINDS.index(kind)))
+    sign = np.where(rng.random(n) < 0.5, -1.0, 1.0)
+    if kind == "mixed":
+        x = rng.standard_normal(n) * GRAD_STD
+        u = rng.random(n)
+        x = np.where(u < 1e-3, sign * rng.uniform(1.0, 2.0, n) * 1e20, x)
+        x = np.where((u >= 1e-3) & (u < 0.051), sign * rng.uniform(1.0, 2.0, n) * 1e-30, x)
+    elif kind == "tiny":
+        x = rng.standard_normal(n) * 1e-25
+    elif kind == "subnormal":
+        x = rng.standard_normal(n) * 1e-40
+    elif kind == "max":
+        x = sign * rng.uniform(0.5, 1.0, n) * 3.3e38
+    elif kind == "sparse_tiny":
+        x = np.where(rng.random(n) < 0.01, sign * rng.uniform(1.0, 2.0, n) * 1e-30, 0.0)
+    else:
+        raise ValueError(kind)
+    return x.astype(np.float32)
+
+
 def host_master(n: int, seed: int, std: float = MASTER_STD) -> np.ndarray:
     return host_normal(n, std, seed, "master")
 
