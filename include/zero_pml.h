@@ -81,6 +81,11 @@ extern "C" {
 #define ZERO_BF16 1
 #define ZERO_F32 2
 
+/* Pointer checks: every device pointer of a call is checked to be memory
+ * the kernels may reach (cudaPointerGetAttributes), except in lists of more
+ * than 64 arrays, where the first and the last array are checked (so that
+ * the host cost of a call does not grow with the list). */
+
 /* Text of a ZERO_* code; for ZERO_ECUDA, the last CUDA error seen by this
  * library on the calling thread is appended.  Never NULL.  The string stays
  * valid until the next call on the same thread. */
@@ -165,15 +170,17 @@ typedef struct zero_tlist {
 
 /* Bytes of device workspace that zero_grad_norm_overflow, zero_adam_step,
  * zero_step and zero_list_prepare need for lists of up to max_tensors arrays
- * holding up to max_total_numel elements in all (zero_accumulate_grads_norm
- * and zero_reduce_grads: one array of n elements; the 1-bit Adam calls:
- * zero_workspace_bytes(Nd, Nd * S)).  The workspace must start on a 256-byte boundary (as
+ * holding up to max_total_numel elements in all -- one rank's partition of
+ * the model states ([ZeRO card §方法适配]), flat or as its tensors -- and
+ * that zero_accumulate_grads_norm and zero_reduce_grads need for one array
+ * of n elements (the 1-bit Adam calls: zero_workspace_bytes(Nd, Nd * S)).
+ * It holds the reduction ticket and partials, the step's binary32 scalars
+ * and a list's tables.  The workspace must start on a 256-byte boundary (as
  * cudaMalloc and PyTorch allocations do) and be zero-filled before its first
  * use; each call leaves its reduction counter at zero again.  One workspace
  * must not be used by two calls that may run at the same time (two streams).
- * Device pointers passed to the library must be device (or managed) memory;
- * this is checked for every array of a one-array list and for the first and
- * last array of a longer list (ZERO_EINVAL). */
+ * Device pointers passed to the library must be device (or managed) memory
+ * (ZERO_EINVAL otherwise; see "Pointer checks" above). */
 size_t zero_workspace_bytes(int64_t max_tensors, int64_t max_total_numel);
 
 /* ------------------------------------------------------------------ calls */
@@ -202,14 +209,26 @@ int zero_accumulate_grads_norm(float *acc, const void *const *g, int32_t n_bufs,
                                size_t ws_bytes, void *stream);
 
 /* Pass 1: unscale + overflow detection + squared norm.
- * For g = float(grad) / loss_scale over every element of `grads`
- * (F16, BF16 or F32), computes sum g^2 (binary32 partial sums of at most 32
- * elements, binary64 above, fixed order: the result is the same bit for bit
- * on every run) and whether any element is +-inf or NaN.  The loss scale is
- * read from d_state.  With accumulate = 0 the results are written to
- * d_state->sumsq / found_inf; with accumulate = 1 they are added, so that
- * several calls (e.g. the Nd shards of a layout on one GPU) fold into one
- * global norm and overflow flag.  d_state: device zero_state_t.
+ * [ZeRO card §瓶颈]: mixed-precision training keeps an fp16 gradient beside
+ * the fp32 optimizer state; [DS news]: the engine manages mixed precision.
+ * The pages print no arithmetic for it; the reading is dynamic loss scaling
+ * (Micikevicius et al. 2018, section 3.2: the gradient arrives multiplied by
+ * the loss scale S; any inf/NaN in it skips the step) and global
+ * gradient-norm clipping, whose norm is taken here.
+ * For g = float(grad) / S over every element of `grads` (F16, BF16 or F32),
+ * computes sum g^2 and whether any element is +-inf or NaN.  The squares are
+ * summed in binary32 over at most 32 elements, then in binary64, in a fixed
+ * order (the result is the same bit for bit on every run); for BF16 and F32
+ * data a group of 8 whose binary32 square sum would overflow or fall below
+ * binary32's normal range is summed in binary64 instead, so every finite
+ * gradient gives a finite norm within 1e-6 of the exact one.
+ * S is read from d_state: the call takes no loss-scale argument, because the
+ * scale lives on the device and changes there (halved on an overflow,
+ * doubled after a clean run) without the host ever reading it back.  With
+ * accumulate = 0 the results are written to d_state->sumsq / found_inf; with
+ * accumulate = 1 they are added, so that several calls (e.g. the Nd shards
+ * of a layout on one GPU) fold into one global norm and overflow flag.
+ * d_state: device zero_state_t.
  * ws: device workspace of ws_bytes >= zero_workspace_bytes(grads->n, total).
  * Errors: ZERO_EINVAL, ZERO_EDTYPE, ZERO_EALIGN, ZERO_EWORKSPACE, ZERO_ECUDA. */
 int zero_grad_norm_overflow(const zero_tlist_t *grads, zero_state_t *d_state,
@@ -244,9 +263,12 @@ int zero_reduce_grads(const void *const *replicas, int32_t n_replicas, int32_t d
  * The scratch (a reduction ticket and per-block partials, 16,640 bytes) is a
  * static device array inside the library; every GPU on which the library is
  * loaded holds it until the process exits.  The first call on a device looks
- * up that array's device address (with the device current) and caches it;
- * make that first call before any stream capture.  Each call resets the
- * ticket on `stream` before its kernel.  All calls share the one array and
+ * up that array's device address (with the device current) and caches it
+ * with the identity of the current context; make that first call before any
+ * stream capture.  A device reset replaces the context, and the next call
+ * after one looks the address up again (so make that call outside capture
+ * too).  Every pointer of the list is checked to be device memory.  Each call
+ * resets the ticket on `stream` before its kernel.  All calls share the one array and
  * it keeps the last call's contents, so calls that can overlap on the GPU
  * (different streams, or several host threads) race and must not be issued.
  * Limit: at most 32 arrays in `grads` (any lengths); a longer list returns
@@ -256,6 +278,13 @@ int zero_grad_norm_overflow_static(const zero_tlist_t *grads, zero_state_t *d_st
                                    int32_t accumulate, void *stream);
 
 /* Pass 2 (preceded by a decision kernel of one small block): the step.
+ * [ZeRO card §瓶颈]: mixed-precision Adam keeps an fp16 parameter and
+ * gradient plus an fp32 parameter copy, momentum and variance (16 bytes per
+ * parameter); [ZeRO card §方法适配]: each data-parallel rank updates only its
+ * own partition of that state.  The update itself, which the pages do not
+ * print, is read as Adam (Kingma & Ba 2015) with decoupled weight decay
+ * (Loshchilov & Hutter 2019), dynamic loss scaling (Micikevicius et al.
+ * 2018, section 3.2) and global gradient-norm clipping.
  * From d_state's global sumsq / found_inf (left there by
  * zero_grad_norm_overflow, summed over ranks if there are several):
  *   - found_inf > 0: the step is skipped -- no state array, p_lp or t is

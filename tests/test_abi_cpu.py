@@ -217,3 +217,22 @@ def test_plan_struct_layout_matches_the_header(zp, tmp_path):
     got = [int(x) for x in subprocess.run([str(exe)], check=True, capture_output=True, text=True).stdout.split()]
     P = binding._ListPlan
     assert got == [ctypes.sizeof(P), P.one.offset, P.n.offset, P.gdtype.offset]
+
+
+def _comment_before(header: str, name: str) -> str:
+    """The comment block that ends right before the declaration of `name`."""
+    import re
+    m = re.search(r"/\*((?:(?!\*/).)*)\*/\s*(?:int|size_t|const char \*)\s*" + name + r"\(", header, re.S)
+    assert m, f"no comment block right before {name}"
+    return m.group(1)
+
+
+@pytest.mark.parametrize("name", ["zero_partition_layout", "zero_workspace_bytes", "zero_accumulate_grads",
+                                  "zero_grad_norm_overflow", "zero_adam_step", "zero_step"])
+def test_hot_path_calls_cite_their_passage(name):
+    """Every call of the hot path's boundary states, in its header comment,
+    the passage of the pages it implements ([ZeRO card §...] or [DS news])."""
+    import os
+    inc = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include", "zero_pml.h")
+    block = _comment_before(open(inc, encoding="utf-8").read(), name)
+    assert "[ZeRO card §" in block or "[DS news]" in block, name
