@@ -3,13 +3,16 @@
 One step = the whole hot path over one rank's shard: pass 1 (unscale,
 overflow, global squared norm), the decision kernel and pass 2 (clip, AdamW,
 cast), all through the C ABI (zero_step on one GPU; zero_grad_norm_overflow,
-the cross-rank sum and zero_adam_step on several).  Default workload: the GPT-2 1.5B model state
-flattened into 16 ZeRO shards, rank 0's shard of 97,350,784 params, fp16
-gradients (x65536 loss scale), fp32 master/momentum/variance, fp16 params.
+the cross-rank sum and zero_adam_step on several).  Default workload: the
+whole GPT-2 1.5B model state on one GPU (Nd = 1, 1,557,611,264 params
+padded: 24.9 GB of fp16 gradient and parameters and fp32 master, momentum
+and variance), fp16 gradients at loss scale 1, global-norm clipping at 1.0.
+--workload gpt2_1p5b_nd16 runs one rank's shard of the same model in 16
+ZeRO shards (97,350,784 params, x65536 loss scale).
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 
-N > 1 (under torchrun): rank r updates shard r of the same layout and the
+N > 1 (under torchrun): rank r updates shard r of the workload's layout and the
 ranks sum their 16-byte (sum g^2, found_inf) partials with one all-reduce
 between the passes: the one exchange of the step (weak scaling).
 --impl reference times the oracle (plain scalar C, host cores) on a bounded
@@ -31,7 +34,12 @@ sys.path.insert(0, ROOT)
 
 METRIC = "Adam-step params/sec & achieved HBM GB/s vs GB300 roofline (28 B/param), 1 GPU"
 UNIT = "params/s"
-WORKLOAD = "gpt2_1p5b_nd16"
+# the default step: the largest single-GPU configuration, the whole GPT-2 1.5B
+# state unpartitioned (24.9 GB of fp16 param/grad + fp32 master/m/v)
+WORKLOAD = "gpt2_1p5b_full"
+# the Nd = 16 layout of the same model: the shard the stage-2, stage-3 and
+# 1-bit workloads use
+SHARDED = "gpt2_1p5b_nd16"
 TITLES = {
     "gpt2_1p5b_nd16": "GPT-2 1.5B state (48 layers, hidden 1600, vocab 50257) in 16 "
                       "ZeRO shards, one shard per GPU",
@@ -57,6 +65,11 @@ def step_config(title, w, S, l2, world=1):
 
 
 L2_BYTES = 129e6
+# nominal HBM3e bandwidth of a GB300 (the fraction "of nominal")
+NOMINAL_HBM_GBS = 7900.0
+# the gradient tail pass 1 loads with evict-last priority for pass 2 (the
+# library's choice for flat shards: 96 MiB)
+KEEP_L2_BYTES = 96 << 20
 
 
 def nvtx(call, *args):
@@ -79,10 +92,11 @@ def kernel_source_hash() -> str:
     return h.hexdigest()[:16]
 
 
-def committed_traffic():
-    """DRAM bytes per pass-2 launch from the committed ncu summary, if it was
-    taken on the current kernel source (else None)."""
-    path = os.path.join(ROOT, "profiles", "adam_pass2_gpt2_nd16_traffic.json")
+def committed_traffic(workload: str = WORKLOAD):
+    """DRAM bytes per pass-2 launch on `workload` from the committed ncu
+    record (profiles/adam_pass2_<workload>_traffic.json), if it was taken on
+    the current kernel source (else None)."""
+    path = os.path.join(ROOT, "profiles", f"adam_pass2_{workload}_traffic.json")
     try:
         d = json.load(open(path))
     except (OSError, ValueError):
@@ -155,6 +169,23 @@ def dist_env():
 
 # ------------------------------------------------------------------ oracle arm
 
+def _oracle_inputs(w, n_sample: int, seed: int):
+    """A sample of the workload's inputs for the oracle: the master, zero
+    moments, the stored gradient of step 0 (the workload's type and loss
+    scale), the hyper-parameters (its clip threshold) and a fresh scaler."""
+    import numpy as np
+
+    import oracle
+    import zero_synth as zs
+    p = zs.host_master(n_sample, seed)
+    m = np.zeros(n_sample, np.float32)
+    v = np.zeros(n_sample, np.float32)
+    plp = np.zeros(n_sample, np.uint16)
+    g = zs.host_grad(n_sample, seed, 0, w["loss_scale"], w["gdtype"])
+    hp = oracle.HParams(**zs.HPARAMS, max_norm=w["max_norm"])
+    return p, m, v, plp, g, hp, oracle.Scaler(loss_scale=w["loss_scale"])
+
+
 def oracle_run(n_sample: int, steps: int, warmup: int, keep: bool = False):
     """The oracle as it stands (single-threaded scalar C) on the first
     n_sample elements of the workload's shard: `warmup` untimed and `steps`
@@ -166,18 +197,13 @@ def oracle_run(n_sample: int, steps: int, warmup: int, keep: bool = False):
     import zero_synth as zs
     w = zs.WORKLOADS[WORKLOAD]
     oracle.build()
-    p = zs.host_master(n_sample, 0)
-    m = np.zeros(n_sample, np.float32)
-    v = np.zeros(n_sample, np.float32)
-    plp = np.zeros(n_sample, np.uint16)
-    g = zs.host_grad(n_sample, 0, 0, w["loss_scale"], "f16")
-    hp = oracle.HParams()
-    sc = oracle.Scaler(loss_scale=w["loss_scale"])
+    p, m, v, plp, g, hp, sc = _oracle_inputs(w, n_sample, 0)
+    gt, pt = w["gdtype"], w["pdtype"]
     for _ in range(warmup):
-        oracle.adam_step([g], "f16", [p], [m], [v], [plp], "f16", hp, sc)
+        oracle.adam_step([g], gt, [p], [m], [v], [plp], pt, hp, sc)
     t0 = time.perf_counter()
     for _ in range(steps):
-        oracle.adam_step([g], "f16", [p], [m], [v], [plp], "f16", hp, sc)
+        oracle.adam_step([g], gt, [p], [m], [v], [plp], pt, hp, sc)
     dt = time.perf_counter() - t0
     return n_sample * steps / dt, dt, ((p, m, v, plp) if keep else None)
 
@@ -195,12 +221,15 @@ def parity_vs_oracle(dev, n_sample: int, steps: int, final) -> dict:
     import zero_synth as zs
     w = zs.WORKLOADS[WORKLOAD]
     p = torch.from_numpy(zs.host_master(n_sample, 0)).to(dev)
-    g = torch.from_numpy(zs.host_grad(n_sample, 0, 0, w["loss_scale"], "f16")).to(dev)
+    hg = zs.host_grad(n_sample, 0, 0, w["loss_scale"], w["gdtype"])
+    g = torch.from_numpy(hg.view(np.int16)).view(torch.bfloat16).to(dev) if w["gdtype"] == "bf16" \
+        else torch.from_numpy(hg).to(dev)
     m, v = torch.zeros_like(p), torch.zeros_like(p)
-    plp = torch.zeros(n_sample, dtype=torch.float16, device=dev)
+    plp = torch.zeros(n_sample, dtype={"f16": torch.float16, "bf16": torch.bfloat16}[w["pdtype"]], device=dev)
     state, ws = zp.new_state(w["loss_scale"], dev), zp.new_workspace(1, n_sample, dev)
+    hp = zp.HParams(**zs.HPARAMS, max_norm=w["max_norm"])
     for _ in range(steps):
-        zp.zero_step(g, p, m, v, plp, zp.HParams(), state, ws)
+        zp.zero_step(g, p, m, v, plp, hp, state, ws)
     torch.cuda.synchronize(dev)
 
     def ordered(a):
@@ -235,19 +264,14 @@ def _oracle_worker(k, n_sample, steps, warmup, barrier, out):
     import zero_synth as zs
     w = zs.WORKLOADS[WORKLOAD]
     oracle.build()
-    p = zs.host_master(n_sample, k)
-    m = np.zeros(n_sample, np.float32)
-    v = np.zeros(n_sample, np.float32)
-    plp = np.zeros(n_sample, np.uint16)
-    g = zs.host_grad(n_sample, k, 0, w["loss_scale"], "f16")
-    hp = oracle.HParams()
-    sc = oracle.Scaler(loss_scale=w["loss_scale"])
+    p, m, v, plp, g, hp, sc = _oracle_inputs(w, n_sample, k)
+    gt, pt = w["gdtype"], w["pdtype"]
     for _ in range(warmup):
-        oracle.adam_step([g], "f16", [p], [m], [v], [plp], "f16", hp, sc)
+        oracle.adam_step([g], gt, [p], [m], [v], [plp], pt, hp, sc)
     barrier.wait()
     t0 = time.time()
     for _ in range(steps):
-        oracle.adam_step([g], "f16", [p], [m], [v], [plp], "f16", hp, sc)
+        oracle.adam_step([g], gt, [p], [m], [v], [plp], pt, hp, sc)
     out.put((k, t0, time.time()))
 
 
@@ -394,9 +418,12 @@ class Workload:
             return 3
         return 2 if (exchange is None and not self.listmode) else 3
 
-    def step(self, stream, exchange=None, ev=None, g=None):
+    def step(self, stream, exchange=None, ev=None, g=None, lp=None):
+        """One step; `g` and `lp` replace the gradient input and the
+        low-precision parameter output (flat shards)."""
         zp = self.zp
         g = self.g if g is None else g
+        lp = self.lp if lp is None else lp
         if self.micro > 1:
             # the accumulation with pass 1 fused, then the decision and pass 2
             zp.zero_accumulate_grads_norm(g, self.bufs, self.state, self.ws, overwrite=True, stream=stream)
@@ -413,7 +440,7 @@ class Workload:
             if getattr(self, "plan", None) is not None:
                 zp.zero_step_prepared(self.plan, self.hp, self.state, self.ws, stream=stream)
             else:
-                zp.zero_step(g, self.p, self.m, self.v, self.lp, self.hp, self.state, self.ws,
+                zp.zero_step(g, self.p, self.m, self.v, lp, self.hp, self.state, self.ws,
                              stream=stream)
             return
         zp.zero_grad_norm_overflow(g, self.state, self.ws, stream=stream)
@@ -421,7 +448,7 @@ class Workload:
             exchange(self.state)
         if ev is not None:
             ev[0].record(stream)
-        zp.zero_adam_step(g, self.p, self.m, self.v, self.lp, self.hp, self.state, self.ws,
+        zp.zero_adam_step(g, self.p, self.m, self.v, lp, self.hp, self.state, self.ws,
                           stream=stream)
         if ev is not None:
             ev[1].record(stream)
@@ -439,6 +466,10 @@ def run_ours(args):
         torch.cuda.set_device(local)
         dist.init_process_group("nccl")
     dev = torch.device("cuda", torch.cuda.current_device())
+    if world > 1 and args.workload == WORKLOAD:
+        # several GPUs: each rank one ZeRO shard of the same model (rank r
+        # shard r of 16), the per-GPU work fixed as N grows
+        args.workload = SHARDED
     wl = Workload(args.workload, args.log2n, rank, dev, prepared=args.prepared)
     S = wl.S
     stream = torch.cuda.current_stream(dev)
@@ -464,11 +495,15 @@ def run_ours(args):
     st = zp.parse_state(wl.state)
     assert st["last_skipped"] == 0 and st["step"] == args.warmup, st
 
-    events = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-              for _ in range(args.steps)]
+    def pairs():
+        return [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                for _ in range(args.steps)]
+
+    events = pairs()          # decision + pass 2, in the instrumented run
     t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    step_events = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-                   for _ in range(args.steps)] if flush is not None else None
+    # per-step times of the whole step: in the timed run itself when L2 is
+    # flushed before each step, else in a run of their own
+    step_events = pairs()
     with ClockSampler(dev.index if world == 1 else local) as clk:
         # the sampler polls every 200 ms: keep the GPU in the same step for a
         # second right before the timed region so that the clock record
@@ -502,11 +537,21 @@ def run_ours(args):
                 flush.fill_(k & 255)
             step(events[k])
         barrier()
+        if flush is None:
+            # and once more with events around each whole step (between
+            # steps, where no launch overlaps anyway)
+            for k in range(args.steps):
+                step_events[k][0].record(stream)
+                step()
+                step_events[k][1].record(stream)
+            barrier()
+    step_times = [a.elapsed_time(b) for a, b in step_events]
+    adam_times = [a.elapsed_time(b) for a, b in events]
     if flush is not None:  # the step alone, L2 flushed before each one
-        ms = sum(a.elapsed_time(b) for a, b in step_events)
+        ms = sum(step_times)
     else:
         ms = t_start.elapsed_time(t_end)
-    adam_ms = statistics.mean(a.elapsed_time(b) for a, b in events)
+    adam_ms = statistics.mean(adam_times)
     st = zp.parse_state(wl.state)
     assert st["last_skipped"] == 0 and st["step"] >= args.warmup + args.steps, st
     if world > 1:
@@ -516,40 +561,58 @@ def run_ours(args):
     ms_per_step = ms / args.steps
     value = world * S / (ms_per_step * 1e-3)
 
-    # end to end through the public API from pinned host memory: every step
-    # copies its gradient in (H2D), runs, and its 64-byte state is copied out
-    # (D2H) and read on the host.  The gradient is double-buffered on the
-    # device: the copy of step k+1 (on its own stream) runs while step k
-    # computes, which is how a loop fed from host memory keeps the link busy.
+    # end to end through the public API between pinned host memory and the
+    # GPU: every step copies its gradient in (H2D), runs, and copies its
+    # product out (D2H) -- the updated low-precision parameters, which the
+    # next forward pass (or the parameter all-gather of ZeRO stages 1 and 2)
+    # consumes -- plus the 64-byte state, read and checked on the host.  The
+    # gradient and the parameter output are double-buffered on the device and
+    # the two copies run on streams of their own, so that step k computes
+    # while step k+1's gradient comes in and step k-1's parameters go out
+    # (the host link carries both directions at once).
     e2e = None
     if not wl.listmode and wl.micro == 1:
         hg = torch.empty(S, dtype=wl.g.dtype, pin_memory=True)
-        hg.copy_(wl.g.cpu())
+        hg.copy_(wl.g)
         gbuf = [wl.g, torch.empty_like(wl.g)]
+        lpbuf = [wl.lp, torch.empty_like(wl.lp)]
+        hlp = [torch.empty(S, dtype=wl.lp.dtype, pin_memory=True) for _ in range(2)]
         hs = [torch.empty(zp.STATE_BYTES, dtype=torch.uint8, pin_memory=True) for _ in range(2)]
-        copy_stream = torch.cuda.Stream(dev)
+        h2d_stream, d2h_stream = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
         h2d_done = [torch.cuda.Event() for _ in range(2)]
         step_done = [torch.cuda.Event() for _ in range(2)]
         res_ready = [torch.cuda.Event() for _ in range(2)]
+        d2h_done = [torch.cuda.Event() for _ in range(2)]
         for b in range(2):
             step_done[b].record(stream)
+            d2h_done[b].record(d2h_stream)
 
         def check(b):
             res_ready[b].synchronize()
+            d2h_done[b].synchronize()
             assert zp.parse_state(bytes(hs[b].numpy().tobytes()))["last_skipped"] == 0
 
         def e2e_steps(count):
             for k in range(count):
                 b = k & 1
-                copy_stream.wait_event(step_done[b])  # the step that last read buffer b
-                with torch.cuda.stream(copy_stream):
+                # the gradient in, once the step that last read buffer b is done
+                h2d_stream.wait_event(step_done[b])
+                with torch.cuda.stream(h2d_stream):
                     gbuf[b].copy_(hg, non_blocking=True)
-                h2d_done[b].record(copy_stream)
+                h2d_done[b].record(h2d_stream)
+                # the step, once its gradient is in and the parameters that
+                # output buffer b held two steps ago are out
                 stream.wait_event(h2d_done[b])
-                wl.step(stream, exchange, g=gbuf[b])
+                stream.wait_event(d2h_done[b])
+                wl.step(stream, exchange, g=gbuf[b], lp=lpbuf[b])
                 step_done[b].record(stream)
                 hs[b].copy_(wl.state, non_blocking=True)
                 res_ready[b].record(stream)
+                # the parameters out
+                d2h_stream.wait_event(step_done[b])
+                with torch.cuda.stream(d2h_stream):
+                    hlp[b].copy_(lpbuf[b], non_blocking=True)
+                d2h_done[b].record(d2h_stream)
                 if k >= 1:
                     check((k - 1) & 1)
             check((count - 1) & 1)
@@ -560,16 +623,23 @@ def run_ours(args):
         e2e_steps(args.steps)
         barrier()
         e2e_s = (time.perf_counter() - t0) / args.steps
+        # the copied-out parameters are the step's product: the last step's
+        # equal the device's copy (checked on its first and last 2^20)
+        last = (args.steps - 1) & 1
+        for sl in (slice(0, 1 << 20), slice(max(0, S - (1 << 20)), S)):
+            assert torch.equal(hlp[last][sl], lpbuf[last][sl].cpu())
         if world > 1:
             t = torch.tensor([e2e_s], dtype=torch.float64, device=dev)
             dist.all_reduce(t, op=dist.ReduceOp.MAX)
             e2e_s = t.item()
-        e2e = {"value": world * S / e2e_s, "unit": UNIT,
-               "h2d_bytes_per_step": hg.numel() * hg.element_size(),
-               "d2h_bytes_per_step": zp.STATE_BYTES,
-               "note": "every step: gradient copied from pinned host memory, the step, state "
-                       "copied back and checked on the host; the next step's copy overlaps "
-                       "this step's compute (double-buffered gradient)"}
+        h2d = hg.numel() * hg.element_size()
+        d2h = hlp[0].numel() * hlp[0].element_size() + zp.STATE_BYTES
+        e2e = {"value": world * S / e2e_s, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+               "ms_per_step": e2e_s * 1e3, "host_link_gbs": (h2d + d2h) / e2e_s / 1e9,
+               "note": "every step: the gradient copied in from pinned host memory, the step, the "
+                       "updated low-precision parameters and the state copied out to pinned host "
+                       "memory and the state checked on the host; copies in and out on their own "
+                       "streams, overlapping the neighbouring steps (double-buffered on the device)"}
 
     if rank != 0:
         if world > 1:
@@ -579,6 +649,7 @@ def run_ours(args):
     peaks = measured_peaks()
     peak = peaks["hbm_gbs"] if peaks else 6800.0
     achieved = wl.bytes_adam * S / (adam_ms * 1e-3) / 1e9
+    whole = wl.bytes_step * S / (ms_per_step * 1e-3) / 1e9
     cpu = None
     if not args.no_cpu_baseline and world == 1:
         # about 10-20 s of CPU work in all: 10 full steps of 2^24 params on
@@ -588,7 +659,7 @@ def run_ours(args):
         av, adt, procs = oracle_run_all_cores(n_sample, c_steps, 1)
         cpu = {"value": av, "unit": UNIT, "cores": procs, "kind": "oracle",
                "sample": f"{procs} processes (one per host core), each {c_steps} full steps on its own "
-                         f"{n_sample} params shaped like the GPT-2 1.5B Nd=16 shard, "
+                         f"{n_sample} params drawn as the workload's ({TITLES[WORKLOAD]}), "
                          f"{adt:.1f} s wall ({procs * adt:.0f} s of CPU); the oracle as it stands "
                          f"(single-threaded scalar C)",
                "single_core": {"value": cv, "unit": UNIT, "cores": 1, "seconds": cdt,
@@ -596,6 +667,14 @@ def run_ours(args):
                # the library on the single-core run's inputs, against its result
                "parity": parity_vs_oracle(dev, n_sample, c_steps + 1, final)}
     default = args.workload == WORKLOAD
+    traffic = committed_traffic(args.workload) if not args.prepared else None
+    # the part of pass 2's gradient reads that pass 1 leaves in L2 (its
+    # evict-last tail): pass-2 fractions above 1 of a copy peak come from it
+    l2_tail = min(KEEP_L2_BYTES, wl.S * wl.g.element_size()) if not wl.listmode and wl.micro == 1 else 0
+
+    def stats(xs):
+        return {"median": statistics.median(xs), "min": min(xs), "max": max(xs), "n": len(xs)}
+
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
@@ -607,23 +686,39 @@ def run_ours(args):
             if flush is not None else
             f"inputs larger than L2 ({wl.bytes_step * S / 1e9:.2f} GB per step vs {L2_BYTES / 1e6:.0f} MB), "
             "no flush", world),
-        "hbm_gbs_adam": wl.bytes_adam * S / (adam_ms * 1e-3) / 1e9,
-        "hbm_gbs_step": wl.bytes_step * S / (ms_per_step * 1e-3) / 1e9,
+        "hbm_gbs_adam": achieved,
+        "hbm_gbs_step": whole,
         "bytes_per_param": {"adam_pass": wl.bytes_adam, "whole_step": wl.bytes_step},
-        "passes_ms": {"adam_step": adam_ms, "whole_step": ms_per_step,
-                      "note": "whole_step from the timed steps; adam_step (decision + pass 2) "
-                              "from a second run of as many steps with events around it"},
+        "passes_ms": {"adam_step": adam_ms, "adam_step_per_step": stats(adam_times),
+                      "whole_step": ms_per_step, "whole_step_per_step": stats(step_times),
+                      "note": "whole_step: the timed steps' total over their count; adam_step (decision "
+                              "+ pass 2): the mean over a second run of as many steps with events around "
+                              "it; *_per_step: median, min and max of the per-step event times"
+                              + ("" if flush is not None else " (the whole step's from a third run with "
+                                 "events between the steps)")},
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
-                     "frac": achieved / peak, "traffic": committed_traffic() if default else None,
-                     "kernel": f"zero_adam_step (decision + pass 2), {wl.bytes_adam} B/param",
+                     "frac": achieved / peak, "traffic": traffic,
+                     "kernel": f"zero_adam_step (decision + pass 2: k_adam_flat), {wl.bytes_adam} B/param",
                      "peak_source": "MEASURED_PEAKS.json hbm_gbs (of measured)" if peaks
-                     else "fallback 6.8 TB/s (of fallback)"},
+                     else "fallback 6.8 TB/s (of fallback)",
+                     "peak_record": {k: peaks.get(k) for k in ("hbm_gbs", "how", "when", "gpu_name", "torch")}
+                     if peaks else None,
+                     "frac_of_nominal": achieved / NOMINAL_HBM_GBS,
+                     "nominal_gbs": NOMINAL_HBM_GBS,
+                     "l2_assisted_bytes": l2_tail,
+                     "l2_assisted_share": l2_tail / (wl.bytes_adam * S),
+                     "whole_step": {"bytes_per_param": wl.bytes_step, "achieved": whole,
+                                    "frac": whole / peak, "frac_of_nominal": whole / NOMINAL_HBM_GBS,
+                                    "note": "every kernel of the step over ms_per_step: no L2 carry-over "
+                                            "counted"}},
         "cpu_baseline": cpu,
         "e2e": e2e,
         "gpu_launches": wl.launches_per_step(exchange) * args.steps,
         "clocks": dict(clk.summary(), window=f"{args.clock_preroll:.1f} s of the same step "
                        "just before the timed region, and the timed region"),
     }
+    if not default:
+        line["config"]["bench_workload"] = args.workload
     print(json.dumps(line), flush=True)
     if world > 1:
         dist.destroy_process_group()
@@ -639,7 +734,7 @@ def run_stage2(args):
     import zero_partitioned_mixed_layout_gb300 as zp
     import zero_synth as zs
     dev = torch.device("cuda", torch.cuda.current_device())
-    w = zs.WORKLOADS[WORKLOAD]
+    w = zs.WORKLOADS[SHARDED]
     S = zp.zero_partition_layout(w["numel"](), w["nd"], w["align"]).shard_numel
     nd = w["nd"]
     scale = w["loss_scale"]
@@ -723,7 +818,7 @@ def run_gather(args):
     import zero_partitioned_mixed_layout_gb300 as zp
     import zero_synth as zs
     dev = torch.device("cuda", torch.cuda.current_device())
-    numel = zs.WORKLOADS[WORKLOAD]["numel"]()
+    numel = zs.WORKLOADS[SHARDED]["numel"]()
     nd, align = 16, 128
     lay = zp.zero_partition_layout(numel, nd, align)
     S, total = lay.shard_numel, sum(numel)
@@ -813,7 +908,7 @@ def run_onebit(args):
     import zero_partitioned_mixed_layout_gb300 as zp
     import zero_synth as zs
     dev = torch.device("cuda", torch.cuda.current_device())
-    numel_list = zs.WORKLOADS[WORKLOAD]["numel"]()
+    numel_list = zs.WORKLOADS[SHARDED]["numel"]()
     nd = 16
     S = zp.zero_partition_layout(numel_list, nd, 128).shard_numel
     numel, n = sum(numel_list), nd * S
@@ -988,7 +1083,7 @@ def run_onebit_server(args):
     import zero_synth as zs
     dev = torch.device("cuda", torch.cuda.current_device())
     nd = 16
-    S = zp.zero_partition_layout(zs.WORKLOADS[WORKLOAD]["numel"](), nd, 128).shard_numel
+    S = zp.zero_partition_layout(zs.WORKLOADS[SHARDED]["numel"](), nd, 128).shard_numel
     gen = torch.Generator(device=dev)
     gen.manual_seed(zs.stream_seed(0, "misc", 43))
     wbits = [torch.randint(-2 ** 31, 2 ** 31 - 1, (S // 32,), dtype=torch.int32, device=dev, generator=gen)
@@ -1066,7 +1161,7 @@ def run_offload(args):
     import zero_partitioned_mixed_layout_gb300 as zp
     import zero_synth as zs
     dev = torch.device("cuda", torch.cuda.current_device())
-    w = zs.WORKLOADS[WORKLOAD]
+    w = zs.WORKLOADS[SHARDED]
     S = zp.zero_partition_layout(w["numel"](), w["nd"], w["align"]).shard_numel
     threads = zp.default_host_threads()
     scale = w["loss_scale"]
@@ -1197,7 +1292,9 @@ def main():
                     choices=["gpt2_1p5b_nd16", "tiny", "gpt2_1p5b_full", "stack_100b_nd400",
                              "frag_10k", "flat", "offload", "stage2", "gather", "onebit", "onebit_server",
                              "graph"],
-                    help="default: the GPT-2 1.5B Nd=16 shard the metric is quoted on")
+                    help="default: the whole GPT-2 1.5B state (Nd = 1), the largest configuration "
+                         "that fits one GPU; under torchrun each rank takes one shard of the same "
+                         "model in 16 ZeRO shards instead")
     ap.add_argument("--log2n", type=int, default=26, help="size of the flat workload (2^k)")
     ap.add_argument("--prepared", action="store_true",
                     help="frag_10k: the list step prepared once (zero_list_prepare / zero_step_prepared)")
