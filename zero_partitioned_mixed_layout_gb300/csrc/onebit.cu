@@ -246,12 +246,16 @@ __global__ void __launch_bounds__(kThreads) k_onebit_worker(const void *g, Momen
 // and adds the remaining workers' terms in rank order.  Same additions,
 // same order, same bits.
 //
-// Data movement: a warp takes 1024 elements at a time (128 vectors of 8;
-// lane l holds vectors v0 + l + 32v, v = 0..3), so that its load of one
-// worker's 32 sign words is one full 128-byte line; shuffles hand each lane
-// the words of its vectors.  A vector's signs from 8 workers are 8 bytes;
-// an 8x8 bit-matrix transpose turns them into one byte per element, bit q
-// for worker q of the group.  Bytes per chunk element: Nd/8 + 4 + 4 + 1/8.
+// Data movement: a warp takes 1024 elements (32 words of signs, 128 vectors
+// of 8) at a time.  Lane l loads the 16 workers' sign words of word l
+// (coalesced: a warp's loads of one worker are one 128-byte line) and turns
+// them around with one 16x32 bit-matrix transpose in registers into each of
+// the word's 32 elements' 16-bit sign pattern; the patterns go through 2 KB
+// of shared memory per warp to the lanes that hold those elements' values,
+// which are read and written coalesced (lane l holds vectors l + 32v).  The
+// staging is swizzled so that both sides are free of bank conflicts.
+// Workers past 16 go the same way, 16 at a time.  Bytes per chunk element:
+// Nd/8 + 4 + 4 + 1/8.
 constexpr int kTableBits = 14;
 // Workers per server call: their pointers and scales (12 bytes each) and
 // the 64 KiB table fit in shared memory.
@@ -263,34 +267,34 @@ struct WorkerPtrs {
     const uint32_t *p[kArgWorkers];
 };
 
-// 8x8 bit-matrix transpose (Hacker's Delight, section 7-3, the three-step
-// swap of 1x1, 2x2 and 4x4 blocks): bit c of byte r <-> bit r of byte c.
-__device__ __forceinline__ uint64_t transpose8(uint64_t x)
+// The signs of 16 workers for the 32 elements of one word, turned around:
+// on entry W[k] holds worker k's word (bit e for element e); on return the
+// low half of W[i] holds element i's signs and the high half element
+// 16 + i's, bit k for worker k.  A 16x16 bit-matrix transpose of each half
+// at once, by the recursive block swap (Hacker's Delight, section 7-3):
+// four stages that exchange the off-diagonal s x s blocks (s = 8, 4, 2, 1)
+// of every 2s x 2s block, five integer operations per row pair.
+template <int S, uint32_t M>
+__device__ __forceinline__ void transpose16_stage(uint32_t *W)
 {
-    uint64_t t = (x ^ (x >> 7)) & 0x00AA00AA00AA00AAull;
-    x ^= t ^ (t << 7);
-    t = (x ^ (x >> 14)) & 0x0000CCCC0000CCCCull;
-    x ^= t ^ (t << 14);
-    t = (x ^ (x >> 28)) & 0x00000000F0F0F0F0ull;
-    x ^= t ^ (t << 28);
-    return x;
+#pragma unroll
+    for (int r = 0; r < 16; ++r) {
+        if ((r & S) == 0) {
+            const uint32_t t = ((W[r] >> S) ^ W[r + S]) & M;
+            W[r + S] ^= t;
+            W[r] ^= t << S;
+        }
+    }
 }
 
-// The signs of 8 workers for this lane's vector (words w[0..7] of the
-// warp's 32-word span, from lane `src`; byte `psel` selects this lane's
-// byte): byte j of the result holds element j's signs, bit q = worker q.
-__device__ __forceinline__ uint64_t group_signs(const uint32_t *w, int src, uint32_t psel)
+// The stages with their shifts and masks as constants, so that every row
+// index is fixed at compile time and the rows stay in registers.
+__device__ __forceinline__ void transpose16(uint32_t *W)
 {
-    uint32_t b[2];
-#pragma unroll
-    for (int h = 0; h < 2; ++h) {
-        const uint32_t x0 = __shfl_sync(0xffffffffu, w[4 * h], src);
-        const uint32_t x1 = __shfl_sync(0xffffffffu, w[4 * h + 1], src);
-        const uint32_t x2 = __shfl_sync(0xffffffffu, w[4 * h + 2], src);
-        const uint32_t x3 = __shfl_sync(0xffffffffu, w[4 * h + 3], src);
-        b[h] = __byte_perm(__byte_perm(x0, x1, psel), __byte_perm(x2, x3, psel), 0x5410);
-    }
-    return transpose8((uint64_t)b[0] | ((uint64_t)b[1] << 32));
+    transpose16_stage<8, 0x00FF00FFu>(W);
+    transpose16_stage<4, 0x0F0F0F0Fu>(W);
+    transpose16_stage<2, 0x33333333u>(W);
+    transpose16_stage<1, 0x55555555u>(W);
 }
 
 // +scale where the sign bit (at bit 31 of t) is set, -scale where it is
@@ -302,10 +306,40 @@ __device__ __forceinline__ float signed_scale(uint32_t scale_bits, uint32_t t)
 
 // The dynamic shared memory of the server: the table, the worker pointers
 // and the scales.
+// Per warp: 32 lanes x 32 elements x 2 bytes of staged sign patterns.
+constexpr size_t kStageBytesPerWarp = 2048;
+
 __host__ __device__ constexpr size_t server_smem_bytes(int nd)
 {
-    return sizeof(float) * ((size_t)1 << (nd < kTableBits ? nd : kTableBits)) +
+    return kStageBytesPerWarp * kWarps + sizeof(float) * ((size_t)1 << (nd < kTableBits ? nd : kTableBits)) +
            (sizeof(void *) + sizeof(float)) * (size_t)nd;
+}
+
+// The 16-byte slot of staging chunk c (chunk 4w + q: the sign patterns of
+// elements 8q .. 8q+7 of the warp's word w): the low two bits of the 16-byte
+// bank group are XORed with bits 3-4 of c, so that the writes (lane w: chunks
+// 4w + q) and the reads (lane l: chunk l + 32v) each spread over all eight
+// bank groups.
+__device__ __forceinline__ int stage_slot(int c) { return c ^ ((c >> 3) & 3); }
+
+// Lane side of the staging: the 16 sign words W (after transpose16) of this
+// lane's word w, packed two patterns to a 32-bit word in element order, into
+// the warp's staging area.
+__device__ __forceinline__ void stage_patterns(const uint32_t *W, uint4 *stage, int lane)
+{
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+        // elements 8q .. 8q+7: low halves of rows 0-7 / 8-15 for q = 0 / 1,
+        // high halves for q = 2 / 3
+        const int r0 = (q & 1) * 8;
+        const uint32_t sel = q < 2 ? 0x5410u : 0x7632u;
+        uint4 c;
+        c.x = __byte_perm(W[r0 + 0], W[r0 + 1], sel);
+        c.y = __byte_perm(W[r0 + 2], W[r0 + 3], sel);
+        c.z = __byte_perm(W[r0 + 4], W[r0 + 5], sel);
+        c.w = __byte_perm(W[r0 + 6], W[r0 + 7], sel);
+        stage[stage_slot(4 * lane + q)] = c;
+    }
 }
 
 template <bool kPow2, bool W32>
@@ -315,8 +349,11 @@ __device__ __forceinline__ void server_body(const uint32_t *const *wbits, const 
 {
     extern __shared__ __align__(16) unsigned char s_raw[];
     const int P = nd < kTableBits ? nd : kTableBits;
-    float *T = reinterpret_cast<float *>(s_raw);
-    const uint32_t **s_ptr = reinterpret_cast<const uint32_t **>(s_raw + sizeof(float) * ((size_t)1 << P));
+    // dynamic shared memory, in server_smem_bytes' order: the warps' staging
+    // areas, the table, the worker pointers, the scales
+    uint4 *stage = reinterpret_cast<uint4 *>(s_raw + kStageBytesPerWarp * (threadIdx.x >> 5));
+    float *T = reinterpret_cast<float *>(s_raw + kStageBytesPerWarp * kWarps);
+    const uint32_t **s_ptr = reinterpret_cast<const uint32_t **>(T + ((size_t)1 << P));
     float *s_scale = reinterpret_cast<float *>(s_ptr + nd);
     pdl_wait();
     // the old scale, read by every block before its ticket
@@ -343,7 +380,6 @@ __device__ __forceinline__ void server_body(const uint32_t *const *wbits, const 
     }
     const bool skip = scp->skip != 0;
     const int lane = threadIdx.x & 31;
-    const uint32_t psel = (uint32_t)(lane & 3) | ((uint32_t)((lane & 3) + 4) << 4);
     const uint32_t pmask = (1u << P) - 1u;
     // workers P..15 that the table leaves out (none when Nd <= 14)
     const int upto16 = nd < 16 ? nd : 16;
@@ -355,8 +391,8 @@ __device__ __forceinline__ void server_body(const uint32_t *const *wbits, const 
     SquareSum acc;
     for (int64_t c = (int64_t)blockIdx.x * kWarps + (threadIdx.x >> 5); c < chunks;
          c += (int64_t)gridDim.x * kWarps) {
-        const int64_t v0 = c << 7, w0 = c << 5;
-        const bool wok = w0 + lane < nw;
+        const int64_t v0 = c << 7, w = (c << 5) + lane;
+        const bool wok = w < nw;
         float y[4][8];
 #pragma unroll
         for (int v = 0; v < 4; ++v) {
@@ -364,48 +400,66 @@ __device__ __forceinline__ void server_body(const uint32_t *const *wbits, const 
             if (i < nv)
                 ld8<W32>(ys + 8 * i, y[v]);
         }
-        float a[4][8];
+        // workers 0-15: the table index (bits 0..P-1 of the pattern) and
+        // workers 14 and 15 added after it
         {
-            uint32_t w[16];
+            uint32_t W[16];
 #pragma unroll
             for (int k = 0; k < 16; ++k)
-                w[k] = k < nd && wok ? __ldg(s_ptr[k] + w0 + lane) : 0u;
+                W[k] = k < nd && wok ? __ldg(s_ptr[k] + w) : 0u;
+            transpose16(W);
+            stage_patterns(W, stage, lane);
+        }
+        __syncwarp();
+        float a[4][8];
 #pragma unroll
-            for (int v = 0; v < 4; ++v) {
-                const int src = 8 * v + (lane >> 2);
-                const uint64_t lo = group_signs(w, src, psel), hi = group_signs(w + 8, src, psel);
+        for (int v = 0; v < 4; ++v) {
+            const uint4 pc = stage[stage_slot(lane + 32 * v)];
+            const uint32_t pw[4] = {pc.x, pc.y, pc.z, pc.w};
 #pragma unroll
-                for (int j = 0; j < 8; ++j) {
-                    const uint32_t pl = (uint32_t)(lo >> (8 * j)) & 0xFFu, ph = (uint32_t)(hi >> (8 * j)) & 0xFFu;
-                    float x = T[(pl | (ph << 8)) & pmask];
-                    if (P == 14 && upto16 > 14)
-                        x = __fadd_rn(x, signed_scale(sb14, ph << 25));
-                    if (P == 14 && upto16 > 15)
-                        x = __fadd_rn(x, signed_scale(sb15, ph << 24));
-                    a[v][j] = x;
-                }
+            for (int j = 0; j < 8; ++j) {
+                // element j's pattern in bits 0-15 of t (16-31 of pw)
+                const uint32_t t = (j & 1) ? pw[j >> 1] >> 16 : pw[j >> 1];
+                float x = T[t & pmask];
+                if (P == 14 && upto16 > 14)
+                    x = __fadd_rn(x, signed_scale(sb14, t << 17));
+                if (P == 14 && upto16 > 15)
+                    x = __fadd_rn(x, signed_scale(sb15, t << 16));
+                a[v][j] = x;
             }
         }
-        // workers 16 and up, 8 at a time
-        for (int g = 16; g < nd; g += 8) {
-            uint32_t w[8];
+        // workers 16 and up, 16 at a time, in rank order
+        for (int g = 16; g < nd; g += 16) {
+            __syncwarp();  // every lane has read the previous patterns
+            {
+                uint32_t W[16];
 #pragma unroll
-            for (int q = 0; q < 8; ++q)
-                w[q] = g + q < nd && wok ? __ldg(s_ptr[g + q] + w0 + lane) : 0u;
+                for (int k = 0; k < 16; ++k)
+                    W[k] = g + k < nd && wok ? __ldg(s_ptr[g + k] + w) : 0u;
+                transpose16(W);
+                stage_patterns(W, stage, lane);
+            }
+            __syncwarp();
+            const int nq = nd - g < 16 ? nd - g : 16;
 #pragma unroll
             for (int v = 0; v < 4; ++v) {
-                const uint64_t gs = group_signs(w, 8 * v + (lane >> 2), psel);
+                const uint4 pc = stage[stage_slot(lane + 32 * v)];
+                const uint32_t pw[4] = {pc.x, pc.y, pc.z, pc.w};
 #pragma unroll
-                for (int q = 0; q < 8; ++q) {
-                    if (g + q < nd) {
+                for (int q = 0; q < 16; ++q) {
+                    if (q < nq) {
                         const uint32_t sb = __float_as_uint(s_scale[g + q]);
 #pragma unroll
-                        for (int j = 0; j < 8; ++j)
-                            a[v][j] = __fadd_rn(a[v][j], signed_scale(sb, (uint32_t)(gs >> (8 * j)) << (31 - q)));
+                        for (int j = 0; j < 8; ++j) {
+                            // worker g + q's sign of element j, moved to bit 31
+                            const uint32_t t = (j & 1) ? pw[j >> 1] << (15 - q) : pw[j >> 1] << (31 - q);
+                            a[v][j] = __fadd_rn(a[v][j], signed_scale(sb, t));
+                        }
                     }
                 }
             }
         }
+        __syncwarp();  // the staging area is reused by the next chunk
 #pragma unroll
         for (int v = 0; v < 4; ++v) {
             const int64_t i = v0 + lane + 32 * v;
@@ -675,10 +729,9 @@ extern "C" int zero_onebit_server(const uint32_t *const *worker_bits, const floa
             return rc;
     }
     const StepScalars *sc = step_scalars(ws);
-    const int64_t nv = S >> 3;
     // persistent: two blocks per SM (each holds its own table), a warp per
     // 1024 elements at a time
-    const int64_t warps = (nv + 127) >> 7;
+    const int64_t warps = ((S >> 3) + 127) >> 7;
     int64_t grid = (int64_t)sm_count() * 2;
     if (grid > (warps + kWarps - 1) / kWarps)
         grid = (warps + kWarps - 1) / kWarps;
