@@ -45,8 +45,11 @@ constexpr int64_t kL2KeepBytes = 96ll << 20;
 
 // ------------------------------------------------------------- pass 1
 
-// Squares of 4 vectors (32 elements), then one binary64 add per thread: the
-// binary64 pipe sees one add per 32 elements.  Binary16: 8 binary32 lanes
+// Vectors (of 8 elements) a thread of pass 1 loads at a time.
+constexpr int kNormVectors = 4;
+
+// Squares of kNormVectors vectors, then one binary64 add per thread: the
+// binary64 pipe sees one add per 8 * kNormVectors elements.  Binary16: 8 binary32 lanes
 // (every square is a normal binary32).  Bfloat16 and binary32: each
 // vector's squares summed in binary32 and range-checked, an out-of-range
 // vector's squares summed in binary64 instead (add_squares_checked).
@@ -57,7 +60,7 @@ __device__ __forceinline__ void norm_group(const uint4 (*w)[Elem<GT>::kWords], i
     if constexpr (GT == ZERO_F16) {
         float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-        for (int k = 0; k < 4; ++k) {
+        for (int k = 0; k < kNormVectors; ++k) {
             if (k < count) {
                 bad |= Elem<GT>::nonfinite(w[k]);
                 float f[8];
@@ -71,7 +74,7 @@ __device__ __forceinline__ void norm_group(const uint4 (*w)[Elem<GT>::kWords], i
     } else {
         float part = 0.0f;
 #pragma unroll
-        for (int k = 0; k < 4; ++k) {
+        for (int k = 0; k < kNormVectors; ++k) {
             if (k < count) {
                 bad |= Elem<GT>::nonfinite(w[k]);
                 float f[8];
@@ -96,7 +99,7 @@ __device__ __forceinline__ uint4 ld_keep(const uint4 *p)
 }
 
 // Vectors [0, nv) of one array, thread `t` of `nt` taking vectors
-// t, t + nt, ... four at a time; then the scalar tail [8*nv, n).  Vectors
+// t, t + nt, ... kNormVectors at a time; then the scalar tail [8*nv, n).  Vectors
 // from `keep_from` on are loaded with evict-last priority: pass 2 walks the
 // shard from its end, so that tail of the gradient is still in L2 when pass
 // 2 reads it again.
@@ -107,11 +110,11 @@ __device__ __forceinline__ void norm_range(const void *g, int64_t n, int64_t t, 
     constexpr int W = Elem<GT>::kWords;
     const uint4 *gv = static_cast<const uint4 *>(g);
     const int64_t nv = n >> 3;
-    for (int64_t i = t; i < nv; i += 4 * nt) {
-        uint4 w[4][W];
+    for (int64_t i = t; i < nv; i += kNormVectors * nt) {
+        uint4 w[kNormVectors][W];
         int count = 0;
 #pragma unroll
-        for (int k = 0; k < 4; ++k) {
+        for (int k = 0; k < kNormVectors; ++k) {
             const int64_t j = i + k * nt;
             if (j < nv) {
                 if (j >= keep_from) {
