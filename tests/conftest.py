@@ -27,4 +27,5 @@ def pytest_terminal_summary(terminalreporter):
     if gc is not None and gc.Parity.steps:
         terminalreporter.write_line(
             f"parity: {gc.Parity.steps} applied steps compared with the oracle; "
-            f"clip coefficient differed in {gc.Parity.clip_differs}")
+            f"clip coefficient differed in {gc.Parity.clip_differs}; "
+            f"elements held to the derived bound beyond 1e-6 rel + 1e-12 abs: {gc.Parity.tight}")
