@@ -342,7 +342,58 @@ __device__ __forceinline__ void stage_patterns(const uint32_t *W, uint4 *stage, 
     }
 }
 
+// The rank-order sums over workers 0-15 of one vector's 8 elements from
+// their staged sign patterns (pc: element j's pattern in half j & 1 of word
+// j >> 1): the table entry for workers 0..P-1, then workers 14 and 15.
+__device__ __forceinline__ void first16_sums(uint4 pc, const float *T, uint32_t pmask, int P, int upto16,
+                                             uint32_t sb14, uint32_t sb15, float *a)
+{
+    const uint32_t pw[4] = {pc.x, pc.y, pc.z, pc.w};
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+        // element j's pattern in bits 0-15 of t (16-31 of pw)
+        const uint32_t t = (j & 1) ? pw[j >> 1] >> 16 : pw[j >> 1];
+        float x = T[t & pmask];
+        if (P == 14 && upto16 > 14)
+            x = __fadd_rn(x, signed_scale(sb14, t << 17));
+        if (P == 14 && upto16 > 15)
+            x = __fadd_rn(x, signed_scale(sb15, t << 16));
+        a[j] = x;
+    }
+}
+
+// One vector (elements 8i .. 8i+7) of the chunk: the mean of its sums plus
+// the error the previous compression left, stored; its squares; its signs,
+// one byte, four lanes' bytes making one word.  Warp code (the word's
+// shuffles): every lane calls it, i >= nv writes nothing.
 template <bool kPow2, bool W32>
+__device__ __forceinline__ void finish_vector(const float *a, float *y, int64_t i, int64_t nv, float inv_nd,
+                                              float count, float prev, float *ys, uint32_t *bits, SquareSum &acc,
+                                              int lane)
+{
+    uint32_t byte = 0;
+    if (i < nv) {
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            // a power-of-two count: the product by its reciprocal is the
+            // correctly rounded quotient itself
+            const float mean = kPow2 ? __fmul_rn(a[j], inv_nd) : __fdiv_rn(a[j], count);
+            y[j] = __fadd_rn(mean, deferred_error(y[j], prev));
+        }
+        st8<W32>(ys + 8 * i, y);
+        acc.add(y);
+        byte = sign_byte(y);
+    }
+    // lanes 4j..4j+3 hold consecutive vectors: one word
+    const uint32_t word = sign_word(byte);
+    if ((lane & 3) == 0 && i < nv)
+        bits[i >> 2] = word;
+}
+
+// kWide: more than 16 workers; at most 16, each vector's sums meet their
+// values as soon as they are formed (a kernel of its own, with fewer live
+// registers).
+template <bool kPow2, bool W32, bool kWide>
 __device__ __forceinline__ void server_body(const uint32_t *const *wbits, const float *wscales, int nd, float inv_nd,
                                             float *ys, int64_t S, const StepScalars *scp, double2 *partials,
                                             WsHeader *hdr, float *scale, uint32_t *bits)
@@ -411,23 +462,23 @@ __device__ __forceinline__ void server_body(const uint32_t *const *wbits, const 
             stage_patterns(W, stage, lane);
         }
         __syncwarp();
+        if constexpr (!kWide) {
+            // each vector's sums meet their values at once: 8 sums live
+            // instead of 32
+#pragma unroll
+            for (int v = 0; v < 4; ++v) {
+                const uint4 pc = stage[stage_slot(lane + 32 * v)];
+                float a[8];
+                first16_sums(pc, T, pmask, P, upto16, sb14, sb15, a);
+                finish_vector<kPow2, W32>(a, y[v], v0 + lane + 32 * v, nv, inv_nd, count, prev, ys, bits, acc, lane);
+            }
+            __syncwarp();  // the staging area is reused by the next chunk
+            continue;
+        }
         float a[4][8];
 #pragma unroll
-        for (int v = 0; v < 4; ++v) {
-            const uint4 pc = stage[stage_slot(lane + 32 * v)];
-            const uint32_t pw[4] = {pc.x, pc.y, pc.z, pc.w};
-#pragma unroll
-            for (int j = 0; j < 8; ++j) {
-                // element j's pattern in bits 0-15 of t (16-31 of pw)
-                const uint32_t t = (j & 1) ? pw[j >> 1] >> 16 : pw[j >> 1];
-                float x = T[t & pmask];
-                if (P == 14 && upto16 > 14)
-                    x = __fadd_rn(x, signed_scale(sb14, t << 17));
-                if (P == 14 && upto16 > 15)
-                    x = __fadd_rn(x, signed_scale(sb15, t << 16));
-                a[v][j] = x;
-            }
-        }
+        for (int v = 0; v < 4; ++v)
+            first16_sums(stage[stage_slot(lane + 32 * v)], T, pmask, P, upto16, sb14, sb15, a[v]);
         // workers 16 and up, 16 at a time, in rank order
         for (int g = 16; g < nd; g += 16) {
             __syncwarp();  // every lane has read the previous patterns
@@ -461,26 +512,8 @@ __device__ __forceinline__ void server_body(const uint32_t *const *wbits, const 
         }
         __syncwarp();  // the staging area is reused by the next chunk
 #pragma unroll
-        for (int v = 0; v < 4; ++v) {
-            const int64_t i = v0 + lane + 32 * v;
-            uint32_t byte = 0;
-            if (i < nv) {
-#pragma unroll
-                for (int j = 0; j < 8; ++j) {
-                    // a power-of-two count: the product by its reciprocal is
-                    // the correctly rounded quotient itself
-                    const float mean = kPow2 ? __fmul_rn(a[v][j], inv_nd) : __fdiv_rn(a[v][j], count);
-                    y[v][j] = __fadd_rn(mean, deferred_error(y[v][j], prev));
-                }
-                st8<W32>(ys + 8 * i, y[v]);
-                acc.add(y[v]);
-                byte = sign_byte(y[v]);
-            }
-            // lanes 4j..4j+3 hold groups 4j..4j+3 of this v: one word
-            const uint32_t word = sign_word(byte);
-            if ((lane & 3) == 0 && i < nv)
-                bits[i >> 2] = word;
-        }
+        for (int v = 0; v < 4; ++v)
+            finish_vector<kPow2, W32>(a[v], y[v], v0 + lane + 32 * v, nv, inv_nd, count, prev, ys, bits, acc, lane);
     }
     scale_finish(acc.total(), partials, hdr, S, scale, skip);
 }
@@ -492,17 +525,17 @@ __global__ void __launch_bounds__(kThreads, 2) k_onebit_server(const uint32_t *c
                                                                const StepScalars *scp, double2 *partials,
                                                                WsHeader *hdr, float *scale, uint32_t *bits)
 {
-    server_body<kPow2, W32>(wbits, wscales, nd, inv_nd, ys, S, scp, partials, hdr, scale, bits);
+    server_body<kPow2, W32, true>(wbits, wscales, nd, inv_nd, ys, S, scp, partials, hdr, scale, bits);
 }
 
-template <bool kPow2, bool W32>
+template <bool kPow2, bool W32, bool kWide>
 __global__ void __launch_bounds__(kThreads, 2) k_onebit_server_args(const __grid_constant__ WorkerPtrs wp,
                                                                     const float *wscales, int nd, float inv_nd,
                                                                     float *ys, int64_t S, const StepScalars *scp,
                                                                     double2 *partials, WsHeader *hdr, float *scale,
                                                                     uint32_t *bits)
 {
-    server_body<kPow2, W32>(wp.p, wscales, nd, inv_nd, ys, S, scp, partials, hdr, scale, bits);
+    server_body<kPow2, W32, kWide>(wp.p, wscales, nd, inv_nd, ys, S, scp, partials, hdr, scale, bits);
 }
 
 // One element of the update with the frozen variance:
@@ -754,8 +787,10 @@ extern "C" int zero_onebit_server(const uint32_t *const *worker_bits, const floa
         WorkerPtrs wp = {};
         for (int32_t k = 0; k < nd; ++k)
             wp.p[k] = worker_bits[k];
-        auto kern = pow2 ? (w32 ? k_onebit_server_args<true, true> : k_onebit_server_args<true, false>)
-                         : (w32 ? k_onebit_server_args<false, true> : k_onebit_server_args<false, false>);
+        auto kern = nd > 16 ? (pow2 ? (w32 ? k_onebit_server_args<true, true, true> : k_onebit_server_args<true, false, true>)
+                                    : (w32 ? k_onebit_server_args<false, true, true> : k_onebit_server_args<false, false, true>))
+                            : (pow2 ? (w32 ? k_onebit_server_args<true, true, false> : k_onebit_server_args<true, false, false>)
+                                    : (w32 ? k_onebit_server_args<false, true, false> : k_onebit_server_args<false, false, false>));
         cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         cudaLaunchKernelEx(&cfg, kern, wp, worker_scales, (int)nd, inv_nd, x_s, S, sc, partials, hdr, scale, bits);
     } else {
