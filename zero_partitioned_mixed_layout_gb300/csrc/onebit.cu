@@ -440,8 +440,22 @@ __device__ __forceinline__ void server_body(const uint32_t *const *wbits, const 
     const int64_t nv = skip ? 0 : S >> 3, nw = S >> 5;
     const int64_t chunks = (nv + 127) >> 7;
     SquareSum acc;
-    for (int64_t c = (int64_t)blockIdx.x * kWarps + (threadIdx.x >> 5); c < chunks;
-         c += (int64_t)gridDim.x * kWarps) {
+    // workers 0-15's sign words of a chunk's word for this lane (zeros past
+    // the chunk's end or the worker count)
+    auto load_words = [&](int64_t cc, uint32_t *Wd) {
+        const int64_t ww = (cc << 5) + lane;
+        const bool ok = cc < chunks && ww < nw;
+#pragma unroll
+        for (int k = 0; k < 16; ++k)
+            Wd[k] = k < nd && ok ? __ldg(s_ptr[k] + ww) : 0u;
+    };
+    const int64_t cstride = (int64_t)gridDim.x * kWarps;
+    // up to 16 workers: the next chunk's words are loaded while this chunk is
+    // worked on (the wide kernel has no registers to spare for them)
+    uint32_t Wn[16];
+    if constexpr (!kWide)
+        load_words((int64_t)blockIdx.x * kWarps + (threadIdx.x >> 5), Wn);
+    for (int64_t c = (int64_t)blockIdx.x * kWarps + (threadIdx.x >> 5); c < chunks; c += cstride) {
         const int64_t v0 = c << 7, w = (c << 5) + lane;
         const bool wok = w < nw;
         float y[4][8];
@@ -455,9 +469,14 @@ __device__ __forceinline__ void server_body(const uint32_t *const *wbits, const 
         // workers 14 and 15 added after it
         {
             uint32_t W[16];
+            if constexpr (!kWide) {
 #pragma unroll
-            for (int k = 0; k < 16; ++k)
-                W[k] = k < nd && wok ? __ldg(s_ptr[k] + w) : 0u;
+                for (int k = 0; k < 16; ++k)
+                    W[k] = Wn[k];
+                load_words(c + cstride, Wn);
+            } else {
+                load_words(c, W);
+            }
             transpose16(W);
             stage_patterns(W, stage, lane);
         }
