@@ -709,6 +709,10 @@ def run_ours(args):
                      "nominal_gbs": NOMINAL_HBM_GBS,
                      "l2_assisted_bytes": l2_tail,
                      "l2_assisted_share": l2_tail / (wl.bytes_adam * S),
+                     "note": "the peak is a copy benchmark (one read and one write stream); a fraction "
+                             "above 1 is this kernel streaming faster than that copy, plus the share of "
+                             "its gradient reads that pass 1 left in L2 (l2_assisted_share); the "
+                             "whole-step figure counts every byte of every kernel of the step",
                      "whole_step": {"bytes_per_param": wl.bytes_step, "achieved": whole,
                                     "frac": whole / peak, "frac_of_nominal": whole / NOMINAL_HBM_GBS,
                                     "note": "every kernel of the step over ms_per_step: no L2 carry-over "
