@@ -28,4 +28,5 @@ def pytest_terminal_summary(terminalreporter):
         terminalreporter.write_line(
             f"parity: {gc.Parity.steps} applied steps compared with the oracle; "
             f"clip coefficient differed in {gc.Parity.clip_differs}; "
-            f"elements held to the derived bound beyond 1e-6 rel + 1e-12 abs: {gc.Parity.tight}")
+            f"of {gc.Parity.bounded} elements compared under a derived bound after such a step, "
+            f"{gc.Parity.tight} were beyond 1e-6 rel + 1e-12 abs (and within the bound)")

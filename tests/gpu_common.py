@@ -68,6 +68,7 @@ def assert_f32(gpu: np.ndarray, ref: np.ndarray, what: str, exact: bool = True, 
     if bound is not None:
         allow = np.maximum(allow, bound)
         Parity.tight += _tight(gpu, ref, bound)
+        Parity.bounded += int(gpu.size)
     bad = ~(np.abs(g64 - r64) <= allow)
     if bad.any():
         i = int(np.flatnonzero(bad)[0])
@@ -131,6 +132,7 @@ class Parity:
     steps = 0
     clip_differs = 0
     tight = 0
+    bounded = 0  # elements compared under a derived bound
 
 
 class Bounds:

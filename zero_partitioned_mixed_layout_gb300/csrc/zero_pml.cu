@@ -48,41 +48,47 @@ constexpr int64_t kL2KeepBytes = 96ll << 20;
 // Vectors (of 8 elements) a thread of pass 1 loads at a time.
 constexpr int kNormVectors = 4;
 
-// Squares of kNormVectors vectors, then one binary64 add per thread: the
-// binary64 pipe sees one add per 8 * kNormVectors elements.  Binary16: 8 binary32 lanes
-// (every square is a normal binary32).  Bfloat16 and binary32: each
-// vector's squares summed in binary32 and range-checked, an out-of-range
-// vector's squares summed in binary64 instead (add_squares_checked).
+// Squares of kNormVectors vectors in 8 binary32 lanes, then one binary64
+// add per thread: the binary64 pipe sees one add per 8 * kNormVectors
+// elements.  Binary16: every square is a normal binary32.  Bfloat16 and
+// binary32: the group's binary32 sum is kept only if it is finite (then no
+// square or lane sum overflowed) and either at least 2^-90 (squares lost
+// below binary32's normal range then change it by less than 2^-31 of
+// itself) or every value is zero; otherwise the group, still in registers,
+// is summed again in binary64.
 template <int GT>
 __device__ __forceinline__ void norm_group(const uint4 (*w)[Elem<GT>::kWords], int count, double &tot,
                                            uint32_t &bad)
 {
+    float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+    uint32_t nz = 0;
+#pragma unroll
+    for (int k = 0; k < kNormVectors; ++k) {
+        if (k < count) {
+            bad |= Elem<GT>::nonfinite(w[k]);
+            if constexpr (GT != ZERO_F16)
+                nz |= Elem<GT>::nonzero(w[k]);
+            float f[8];
+            Elem<GT>::to_float(w[k], f);
+#pragma unroll
+            for (int e = 0; e < 8; ++e)
+                acc[e] = __fmaf_rn(f[e], f[e], acc[e]);
+        }
+    }
+    const float s = tree8(acc);
     if constexpr (GT == ZERO_F16) {
-        float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-        for (int k = 0; k < kNormVectors; ++k) {
-            if (k < count) {
-                bad |= Elem<GT>::nonfinite(w[k]);
-                float f[8];
-                Elem<GT>::to_float(w[k], f);
-#pragma unroll
-                for (int e = 0; e < 8; ++e)
-                    acc[e] = __fmaf_rn(f[e], f[e], acc[e]);
-            }
-        }
-        tot += (double)tree8(acc);
+        tot += (double)s;
+    } else if (s < __int_as_float(0x7F800000) && (s >= 0x1p-90f || nz == 0u)) {
+        tot += (double)s;
     } else {
-        float part = 0.0f;
 #pragma unroll
         for (int k = 0; k < kNormVectors; ++k) {
             if (k < count) {
-                bad |= Elem<GT>::nonfinite(w[k]);
                 float f[8];
                 Elem<GT>::to_float(w[k], f);
-                add_squares_checked(f, Elem<GT>::nonzero(w[k]), part, tot);
+                tot += squares_wide(f);
             }
         }
-        tot += (double)part;
     }
 }
 
