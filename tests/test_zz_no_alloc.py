@@ -122,3 +122,57 @@ def test_static_scratch_rejects_long_lists(zp):
     assert call_static(zp, arrays[:32], state) == 0
     torch.cuda.synchronize()
     assert head(zp, state) == (32 * 16.0, 0.0)
+
+
+_RESET_SCRIPT = r'''
+import ctypes, sys
+import numpy as np
+sys.path.insert(0, sys.argv[1])
+import zero_partitioned_mixed_layout_gb300 as zp
+from zero_partitioned_mixed_layout_gb300.binding import _TList
+so = zp.lib()
+rt = ctypes.CDLL("libcudart.so.13")
+vp = ctypes.c_void_p
+so.zero_grad_norm_overflow_static.argtypes = [ctypes.POINTER(_TList), vp, ctypes.c_int32, vp]
+so.zero_grad_norm_overflow_static.restype = ctypes.c_int
+rng = np.random.default_rng(7)
+g = (rng.standard_normal(100_003) * 1e-3).astype(np.float16)
+init = zp.zero_state_init(1.0)
+
+def run():
+    dg, ds = vp(), vp()
+    assert rt.cudaMalloc(ctypes.byref(dg), ctypes.c_size_t(g.nbytes)) == 0
+    assert rt.cudaMalloc(ctypes.byref(ds), ctypes.c_size_t(64)) == 0
+    assert rt.cudaMemcpy(dg, g.ctypes.data_as(vp), ctypes.c_size_t(g.nbytes), 1) == 0
+    assert rt.cudaMemcpy(ds, ctypes.c_char_p(init), ctypes.c_size_t(64), 1) == 0
+    ptrs = (vp * 1)(dg)
+    numel = (ctypes.c_int64 * 1)(g.size)
+    rc = so.zero_grad_norm_overflow_static(ctypes.byref(_TList(ptrs, numel, 1, 0)), ds, 0, None)
+    assert rc == 0, zp.zero_strerror(rc)
+    out = ctypes.create_string_buffer(64)
+    assert rt.cudaMemcpy(out, ds, ctypes.c_size_t(64), 2) == 0
+    assert rt.cudaFree(dg) == 0 and rt.cudaFree(ds) == 0
+    return zp.parse_state(out.raw)["sumsq"]
+
+first = run()
+assert rt.cudaDeviceReset() == 0
+second = run()
+print(first, second)
+assert first == second and first > 0
+'''
+
+
+def test_static_scratch_after_a_device_reset(zp, tmp_path):
+    """A device reset replaces the context and the library's module with it:
+    the first call after it looks the scratch address up again.  In a child
+    process with the CUDA runtime alone (a reset would invalidate this
+    process's tensors): the same gradient gives the same sum of squares
+    before and after the reset."""
+    import os
+    import subprocess
+    import sys
+    script = tmp_path / "reset.py"
+    script.write_text(_RESET_SCRIPT)
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    r = subprocess.run([sys.executable, str(script), root], capture_output=True, text=True, timeout=300)
+    assert r.returncode == 0, r.stdout + r.stderr
