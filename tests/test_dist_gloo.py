@@ -1,11 +1,14 @@
 """The N > 1 path on CPU: two gloo ranks, each owning one shard of a layout.
-Each rank forms its partial (sum g^2, found_inf) with the oracle, packs it
-into a zero_state_t (the library's own host-side state init), sums it with
-the other rank through the package's exchange (a real all-reduce, gloo), and
-steps its shard with the summed values.  The concatenated shards must equal
-the unpartitioned oracle step; an overflow on one rank must skip the step on
-both; a rank that dies before the exchange must make the other rank's
-exchange fail with an error, not hang."""
+Each rank forms its partial (sum g^2, found_inf) with the oracle (pass 1
+itself needs a GPU), packs it into a zero_state_t (the library's own
+host-side state init), sums it with the other rank through the package's
+exchange (a real all-reduce, gloo), and steps its shard with the summed
+values: with the oracle's decision and update, or with the library's own
+(its host decision and element update, the code of its host-core offload
+path, on a state that persists across the steps as on the device).  The
+concatenated shards must equal the unpartitioned oracle step; an overflow on
+one rank must skip the step on both; a rank that dies before the exchange
+must make the other rank's exchange fail with an error, not hang."""
 import datetime
 import os
 import socket
@@ -27,7 +30,7 @@ def free_port():
         return s.getsockname()[1]
 
 
-def rank_main(rank, world, port, mode, out_dir):
+def rank_main(rank, world, port, mode, out_dir, stepper="oracle"):
     import sys
     sys.path.insert(0, ROOT)
     try:
@@ -47,28 +50,50 @@ def rank_main(rank, world, port, mode, out_dir):
         m, v = np.zeros(S, np.float32), np.zeros(S, np.float32)
         plp = np.zeros(S, np.uint16)
         hp = oracle.HParams(max_norm=0.05 if mode == "clip" else 0.0)
+        zhp = zp.HParams(max_norm=hp.max_norm)
         sc = oracle.Scaler(loss_scale=1024.0)
+        # the library's state, kept across the steps (library stepper)
+        lstate = torch.frombuffer(bytearray(zp.zero_state_init(sc.loss_scale)), dtype=torch.uint8).clone()
         skips = []
         for k in range(3):
+            # the gradient arrives multiplied by the loss scale in force:
+            # the one the stepper's own state holds
+            scale_now = zp.parse_state(lstate)["loss_scale"] if stepper == "library" else sc.loss_scale
             g = np.zeros(lay.padded_total, np.float16)
-            g[:total] = zs.host_grad(total, 0, k, sc.loss_scale, "f16")
+            g[:total] = zs.host_grad(total, 0, k, scale_now, "f16")
             if mode == "overflow" and k == 1:
                 g[lay.padded_total - S + 5] = np.inf  # lands in the last rank's shard
             gr = np.ascontiguousarray(g[rank * S:(rank + 1) * S])
-            sumsq, bad = oracle.norm_overflow([gr], "f16", sc.loss_scale)
-            state = torch.frombuffer(bytearray(zp.zero_state_init(sc.loss_scale)),
-                                     dtype=torch.uint8).clone()
+            if stepper == "library":
+                # the partial of this rank's shard, unscaled as pass 1 leaves
+                # it in the state
+                sumsq, bad = oracle.norm_overflow([gr], "f16", scale_now)
+                state = lstate
+            else:
+                sumsq, bad = oracle.norm_overflow([gr], "f16", sc.loss_scale)
+                state = torch.frombuffer(bytearray(zp.zero_state_init(sc.loss_scale)),
+                                         dtype=torch.uint8).clone()
             state[:16].view(torch.float64).copy_(torch.tensor([sumsq, float(bad)],
                                                               dtype=torch.float64))
             if mode == "die" and rank == 1:
                 os._exit(3)  # leaves between steps, before the exchange
             exchange_partials(state)
-            head = zp.parse_state(state)
-            st = oracle.decide(hp, sc, head["sumsq"], int(head["found_inf"] > 0))
-            skips.append(st.skip)
-            oracle.adam_apply(gr, "f16", p, m, v, plp, "f16", st)
+            if stepper == "library":
+                scalars = zp.zero_offload_decide(state, zhp)
+                skips.append(bool(zp.parse_state(state)["last_skipped"]))
+                zp.zero_offload_apply(gr, p, m, v, plp, scalars, gdtype="f16", pdtype="f16", n_threads=2)
+            else:
+                head = zp.parse_state(state)
+                st = oracle.decide(hp, sc, head["sumsq"], int(head["found_inf"] > 0))
+                skips.append(st.skip)
+                oracle.adam_apply(gr, "f16", p, m, v, plp, "f16", st)
+        if stepper == "library":
+            final = zp.parse_state(lstate)
+            step, scale = final["step"], final["loss_scale"]
+        else:
+            step, scale = sc.step, sc.loss_scale
         np.savez(os.path.join(out_dir, f"rank{rank}.npz"), p=p, m=m, v=v, plp=plp,
-                 skips=np.array(skips), step=sc.step, scale=sc.loss_scale)
+                 skips=np.array(skips), step=step, scale=scale)
         dist.destroy_process_group()
     except Exception:
         with open(os.path.join(out_dir, f"rank{rank}.err"), "w") as f:
@@ -76,10 +101,10 @@ def rank_main(rank, world, port, mode, out_dir):
         raise
 
 
-def run(mode, tmp_path, world=2):
+def run(mode, tmp_path, world=2, stepper="oracle"):
     port = free_port()
     ctx = mp.get_context("spawn")
-    procs = [ctx.Process(target=rank_main, args=(r, world, port, mode, str(tmp_path)))
+    procs = [ctx.Process(target=rank_main, args=(r, world, port, mode, str(tmp_path), stepper))
              for r in range(world)]
     for pr in procs:
         pr.start()
@@ -114,9 +139,10 @@ def reference(mode, world=2):
     return p, m, v, plp, sc
 
 
+@pytest.mark.parametrize("stepper", ["oracle", "library"])
 @pytest.mark.parametrize("mode", ["plain", "clip", "overflow"])
-def test_two_gloo_ranks_equal_unpartitioned(mode, tmp_path):
-    codes = run(mode, tmp_path)
+def test_two_gloo_ranks_equal_unpartitioned(mode, stepper, tmp_path):
+    codes = run(mode, tmp_path, stepper=stepper)
     errs = [open(os.path.join(tmp_path, f)).read() for f in os.listdir(tmp_path)
             if f.endswith(".err")]
     assert codes == [0, 0], errs
