@@ -115,6 +115,33 @@ struct SquareSum {
         }
     }
     __device__ __forceinline__ double total() const { return tot + (double)part; }
+    // The first `count` of 4 vectors (32 elements) still in registers: their
+    // squares by FMA in 8 binary32 lanes and one range check of the lanes'
+    // sum (finite, and at least 2^-90 unless every value is zero); an
+    // out-of-range group is summed again in binary64.
+    __device__ __forceinline__ void add4(const float (*y)[8], int count)
+    {
+        float lanes[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+        uint32_t nz = 0;
+#pragma unroll
+        for (int v = 0; v < 4; ++v) {
+            if (v < count) {
+                nz |= nonzero8(y[v]);
+#pragma unroll
+                for (int k = 0; k < 8; ++k)
+                    lanes[k] = __fmaf_rn(y[v][k], y[v][k], lanes[k]);
+            }
+        }
+        const float s = tree8(lanes);
+        if (s < __int_as_float(0x7F800000) && (s >= 0x1p-90f || nz == 0u)) {
+            tot += (double)s;
+        } else {
+#pragma unroll
+            for (int v = 0; v < 4; ++v)
+                if (v < count)
+                    tot += squares_wide(y[v]);
+        }
+    }
 };
 
 // The error a compression left, from its input x and scale sc: x - sc where
@@ -366,7 +393,7 @@ __device__ __forceinline__ void first16_sums(uint4 pc, const float *T, uint32_t 
 // the error the previous compression left, stored; its squares; its signs,
 // one byte, four lanes' bytes making one word.  Warp code (the word's
 // shuffles): every lane calls it, i >= nv writes nothing.
-template <bool kPow2, bool W32>
+template <bool kPow2, bool W32, bool kSquares = true>
 __device__ __forceinline__ void finish_vector(const float *a, float *y, int64_t i, int64_t nv, float inv_nd,
                                               float count, float prev, float *ys, uint32_t *bits, SquareSum &acc,
                                               int lane)
@@ -381,7 +408,8 @@ __device__ __forceinline__ void finish_vector(const float *a, float *y, int64_t 
             y[j] = __fadd_rn(mean, deferred_error(y[j], prev));
         }
         st8<W32>(ys + 8 * i, y);
-        acc.add(y);
+        if (kSquares)
+            acc.add(y);
         byte = sign_byte(y);
     }
     // lanes 4j..4j+3 hold consecutive vectors: one word
@@ -489,8 +517,13 @@ __device__ __forceinline__ void server_body(const uint32_t *const *wbits, const 
                 const uint4 pc = stage[stage_slot(lane + 32 * v)];
                 float a[8];
                 first16_sums(pc, T, pmask, P, upto16, sb14, sb15, a);
-                finish_vector<kPow2, W32>(a, y[v], v0 + lane + 32 * v, nv, inv_nd, count, prev, ys, bits, acc, lane);
+                finish_vector<kPow2, W32, false>(a, y[v], v0 + lane + 32 * v, nv, inv_nd, count, prev, ys, bits, acc,
+                                                 lane);
             }
+            // the squares of the lane's vectors, still in registers, at once:
+            // vector v is v0 + lane + 32v, present while below nv
+            const int64_t left = nv - (v0 + lane);
+            acc.add4(y, left <= 0 ? 0 : left >= 97 ? 4 : (int)((left + 31) / 32));
             __syncwarp();  // the staging area is reused by the next chunk
             continue;
         }
