@@ -390,13 +390,13 @@ __device__ __forceinline__ void first16_sums(uint4 pc, const float *T, uint32_t 
 }
 
 // One vector (elements 8i .. 8i+7) of the chunk: the mean of its sums plus
-// the error the previous compression left, stored; its squares; its signs,
-// one byte, four lanes' bytes making one word.  Warp code (the word's
-// shuffles): every lane calls it, i >= nv writes nothing.
-template <bool kPow2, bool W32, bool kSquares = true>
+// the error the previous compression left, stored (its squares are summed
+// with the lane's other vectors at the end of the chunk); its signs, one
+// byte, four lanes' bytes making one word.  Warp code (the word's shuffles):
+// every lane calls it, i >= nv writes nothing.
+template <bool kPow2, bool W32>
 __device__ __forceinline__ void finish_vector(const float *a, float *y, int64_t i, int64_t nv, float inv_nd,
-                                              float count, float prev, float *ys, uint32_t *bits, SquareSum &acc,
-                                              int lane)
+                                              float count, float prev, float *ys, uint32_t *bits, int lane)
 {
     uint32_t byte = 0;
     if (i < nv) {
@@ -408,8 +408,6 @@ __device__ __forceinline__ void finish_vector(const float *a, float *y, int64_t 
             y[j] = __fadd_rn(mean, deferred_error(y[j], prev));
         }
         st8<W32>(ys + 8 * i, y);
-        if (kSquares)
-            acc.add(y);
         byte = sign_byte(y);
     }
     // lanes 4j..4j+3 hold consecutive vectors: one word
@@ -517,8 +515,7 @@ __device__ __forceinline__ void server_body(const uint32_t *const *wbits, const 
                 const uint4 pc = stage[stage_slot(lane + 32 * v)];
                 float a[8];
                 first16_sums(pc, T, pmask, P, upto16, sb14, sb15, a);
-                finish_vector<kPow2, W32, false>(a, y[v], v0 + lane + 32 * v, nv, inv_nd, count, prev, ys, bits, acc,
-                                                 lane);
+                finish_vector<kPow2, W32>(a, y[v], v0 + lane + 32 * v, nv, inv_nd, count, prev, ys, bits, lane);
             }
             // the squares of the lane's vectors, still in registers, at once:
             // vector v is v0 + lane + 32v, present while below nv
@@ -565,7 +562,9 @@ __device__ __forceinline__ void server_body(const uint32_t *const *wbits, const 
         __syncwarp();  // the staging area is reused by the next chunk
 #pragma unroll
         for (int v = 0; v < 4; ++v)
-            finish_vector<kPow2, W32>(a[v], y[v], v0 + lane + 32 * v, nv, inv_nd, count, prev, ys, bits, acc, lane);
+            finish_vector<kPow2, W32>(a[v], y[v], v0 + lane + 32 * v, nv, inv_nd, count, prev, ys, bits, lane);
+        const int64_t left = nv - (v0 + lane);
+        acc.add4(y, left <= 0 ? 0 : left >= 97 ? 4 : (int)((left + 31) / 32));
     }
     scale_finish(acc.total(), partials, hdr, S, scale, skip);
 }
