@@ -31,7 +31,8 @@
  *   - `stream` is a cudaStream_t passed as void* (NULL = the legacy default
  *     stream).  Device work is enqueued asynchronously on it, on the calling
  *     thread's current CUDA device; no call synchronises the host (a table
- *     copy may wait for the copy two table copies earlier to have finished).
+ *     copy may wait for the copy two table copies earlier to have finished)
+ *     except zero_workspace_stalls, whose job is to read a device count.
  *   - Device arrays must start on a 16-byte boundary (ZERO_EALIGN otherwise);
  *     any element count is accepted, including 0 and counts of 2^31 and more.
  *   - Element types: ZERO_F16 (IEEE binary16), ZERO_BF16 (bfloat16),
@@ -182,6 +183,18 @@ typedef struct zero_tlist {
  * Device pointers passed to the library must be device (or managed) memory
  * (ZERO_EINVAL otherwise; see "Pointer checks" above). */
 size_t zero_workspace_bytes(int64_t max_tensors, int64_t max_total_numel);
+
+/* Waits that gave up.  Pass 1 over a large flat shard stages the gradient
+ * through shared memory with bulk copies and waits for each to land; a wait
+ * that has not ended after 1 s gives up rather than hang the GPU: that call
+ * then reports the gradient as non-finite (found_inf > 0, so the step is
+ * skipped) and adds one to a count kept in the workspace.  This call copies
+ * that count (every wait that gave up since the workspace was zero-filled)
+ * into *stalls.  It is the one call that waits for the GPU: it returns once
+ * `stream` has reached the copy.  ws: a device workspace as above; stalls:
+ * host.  Errors: ZERO_EINVAL (NULL argument, ws not device memory),
+ * ZERO_EALIGN (ws not on a 256-byte boundary), ZERO_ECUDA. */
+int zero_workspace_stalls(const void *ws, uint32_t *stalls, void *stream);
 
 /* ------------------------------------------------------------------ calls */
 

@@ -42,6 +42,7 @@ from .binding import (  # noqa: F401
     zero_step_prepared,
     zero_strerror,
     zero_workspace_bytes,
+    zero_workspace_stalls,
     GatherPlan,
     zero_gather_params,
     zero_gather_plan,

@@ -91,7 +91,8 @@ def lib():
         so.zero_step.argtypes = so.zero_adam_step.argtypes
         so.zero_reduce_grads.argtypes = [ctypes.POINTER(vp), i32, i32, i64, vp, i32, vp, i32, vp,
                                          ctypes.c_size_t, vp]
-        for f in ("zero_partition_layout", "zero_state_init", "zero_accumulate_grads",
+        so.zero_workspace_stalls.argtypes = [vp, ctypes.POINTER(ctypes.c_uint32), vp]
+        for f in ("zero_partition_layout", "zero_state_init", "zero_accumulate_grads", "zero_workspace_stalls",
                   "zero_accumulate_grads_norm", "zero_grad_norm_overflow", "zero_adam_step", "zero_step",
                   "zero_reduce_grads"):
             getattr(so, f).restype = ctypes.c_int
@@ -170,6 +171,16 @@ def new_workspace(max_tensors: int, max_total_numel: int, device="cuda"):
     import torch
     return torch.zeros(zero_workspace_bytes(max_tensors, max_total_numel), dtype=torch.uint8,
                        device=device)
+
+
+def zero_workspace_stalls(ws, stream=None) -> int:
+    """Waits that gave up in calls on this workspace (0 in a healthy run);
+    waits for `stream` (default: the current stream) to reach the read."""
+    out = ctypes.c_uint32()
+    rc = lib().zero_workspace_stalls(ctypes.c_void_p(ws.data_ptr()), ctypes.byref(out),
+                                     _stream_ptr(stream, ws.device))
+    _check(rc, "zero_workspace_stalls")
+    return int(out.value)
 
 
 # ------------------------------------------------------------------ marshalling

@@ -199,6 +199,86 @@ __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;"
 // successor needs few SM slots while it waits.
 __device__ __forceinline__ void pdl_launch_next() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 
+// ------------------------------------------------------------- bulk copies
+
+// Bulk asynchronous copies from global into shared memory (cp.async.bulk,
+// the untiled TMA copy) that complete on an mbarrier: the issuing thread
+// arms the barrier with the byte count, the copy engine counts the bytes
+// down, and the barrier's phase flips when all have landed.  Both addresses
+// are 16-byte aligned and the size a multiple of 16.
+
+__device__ __forceinline__ uint32_t smem_addr(const void *p)
+{
+    return (uint32_t)__cvta_generic_to_shared(p);
+}
+
+// Nanoseconds of the GPU's global timer (for wait limits).
+__device__ __forceinline__ uint64_t global_ns()
+{
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+// One-thread set-up of `count` barriers expecting one arrival each, made
+// visible to the copy engine (async proxy) before the first copy.
+__device__ __forceinline__ void mbar_init(uint64_t *bars, int count)
+{
+    for (int s = 0; s < count; ++s)
+        asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(smem_addr(bars + s)) : "memory");
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+// Waits for the phase of parity `parity` of a barrier to complete, until the
+// global timer passes `deadline_ns`; false if it gave up.
+__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, uint64_t deadline_ns)
+{
+    for (uint32_t it = 0;; ++it) {
+        uint32_t done;
+        asm volatile(
+            "{\n\t.reg .pred p;\n\t"
+            "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+            "selp.u32 %0, 1, 0, p;\n\t}"
+            : "=r"(done)
+            : "r"(smem_addr(bar)), "r"(parity)
+            : "memory");
+        if (done)
+            return true;
+        if ((it & 63u) == 63u && global_ns() > deadline_ns)
+            return false;
+    }
+}
+
+// L2 eviction priorities for a copy's lines: evict-last keeps them for a
+// later kernel, evict-first lets a stream pass through.
+__device__ __forceinline__ uint64_t l2_policy(bool keep)
+{
+    uint64_t pol;
+    if (keep)
+        asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(pol));
+    else
+        asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+    return pol;
+}
+
+// Arms `bar` for `bytes` and starts the copy of [src, src + bytes) into
+// shared memory at dst (one thread).  Before reusing a buffer that threads
+// have read, the issuing thread orders those reads before the copy's writes
+// with fence.proxy.async (after a block barrier).
+__device__ __forceinline__ void bulk_load(void *dst, const void *src, uint32_t bytes, uint64_t *bar, uint64_t policy)
+{
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_addr(bar)), "r"(bytes)
+                 : "memory");
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], %2, [%3], %4;" ::
+            "r"(smem_addr(dst)),
+        "l"(src), "r"(bytes), "r"(smem_addr(bar)), "l"(policy)
+        : "memory");
+}
+
+__device__ __forceinline__ void fence_proxy_async() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
+
 // ------------------------------------------------------------- reductions
 
 __device__ __forceinline__ double warp_sum(double x)

@@ -177,6 +177,111 @@ __global__ void __launch_bounds__(kThreads, 4)
     }
 }
 
+// Pass 1 over a large flat shard, the gradient staged through shared
+// memory by bulk copies.  Each block holds a ring of kStages buffers of
+// kStageBytes; one thread keeps the ring's chunks in flight, the block's
+// threads read each chunk out of shared memory as it lands.  Block b takes
+// the kStageBytes-chunks b, b + G, b + 2G, ... of the array (G blocks, two
+// per SM).  Measured on GB300 over a binary16 gradient with L2 flushed:
+// 455 us against 480 us for the register-loaded kernel at 1.56G elements,
+// 94.9 against 98.9 us at 268M, level at 97M; the whole step 6.575 against
+// 6.596 ms on the 1.56G shard and 0.4227 against 0.4249 ms on the 97.35M
+// one.  Two blocks of three stages per SM measured best among one to four
+// blocks of two to six stages: one block of eight warps per SM could not
+// consume the chunks as fast as they landed (wait and barrier stalls), and
+// deeper rings read more slowly.
+constexpr int kStages = 3;
+constexpr int kStageBytes = 16 << 10;
+constexpr int kNormBulkBlocksPerSM = 2;
+constexpr size_t kNormBulkSmem = (size_t)kStages * kStageBytes;
+// Flat shards of at least this many whole chunks per SM take the staged
+// kernel; smaller ones finish within a few memory round trips either way.
+constexpr int64_t kBulkMinChunksPerSM = 8;
+// A wait for a chunk gives up after this long (a copy that never lands);
+// the block then reports the gradient as non-finite (the step is skipped)
+// and counts the stall in the workspace header.
+constexpr uint64_t kWaitLimitNs = 1000000000ull;
+
+template <int GT>
+__global__ void __launch_bounds__(kThreads, kNormBulkBlocksPerSM)
+    k_norm_bulk(const void *__restrict__ g, int64_t n, double2 *partials, WsHeader *hdr, zero_state_t *st,
+                int accumulate, int trigger, FoldedDecision fd, int64_t keep_chunk)
+{
+    extern __shared__ __align__(128) unsigned char ring[];
+    __shared__ __align__(8) uint64_t full[kStages];
+    if (trigger)
+        pdl_launch_next();
+    pdl_wait();
+    constexpr int W = Elem<GT>::kWords;
+    constexpr int kWordsPerThread = kStageBytes / 16 / kThreads;  // 4: 32 or 16 elements
+    static_assert(kWordsPerThread % W == 0 && kWordsPerThread / W <= kNormVectors, "one norm group per chunk");
+    const unsigned char *gb = static_cast<const unsigned char *>(g);
+    const int64_t nch = n * Elem<GT>::kBytes / kStageBytes;
+    const int64_t mine = (int64_t)blockIdx.x < nch ? (nch - 1 - blockIdx.x) / gridDim.x + 1 : 0;
+    const uint64_t pol_keep = l2_policy(true), pol_stream = l2_policy(false);
+    // chunk k of this block into buffer k mod kStages; the chunks of the
+    // gradient's last kL2KeepBytes with evict-last priority (pass 2 starts
+    // there)
+    auto issue = [&](int64_t k) {
+        const int64_t c = (int64_t)blockIdx.x + k * gridDim.x;
+        const int s = (int)(k % kStages);
+        bulk_load(ring + (size_t)s * kStageBytes, gb + c * kStageBytes, kStageBytes, &full[s],
+                  c >= keep_chunk ? pol_keep : pol_stream);
+    };
+    if (threadIdx.x == 0) {
+        mbar_init(full, kStages);
+        for (int64_t k = 0; k < kStages && k < mine; ++k)
+            issue(k);
+    }
+    __syncthreads();
+    double tot = 0.0;
+    uint32_t bad = 0;
+    const uint64_t deadline = global_ns() + kWaitLimitNs;
+    int64_t k = 0;
+    for (; k < mine; ++k) {
+        const int s = (int)(k % kStages);
+        const bool ok = mbar_wait(&full[s], (uint32_t)((k / kStages) & 1), deadline);
+        const uint4 *words = reinterpret_cast<const uint4 *>(ring + (size_t)s * kStageBytes);
+        uint4 w[kWordsPerThread];
+#pragma unroll
+        for (int q = 0; q < kWordsPerThread; ++q)
+            w[q] = words[q * kThreads + threadIdx.x];
+        if (ok)
+            norm_group<GT>(reinterpret_cast<const uint4(*)[W]>(w), kWordsPerThread / W, tot, bad);
+        // every thread has read buffer s: it may be refilled
+        if (!__syncthreads_and(ok))
+            break;
+        if (threadIdx.x == 0 && k + kStages < mine) {
+            fence_proxy_async();
+            issue(k + kStages);
+        }
+    }
+    if (k < mine) {
+        // a chunk did not land in time: report the gradient as non-finite,
+        // count the stall, and let the copies still in flight land (with a
+        // limit of their own) before the block's shared memory is released
+        bad = 1;
+        if (threadIdx.x == 0) {
+            atomicAdd(&hdr->stalls, 1u);
+            const uint64_t d2 = global_ns() + kWaitLimitNs;
+            for (int64_t j = k; j < mine && j < k + kStages; ++j)
+                mbar_wait(&full[j % kStages], (uint32_t)((j / kStages) & 1), d2);
+        }
+        __syncthreads();
+    }
+    // the elements after the last whole chunk (less than kStageBytes), by
+    // the last block with plain loads
+    if (blockIdx.x == gridDim.x - 1) {
+        const int64_t first = nch * kStageBytes / Elem<GT>::kBytes;
+        norm_range<GT>(gb + nch * kStageBytes, n - first, threadIdx.x, kThreads, tot, bad);
+    }
+    __shared__ DecideShared sh;
+    if (norm_finish(tot, bad, partials, hdr, st, accumulate, &sh, fd.scp ? fd.cache : nullptr) && fd.scp) {
+        __syncthreads();
+        decide_block(st, fd.scp, sh, fd.a);
+    }
+}
+
 template <int GT>
 __global__ void __launch_bounds__(kThreads, 4)
     k_norm_list(const TensorEntry *__restrict__ ents, const WorkItem *__restrict__ chunks, int64_t n_chunks,
@@ -719,6 +824,21 @@ int launch_norm(const zero_tlist_t *grads, int64_t total, zero_state_t *st, int 
     if (grads->n <= 1) {
         const void *g = grads->n == 1 ? grads->ptrs[0] : nullptr;
         const int64_t n = grads->n == 1 ? grads->numel[0] : 0;
+        const int64_t chunks = n * Elem<GT>::kBytes / kStageBytes;
+        const int sms = sm_count();
+        if (sms > 0 && chunks >= kBulkMinChunksPerSM * sms) {
+            // two blocks per SM, the gradient staged through shared memory
+            const int64_t keep_chunk = chunks - kL2KeepBytes / kStageBytes;
+            cudaFuncSetAttribute(k_norm_bulk<GT>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kNormBulkSmem);
+            cudaLaunchConfig_t cfg = {};
+            cfg.gridDim = dim3((unsigned)(sms * kNormBulkBlocksPerSM));
+            cfg.blockDim = dim3((unsigned)kThreads);
+            cfg.dynamicSmemBytes = kNormBulkSmem;
+            cfg.stream = stream;
+            cudaLaunchKernelEx(&cfg, k_norm_bulk<GT>, g, n, partials, hdr, st, accumulate, (int)trigger, fd,
+                               keep_chunk);
+            return check_launch("zero_grad_norm_overflow");
+        }
         // persistent grid of 4 blocks per SM (measured best for this pass)
         const int64_t items = ((n >> 3) + 4 * kThreads - 1) / (4 * kThreads);
         const int grid = grid_for((const void *)k_norm_flat<GT>, items, kMaxBlocks, 4);
@@ -1091,6 +1211,28 @@ extern "C" int zero_reduce_grads(const void *const *replicas, int32_t n_replicas
     case ZERO_BF16: return launch_reduce_ot<ZERO_BF16>(out_dtype, r, n_replicas, out, n, d_state, accumulate, ws, s);
     default: return launch_reduce_ot<ZERO_F32>(out_dtype, r, n_replicas, out, n, d_state, accumulate, ws, s);
     }
+}
+
+extern "C" int zero_workspace_stalls(const void *ws, uint32_t *stalls, void *stream)
+{
+    if (!ws || !stalls)
+        return ZERO_EINVAL;
+    if ((reinterpret_cast<uintptr_t>(ws) & 255u) != 0)
+        return ZERO_EALIGN;
+    if (!device_ptr(ws))
+        return ZERO_EINVAL;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const WsHeader *hdr = static_cast<const WsHeader *>(ws);
+    unsigned int v = 0;
+    cudaError_t e = cudaMemcpyAsync(&v, &hdr->stalls, sizeof v, cudaMemcpyDeviceToHost, s);
+    if (e == cudaSuccess)
+        e = cudaStreamSynchronize(s);
+    if (e != cudaSuccess) {
+        set_cuda_error("zero_workspace_stalls", (int)e, cudaGetErrorString(e));
+        return ZERO_ECUDA;
+    }
+    *stalls = v;
+    return ZERO_OK;
 }
 
 extern "C" int zero_grad_norm_overflow(const zero_tlist_t *grads, zero_state_t *d_state, int32_t accumulate,

@@ -82,7 +82,7 @@ struct WorkItem {
 };
 
 // Workspace layout (all offsets 128-byte aligned):
-//   [0, 256)            header: reduction ticket
+//   [0, 256)            header: reduction ticket, count of waits that gave up
 //   [256, 384)          StepScalars of the current step
 //   [384, 768)          PowCache: the bias corrections of a window of steps
 //   [768, 768 + 16*kMaxBlocks)  per-block partials of the norm pass (double2)
@@ -95,6 +95,9 @@ struct WorkItem {
 //                       here instead
 struct WsHeader {
     unsigned int ticket;
+    // waits of a kernel that gave up (a bulk copy not landed within its
+    // limit), since the workspace was zero-filled; sticky
+    unsigned int stalls;
 };
 constexpr size_t kWsScalars = 256;
 constexpr size_t kWsPowCache = 384;
