@@ -669,17 +669,41 @@ __device__ __forceinline__ void decide_block(zero_state_t *st, StepScalars *out,
         decide_write(st, out, a, s, s_val, s_norm);
 }
 
+// The step's scalars, read after the decision wrote them.  One volatile
+// 16-byte load per word: a kernel launched with programmatic dependent
+// launch must not read them before its griddepcontrol.wait (which makes the
+// previous kernel's writes visible), and the compiler may move a plain load
+// of memory it takes for read-only (a const __restrict__ pointer) above
+// that wait; an asm volatile load stays in program order with it.  The load
+// may be served by L1: every warp of the grid reads these 80 bytes, and
+// sent to L2 each time (ld.global.cg) they made one L2 slice the step's
+// bottleneck (a 1.56G-element step took 10.1 ms instead of 6.56).
+__device__ __forceinline__ StepScalars load_scalars(const StepScalars *p)
+{
+    static_assert(sizeof(StepScalars) % 16 == 0, "StepScalars is read in 16-byte words");
+    StepScalars s;
+    uint4 *d = reinterpret_cast<uint4 *>(&s);
+    const uint4 *q = reinterpret_cast<const uint4 *>(p);
+#pragma unroll
+    for (int k = 0; k < (int)(sizeof(StepScalars) / 16); ++k)
+        asm volatile("ld.global.v4.u32 {%0,%1,%2,%3}, [%4];"
+                     : "=r"(d[k].x), "=r"(d[k].y), "=r"(d[k].z), "=r"(d[k].w)
+                     : "l"(q + k)
+                     : "memory");
+    return s;
+}
+
 // The bias-correction window for the next applied step, if the cache does
 // not cover it: warp code (all 32 lanes of one warp), lanes 0..15 taking
 // 1 - beta1^t and lanes 16..31 1 - beta2^t for t = next_t .. next_t + 15 in
 // one converged pow.  The same expressions as the decision's own.  A change
 // of the learning rate alone refills nothing: the decision then divides the
 // new rate by the cached 1 - beta1^t (a schedule changes it every step).
-__device__ __forceinline__ void refill_pow_window(const StepScalars *scp, PowCache *cache)
+__device__ __forceinline__ void refill_pow_window(const StepScalars &sc, PowCache *cache)
 {
     const int lane = threadIdx.x & 31;
-    const int64_t tn = scp->next_t;
-    const double lr = scp->lr, beta1 = scp->beta1, beta2 = scp->beta2;
+    const int64_t tn = sc.next_t;
+    const double lr = sc.lr, beta1 = sc.beta1, beta2 = sc.beta2;
     if (cache->t0 > 0 && tn >= cache->t0 && tn < cache->t0 + kPowWindow && cache->beta1 == beta1 &&
         cache->beta2 == beta2)
         return;
@@ -715,8 +739,11 @@ __global__ void k_decide(zero_state_t *st, StepScalars *out, PowCache *cache, De
     if (!refill)
         return;
     __syncthreads();
-    if (threadIdx.x < 32 && !out->skip)
-        refill_pow_window(out, cache);
+    if (threadIdx.x < 32) {
+        const StepScalars o = load_scalars(out);
+        if (!o.skip)
+            refill_pow_window(o, cache);
+    }
 }
 // ------------------------------------------------------------- host helpers
 
@@ -890,6 +917,19 @@ bool device_ptr(const void *p)
         return false;
     }
     return a.type == cudaMemoryTypeDevice || a.type == cudaMemoryTypeManaged;
+}
+
+// True for plain device memory (cudaMalloc), the only memory the kernels
+// read with bulk asynchronous copies: managed or host memory takes the
+// paths that use ordinary loads.
+bool plain_device_ptr(const void *p)
+{
+    cudaPointerAttributes a;
+    if (cudaPointerGetAttributes(&a, p) != cudaSuccess) {
+        cudaGetLastError();
+        return false;
+    }
+    return a.type == cudaMemoryTypeDevice;
 }
 
 // True for memory the kernels may reach that lives in host memory: pinned

@@ -217,7 +217,7 @@ __global__ void __launch_bounds__(kThreads) k_onebit_worker(const void *g, Momen
                                                             WsHeader *hdr, float *scale, uint32_t *bits)
 {
     pdl_wait();
-    const StepScalars s = *scp;
+    const StepScalars s = load_scalars(scp);
     // every block reads the old scale before its ticket; the new one is
     // written by the last block, after every ticket
     const float prev = *scale;
@@ -455,7 +455,7 @@ __device__ __forceinline__ void server_body(const uint32_t *const *wbits, const 
         }
         __syncthreads();
     }
-    const bool skip = scp->skip != 0;
+    const bool skip = load_scalars(scp).skip != 0;
     const int lane = threadIdx.x & 31;
     const uint32_t pmask = (1u << P) - 1u;
     // workers P..15 that the table leaves out (none when Nd <= 14)
@@ -610,7 +610,7 @@ __global__ void __launch_bounds__(kThreads) k_onebit_update(const uint32_t *bits
                                                             int64_t n, int64_t numel, float *p, float *m,
                                                             const float *v, void *plp, const StepScalars *scp)
 {
-    const StepScalars s = *scp;
+    const StepScalars s = load_scalars(scp);
     const int64_t i = (int64_t)blockIdx.x * kThreads + threadIdx.x;
     const int64_t nv = s.skip ? 0 : n >> 3;
     if (i >= nv)

@@ -194,8 +194,9 @@ constexpr int kStages = 3;
 constexpr int kStageBytes = 16 << 10;
 constexpr int kNormBulkBlocksPerSM = 2;
 constexpr size_t kNormBulkSmem = (size_t)kStages * kStageBytes;
-// Flat shards of at least this many whole chunks per SM take the staged
-// kernel; smaller ones finish within a few memory round trips either way.
+// Flat shards of at least this many whole chunks per SM, in plain device
+// memory, take the staged kernel; smaller ones finish within a few memory
+// round trips either way.
 constexpr int64_t kBulkMinChunksPerSM = 8;
 // A wait for a chunk gives up after this long (a copy that never lands);
 // the block then reports the gradient as non-finite (the step is skipped)
@@ -509,11 +510,11 @@ __device__ __forceinline__ void st8f(float *p, const float *f)
 }
 
 // Vector i (elements 8i .. 8i+7) of one array set.
-template <int GT, int PT, bool V32>
-__device__ __forceinline__ void adam_vec(const void *g, float *p, float *m, float *v, void *plp, int64_t i,
-                                         const StepScalars &s)
+// The inputs of vector i (elements 8i .. 8i+7) of one array set.
+template <int GT, bool V32>
+__device__ __forceinline__ void adam_load(const void *g, const float *p, const float *m, const float *v, int64_t i,
+                                          float *gf, float *pf, float *mf, float *vf)
 {
-    float gf[8], pf[8], mf[8], vf[8];
     if (GT == ZERO_F32) {
         ld8f<V32>(static_cast<const float *>(g) + 8 * i, gf);
     } else {
@@ -523,6 +524,13 @@ __device__ __forceinline__ void adam_vec(const void *g, float *p, float *m, floa
     ld8f<V32>(p + 8 * i, pf);
     ld8f<V32>(m + 8 * i, mf);
     ld8f<V32>(v + 8 * i, vf);
+}
+
+// The update of vector i from its loaded inputs, and its stores.
+template <int PT, bool V32>
+__device__ __forceinline__ void adam_store(float *p, float *m, float *v, void *plp, int64_t i, const float *gf,
+                                           float *pf, float *mf, float *vf, const StepScalars &s)
+{
 #pragma unroll
     for (int e = 0; e < 8; ++e)
         adam_elem(gf[e], pf[e], mf[e], vf[e], s);
@@ -531,6 +539,15 @@ __device__ __forceinline__ void adam_vec(const void *g, float *p, float *m, floa
     st8f<V32>(v + 8 * i, vf);
     if (plp)
         __stcs(static_cast<uint4 *>(plp) + i, LowP<PT>::pack(pf));
+}
+
+template <int GT, int PT, bool V32>
+__device__ __forceinline__ void adam_vec(const void *g, float *p, float *m, float *v, void *plp, int64_t i,
+                                         const StepScalars &s)
+{
+    float gf[8], pf[8], mf[8], vf[8];
+    adam_load<GT, V32>(g, p, m, v, i, gf, pf, mf, vf);
+    adam_store<PT, V32>(p, m, v, plp, i, gf, pf, mf, vf, s);
 }
 
 template <int GT, int PT>
@@ -556,20 +573,28 @@ __global__ void __launch_bounds__(kThreads, 4)
     k_adam_flat(const void *__restrict__ g, float *__restrict__ p, float *__restrict__ m, float *__restrict__ v,
                 void *__restrict__ plp, int64_t n, const StepScalars *__restrict__ scp, PowCache *cache)
 {
-    pdl_wait();
-    const StepScalars s = *scp;
-    if (s.skip)
-        return;
     const int64_t nv = n >> 3;
     // blocks walk the shard from its end: pass 1 left that end of the
     // gradient in L2
     const int64_t i = (int64_t)(gridDim.x - 1 - blockIdx.x) * kThreads + threadIdx.x;
+    // the vector's inputs are loaded before the wait for the previous
+    // kernel: that kernel (pass 1 or the decision, of the same call) writes
+    // none of them, and it started only once all earlier work in the stream
+    // had finished; so the blocks resident while it drains have their loads
+    // in flight
+    float gf[8], pf[8], mf[8], vf[8];
     if (i < nv)
-        adam_vec<GT, PT, V32>(g, p, m, v, plp, i, s);
+        adam_load<GT, V32>(g, p, m, v, i, gf, pf, mf, vf);
+    pdl_wait();
+    const StepScalars s = load_scalars(scp);
+    if (s.skip)
+        return;
+    if (i < nv)
+        adam_store<PT, V32>(p, m, v, plp, i, gf, pf, mf, vf, s);
     else if (i - nv < (n & 7))
         adam_scalar<GT, PT>(g, p, m, v, plp, (nv << 3) + (i - nv), s);
     if (blockIdx.x == 0 && threadIdx.x < 32)
-        refill_pow_window(scp, cache);
+        refill_pow_window(s, cache);
 }
 
 // Pass 2 over a list: one block per tile of kTile elements of one tensor,
@@ -583,11 +608,11 @@ __global__ void __launch_bounds__(kThreads, 4)
                 const StepScalars *__restrict__ scp, PowCache *cache)
 {
     pdl_wait();
-    const StepScalars s = *scp;
+    const StepScalars s = load_scalars(scp);
     if (s.skip)
         return;
     if (blockIdx.x == 0 && threadIdx.x < 32)
-        refill_pow_window(scp, cache);
+        refill_pow_window(s, cache);
     const WorkItem tl = tiles[blockIdx.x];
     const TensorEntry e = ents[tl.tensor];
     const int64_t start = (int64_t)tl.index * kTile;
@@ -826,7 +851,7 @@ int launch_norm(const zero_tlist_t *grads, int64_t total, zero_state_t *st, int 
         const int64_t n = grads->n == 1 ? grads->numel[0] : 0;
         const int64_t chunks = n * Elem<GT>::kBytes / kStageBytes;
         const int sms = sm_count();
-        if (sms > 0 && chunks >= kBulkMinChunksPerSM * sms) {
+        if (sms > 0 && chunks >= kBulkMinChunksPerSM * sms && plain_device_ptr(g)) {
             // two blocks per SM, the gradient staged through shared memory
             const int64_t keep_chunk = chunks - kL2KeepBytes / kStageBytes;
             cudaFuncSetAttribute(k_norm_bulk<GT>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kNormBulkSmem);
