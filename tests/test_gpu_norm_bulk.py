@@ -186,3 +186,37 @@ def test_stalls_argument_errors(zp):
     addr = (ctypes.addressof(host) + 255) & ~255
     assert lib.zero_workspace_stalls(ctypes.c_void_p(addr), ctypes.byref(out), None) == EINVAL
     assert zp.zero_workspace_stalls(ws) == 0
+
+
+def test_managed_gradient_is_read_with_ordinary_loads(zp):
+    """A gradient in managed memory (cudaMallocManaged) above the staged
+    kernel's size: the library never points a bulk copy at memory that may
+    have to be faulted in, so pass 1 takes the register-loaded kernel here,
+    and the norm is still the oracle's within 1e-6."""
+    import ctypes
+    from zero_partitioned_mixed_layout_gb300.binding import _TList
+    rt = ctypes.CDLL("libcudart.so.13")
+    vp = ctypes.c_void_p
+    n = SHAPES["ragged"](threshold("f16"), chunk_elems("f16"))
+    g = grad(n, "f16", 18, 1024.0)
+    dg = vp()
+    assert rt.cudaMallocManaged(ctypes.byref(dg), ctypes.c_size_t(g.nbytes), 1) == 0  # attach global
+    try:
+        assert rt.cudaDeviceSynchronize() == 0
+        ctypes.memmove(dg, g.ctypes.data, g.nbytes)
+        state, ws = zp.new_state(1024.0), zp.new_workspace(1, n)
+        ptrs = (vp * 1)(dg)
+        numel = (ctypes.c_int64 * 1)(n)
+        tl = _TList(ptrs, numel, 1, 0)
+        torch.cuda.synchronize()
+        rc = zp.lib().zero_grad_norm_overflow(ctypes.byref(tl), vp(state.data_ptr()), 0, vp(ws.data_ptr()),
+                                              ws.numel(), vp(torch.cuda.current_stream().cuda_stream))
+        assert rc == 0, zp.zero_strerror(rc)
+        torch.cuda.synchronize()
+        sumsq, found = norm_of(zp, state)
+        ora, bad = oracle.norm_overflow([g], "f16", 1024.0)
+        assert found == 0.0 and bad == 0
+        assert abs(np.sqrt(sumsq) - np.sqrt(ora)) <= NORM_REL * np.sqrt(ora)
+        assert zp.zero_workspace_stalls(ws) == 0
+    finally:
+        assert rt.cudaFree(dg) == 0
