@@ -410,13 +410,13 @@ class Workload:
 
     def launches_per_step(self, exchange=None) -> int:
         """Library kernels one timed step launches: zero_step on a flat shard
-        is pass 1 (with the decision in its last block) and pass 2; a list,
-        or a step with a cross-rank exchange, also launches the decision
+        or a list is pass 1 (with the decision in its last block) and pass
+        2; a step with a cross-rank exchange also launches the decision
         kernel; micro-batches: the accumulation with pass 1, the decision
         and pass 2."""
         if self.micro > 1:
             return 3
-        return 2 if (exchange is None and not self.listmode) else 3
+        return 2 if exchange is None else 3
 
     def step(self, stream, exchange=None, ev=None, g=None, lp=None):
         """One step; `g` and `lp` replace the gradient input and the

@@ -328,7 +328,7 @@ int zero_adam_step(const zero_tlist_t *grads, const zero_tlist_t *master, const 
  * same results bit for bit.  Use it when no cross-rank sum has to happen
  * between the passes ([ZeRO card §方法适配]: each rank updates its own
  * partition; with one rank, or when the norm and overflow of this shard
- * alone decide the step).  For a one-array list the last block of pass 1
+ * alone decide the step).  For a non-empty list the last block of pass 1
  * takes the decision (no decision kernel) and pass 2 is scheduled while
  * pass 1 drains.  Arguments and errors as zero_adam_step. */
 int zero_step(const zero_tlist_t *grads, const zero_tlist_t *master, const zero_tlist_t *m,

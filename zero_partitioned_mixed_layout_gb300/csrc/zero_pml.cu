@@ -286,8 +286,10 @@ __global__ void __launch_bounds__(kThreads, kNormBulkBlocksPerSM)
 template <int GT>
 __global__ void __launch_bounds__(kThreads, 4)
     k_norm_list(const TensorEntry *__restrict__ ents, const WorkItem *__restrict__ chunks, int64_t n_chunks,
-                double2 *partials, WsHeader *hdr, zero_state_t *st, int accumulate)
+                double2 *partials, WsHeader *hdr, zero_state_t *st, int accumulate, int trigger, FoldedDecision fd)
 {
+    if (trigger)
+        pdl_launch_next();
     pdl_wait();
     double tot = 0.0;
     uint32_t bad = 0;
@@ -306,7 +308,12 @@ __global__ void __launch_bounds__(kThreads, 4)
         norm_range<GT>(g, len, lane, 32, tot, bad);
     }
     __shared__ DecideShared sh;
-    norm_finish(tot, bad, partials, hdr, st, accumulate, &sh);
+    if (norm_finish(tot, bad, partials, hdr, st, accumulate, &sh, fd.scp ? fd.cache : nullptr) && fd.scp) {
+        // the last block, its totals in the state: the step decision here,
+        // as over a flat shard
+        __syncthreads();
+        decide_block(st, fd.scp, sh, fd.a);
+    }
 }
 
 // ------------------------------------------------------------- stage-2 reduction
@@ -881,7 +888,7 @@ int launch_norm(const zero_tlist_t *grads, int64_t total, zero_state_t *st, int 
     }
     const int grid = grid_for((const void *)k_norm_list<GT>, (L.n_chunks + kWarps - 1) / kWarps, kMaxBlocks, 4);
     launch_k(k_norm_list<GT>, grid, kThreads, stream, false, L.ents, L.chunks, L.n_chunks, partials, hdr, st,
-             accumulate);
+             accumulate, (int)trigger, fd);
     (void)total;
     return check_launch("zero_grad_norm_overflow");
 }
@@ -1299,6 +1306,26 @@ extern "C" int zero_adam_step(const zero_tlist_t *grads, const zero_tlist_t *mas
     return run_step(grads, master, m, v, p_lp, hp, d_state, ws, static_cast<cudaStream_t>(stream), false);
 }
 
+// The step over a list whose table is in the workspace: pass 1 with the
+// decision in its last block, then pass 2 (PDL) -- no decision kernel.
+int list_step(const zero_tlist_t *grads, const zero_tlist_t *master, const zero_tlist_t *m, const zero_tlist_t *v,
+              const zero_tlist_t *p_lp, const zero_hparams_t *hp, zero_state_t *d_state, void *ws, cudaStream_t s,
+              const ListDev &L, int64_t total)
+{
+    unsigned char *w = static_cast<unsigned char *>(ws);
+    StepScalars *sc = reinterpret_cast<StepScalars *>(w + kWsScalars);
+    const FoldedDecision fd = {sc, reinterpret_cast<const PowCache *>(w + kWsPowCache), decide_args(hp)};
+    int rc;
+    switch (grads->dtype) {
+    case ZERO_F16: rc = launch_norm<ZERO_F16>(grads, total, d_state, 0, ws, s, true, fd, &L); break;
+    case ZERO_BF16: rc = launch_norm<ZERO_BF16>(grads, total, d_state, 0, ws, s, true, fd, &L); break;
+    default: rc = launch_norm<ZERO_F32>(grads, total, d_state, 0, ws, s, true, fd, &L); break;
+    }
+    if (rc != ZERO_OK)
+        return rc;
+    return launch_pass2(grads, master, m, v, p_lp, sc, ws, s, L, L.aligned32);
+}
+
 extern "C" int zero_step(const zero_tlist_t *grads, const zero_tlist_t *master, const zero_tlist_t *m,
                          const zero_tlist_t *v, const zero_tlist_t *p_lp, const zero_hparams_t *hp,
                          zero_state_t *d_state, void *ws, size_t ws_bytes, void *stream)
@@ -1324,19 +1351,25 @@ extern "C" int zero_step(const zero_tlist_t *grads, const zero_tlist_t *master, 
             return rc;
         return launch_pass2(grads, master, m, v, p_lp, sc, ws, s, ListDev{}, flat_aligned32(grads, master, m, v));
     }
-    // a list: its table copied once, for both passes, before pass 1
-    ListDev L;
-    if (grads->n > 1 && (rc = upload_list(grads, master, m, v, p_lp, ws, s, &L)) != ZERO_OK)
-        return rc;
-    const ListDev *pre = grads->n > 1 ? &L : nullptr;
-    switch (grads->dtype) {
-    case ZERO_F16: rc = launch_norm<ZERO_F16>(grads, total, d_state, 0, ws, s, false, FoldedDecision{}, pre); break;
-    case ZERO_BF16: rc = launch_norm<ZERO_BF16>(grads, total, d_state, 0, ws, s, false, FoldedDecision{}, pre); break;
-    default: rc = launch_norm<ZERO_F32>(grads, total, d_state, 0, ws, s, false, FoldedDecision{}, pre); break;
+    if (grads->n == 0) {
+        // nothing to update: pass 1 (an empty sum into the state), then the
+        // decision kernel
+        switch (grads->dtype) {
+        case ZERO_F16: rc = launch_norm<ZERO_F16>(grads, total, d_state, 0, ws, s, false); break;
+        case ZERO_BF16: rc = launch_norm<ZERO_BF16>(grads, total, d_state, 0, ws, s, false); break;
+        default: rc = launch_norm<ZERO_F32>(grads, total, d_state, 0, ws, s, false); break;
+        }
+        if (rc != ZERO_OK)
+            return rc;
+        return run_step(grads, master, m, v, p_lp, hp, d_state, ws, s, false, nullptr);
     }
-    if (rc != ZERO_OK)
+    // a list: its table copied once, for both passes, before pass 1; the
+    // last block of pass 1 takes the decision and pass 2 follows, as over a
+    // flat shard
+    ListDev L;
+    if ((rc = upload_list(grads, master, m, v, p_lp, ws, s, &L)) != ZERO_OK)
         return rc;
-    return run_step(grads, master, m, v, p_lp, hp, d_state, ws, s, pre != nullptr, pre);
+    return list_step(grads, master, m, v, p_lp, hp, d_state, ws, s, L, total);
 }
 
 // ------------------------------------------------------------- prepared steps
@@ -1414,14 +1447,7 @@ extern "C" int zero_step_prepared(const zero_list_plan_t *plan, const zero_hpara
     L.n_chunks = plan->n_chunks;
     L.aligned32 = plan->aligned32 != 0;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    switch (plan->gdtype) {
-    case ZERO_F16: rc = launch_norm<ZERO_F16>(&tg, plan->total, d_state, 0, ws, s, false, FoldedDecision{}, &L); break;
-    case ZERO_BF16: rc = launch_norm<ZERO_BF16>(&tg, plan->total, d_state, 0, ws, s, false, FoldedDecision{}, &L); break;
-    default: rc = launch_norm<ZERO_F32>(&tg, plan->total, d_state, 0, ws, s, false, FoldedDecision{}, &L); break;
-    }
-    if (rc != ZERO_OK)
-        return rc;
-    return run_step(&tg, &tf, &tf, &tf, plan->pdtype >= 0 ? &tl : nullptr, hp, d_state, ws, s, true, &L);
+    return list_step(&tg, &tf, &tf, &tf, plan->pdtype >= 0 ? &tl : nullptr, hp, d_state, ws, s, L, plan->total);
 }
 
 // ------------------------------------------------------------- pass 1 without workspace
