@@ -220,3 +220,21 @@ def test_managed_gradient_is_read_with_ordinary_loads(zp):
         assert zp.zero_workspace_stalls(ws) == 0
     finally:
         assert rt.cudaFree(dg) == 0
+
+
+@pytest.mark.parametrize("gdtype", ["f16", "f32"])
+def test_many_calls_give_the_same_bits(zp, gdtype):
+    """400 calls back to back on one stream over the same gradient: the ring
+    of bulk copies and its barriers give the same sum of squares bit for bit
+    every time, and no wait gives up."""
+    n = SHAPES["almost"](threshold(gdtype), chunk_elems(gdtype))
+    g = to_dev(grad(n, gdtype, 19, 1.0), gdtype)
+    state, ws = zp.new_state(1.0), zp.new_workspace(1, n)
+    sums = torch.empty(400, dtype=torch.float64, device="cuda")
+    head = state[:8].view(torch.float64)
+    for k in range(400):
+        zp.zero_grad_norm_overflow(g, state, ws)
+        sums[k] = head[0]
+    torch.cuda.synchronize()
+    assert torch.unique(sums).numel() == 1 and sums[0].item() > 0
+    assert zp.zero_workspace_stalls(ws) == 0
