@@ -191,9 +191,10 @@ size_t zero_workspace_bytes(int64_t max_tensors, int64_t max_total_numel);
  * skipped) and adds one to a count kept in the workspace.  This call copies
  * that count (every wait that gave up since the workspace was zero-filled)
  * into *stalls.  It is the one call that waits for the GPU: it returns once
- * `stream` has reached the copy.  ws: a device workspace as above; stalls:
- * host.  Errors: ZERO_EINVAL (NULL argument, ws not device memory),
- * ZERO_EALIGN (ws not on a 256-byte boundary), ZERO_ECUDA. */
+ * `stream` has reached the copy (so it cannot be issued while `stream` is
+ * being captured into a graph: ZERO_ECUDA).  ws: a device workspace as
+ * above; stalls: host.  Errors: ZERO_EINVAL (NULL argument, ws not device
+ * memory), ZERO_EALIGN (ws not on a 256-byte boundary), ZERO_ECUDA. */
 int zero_workspace_stalls(const void *ws, uint32_t *stalls, void *stream);
 
 /* ------------------------------------------------------------------ calls */
