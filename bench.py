@@ -186,7 +186,16 @@ def _oracle_inputs(w, n_sample: int, seed: int):
     return p, m, v, plp, g, hp, oracle.Scaler(loss_scale=w["loss_scale"])
 
 
-def oracle_run(n_sample: int, steps: int, warmup: int, keep: bool = False):
+def oracle_workload(name: str) -> str:
+    """The workload whose inputs the oracle legs draw: the timed one when it
+    is a single-buffer flat step (one gradient array, the oracle's own full
+    step), else the bench line's default."""
+    import zero_synth as zs
+    w = zs.WORKLOADS.get(name)
+    return name if w is not None and w.get("micro_batches", 1) == 1 and name != "frag_10k" else WORKLOAD
+
+
+def oracle_run(n_sample: int, steps: int, warmup: int, keep: bool = False, name: str = WORKLOAD):
     """The oracle as it stands (single-threaded scalar C) on the first
     n_sample elements of the workload's shard: `warmup` untimed and `steps`
     timed full steps (norm, decision, update).  Returns (params/s, seconds,
@@ -195,7 +204,7 @@ def oracle_run(n_sample: int, steps: int, warmup: int, keep: bool = False):
 
     import oracle
     import zero_synth as zs
-    w = zs.WORKLOADS[WORKLOAD]
+    w = zs.WORKLOADS[name]
     oracle.build()
     p, m, v, plp, g, hp, sc = _oracle_inputs(w, n_sample, 0)
     gt, pt = w["gdtype"], w["pdtype"]
@@ -208,7 +217,7 @@ def oracle_run(n_sample: int, steps: int, warmup: int, keep: bool = False):
     return n_sample * steps / dt, dt, ((p, m, v, plp) if keep else None)
 
 
-def parity_vs_oracle(dev, n_sample: int, steps: int, final) -> dict:
+def parity_vs_oracle(dev, n_sample: int, steps: int, final, name: str = WORKLOAD) -> dict:
     """The library on the oracle run's inputs (the same seeded arrays and
     hyper-parameters, the same number of steps), outside the timed region:
     its final state against the oracle's, element by element.  ulp distances
@@ -219,7 +228,7 @@ def parity_vs_oracle(dev, n_sample: int, steps: int, final) -> dict:
 
     import zero_partitioned_mixed_layout_gb300 as zp
     import zero_synth as zs
-    w = zs.WORKLOADS[WORKLOAD]
+    w = zs.WORKLOADS[name]
     p = torch.from_numpy(zs.host_master(n_sample, 0)).to(dev)
     hg = zs.host_grad(n_sample, 0, 0, w["loss_scale"], w["gdtype"])
     g = torch.from_numpy(hg.view(np.int16)).view(torch.bfloat16).to(dev) if w["gdtype"] == "bf16" \
@@ -255,14 +264,14 @@ def parity_vs_oracle(dev, n_sample: int, steps: int, final) -> dict:
     return out
 
 
-def _oracle_worker(k, n_sample, steps, warmup, barrier, out):
+def _oracle_worker(k, n_sample, steps, warmup, barrier, out, name=WORKLOAD):
     """One process of the all-core oracle timing: its own slice of inputs
     (seeded by its index), then steps in lockstep start with the others."""
     import numpy as np
 
     import oracle
     import zero_synth as zs
-    w = zs.WORKLOADS[WORKLOAD]
+    w = zs.WORKLOADS[name]
     oracle.build()
     p, m, v, plp, g, hp, sc = _oracle_inputs(w, n_sample, k)
     gt, pt = w["gdtype"], w["pdtype"]
@@ -275,7 +284,7 @@ def _oracle_worker(k, n_sample, steps, warmup, barrier, out):
     out.put((k, t0, time.time()))
 
 
-def oracle_run_all_cores(n_sample: int, steps: int, warmup: int):
+def oracle_run_all_cores(n_sample: int, steps: int, warmup: int, name: str = WORKLOAD):
     """The same single-threaded oracle on every host core at once: one
     process per core (started with spawn), each on its own n_sample
     elements; params/s = all processes' elements x steps / the wall time
@@ -288,7 +297,7 @@ def oracle_run_all_cores(n_sample: int, steps: int, warmup: int):
         procs = os.cpu_count() or 1
     ctx = mp.get_context("spawn")
     barrier, out = ctx.Barrier(procs), ctx.Queue()
-    ps = [ctx.Process(target=_oracle_worker, args=(k, n_sample, steps, warmup, barrier, out))
+    ps = [ctx.Process(target=_oracle_worker, args=(k, n_sample, steps, warmup, barrier, out, name))
           for k in range(procs)]
     for q in ps:
         q.start()
@@ -305,20 +314,21 @@ def run_reference(args):
         return
     import oracle
     import zero_synth as zs
-    w = zs.WORKLOADS[WORKLOAD]
+    name = oracle_workload(args.workload)
+    w = zs.WORKLOADS[name]
     S = oracle.partition_layout(w["numel"](), w["nd"], w["align"]).shard_numel
-    n_sample = 1 << 24
-    one, one_dt, _ = oracle_run(n_sample, args.steps, args.warmup)
-    value, dt, procs = oracle_run_all_cores(n_sample, args.steps, args.warmup)
+    n_sample = min(1 << 24, S)
+    one, one_dt, _ = oracle_run(n_sample, args.steps, args.warmup, name=name)
+    value, dt, procs = oracle_run_all_cores(n_sample, args.steps, args.warmup, name=name)
     sample = (f"{procs} processes (one per host core), each on its own {n_sample} params of the "
-              f"{WORKLOAD} rank-0 shard's inputs, {args.steps} timed steps after {args.warmup} "
+              f"{name} rank-0 shard's inputs, {args.steps} timed steps after {args.warmup} "
               f"warm-up; full step (norm, decision, update) per step")
     line = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * dt / args.steps,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
         "data": "synthetic",
-        "config": dict(step_config(TITLES[WORKLOAD], w, S, "host cores: each process steps its own sample of the "
+        "config": dict(step_config(TITLES[name], w, S, "host cores: each process steps its own sample of the "
                                    "shard (the oracle does not use the GPU)", args.gpus),
                        sample_params=n_sample),
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": procs, "kind": "oracle",
@@ -656,18 +666,21 @@ def run_ours(args):
     if not args.no_cpu_baseline and world == 1:
         # about 10-20 s of CPU work in all: 10 full steps of 2^24 params on
         # one core, then on every core at once
+        oname = oracle_workload(args.workload)
         n_sample, c_steps = 1 << 24, 10
-        cv, cdt, final = oracle_run(n_sample, c_steps, 1, keep=True)
-        av, adt, procs = oracle_run_all_cores(n_sample, c_steps, 1)
+        if oname == args.workload:
+            n_sample = min(n_sample, S)
+        cv, cdt, final = oracle_run(n_sample, c_steps, 1, keep=True, name=oname)
+        av, adt, procs = oracle_run_all_cores(n_sample, c_steps, 1, name=oname)
         cpu = {"value": av, "unit": UNIT, "cores": procs, "kind": "oracle",
                "sample": f"{procs} processes (one per host core), each {c_steps} full steps on its own "
-                         f"{n_sample} params drawn as the workload's ({TITLES[WORKLOAD]}), "
+                         f"{n_sample} params drawn as the workload's ({TITLES[oname]}), "
                          f"{adt:.1f} s wall ({procs * adt:.0f} s of CPU); the oracle as it stands "
                          f"(single-threaded scalar C)",
                "single_core": {"value": cv, "unit": UNIT, "cores": 1, "seconds": cdt,
                                "sample": f"first {n_sample} params of the shard, {c_steps} full steps"},
                # the library on the single-core run's inputs, against its result
-               "parity": parity_vs_oracle(dev, n_sample, c_steps + 1, final)}
+               "parity": parity_vs_oracle(dev, n_sample, c_steps + 1, final, oname)}
     default = args.workload == WORKLOAD
     traffic = committed_traffic(args.workload) if not args.prepared else None
     # the part of pass 2's gradient reads that pass 1 leaves in L2 (its
